@@ -1,0 +1,197 @@
+"""Python driver for the fp64 CPU oracle (``spec_oracle.c``).
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg import this module.  The CUDA product path never imports it, and it
+imports nothing from the product package.
+
+Every function here is argument marshalling around the C oracle; the arithmetic lives in
+``spec_oracle.c`` and follows the pages cited there.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+F32, BF16, F64 = 0, 1, 2
+ROW_OK, ROW_NONFINITE, ROW_DEGENERATE, ROW_BAD_TOKEN = 0, 1, 2, 3
+ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM = 5, 6, 7
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``spec_oracle.c`` into ``liboracle.so`` next to it (plain gcc, -O2, fp64)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P, I, D, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+    lib.oracle_spec_verify.argtypes = [P, P, I, P, P, I, I, I, D, I, P, P, P, P, P, P, P]
+    lib.oracle_spec_verify.restype = I
+    lib.oracle_tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P]
+    lib.oracle_tree_verify_greedy.restype = I
+    lib.oracle_row_probs.argtypes = [P, I, Z, I, D, I, P, P, P]
+    lib.oracle_row_probs.restype = I
+    lib.oracle_lse_online.argtypes = [P, I, I]
+    lib.oracle_lse_online.restype = D
+    lib.oracle_lse_maxshift.argtypes = [P, I]
+    lib.oracle_lse_maxshift.restype = D
+    lib.oracle_alpha.argtypes = [P, P, I]
+    lib.oracle_alpha.restype = D
+    lib.oracle_residual.argtypes = [P, P, I, P]
+    lib.oracle_residual.restype = D
+    lib.oracle_inverse_cdf.argtypes = [P, I, D, P, P]
+    lib.oracle_inverse_cdf.restype = I
+    lib.oracle_kth_largest.argtypes = [P, I, I]
+    lib.oracle_kth_largest.restype = D
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a: np.ndarray):
+    """Map a logits array to (contiguous array, oracle dtype code).  bf16 travels as uint16 bits."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float64:
+        return a, F64
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype in (np.uint16, np.int16):
+        return a.view(np.uint16), BF16
+    raise TypeError(f"unsupported logits dtype {a.dtype}")
+
+
+def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k: int = 0):
+    """Exact speculative-sampling verify over B requests (fp64).
+
+    target [B, gamma+1, V], draft [B, gamma, V] (float64, float32, or bf16 bits as uint16),
+    draft_tokens [B, gamma] int32, uniforms [B, gamma+2] float32.  Returns a dict with
+    accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin.
+    """
+    lib = _load()
+    t, dt = _logits(target)
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    if gamma > 0:
+        d, dd = _logits(draft)
+        assert dd == dt and d.shape == (B, gamma, V)
+    else:
+        d = np.zeros((B, 0, V), dtype=t.dtype)
+    tok = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, gamma)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, gamma + 2)
+    out = dict(
+        accepted_len=np.empty(B, np.int32),
+        out_tokens=np.empty((B, gamma + 1), np.int32),
+        row_status=np.empty(B, np.int32),
+        lse_p=np.empty((B, gamma + 1)),
+        lse_q=np.empty((B, gamma)),
+        accept=np.empty((B, gamma)),
+        margin=np.empty(B),
+    )
+    rc = lib.oracle_spec_verify(
+        _ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V, float(temperature), int(top_k),
+        _ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["row_status"]),
+        _ptr(out["lse_p"]), _ptr(out["lse_q"]), _ptr(out["accept"]), _ptr(out["margin"]),
+    )
+    if rc != 0:
+        raise ValueError("oracle_spec_verify rejected its arguments")
+    return out
+
+
+def tree_verify_greedy(logits, parents, tokens, max_out: int | None = None):
+    """Greedy tree verify (fp64 / exact compares).  logits [B, N+1, V]; parents, tokens [B, N]."""
+    lib = _load()
+    lg, dt = _logits(logits)
+    B, n1, V = lg.shape
+    N = n1 - 1
+    if max_out is None:
+        max_out = N + 1
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    out = dict(
+        accepted_len=np.empty(B, np.int32),
+        out_tokens=np.empty((B, max_out), np.int32),
+        out_nodes=np.empty((B, max(max_out - 1, 0)), np.int32),
+        row_status=np.empty(B, np.int32),
+        amax=np.empty((B, N + 1), np.int32),
+    )
+    rc = lib.oracle_tree_verify_greedy(
+        _ptr(lg), dt, _ptr(par), _ptr(tok), B, N, V, int(max_out),
+        _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
+        _ptr(out["out_nodes"]) if max_out > 1 else None, _ptr(out["row_status"]), _ptr(out["amax"]),
+    )
+    if rc != 0:
+        raise ValueError("oracle_tree_verify_greedy rejected its arguments")
+    return out
+
+
+def row_probs(logits_row, temperature: float, top_k: int = 0):
+    """Processed probability row p = softmax(topk(logits)/T).  Returns (status, p, lse, thr)."""
+    lib = _load()
+    x, dt = _logits(np.asarray(logits_row).reshape(-1))
+    V = x.shape[0]
+    p = np.zeros(V)
+    lse = ctypes.c_double(0.0)
+    thr = ctypes.c_double(0.0)
+    st = lib.oracle_row_probs(_ptr(x), dt, 0, V, float(temperature), int(top_k), _ptr(p),
+                              ctypes.byref(lse), ctypes.byref(thr))
+    return st, p, lse.value, thr.value
+
+
+def lse_online(z, block: int) -> float:
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    return _load().oracle_lse_online(_ptr(z), z.shape[0], int(block))
+
+
+def lse_maxshift(z) -> float:
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    return _load().oracle_lse_maxshift(_ptr(z), z.shape[0])
+
+
+def alpha(p, q) -> float:
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    return _load().oracle_alpha(_ptr(p), _ptr(q), p.shape[0])
+
+
+def residual(p, q):
+    """Returns (normalised residual, Z)."""
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    out = np.empty_like(p)
+    Z = _load().oracle_residual(_ptr(p), _ptr(q), p.shape[0], _ptr(out))
+    return out, Z
+
+
+def inverse_cdf(r, u: float):
+    """Returns (token, C(v-1)/Z, C(v)/Z); token -1 when the mass is not positive."""
+    r = np.ascontiguousarray(r, dtype=np.float64)
+    lo = ctypes.c_double(0.0)
+    hi = ctypes.c_double(0.0)
+    v = _load().oracle_inverse_cdf(_ptr(r), r.shape[0], float(u), ctypes.byref(lo), ctypes.byref(hi))
+    return v, lo.value, hi.value
+
+
+def kth_largest(x, k: int) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    return _load().oracle_kth_largest(_ptr(x), x.shape[0], int(k))

@@ -1,0 +1,388 @@
+/*
+ * spec_oracle.c -- TEST INFRASTRUCTURE, NOT PRODUCT CODE.
+ *
+ * A plain, slow, fp64 CPU statement of the target-side verify step of speculative decoding.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg load this file's
+ * library; the CUDA product path never calls it and shares no code, header or table with it.
+ *
+ * Every function follows the page that defines the operation (page title + section):
+ *   [M7.1]  "M7.1 - Speculative Decoding: Draft, Verify, Accept, Reject"
+ *           (transformer-system.numinens.com), sections 0x03, 0x03B-0x03D, 0x03F-0x03H, 0x04, 0x04J.
+ *   [M16]   "Module 16" speculative-decoding lesson (learnllm.pages.dev), "The Math: Speculative
+ *           Sampling", "The Candidate Tree", "Verify the Tree -- and Why It's Exact".
+ *   [M7.7]  "M7.7 - Draft Sources, Dependent Heads, Hardware-Aware Trees", section 0x07E
+ *           (candidate row / predictor row convention).
+ *   [TRLM]  "Exact speculative and assisted decoding for TinyRustLM" (mikekappel.com),
+ *           "Normative stochastic pseudocode", "Normative edge-case behavior".
+ *
+ * Readings taken where the pages are silent (each is listed in the design notes):
+ *   - accept iff u < a with u in [0,1)                            ([M16] accept rule)
+ *   - one uniform draws a categorical by inverse CDF in ascending token order on the
+ *     unnormalised mass: the smallest v with u*Z < C(v); if rounding runs off the end,
+ *     the largest v with positive mass
+ *   - uniform slot gamma feeds the correction draw, slot gamma+1 the bonus draw
+ *   - top-k keeps every token whose stored logit is >= the k-th largest stored logit
+ *     (counted with multiplicity), applied to target and draft rows alike, before temperature
+ *   - a request whose rows hold NaN or +inf, or a row with no finite-or-minus-inf mass, is
+ *     reported as non-finite; a draft token outside [0,V) or with q(x) = 0 is a bad token;
+ *     uniforms outside [0,1) are a bad uniform; such requests emit nothing (-1).
+ *   - tree argmax ties go to the lowest token index; the deepest valid node wins, ties to the
+ *     lowest node index.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
+enum {
+    OR_ROW_OK = 0,
+    OR_ROW_NONFINITE = 1,
+    OR_ROW_DEGENERATE = 2,
+    OR_ROW_BAD_TOKEN = 3,
+    OR_ROW_BAD_PARENT = 5,
+    OR_ROW_OVERFLOW = 6,
+    OR_ROW_BAD_UNIFORM = 7
+};
+
+/* ---------------------------------------------------------------- element access */
+
+static double load_logit(const void* base, int dtype, size_t i)
+{
+    if (dtype == OR_F64) return ((const double*)base)[i];
+    if (dtype == OR_F32) return (double)((const float*)base)[i];
+    /* bf16: the stored 16 bits are the high half of an IEEE binary32 */
+    uint16_t h = ((const uint16_t*)base)[i];
+    uint32_t w = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* ---------------------------------------------------------------- top-k threshold */
+
+static int cmp_desc(const void* a, const void* b)
+{
+    double x = *(const double*)a, y = *(const double*)b;
+    return (x < y) - (x > y);
+}
+
+/* k-th largest of x[0..n) counted with multiplicity: sort a copy in descending order. */
+double oracle_kth_largest(const double* x, int n, int k)
+{
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    memcpy(s, x, sizeof(double) * (size_t)n);
+    qsort(s, (size_t)n, sizeof(double), cmp_desc);
+    double t = s[k - 1];
+    free(s);
+    return t;
+}
+
+/* ---------------------------------------------------------------- processors + softmax */
+
+/*
+ * One probability row after the declared processors ([M7.1] 0x02A: p_i = Pi_T(logits)):
+ *   optional top-k on the stored logits, then z = logit / T, then max-shift softmax
+ *   ([M7.1] 0x04J backend 1).  Returns a row status; fills p[0..V) and *lse (natural log of the
+ *   normaliser of z over the kept tokens) and *thr (the top-k threshold, -inf without top-k).
+ */
+int oracle_row_probs(const void* base, int dtype, size_t off, int V, double T, int top_k,
+                     double* p, double* lse, double* thr)
+{
+    if (V < 1) return OR_ROW_NONFINITE;
+    double* x = (double*)malloc(sizeof(double) * (size_t)V);
+    int v;
+    for (v = 0; v < V; ++v) {
+        x[v] = load_logit(base, dtype, off + (size_t)v);
+        if (isnan(x[v]) || (isinf(x[v]) && x[v] > 0)) { free(x); return OR_ROW_NONFINITE; }
+    }
+    double t = -INFINITY;
+    if (top_k > 0 && top_k < V) t = oracle_kth_largest(x, V, top_k);
+    *thr = t;
+
+    /* z over the kept set; -inf elsewhere */
+    double m = -INFINITY;
+    for (v = 0; v < V; ++v) {
+        double z = (x[v] >= t) ? x[v] / T : -INFINITY;
+        x[v] = z;
+        if (z > m) m = z;
+    }
+    if (m == -INFINITY) { free(x); return OR_ROW_NONFINITE; } /* no valid token */
+    double S = 0.0;
+    for (v = 0; v < V; ++v) {
+        double e = (x[v] == -INFINITY) ? 0.0 : exp(x[v] - m);
+        p[v] = e;
+        S += e;
+    }
+    for (v = 0; v < V; ++v) p[v] /= S;
+    *lse = m + log(S);
+    free(x);
+    return OR_ROW_OK;
+}
+
+/* Backend 2 of [M7.1] 0x04J: an online (m, l) merge over vocabulary blocks of width `block`.
+ * Returns the log-normaliser of z[0..n). */
+double oracle_lse_online(const double* z, int n, int block)
+{
+    double m = -INFINITY, l = 0.0;
+    for (int s = 0; s < n; s += block) {
+        int e = s + block < n ? s + block : n;
+        double bm = -INFINITY, bl = 0.0;
+        for (int v = s; v < e; ++v) if (z[v] > bm) bm = z[v];
+        if (bm == -INFINITY) continue;
+        for (int v = s; v < e; ++v) bl += exp(z[v] - bm);
+        double nm = bm > m ? bm : m;
+        l = l * exp(m - nm) + bl * exp(bm - nm);
+        m = nm;
+    }
+    return m + log(l);
+}
+
+/* Backend 1 of [M7.1] 0x04J: conventional max-shift log-normaliser. */
+double oracle_lse_maxshift(const double* z, int n)
+{
+    double m = -INFINITY, S = 0.0;
+    for (int v = 0; v < n; ++v) if (z[v] > m) m = z[v];
+    for (int v = 0; v < n; ++v) S += exp(z[v] - m);
+    return m + log(S);
+}
+
+/* Acceptance rate alpha = sum_x min(p(x), q(x))  ([M7.1] 0x03B). */
+double oracle_alpha(const double* p, const double* q, int V)
+{
+    double a = 0.0;
+    for (int v = 0; v < V; ++v) a += p[v] < q[v] ? p[v] : q[v];
+    return a;
+}
+
+/* Normalised positive residual [p - q]_+ / Z ([M7.1] 0x03C); returns Z. */
+double oracle_residual(const double* p, const double* q, int V, double* out)
+{
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double r = p[v] - q[v];
+        out[v] = r > 0.0 ? r : 0.0; /* clamp tiny negatives ([M7.1] 0x03D) */
+        Z += out[v];
+    }
+    if (Z > 0.0)
+        for (int v = 0; v < V; ++v) out[v] /= Z;
+    return Z;
+}
+
+/*
+ * Inverse-CDF draw from unnormalised mass r[0..V) with one uniform u: the smallest v with
+ * u*Z < C(v), C the running sum in ascending index order.  Returns -1 when Z <= 0.  *lo and *hi
+ * receive C(v-1)/Z and C(v)/Z of the chosen token (for boundary-distance reporting).
+ */
+int oracle_inverse_cdf(const double* r, int V, double u, double* lo, double* hi)
+{
+    double Z = 0.0;
+    int v;
+    for (v = 0; v < V; ++v) Z += r[v];
+    if (!(Z > 0.0)) return -1;
+    double t = u * Z, C = 0.0, Cprev = 0.0;
+    for (v = 0; v < V; ++v) {
+        Cprev = C;
+        C += r[v];
+        if (t < C) { *lo = Cprev / Z; *hi = C / Z; return v; }
+    }
+    for (v = V - 1; v >= 0; --v) /* rounding ran off the end */
+        if (r[v] > 0.0) { *lo = 1.0; *hi = 1.0; return v; }
+    return -1;
+}
+
+/* ---------------------------------------------------------------- the verify round */
+
+/*
+ * Exact speculative sampling verify for B independent requests ([M7.1] 0x04 loop body,
+ * [TRLM] exact_speculative_round, [M16] accept rule + residual):
+ *
+ *   target  [B, gamma+1, V]  row i scores draft token i; row gamma scores the bonus position
+ *   draft   [B, gamma,   V]  row i is the proposal row that sampled draft token i
+ *   tokens  [B, gamma]
+ *   uniforms[B, gamma+2]     slots 0..gamma-1 accept draws, slot gamma correction, gamma+1 bonus
+ *
+ * Outputs: accepted_len[B] (A, or -1), out_tokens[B, gamma+1] (accepted prefix, correction or
+ * bonus, then -1), row_status[B], lse_p[B, gamma+1], lse_q[B, gamma], accept[B, gamma]
+ * (a_i = min(1, p_i(x_i)/q_i(x_i)) at every position), margin[B] (smallest distance between a
+ * used uniform and a decision boundary it was compared with: |u_i - a_i| for every reached
+ * accept test and |u - C(v-1)/Z|, |u - C(v)/Z| for the drawn token).
+ * Any output pointer except the first two may be NULL.
+ */
+int oracle_spec_verify(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                       const float* uniforms, int B, int gamma, int V, double T, int top_k,
+                       int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                       double* lse_p, double* lse_q, double* accept, double* margin)
+{
+    if (B < 0 || gamma < 0 || V < 1 || !(T > 0.0)) return 1;
+    double* p = (double*)malloc(sizeof(double) * (size_t)(gamma + 1) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)(gamma > 0 ? gamma : 1) * (size_t)V);
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int b = 0; b < B; ++b) {
+        int st = OR_ROW_OK;
+        double thr;
+        for (int i = 0; i <= gamma; ++i) {
+            double l = NAN;
+            size_t off = ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * (size_t)V;
+            int s = oracle_row_probs(target, dtype, off, V, T, top_k, p + (size_t)i * V, &l, &thr);
+            if (s != OR_ROW_OK) st = OR_ROW_NONFINITE;
+            if (lse_p) lse_p[(size_t)b * (gamma + 1) + i] = l;
+        }
+        for (int i = 0; i < gamma; ++i) {
+            double l = NAN;
+            size_t off = ((size_t)b * (size_t)gamma + (size_t)i) * (size_t)V;
+            int s = oracle_row_probs(draft, dtype, off, V, T, top_k, q + (size_t)i * V, &l, &thr);
+            if (s != OR_ROW_OK) st = OR_ROW_NONFINITE;
+            if (lse_q) lse_q[(size_t)b * gamma + i] = l;
+        }
+        const int32_t* tok = tokens + (size_t)b * gamma;
+        const float* u = uniforms + (size_t)b * (gamma + 2);
+        if (st == OR_ROW_OK)
+            for (int i = 0; i < gamma; ++i)
+                if (tok[i] < 0 || tok[i] >= V) st = OR_ROW_BAD_TOKEN;
+        double* a = (double*)malloc(sizeof(double) * (size_t)(gamma > 0 ? gamma : 1));
+        for (int i = 0; i < gamma; ++i) a[i] = NAN;
+        if (st == OR_ROW_OK) {
+            for (int i = 0; i < gamma; ++i) {
+                double pi = p[(size_t)i * V + tok[i]], qi = q[(size_t)i * V + tok[i]];
+                if (qi == 0.0) { st = OR_ROW_BAD_TOKEN; break; } /* q never proposes x */
+                double ratio = pi / qi;
+                a[i] = ratio < 1.0 ? ratio : 1.0;
+            }
+        }
+        if (st == OR_ROW_OK)
+            for (int i = 0; i < gamma + 2; ++i)
+                if (!(u[i] >= 0.0f && u[i] < 1.0f)) st = OR_ROW_BAD_UNIFORM;
+        if (accept)
+            for (int i = 0; i < gamma; ++i) accept[(size_t)b * gamma + i] = a[i];
+
+        int32_t* out = out_tokens + (size_t)b * (gamma + 1);
+        for (int i = 0; i <= gamma; ++i) out[i] = -1;
+        double mg = INFINITY;
+        int A = -1;
+        if (st == OR_ROW_OK) {
+            /* first rejection ([M7.1] 0x03G) */
+            A = gamma;
+            for (int i = 0; i < gamma; ++i) {
+                double d = fabs((double)u[i] - a[i]);
+                if (d < mg) mg = d;
+                if (!((double)u[i] < a[i])) { A = i; break; }
+            }
+            double uu;
+            if (A < gamma) { /* correction from the positive residual ([M7.1] 0x03C) */
+                for (int v = 0; v < V; ++v) {
+                    double d = p[(size_t)A * V + v] - q[(size_t)A * V + v];
+                    r[v] = d > 0.0 ? d : 0.0;
+                }
+                uu = (double)u[gamma];
+            } else {       /* bonus from the target row after the full draft ([M7.1] 0x03H) */
+                for (int v = 0; v < V; ++v) r[v] = p[(size_t)gamma * V + v];
+                uu = (double)u[gamma + 1];
+            }
+            double lo = 0.0, hi = 0.0;
+            int y = oracle_inverse_cdf(r, V, uu, &lo, &hi);
+            if (y < 0) {
+                st = OR_ROW_DEGENERATE;
+                A = -1;
+            } else {
+                double d1 = fabs(uu - lo), d2 = fabs(uu - hi);
+                if (d1 < mg) mg = d1;
+                if (d2 < mg) mg = d2;
+                for (int i = 0; i < A; ++i) out[i] = tok[i];
+                out[A] = y;
+            }
+        }
+        if (st != OR_ROW_OK) A = -1;
+        accepted_len[b] = A;
+        if (row_status) row_status[b] = st;
+        if (margin) margin[b] = mg;
+        free(a);
+    }
+    free(p);
+    free(q);
+    free(r);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- greedy tree verify */
+
+/*
+ * Medusa-style greedy tree verify ([M16] "Verify the Tree", [M7.7] 0x07E row convention):
+ *   logits  [B, N+1, V]  row 0 = prefix frontier, row i+1 = produced at candidate node i
+ *   parents [B, N]       parent node of node i, -1 for a depth-1 node, else in [0, i)
+ *   tokens  [B, N]       candidate token of node i
+ * Node i is valid when its token equals the argmax of its predictor row (frontier row for a
+ * depth-1 node, row parent+1 otherwise) and its parent is valid.  The deepest valid node (lowest
+ * index on ties) is accepted with its root path; the bonus is the argmax of that node's own row
+ * (of the frontier row when no node is valid).
+ * Outputs: accepted_len[B], out_tokens[B, max_out] (path tokens, bonus, then -1),
+ * out_nodes[B, max_out-1] (node ids on the path, then -1; may be NULL), row_status[B],
+ * amax[B, N+1] (argmax of each row; may be NULL).
+ */
+int oracle_tree_verify_greedy(const void* logits, int dtype, const int32_t* parents,
+                              const int32_t* tokens, int B, int N, int V, int max_out,
+                              int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                              int32_t* row_status, int32_t* amax_out)
+{
+    if (B < 0 || N < 0 || V < 1 || max_out < 1) return 1;
+    int32_t* amax = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N + 1));
+    int32_t* valid = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    int32_t* depth = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    int32_t* path = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N + 1));
+    for (int b = 0; b < B; ++b) {
+        int st = OR_ROW_OK;
+        for (int j = 0; j <= N; ++j) {
+            size_t off = ((size_t)b * (size_t)(N + 1) + (size_t)j) * (size_t)V;
+            double best = -INFINITY;
+            int bi = -1;
+            for (int v = 0; v < V; ++v) {
+                double x = load_logit(logits, dtype, off + (size_t)v);
+                if (isnan(x)) { st = OR_ROW_NONFINITE; continue; }
+                if (bi < 0 ? x > -INFINITY : x > best) { best = x; bi = v; }
+            }
+            if (bi < 0) st = OR_ROW_NONFINITE; /* every entry -inf: no valid token */
+            amax[j] = bi;
+            if (amax_out) amax_out[(size_t)b * (N + 1) + j] = bi;
+        }
+        const int32_t* par = parents + (size_t)b * N;
+        const int32_t* tok = tokens + (size_t)b * N;
+        if (st == OR_ROW_OK)
+            for (int i = 0; i < N; ++i) {
+                if (par[i] < -1 || par[i] >= i) { st = OR_ROW_BAD_PARENT; break; }
+                if (tok[i] < 0 || tok[i] >= V) st = OR_ROW_BAD_TOKEN;
+            }
+        int best = -1, bestd = 0;
+        if (st == OR_ROW_OK) {
+            for (int i = 0; i < N; ++i) {
+                int pr = par[i];
+                int row = pr < 0 ? 0 : pr + 1;
+                valid[i] = (tok[i] == amax[row]) && (pr < 0 || valid[pr]);
+                depth[i] = pr < 0 ? 1 : depth[pr] + 1;
+                if (valid[i] && depth[i] > bestd) { bestd = depth[i]; best = i; }
+            }
+            if (bestd + 1 > max_out) st = OR_ROW_OVERFLOW;
+        }
+        int32_t* out = out_tokens + (size_t)b * max_out;
+        int32_t* on = out_nodes ? out_nodes + (size_t)b * (max_out - 1) : NULL;
+        for (int i = 0; i < max_out; ++i) out[i] = -1;
+        if (on) for (int i = 0; i < max_out - 1; ++i) on[i] = -1;
+        if (st == OR_ROW_OK) {
+            int n = 0;
+            for (int i = best; i >= 0; i = par[i]) path[n++] = i;
+            for (int j = 0; j < n; ++j) {
+                out[j] = tok[path[n - 1 - j]];
+                if (on) on[j] = path[n - 1 - j];
+            }
+            out[n] = amax[best < 0 ? 0 : best + 1];
+            accepted_len[b] = n;
+        } else {
+            accepted_len[b] = -1;
+        }
+        if (row_status) row_status[b] = st;
+    }
+    free(amax);
+    free(valid);
+    free(depth);
+    free(path);
+    return 0;
+}
