@@ -1,0 +1,161 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding verify library.
+ *
+ * Three verify calls, each one pass of the target-side verify step over a batch of B independent
+ * requests, entirely on the GPU:
+ *
+ *   spec_verify        exact speculative sampling with temperature
+ *   spec_verify_topk   the same with a top-k processor applied identically to target and draft
+ *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
+ *
+ * Sources (page title + section):
+ *   "M7.1 - Speculative Decoding: Draft, Verify, Accept, Reject": 0x03 (accept probability and
+ *     correction distribution), 0x03C-0x03D (positive residual, support and numerical cases),
+ *     0x03G (stop at the first rejection), 0x03H (bonus token), 0x04 (round loop), 0x04J (online
+ *     (m, l) merge over vocabulary blocks).
+ *   Module 16 speculative-decoding lesson: "The Math: Speculative Sampling" (accept iff
+ *     u < min(1, p(x)/q(x))), "Verify the Tree -- and Why It's Exact" (greedy tree walk).
+ *   "M7.7 - Draft Sources, Dependent Heads, Hardware-Aware Trees": 0x07E (candidate row vs
+ *     predictor row: a depth-1 node is scored by the frontier row, any other node by its
+ *     parent's row).
+ *   "Exact speculative and assisted decoding for TinyRustLM": "Normative stochastic pseudocode"
+ *     (separate accept / correction / extra-token random streams, abort without emitting on
+ *     non-finite rows or a non-positive residual), "Minimum target API" (row i predicts proposal
+ *     i, the last row predicts the extra token).
+ *
+ * Conventions shared by every call:
+ *   - All tensors are dense, row-major, vocabulary (V) fastest.  Logits are bf16 (raw 16-bit
+ *     patterns) or fp32 (spec_dtype).  Any alignment works; rows whose start is 16-byte aligned
+ *     are read with 16-byte vector loads.
+ *   - Every pointer passed to a verify call is a DEVICE pointer owned by the caller.  The library
+ *     allocates nothing and never modifies inputs.  `stream` is a cudaStream_t (NULL = legacy
+ *     default stream); all work is enqueued asynchronously on it and the host never waits.
+ *   - `workspace` is caller-owned device scratch of at least spec_workspace_bytes(...) bytes,
+ *     16-byte aligned.  Its contents need no initialisation: each call first clears the few
+ *     completion counters it uses (one cudaMemsetAsync on `stream`), then launches its kernels.
+ *     Calls that share a workspace must not overlap on the GPU (issue them on one stream).
+ *   - Call-level status (the return value) covers what the host can check: sizes, temperature,
+ *     top_k, null or misaligned pointers, workspace size, and CUDA launch errors.  Per-request
+ *     conditions found on the device are reported in row_status[b] (SPEC_ROW_*); such a request
+ *     emits nothing: accepted_len[b] = -1 and every out_tokens entry of the request is -1.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* a size, temperature, top_k or pointer failed host validation */
+    SPEC_ERR_CUDA = 2,        /* a CUDA launch, memset or attribute call failed */
+    SPEC_ERR_WORKSPACE = 3    /* workspace missing, misaligned or smaller than required */
+} spec_status;
+
+/* Per-request status codes written to row_status[b]. */
+enum {
+    SPEC_ROW_OK = 0,
+    SPEC_ROW_NONFINITE = 1,            /* a logit row of the request holds NaN or +inf, or has no
+                                          finite entry left after the processors */
+    SPEC_ROW_DEGENERATE_RESIDUAL = 2,  /* the correction residual mass is not positive */
+    SPEC_ROW_BAD_TOKEN = 3,            /* a draft / node token is outside [0, V), or a drafted
+                                          token has q(x) = 0 (it cannot have been sampled) */
+    SPEC_ROW_TIMEOUT = 4,              /* reserved: no kernel of this library waits on a flag */
+    SPEC_ROW_BAD_PARENT = 5,           /* tree: parents[b,i] is not in [-1, i) */
+    SPEC_ROW_OUTPUT_OVERFLOW = 6,      /* tree: accepted path + bonus does not fit in max_out */
+    SPEC_ROW_BAD_UNIFORM = 7           /* a uniform of the request is not in [0, 1) */
+};
+
+/*
+ * Bytes of workspace needed by one call.
+ *   spec_verify:        spec_workspace_bytes(B, gamma, V, 0, 0)
+ *   spec_verify_topk:   spec_workspace_bytes(B, gamma, V, top_k, 0)
+ *   tree_verify_greedy: spec_workspace_bytes(B, 0, V, 0, N)   (tree_nodes = N > 0)
+ * The value is an upper bound valid for both dtypes, any alignment and any GPU.
+ * Returns 0 for invalid sizes.
+ */
+size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes);
+
+/*
+ * Exact speculative sampling verify (M7.1 0x03-0x04; Module 16 accept rule).
+ *
+ *   target_logits [B, gamma+1, V]  row i < gamma scores draft token i; row gamma scores the
+ *                                  bonus position after the whole draft
+ *   draft_logits  [B, gamma, V]    row i is the draft row that sampled draft token i
+ *                                  (may be NULL when gamma == 0)
+ *   draft_tokens  [B, gamma]       int32
+ *   uniforms      [B, gamma+2]     fp32 in [0, 1): slots 0..gamma-1 are the accept draws,
+ *                                  slot gamma the correction draw, slot gamma+1 the bonus draw
+ *   temperature   > 0, finite;     p = softmax(target/T), q = softmax(draft/T)
+ *
+ * With A = the first i such that u[b,i] >= min(1, p_i(x_i)/q_i(x_i)) (A = gamma if none):
+ *   accepted_len[b] = A
+ *   out_tokens[b, 0..A-1] = draft_tokens[b, 0..A-1]
+ *   out_tokens[b, A]      = correction: inverse-CDF draw with u[b,gamma] from max(p_A - q_A, 0)
+ *                           when A < gamma; bonus: inverse-CDF draw with u[b,gamma+1] from p_gamma
+ *                           when A == gamma.  The draw is the smallest token v, in ascending
+ *                           index order, whose running mass exceeds u * (total mass).
+ *   out_tokens[b, A+1..gamma] = -1
+ * Optional outputs (NULL to skip): row_status [B]; aux_lse_p [B, gamma+1] and aux_lse_q
+ * [B, gamma] (natural-log normaliser of logits/T over the kept tokens); aux_accept [B, gamma]
+ * (min(1, p_i(x_i)/q_i(x_i)) at every position, reached or not).
+ */
+spec_status spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                        const int32_t* draft_tokens, const float* uniforms,
+                        int B, int gamma, int V, float temperature,
+                        int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                        float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify with a top-k processor on both p and q (M7.1 0x03D: truncation keeps exactness when
+ * q is the truncated distribution that sampled the draft).  Each row keeps every token whose
+ * stored logit is >= the row's k-th largest stored logit (counted with multiplicity, signed zeros
+ * equal), so ties at the threshold are all kept; the rest get probability 0.  top_k in [1, V];
+ * top_k == V is identical to spec_verify.  Other arguments as spec_verify.
+ */
+spec_status spec_verify_topk(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                             const int32_t* draft_tokens, const float* uniforms,
+                             int B, int gamma, int V, float temperature, int top_k,
+                             int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                             float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Greedy tree verify (Module 16 "Verify the Tree"; M7.7 0x07E row convention).
+ *
+ *   logits  [B, N+1, V]  row 0 = prefix-frontier logits, row i+1 = logits produced at node i
+ *   parents [B, N]       int32, parents[b,i] in [-1, i) (-1: depth-1 node)
+ *   tokens  [B, N]       int32 candidate token of each node
+ *   max_out >= 1         length of an out_tokens row; must hold depth(best)+1 entries
+ *
+ * amax(row) = argmax over V, ties to the lowest index.  Node i is valid when tokens[i] ==
+ * amax(predictor row of i) and its parent is valid.  The accepted node is the deepest valid node
+ * (lowest index on ties); with none valid, nothing is accepted.
+ *   accepted_len[b]                = depth of the accepted node (0 if none)
+ *   out_tokens[b, 0..A-1]          = tokens on the root->node path; out_tokens[b, A] = amax of the
+ *                                    accepted node's own row (row 0 if none); rest -1
+ *   out_nodes [B, max_out-1]       = node ids on the path, then -1 (nullable)
+ *   row_status [B]                 nullable
+ */
+spec_status tree_verify_greedy(const void* logits, spec_dtype dtype,
+                               const int32_t* parents, const int32_t* tokens,
+                               int B, int N, int V, int max_out,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                               int32_t* row_status, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Static description of a call-level status code. */
+const char* spec_status_string(spec_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,16 @@
+"""GB300 (sm_103a) speculative-decoding verify step: exact speculative sampling, its top-k
+variant, and greedy tree verify, as hand-written CUDA behind a C ABI (include/spec_verify.h).
+
+The binding functions load the compiled library on first use and raise if it is missing: there is
+no CPU fallback.
+"""
+from .binding import (  # noqa: F401
+    EXPORTS,
+    SpecVerifyError,
+    Workspace,
+    load,
+    spec_verify,
+    spec_verify_topk,
+    tree_verify_greedy,
+    workspace_bytes,
+)

@@ -1,0 +1,182 @@
+"""Thin ctypes binding over the C ABI in ``include/spec_verify.h``.
+
+Argument marshalling only: every step of the verify path runs in the CUDA kernels of
+``libspecverify.so``.  PyTorch supplies device memory and the current stream.  There is no CPU
+fallback: if the library is missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build_ext
+
+SPEC_F32, SPEC_BF16 = 0, 1
+ROW_OK, ROW_NONFINITE, ROW_DEGENERATE, ROW_BAD_TOKEN, ROW_TIMEOUT = 0, 1, 2, 3, 4
+ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM = 5, 6, 7
+
+# every symbol the header declares
+EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
+           "spec_status_string")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def load(path: str | None = None):
+    """Load the compiled library (building it first if the sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or build_ext.LIB
+    if not os.path.exists(path):
+        raise SpecVerifyError(
+            f"CUDA extension {path} is missing; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.spec_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.spec_workspace_bytes.restype = Z
+    lib.spec_verify.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify.restype = I
+    lib.spec_verify_topk.argtypes = [P, P, I, P, P, I, I, I, F, I, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_topk.restype = I
+    lib.tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
+    lib.tree_verify_greedy.restype = I
+    lib.spec_status_string.argtypes = [I]
+    lib.spec_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise SpecVerifyError(load().spec_status_string(rc).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype in (torch.bfloat16, torch.int16):  # int16 = raw bf16 bit patterns
+        return SPEC_BF16
+    raise TypeError(f"logits must be bfloat16 (or its int16 bits) or float32, got {t.dtype}")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise SpecVerifyError("verify inputs must be CUDA tensors (there is no CPU path)")
+
+
+class Workspace:
+    """Device scratch for the verify calls, grown on demand (plain torch allocation)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(ws, device):
+    if ws is not None:
+        return ws
+    key = str(device)
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(device)
+    return _default_ws[key]
+
+
+def workspace_bytes(B, gamma, V, top_k=0, tree_nodes=0) -> int:
+    return int(load().spec_workspace_bytes(B, gamma, V, top_k, tree_nodes))
+
+
+def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, top_k: int = 0,
+                aux: bool = False, out=None, workspace: Workspace | None = None, stream=None):
+    """Exact speculative-sampling verify on the GPU.
+
+    target [B, gamma+1, V], draft [B, gamma, V] (bf16 / int16 bf16 bits / fp32, CUDA),
+    draft_tokens [B, gamma] int32, uniforms [B, gamma+2] fp32.  ``top_k`` > 0 applies the top-k
+    processor (spec_verify_topk).  Returns a dict of CUDA tensors: accepted_len, out_tokens,
+    row_status (and lse_p, lse_q, accept when ``aux``).
+    """
+    lib = load()
+    _need_cuda(target, draft, draft_tokens, uniforms)
+    B, g1, V = target.shape
+    gamma = g1 - 1
+    dev = target.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, gamma + 1, dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+        if aux:
+            out["lse_p"] = torch.empty(B, gamma + 1, dtype=torch.float32, device=dev)
+            out["lse_q"] = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+            out["accept"] = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+    nbytes = workspace_bytes(B, gamma, V, top_k)
+    ws = _workspace(workspace, dev).get(nbytes)
+    common = [_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tokens), _ptr(uniforms),
+              B, gamma, V, float(temperature)]
+    tail = [_ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out.get("row_status")),
+            _ptr(out.get("lse_p")), _ptr(out.get("lse_q")), _ptr(out.get("accept")),
+            _ptr(ws), ws.numel(), _stream(stream)]
+    if top_k:
+        rc = lib.spec_verify_topk(*common, int(top_k), *tail)
+    else:
+        rc = lib.spec_verify(*common, *tail)
+    _check(rc)
+    return out
+
+
+def spec_verify_topk(target, draft, draft_tokens, uniforms, temperature: float, top_k: int, **kw):
+    if top_k < 1:
+        raise ValueError("top_k must be >= 1")
+    return spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=top_k, **kw)
+
+
+def tree_verify_greedy(logits, parents, tokens, *, max_out: int | None = None, out=None,
+                       workspace: Workspace | None = None, stream=None):
+    """Greedy tree verify on the GPU.  logits [B, N+1, V]; parents, tokens [B, N] int32."""
+    lib = load()
+    _need_cuda(logits, parents, tokens)
+    B, n1, V = logits.shape
+    N = n1 - 1
+    max_out = N + 1 if max_out is None else int(max_out)
+    dev = logits.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, max_out, dtype=torch.int32, device=dev),
+            out_nodes=torch.empty(B, max(max_out - 1, 1), dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+    nbytes = workspace_bytes(B, 0, V, 0, max(N, 1))
+    ws = _workspace(workspace, dev).get(nbytes)
+    rc = lib.tree_verify_greedy(_ptr(logits), _dtype_code(logits), _ptr(parents), _ptr(tokens),
+                                B, N, V, max_out, _ptr(out["accepted_len"]),
+                                _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")),
+                                _ptr(out.get("row_status")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc)
+    return out

@@ -1,0 +1,349 @@
+// sv_capi.cu -- the C ABI (include/spec_verify.h): host-side validation, chunking, workspace
+// layout and kernel launches.  No allocation, no host synchronisation.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/spec_verify.h"
+#include "sv_common.cuh"
+
+namespace sv {
+
+constexpr size_t ALIGN = 256;
+static inline size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+static inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// --------------------------------------------------------------------------- chunking
+
+struct Shape {
+    int vec;
+    long long nvec;
+};
+
+static Shape row_shape(int V, int vec)
+{
+    Shape s;
+    s.vec = vec;
+    s.nvec = (vec == 1) ? V : V / vec;
+    return s;
+}
+
+static int stats_step(int vec) { return NT * ((vec == 1) ? 8 : 4); }  // vectors per CTA step
+static int max_c1(const Shape& s) { return (int)std::max(1LL, std::min(cdiv(s.nvec, stats_step(s.vec)), 32LL)); }
+static int max_c2(const Shape& s) { return (int)std::max(1LL, std::min(cdiv(s.nvec, NT), 64LL)); }
+
+static int pick_chunks(long long rows, int cmax, int sms, int per_sm)
+{
+    long long want = cdiv((long long)sms * per_sm, std::max(1LL, rows));
+    return (int)std::max(1LL, std::min((long long)cmax, want));
+}
+
+static int topk_ept(int dtype) { return dtype == DT_BF16 ? 80 : 40; }
+static int topk_cap(int k) { return (int)std::min(2048LL, (long long)((2 * (long long)k + 64 + 31) / 32 * 32)); }
+
+// --------------------------------------------------------------------------- workspace layout
+
+struct SpecLayout {
+    size_t ctr_bytes = 0, bytes = 0;
+    size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0;
+    size_t o_partials = 0, o_rstats = 0, o_plan = 0, o_segs = 0;
+    size_t o_clist = 0, o_ccount = 0, o_klist = 0;
+};
+
+// Sizes for given chunk counts (C1, nseg = segments per request, CT, cap).
+static SpecLayout spec_layout(int B, int R, int C1, long long nseg, bool topk, int CT, int cap)
+{
+    SpecLayout L;
+    size_t o = 0;
+    L.o_row_ctr = o; o += (size_t)B * R * sizeof(unsigned);
+    L.o_req_ctr = o; o += (size_t)B * sizeof(unsigned);
+    L.o_res_ctr = o; o += (size_t)B * sizeof(unsigned);
+    L.o_dense_ctr = o; o += (size_t)B * sizeof(unsigned);
+    L.o_ndense = o; o += (size_t)B * sizeof(int);
+    L.ctr_bytes = o;
+    o = align_up(o);
+    L.o_partials = o; o = align_up(o + (size_t)B * R * C1 * sizeof(Partial));
+    L.o_rstats = o; o = align_up(o + (size_t)B * R * sizeof(RowStats));
+    L.o_plan = o; o = align_up(o + (size_t)B * sizeof(Plan));
+    L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
+    if (topk) {
+        L.o_clist = o; o = align_up(o + (size_t)B * R * CT * cap * sizeof(TopkEntry));
+        L.o_ccount = o; o = align_up(o + (size_t)B * R * CT * sizeof(int));
+        L.o_klist = o; o = align_up(o + (size_t)B * R * cap * sizeof(TopkEntry));
+    }
+    L.bytes = o;
+    return L;
+}
+
+static long long max_segments(const Shape& s)
+{
+    long long best = 0;
+    for (int c2 = 1; c2 <= max_c2(s); ++c2) {
+        long long cv = cdiv(s.nvec, c2);
+        best = std::max(best, (long long)c2 * cdiv(cv, NT) * WARPS);
+    }
+    return best;
+}
+
+struct TreeLayout {
+    size_t ctr_bytes = 0, bytes = 0;
+    size_t o_req_ctr = 0, o_partials = 0, o_amax = 0, o_scratch = 0;
+};
+
+static TreeLayout tree_layout(int B, int N, int C)
+{
+    TreeLayout L;
+    const int R = N + 1;
+    size_t o = 0;
+    L.o_req_ctr = o; o += (size_t)B * sizeof(unsigned);
+    L.ctr_bytes = o;
+    o = align_up(o);
+    L.o_partials = o; o = align_up(o + (size_t)B * R * C * sizeof(ArgmaxPartial));
+    L.o_amax = o; o = align_up(o + (size_t)B * R * sizeof(int32_t));
+    L.o_scratch = o; o = align_up(o + (size_t)B * (N > 0 ? N : 1) * 2 * sizeof(int32_t));
+    L.bytes = o;
+    return L;
+}
+
+// --------------------------------------------------------------------------- device queries
+
+static int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static int pick_vec(int dtype, int V, const void* a, const void* b)
+{
+    const size_t es = dtype == DT_BF16 ? 2 : 4;
+    const int vec = dtype == DT_BF16 ? 8 : 4;
+    if (((size_t)V * es) % 16 != 0) return 1;
+    if (!aligned(a, 16)) return 1;
+    if (b && !aligned(b, 16)) return 1;
+    return vec;
+}
+
+// --------------------------------------------------------------------------- launches
+
+static spec_status spec_common(const void* target, const void* draft, spec_dtype dtype,
+                               const int32_t* tokens, const float* uniforms, int B, int gamma,
+                               int V, float temperature, int top_k, int32_t* accepted_len,
+                               int32_t* out_tokens, int32_t* row_status, float* aux_lse_p,
+                               float* aux_lse_q, float* aux_accept, void* workspace,
+                               size_t workspace_bytes, void* stream)
+{
+    if (B < 0 || gamma < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+    const double T = (double)temperature;
+    const float c = (float)(1.4426950408889634 / T);
+    if (!std::isfinite(c) || !(c > 0.0f)) return SPEC_ERR_INVALID_ARG;
+    if (top_k < 0 || top_k > V) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    const int R = 2 * gamma + 1;
+    if ((long long)B * R > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+    const size_t es = dtype == SPEC_BF16 ? 2 : 4;
+    if (!target || !aligned(target, es)) return SPEC_ERR_INVALID_ARG;
+    if (gamma > 0 && (!draft || !aligned(draft, es) || !tokens || !aligned(tokens, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_INVALID_ARG;
+    if (!accepted_len || !out_tokens || !aligned(accepted_len, 4) || !aligned(out_tokens, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if ((row_status && !aligned(row_status, 4)) || (aux_lse_p && !aligned(aux_lse_p, 4)) ||
+        (aux_lse_q && !aligned(aux_lse_q, 4)) || (aux_accept && !aligned(aux_accept, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16)) return SPEC_ERR_WORKSPACE;
+
+    const bool topk = top_k > 0 && top_k < V;
+    const int dt = (dtype == SPEC_BF16) ? DT_BF16 : DT_F32;
+    const int vec = pick_vec(dt, V, target, gamma > 0 ? draft : nullptr);
+    const Shape sh = row_shape(V, vec);
+    const int sms = sm_count();
+
+    SpecParams P;
+    std::memset(&P, 0, sizeof P);
+    P.target = target;
+    P.draft = draft;
+    P.tokens = tokens;
+    P.uniforms = uniforms;
+    P.B = B; P.gamma = gamma; P.V = V; P.R = R;
+    P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
+    P.c = c; P.T = T; P.top_k = top_k;
+    P.C1 = pick_chunks((long long)B * R, max_c1(sh), sms, 16);
+    P.cv1 = cdiv(sh.nvec, P.C1);
+    P.C2 = pick_chunks(B, max_c2(sh), sms, 8);
+    P.cv2 = cdiv(sh.nvec, P.C2);
+    P.iters2 = (int)cdiv(P.cv2, NT);
+    const long long nseg = (long long)P.C2 * P.iters2 * WARPS;
+    if (topk) {
+        P.CT = (int)cdiv(V, (long long)NT * topk_ept(dt));
+        P.cvt = 0;
+        P.cap_w = topk_cap(top_k);
+        P.cap_k = P.cap_w;
+    }
+    const SpecLayout L = spec_layout(B, R, P.C1, nseg, topk, P.CT, P.cap_w);
+    if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+    if ((long long)B * R * std::max(P.C1, topk ? P.CT : 1) >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+
+    char* ws = static_cast<char*>(workspace);
+    P.accepted_len = accepted_len;
+    P.out_tokens = out_tokens;
+    P.row_status = row_status;
+    P.aux_lse_p = aux_lse_p;
+    P.aux_lse_q = aux_lse_q;
+    P.aux_accept = aux_accept;
+    P.row_ctr = reinterpret_cast<unsigned*>(ws + L.o_row_ctr);
+    P.req_ctr = reinterpret_cast<unsigned*>(ws + L.o_req_ctr);
+    P.res_ctr = reinterpret_cast<unsigned*>(ws + L.o_res_ctr);
+    P.dense_ctr = reinterpret_cast<unsigned*>(ws + L.o_dense_ctr);
+    P.ndense = reinterpret_cast<int*>(ws + L.o_ndense);
+    P.partials = reinterpret_cast<Partial*>(ws + L.o_partials);
+    P.rstats = reinterpret_cast<RowStats*>(ws + L.o_rstats);
+    P.plan = reinterpret_cast<Plan*>(ws + L.o_plan);
+    P.segs = reinterpret_cast<float*>(ws + L.o_segs);
+    if (topk) {
+        P.clist = reinterpret_cast<TopkEntry*>(ws + L.o_clist);
+        P.ccount = reinterpret_cast<int*>(ws + L.o_ccount);
+        P.klist = reinterpret_cast<TopkEntry*>(ws + L.o_klist);
+    }
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+    cudaError_t err;
+    if (!topk) {
+        const unsigned g1 = (unsigned)((long long)B * R * P.C1), g2 = (unsigned)((long long)B * P.C2);
+        err = launch_softmax_path(P, g1, g2, st);
+    } else {
+        const unsigned g1 = (unsigned)((long long)B * R * P.CT), g2 = (unsigned)((long long)B * R);
+        err = launch_topk_path(P, g1, g2, st);
+    }
+    return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
+{
+    if (B < 0 || gamma < 0 || V < 1 || top_k < 0 || tree_nodes < 0) return 0;
+    size_t best = ALIGN;
+    for (int vec : {1, 4, 8}) {
+        const Shape sh = row_shape(V, vec);
+        if (tree_nodes > 0) {
+            const TreeLayout L = tree_layout(B, tree_nodes, max_c1(sh));
+            best = std::max(best, L.bytes);
+        } else {
+            const bool topk = top_k > 0 && top_k < V;
+            int CT = 0;
+            if (topk) CT = (int)cdiv(V, (long long)NT * std::min(topk_ept(DT_BF16), topk_ept(DT_F32)));
+            const SpecLayout L = spec_layout(B, 2 * gamma + 1, max_c1(sh), max_segments(sh), topk,
+                                             CT, topk ? topk_cap(top_k) : 0);
+            best = std::max(best, L.bytes);
+        }
+    }
+    return best;
+}
+
+spec_status spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                        const int32_t* draft_tokens, const float* uniforms, int B, int gamma, int V,
+                        float temperature, int32_t* accepted_len, int32_t* out_tokens,
+                        int32_t* row_status, float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                        void* workspace, size_t workspace_bytes, void* stream)
+{
+    return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
+                       temperature, 0, accepted_len, out_tokens, row_status, aux_lse_p, aux_lse_q,
+                       aux_accept, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_verify_topk(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                             const int32_t* draft_tokens, const float* uniforms, int B, int gamma,
+                             int V, float temperature, int top_k, int32_t* accepted_len,
+                             int32_t* out_tokens, int32_t* row_status, float* aux_lse_p,
+                             float* aux_lse_q, float* aux_accept, void* workspace,
+                             size_t workspace_bytes, void* stream)
+{
+    if (top_k < 1 || top_k > V) return SPEC_ERR_INVALID_ARG;
+    return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
+                       temperature, top_k, accepted_len, out_tokens, row_status, aux_lse_p,
+                       aux_lse_q, aux_accept, workspace, workspace_bytes, stream);
+}
+
+spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32_t* parents,
+                               const int32_t* tokens, int B, int N, int V, int max_out,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                               int32_t* row_status, void* workspace, size_t workspace_bytes,
+                               void* stream)
+{
+    if (B < 0 || N < 0 || V < 1 || max_out < 1) return SPEC_ERR_INVALID_ARG;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    const int R = N + 1;
+    if ((long long)B * R > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+    const size_t es = dtype == SPEC_BF16 ? 2 : 4;
+    if (!logits || !aligned(logits, es)) return SPEC_ERR_INVALID_ARG;
+    if (N > 0 && (!parents || !tokens || !aligned(parents, 4) || !aligned(tokens, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!accepted_len || !out_tokens || !aligned(accepted_len, 4) || !aligned(out_tokens, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if ((out_nodes && !aligned(out_nodes, 4)) || (row_status && !aligned(row_status, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16)) return SPEC_ERR_WORKSPACE;
+
+    const int dt = (dtype == SPEC_BF16) ? DT_BF16 : DT_F32;
+    const int vec = pick_vec(dt, V, logits, nullptr);
+    const Shape sh = row_shape(V, vec);
+    TreeParams P;
+    std::memset(&P, 0, sizeof P);
+    P.logits = logits;
+    P.parents = parents;
+    P.tokens = tokens;
+    P.B = B; P.N = N; P.V = V; P.R = R;
+    P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
+    P.C = pick_chunks((long long)B * R, max_c1(sh), sm_count(), 16);
+    P.cv = cdiv(sh.nvec, P.C);
+    P.max_out = max_out;
+    const TreeLayout L = tree_layout(B, N, P.C);
+    if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+    if ((long long)B * R * P.C >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+    char* ws = static_cast<char*>(workspace);
+    P.accepted_len = accepted_len;
+    P.out_tokens = out_tokens;
+    P.out_nodes = (max_out > 1) ? out_nodes : nullptr;
+    P.row_status = row_status;
+    P.req_ctr = reinterpret_cast<unsigned*>(ws + L.o_req_ctr);
+    P.partials = reinterpret_cast<ArgmaxPartial*>(ws + L.o_partials);
+    P.amax = reinterpret_cast<int32_t*>(ws + L.o_amax);
+    P.scratch = reinterpret_cast<int32_t*>(ws + L.o_scratch);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+    const unsigned grid = (unsigned)((long long)B * R * P.C);
+    const cudaError_t err = launch_tree_path(P, grid, st);
+    return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+const char* spec_status_string(spec_status s)
+{
+    switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_CUDA: return "CUDA launch error";
+    case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,349 @@
+// sv_common.cuh -- shared device helpers, parameter blocks and workspace layout of the GB300
+// speculative-decoding verify kernels.
+//
+// Arithmetic conventions used by every kernel:
+//   * logits are read as fp32 (bf16 is widened exactly by a 16-bit shift);
+//   * with c = log2(e)/T in fp32, a row's normaliser is kept as (MC, S) with MC = fp32(M * c),
+//     M the row maximum, and S = sum_v 2^(fma(x_v, c, -MC)), so that p(v) = 2^(fma(x_v,c,-MC)) / S.
+//     fma() rounds once after the exact product, so the exponent carries only a small error near
+//     the row maximum, where probability mass sits; the rounding of MC shifts every exponent of a
+//     row equally and cancels between numerator and S.
+//   * per-thread and per-warp partial sums are fp32; sums across warps, chunks and segments are
+//     fp64, always in a fixed order, so results do not depend on CTA scheduling.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int NT = 256;           // threads per CTA, every kernel
+constexpr int WARPS = NT / 32;
+constexpr float NEG_INF = -__builtin_huge_valf();
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum {
+    ROW_OK = 0,
+    ROW_NONFINITE = 1,
+    ROW_DEGENERATE = 2,
+    ROW_BAD_TOKEN = 3,
+    ROW_BAD_PARENT = 5,
+    ROW_OVERFLOW = 6,
+    ROW_BAD_UNIFORM = 7
+};
+
+// ---------------------------------------------------------------- workspace records
+
+struct Partial {      // one (row, chunk) of the softmax statistics
+    float M;          // chunk maximum of the raw logits (-inf if none)
+    float MC;         // fp32(M * c)
+    double S;         // sum over the chunk of 2^(fma(x, c, -MC))
+};
+
+struct RowStats {     // one logit row after its chunks are combined
+    float M, MC;
+    double S;
+    float thr;        // top-k threshold on the stored logit (-inf without top-k)
+    int status;       // ROW_OK or ROW_NONFINITE
+    int klist_n;      // top-k: number of kept (index, value) pairs listed, -1 if not listed
+    int dense;        // top-k: row needs the exact fallback path
+};
+
+struct Plan {         // one request, after the acceptance scan
+    int status;
+    int A;            // accepted draft count
+    int rp, rq;       // row of p (target) and q (draft, -1 for the bonus draw)
+    float MCp, MCq, invSp, invSq, thrp, thrq;
+    double u;         // correction or bonus uniform
+};
+
+struct TopkEntry {    // one kept top-k candidate
+    float x;
+    int idx;
+};
+
+struct ArgmaxPartial {
+    float best;
+    int idx;
+    int nan;
+    int pad;
+};
+
+// ---------------------------------------------------------------- parameter blocks
+
+struct SpecParams {
+    const void* target;   // [B, gamma+1, V]
+    const void* draft;    // [B, gamma, V]
+    const int32_t* tokens;
+    const float* uniforms;
+    int B, gamma, V, R;   // R = 2*gamma+1 rows per request
+    int dtype, vec;       // elements per vector load (8 bf16 / 4 fp32 / 1 unaligned)
+    long long nvec;       // vectors per row
+    float c;              // log2(e)/T
+    double T;
+    int top_k;
+    // stats chunking
+    int C1;
+    long long cv1;
+    // resample chunking
+    int C2, iters2;
+    long long cv2;
+    // top-k chunking and capacities
+    int CT;
+    long long cvt;
+    int cap_w;            // per-chunk list capacity (entries)
+    int cap_k;            // per-row kept-list capacity
+    // outputs
+    int32_t* accepted_len;
+    int32_t* out_tokens;
+    int32_t* row_status;
+    float* aux_lse_p;
+    float* aux_lse_q;
+    float* aux_accept;
+    // workspace
+    Partial* partials;    // [B*R*C1]
+    RowStats* rstats;     // [B*R]
+    Plan* plan;           // [B]
+    float* segs;          // [B*C2*iters2*WARPS]
+    unsigned* row_ctr;    // [B*R]
+    unsigned* req_ctr;    // [B]
+    unsigned* res_ctr;    // [B]
+    TopkEntry* clist;     // [B*R*CT*cap_w] per-chunk candidate lists
+    int* ccount;          // [B*R*CT] entries per chunk list (-1 = overflow)
+    TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
+    unsigned* dense_ctr;  // [B]
+    int* ndense;          // [B]
+};
+
+struct TreeParams {
+    const void* logits;   // [B, N+1, V]
+    const int32_t* parents;
+    const int32_t* tokens;
+    int B, N, V, R;       // R = N+1
+    int dtype, vec;
+    long long nvec;
+    int C;
+    long long cv;
+    int max_out;
+    int32_t* accepted_len;
+    int32_t* out_tokens;
+    int32_t* out_nodes;
+    int32_t* row_status;
+    ArgmaxPartial* partials;  // [B*R*C]
+    unsigned* req_ctr;        // [B]
+    int32_t* amax;            // [B*R]
+    int32_t* scratch;         // [B*N*2] depth / valid of each node
+};
+
+// ---------------------------------------------------------------- small device helpers
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// packed bf16x2 maximum; NaN lanes are ignored unless both inputs are NaN
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// packed bf16x2 maximum that propagates NaN
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// one logit as fp32 (scalar path)
+__device__ __forceinline__ float load_logit(const void* row, int dtype, long long i)
+{
+    if (dtype == DT_BF16) {
+        unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+        return __uint_as_float(((uint32_t)h) << 16);
+    }
+    return __ldg(reinterpret_cast<const float*>(row) + i);
+}
+
+__device__ __forceinline__ size_t esize(int dtype) { return dtype == DT_BF16 ? 2 : 4; }
+
+// request b, row r (r <= gamma: target row r; r > gamma: draft row r - gamma - 1)
+__device__ __forceinline__ const char* spec_row_ptr(const SpecParams& P, int b, int r)
+{
+    const size_t es = esize(P.dtype);
+    if (r <= P.gamma)
+        return reinterpret_cast<const char*>(P.target) +
+               ((size_t)b * (P.gamma + 1) + r) * (size_t)P.V * es;
+    return reinterpret_cast<const char*>(P.draft) +
+           ((size_t)b * P.gamma + (r - P.gamma - 1)) * (size_t)P.V * es;
+}
+
+// Vector v of a row as fp32 values.  VEC = 8 (bf16, 16-byte aligned rows), 4 (fp32, aligned) or
+// 1 (any layout).  Only called for in-range vectors.
+template <int DT, int VEC>
+__device__ __forceinline__ void load_vec(const char* row, long long v, float (&x)[VEC])
+{
+    if constexpr (VEC == 1) {
+        x[0] = load_logit(row, DT, v);
+    } else if constexpr (DT == DT_BF16) {
+        static_assert(VEC == 8, "bf16 vectors hold 8 values");
+        uint4 w = ld_stream_v4(row + v * 16);
+        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+        x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+    } else {
+        static_assert(VEC == 4, "fp32 vectors hold 4 values");
+        uint4 w = ld_stream_v4(row + v * 16);
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// inclusive prefix sum across a warp
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        T n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// block-wide maximum (all threads receive it)
+__device__ __forceinline__ float block_max(float v, float* sh /* >= WARPS floats */)
+{
+    v = warp_max(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = sh[0];
+#pragma unroll
+    for (int w = 1; w < WARPS; ++w) r = fmaxf(r, sh[w]);
+    return r;
+}
+
+// block-wide sum: fp32 within warps, fp64 across warps in warp order (all threads receive it)
+__device__ __forceinline__ double block_sum_f32(float v, double* sh /* >= WARPS doubles */)
+{
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = (double)v;
+    __syncthreads();
+    double r = 0.0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) r += sh[w];
+    return r;
+}
+
+__device__ __forceinline__ int block_sum_int(int v, int* sh)
+{
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int r = 0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) r += sh[w];
+    return r;
+}
+
+// block-wide exclusive prefix sum in fp64 (thread order); returns the exclusive prefix and
+// writes the total to *total
+__device__ __forceinline__ double block_excl_scan_f64(double v, double* sh, double* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const double incl = warp_incl_scan(v);
+    __syncthreads();
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    double before = 0.0, tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+        if (w < warp) before += sh[w];
+        tot += sh[w];
+    }
+    *total = tot;
+    return before + (incl - v);
+}
+
+// Arrive on a completion counter after this CTA's global writes; returns true in every thread of
+// the CTA that arrived last.  Never waits.  The counters are cleared by the host call before the
+// first kernel of the call.
+__device__ __forceinline__ bool arrive_last(unsigned* ctr, unsigned expected, int* sh_flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        unsigned prev = atomicAdd(ctr, 1u);
+        int last = (prev == expected - 1);
+        if (last) __threadfence();
+        *sh_flag = last;
+    }
+    __syncthreads();
+    return *sh_flag != 0;
+}
+
+// ---------------------------------------------------------------- outputs
+
+// Writes a request's outputs: the accepted draft prefix, the drawn token, -1 padding.
+__device__ __forceinline__ void emit_spec(const SpecParams& P, int b, int status, int A, int tok)
+{
+    const int g = P.gamma;
+    int32_t* out = P.out_tokens + (size_t)b * (g + 1);
+    const int32_t* dt = P.tokens + (size_t)b * g;
+    for (int i = threadIdx.x; i <= g; i += NT) {
+        int v = -1;
+        if (status == ROW_OK) v = (i < A) ? dt[i] : (i == A ? tok : -1);
+        out[i] = v;
+    }
+    if (threadIdx.x == 0) {
+        P.accepted_len[b] = (status == ROW_OK) ? A : -1;
+        if (P.row_status) P.row_status[b] = status;
+    }
+}
+
+// ---------------------------------------------------------------- host launchers (one per .cu)
+
+// spec_stats_kernel + spec_resample_kernel for the dtype / vector width in P
+cudaError_t launch_softmax_path(const SpecParams& P, unsigned grid_stats, unsigned grid_resample,
+                                cudaStream_t st);
+// topk_stats_kernel + topk_dense_kernel
+cudaError_t launch_topk_path(const SpecParams& P, unsigned grid_stats, unsigned grid_dense,
+                             cudaStream_t st);
+// tree_argmax_kernel
+cudaError_t launch_tree_path(const TreeParams& P, unsigned grid, cudaStream_t st);
+
+}  // namespace sv

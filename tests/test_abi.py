@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every function the header declares; host-side
+argument validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import speculative_decoding_verification_spec_gb300 as sv
+from speculative_decoding_verification_spec_gb300 import build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[a-z_ ]+?[\s\*]+([a-z_]+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_ext.build()
+    return sv.load()
+
+
+def test_header_declares_the_three_verify_calls():
+    names = declared_functions()
+    for n in ("spec_verify", "spec_verify_topk", "tree_verify_greedy", "spec_workspace_bytes",
+              "spec_status_string"):
+        assert n in names
+    assert set(names) == set(sv.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build_ext.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_workspace_bytes(lib):
+    a = sv.workspace_bytes(64, 5, 128256)
+    assert a > 0 and a % 256 == 0
+    assert sv.workspace_bytes(128, 5, 128256) >= a
+    assert sv.workspace_bytes(64, 5, 128256, 50) > a
+    assert sv.workspace_bytes(32, 0, 128256, 0, 64) > 0
+    assert lib.spec_workspace_bytes(-1, 5, 10, 0, 0) == 0
+    assert lib.spec_workspace_bytes(1, 5, 0, 0, 0) == 0
+
+
+def test_host_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: validation fails first
+    ws = P(0x20000)
+    INVALID, WORKSPACE = 1, 3
+
+    def sv_call(B=2, gamma=3, V=100, T=1.0, dtype=1, target=fake, draft=fake, tok=fake, u=fake,
+                acc=fake, out=fake, wsp=ws, wsb=1 << 30, topk=None):
+        args = [target, draft, dtype, tok, u, B, gamma, V, T]
+        tail = [acc, out, None, None, None, None, wsp, wsb, None]
+        if topk is None:
+            return lib.spec_verify(*args, *tail)
+        return lib.spec_verify_topk(*args, topk, *tail)
+
+    assert sv_call(B=0) == 0
+    assert sv_call(B=-1) == INVALID
+    assert sv_call(gamma=-1) == INVALID
+    assert sv_call(V=0) == INVALID
+    assert sv_call(T=0.0) == INVALID
+    assert sv_call(T=float("nan")) == INVALID
+    assert sv_call(T=float("inf")) == INVALID
+    assert sv_call(T=1e-45) == INVALID
+    assert sv_call(dtype=7) == INVALID
+    assert sv_call(target=None) == INVALID
+    assert sv_call(draft=None) == INVALID
+    assert sv_call(u=None) == INVALID
+    assert sv_call(out=None) == INVALID
+    assert sv_call(target=P(0x10001)) == INVALID       # bf16 needs 2-byte alignment
+    assert sv_call(wsp=None) == WORKSPACE
+    assert sv_call(wsp=P(0x20008)) == WORKSPACE       # 16-byte alignment
+    assert sv_call(wsb=16) == WORKSPACE
+    assert sv_call(topk=0) == INVALID
+    assert sv_call(topk=101) == INVALID
+    assert lib.tree_verify_greedy(fake, 1, fake, fake, 2, 4, 10, 0, fake, fake, None, None, ws,
+                                  1 << 30, None) == INVALID
+    assert lib.tree_verify_greedy(fake, 1, None, fake, 2, 4, 10, 5, fake, fake, None, None, ws,
+                                  1 << 30, None) == INVALID
+    assert lib.tree_verify_greedy(fake, 1, fake, fake, 2, 4, 10, 5, fake, fake, None, None, ws,
+                                  64, None) == WORKSPACE
+    assert lib.spec_status_string(0) == b"ok"
+
+
+def test_no_cpu_fallback_in_the_binding():
+    import torch
+    x = torch.zeros(1, 2, 8)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_verify(x, x[:, :1], torch.zeros(1, 1, dtype=torch.int32),
+                       torch.zeros(1, 3), 1.0)
