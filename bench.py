@@ -1,0 +1,445 @@
+"""Benchmark of the GB300 speculative-decoding verify step.
+
+One step = one pass of the whole hot path over one batch of synthetic inputs per workload:
+  c3  spec_verify       B=64  gamma=5 V=128256 bf16 T=0.7         (temperature softmax, residual)
+  c4  spec_verify_topk  B=256 gamma=7 V=152064 bf16 T=0.8 k=50    (top-k processor)
+  c5  tree_verify_greedy B=32 N=64(+1) V=128256 bf16              (greedy tree walk)
+issued back to back on one stream.  ``--workload`` selects a single configuration instead.
+
+value     logit rows per second, inputs resident in HBM (whole job, all ranks)
+e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
+          each step's inputs and a device -> host read of its outputs inside the timed region
+roofline  the dominant kernel (the top-k row statistics kernel of c4) against measured HBM copy
+          bandwidth; achieved = algorithmic bytes per launch / event-timed call duration
+cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the same workload
+
+Multi-GPU (torchrun): every rank verifies its own batch (independent requests, no collective on
+the data path); only the timing uses a barrier and a max over ranks.  ``--impl reference`` times
+the oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify rows/sec and achieved HBM GB/s (fraction of GB300 peak) per config"
+L2_BYTES = 129 * 10**6
+SUITE = ("c3", "c4", "c5")
+DOMINANT = ("c4", "topk_stats_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.cuh"])
+
+
+# ------------------------------------------------------------------ workloads
+
+def workload_batches(names, rank):
+    from speculative_decoding_verification_spec_gb300 import synth as S
+    out = {}
+    for n in names:
+        if n in S.CONFIGS:
+            cfg = S.CONFIGS[n]
+            out[n] = S.make_spec_batch(S.scaled(cfg, seed=cfg.seed + 7919 * rank))
+        else:
+            cfg = S.TREE_CONFIGS[n]
+            out[n] = S.make_tree_batch(S.scaled(cfg, seed=cfg.seed + 7919 * rank))
+    return out
+
+
+def describe(names):
+    from speculative_decoding_verification_spec_gb300 import synth as S
+    parts = []
+    for n in names:
+        if n in S.CONFIGS:
+            c = S.CONFIGS[n]
+            op = "spec_verify_topk" if c.top_k else "spec_verify"
+            parts.append(f"{n} {op} B={c.B} gamma={c.gamma} V={c.V} {c.dtype} T={c.temperature}"
+                         + (f" top_k={c.top_k}" if c.top_k else ""))
+        else:
+            c = S.TREE_CONFIGS[n]
+            parts.append(f"{n} tree_verify_greedy B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
+                         f"{c.dtype} tree {'/'.join(map(str, c.branching))}")
+    return " + ".join(parts)
+
+
+def kernels_per_call(name):
+    return 1 if name.startswith("c5") else 2
+
+
+# ------------------------------------------------------------------ clocks
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "speculative_decoding_verification_spec_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel, sha):
+    """dram bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[kernel]
+        if rec.get("source_sha") == sha:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(names, budget_s=15.0):
+    """The oracle as it stands, single thread, on a bounded sample of each workload."""
+    from oracle import oracle as O
+    batches = workload_batches(names, 0)
+    per_row_s, sample = {}, []
+    share = budget_s / len(names)
+    for n, b in batches.items():
+        rows_done, t_used, i = 0, 0.0, 0
+        B = b.logits.shape[0] if hasattr(b, "parents") else b.cfg.B
+        while t_used < share and i < B:
+            t0 = time.perf_counter()
+            if hasattr(b, "parents"):
+                O.tree_verify_greedy(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1])
+                rows_done += b.logits.shape[1]
+            else:
+                O.spec_verify(b.target[i:i + 1], b.draft[i:i + 1], b.draft_tokens[i:i + 1],
+                              b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k)
+                rows_done += 2 * b.cfg.gamma + 1
+            t_used += time.perf_counter() - t0
+            i += 1
+        per_row_s[n] = t_used / rows_done
+        sample.append(f"{n}: {i} requests ({rows_done} rows)")
+    rows = {n: batches[n].rows for n in names}
+    step_s = sum(per_row_s[n] * rows[n] for n in names)
+    return {"value": sum(rows.values()) / step_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": "; ".join(sample) + "; single-threaded fp64 C oracle, scaled to one step"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_spec_gb300 as sv
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    names = SUITE if args.workload == "suite" else (args.workload,)
+    batches = workload_batches(names, rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    host, devin, outs, wss = {}, {}, {}, {}
+    for n, b in batches.items():
+        if hasattr(b, "parents"):
+            arrs = dict(logits=b.logits, parents=b.parents, tokens=b.tokens)
+        else:
+            arrs = dict(target=b.target, draft=b.draft, tokens=b.draft_tokens, uniforms=b.uniforms)
+        host[n] = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16
+                                       else np.ascontiguousarray(v)).pin_memory()
+                   for k, v in arrs.items()}
+        devin[n] = {k: v.to(dev) for k, v in host[n].items()}
+        wss[n] = sv.Workspace(dev)
+
+    def call(n, ins, out=None):
+        b = batches[n]
+        if hasattr(b, "parents"):
+            return sv.tree_verify_greedy(ins["logits"], ins["parents"], ins["tokens"], out=out,
+                                         workspace=wss[n], stream=stream)
+        return sv.spec_verify(ins["target"], ins["draft"], ins["tokens"], ins["uniforms"],
+                              b.cfg.temperature, top_k=b.cfg.top_k, out=out, workspace=wss[n],
+                              stream=stream)
+
+    for n in names:  # allocate outputs once
+        outs[n] = call(n, devin[n])
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-resident timing
+    for _ in range(args.warmup):
+        for n in names:
+            call(n, devin[n], outs[n])
+    ev = {n: [] for n in names}
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(args.steps):
+            for n in names:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(n, devin[n], outs[n])
+                e1.record(stream)
+                ev[n].append((e0, e1))
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    elapsed = start.elapsed_time(end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    call_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_out = {n: {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                        for k, v in outs[n].items()} for n in names}
+        h2d = sum(v.numel() * v.element_size() for n in names for v in host[n].values())
+        d2h = sum(v.numel() * v.element_size() for n in names for v in host_out[n].values())
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for n in names:
+                for k, v in host[n].items():
+                    devin[n][k].copy_(v, non_blocking=True)
+                call(n, devin[n], outs[n])
+                for k, v in outs[n].items():
+                    host_out[n][k].copy_(v, non_blocking=True)
+            torch.cuda.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_el = s0.elapsed_time(s1) / 1e3
+        if world > 1:
+            t = torch.tensor([e_el], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_el = float(t.item())
+        rows_step = sum(batches[n].rows for n in names)
+        e2e = {"value": rows_step * world * e2e_steps / e_el, "unit": "rows/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": e2e_steps}
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peak()
+    rows_step = sum(batches[n].rows for n in names)
+    bytes_step = sum(batches[n].logit_bytes for n in names)
+    per_cfg = {}
+    for n in names:
+        gbs = batches[n].logit_bytes / (call_ms[n] / 1e3) / 1e9
+        per_cfg[n] = {"call_ms": round(call_ms[n], 5), "rows_per_s": batches[n].rows / (call_ms[n] / 1e3),
+                      "calls_per_s": 1e3 / call_ms[n], "logit_bytes": batches[n].logit_bytes,
+                      "hbm_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                      "frac_of_8tbs": round(gbs / 8000.0, 4)}
+    dom_cfg, dom_kernel, dom_files = DOMINANT
+    if dom_cfg not in names:
+        dom_cfg = names[0]
+        dom_kernel = "tree_argmax_kernel" if dom_cfg == "c5" else (
+            "topk_stats_kernel" if batches[dom_cfg].cfg.top_k else "spec_stats_kernel")
+        dom_files = ["sv_tree.cu" if dom_cfg == "c5" else
+                     ("sv_topk.cu" if dom_kernel == "topk_stats_kernel" else "sv_softmax.cu"),
+                     "sv_common.cuh", "sv_plan.cuh"]
+    sha = source_sha(dom_files)
+    achieved = batches[dom_cfg].logit_bytes / (call_ms[dom_cfg] / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": rows_step * world * args.steps / elapsed,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": describe(names), "input_dtype": "bf16",
+                   "logit_rows_per_step": rows_step, "logit_bytes_per_step": bytes_step,
+                   "l2": f"inputs larger than L2 ({bytes_step / 1e6:.0f} MB per step > 129 MB); no flush",
+                   "parallelism": f"replicas x{world} (independent requests per rank)"},
+        "hbm_gbs": bytes_step * world * args.steps / elapsed / 1e9,
+        "per_config": per_cfg,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "workload": dom_cfg,
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(dom_kernel, sha), "source_sha": sha,
+                     "timing": "event-timed verify call (counter memset + kernels) on its stream"},
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps * sum(kernels_per_call(n) for n in names),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(names, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    names = SUITE if args.workload == "suite" else (args.workload,)
+    from oracle import oracle as O
+    O.build()
+    batches = workload_batches(names, 0)
+    # each step verifies a bounded sample of every workload: one request each
+    def step(i):
+        rows = 0
+        for n in names:
+            b = batches[n]
+            if hasattr(b, "parents"):
+                j = i % b.logits.shape[0]
+                O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
+                rows += b.logits.shape[1]
+            else:
+                j = i % b.cfg.B
+                O.spec_verify(b.target[j:j + 1], b.draft[j:j + 1], b.draft_tokens[j:j + 1],
+                              b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.top_k)
+                rows += 2 * b.cfg.gamma + 1
+        return rows
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    rows = 0
+    for i in range(args.steps):
+        rows += step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = rows / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(names), "input_dtype": "bf16",
+                       "sample_per_step": "one request of each workload"},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": "one request of each workload per step, single thread"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5"], default="suite")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()
