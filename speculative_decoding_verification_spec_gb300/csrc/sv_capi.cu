@@ -1,4 +1,4 @@
-// sv_capi.cu -- the C ABI (include/spec_verify.h): host-side validation, chunking, workspace
+// sv_capi.cu -- the C ABI (include/spec_verify.h): host-side validation, task geometry, workspace
 // layout and kernel launches.  No allocation, no host synchronisation.
 #include <algorithm>
 #include <cmath>
@@ -14,7 +14,7 @@ constexpr size_t ALIGN = 256;
 static inline size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 static inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// --------------------------------------------------------------------------- chunking
+// --------------------------------------------------------------------------- geometry
 
 struct Shape {
     int vec;
@@ -29,30 +29,34 @@ static Shape row_shape(int V, int vec)
     return s;
 }
 
-static int stats_step(int vec) { return NT * ((vec == 1) ? 8 : 4); }  // vectors per CTA step
-static int max_c1(const Shape& s) { return (int)std::max(1LL, std::min(cdiv(s.nvec, stats_step(s.vec)), 32LL)); }
-static int max_c2(const Shape& s) { return (int)std::max(1LL, std::min(cdiv(s.nvec, NT), 64LL)); }
-
-static int pick_chunks(long long rows, int cmax, int sms, int per_sm)
+static long long slices1(const Shape& s) { return std::max(1LL, cdiv(s.nvec, TV1)); }
+static long long chunks1(const Shape& s) { return std::max(1LL, cdiv(s.nvec, CHUNK_VECS)); }
+// softmax partials per row: one per warp task (scalar path) or one per warp of each chunk CTA
+static long long partials_per_row(const Shape& s)
 {
-    long long want = cdiv((long long)sms * per_sm, std::max(1LL, rows));
-    return (int)std::max(1LL, std::min((long long)cmax, want));
+    return s.vec > 1 ? chunks1(s) * WARPS : slices1(s);
 }
+static long long slices2(const Shape& s) { return std::max(1LL, cdiv(s.nvec, TV2)); }
+static long long nsegs(const Shape& s) { return std::max(1LL, cdiv(s.nvec, SEGV)); }
+
+// L2 budget for the row pairs most likely to be corrected (read evict_last by the stats kernel)
+constexpr double PIN_BYTES = 80e6;
 
 static int topk_ept(int dtype) { return dtype == DT_BF16 ? 80 : 40; }
-static int topk_cap(int k) { return (int)std::min(2048LL, (long long)((2 * (long long)k + 64 + 31) / 32 * 32)); }
+static int topk_cap(int k) { return (int)std::min(2048LL, (2 * (long long)k + 64 + 31) / 32 * 32); }
 
 // --------------------------------------------------------------------------- workspace layout
 
 struct SpecLayout {
     size_t ctr_bytes = 0, bytes = 0;
-    size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0;
+    size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0, o_work = 0;
     size_t o_partials = 0, o_rstats = 0, o_plan = 0, o_segs = 0;
     size_t o_clist = 0, o_ccount = 0, o_klist = 0;
 };
 
-// Sizes for given chunk counts (C1, nseg = segments per request, CT, cap).
-static SpecLayout spec_layout(int B, int R, int C1, long long nseg, bool topk, int CT, int cap)
+// Byte layout for `ppr` softmax partials per row, nseg residual segments per request and (top-k) CT
+// chunks of `cap` list entries.  All counters sit at the front so one memset clears them.
+static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool topk, int CT, int cap)
 {
     SpecLayout L;
     size_t o = 0;
@@ -61,9 +65,10 @@ static SpecLayout spec_layout(int B, int R, int C1, long long nseg, bool topk, i
     L.o_res_ctr = o; o += (size_t)B * sizeof(unsigned);
     L.o_dense_ctr = o; o += (size_t)B * sizeof(unsigned);
     L.o_ndense = o; o += (size_t)B * sizeof(int);
+    L.o_work = o; o += 2 * sizeof(unsigned);
     L.ctr_bytes = o;
     o = align_up(o);
-    L.o_partials = o; o = align_up(o + (size_t)B * R * C1 * sizeof(Partial));
+    L.o_partials = o; o = align_up(o + (size_t)B * R * ppr * sizeof(Partial));
     L.o_rstats = o; o = align_up(o + (size_t)B * R * sizeof(RowStats));
     L.o_plan = o; o = align_up(o + (size_t)B * sizeof(Plan));
     L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
@@ -76,30 +81,21 @@ static SpecLayout spec_layout(int B, int R, int C1, long long nseg, bool topk, i
     return L;
 }
 
-static long long max_segments(const Shape& s)
-{
-    long long best = 0;
-    for (int c2 = 1; c2 <= max_c2(s); ++c2) {
-        long long cv = cdiv(s.nvec, c2);
-        best = std::max(best, (long long)c2 * cdiv(cv, NT) * WARPS);
-    }
-    return best;
-}
-
 struct TreeLayout {
     size_t ctr_bytes = 0, bytes = 0;
-    size_t o_req_ctr = 0, o_partials = 0, o_amax = 0, o_scratch = 0;
+    size_t o_req_ctr = 0, o_work = 0, o_partials = 0, o_amax = 0, o_scratch = 0;
 };
 
-static TreeLayout tree_layout(int B, int N, int C)
+static TreeLayout tree_layout(int B, int N, long long S1)
 {
     TreeLayout L;
     const int R = N + 1;
     size_t o = 0;
     L.o_req_ctr = o; o += (size_t)B * sizeof(unsigned);
+    L.o_work = o; o += sizeof(unsigned);
     L.ctr_bytes = o;
     o = align_up(o);
-    L.o_partials = o; o = align_up(o + (size_t)B * R * C * sizeof(ArgmaxPartial));
+    L.o_partials = o; o = align_up(o + (size_t)B * R * S1 * sizeof(ArgmaxPartial));
     L.o_amax = o; o = align_up(o + (size_t)B * R * sizeof(int32_t));
     L.o_scratch = o; o = align_up(o + (size_t)B * (N > 0 ? N : 1) * 2 * sizeof(int32_t));
     L.bytes = o;
@@ -133,7 +129,7 @@ static int pick_vec(int dtype, int V, const void* a, const void* b)
     return vec;
 }
 
-// --------------------------------------------------------------------------- launches
+// --------------------------------------------------------------------------- the calls
 
 static spec_status spec_common(const void* target, const void* draft, spec_dtype dtype,
                                const int32_t* tokens, const float* uniforms, int B, int gamma,
@@ -179,21 +175,23 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.B = B; P.gamma = gamma; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
     P.c = c; P.T = T; P.top_k = top_k;
-    P.C1 = pick_chunks((long long)B * R, max_c1(sh), sms, 16);
-    P.cv1 = cdiv(sh.nvec, P.C1);
-    P.C2 = pick_chunks(B, max_c2(sh), sms, 8);
-    P.cv2 = cdiv(sh.nvec, P.C2);
-    P.iters2 = (int)cdiv(P.cv2, NT);
-    const long long nseg = (long long)P.C2 * P.iters2 * WARPS;
+    // chunk kernels (16-byte vectors) take CHUNK_VECS / 2048 vectors per CTA; the scalar path's
+    // persistent warps take TV1 / TV2 vectors per task
+    P.S1 = (int)(vec > 1 ? chunks1(sh) : slices1(sh));
+    P.S2 = (int)(vec > 1 ? std::max(1LL, cdiv(sh.nvec, NT * 8)) : slices2(sh));
+    P.nseg = (int)nsegs(sh);
+    P.tasks1 = (long long)B * R * P.S1;
+    P.tasks2 = (long long)B * P.S2;
+    P.pin_pairs = (int)std::min(2.0, std::floor(PIN_BYTES / ((double)B * 2.0 * (double)V * (double)es)));
     if (topk) {
         P.CT = (int)cdiv(V, (long long)NT * topk_ept(dt));
-        P.cvt = 0;
         P.cap_w = topk_cap(top_k);
         P.cap_k = P.cap_w;
     }
-    const SpecLayout L = spec_layout(B, R, P.C1, nseg, topk, P.CT, P.cap_w);
+    const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.CT, P.cap_w);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
-    if ((long long)B * R * std::max(P.C1, topk ? P.CT : 1) >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+    if ((long long)B * R * (topk ? P.CT : 1) >= (1LL << 31) || P.tasks1 >= (1LL << 31))
+        return SPEC_ERR_INVALID_ARG;
 
     char* ws = static_cast<char*>(workspace);
     P.accepted_len = accepted_len;
@@ -207,6 +205,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.res_ctr = reinterpret_cast<unsigned*>(ws + L.o_res_ctr);
     P.dense_ctr = reinterpret_cast<unsigned*>(ws + L.o_dense_ctr);
     P.ndense = reinterpret_cast<int*>(ws + L.o_ndense);
+    P.work = reinterpret_cast<unsigned*>(ws + L.o_work);
     P.partials = reinterpret_cast<Partial*>(ws + L.o_partials);
     P.rstats = reinterpret_cast<RowStats*>(ws + L.o_rstats);
     P.plan = reinterpret_cast<Plan*>(ws + L.o_plan);
@@ -221,8 +220,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
     cudaError_t err;
     if (!topk) {
-        const unsigned g1 = (unsigned)((long long)B * R * P.C1), g2 = (unsigned)((long long)B * P.C2);
-        err = launch_softmax_path(P, g1, g2, st);
+        err = launch_softmax_path(P, sms, st);
     } else {
         const unsigned g1 = (unsigned)((long long)B * R * P.CT), g2 = (unsigned)((long long)B * R);
         err = launch_topk_path(P, g1, g2, st);
@@ -243,14 +241,13 @@ size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
     for (int vec : {1, 4, 8}) {
         const Shape sh = row_shape(V, vec);
         if (tree_nodes > 0) {
-            const TreeLayout L = tree_layout(B, tree_nodes, max_c1(sh));
-            best = std::max(best, L.bytes);
+            best = std::max(best, tree_layout(B, tree_nodes, slices1(sh)).bytes);
         } else {
             const bool topk = top_k > 0 && top_k < V;
             int CT = 0;
             if (topk) CT = (int)cdiv(V, (long long)NT * std::min(topk_ept(DT_BF16), topk_ept(DT_F32)));
-            const SpecLayout L = spec_layout(B, 2 * gamma + 1, max_c1(sh), max_segments(sh), topk,
-                                             CT, topk ? topk_cap(top_k) : 0);
+            const SpecLayout L = spec_layout(B, 2 * gamma + 1, partials_per_row(sh), nsegs(sh), topk, CT,
+                                             topk ? topk_cap(top_k) : 0);
             best = std::max(best, L.bytes);
         }
     }
@@ -312,26 +309,26 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     P.tokens = tokens;
     P.B = B; P.N = N; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
-    P.C = pick_chunks((long long)B * R, max_c1(sh), sm_count(), 16);
-    P.cv = cdiv(sh.nvec, P.C);
+    P.S1 = (int)(vec > 1 ? chunks1(sh) : slices1(sh));
+    P.tasks = (long long)B * R * P.S1;
     P.max_out = max_out;
-    const TreeLayout L = tree_layout(B, N, P.C);
+    if (P.tasks >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+    const TreeLayout L = tree_layout(B, N, P.S1);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
-    if ((long long)B * R * P.C >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
     char* ws = static_cast<char*>(workspace);
     P.accepted_len = accepted_len;
     P.out_tokens = out_tokens;
     P.out_nodes = (max_out > 1) ? out_nodes : nullptr;
     P.row_status = row_status;
     P.req_ctr = reinterpret_cast<unsigned*>(ws + L.o_req_ctr);
+    P.work = reinterpret_cast<unsigned*>(ws + L.o_work);
     P.partials = reinterpret_cast<ArgmaxPartial*>(ws + L.o_partials);
     P.amax = reinterpret_cast<int32_t*>(ws + L.o_amax);
     P.scratch = reinterpret_cast<int32_t*>(ws + L.o_scratch);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
-    const unsigned grid = (unsigned)((long long)B * R * P.C);
-    const cudaError_t err = launch_tree_path(P, grid, st);
+    const cudaError_t err = launch_tree_path(P, sm_count(), st);
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

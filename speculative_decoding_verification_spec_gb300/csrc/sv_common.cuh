@@ -71,6 +71,13 @@ struct ArgmaxPartial {
 
 // ---------------------------------------------------------------- parameter blocks
 
+// Streaming task geometry (persistent warps).  A task is a contiguous run of vectors of one row
+// (or row pair): STEPS steps of 32 lanes x U vectors; lane l of step j reads vectors
+// base + j*32*U + u*32 + l, so every load instruction of a warp covers 32 consecutive vectors.
+constexpr int U1 = 8, ST1 = 4, TV1 = 32 * U1 * ST1;  // row statistics / argmax: 1024 vectors
+constexpr int U2 = 4, ST2 = 4, TV2 = 32 * U2 * ST2;  // residual pass over a row pair: 512 vectors
+constexpr int SEGV = 32;                             // vectors per residual segment
+
 struct SpecParams {
     const void* target;   // [B, gamma+1, V]
     const void* draft;    // [B, gamma, V]
@@ -82,15 +89,12 @@ struct SpecParams {
     float c;              // log2(e)/T
     double T;
     int top_k;
-    // stats chunking
-    int C1;
-    long long cv1;
-    // resample chunking
-    int C2, iters2;
-    long long cv2;
+    int pin_pairs;        // row pairs 0..pin_pairs-1 are read with L2 evict_last
+    // softmax path: stats tasks (row, slice) and residual tasks (request, slice)
+    int S1, S2, nseg;
+    long long tasks1, tasks2;
     // top-k chunking and capacities
     int CT;
-    long long cvt;
     int cap_w;            // per-chunk list capacity (entries)
     int cap_k;            // per-row kept-list capacity
     // outputs
@@ -101,13 +105,14 @@ struct SpecParams {
     float* aux_lse_q;
     float* aux_accept;
     // workspace
-    Partial* partials;    // [B*R*C1]
+    Partial* partials;    // [B*R*S1]
     RowStats* rstats;     // [B*R]
     Plan* plan;           // [B]
-    float* segs;          // [B*C2*iters2*WARPS]
+    float* segs;          // [B*nseg]
     unsigned* row_ctr;    // [B*R]
     unsigned* req_ctr;    // [B]
     unsigned* res_ctr;    // [B]
+    unsigned* work;       // [2] task counters of the two streaming kernels
     TopkEntry* clist;     // [B*R*CT*cap_w] per-chunk candidate lists
     int* ccount;          // [B*R*CT] entries per chunk list (-1 = overflow)
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
@@ -122,15 +127,16 @@ struct TreeParams {
     int B, N, V, R;       // R = N+1
     int dtype, vec;
     long long nvec;
-    int C;
-    long long cv;
+    int S1;               // slices per row
+    long long tasks;
     int max_out;
     int32_t* accepted_len;
     int32_t* out_tokens;
     int32_t* out_nodes;
     int32_t* row_status;
-    ArgmaxPartial* partials;  // [B*R*C]
+    ArgmaxPartial* partials;  // [B*R*S1]
     unsigned* req_ctr;        // [B]
+    unsigned* work;           // [1]
     int32_t* amax;            // [B*R]
     int32_t* scratch;         // [B*N*2] depth / valid of each node
 };
@@ -142,6 +148,46 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// L2 cache policies for 16-byte streaming loads (L1 bypassed)
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal()
+{
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_stream_v4_pol(const void* p, uint64_t pol)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ unsigned short ld_u16_pol(const void* p, uint64_t pol)
+{
+    unsigned short r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(r) : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_u32_pol(const void* p, uint64_t pol)
+{
+    uint32_t r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "l"(pol));
+    return r;
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p)
@@ -212,6 +258,129 @@ __device__ __forceinline__ void load_vec(const char* row, long long v, float (&x
         x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
         x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
     }
+}
+
+// Vector v of a row as fp32 values, loaded with an L2 cache policy.
+template <int DT, int VEC>
+__device__ __forceinline__ void load_vec_pol(const char* row, long long v, uint64_t pol, float (&x)[VEC])
+{
+    if constexpr (VEC == 1) {
+        if constexpr (DT == DT_BF16) x[0] = __uint_as_float(((uint32_t)ld_u16_pol(row + v * 2, pol)) << 16);
+        else x[0] = __uint_as_float(ld_u32_pol(row + v * 4, pol));
+    } else if constexpr (DT == DT_BF16) {
+        uint4 w = ld_stream_v4_pol(row + v * 16, pol);
+        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+        x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+    } else {
+        uint4 w = ld_stream_v4_pol(row + v * 16, pol);
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+    }
+}
+
+// ---------------------------------------------------------------- per-warp cp.async ring
+//
+// Each lane copies its own 16-byte vectors global -> shared with cp.async (L1 bypassed, L2 policy
+// hint) and later reads back exactly the vectors it copied, so a lane waits only on its own copy
+// groups (cp.async.wait_group): no cross-thread synchronisation and no flag waits.  PS stages of
+// U vectors per lane keep (PS-1) * U * 512 bytes per warp in flight while one stage is consumed.
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint64_t pol)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 :: "r"(d), "l"(gsrc), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(const uint4* p)
+{
+    uint4 r;
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a) : "memory");
+    return r;
+}
+
+// Chunk kernels: one CTA of NT threads per chunk of CHUNK_VECS vectors.  Thread t copies vectors
+// t + i*NT (i < CV) into shared slot i*NT + t with cp.async, CG commit groups of CV/CG vectors,
+// all issued before the first is consumed (64 KB per CTA in flight; three CTAs per SM).
+constexpr int CV = 16;
+constexpr int CG = 4;
+constexpr int CVG = CV / CG;
+constexpr int CHUNK_VECS = NT * CV;
+constexpr size_t CHUNK_SMEM = (size_t)CHUNK_VECS * sizeof(uint4);
+
+// Ring kernels: CTAs of 8 warps; each warp owns PS stages of RU vectors per lane (2 KB per stage),
+// so three CTAs (24 warps, 192 KB) fit on an SM with ~144 KB of copies in flight.  A ring task is
+// RST steps of RU vectors per lane: the same TV1 = 1024 vectors as the plain kernels' tasks.
+constexpr int NT_RING = 256;
+constexpr int WARPS_RING = NT_RING / 32;
+constexpr int PS = 4;
+constexpr int RU = 4;
+constexpr int RST = TV1 / (32 * RU);
+constexpr int RING_VECS_PER_WARP = PS * RU * 32;  // uint4 per warp ring
+constexpr size_t RING_SMEM = (size_t)WARPS_RING * RING_VECS_PER_WARP * sizeof(uint4);
+static_assert(RST * 32 * RU == TV1, "ring task geometry");
+constexpr int RU2 = RU / 2;               // residual ring: RU2 vectors of p and of q per step
+constexpr int RST2 = TV2 / (32 * RU2);
+static_assert(RST2 * 32 * RU2 == TV2, "residual ring task geometry");
+
+// One vector of a row kept as raw bits until it is used: 16 bytes (8 bf16 or 4 fp32) or a single
+// element for the unaligned path.
+template <int DT, int VEC>
+struct RawVec {
+    uint4 w;
+    __device__ __forceinline__ void load(const char* row, long long v, uint64_t pol)
+    {
+        if constexpr (VEC == 1) {
+            if constexpr (DT == DT_BF16) w.x = ((uint32_t)ld_u16_pol(row + v * 2, pol)) << 16;
+            else w.x = ld_u32_pol(row + v * 4, pol);
+        } else {
+            w = ld_stream_v4_pol(row + v * 16, pol);
+        }
+    }
+    __device__ __forceinline__ void fill_neg_inf()
+    {
+        const uint32_t p = (DT == DT_BF16 && VEC == 8) ? 0xff80ff80u : 0xff800000u;
+        w = make_uint4(p, p, p, p);
+    }
+    __device__ __forceinline__ float get(int e) const
+    {
+        if constexpr (VEC == 1) {
+            return __uint_as_float(w.x);
+        } else if constexpr (DT == DT_BF16) {
+            const uint32_t q = (e >> 1) == 0 ? w.x : (e >> 1) == 1 ? w.y : (e >> 1) == 2 ? w.z : w.w;
+            return (e & 1) ? bf16hi(q) : bf16lo(q);
+        } else {
+            return __uint_as_float(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
+        }
+    }
+};
+
+// warp-wide claim of the next task index from a global counter (lane 0 increments)
+__device__ __forceinline__ long long claim_task(unsigned* ctr)
+{
+    unsigned t = 0;
+    if ((threadIdx.x & 31) == 0) t = atomicAdd(ctr, 1u);
+    return (long long)__shfl_sync(0xffffffffu, t, 0);
+}
+
+// Warp-level arrive: after this warp's global writes, lane 0 increments the counter; returns true
+// in every lane of the warp that arrived last.  Never waits.
+__device__ __forceinline__ bool warp_arrive_last(unsigned* ctr, unsigned expected)
+{
+    int last = 0;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        __threadfence();
+        last = (atomicAdd(ctr, 1u) == expected - 1);
+        if (last) __threadfence();
+    }
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
 template <typename T>
@@ -318,32 +487,61 @@ __device__ __forceinline__ bool arrive_last(unsigned* ctr, unsigned expected, in
 
 // ---------------------------------------------------------------- outputs
 
-// Writes a request's outputs: the accepted draft prefix, the drawn token, -1 padding.
-__device__ __forceinline__ void emit_spec(const SpecParams& P, int b, int status, int A, int tok)
+// Writes a request's outputs: the accepted draft prefix, the drawn token, -1 padding.  Called by
+// `n` cooperating threads with ranks 0..n-1.
+__device__ __forceinline__ void emit_spec_n(const SpecParams& P, int b, int status, int A, int tok,
+                                            int rank, int n)
 {
     const int g = P.gamma;
     int32_t* out = P.out_tokens + (size_t)b * (g + 1);
     const int32_t* dt = P.tokens + (size_t)b * g;
-    for (int i = threadIdx.x; i <= g; i += NT) {
+    for (int i = rank; i <= g; i += n) {
         int v = -1;
         if (status == ROW_OK) v = (i < A) ? dt[i] : (i == A ? tok : -1);
         out[i] = v;
     }
-    if (threadIdx.x == 0) {
+    if (rank == 0) {
         P.accepted_len[b] = (status == ROW_OK) ? A : -1;
         if (P.row_status) P.row_status[b] = status;
     }
 }
+__device__ __forceinline__ void emit_spec(const SpecParams& P, int b, int status, int A, int tok)
+{
+    emit_spec_n(P, b, status, A, tok, threadIdx.x, NT);
+}
+__device__ __forceinline__ void emit_spec_warp(const SpecParams& P, int b, int status, int A, int tok)
+{
+    emit_spec_n(P, b, status, A, tok, threadIdx.x & 31, 32);
+}
 
 // ---------------------------------------------------------------- host launchers (one per .cu)
 
+// Persistent grid for kernel K: enough CTAs for every task warp, at most the CTAs that fit on
+// `sms` SMs at once.  The occupancy (and the dynamic shared-memory opt-in above 48 KB) is queried
+// once per kernel.
+template <auto K>
+inline unsigned persistent_grid(long long tasks, int sms, int threads = NT, size_t smem = 0)
+{
+    static int per_sm = 0;
+    if (per_sm < 1) {
+        int n = 0;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, threads, smem) != cudaSuccess || n < 1) n = 1;
+        per_sm = n;
+    }
+    const int wpc = threads / 32;
+    const long long want = (tasks + wpc - 1) / wpc;
+    const long long cap = (long long)per_sm * sms;
+    return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
 // spec_stats_kernel + spec_resample_kernel for the dtype / vector width in P
-cudaError_t launch_softmax_path(const SpecParams& P, unsigned grid_stats, unsigned grid_resample,
-                                cudaStream_t st);
+cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st);
 // topk_stats_kernel + topk_dense_kernel
 cudaError_t launch_topk_path(const SpecParams& P, unsigned grid_stats, unsigned grid_dense,
                              cudaStream_t st);
 // tree_argmax_kernel
-cudaError_t launch_tree_path(const TreeParams& P, unsigned grid, cudaStream_t st);
+cudaError_t launch_tree_path(const TreeParams& P, int sms, cudaStream_t st);
 
 }  // namespace sv

@@ -61,43 +61,43 @@ __device__ __forceinline__ float row_lse(const RowStats& rs, float c, double T)
     return (float)((double)rs.M / T + log(rs.S) - LN2 * (exact - (double)rs.MC));
 }
 
-// Computes the plan of request b.  Must be called by all NT threads of a CTA.
+// Computes the plan of request b.  Must be called by all 32 lanes of one warp; every lane gets the
+// plan.  Writes the aux outputs (lse per row, accept ratio per position).
 template <int DT>
-__device__ Plan compute_plan(const SpecParams& P, int b, bool topk)
+__device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
 {
-    __shared__ int s_A;
-    const int g = P.gamma, R = P.R, tid = threadIdx.x;
-    if (tid == 0) s_A = g;
+    const int g = P.gamma, R = P.R, lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
 
     int bad = 0;
-    for (int r = tid; r < R; r += NT) {
+    for (int r = lane; r < R; r += 32) {
         RowStats rs = ld_rowstats(P.rstats + (size_t)b * R + r);
         if (rs.status != ROW_OK) bad = 1;
-        float lse = row_lse(rs, P.c, P.T);
+        const float lse = row_lse(rs, P.c, P.T);
         if (r <= g) {
             if (P.aux_lse_p) P.aux_lse_p[(size_t)b * (g + 1) + r] = lse;
         } else if (P.aux_lse_q) {
             P.aux_lse_q[(size_t)b * g + (r - g - 1)] = lse;
         }
     }
-    const int nonfinite = __syncthreads_or(bad);
+    const int nonfinite = __any_sync(FULL, bad);
 
     // acceptance ratios at every position
     int badtok = 0;
     int rej_first = g;
     const float* u = P.uniforms + (size_t)b * (g + 2);
-    for (int i = tid; i < g; i += NT) {
+    for (int i = lane; i < g; i += 32) {
         const int x = P.tokens[(size_t)b * g + i];
         double a = __longlong_as_double(0x7ff8000000000000ll);
         if (x < 0 || x >= P.V) {
             badtok = 1;
         } else if (!nonfinite) {
-            RowStats rp = ld_rowstats(P.rstats + (size_t)b * R + i);
-            RowStats rq = ld_rowstats(P.rstats + (size_t)b * R + g + 1 + i);
-            float xp = load_logit(spec_row_ptr(P, b, i), DT, x);
-            float xq = load_logit(spec_row_ptr(P, b, g + 1 + i), DT, x);
-            double lp = row_log2prob(xp, rp, P.c, topk);
-            double lq = row_log2prob(xq, rq, P.c, topk);
+            const RowStats rp = ld_rowstats(P.rstats + (size_t)b * R + i);
+            const RowStats rq = ld_rowstats(P.rstats + (size_t)b * R + g + 1 + i);
+            const float xp = load_logit(spec_row_ptr(P, b, i), DT, x);
+            const float xq = load_logit(spec_row_ptr(P, b, g + 1 + i), DT, x);
+            const double lp = row_log2prob(xp, rp, P.c, topk);
+            const double lq = row_log2prob(xq, rq, P.c, topk);
             if (lq == -INFINITY) {
                 badtok = 1;  // q(x) = 0: the draft cannot have proposed x
             } else {
@@ -107,27 +107,25 @@ __device__ Plan compute_plan(const SpecParams& P, int b, bool topk)
         }
         if (P.aux_accept) P.aux_accept[(size_t)b * g + i] = (float)a;
     }
-    badtok = __syncthreads_or(badtok);
+    badtok = __any_sync(FULL, badtok);
     int badu = 0;
-    for (int i = tid; i < g + 2; i += NT) {
-        float v = u[i];
+    for (int i = lane; i < g + 2; i += 32) {
+        const float v = u[i];
         if (!(v >= 0.0f && v < 1.0f)) badu = 1;
     }
-    badu = __syncthreads_or(badu);
-    if (rej_first < g) atomicMin(&s_A, rej_first);
-    __syncthreads();
+    badu = __any_sync(FULL, badu);
 
     Plan pl;
     pl.status = nonfinite ? ROW_NONFINITE : badtok ? ROW_BAD_TOKEN : badu ? ROW_BAD_UNIFORM : ROW_OK;
-    pl.A = s_A;
+    pl.A = __reduce_min_sync(FULL, rej_first);
     pl.rp = (pl.A < g) ? pl.A : g;
     pl.rq = (pl.A < g) ? g + 1 + pl.A : -1;
-    RowStats sp = ld_rowstats(P.rstats + (size_t)b * R + pl.rp);
+    const RowStats sp = ld_rowstats(P.rstats + (size_t)b * R + pl.rp);
     pl.MCp = sp.MC;
     pl.invSp = (float)(1.0 / sp.S);
     pl.thrp = sp.thr;
     if (pl.rq >= 0) {
-        RowStats sq = ld_rowstats(P.rstats + (size_t)b * R + pl.rq);
+        const RowStats sq = ld_rowstats(P.rstats + (size_t)b * R + pl.rq);
         pl.MCq = sq.MC;
         pl.invSq = (float)(1.0 / sq.S);
         pl.thrq = sq.thr;
@@ -137,7 +135,6 @@ __device__ Plan compute_plan(const SpecParams& P, int b, bool topk)
         pl.thrq = 0.f;
     }
     pl.u = (double)u[(pl.A < g) ? g : g + 1];
-    __syncthreads();
     return pl;
 }
 

@@ -1,52 +1,51 @@
-// sv_softmax.cu -- exact speculative sampling without top-k: the one-pass row normalisers and
-// the residual / bonus inverse-CDF draw.
+// sv_softmax.cu -- exact speculative sampling without top-k: one-pass row normalisers and the
+// residual / bonus inverse-CDF draw.
 //
-// Kernel 1 (spec_stats_kernel): one CTA per (row, chunk of V).  Each thread streams 16-byte
-// vectors, keeps an online (max, sum of 2^(x*c - max*c)) pair -- the online (m, l) merge over
-// vocabulary blocks of M7.1 section 0x04J -- and the CTA writes one partial.  The last CTA of a row
-// merges the row's partials (fp64), and the last row of a request runs the acceptance scan
-// (sv_plan.cuh).  Completion is counted with atomics ("last CTA done"); nothing ever waits.
+// Kernel 1 (row statistics): each lane keeps an online (max, sum of 2^(x*c - max*c)) pair -- the
+// online (m, l) merge over vocabulary blocks of M7.1 section 0x04J.  For rows of 16-byte vectors
+// one CTA takes a chunk of CHUNK_VECS vectors, all of it prefetched into shared memory by cp.async
+// before the first group is consumed; the CTA writes one partial.  The last CTA of a row merges its
+// partials (fp64, chunk order) and the last row of a request runs the acceptance scan
+// (sv_plan.cuh).  Completion is counted with atomics; nothing waits.  Rows that are not 16-byte
+// aligned use persistent warps with plain loads instead.
 //
-// Kernel 2 (spec_resample_kernel): one CTA per (request, chunk of V).  Each warp turns 32 vectors of
-// the selected row pair into residual mass r = max(p - q, 0) (M7.1 section 0x03C; p alone for the
-// bonus, 0x03H) and stores one segment sum.  The last CTA of the request scans the segment sums in
-// fp64 in index order, finds the segment where the running mass passes u * Z, and one warp
-// resolves the token inside that segment.
+// Kernel 2 (residual draw): r = max(p - q, 0) (M7.1 section 0x03C; p alone for the bonus, 0x03H)
+// over the selected row pair, summed per segment of 32 vectors; the last CTA of a request scans the
+// segment sums in fp64 in index order, finds the segment where the running mass passes u * Z, and
+// resolves the token inside it.
+//
+// Rows of the two row pairs most likely to be corrected (pairs 0 and 1) are read with the L2
+// evict_normal policy and all other rows evict_first, so that kernel 2 tends to find them in L2.
 #include "sv_plan.cuh"
 
 namespace sv {
 
-// Row visiting order: all requests' bonus rows first, then draft pairs gamma-1 .. 0 (target row
-// then draft row).  Pair 0 -- the most likely correction pair -- is read last, so it is the most
-// likely to still sit in L2 when the resample kernel needs it.
-__device__ __forceinline__ int slot_to_row(int slot, int gamma)
-{
-    if (slot == 0) return gamma;
-    const int j = (slot - 1) >> 1;
-    const int pos = gamma - 1 - j;
-    return ((slot - 1) & 1) ? gamma + 1 + pos : pos;
-}
+// ---------------------------------------------------------------- kernel 1: row statistics
 
-// Online softmax statistics of vectors [v0, v1) of one row: per thread (m, mc, s) with
-// mc = fp32(m*c) and s = sum 2^(fma(x, c, -mc)).
+// Online softmax statistics of one task: lane accumulators (m, mc, s), mc = fp32(m*c),
+// s = sum 2^(fma(x, c, -mc)).
 template <int DT, int VEC>
-__device__ __forceinline__ void chunk_softmax_stats(const char* row, long long v0, long long v1,
-                                                    float c, float& m, float& mc, float& s)
+__device__ __forceinline__ void task_softmax_stats(const char* row, long long t0, long long t1,
+                                                   float c, uint64_t pol, float& m, float& mc,
+                                                   float& s)
 {
-    constexpr int U = (VEC == 1) ? 8 : 4;  // vectors per thread per step
-    for (long long base = v0 + threadIdx.x; base < v1; base += (long long)NT * U) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int step = 0; step < ST1; ++step) {
+        const long long base = t0 + (long long)step * 32 * U1 + lane;
+        if (t0 + (long long)step * 32 * U1 >= t1) break;
         if constexpr (DT == DT_BF16 && VEC == 8) {
-            uint4 w[U];
+            uint4 w[U1];
 #pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const long long v = base + (long long)j * NT;
-                if (v < v1) w[j] = ld_stream_v4(row + v * 16);
-                else w[j] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+            for (int u = 0; u < U1; ++u) {
+                const long long v = base + u * 32;
+                if (v < t1) w[u] = ld_stream_v4_pol(row + v * 16, pol);
+                else w[u] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
             }
             uint32_t pm = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
 #pragma unroll
-            for (int j = 1; j < U; ++j)
-                pm = bmax2(pm, bmax2(bmax2(w[j].x, w[j].y), bmax2(w[j].z, w[j].w)));
+            for (int u = 1; u < U1; ++u)
+                pm = bmax2(pm, bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w)));
             const float bm = fmaxf(bf16lo(pm), bf16hi(pm));
             if (bm > m) {
                 const float mcn = bm * c;
@@ -55,40 +54,37 @@ __device__ __forceinline__ void chunk_softmax_stats(const char* row, long long v
                 mc = mcn;
             }
             if (mc != NEG_INF) {
-                float acc[U];
+                float acc[U1];
 #pragma unroll
-                for (int j = 0; j < U; ++j) {
-                    const uint32_t q[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+                for (int u = 0; u < U1; ++u) {
+                    const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
                     float e[8];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         e[2 * k] = ex2(fmaf(bf16lo(q[k]), c, -mc));
                         e[2 * k + 1] = ex2(fmaf(bf16hi(q[k]), c, -mc));
                     }
-                    acc[j] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+                    acc[u] = tree_sum(e);
                 }
-                float t = acc[0];
-#pragma unroll
-                for (int j = 1; j < U; ++j) t += acc[j];
-                s += t;
+                s += tree_sum(acc);
             }
         } else {
-            float x[U][VEC];
+            float x[U1][VEC];
 #pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const long long v = base + (long long)j * NT;
-                if (v < v1) {
-                    load_vec<DT, VEC>(row, v, x[j]);
+            for (int u = 0; u < U1; ++u) {
+                const long long v = base + u * 32;
+                if (v < t1) {
+                    load_vec_pol<DT, VEC>(row, v, pol, x[u]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) x[j][e] = NEG_INF;
+                    for (int e = 0; e < VEC; ++e) x[u][e] = NEG_INF;
                 }
             }
             float bm = NEG_INF;
 #pragma unroll
-            for (int j = 0; j < U; ++j)
+            for (int u = 0; u < U1; ++u)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, x[j][e]);
+                for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, x[u][e]);
             if (bm > m) {
                 const float mcn = bm * c;
                 s *= ex2(mc - mcn);
@@ -96,13 +92,13 @@ __device__ __forceinline__ void chunk_softmax_stats(const char* row, long long v
                 mc = mcn;
             }
             if (mc != NEG_INF) {
-                float acc[U];
+                float acc[U1];
 #pragma unroll
-                for (int j = 0; j < U; ++j) {
+                for (int u = 0; u < U1; ++u) {
                     float e[VEC];
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(x[j][k], c, -mc));
-                    acc[j] = tree_sum(e);
+                    for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(x[u][k], c, -mc));
+                    acc[u] = tree_sum(e);
                 }
                 s += tree_sum(acc);
             }
@@ -119,96 +115,249 @@ __device__ __forceinline__ Partial ld_partial(const Partial* p)
     return r;
 }
 
-template <int DT, int VEC>
-__global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
+// task t -> (request b, row r, slice s); request-major, rows in index order
+__device__ __forceinline__ void decode_stats_task(const SpecParams& P, long long t, int& b, int& r,
+                                                  int& s)
 {
-    __shared__ float sh_f[WARPS];
-    __shared__ double sh_d[WARPS];
-    __shared__ int sh_flag;
+    s = (int)(t % P.S1);
+    const long long rr = t / P.S1;
+    r = (int)(rr % P.R);
+    b = (int)(rr / P.R);
+}
 
-    const long long idx = blockIdx.x;
-    const int chunk = (int)(idx % P.C1);
-    const long long rs = idx / P.C1;
-    const int slot = (int)(rs / P.B), b = (int)(rs % P.B);
-    const int r = slot_to_row(slot, P.gamma);
-    const char* row = spec_row_ptr(P, b, r);
-    const long long v0 = (long long)chunk * P.cv1;
-    const long long v1 = min(v0 + P.cv1, P.nvec);
+// Rows of the first pin_pairs row pairs (target row i and draft row i) are kept in L2.
+__device__ __forceinline__ bool pinned_row(const SpecParams& P, int r)
+{
+    if (r == P.gamma) return P.gamma < P.pin_pairs;  // the bonus row matters when all are accepted
+    const int pos = (r < P.gamma) ? r : r - P.gamma - 1;
+    return pos < P.pin_pairs;
+}
 
-    float m = NEG_INF, mc = NEG_INF, s = 0.f;
-    chunk_softmax_stats<DT, VEC>(row, v0, v1, P.c, m, mc, s);
+template <int DT>
+__device__ void row_merge_and_plan(const SpecParams& P, int b, int row_id, int nparts);
 
-    const float M = block_max(m, sh_f);
+// End of a stats task: warp merge of the lane accumulators, the slice partial, and -- for the warp
+// that completes a row / a request -- the row merge and the acceptance scan.
+template <int DT>
+__device__ __forceinline__ void stats_finalize(const SpecParams& P, int b, int r, int s, float m,
+                                               float mc, float acc)
+{
+    const int lane = threadIdx.x & 31;
+    const float M = warp_max(m);
     const float MC = M * P.c;
-    const float sc = (mc == NEG_INF) ? 0.f : s * ex2(mc - MC);
-    const double S = block_sum_f32(sc, sh_d);
+    const float sc = (mc == NEG_INF) ? 0.f : acc * ex2(mc - MC);
+    const float S = warp_sum(sc);
     const int row_id = b * P.R + r;
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
         Partial pt;
         pt.M = M;
         pt.MC = MC;
-        pt.S = S;
-        P.partials[(size_t)row_id * P.C1 + chunk] = pt;
+        pt.S = (double)S;
+        P.partials[(size_t)row_id * P.S1 + s] = pt;
     }
-    if (!arrive_last(&P.row_ctr[row_id], (unsigned)P.C1, &sh_flag)) return;
-
-    // last CTA of this row: merge the chunk partials in chunk order
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const Partial* pp = P.partials + (size_t)row_id * P.C1;
-        float Mr = NEG_INF;
-        for (int k = lane; k < P.C1; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
-        Mr = warp_max(Mr);
-        const float MCr = Mr * P.c;
-        double Sr = 0.0;
-        for (int k = lane; k < P.C1; k += 32) {
-            Partial q = ld_partial(pp + k);
-            if (q.S != 0.0) Sr += q.S * exp2((double)q.MC - (double)MCr);
-        }
-        Sr = warp_sum(Sr);
-        if (lane == 0) {
-            RowStats st;
-            st.M = Mr;
-            st.MC = MCr;
-            st.S = Sr;
-            st.thr = NEG_INF;
-            st.klist_n = -1;
-            st.dense = 0;
-            const bool ok = isfinite(Sr) && Sr > 0.0 && Mr != NEG_INF && isfinite(Mr);
-            st.status = ok ? ROW_OK : ROW_NONFINITE;
-            P.rstats[row_id] = st;
-        }
-    }
-    if (!arrive_last(&P.req_ctr[b], (unsigned)P.R, &sh_flag)) return;
-
-    // last row of this request: acceptance scan
-    Plan pl = compute_plan<DT>(P, b, false);
-    if (threadIdx.x == 0) P.plan[b] = pl;
+    if (warp_arrive_last(&P.row_ctr[row_id], (unsigned)P.S1)) row_merge_and_plan<DT>(P, b, row_id, P.S1);
 }
 
-// ---------------------------------------------------------------- resample
+// Called by the warp that completed row `row_id`: merge its `nparts` partials in order into
+// RowStats; the warp that completes the last row of request b then runs the acceptance scan.
+template <int DT>
+__device__ void row_merge_and_plan(const SpecParams& P, int b, int row_id, int nparts)
+{
+    const int lane = threadIdx.x & 31;
+    const Partial* pp = P.partials + (size_t)row_id * nparts;
+    float Mr = NEG_INF;
+    for (int k = lane; k < nparts; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
+    Mr = warp_max(Mr);
+    const float MCr = Mr * P.c;
+    double Sr = 0.0;
+    for (int k = lane; k < nparts; k += 32) {
+        const Partial q = ld_partial(pp + k);
+        if (q.S != 0.0) Sr += q.S * exp2((double)q.MC - (double)MCr);
+    }
+    Sr = warp_sum(Sr);
+    if (lane == 0) {
+        RowStats st;
+        st.M = Mr;
+        st.MC = MCr;
+        st.S = Sr;
+        st.thr = NEG_INF;
+        st.klist_n = -1;
+        st.dense = 0;
+        const bool ok = isfinite(Sr) && Sr > 0.0 && Mr != NEG_INF && isfinite(Mr);
+        st.status = ok ? ROW_OK : ROW_NONFINITE;
+        P.rstats[row_id] = st;
+    }
+    if (warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) {
+        const Plan pl = compute_plan_warp<DT>(P, b, false);
+        if (lane == 0) P.plan[b] = pl;
+    }
+}
 
-// Resolve the token inside segment s (vectors base .. base+31 of the chunk, one per lane) given
-// the mass t_local still to pass within the segment.  Runs in one warp.  Returns the token.
+// Online update of the lane accumulators with one step of 16-byte vectors (raw bits).
+template <int DT, int NU>
+__device__ __forceinline__ void stats_step(const uint4 (&w)[NU], float c, float& m, float& mc,
+                                           float& s)
+{
+    float bm;
+    if constexpr (DT == DT_BF16) {
+        uint32_t pm = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
+#pragma unroll
+        for (int u = 1; u < NU; ++u) pm = bmax2(pm, bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w)));
+        bm = fmaxf(bf16lo(pm), bf16hi(pm));
+    } else {
+        bm = NEG_INF;
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+            bm = fmaxf(fmaxf(bm, fmaxf(__uint_as_float(w[u].x), __uint_as_float(w[u].y))),
+                       fmaxf(__uint_as_float(w[u].z), __uint_as_float(w[u].w)));
+    }
+    if (bm > m) {
+        const float mcn = bm * c;
+        s *= ex2(mc - mcn);
+        m = bm;
+        mc = mcn;
+    }
+    if (mc == NEG_INF) return;
+    float acc[NU];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+        if constexpr (DT == DT_BF16) {
+            float e[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                e[2 * k] = ex2(fmaf(bf16lo(q[k]), c, -mc));
+                e[2 * k + 1] = ex2(fmaf(bf16hi(q[k]), c, -mc));
+            }
+            acc[u] = tree_sum(e);
+        } else {
+            float e[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) e[k] = ex2(fmaf(__uint_as_float(q[k]), c, -mc));
+            acc[u] = tree_sum(e);
+        }
+    }
+    s += tree_sum(acc);
+}
+
+// Scalar-path kernel (rows not 16-byte aligned): plain loads, one task per warp at a time.
+template <int DT, int VEC>
+__global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
+{
+    const uint64_t pol_first = policy_evict_first(), pol_keep = policy_evict_normal();
+    long long t = claim_task(&P.work[0]);
+    while (t < P.tasks1) {
+        const long long next = claim_task(&P.work[0]);  // claimed early: hides the atomic latency
+        int b, r, s;
+        decode_stats_task(P, t, b, r, s);
+        const char* row = spec_row_ptr(P, b, r);
+        const long long t0 = (long long)s * TV1;
+        const long long t1 = min(t0 + TV1, P.nvec);
+        float m = NEG_INF, mc = NEG_INF, acc = 0.f;
+        task_softmax_stats<DT, VEC>(row, t0, t1, P.c, pinned_row(P, r) ? pol_keep : pol_first,
+                                    m, mc, acc);
+        stats_finalize<DT>(P, b, r, s, m, mc, acc);
+        t = next;
+    }
+}
+
+// Chunk kernel for 16-byte vectors: one CTA per (request, row, chunk of CHUNK_VECS contiguous
+// vectors).  Thread t loads vectors t + i*NT (i < CV), U1 at a time straight into registers, and
+// keeps its online (max, sum) pair; each warp writes its own partial (no block-wide reduction), and
+// the last CTA of a row merges the row's WARPS * S1 partials.
+template <int DT>
+__global__ void __launch_bounds__(NT) spec_stats_chunk_kernel(SpecParams P)
+{
+    __shared__ int sh_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x % P.S1;
+    const int rr = blockIdx.x / P.S1;
+    const int r = rr % P.R, b = rr / P.R;
+    const char* row = spec_row_ptr(P, b, r);
+    const int c0 = c * CHUNK_VECS;
+    const int c1 = (int)min((long long)c0 + CHUNK_VECS, P.nvec);
+    const uint64_t pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
+    const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+    float m = NEG_INF, mc = NEG_INF, acc = 0.f;
+#pragma unroll
+    for (int it = 0; it < CV / U1; ++it) {
+        const int vb = c0 + it * U1 * NT + tid;
+        if (vb >= c1) break;
+        uint4 w[U1];
+#pragma unroll
+        for (int u = 0; u < U1; ++u) {
+            const int v = vb + u * NT;
+            w[u] = v < c1 ? ld_stream_v4_pol(row + (size_t)v * 16, pol) : make_uint4(pad, pad, pad, pad);
+        }
+        stats_step<DT, U1>(w, P.c, m, mc, acc);
+    }
+    // per-warp partial
+    const float M = warp_max(m);
+    const float MC = M * P.c;
+    const float sc = (mc == NEG_INF) ? 0.f : acc * ex2(mc - MC);
+    const float S = warp_sum(sc);
+    const int row_id = b * P.R + r;
+    if (lane == 0) {
+        Partial pt;
+        pt.M = M;
+        pt.MC = MC;
+        pt.S = (double)S;
+        P.partials[((size_t)row_id * P.S1 + c) * WARPS + warp] = pt;
+    }
+    if (!arrive_last(&P.row_ctr[row_id], (unsigned)P.S1, &sh_flag)) return;
+    if (tid < 32) row_merge_and_plan<DT>(P, b, row_id, P.S1 * WARPS);
+}
+
+// ---------------------------------------------------------------- kernel 2: residual draw
+
+// residual mass of one vector from already-loaded values (bit-identical wherever recomputed)
+template <int VEC>
+__device__ __forceinline__ void residual_from(const float (&xp)[VEC], const float (&xq)[VEC],
+                                              bool has_q, const Plan& pl, float c, float (&r)[VEC])
+{
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        const float pp = __fmul_rn(ex2(fmaf(xp[e], c, -pl.MCp)), pl.invSp);
+        if (has_q) {
+            const float qq = __fmul_rn(ex2(fmaf(xq[e], c, -pl.MCq)), pl.invSq);
+            r[e] = fmaxf(__fsub_rn(pp, qq), 0.f);
+        } else {
+            r[e] = pp;
+        }
+    }
+}
+
+// Resolve the token inside the segment of 32 vectors starting at vbase (one per lane), given the
+// mass t_local still to pass within it.  Runs in one warp; returns the token in every lane.
 template <int DT, int VEC>
 __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const char* rowq,
-                                  const Plan& pl, long long vbase, long long vend, double t_local)
+                                  const Plan& pl, long long vbase, double t_local)
 {
     const int lane = threadIdx.x & 31;
     const long long v = vbase + lane;
     float r[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) r[e] = 0.f;
-    if (v < vend) residual_vec<DT, VEC>(rowp, rowq, v, pl, P.c, false, r);
+    if (v < P.nvec) {
+        float xp[VEC], xq[VEC];
+        load_vec<DT, VEC>(rowp, v, xp);
+        if (rowq) {
+            load_vec<DT, VEC>(rowq, v, xq);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) xq[e] = 0.f;
+        }
+        residual_from<VEC>(xp, xq, rowq != nullptr, pl, P.c, r);
+    }
     const float ls = tree_sum(r);
     const double incl = warp_incl_scan((double)ls);
     const double excl = __shfl_up_sync(0xffffffffu, incl, 1);
     const double start = lane ? excl : 0.0;
-    const unsigned hit = __ballot_sync(0xffffffffu, t_local < incl);
+    const unsigned hit = __ballot_sync(0xffffffffu, t_local < incl && ls > 0.f);
     int owner;
     if (hit) {
         owner = __ffs(hit) - 1;
-    } else {  // rounding left t_local past the segment: take its last positive entry
+    } else {  // rounding left t_local past the segment: its last positive entry
         const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
         owner = pos ? 31 - __clz(pos) : 0;
     }
@@ -227,118 +376,190 @@ __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const c
     return __shfl_sync(0xffffffffu, tok, owner);
 }
 
+// Request b's draw from its segment sums (one warp).  Returns the token, -1 if degenerate.
+template <int DT, int VEC>
+__device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, const char* rowp,
+                                  const char* rowq)
+{
+    const int lane = threadIdx.x & 31;
+    const float* segs = P.segs + (size_t)b * P.nseg;
+    const int per = (P.nseg + 31) / 32;
+    const int s0 = min(lane * per, P.nseg), s1 = min(s0 + per, P.nseg);
+    double mine = 0.0;
+    for (int s = s0; s < s1; ++s) mine += (double)__ldcg(segs + s);
+    const double incl = warp_incl_scan(mine);
+    const double Z = __shfl_sync(0xffffffffu, incl, 31);
+    if (!(Z > 0.0) || !isfinite(Z)) return -1;
+    const double excl = incl - mine;
+    const double t = pl.u * Z;
+    unsigned own = __ballot_sync(0xffffffffu, mine > 0.0 && t < excl + mine);
+    if (!own) {  // rounding: the last lane holding positive mass
+        const unsigned pos = __ballot_sync(0xffffffffu, mine > 0.0);
+        own = pos ? (1u << (31 - __clz(pos))) : 0u;
+        if (!own) return -1;
+    }
+    const int owner = __ffs(own) - 1;
+    int seg = -1;
+    double base = 0.0;
+    if (lane == owner) {
+        double run = 0.0, lastbase = excl;
+        int lastpos = -1;
+        for (int s = s0; s < s1; ++s) {
+            const double sv = (double)__ldcg(segs + s);
+            if (sv > 0.0) { lastpos = s; lastbase = excl + run; }
+            if (sv > 0.0 && t < excl + run + sv) { seg = s; base = excl + run; break; }
+            run += sv;
+        }
+        if (seg < 0) { seg = lastpos; base = lastbase; }
+    }
+    seg = __shfl_sync(0xffffffffu, seg, owner);
+    base = __shfl_sync(0xffffffffu, base, owner);
+    if (seg < 0) return -1;
+    return resolve_in_segment<DT, VEC>(P, rowp, rowq, pl, (long long)seg * SEGV, t - base);
+}
+
 template <int DT, int VEC>
 __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
 {
-    __shared__ double sh_d[WARPS];
-    __shared__ int sh_flag, sh_owner, sh_seg;
-    __shared__ double sh_base;
-
-    const int b = blockIdx.x / P.C2, c = blockIdx.x % P.C2;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Plan pl = ld_plan(P.plan + b);
-    const int nseg_chunk = P.iters2 * WARPS;
-    const char* rowp = spec_row_ptr(P, b, pl.rp);
-    const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
-
-    if (pl.status == ROW_OK) {
-        const long long cb = (long long)c * P.cv2;
-        const long long ce = min(cb + P.cv2, P.nvec);
-        float* segs = P.segs + ((size_t)b * P.C2 + c) * nseg_chunk;
-        for (int it = 0; it < P.iters2; ++it) {
-            const long long v = cb + (long long)it * NT + tid;
-            float ls = 0.f;
-            if (v < ce) {
-                float r[VEC];
-                residual_vec<DT, VEC>(rowp, rowq, v, pl, P.c, false, r);
-                ls = tree_sum(r);
+    const int lane = threadIdx.x & 31;
+    const uint64_t pol = policy_evict_first();
+    long long t = claim_task(&P.work[1]);
+    while (t < P.tasks2) {
+        const long long next = claim_task(&P.work[1]);
+        const int b = (int)(t / P.S2), s = (int)(t % P.S2);
+        const Plan pl = ld_plan(P.plan + b);
+        const char* rowp = spec_row_ptr(P, b, pl.rp);
+        const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
+        if (pl.status == ROW_OK) {
+            const long long t0 = (long long)s * TV2;
+            const long long t1 = min(t0 + TV2, P.nvec);
+            float* segs = P.segs + (size_t)b * P.nseg;
+#pragma unroll 1
+            for (int step = 0; step < ST2; ++step) {
+                const long long sb = t0 + (long long)step * 32 * U2;
+                if (sb >= t1) break;
+                RawVec<DT, VEC> xp[U2], xq[U2];
+#pragma unroll
+                for (int u = 0; u < U2; ++u) {
+                    const long long v = sb + u * 32 + lane;
+                    xp[u].fill_neg_inf();
+                    xq[u].fill_neg_inf();
+                    if (v < t1) {
+                        xp[u].load(rowp, v, pol);
+                        if (rowq) xq[u].load(rowq, v, pol);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U2; ++u) {
+                    const long long v = sb + u * 32 + lane;
+                    float ls = 0.f;
+                    if (v < t1) {
+                        float a[VEC], q[VEC], r[VEC];
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) { a[e] = xp[u].get(e); q[e] = xq[u].get(e); }
+                        residual_from<VEC>(a, q, rowq != nullptr, pl, P.c, r);
+                        ls = tree_sum(r);
+                    }
+                    const float ws = warp_sum(ls);
+                    if (lane == 0 && sb + u * 32 < t1) segs[(sb + u * 32) / SEGV] = ws;
+                }
             }
-            const float ws = warp_sum(ls);
-            if (lane == 0) segs[it * WARPS + warp] = ws;
         }
-    }
-    if (!arrive_last(&P.res_ctr[b], (unsigned)P.C2, &sh_flag)) return;
-    if (pl.status != ROW_OK) {
-        emit_spec(P, b, pl.status, 0, -1);
-        return;
-    }
-
-    // fp64 scan of the request's segment sums in index order
-    const int nseg = P.C2 * nseg_chunk;
-    const float* segs = P.segs + (size_t)b * nseg;
-    const int per = (nseg + NT - 1) / NT;
-    const int s0 = min(tid * per, nseg), s1 = min(s0 + per, nseg);
-    double mine = 0.0;
-    for (int s = s0; s < s1; ++s) mine += (double)__ldcg(segs + s);
-    double Z;
-    const double excl = block_excl_scan_f64(mine, sh_d, &Z);
-    if (!(Z > 0.0) || !isfinite(Z)) {
-        emit_spec(P, b, ROW_DEGENERATE, 0, -1);
-        return;
-    }
-    const double t = pl.u * Z;
-    if (tid == 0) sh_owner = NT;
-    __syncthreads();
-    if (s1 > s0 && mine > 0.0 && t < excl + mine) atomicMin(&sh_owner, tid);
-    __syncthreads();
-    int owner = sh_owner;
-    if (owner == NT) {  // rounding: fall back to the last thread holding positive mass
-        if (tid == 0) sh_owner = -1;
-        __syncthreads();
-        if (mine > 0.0) atomicMax(&sh_owner, tid);
-        __syncthreads();
-        owner = sh_owner;
-    }
-    if (tid == owner) {
-        double run = 0.0;
-        int seg = -1, lastpos = -1;
-        double base = excl, lastbase = excl;
-        for (int s = s0; s < s1; ++s) {
-            const double sv = (double)__ldcg(segs + s);
-            const double nx = run + sv;
-            if (sv > 0.0) { lastpos = s; lastbase = excl + run; }
-            if (t < excl + nx && sv > 0.0) { seg = s; base = excl + run; break; }
-            run = nx;
+        if (warp_arrive_last(&P.res_ctr[b], (unsigned)P.S2)) {
+            int st = pl.status, tok = -1;
+            if (st == ROW_OK) {
+                tok = draw_from_segments<DT, VEC>(P, b, pl, rowp, rowq);
+                if (tok < 0) st = ROW_DEGENERATE;
+            }
+            emit_spec_warp(P, b, st, pl.A, tok);
         }
-        if (seg < 0) { seg = lastpos; base = lastbase; }
-        sh_seg = seg;
-        sh_base = base;
+        t = next;
     }
-    __syncthreads();
-    if (sh_seg < 0) {  // no segment holds positive mass (cannot happen when Z > 0)
-        emit_spec(P, b, ROW_DEGENERATE, 0, -1);
-        return;
-    }
-    if (warp == 0) {
-        const int seg = sh_seg;
-        const int cc = seg / nseg_chunk, rem = seg % nseg_chunk;
-        const int it = rem / WARPS, w = rem % WARPS;
-        const long long cb = (long long)cc * P.cv2;
-        const long long ce = min(cb + P.cv2, P.nvec);
-        const long long vbase = cb + (long long)it * NT + (long long)w * 32;
-        const int tok = resolve_in_segment<DT, VEC>(P, rowp, rowq, pl, vbase, ce, t - sh_base);
-        if (lane == 0) sh_seg = tok;
-    }
-    __syncthreads();
-    const int tok = sh_seg;
-    emit_spec(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
 }
 
-cudaError_t launch_softmax_path(const SpecParams& P, unsigned g1, unsigned g2, cudaStream_t st)
+// Chunk kernel for 16-byte vectors: one CTA per (request, chunk of RCHUNK contiguous vectors of the
+// selected row pair).  Thread t loads vectors t + i*NT (i < RCV) of both rows, U2 of each at a time
+// into registers.  Each warp's 32 vectors of one i form one segment; the last CTA of a request draws
+// the token.
+constexpr int RCV = 8;                 // vectors per row per thread
+constexpr int RCHUNK = NT * RCV;
+
+template <int DT>
+__global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
 {
-    if (P.dtype == DT_BF16 && P.vec == 8) {
-        spec_stats_kernel<DT_BF16, 8><<<g1, NT, 0, st>>>(P);
-        spec_resample_kernel<DT_BF16, 8><<<g2, NT, 0, st>>>(P);
-    } else if (P.dtype == DT_BF16) {
-        spec_stats_kernel<DT_BF16, 1><<<g1, NT, 0, st>>>(P);
-        spec_resample_kernel<DT_BF16, 1><<<g2, NT, 0, st>>>(P);
-    } else if (P.vec == 4) {
-        spec_stats_kernel<DT_F32, 4><<<g1, NT, 0, st>>>(P);
-        spec_resample_kernel<DT_F32, 4><<<g2, NT, 0, st>>>(P);
-    } else {
-        spec_stats_kernel<DT_F32, 1><<<g1, NT, 0, st>>>(P);
-        spec_resample_kernel<DT_F32, 1><<<g2, NT, 0, st>>>(P);
+    constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
+    __shared__ int sh_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x / P.S2, c = blockIdx.x % P.S2;
+    const Plan pl = ld_plan(P.plan + b);
+    const char* rowp = spec_row_ptr(P, b, pl.rp);
+    const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
+    const int c0 = c * RCHUNK;
+    const int c1 = (int)min((long long)c0 + RCHUNK, P.nvec);
+    if (pl.status == ROW_OK) {
+        const uint64_t pol = policy_evict_first();
+        float* segs = P.segs + (size_t)b * P.nseg;
+#pragma unroll
+        for (int it = 0; it < RCV / U2; ++it) {
+            RawVec<DT, VEC> a[U2], q[U2];
+#pragma unroll
+            for (int u = 0; u < U2; ++u) {
+                const int v = c0 + (it * U2 + u) * NT + tid;
+                a[u].w = make_uint4(0, 0, 0, 0);
+                q[u].w = make_uint4(0, 0, 0, 0);
+                if (v < c1) {
+                    a[u].load(rowp, v, pol);
+                    if (rowq) q[u].load(rowq, v, pol);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U2; ++u) {
+                const int seg0 = c0 + (it * U2 + u) * NT + warp * 32;
+                const int v = seg0 + lane;
+                float ls = 0.f;
+                if (v < c1) {
+                    float xp[VEC], xq[VEC], rv[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) { xp[e] = a[u].get(e); xq[e] = q[u].get(e); }
+                    residual_from<VEC>(xp, xq, rowq != nullptr, pl, P.c, rv);
+                    ls = tree_sum(rv);
+                }
+                const float ws = warp_sum(ls);
+                if (lane == 0 && seg0 < c1) segs[seg0 / SEGV] = ws;
+            }
+        }
     }
+    if (!arrive_last(&P.res_ctr[b], (unsigned)P.S2, &sh_flag)) return;
+    if (warp == 0) {
+        int st = pl.status, tok = -1;
+        if (st == ROW_OK) {
+            tok = draw_from_segments<DT, VEC>(P, b, pl, rowp, rowq);
+            if (tok < 0) st = ROW_DEGENERATE;
+        }
+        emit_spec_warp(P, b, st, pl.A, tok);
+    }
+}
+
+template <int DT, int VEC>
+static void launch_softmax_plain(const SpecParams& P, int sms, cudaStream_t st)
+{
+    spec_stats_kernel<DT, VEC><<<persistent_grid<spec_stats_kernel<DT, VEC>>(P.tasks1, sms), NT, 0, st>>>(P);
+    spec_resample_kernel<DT, VEC><<<persistent_grid<spec_resample_kernel<DT, VEC>>(P.tasks2, sms), NT, 0, st>>>(P);
+}
+
+template <int DT>
+static void launch_softmax_chunk(const SpecParams& P, cudaStream_t st)
+{
+    spec_stats_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.R * P.S1), NT, 0, st>>>(P);
+    spec_resample_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.S2), NT, 0, st>>>(P);
+}
+
+cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st)
+{
+    if (P.dtype == DT_BF16 && P.vec == 8) launch_softmax_chunk<DT_BF16>(P, st);
+    else if (P.dtype == DT_BF16) launch_softmax_plain<DT_BF16, 1>(P, sms, st);
+    else if (P.vec == 4) launch_softmax_chunk<DT_F32>(P, st);
+    else launch_softmax_plain<DT_F32, 1>(P, sms, st);
     return cudaGetLastError();
 }
 

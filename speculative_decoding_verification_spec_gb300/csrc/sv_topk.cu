@@ -149,7 +149,7 @@ struct TopkSmem {
 };
 
 template <int DT, int VEC>
-__global__ void __launch_bounds__(NT) topk_stats_kernel(SpecParams P)
+__global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
 {
     using Shape = TopkShape<DT>;
     constexpr int EPT = Shape::EPT, NREG = Shape::NREG;
@@ -200,18 +200,32 @@ __global__ void __launch_bounds__(NT) topk_stats_kernel(SpecParams P)
         }
     }
 
-    // ---- thread maximum (NaN-propagating) and non-finite detection
+    // ---- group maxima (G registers each), thread maximum; NaN-propagating
+    constexpr int G = 8, NG = NREG / G;
+    static_assert(NREG % G == 0, "register groups");
+    uint32_t gm[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        uint32_t m = w[g * G];
+#pragma unroll
+        for (int j = 1; j < G; ++j) {
+            if constexpr (DT == DT_BF16) m = bmax2_nan(m, w[g * G + j]);
+            else m = __float_as_uint(fmax_nan_f(__uint_as_float(m), __uint_as_float(w[g * G + j])));
+        }
+        gm[g] = m;
+    }
     float tmax;
     if constexpr (DT == DT_BF16) {
-        uint32_t pm = w[0];
+        uint32_t pm = gm[0];
 #pragma unroll
-        for (int j = 1; j < NREG; ++j) pm = bmax2_nan(pm, w[j]);
+        for (int g = 1; g < NG; ++g) pm = bmax2_nan(pm, gm[g]);
         tmax = fmax_nan_f(bf16lo(pm), bf16hi(pm));
     } else {
-        tmax = __uint_as_float(w[0]);
+        tmax = __uint_as_float(gm[0]);
 #pragma unroll
-        for (int j = 1; j < NREG; ++j) tmax = fmax_nan_f(tmax, __uint_as_float(w[j]));
+        for (int g = 1; g < NG; ++g) tmax = fmax_nan_f(tmax, __uint_as_float(gm[g]));
     }
+    if (threadIdx.x == 0) sm.n = 0;
     const int nonfinite = __syncthreads_or((tmax != tmax) || tmax == __int_as_float(0x7f800000));
 
     // ---- lower bound tau: k-th largest of the NT thread maxima (valid for k <= NT)
@@ -219,59 +233,45 @@ __global__ void __launch_bounds__(NT) topk_stats_kernel(SpecParams P)
     if (!nonfinite && k <= NT) tau_key = block_kth_key_per_thread<DT>(okey(tmax), k);
     const float tau = key_value(tau_key);
 
-    // ---- count and list the elements >= tau
-    int mine = 0;
-    if (!nonfinite) {
+    // ---- append every element >= tau to this chunk's list (unordered; the row merge sorts)
+    TopkEntry* dst = P.clist + ((size_t)row_id * P.CT + chunk) * P.cap_w;
+    const bool too_many = (k > NT) && (cend - cbase > P.cap_w);
+    if (!nonfinite && !too_many) {
+        auto append = [&](int slot, float x) {
+            const long long e = slot_elem<VEC>(cbase, slot);
+            if (e < cend) {
+                const int pos = atomicAdd(&sm.n, 1);
+                if (pos < P.cap_w) { TopkEntry en; en.x = x; en.idx = (int)e; dst[pos] = en; }
+            }
+        };
         if constexpr (DT == DT_BF16) {
             const __nv_bfloat162 t2 = __floats2bfloat162_rn(tau, tau);
 #pragma unroll
-            for (int j = 0; j < NREG; ++j) {
-                const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[j]), t2);
-                if (msk) {
-                    if ((msk & 0xffffu) && slot_elem<VEC>(cbase, 2 * j) < cend) ++mine;
-                    if ((msk >> 16) && slot_elem<VEC>(cbase, 2 * j + 1) < cend) ++mine;
+            for (int g = 0; g < NG; ++g) {
+                if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
+#pragma unroll
+                    for (int j = g * G; j < g * G + G; ++j) {
+                        const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[j]), t2);
+                        if (msk & 0xffffu) append(2 * j, bf16lo(w[j]));
+                        if (msk >> 16) append(2 * j + 1, bf16hi(w[j]));
+                    }
                 }
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < NREG; ++j)
-                if (__uint_as_float(w[j]) >= tau && slot_elem<VEC>(cbase, j) < cend) ++mine;
-        }
-    }
-    int total;
-    const int off = block_excl_scan_int(mine, sm.red, &total);
-    const bool overflow = total > CAP_S;
-    if (!nonfinite && !overflow && mine) {
-        int o = off;
+            for (int g = 0; g < NG; ++g) {
+                if (__uint_as_float(gm[g]) >= tau) {
 #pragma unroll
-        for (int s = 0; s < EPT; ++s) {
-            const float x = reg_value<DT, VEC>(w, s);
-            const long long e = slot_elem<VEC>(cbase, s);
-            if (x >= tau && e < cend) { sm.cand[o].x = x; sm.cand[o].idx = (int)e; ++o; }
+                    for (int j = g * G; j < g * G + G; ++j)
+                        if (__uint_as_float(w[j]) >= tau) append(j, __uint_as_float(w[j]));
+                }
+            }
         }
     }
     __syncthreads();
-
-    // ---- exact chunk-local k-th largest l_c; list every element >= l_c
-    int* rec = P.ccount + (size_t)row_id * P.CT + chunk;
-    if (nonfinite) {
-        if (threadIdx.x == 0) *rec = -2;
-    } else if (overflow) {
-        if (threadIdx.x == 0) *rec = -1;
-    } else {
-        const uint32_t lkey = (total >= k) ? block_kth_key<DT>(sm.cand, total, k, sm.red) : okey(NEG_INF);
-        if (threadIdx.x == 0) sm.n = 0;
-        __syncthreads();
-        TopkEntry* dst = P.clist + ((size_t)row_id * P.CT + chunk) * P.cap_w;
-        for (int i = threadIdx.x; i < total; i += NT) {
-            const TopkEntry en = sm.cand[i];
-            if (okey(en.x) >= lkey) {
-                const int o = atomicAdd(&sm.n, 1);
-                if (o < P.cap_w) dst[o] = en;
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) *rec = (sm.n <= P.cap_w) ? sm.n : -1;
+    if (threadIdx.x == 0) {
+        const int n = sm.n;
+        P.ccount[(size_t)row_id * P.CT + chunk] = nonfinite ? -2 : ((too_many || n > P.cap_w) ? -1 : n);
     }
     if (!arrive_last(&P.row_ctr[row_id], (unsigned)P.CT, &sm.flag)) return;
 
@@ -357,7 +357,13 @@ __global__ void __launch_bounds__(NT) topk_stats_kernel(SpecParams P)
         if (threadIdx.x == 0) P.ndense[b] = nd;
         return;
     }
-    const Plan pl = compute_plan<DT>(P, b, true);
+    __shared__ Plan sh_plan;
+    if (threadIdx.x < 32) {
+        const Plan p0 = compute_plan_warp<DT>(P, b, true);
+        if (threadIdx.x == 0) sh_plan = p0;
+    }
+    __syncthreads();
+    const Plan pl = sh_plan;
     if (pl.status != ROW_OK) {
         emit_spec(P, b, pl.status, 0, -1);
         return;
@@ -480,7 +486,13 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
     if (!arrive_last(&P.dense_ctr[b], nd, &sh_flag)) return;
     if (threadIdx.x == 0) P.ndense[b] = 0;
 
-    const Plan pl = compute_plan<DT>(P, b, true);
+    __shared__ Plan sh_plan;
+    if (threadIdx.x < 32) {
+        const Plan p0 = compute_plan_warp<DT>(P, b, true);
+        if (threadIdx.x == 0) sh_plan = p0;
+    }
+    __syncthreads();
+    const Plan pl = sh_plan;
     if (pl.status != ROW_OK) {
         emit_spec(P, b, pl.status, 0, -1);
         return;
