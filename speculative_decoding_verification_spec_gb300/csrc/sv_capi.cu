@@ -44,19 +44,23 @@ constexpr double PIN_BYTES = 80e6;
 
 static int topk_ept(int dtype) { return dtype == DT_BF16 ? 80 : 40; }
 static int topk_cap(int k) { return (int)std::min(2048LL, (2 * (long long)k + 64 + 31) / 32 * 32); }
+// per-row union capacity: CT chunks of up to topk_cap(k) candidates each, at most 2048
+static int topk_ucap(int CT, int k) { return (int)std::min(2048LL, (long long)CT * topk_cap(k)); }
 
 // --------------------------------------------------------------------------- workspace layout
 
 struct SpecLayout {
     size_t ctr_bytes = 0, bytes = 0;
     size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0, o_work = 0;
+    size_t o_ucount = 0, o_uflags = 0;
     size_t o_partials = 0, o_rstats = 0, o_plan = 0, o_segs = 0;
-    size_t o_clist = 0, o_ccount = 0, o_klist = 0;
+    size_t o_ulist = 0, o_klist = 0;
 };
 
-// Byte layout for `ppr` softmax partials per row, nseg residual segments per request and (top-k) CT
-// chunks of `cap` list entries.  All counters sit at the front so one memset clears them.
-static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool topk, int CT, int cap)
+// Byte layout for `ppr` softmax partials per row, nseg residual segments per request and (top-k)
+// per-row unions of `cap_u` and kept lists of `cap_k` entries.  All counters sit at the front so
+// one memset clears them.
+static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool topk, int cap_u, int cap_k)
 {
     SpecLayout L;
     size_t o = 0;
@@ -66,6 +70,10 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_dense_ctr = o; o += (size_t)B * sizeof(unsigned);
     L.o_ndense = o; o += (size_t)B * sizeof(int);
     L.o_work = o; o += 2 * sizeof(unsigned);
+    if (topk) {
+        L.o_ucount = o; o += (size_t)B * R * sizeof(int);
+        L.o_uflags = o; o += (size_t)B * R * sizeof(int);
+    }
     L.ctr_bytes = o;
     o = align_up(o);
     L.o_partials = o; o = align_up(o + (size_t)B * R * ppr * sizeof(Partial));
@@ -73,9 +81,8 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_plan = o; o = align_up(o + (size_t)B * sizeof(Plan));
     L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
     if (topk) {
-        L.o_clist = o; o = align_up(o + (size_t)B * R * CT * cap * sizeof(TopkEntry));
-        L.o_ccount = o; o = align_up(o + (size_t)B * R * CT * sizeof(int));
-        L.o_klist = o; o = align_up(o + (size_t)B * R * cap * sizeof(TopkEntry));
+        L.o_ulist = o; o = align_up(o + (size_t)B * R * cap_u * sizeof(TopkEntry));
+        L.o_klist = o; o = align_up(o + (size_t)B * R * cap_k * sizeof(TopkEntry));
     }
     L.bytes = o;
     return L;
@@ -185,10 +192,10 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.pin_pairs = (int)std::min(2.0, std::floor(PIN_BYTES / ((double)B * 2.0 * (double)V * (double)es)));
     if (topk) {
         P.CT = (int)cdiv(V, (long long)NT * topk_ept(dt));
-        P.cap_w = topk_cap(top_k);
-        P.cap_k = P.cap_w;
+        P.cap_k = topk_cap(top_k);
+        P.cap_u = topk_ucap(P.CT, top_k);
     }
-    const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.CT, P.cap_w);
+    const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.cap_u, P.cap_k);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
     if ((long long)B * R * (topk ? P.CT : 1) >= (1LL << 31) || P.tasks1 >= (1LL << 31))
         return SPEC_ERR_INVALID_ARG;
@@ -211,8 +218,9 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.plan = reinterpret_cast<Plan*>(ws + L.o_plan);
     P.segs = reinterpret_cast<float*>(ws + L.o_segs);
     if (topk) {
-        P.clist = reinterpret_cast<TopkEntry*>(ws + L.o_clist);
-        P.ccount = reinterpret_cast<int*>(ws + L.o_ccount);
+        P.ulist = reinterpret_cast<TopkEntry*>(ws + L.o_ulist);
+        P.ucount = reinterpret_cast<int*>(ws + L.o_ucount);
+        P.uflags = reinterpret_cast<int*>(ws + L.o_uflags);
         P.klist = reinterpret_cast<TopkEntry*>(ws + L.o_klist);
     }
 
@@ -246,8 +254,8 @@ size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
             const bool topk = top_k > 0 && top_k < V;
             int CT = 0;
             if (topk) CT = (int)cdiv(V, (long long)NT * std::min(topk_ept(DT_BF16), topk_ept(DT_F32)));
-            const SpecLayout L = spec_layout(B, 2 * gamma + 1, partials_per_row(sh), nsegs(sh), topk, CT,
-                                             topk ? topk_cap(top_k) : 0);
+            const SpecLayout L = spec_layout(B, 2 * gamma + 1, partials_per_row(sh), nsegs(sh), topk,
+                                             topk ? topk_ucap(CT, top_k) : 0, topk ? topk_cap(top_k) : 0);
             best = std::max(best, L.bytes);
         }
     }

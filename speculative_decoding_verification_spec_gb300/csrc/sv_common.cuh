@@ -95,8 +95,8 @@ struct SpecParams {
     long long tasks1, tasks2;
     // top-k chunking and capacities
     int CT;
-    int cap_w;            // per-chunk list capacity (entries)
     int cap_k;            // per-row kept-list capacity
+    int cap_u;            // per-row union capacity (entries)
     // outputs
     int32_t* accepted_len;
     int32_t* out_tokens;
@@ -113,8 +113,9 @@ struct SpecParams {
     unsigned* req_ctr;    // [B]
     unsigned* res_ctr;    // [B]
     unsigned* work;       // [2] task counters of the two streaming kernels
-    TopkEntry* clist;     // [B*R*CT*cap_w] per-chunk candidate lists
-    int* ccount;          // [B*R*CT] entries per chunk list (-1 = overflow)
+    TopkEntry* ulist;     // [B*R*cap_u] per-row union of the chunks' candidates (unordered)
+    int* ucount;          // [B*R] entries reserved in ulist
+    int* uflags;          // [B*R] 1 = non-finite row, 2 = candidates overflowed (dense row)
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
     unsigned* dense_ctr;  // [B]
     int* ndense;          // [B]

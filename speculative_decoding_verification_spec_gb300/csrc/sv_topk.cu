@@ -5,26 +5,24 @@
 // whose stored logit is >= the row's k-th largest stored logit (counted with multiplicity), so ties
 // at the threshold are all kept.
 //
-// Kernel 1 (topk_stats_kernel): one CTA per (row, chunk of NT*EPT elements), the chunk held in
-// registers.  A lower bound tau of the chunk's k-th largest value is the k-th largest of the NT
-// per-thread maxima (NT disjoint groups, so at least k chunk elements are >= tau); only elements
-// >= tau -- a few dozen for k = 50 -- leave the registers.  The chunk's exact k-th largest value l_c
-// is selected among them and every element >= l_c is listed.  Since the row's k-th largest value g
-// satisfies g >= l_c for every chunk, the union of the chunk lists holds every element >= g, and the
-// last CTA of the row selects g exactly from the union, keeps the entries >= g sorted by index, and
-// forms (M, S) over them.  The last row of a request runs the acceptance scan and draws the
-// correction / bonus token directly from the kept lists: the residual vanishes outside K_p, so no
-// second pass over V is needed.
+// Kernel 1 (topk_stats_kernel): one CTA per (row, contiguous chunk of NT*EPT elements), the chunk
+// held in registers.  A lower bound tau of the chunk's k-th largest value is the k-th largest of the
+// NT per-thread maxima (NT disjoint groups, so at least k chunk elements are >= tau), selected by
+// one warp; only elements >= tau -- a few dozen for k = 50 -- leave the registers: collected in
+// shared memory, then appended to the row's union buffer with one reservation per chunk.  Since the
+// row's k-th largest value g is >= every chunk's tau, the union holds every element >= g.  One warp of the last CTA of the row selects g exactly from
+// the union, keeps the entries >= g sorted by index and forms (M, S) over them; one warp of the last
+// row of a request runs the acceptance scan and draws the correction / bonus token directly from
+// the kept list: the residual vanishes outside K_p, so no second pass over V is needed.
 //
-// Rows whose candidates overflow the on-chip capacities (massive ties, k > NT, ...) are marked
-// dense and finished exactly by kernel 2 (topk_dense_kernel) with full-row passes.
+// Rows whose candidates overflow the capacities (massive ties, k > NT, ...) are marked dense and
+// finished exactly by kernel 2 (topk_dense_kernel) with full-row passes.
 #include <cuda_bf16.h>
 
 #include "sv_plan.cuh"
 
 namespace sv {
 
-constexpr int CAP_S = 2048;  // candidate entries a chunk CTA holds on chip
 constexpr int CAP_U = 2048;  // union entries the row epilogue holds on chip
 
 // order-preserving 32-bit key of a float; -0 and +0 map to the same key
@@ -45,33 +43,20 @@ __device__ __forceinline__ float fmax_nan_f(float a, float b)
     return r;
 }
 
-// Largest key P with count(key >= P) >= k over the n entries (the k-th largest key).  bf16-valued
-// entries only differ in the top 16 key bits.  All threads of the CTA must call it.
-template <int DT>
-__device__ uint32_t block_kth_key(const TopkEntry* e, int n, int k, int* sh_red)
+// The k-th largest key (largest P with count(key >= P) >= k) among n keys produced by key_at(i),
+// by one warp: bitwise search from the top bit, counting with a warp reduction per bit.
+// bf16-valued keys differ only in their top 16 bits.
+template <int DT, class KeyAt>
+__device__ uint32_t warp_kth_key(int n, int k, KeyAt key_at)
 {
+    const int lane = threadIdx.x & 31;
     uint32_t prefix = 0;
     constexpr int lo = (DT == DT_BF16) ? 16 : 0;
     for (int bit = 31; bit >= lo; --bit) {
         const uint32_t want = prefix | (1u << bit);
-        int cnt = 0;
-        for (int i = threadIdx.x; i < n; i += NT) cnt += okey(e[i].x) >= want;
-        cnt = block_sum_int(cnt, sh_red);
-        if (cnt >= k) prefix = want;
-    }
-    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-    return prefix;
-}
-
-// same over one value per thread
-template <int DT>
-__device__ uint32_t block_kth_key_per_thread(uint32_t key, int k)
-{
-    uint32_t prefix = 0;
-    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-    for (int bit = 31; bit >= lo; --bit) {
-        const uint32_t want = prefix | (1u << bit);
-        if (__syncthreads_count(key >= want) >= k) prefix = want;
+        unsigned cnt = 0;
+        for (int i = lane; i < n; i += 32) cnt += key_at(i) >= want;
+        if ((int)__reduce_add_sync(0xffffffffu, cnt) >= k) prefix = want;
     }
     if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
     return prefix;
@@ -82,71 +67,180 @@ template <int DT> struct TopkShape;
 template <> struct TopkShape<DT_BF16> { static constexpr int EPT = 80, NREG = 40; };
 template <> struct TopkShape<DT_F32> { static constexpr int EPT = 40, NREG = 40; };
 
-// element index of register slot s of this thread (slot order = vector j, then lane e of it)
+// element index (within the row) of register slot s of this thread: vector j = s / VEC, element
+// e = s % VEC of it; vectors of a thread are NT apart
 template <int VEC>
-__device__ __forceinline__ long long slot_elem(long long cbase, int s)
+__device__ __forceinline__ int slot_elem(int cbase, int s)
 {
-    if constexpr (VEC == 1) return cbase + (long long)s * NT + threadIdx.x;
-    else return cbase + ((long long)(s / VEC) * NT + threadIdx.x) * VEC + (s % VEC);
+    if constexpr (VEC == 1) return cbase + s * NT + (int)threadIdx.x;
+    else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
 }
 
-template <int DT, int VEC>
-__device__ __forceinline__ float reg_value(const uint32_t (&w)[TopkShape<DT>::NREG], int s)
-{
-    if constexpr (DT == DT_BF16) return (s & 1) ? bf16hi(w[s >> 1]) : bf16lo(w[s >> 1]);
-    else return __uint_as_float(w[s]);
-}
+constexpr int CAP_C = 1024;  // candidates a chunk CTA collects on chip
 
-// block exclusive scan of an int; returns exclusive prefix, total in *tot
-__device__ __forceinline__ int block_excl_scan_int(int v, int* sh, int* tot)
+struct TopkSmem {
+    union {
+        TopkEntry cand[CAP_C];  // chunk phase: this chunk's candidates
+        TopkEntry u[CAP_U];     // row epilogue: union of the chunks' candidates
+        double rr[CAP_U];       // request epilogue: residual mass of the kept list
+    };
+    TopkEntry kept[CAP_U];
+    float tmax[NT];
+    float tau;
+    int n, base, flag, nonfinite;
+};
+
+// append one candidate to the chunk's on-chip list (the slot beyond CAP_C only counts)
+__device__ __forceinline__ void cand_push(TopkSmem& sm, float x, int e)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int incl = warp_incl_scan(v);
-    __syncthreads();
-    if (lane == 31) sh[warp] = incl;
-    __syncthreads();
-    int before = 0, t = 0;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) {
-        if (w < warp) before += sh[w];
-        t += sh[w];
+    const int pos = atomicAdd(&sm.n, 1);
+    if (pos < CAP_C) {
+        sm.cand[pos].x = x;
+        sm.cand[pos].idx = e;
     }
-    *tot = t;
-    return before + incl - v;
 }
 
-// bitonic sort of n entries by index (ascending), padded to a power of two with idx = INT_MAX
-__device__ void block_sort_by_index(TopkEntry* e, int n)
+// Warp-level bitonic sort of e[0..n) by index (ascending), padding to a power of two.
+__device__ void warp_sort_by_index(TopkEntry* e, int n)
 {
+    const int lane = threadIdx.x & 31;
     int m = 1;
     while (m < n) m <<= 1;
-    for (int i = n + threadIdx.x; i < m; i += NT) { e[i].idx = 0x7fffffff; e[i].x = NEG_INF; }
-    __syncthreads();
+    for (int i = n + lane; i < m; i += 32) { e[i].idx = 0x7fffffff; e[i].x = NEG_INF; }
+    __syncwarp();
     for (int size = 2; size <= m; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < m; i += NT) {
+            for (int i = lane; i < m; i += 32) {
                 const int j = i ^ stride;
                 if (j > i) {
                     const bool up = (i & size) == 0;
-                    TopkEntry a = e[i], b = e[j];
+                    const TopkEntry a = e[i], b = e[j];
                     if ((a.idx > b.idx) == up) { e[i] = b; e[j] = a; }
                 }
             }
-            __syncthreads();
+            __syncwarp();
         }
     }
 }
 
-struct TopkSmem {
-    union {
-        TopkEntry cand[CAP_S];  // chunk candidates, then the row's union
-        double rr[CAP_S];       // request epilogue: residual mass of the kept list
-    };
-    TopkEntry kept[CAP_U];
-    int red[WARPS];
-    float redf[WARPS];
-    int flag, n;
-};
+// One warp of the last CTA of a row: exact threshold over the union of the chunk lists, kept list
+// sorted by index, normaliser over it.  Returns the row's stats.
+template <int DT>
+__device__ RowStats topk_row_epilogue(const SpecParams& P, TopkSmem& sm, int row_id)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    RowStats st;
+    st.M = NEG_INF; st.MC = NEG_INF; st.S = 0.0; st.thr = NEG_INF;
+    st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
+    const int flags = __ldcg(P.uflags + row_id);
+    const int total = __ldcg(P.ucount + row_id);
+    if (flags & 1) { st.status = ROW_NONFINITE; return st; }
+    if ((flags & 2) || total > P.cap_u) { st.dense = 1; return st; }
+    // the union, contiguous: independent loads, several in flight per lane
+    const TopkEntry* src = P.ulist + (size_t)row_id * P.cap_u;
+#pragma unroll 8
+    for (int i = lane; i < total; i += 32) {
+        TopkEntry en;
+        en.x = __ldcg(&src[i].x);
+        en.idx = __ldcg(&src[i].idx);
+        sm.u[i] = en;
+    }
+    __syncwarp();
+    const int k = P.top_k;
+    const uint32_t gkey = (total >= k) ? warp_kth_key<DT>(total, k, [&](int i) { return okey(sm.u[i].x); })
+                                       : okey(NEG_INF);
+    // stable ballot compaction of the entries >= g
+    int nk = 0;
+    for (int i0 = 0; i0 < total; i0 += 32) {
+        const int i = i0 + lane;
+        const bool keep = i < total && okey(sm.u[i].x) >= gkey;
+        const unsigned bal = __ballot_sync(FULL, keep);
+        if (keep) sm.kept[nk + __popc(bal & ((1u << lane) - 1u))] = sm.u[i];
+        nk += __popc(bal);
+    }
+    __syncwarp();
+    if (nk > P.cap_k) { st.dense = 1; return st; }
+    warp_sort_by_index(sm.kept, nk);
+    float mx = NEG_INF;
+    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, sm.kept[i].x);
+    const float M = warp_max(mx);
+    const float MC = M * P.c;
+    double acc = 0.0;
+    if (M != NEG_INF)
+        for (int i = lane; i < nk; i += 32) acc += (double)ex2(fmaf(sm.kept[i].x, P.c, -MC));
+    const double S = warp_sum(acc);
+    TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
+    for (int i = lane; i < nk; i += 32) kl[i] = sm.kept[i];
+    st.M = M;
+    st.MC = MC;
+    st.S = S;
+    st.thr = key_value(gkey);
+    st.klist_n = nk;
+    st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
+    return st;
+}
+
+// One warp: acceptance scan of request b and the correction / bonus draw from the kept list of
+// the p row (index order); the residual is zero outside K_p.
+template <int DT>
+__device__ void topk_request_epilogue(const SpecParams& P, TopkSmem& sm, int b)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    const Plan pl = compute_plan_warp<DT>(P, b, true);
+    if (pl.status != ROW_OK) {
+        emit_spec_warp(P, b, pl.status, 0, -1);
+        return;
+    }
+    const RowStats sp = ld_rowstats(P.rstats + (size_t)b * P.R + pl.rp);
+    const int nk = sp.klist_n;
+    const TopkEntry* kl = P.klist + ((size_t)b * P.R + pl.rp) * P.cap_k;
+    const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
+    // each lane owns a contiguous block of the kept list
+    const int per = (nk + 31) / 32;
+    const int i0 = min(lane * per, nk), i1 = min(i0 + per, nk);
+    double mine = 0.0;
+    for (int i = i0; i < i1; ++i) {
+        const float xp = __ldcg(&kl[i].x);
+        const int v = __ldcg(&kl[i].idx);
+        const float pp = __fmul_rn(ex2(fmaf(xp, P.c, -pl.MCp)), pl.invSp);
+        float res = pp;
+        if (rowq) {
+            const float xq = load_logit(rowq, DT, v);
+            const float qq = (xq >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq, P.c, -pl.MCq)), pl.invSq) : 0.f;
+            res = fmaxf(__fsub_rn(pp, qq), 0.f);
+        }
+        sm.rr[i] = (double)res;
+        mine += (double)res;
+    }
+    const double incl = warp_incl_scan(mine);
+    const double Z = __shfl_sync(FULL, incl, 31);
+    int tok = -1;
+    if (Z > 0.0 && isfinite(Z)) {
+        const double t = pl.u * Z, excl = incl - mine;
+        unsigned own = __ballot_sync(FULL, mine > 0.0 && t < excl + mine);
+        if (!own) {
+            const unsigned pos = __ballot_sync(FULL, mine > 0.0);
+            own = pos ? (1u << (31 - __clz(pos))) : 0u;
+        }
+        if (own) {
+            const int owner = __ffs(own) - 1;
+            if (lane == owner) {
+                double run = excl;
+                int lastpos = -1;
+                for (int i = i0; i < i1; ++i) {
+                    if (sm.rr[i] > 0.0) lastpos = i;
+                    run += sm.rr[i];
+                    if (t < run && sm.rr[i] > 0.0) { tok = __ldcg(&kl[i].idx); break; }
+                }
+                if (tok < 0 && lastpos >= 0) tok = __ldcg(&kl[lastpos].idx);
+            }
+            tok = __shfl_sync(FULL, tok, owner);
+        }
+    }
+    emit_spec_warp(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
+}
 
 template <int DT, int VEC>
 __global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
@@ -155,52 +249,58 @@ __global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
     constexpr int EPT = Shape::EPT, NREG = Shape::NREG;
     static_assert(sizeof(TopkSmem) <= 48 * 1024, "static shared memory");
     __shared__ TopkSmem sm;
-
-    const long long idx = blockIdx.x;
-    const int chunk = (int)(idx % P.CT);
-    const long long rs = idx / P.CT;
-    const int b = (int)(rs / P.R), r = (int)(rs % P.R);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chunk = blockIdx.x % P.CT;
+    const int rs = blockIdx.x / P.CT;
+    const int b = rs / P.R, r = rs % P.R;
     const int row_id = b * P.R + r;
     const char* row = spec_row_ptr(P, b, r);
-    const long long CE = (long long)NT * EPT;
-    const long long cbase = (long long)chunk * CE;
-    const long long cend = min(cbase + CE, (long long)P.V);
+    const int cbase = chunk * NT * EPT;
+    const int cend = min(cbase + NT * EPT, P.V);
     const int k = P.top_k;
+    const uint64_t pol = policy_evict_first();
 
     // ---- load the chunk into registers (-inf padding)
     uint32_t w[NREG];
     if constexpr (VEC > 1) {
         constexpr int NV = EPT / VEC;  // vectors per thread
+        constexpr int ES = (DT == DT_BF16) ? 2 : 4;
+        const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+        const char* tp = row + ((size_t)cbase + (size_t)tid * VEC) * ES;  // this thread's first vector
+        if (cbase + NT * EPT <= cend) {  // full chunk: fixed offsets, no bounds checks
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const long long e0 = slot_elem<VEC>(cbase, j * VEC);
-            uint4 q = make_uint4(0, 0, 0, 0);
-            const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-            if (e0 < cend) q = ld_stream_v4(row + e0 * (DT == DT_BF16 ? 2 : 4));
-            else q = make_uint4(pad, pad, pad, pad);
-            w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
-        }
-    } else {
-        if constexpr (DT == DT_BF16) {
-            const unsigned short* rp = reinterpret_cast<const unsigned short*>(row);
-#pragma unroll
-            for (int j = 0; j < NREG; ++j) {
-                const long long e0 = slot_elem<1>(cbase, 2 * j), e1 = slot_elem<1>(cbase, 2 * j + 1);
-                const uint32_t lo = e0 < cend ? __ldg(rp + e0) : 0xff80u;
-                const uint32_t hi = e1 < cend ? __ldg(rp + e1) : 0xff80u;
-                w[j] = lo | (hi << 16);
+            for (int j = 0; j < NV; ++j) {
+                const uint4 q = ld_stream_v4_pol(tp + (size_t)j * NT * VEC * ES, pol);
+                w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
             }
         } else {
-            const float* rp = reinterpret_cast<const float*>(row);
 #pragma unroll
-            for (int j = 0; j < NREG; ++j) {
-                const long long e0 = slot_elem<1>(cbase, j);
-                w[j] = e0 < cend ? __float_as_uint(__ldg(rp + e0)) : 0xff800000u;
+            for (int j = 0; j < NV; ++j) {
+                const int e0 = cbase + (j * NT + tid) * VEC;
+                const uint4 q = e0 < cend ? ld_stream_v4_pol(tp + (size_t)j * NT * VEC * ES, pol)
+                                          : make_uint4(pad, pad, pad, pad);
+                w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
             }
+        }
+    } else if constexpr (DT == DT_BF16) {
+        const unsigned short* rp = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+        for (int j = 0; j < NREG; ++j) {
+            const int e0 = slot_elem<1>(cbase, 2 * j), e1 = slot_elem<1>(cbase, 2 * j + 1);
+            const uint32_t lo = e0 < cend ? __ldg(rp + e0) : 0xff80u;
+            const uint32_t hi = e1 < cend ? __ldg(rp + e1) : 0xff80u;
+            w[j] = lo | (hi << 16);
+        }
+    } else {
+        const float* rp = reinterpret_cast<const float*>(row);
+#pragma unroll
+        for (int j = 0; j < NREG; ++j) {
+            const int e0 = slot_elem<1>(cbase, j);
+            w[j] = e0 < cend ? __float_as_uint(__ldg(rp + e0)) : 0xff800000u;
         }
     }
 
-    // ---- group maxima (G registers each), thread maximum; NaN-propagating
+    // ---- group maxima (G registers each) and the thread maximum, NaN-propagating
     constexpr int G = 8, NG = NREG / G;
     static_assert(NREG % G == 0, "register groups");
     uint32_t gm[NG];
@@ -225,188 +325,115 @@ __global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
 #pragma unroll
         for (int g = 1; g < NG; ++g) tmax = fmax_nan_f(tmax, __uint_as_float(gm[g]));
     }
-    if (threadIdx.x == 0) sm.n = 0;
-    const int nonfinite = __syncthreads_or((tmax != tmax) || tmax == __int_as_float(0x7f800000));
+    sm.tmax[tid] = tmax;
+    __syncthreads();
 
-    // ---- lower bound tau: k-th largest of the NT thread maxima (valid for k <= NT)
-    uint32_t tau_key = okey(NEG_INF);
-    if (!nonfinite && k <= NT) tau_key = block_kth_key_per_thread<DT>(okey(tmax), k);
-    const float tau = key_value(tau_key);
-
-    // ---- append every element >= tau to this chunk's list (unordered; the row merge sorts)
-    TopkEntry* dst = P.clist + ((size_t)row_id * P.CT + chunk) * P.cap_w;
-    const bool too_many = (k > NT) && (cend - cbase > P.cap_w);
-    if (!nonfinite && !too_many) {
-        auto append = [&](int slot, float x) {
-            const long long e = slot_elem<VEC>(cbase, slot);
-            if (e < cend) {
-                const int pos = atomicAdd(&sm.n, 1);
-                if (pos < P.cap_w) { TopkEntry en; en.x = x; en.idx = (int)e; dst[pos] = en; }
-            }
-        };
-        if constexpr (DT == DT_BF16) {
-            const __nv_bfloat162 t2 = __floats2bfloat162_rn(tau, tau);
+    // ---- one warp: non-finite check and tau = k-th largest thread maximum (valid for k <= NT)
+    if (warp == 0) {
+        int bad = 0;
+        for (int i = lane; i < NT; i += 32) {
+            const float x = sm.tmax[i];
+            if (x != x || x == __int_as_float(0x7f800000)) bad = 1;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        uint32_t tk = okey(NEG_INF);
+        if (!bad && k <= NT) {
+            uint32_t keys[NT / 32];
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
+            for (int i = 0; i < NT / 32; ++i) keys[i] = okey(sm.tmax[lane + 32 * i]);
+            uint32_t prefix = 0;
+            constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+            for (int bit = 31; bit >= lo; --bit) {
+                const uint32_t want = prefix | (1u << bit);
+                unsigned cnt = 0;
+#pragma unroll
+                for (int i = 0; i < NT / 32; ++i) cnt += keys[i] >= want;
+                if ((int)__reduce_add_sync(0xffffffffu, cnt) >= k) prefix = want;
+            }
+            if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+            tk = prefix;
+        }
+        if (lane == 0) {
+            sm.tau = key_value(tk);
+            sm.nonfinite = bad;
+            sm.n = 0;
+        }
+    }
+    __syncthreads();
+    const float tau = sm.tau;
+    const int nonfinite = sm.nonfinite;
+
+    // ---- collect every element >= tau on chip (unordered; the row merge sorts)
+    const bool too_many = (k > NT) && (cend - cbase > CAP_C);
+    if (!nonfinite && !too_many) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            if constexpr (DT == DT_BF16) {
+                const __nv_bfloat162 t2 = __floats2bfloat162_rn(tau, tau);
                 if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
 #pragma unroll
-                    for (int j = g * G; j < g * G + G; ++j) {
-                        const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[j]), t2);
-                        if (msk & 0xffffu) append(2 * j, bf16lo(w[j]));
-                        if (msk >> 16) append(2 * j + 1, bf16hi(w[j]));
+                    for (int j = 0; j < G; ++j) {
+                        const uint32_t wd = w[g * G + j];
+                        const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd), t2);
+                        if (msk & 0xffffu) {
+                            const int e = slot_elem<VEC>(cbase, 2 * (g * G + j));
+                            if (e < cend) cand_push(sm, bf16lo(wd), e);
+                        }
+                        if (msk >> 16) {
+                            const int e = slot_elem<VEC>(cbase, 2 * (g * G + j) + 1);
+                            if (e < cend) cand_push(sm, bf16hi(wd), e);
+                        }
+                    }
+                }
+            } else {
+                if (__uint_as_float(gm[g]) >= tau) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const float x = __uint_as_float(w[g * G + j]);
+                        if (x >= tau) {
+                            const int e = slot_elem<VEC>(cbase, g * G + j);
+                            if (e < cend) cand_push(sm, x, e);
+                        }
                     }
                 }
             }
-        } else {
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                if (__uint_as_float(gm[g]) >= tau) {
-#pragma unroll
-                    for (int j = g * G; j < g * G + G; ++j)
-                        if (__uint_as_float(w[j]) >= tau) append(j, __uint_as_float(w[j]));
-                }
-            }
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    // ---- reserve room in the row's union and copy the candidates there (coalesced)
+    if (tid == 0) {
         const int n = sm.n;
-        P.ccount[(size_t)row_id * P.CT + chunk] = nonfinite ? -2 : ((too_many || n > P.cap_w) ? -1 : n);
+        int base = -1;
+        if (nonfinite) atomicOr(P.uflags + row_id, 1);
+        else if (too_many || n > CAP_C) atomicOr(P.uflags + row_id, 2);
+        else if (n > 0) {
+            base = atomicAdd(P.ucount + row_id, n);
+            if (base + n > P.cap_u) { atomicOr(P.uflags + row_id, 2); base = -1; }
+        }
+        sm.base = base;
+    }
+    __syncthreads();
+    if (sm.base >= 0) {
+        TopkEntry* dst = P.ulist + (size_t)row_id * P.cap_u + sm.base;
+        for (int i = tid; i < sm.n; i += NT) dst[i] = sm.cand[i];
     }
     if (!arrive_last(&P.row_ctr[row_id], (unsigned)P.CT, &sm.flag)) return;
+    if (warp != 0) return;
 
-    // ==== last CTA of the row: exact threshold over the union of the chunk lists
-    int bad = 0, over = 0, n_my = 0;
-    for (int c = threadIdx.x; c < P.CT; c += NT) {
-        const int n = __ldcg(P.ccount + (size_t)row_id * P.CT + c);
-        if (n == -2) bad = 1;
-        else if (n < 0) over = 1;
-        else n_my += n;
-    }
-    bad = __syncthreads_or(bad);
-    over = __syncthreads_or(over);
-    const int utotal = block_sum_int(n_my, sm.red);
-    RowStats st;
-    st.M = NEG_INF; st.MC = NEG_INF; st.S = 0.0; st.thr = NEG_INF;
-    st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
-    if (bad) {
-        st.status = ROW_NONFINITE;
-    } else if (over || utotal > CAP_U) {
-        st.dense = 1;
-    } else {
-        // gather the union (chunk order)
-        {
-            int base = 0;
-            for (int c = 0; c < P.CT; ++c) {
-                const int n = __ldcg(P.ccount + (size_t)row_id * P.CT + c);
-                const TopkEntry* src = P.clist + ((size_t)row_id * P.CT + c) * P.cap_w;
-                for (int i = threadIdx.x; i < n; i += NT) {
-                    TopkEntry en;
-                    en.x = __ldcg(&src[i].x);
-                    en.idx = __ldcg(&src[i].idx);
-                    sm.cand[base + i] = en;
-                }
-                base += n;
-            }
-        }
-        __syncthreads();
-        const uint32_t gkey = (utotal >= k) ? block_kth_key<DT>(sm.cand, utotal, k, sm.red) : okey(NEG_INF);
-        const float g = key_value(gkey);
-        // keep entries >= g (stable order is not needed: they are sorted by index next)
-        if (threadIdx.x == 0) sm.n = 0;
-        __syncthreads();
-        for (int i = threadIdx.x; i < utotal; i += NT) {
-            const TopkEntry en = sm.cand[i];
-            if (okey(en.x) >= gkey) sm.kept[atomicAdd(&sm.n, 1)] = en;
-        }
-        __syncthreads();
-        const int nk = sm.n;
-        if (nk > P.cap_k) {
-            st.dense = 1;
-        } else {
-            block_sort_by_index(sm.kept, nk);
-            float mx = NEG_INF;
-            for (int i = threadIdx.x; i < nk; i += NT) mx = fmaxf(mx, sm.kept[i].x);
-            const float M = block_max(mx, sm.redf);
-            const float MC = M * P.c;
-            double S = 0.0;
-            if (threadIdx.x < 32) {
-                double acc = 0.0;
-                if (M != NEG_INF)
-                    for (int i = threadIdx.x; i < nk; i += 32) acc += (double)ex2(fmaf(sm.kept[i].x, P.c, -MC));
-                S = warp_sum(acc);
-            }
-            TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
-            for (int i = threadIdx.x; i < nk; i += NT) kl[i] = sm.kept[i];
-            st.M = M;
-            st.MC = MC;
-            st.S = S;
-            st.thr = g;
-            st.klist_n = nk;
-            st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
-        }
-    }
-    if (threadIdx.x == 0) P.rstats[row_id] = st;
-    if (!arrive_last(&P.req_ctr[b], (unsigned)P.R, &sm.flag)) return;
+    // ==== one warp of the last CTA of the row
+    const RowStats st = topk_row_epilogue<DT>(P, sm, row_id);
+    if (lane == 0) P.rstats[row_id] = st;
+    if (!warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) return;
 
-    // ==== last row of the request
+    // ==== the same warp, last row of the request
     int nd = 0;
-    for (int rr = threadIdx.x; rr < P.R; rr += NT) nd += __ldcg(&P.rstats[(size_t)b * P.R + rr].dense);
-    nd = block_sum_int(nd, sm.red);
+    for (int rr = lane; rr < P.R; rr += 32) nd += __ldcg(&P.rstats[(size_t)b * P.R + rr].dense);
+    nd = __reduce_add_sync(0xffffffffu, nd);
     if (nd > 0) {  // finished by topk_dense_kernel
-        if (threadIdx.x == 0) P.ndense[b] = nd;
+        if (lane == 0) P.ndense[b] = nd;
         return;
     }
-    __shared__ Plan sh_plan;
-    if (threadIdx.x < 32) {
-        const Plan p0 = compute_plan_warp<DT>(P, b, true);
-        if (threadIdx.x == 0) sh_plan = p0;
-    }
-    __syncthreads();
-    const Plan pl = sh_plan;
-    if (pl.status != ROW_OK) {
-        emit_spec(P, b, pl.status, 0, -1);
-        return;
-    }
-    // residual over the kept list of the p row (index order); r vanishes outside K_p
-    const RowStats sp = ld_rowstats(P.rstats + (size_t)b * P.R + pl.rp);
-    const int nk = sp.klist_n;
-    const TopkEntry* kl = P.klist + ((size_t)b * P.R + pl.rp) * P.cap_k;
-    const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
-    for (int i = threadIdx.x; i < nk; i += NT) {
-        const float xp = __ldcg(&kl[i].x);
-        const int v = __ldcg(&kl[i].idx);
-        float pp = __fmul_rn(ex2(fmaf(xp, P.c, -pl.MCp)), pl.invSp);
-        float res = pp;
-        if (rowq) {
-            const float xq = load_logit(rowq, DT, v);
-            const float qq = (xq >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq, P.c, -pl.MCq)), pl.invSq) : 0.f;
-            res = fmaxf(__fsub_rn(pp, qq), 0.f);
-        }
-        sm.rr[i] = (double)res;
-        sm.kept[i].idx = v;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double Z = 0.0;
-        for (int i = 0; i < nk; ++i) Z += sm.rr[i];
-        int tok = -1;
-        if (Z > 0.0 && isfinite(Z)) {
-            const double t = pl.u * Z;
-            double C = 0.0;
-            int lastpos = -1;
-            for (int i = 0; i < nk; ++i) {
-                if (sm.rr[i] > 0.0) lastpos = i;
-                C += sm.rr[i];
-                if (t < C && sm.rr[i] > 0.0) { tok = sm.kept[i].idx; break; }
-            }
-            if (tok < 0 && lastpos >= 0) tok = sm.kept[lastpos].idx;
-        }
-        sm.n = tok;
-    }
-    __syncthreads();
-    const int tok = sm.n;
-    emit_spec(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
+    topk_request_epilogue<DT>(P, sm, b);
 }
 
 // ---------------------------------------------------------------- exact fallback for dense rows
