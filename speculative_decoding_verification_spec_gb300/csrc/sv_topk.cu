@@ -76,6 +76,19 @@ __device__ __forceinline__ int slot_elem(int cbase, int s)
     else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
 }
 
+// w[base + j] for a run-time j in [0, 8) and a compile-time base, by a select tree (no local memory)
+template <int N>
+__device__ __forceinline__ uint32_t select8(const uint32_t (&w)[N], int base, int j)
+{
+    const uint32_t a0 = (j & 1) ? w[base + 1] : w[base];
+    const uint32_t a1 = (j & 1) ? w[base + 3] : w[base + 2];
+    const uint32_t a2 = (j & 1) ? w[base + 5] : w[base + 4];
+    const uint32_t a3 = (j & 1) ? w[base + 7] : w[base + 6];
+    const uint32_t c0 = (j & 2) ? a1 : a0;
+    const uint32_t c1 = (j & 2) ? a3 : a2;
+    return (j & 4) ? c1 : c0;
+}
+
 constexpr int CAP_C = 1024;  // candidates a chunk CTA collects on chip
 
 struct TopkSmem {
@@ -363,39 +376,44 @@ __global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
     const float tau = sm.tau;
     const int nonfinite = sm.nonfinite;
 
-    // ---- collect every element >= tau on chip (unordered; the row merge sorts)
+    // ---- collect every element >= tau on chip (unordered; the row merge sorts).  A group whose
+    // maximum passes tau yields a bitmask of its passing slots; only the set bits are visited.
     const bool too_many = (k > NT) && (cend - cbase > CAP_C);
     if (!nonfinite && !too_many) {
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
+            uint32_t bits = 0;
             if constexpr (DT == DT_BF16) {
                 const __nv_bfloat162 t2 = __floats2bfloat162_rn(tau, tau);
                 if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
                         const uint32_t wd = w[g * G + j];
-                        const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd), t2);
-                        if (msk & 0xffffu) {
-                            const int e = slot_elem<VEC>(cbase, 2 * (g * G + j));
-                            if (e < cend) cand_push(sm, bf16lo(wd), e);
-                        }
-                        if (msk >> 16) {
-                            const int e = slot_elem<VEC>(cbase, 2 * (g * G + j) + 1);
-                            if (e < cend) cand_push(sm, bf16hi(wd), e);
-                        }
+                        bits |= (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd), t2) & 0x00010001u) << j;
                     }
                 }
             } else {
                 if (__uint_as_float(gm[g]) >= tau) {
 #pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        const float x = __uint_as_float(w[g * G + j]);
-                        if (x >= tau) {
-                            const int e = slot_elem<VEC>(cbase, g * G + j);
-                            if (e < cend) cand_push(sm, x, e);
-                        }
-                    }
+                    for (int j = 0; j < G; ++j) bits |= (uint32_t)(__uint_as_float(w[g * G + j]) >= tau) << j;
                 }
+            }
+            while (bits) {
+                const int bp = __ffs(bits) - 1;
+                bits &= bits - 1;
+                const int j = bp & 15, half = bp >> 4;  // register j of the group, bf16 half
+                const uint32_t wd = select8(w, g * G, j);
+                float x;
+                int s;
+                if constexpr (DT == DT_BF16) {
+                    x = half ? bf16hi(wd) : bf16lo(wd);
+                    s = 2 * (g * G + j) + half;
+                } else {
+                    x = __uint_as_float(wd);
+                    s = g * G + j;
+                }
+                const int e = slot_elem<VEC>(cbase, s);
+                if (e < cend) cand_push(sm, x, e);
             }
         }
     }
