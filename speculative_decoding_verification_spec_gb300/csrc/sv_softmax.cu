@@ -3,11 +3,11 @@
 //
 // Kernel 1 (row statistics): each lane keeps an online (max, sum of 2^(x*c - max*c)) pair -- the
 // online (m, l) merge over vocabulary blocks of M7.1 section 0x04J.  For rows of 16-byte vectors
-// one CTA takes a chunk of CHUNK_VECS vectors, all of it prefetched into shared memory by cp.async
-// before the first group is consumed; the CTA writes one partial.  The last CTA of a row merges its
-// partials (fp64, chunk order) and the last row of a request runs the acceptance scan
-// (sv_plan.cuh).  Completion is counted with atomics; nothing waits.  Rows that are not 16-byte
-// aligned use persistent warps with plain loads instead.
+// one CTA takes a contiguous chunk of CHUNK_VECS vectors, loaded straight into registers, and each
+// warp writes one partial.  The last CTA of a row merges the row's partials (fp64, chunk order) and
+// the last row of a request runs the acceptance scan (sv_plan.cuh).  Completion is counted with
+// atomics; nothing waits.  Rows that are not 16-byte aligned use persistent warps with plain loads
+// instead.
 //
 // Kernel 2 (residual draw): r = max(p - q, 0) (M7.1 section 0x03C; p alone for the bonus, 0x03H)
 // over the selected row pair, summed per segment of 32 vectors; the last CTA of a request scans the
