@@ -55,7 +55,9 @@ typedef enum {
     SPEC_OK = 0,
     SPEC_ERR_INVALID_ARG = 1, /* a size, temperature, top_k or pointer failed host validation */
     SPEC_ERR_CUDA = 2,        /* a CUDA launch, memset or attribute call failed */
-    SPEC_ERR_WORKSPACE = 3    /* workspace missing, misaligned or smaller than required */
+    SPEC_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or smaller than required */
+    SPEC_ERR_TOO_LARGE = 4    /* spec_verify_noalloc: the sizes need more scratch than its fixed
+                                 device array holds (SPEC_NOALLOC_SCRATCH_BYTES) */
 } spec_status;
 
 /* Per-request status codes written to row_status[b]. */
@@ -150,6 +152,40 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype,
                                int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
                                int32_t* row_status, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/*
+ * spec_verify for callers that cannot allocate device memory.  The paper has no counterpart: this
+ * call only changes where spec_verify's scratch lives.
+ *
+ * Some callers may not call cudaMalloc at all -- a host that hands the library only pre-placed
+ * buffers, code running under an allocator that forbids new device allocations, or a caller
+ * that must not grow its memory footprint after start-up -- and so cannot provide the
+ * `workspace` that spec_verify needs.  This call takes the same inputs and outputs as
+ * spec_verify (device pointers owned by the caller) and runs the same kernels, but keeps the
+ * scratch in a fixed array of SPEC_NOALLOC_SCRATCH_BYTES bytes inside the library, one per GPU,
+ * held from the moment the library's code is loaded on that GPU until the process exits.
+ *
+ *   - Work runs on the calling thread's current device.  The first call on a device looks up
+ *     the array's device address there (cudaGetSymbolAddress, which may load the library's code
+ *     onto that device); make that first call before any stream capture on the device.
+ *   - Sizes whose spec_workspace_bytes(B, gamma, V, 0, 0) exceeds SPEC_NOALLOC_SCRATCH_BYTES
+ *     are rejected with SPEC_ERR_TOO_LARGE before anything is enqueued; other invalid
+ *     arguments give the same status as spec_verify.
+ *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Every call on a device shares that device's array, and the array keeps the previous
+ *     call's contents.  Each call clears the counters it relies on before its kernels run, so
+ *     stale contents are harmless, but calls that overlap on the GPU (different streams without
+ *     ordering between them, or several host threads) race on the array and give wrong results.
+ *     Issue them on one stream, or order them.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+spec_status spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                                spec_dtype dtype, const int32_t* draft_tokens,
+                                const float* uniforms, int B, int gamma, int V, float temperature,
+                                int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                                float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                                void* stream);
 
 /* Static description of a call-level status code. */
 const char* spec_status_string(spec_status s);

@@ -6,10 +6,12 @@ no CPU fallback.
 """
 from .binding import (  # noqa: F401
     EXPORTS,
+    NOALLOC_SCRATCH_BYTES,
     SpecVerifyError,
     Workspace,
     load,
     spec_verify,
+    spec_verify_noalloc,
     spec_verify_topk,
     tree_verify_greedy,
     workspace_bytes,

@@ -19,7 +19,11 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM = 5, 6, 7
 
 # every symbol the header declares
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
-           "spec_status_string")
+           "spec_verify_noalloc", "spec_status_string")
+
+# fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
+NOALLOC_SCRATCH_BYTES = 8 << 20
+SPEC_ERR_TOO_LARGE = 4
 
 _lib = None
 
@@ -47,6 +51,8 @@ def load(path: str | None = None):
     lib.spec_verify_topk.restype = I
     lib.tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
     lib.tree_verify_greedy.restype = I
+    lib.spec_verify_noalloc.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P]
+    lib.spec_verify_noalloc.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -146,6 +152,40 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, to
         rc = lib.spec_verify_topk(*common, int(top_k), *tail)
     else:
         rc = lib.spec_verify(*common, *tail)
+    _check(rc)
+    return out
+
+
+def spec_verify_noalloc(target, draft, draft_tokens, uniforms, temperature: float, *,
+                        aux: bool = False, out=None, stream=None):
+    """spec_verify through the entry point that allocates no device scratch.
+
+    For callers that cannot allocate device memory: the library keeps the scratch in a fixed
+    per-GPU array of NOALLOC_SCRATCH_BYTES, shared by every call on that GPU, so calls must not
+    overlap on the GPU.  Pass ``out`` (preallocated CUDA tensors, same keys as spec_verify's
+    result) to keep this wrapper itself from allocating.  Sizes that need more scratch than the
+    array holds raise SpecVerifyError.
+    """
+    lib = load()
+    _need_cuda(target, draft, draft_tokens, uniforms)
+    B, g1, V = target.shape
+    gamma = g1 - 1
+    dev = target.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, gamma + 1, dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+        if aux:
+            out["lse_p"] = torch.empty(B, gamma + 1, dtype=torch.float32, device=dev)
+            out["lse_q"] = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+            out["accept"] = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+    rc = lib.spec_verify_noalloc(
+        _ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tokens), _ptr(uniforms),
+        B, gamma, V, float(temperature), _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
+        _ptr(out.get("row_status")), _ptr(out.get("lse_p")), _ptr(out.get("lse_q")),
+        _ptr(out.get("accept")), _stream(stream))
     _check(rc)
     return out
 

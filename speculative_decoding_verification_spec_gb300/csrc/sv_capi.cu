@@ -347,6 +347,7 @@ const char* spec_status_string(spec_status s)
     case SPEC_ERR_INVALID_ARG: return "invalid argument";
     case SPEC_ERR_CUDA: return "CUDA launch error";
     case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPEC_ERR_TOO_LARGE: return "sizes need more scratch than the no-allocation entry point holds";
     }
     return "unknown status";
 }

@@ -93,6 +93,12 @@ def test_host_validation_without_gpu(lib):
     assert lib.tree_verify_greedy(fake, 1, fake, fake, 2, 4, 10, 5, fake, fake, None, None, ws,
                                   64, None) == WORKSPACE
     assert lib.spec_status_string(0) == b"ok"
+    # the no-allocation entry point refuses oversized or invalid sizes before any CUDA call
+    TOO_LARGE = 4
+    assert lib.spec_verify_noalloc(fake, fake, 1, fake, fake, 1024, 7, 152064, 1.0, fake, fake,
+                                   None, None, None, None, None) == TOO_LARGE
+    assert lib.spec_verify_noalloc(fake, fake, 1, fake, fake, 2, 3, 0, 1.0, fake, fake,
+                                   None, None, None, None, None) == INVALID
 
 
 def test_no_cpu_fallback_in_the_binding():
