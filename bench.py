@@ -42,16 +42,16 @@ DOMINANT = ("c4", "topk_stats_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.
 
 # ------------------------------------------------------------------ workloads
 
-def workload_batches(names, rank):
+def workload_batches(names, rank, requests=None):
     from speculative_decoding_verification_spec_gb300 import synth as S
     out = {}
     for n in names:
-        if n in S.CONFIGS:
-            cfg = S.CONFIGS[n]
-            out[n] = S.make_spec_batch(S.scaled(cfg, seed=cfg.seed + 7919 * rank))
-        else:
-            cfg = S.TREE_CONFIGS[n]
-            out[n] = S.make_tree_batch(S.scaled(cfg, seed=cfg.seed + 7919 * rank))
+        cfg = S.CONFIGS[n] if n in S.CONFIGS else S.TREE_CONFIGS[n]
+        kw = dict(seed=cfg.seed + 7919 * rank)
+        if requests:
+            kw["B"] = requests
+        cfg = S.scaled(cfg, **kw)
+        out[n] = S.make_spec_batch(cfg) if n in S.CONFIGS else S.make_tree_batch(cfg)
     return out
 
 
@@ -206,7 +206,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     names = SUITE if args.workload == "suite" else (args.workload,)
-    batches = workload_batches(names, rank)
+    batches = workload_batches(names, rank, args.requests)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
 
@@ -353,7 +353,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": describe(names), "input_dtype": "bf16",
                    "logit_rows_per_step": rows_step, "logit_bytes_per_step": bytes_step,
                    "l2": f"inputs larger than L2 ({bytes_step / 1e6:.0f} MB per step > 129 MB); no flush",
-                   "parallelism": f"replicas x{world} (independent requests per rank)"},
+                   "parallelism": f"replicas x{world} (independent requests per rank)",
+                   **({"requests_override": args.requests} if args.requests else {})},
         "hbm_gbs": bytes_step * world * args.steps / elapsed / 1e9,
         "per_config": per_cfg,
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "workload": dom_cfg,
@@ -427,6 +428,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--requests", type=int, default=None,
+                    help="profiling aid: run the selected workload with this many requests instead "
+                         "of its own B (the line's config records it; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

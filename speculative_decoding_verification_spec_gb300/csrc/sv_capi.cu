@@ -42,25 +42,44 @@ static long long nsegs(const Shape& s) { return std::max(1LL, cdiv(s.nvec, SEGV)
 // L2 budget for the row pairs most likely to be corrected (read evict_last by the stats kernel)
 constexpr double PIN_BYTES = 80e6;
 
-static int topk_ept(int dtype) { return dtype == DT_BF16 ? 80 : 40; }
-static int topk_cap(int k) { return (int)std::min(2048LL, (2 * (long long)k + 64 + 31) / 32 * 32); }
-// per-row union capacity: CT chunks of up to topk_cap(k) candidates each, at most 2048
-static int topk_ucap(int CT, int k) { return (int)std::min(2048LL, (long long)CT * topk_cap(k)); }
+// top-k chunks are 32 KB of one row: 16384 bf16 or 8192 fp32 elements
+static long long topk_chunk_elems(int dtype) { return dtype == DT_BF16 ? 16384 : 8192; }
+static int topk_chunks(int dtype, int V) { return (int)cdiv(V, topk_chunk_elems(dtype)); }
+// Segments per row: a row is split into up to 4 runs of chunks so that the streaming kernel's
+// ~2 CTAs per SM have at least a dozen segments each (load balance at small B).
+constexpr int TK_MAX_SEGR = 4;
+static int topk_segments(long long rows, int CT, int sms)
+{
+    const long long want = cdiv(24LL * sms, std::max(1LL, rows));
+    const int ns = (int)std::max(1LL, std::min<long long>(want, std::min(TK_MAX_SEGR, CT)));
+    const int sps = (int)cdiv(CT, ns);
+    return (int)cdiv(CT, sps);
+}
+// Rows with k > NT take the dense path, so capacities are sized for min(k, NT).
+// per-chunk candidate slot: 2k + 64 entries
+static int topk_slot_cap(int k) { return (int)((2LL * std::min(k, NT) + 64 + 31) / 32 * 32); }
+// per-row kept list: the same, rounded up to a power of two (the on-chip sort pads to one)
+static int topk_kept_cap(int k)
+{
+    int c = 1;
+    while (c < topk_slot_cap(k)) c <<= 1;
+    return c;
+}
 
 // --------------------------------------------------------------------------- workspace layout
 
 struct SpecLayout {
     size_t ctr_bytes = 0, bytes = 0;
     size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0, o_work = 0;
-    size_t o_ucount = 0, o_uflags = 0;
     size_t o_partials = 0, o_rstats = 0, o_plan = 0, o_segs = 0;
-    size_t o_ulist = 0, o_klist = 0;
+    size_t o_clist = 0, o_ccount = 0, o_klist = 0;
 };
 
 // Byte layout for `ppr` softmax partials per row, nseg residual segments per request and (top-k)
-// per-row unions of `cap_u` and kept lists of `cap_k` entries.  All counters sit at the front so
-// one memset clears them.
-static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool topk, int cap_u, int cap_k)
+// (top-k) `nsegr` segment lists of `cap_s` candidates per row and kept lists of `cap_k` entries.
+// All counters sit at the front so one memset clears them.
+static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool topk, int nsegr,
+                              int cap_s, int cap_k)
 {
     SpecLayout L;
     size_t o = 0;
@@ -70,10 +89,6 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_dense_ctr = o; o += (size_t)B * sizeof(unsigned);
     L.o_ndense = o; o += (size_t)B * sizeof(int);
     L.o_work = o; o += 2 * sizeof(unsigned);
-    if (topk) {
-        L.o_ucount = o; o += (size_t)B * R * sizeof(int);
-        L.o_uflags = o; o += (size_t)B * R * sizeof(int);
-    }
     L.ctr_bytes = o;
     o = align_up(o);
     L.o_partials = o; o = align_up(o + (size_t)B * R * ppr * sizeof(Partial));
@@ -81,7 +96,8 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_plan = o; o = align_up(o + (size_t)B * sizeof(Plan));
     L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
     if (topk) {
-        L.o_ulist = o; o = align_up(o + (size_t)B * R * cap_u * sizeof(TopkEntry));
+        L.o_clist = o; o = align_up(o + (size_t)B * R * nsegr * cap_s * sizeof(TopkEntry));
+        L.o_ccount = o; o = align_up(o + (size_t)B * R * nsegr * sizeof(int));
         L.o_klist = o; o = align_up(o + (size_t)B * R * cap_k * sizeof(TopkEntry));
     }
     L.bytes = o;
@@ -191,11 +207,13 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.tasks2 = (long long)B * P.S2;
     P.pin_pairs = (int)std::min(2.0, std::floor(PIN_BYTES / ((double)B * 2.0 * (double)V * (double)es)));
     if (topk) {
-        P.CT = (int)cdiv(V, (long long)NT * topk_ept(dt));
-        P.cap_k = topk_cap(top_k);
-        P.cap_u = topk_ucap(P.CT, top_k);
+        P.CT = topk_chunks(dt, V);
+        P.nsegr = topk_segments((long long)B * R, P.CT, sms);
+        P.sps = (int)cdiv(P.CT, P.nsegr);
+        P.cap_s = topk_slot_cap(top_k);
+        P.cap_k = topk_kept_cap(top_k);
     }
-    const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.cap_u, P.cap_k);
+    const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.nsegr, P.cap_s, P.cap_k);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
     if ((long long)B * R * (topk ? P.CT : 1) >= (1LL << 31) || P.tasks1 >= (1LL << 31))
         return SPEC_ERR_INVALID_ARG;
@@ -218,9 +236,8 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.plan = reinterpret_cast<Plan*>(ws + L.o_plan);
     P.segs = reinterpret_cast<float*>(ws + L.o_segs);
     if (topk) {
-        P.ulist = reinterpret_cast<TopkEntry*>(ws + L.o_ulist);
-        P.ucount = reinterpret_cast<int*>(ws + L.o_ucount);
-        P.uflags = reinterpret_cast<int*>(ws + L.o_uflags);
+        P.clist = reinterpret_cast<TopkEntry*>(ws + L.o_clist);
+        P.ccount = reinterpret_cast<int*>(ws + L.o_ccount);
         P.klist = reinterpret_cast<TopkEntry*>(ws + L.o_klist);
     }
 
@@ -230,8 +247,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     if (!topk) {
         err = launch_softmax_path(P, sms, st);
     } else {
-        const unsigned g1 = (unsigned)((long long)B * R * P.CT), g2 = (unsigned)((long long)B * R);
-        err = launch_topk_path(P, g1, g2, st);
+        err = launch_topk_path(P, sms, st);
     }
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -252,10 +268,11 @@ size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
             best = std::max(best, tree_layout(B, tree_nodes, slices1(sh)).bytes);
         } else {
             const bool topk = top_k > 0 && top_k < V;
-            int CT = 0;
-            if (topk) CT = (int)cdiv(V, (long long)NT * std::min(topk_ept(DT_BF16), topk_ept(DT_F32)));
+            const int CT = topk ? std::max(topk_chunks(DT_BF16, V), topk_chunks(DT_F32, V)) : 0;
             const SpecLayout L = spec_layout(B, 2 * gamma + 1, partials_per_row(sh), nsegs(sh), topk,
-                                             topk ? topk_ucap(CT, top_k) : 0, topk ? topk_cap(top_k) : 0);
+                                             std::min(TK_MAX_SEGR, std::max(CT, 1)),
+                                             topk ? topk_slot_cap(top_k) : 0,
+                                             topk ? topk_kept_cap(top_k) : 0);
             best = std::max(best, L.bytes);
         }
     }

@@ -27,6 +27,7 @@ enum {
     ROW_NONFINITE = 1,
     ROW_DEGENERATE = 2,
     ROW_BAD_TOKEN = 3,
+    ROW_TIMEOUT = 4,
     ROW_BAD_PARENT = 5,
     ROW_OVERFLOW = 6,
     ROW_BAD_UNIFORM = 7
@@ -94,9 +95,10 @@ struct SpecParams {
     int S1, S2, nseg;
     long long tasks1, tasks2;
     // top-k chunking and capacities
-    int CT;
+    int CT;               // 32 KB chunks per row
+    int nsegr, sps;       // segments per row (<= 4) and chunks per segment
+    int cap_s;            // per-segment candidate list capacity (entries)
     int cap_k;            // per-row kept-list capacity
-    int cap_u;            // per-row union capacity (entries)
     // outputs
     int32_t* accepted_len;
     int32_t* out_tokens;
@@ -113,9 +115,8 @@ struct SpecParams {
     unsigned* req_ctr;    // [B]
     unsigned* res_ctr;    // [B]
     unsigned* work;       // [2] task counters of the two streaming kernels
-    TopkEntry* ulist;     // [B*R*cap_u] per-row union of the chunks' candidates (unordered)
-    int* ucount;          // [B*R] entries reserved in ulist
-    int* uflags;          // [B*R] 1 = non-finite row, 2 = candidates overflowed (dense row)
+    TopkEntry* clist;     // [B*R*nsegr*cap_s] each segment's entries >= its k-th largest (unordered)
+    int* ccount;          // [B*R*nsegr] entries listed, or TK_NONFINITE / TK_OVERFLOW / TK_TIMEOUT
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
     unsigned* dense_ctr;  // [B]
     int* ndense;          // [B]
@@ -304,6 +305,50 @@ __device__ __forceinline__ uint4 lds128(const uint4* p)
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a) : "memory");
     return r;
+}
+
+// ---------------------------------------------------------------- bulk copies (TMA engine)
+//
+// One thread arms an mbarrier with the byte count and issues cp.async.bulk global -> shared; the
+// consumers poll the barrier's phase.  Every wait is bounded: after MBAR_SPIN_LIMIT polls it gives
+// up and reports failure, and the caller turns that into a status instead of hanging.
+
+constexpr int MBAR_SPIN_LIMIT = 1 << 22;
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+// makes barrier initialisation visible to the async proxy before the first copy uses it
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// orders this CTA's generic-proxy shared-memory accesses before later async-proxy (bulk copy) ones
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to shared memory,
+// completing on `bar`, with an L2 cache policy.  Called by one thread.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar,
+                                          uint64_t pol)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol) : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` of `bar` to complete; false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
+{
+    const unsigned a = smem_addr(bar);
+    for (int i = 0; i < MBAR_SPIN_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
 }
 
 // Chunk kernels: one CTA of NT threads per chunk of CHUNK_VECS vectors.  Thread t copies vectors
@@ -539,9 +584,8 @@ inline unsigned persistent_grid(long long tasks, int sms, int threads = NT, size
 
 // spec_stats_kernel + spec_resample_kernel for the dtype / vector width in P
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st);
-// topk_stats_kernel + topk_dense_kernel
-cudaError_t launch_topk_path(const SpecParams& P, unsigned grid_stats, unsigned grid_dense,
-                             cudaStream_t st);
+// topk_stream_kernel + topk_finish_kernel + topk_dense_kernel
+cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st);
 // tree_argmax_kernel
 cudaError_t launch_tree_path(const TreeParams& P, int sms, cudaStream_t st);
 

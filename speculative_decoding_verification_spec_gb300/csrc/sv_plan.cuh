@@ -69,10 +69,11 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
     const int g = P.gamma, R = P.R, lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
 
-    int bad = 0;
+    int bad = 0, tmo = 0;
     for (int r = lane; r < R; r += 32) {
         RowStats rs = ld_rowstats(P.rstats + (size_t)b * R + r);
         if (rs.status != ROW_OK) bad = 1;
+        if (rs.status == ROW_TIMEOUT) tmo = 1;
         const float lse = row_lse(rs, P.c, P.T);
         if (r <= g) {
             if (P.aux_lse_p) P.aux_lse_p[(size_t)b * (g + 1) + r] = lse;
@@ -81,6 +82,7 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
         }
     }
     const int nonfinite = __any_sync(FULL, bad);
+    const int timeout = __any_sync(FULL, tmo);
 
     // acceptance ratios at every position
     int badtok = 0;
@@ -116,7 +118,7 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
     badu = __any_sync(FULL, badu);
 
     Plan pl;
-    pl.status = nonfinite ? ROW_NONFINITE : badtok ? ROW_BAD_TOKEN : badu ? ROW_BAD_UNIFORM : ROW_OK;
+    pl.status = timeout ? ROW_TIMEOUT : nonfinite ? ROW_NONFINITE : badtok ? ROW_BAD_TOKEN : badu ? ROW_BAD_UNIFORM : ROW_OK;
     pl.A = __reduce_min_sync(FULL, rej_first);
     pl.rp = (pl.A < g) ? pl.A : g;
     pl.rq = (pl.A < g) ? g + 1 + pl.A : -1;

@@ -5,25 +5,41 @@
 // whose stored logit is >= the row's k-th largest stored logit (counted with multiplicity), so ties
 // at the threshold are all kept.
 //
-// Kernel 1 (topk_stats_kernel): one CTA per (row, contiguous chunk of NT*EPT elements), the chunk
-// held in registers.  A lower bound tau of the chunk's k-th largest value is the k-th largest of the
-// NT per-thread maxima (NT disjoint groups, so at least k chunk elements are >= tau), selected by
-// one warp; only elements >= tau -- a few dozen for k = 50 -- leave the registers: collected in
-// shared memory, then appended to the row's union buffer with one reservation per chunk.  Since the
-// row's k-th largest value g is >= every chunk's tau, the union holds every element >= g.  One warp of the last CTA of the row selects g exactly from
-// the union, keeps the entries >= g sorted by index and forms (M, S) over them; one warp of the last
-// row of a request runs the acceptance scan and draws the correction / bonus token directly from
-// the kept list: the residual vanishes outside K_p, so no second pass over V is needed.
+// Kernel 1 (topk_stream_kernel) streams every logit row once.  Rows are cut into 32 KB chunks and
+// runs of chunks (segments, at most 4 per row); persistent CTAs take segments round-robin and, for
+// 16-byte aligned rows, fetch their chunks with bulk copies (TMA engine) into a ring of TK_STAGES
+// shared-memory stages, so the next chunks are in flight while one is filtered.  Each thread holds
+// its 64 (bf16) or 32 (fp32) elements of a chunk in registers.  The k-th largest of the NT
+// per-thread maxima (NT disjoint groups, so at least k chunk elements are >= it) bounds the chunk's
+// k-th largest value from below; every warp selects it from shared memory by itself, so no warp
+// waits for another.  With the bound carried over from the segment's earlier chunks it forms beta,
+// and only elements >= beta -- a few dozen per chunk at k = 50 -- join the segment's candidate set
+// in shared memory.  When the set grows large, and at the end of the segment, one warp cuts it to
+// the entries >= its exact k-th largest value, which becomes the new bound; the segment's list is
+// what remains.  Every bound is <= the row's k-th largest value g, so the lists hold every
+// element >= g.
+//
+// Kernel 2 (topk_finish_kernel), one CTA per request: one warp per row selects g exactly from the
+// union of the row's segment lists, keeps the entries >= g sorted by index and forms the
+// normaliser (M, S).  Then one warp runs the acceptance scan and draws the correction or bonus
+// token directly from the kept list of the p row: the residual vanishes outside K_p, so no second
+// pass over V is needed.
 //
 // Rows whose candidates overflow the capacities (massive ties, k > NT, ...) are marked dense and
-// finished exactly by kernel 2 (topk_dense_kernel) with full-row passes.
+// finished exactly by kernel 3 (topk_dense_kernel) with full-row passes.
 #include <cuda_bf16.h>
 
 #include "sv_plan.cuh"
 
 namespace sv {
 
-constexpr int CAP_U = 2048;  // union entries the row epilogue holds on chip
+constexpr int TK_CHUNK_BYTES = 32768;                 // bytes of one row per chunk
+constexpr int TK_NREG = TK_CHUNK_BYTES / (NT * 4);    // 32-bit words per thread (32)
+constexpr int TK_NV = TK_NREG / 4;                    // 16-byte vectors per thread (8)
+constexpr int TK_STAGES = 3;                          // bulk-copy ring depth
+constexpr int TK_SMEM = TK_STAGES * TK_CHUNK_BYTES;   // dynamic shared memory of kernel 1
+// per-chunk candidate count codes
+constexpr int TK_OVERFLOW = -1, TK_NONFINITE = -2, TK_TIMEOUT = -3;
 
 // order-preserving 32-bit key of a float; -0 and +0 map to the same key
 __device__ __forceinline__ uint32_t okey(float x)
@@ -62,20 +78,6 @@ __device__ uint32_t warp_kth_key(int n, int k, KeyAt key_at)
     return prefix;
 }
 
-// elements per thread held in registers, per dtype
-template <int DT> struct TopkShape;
-template <> struct TopkShape<DT_BF16> { static constexpr int EPT = 80, NREG = 40; };
-template <> struct TopkShape<DT_F32> { static constexpr int EPT = 40, NREG = 40; };
-
-// element index (within the row) of register slot s of this thread: vector j = s / VEC, element
-// e = s % VEC of it; vectors of a thread are NT apart
-template <int VEC>
-__device__ __forceinline__ int slot_elem(int cbase, int s)
-{
-    if constexpr (VEC == 1) return cbase + s * NT + (int)threadIdx.x;
-    else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
-}
-
 // w[base + j] for a run-time j in [0, 8) and a compile-time base, by a select tree (no local memory)
 template <int N>
 __device__ __forceinline__ uint32_t select8(const uint32_t (&w)[N], int base, int j)
@@ -87,30 +89,6 @@ __device__ __forceinline__ uint32_t select8(const uint32_t (&w)[N], int base, in
     const uint32_t c0 = (j & 2) ? a1 : a0;
     const uint32_t c1 = (j & 2) ? a3 : a2;
     return (j & 4) ? c1 : c0;
-}
-
-constexpr int CAP_C = 1024;  // candidates a chunk CTA collects on chip
-
-struct TopkSmem {
-    union {
-        TopkEntry cand[CAP_C];  // chunk phase: this chunk's candidates
-        TopkEntry u[CAP_U];     // row epilogue: union of the chunks' candidates
-        double rr[CAP_U];       // request epilogue: residual mass of the kept list
-    };
-    TopkEntry kept[CAP_U];
-    float tmax[NT];
-    float tau;
-    int n, base, flag, nonfinite;
-};
-
-// append one candidate to the chunk's on-chip list (the slot beyond CAP_C only counts)
-__device__ __forceinline__ void cand_push(TopkSmem& sm, float x, int e)
-{
-    const int pos = atomicAdd(&sm.n, 1);
-    if (pos < CAP_C) {
-        sm.cand[pos].x = x;
-        sm.cand[pos].idx = e;
-    }
 }
 
 // Warp-level bitonic sort of e[0..n) by index (ascending), padding to a power of two.
@@ -136,68 +114,10 @@ __device__ void warp_sort_by_index(TopkEntry* e, int n)
     }
 }
 
-// One warp of the last CTA of a row: exact threshold over the union of the chunk lists, kept list
-// sorted by index, normaliser over it.  Returns the row's stats.
-template <int DT>
-__device__ RowStats topk_row_epilogue(const SpecParams& P, TopkSmem& sm, int row_id)
-{
-    const int lane = threadIdx.x & 31;
-    const unsigned FULL = 0xffffffffu;
-    RowStats st;
-    st.M = NEG_INF; st.MC = NEG_INF; st.S = 0.0; st.thr = NEG_INF;
-    st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
-    const int flags = __ldcg(P.uflags + row_id);
-    const int total = __ldcg(P.ucount + row_id);
-    if (flags & 1) { st.status = ROW_NONFINITE; return st; }
-    if ((flags & 2) || total > P.cap_u) { st.dense = 1; return st; }
-    // the union, contiguous: independent loads, several in flight per lane
-    const TopkEntry* src = P.ulist + (size_t)row_id * P.cap_u;
-#pragma unroll 8
-    for (int i = lane; i < total; i += 32) {
-        TopkEntry en;
-        en.x = __ldcg(&src[i].x);
-        en.idx = __ldcg(&src[i].idx);
-        sm.u[i] = en;
-    }
-    __syncwarp();
-    const int k = P.top_k;
-    const uint32_t gkey = (total >= k) ? warp_kth_key<DT>(total, k, [&](int i) { return okey(sm.u[i].x); })
-                                       : okey(NEG_INF);
-    // stable ballot compaction of the entries >= g
-    int nk = 0;
-    for (int i0 = 0; i0 < total; i0 += 32) {
-        const int i = i0 + lane;
-        const bool keep = i < total && okey(sm.u[i].x) >= gkey;
-        const unsigned bal = __ballot_sync(FULL, keep);
-        if (keep) sm.kept[nk + __popc(bal & ((1u << lane) - 1u))] = sm.u[i];
-        nk += __popc(bal);
-    }
-    __syncwarp();
-    if (nk > P.cap_k) { st.dense = 1; return st; }
-    warp_sort_by_index(sm.kept, nk);
-    float mx = NEG_INF;
-    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, sm.kept[i].x);
-    const float M = warp_max(mx);
-    const float MC = M * P.c;
-    double acc = 0.0;
-    if (M != NEG_INF)
-        for (int i = lane; i < nk; i += 32) acc += (double)ex2(fmaf(sm.kept[i].x, P.c, -MC));
-    const double S = warp_sum(acc);
-    TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
-    for (int i = lane; i < nk; i += 32) kl[i] = sm.kept[i];
-    st.M = M;
-    st.MC = MC;
-    st.S = S;
-    st.thr = key_value(gkey);
-    st.klist_n = nk;
-    st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
-    return st;
-}
-
 // One warp: acceptance scan of request b and the correction / bonus draw from the kept list of
 // the p row (index order); the residual is zero outside K_p.
 template <int DT>
-__device__ void topk_request_epilogue(const SpecParams& P, TopkSmem& sm, int b)
+__device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
@@ -224,7 +144,7 @@ __device__ void topk_request_epilogue(const SpecParams& P, TopkSmem& sm, int b)
             const float qq = (xq >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq, P.c, -pl.MCq)), pl.invSq) : 0.f;
             res = fmaxf(__fsub_rn(pp, qq), 0.f);
         }
-        sm.rr[i] = (double)res;
+        rr[i] = (double)res;
         mine += (double)res;
     }
     const double incl = warp_incl_scan(mine);
@@ -243,9 +163,9 @@ __device__ void topk_request_epilogue(const SpecParams& P, TopkSmem& sm, int b)
                 double run = excl;
                 int lastpos = -1;
                 for (int i = i0; i < i1; ++i) {
-                    if (sm.rr[i] > 0.0) lastpos = i;
-                    run += sm.rr[i];
-                    if (t < run && sm.rr[i] > 0.0) { tok = __ldcg(&kl[i].idx); break; }
+                    if (rr[i] > 0.0) lastpos = i;
+                    run += rr[i];
+                    if (t < run && rr[i] > 0.0) { tok = __ldcg(&kl[i].idx); break; }
                 }
                 if (tok < 0 && lastpos >= 0) tok = __ldcg(&kl[lastpos].idx);
             }
@@ -255,195 +175,467 @@ __device__ void topk_request_epilogue(const SpecParams& P, TopkSmem& sm, int b)
     emit_spec_warp(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
 }
 
-template <int DT, int VEC>
-__global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
+
+// element index (within the row) of register slot s of this thread: vector j = s / VEC, element
+// e = s % VEC of it; vectors of a thread are NT apart
+template <int VEC>
+__device__ __forceinline__ int slot_elem(int cbase, int s)
 {
-    using Shape = TopkShape<DT>;
-    constexpr int EPT = Shape::EPT, NREG = Shape::NREG;
-    static_assert(sizeof(TopkSmem) <= 48 * 1024, "static shared memory");
-    __shared__ TopkSmem sm;
+    if constexpr (VEC == 1) return cbase + s * NT + (int)threadIdx.x;
+    else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
+}
+
+// Bits of a group's passing-slot mask (as built in topk_stream_kernel) whose elements lie before
+// cend.  Group g holds registers 8g..8g+7 of the thread: for bf16 bit j is the low half of register
+// 8g+j and bit 16+j its high half; for fp32 bit j is register 8g+j.
+template <int DT, int VEC>
+__device__ __forceinline__ uint32_t valid_bits(int cbase, int cend, int g)
+{
+    uint32_t m = 0;
+    constexpr int PER = (DT == DT_BF16) ? 2 : 1;  // elements per register
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+            if (slot_elem<VEC>(cbase, PER * (8 * g + j) + h) < cend) m |= 1u << (j + 16 * h);
+    return m;
+}
+
+// k-th largest key (as warp_kth_key) of e[0..n), n <= 32 * KPL, with the keys held in registers.
+template <int DT, int KPL>
+__device__ uint32_t warp_kth_key_regs(const TopkEntry* e, int n, int k)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t key[KPL];
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+        const int i = lane + 32 * j;
+        key[j] = i < n ? okey(e[i].x) : 0u;  // 0: below every key a value can have
+    }
+    uint32_t prefix = 0;
+    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+    for (int bit = 31; bit >= lo; --bit) {
+        const uint32_t want = prefix | (1u << bit);
+        unsigned cnt = 0;
+#pragma unroll
+        for (int j = 0; j < KPL; ++j) cnt += key[j] >= want;
+        if ((int)__reduce_add_sync(0xffffffffu, cnt) >= k) prefix = want;
+    }
+    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+    return prefix;
+}
+
+constexpr int TK_CAPC = 1024;  // on-chip candidate set of the segment being streamed
+
+// Kernel 1.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage ring; otherwise
+// element loads straight into registers.  A CTA takes segments (runs of up to P.sps chunks of one
+// row) round-robin and streams them chunk by chunk.
+template <int DT, bool BULK>
+__global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
+{
+    constexpr int NREG = TK_NREG;
+    constexpr int EPT = (DT == DT_BF16) ? 2 * NREG : NREG;  // elements per thread
+    constexpr int CHUNK = NT * EPT;                          // elements per chunk
+    constexpr int VEC = BULK ? ((DT == DT_BF16) ? 8 : 4) : 1;
+    constexpr int ES = (DT == DT_BF16) ? 2 : 4;
+    constexpr int G = 8, NG = NREG / G;
+    static_assert(NREG % G == 0, "register groups");
+    extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
+    __shared__ float tmax[NT];
+    __shared__ TopkEntry cset[TK_CAPC];
+    __shared__ int ncset;     // candidates in cset (may exceed TK_CAPC: then the segment overflowed)
+    __shared__ float sbeta;   // running lower bound of the segment's k-th largest value
+    __shared__ int sover;     // the segment's candidates overflowed
+    __shared__ int sbad[2];   // a NaN or +inf was seen in the chunk (double-buffered by parity)
+    __shared__ __align__(8) uint64_t full[TK_STAGES];
+
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int chunk = blockIdx.x % P.CT;
-    const int rs = blockIdx.x / P.CT;
-    const int b = rs / P.R, r = rs % P.R;
-    const int row_id = b * P.R + r;
-    const char* row = spec_row_ptr(P, b, r);
-    const int cbase = chunk * NT * EPT;
-    const int cend = min(cbase + NT * EPT, P.V);
+    const unsigned FULL = 0xffffffffu;
+    const long long nsegs = (long long)P.B * P.R * P.nsegr;
+    const long long G0 = gridDim.x;
     const int k = P.top_k;
     const uint64_t pol = policy_evict_first();
 
-    // ---- load the chunk into registers (-inf padding)
-    uint32_t w[NREG];
-    if constexpr (VEC > 1) {
-        constexpr int NV = EPT / VEC;  // vectors per thread
-        constexpr int ES = (DT == DT_BF16) ? 2 : 4;
-        const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-        const char* tp = row + ((size_t)cbase + (size_t)tid * VEC) * ES;  // this thread's first vector
-        if (cbase + NT * EPT <= cend) {  // full chunk: fixed offsets, no bounds checks
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                const uint4 q = ld_stream_v4_pol(tp + (size_t)j * NT * VEC * ES, pol);
-                w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                const int e0 = cbase + (j * NT + tid) * VEC;
-                const uint4 q = e0 < cend ? ld_stream_v4_pol(tp + (size_t)j * NT * VEC * ES, pol)
-                                          : make_uint4(pad, pad, pad, pad);
-                w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
-            }
-        }
-    } else if constexpr (DT == DT_BF16) {
-        const unsigned short* rp = reinterpret_cast<const unsigned short*>(row);
-#pragma unroll
-        for (int j = 0; j < NREG; ++j) {
-            const int e0 = slot_elem<1>(cbase, 2 * j), e1 = slot_elem<1>(cbase, 2 * j + 1);
-            const uint32_t lo = e0 < cend ? __ldg(rp + e0) : 0xff80u;
-            const uint32_t hi = e1 < cend ? __ldg(rp + e1) : 0xff80u;
-            w[j] = lo | (hi << 16);
-        }
-    } else {
-        const float* rp = reinterpret_cast<const float*>(row);
-#pragma unroll
-        for (int j = 0; j < NREG; ++j) {
-            const int e0 = slot_elem<1>(cbase, j);
-            w[j] = e0 < cend ? __float_as_uint(__ldg(rp + e0)) : 0xff800000u;
-        }
-    }
+    auto seg_stages = [&](long long sg) -> int {
+        const int si = (int)(sg % P.nsegr);
+        return min(P.sps, P.CT - si * P.sps);
+    };
+    // row and element range of chunk `st` of segment `sg`
+    auto chunk_of = [&](long long sg, int st, int& row_id, int& cbase, int& cend) {
+        row_id = (int)(sg / P.nsegr);
+        const int c = (int)(sg % P.nsegr) * P.sps + st;
+        cbase = c * CHUNK;
+        cend = min(cbase + CHUNK, P.V);
+    };
 
-    // ---- group maxima (G registers each) and the thread maximum, NaN-propagating
-    constexpr int G = 8, NG = NREG / G;
-    static_assert(NREG % G == 0, "register groups");
-    uint32_t gm[NG];
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-        uint32_t m = w[g * G];
-#pragma unroll
-        for (int j = 1; j < G; ++j) {
-            if constexpr (DT == DT_BF16) m = bmax2_nan(m, w[g * G + j]);
-            else m = __float_as_uint(fmax_nan_f(__uint_as_float(m), __uint_as_float(w[g * G + j])));
+    // producer cursor (thread 0): the next (segment, chunk) to fetch, in this CTA's consumption order
+    long long pseg = blockIdx.x;
+    int pst = 0;
+    long long nissued = 0;
+    auto issue_next = [&](int s) {
+        if (pseg >= nsegs) return;
+        int row_id, cbase, cend;
+        chunk_of(pseg, pst, row_id, cbase, cend);
+        const char* src = spec_row_ptr(P, row_id / P.R, row_id % P.R) + (size_t)cbase * ES;
+        bulk_load(ring + (size_t)s * NT * TK_NV, src, (unsigned)(cend - cbase) * ES, &full[s], pol);
+        ++nissued;
+        if (++pst == seg_stages(pseg)) {
+            pst = 0;
+            pseg += G0;
         }
-        gm[g] = m;
-    }
-    float tmax;
-    if constexpr (DT == DT_BF16) {
-        uint32_t pm = gm[0];
-#pragma unroll
-        for (int g = 1; g < NG; ++g) pm = bmax2_nan(pm, gm[g]);
-        tmax = fmax_nan_f(bf16lo(pm), bf16hi(pm));
-    } else {
-        tmax = __uint_as_float(gm[0]);
-#pragma unroll
-        for (int g = 1; g < NG; ++g) tmax = fmax_nan_f(tmax, __uint_as_float(gm[g]));
-    }
-    sm.tmax[tid] = tmax;
-    __syncthreads();
+    };
 
-    // ---- one warp: non-finite check and tau = k-th largest thread maximum (valid for k <= NT)
-    if (warp == 0) {
-        int bad = 0;
-        for (int i = lane; i < NT; i += 32) {
-            const float x = sm.tmax[i];
-            if (x != x || x == __int_as_float(0x7f800000)) bad = 1;
-        }
-        bad = __any_sync(0xffffffffu, bad);
-        uint32_t tk = okey(NEG_INF);
-        if (!bad && k <= NT) {
-            uint32_t keys[NT / 32];
-#pragma unroll
-            for (int i = 0; i < NT / 32; ++i) keys[i] = okey(sm.tmax[lane + 32 * i]);
-            uint32_t prefix = 0;
-            constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-            for (int bit = 31; bit >= lo; --bit) {
-                const uint32_t want = prefix | (1u << bit);
-                unsigned cnt = 0;
-#pragma unroll
-                for (int i = 0; i < NT / 32; ++i) cnt += keys[i] >= want;
-                if ((int)__reduce_add_sync(0xffffffffu, cnt) >= k) prefix = want;
-            }
-            if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-            tk = prefix;
-        }
-        if (lane == 0) {
-            sm.tau = key_value(tk);
-            sm.nonfinite = bad;
-            sm.n = 0;
+    if (tid == 0) {
+        ncset = 0;
+        sbeta = NEG_INF;
+        sover = 0;
+        sbad[0] = 0;
+        sbad[1] = 0;
+        if constexpr (BULK) {
+            for (int s = 0; s < TK_STAGES; ++s) mbar_init(&full[s], 1);
+            fence_mbar_init();
+            for (int s = 0; s < TK_STAGES; ++s) issue_next(s);
         }
     }
     __syncthreads();
-    const float tau = sm.tau;
-    const int nonfinite = sm.nonfinite;
 
-    // ---- collect every element >= tau on chip (unordered; the row merge sorts).  A group whose
-    // maximum passes tau yields a bitmask of its passing slots; only the set bits are visited.
-    const bool too_many = (k > NT) && (cend - cbase > CAP_C);
-    if (!nonfinite && !too_many) {
+    bool failed = false;  // a bulk-copy wait ran out: the remaining segments are reported, not read
+    long long fail_it = 0;
+    long long it = 0;
+    for (long long sg = blockIdx.x; sg < nsegs; sg += G0) {
+        const int nst = seg_stages(sg);
+        int seg_bad = 0;
+        for (int st = 0; st < nst; ++st, ++it) {
+            int row_id, cbase, cend;
+            chunk_of(sg, st, row_id, cbase, cend);
+            const bool partial = cbase + CHUNK > cend;
+
+            // ---- the chunk into registers (-inf padding past the row's end)
+            uint32_t w[NREG];
+            bool ok = !failed;
+            if constexpr (BULK) {
+                const int s = (int)(it % TK_STAGES);
+                if (ok) ok = mbar_wait(&full[s], (unsigned)(it / TK_STAGES) & 1u);
+                const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+                const uint4* sb = ring + (size_t)s * NT * TK_NV;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            uint32_t bits = 0;
-            if constexpr (DT == DT_BF16) {
-                const __nv_bfloat162 t2 = __floats2bfloat162_rn(tau, tau);
-                if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        const uint32_t wd = w[g * G + j];
-                        bits |= (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd), t2) & 0x00010001u) << j;
-                    }
+                for (int j = 0; j < TK_NV; ++j) {
+                    uint4 q = make_uint4(pad, pad, pad, pad);
+                    if (ok && (!partial || cbase + (j * NT + tid) * VEC < cend)) q = lds128(sb + j * NT + tid);
+                    w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
                 }
             } else {
-                if (__uint_as_float(gm[g]) >= tau) {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) bits |= (uint32_t)(__uint_as_float(w[g * G + j]) >= tau) << j;
-                }
-            }
-            while (bits) {
-                const int bp = __ffs(bits) - 1;
-                bits &= bits - 1;
-                const int j = bp & 15, half = bp >> 4;  // register j of the group, bf16 half
-                const uint32_t wd = select8(w, g * G, j);
-                float x;
-                int s;
+                const char* row = spec_row_ptr(P, row_id / P.R, row_id % P.R);
                 if constexpr (DT == DT_BF16) {
-                    x = half ? bf16hi(wd) : bf16lo(wd);
-                    s = 2 * (g * G + j) + half;
+                    const unsigned short* rp = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+                    for (int j = 0; j < NREG; ++j) {
+                        const int e0 = slot_elem<1>(cbase, 2 * j), e1 = slot_elem<1>(cbase, 2 * j + 1);
+                        const uint32_t lo = e0 < cend ? __ldg(rp + e0) : 0xff80u;
+                        const uint32_t hi = e1 < cend ? __ldg(rp + e1) : 0xff80u;
+                        w[j] = lo | (hi << 16);
+                    }
                 } else {
-                    x = __uint_as_float(wd);
-                    s = g * G + j;
+                    const float* rp = reinterpret_cast<const float*>(row);
+#pragma unroll
+                    for (int j = 0; j < NREG; ++j) {
+                        const int e0 = slot_elem<1>(cbase, j);
+                        w[j] = e0 < cend ? __float_as_uint(__ldg(rp + e0)) : 0xff800000u;
+                    }
                 }
-                const int e = slot_elem<VEC>(cbase, s);
-                if (e < cend) cand_push(sm, x, e);
+            }
+
+            // ---- group maxima (G registers each) and the thread maximum, NaN-propagating
+            uint32_t gm[NG];
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                uint32_t m = w[g * G];
+#pragma unroll
+                for (int j = 1; j < G; ++j) {
+                    if constexpr (DT == DT_BF16) m = bmax2_nan(m, w[g * G + j]);
+                    else m = __float_as_uint(fmax_nan_f(__uint_as_float(m), __uint_as_float(w[g * G + j])));
+                }
+                gm[g] = m;
+            }
+            float tm;
+            if constexpr (DT == DT_BF16) {
+                uint32_t pm = gm[0];
+#pragma unroll
+                for (int g = 1; g < NG; ++g) pm = bmax2_nan(pm, gm[g]);
+                tm = fmax_nan_f(bf16lo(pm), bf16hi(pm));
+            } else {
+                tm = __uint_as_float(gm[0]);
+#pragma unroll
+                for (int g = 1; g < NG; ++g) tm = fmax_nan_f(tm, __uint_as_float(gm[g]));
+            }
+            tmax[tid] = tm;
+            if (tm != tm || tm == __int_as_float(0x7f800000)) sbad[it & 1] = 1;
+            if (tid == 0) sbad[(it + 1) & 1] = 0;  // the next chunk's flag
+            // every thread has read its part of the stage, every thread maximum is published, and
+            // warp 0 has finished with the previous chunk's candidate set
+            const int anyfail = __syncthreads_or(!ok);
+            if (anyfail && !failed) {
+                failed = true;
+                fail_it = it;
+            }
+            if constexpr (BULK) {
+                if (tid == 0 && !failed) {
+                    fence_proxy_async_smem();
+                    issue_next((int)(it % TK_STAGES));
+                }
+            }
+            if (failed) {
+                if (tid == 0 && st + 1 == nst) P.ccount[sg] = TK_TIMEOUT;
+                continue;
+            }
+
+            // ---- the bound for this chunk.  On a segment's first chunk (or while no finite bound
+            // exists) every warp selects tau = the k-th largest thread maximum (valid for k <= NT)
+            // by itself; later chunks reuse the segment's running bound, which is already tighter.
+            const int bad = sbad[it & 1];
+            seg_bad |= bad;
+            float beta = (st == 0) ? NEG_INF : sbeta;
+            if (!bad && k <= NT && beta == NEG_INF) {
+                uint32_t keys[NT / 32];
+#pragma unroll
+                for (int i = 0; i < NT / 32; ++i) keys[i] = okey(tmax[lane + 32 * i]);
+                uint32_t prefix = 0;
+                constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+                for (int bit = 31; bit >= lo; --bit) {
+                    const uint32_t want = prefix | (1u << bit);
+                    unsigned cnt = 0;
+#pragma unroll
+                    for (int i = 0; i < NT / 32; ++i) cnt += keys[i] >= want;
+                    if ((int)__reduce_add_sync(FULL, cnt) >= k) prefix = want;
+                }
+                if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+                // tau and the carried bound are both <= the segment's k-th largest value, hence
+                // <= the row's
+                beta = key_value(prefix);
+            }
+
+            // ---- every element >= beta joins the candidate set.  A group whose maximum reaches
+            // beta yields a bitmask of its passing slots (slots past the row's end masked off);
+            // each warp reserves room for all of its candidates with one shared-memory atomic and
+            // every thread then writes its own at consecutive positions.
+            if (!seg_bad && !sover && k <= NT) {
+                uint32_t bits[NG];
+                int mine = 0;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                    uint32_t bt = 0;
+                    if constexpr (DT == DT_BF16) {
+                        const __nv_bfloat162 t2 = __floats2bfloat162_rn(beta, beta);
+                        if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) {
+                                const uint32_t wd = w[g * G + j];
+                                bt |= (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd), t2) & 0x00010001u) << j;
+                            }
+                        }
+                    } else {
+                        if (__uint_as_float(gm[g]) >= beta) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) bt |= (uint32_t)(__uint_as_float(w[g * G + j]) >= beta) << j;
+                        }
+                    }
+                    if (partial && bt) bt &= valid_bits<DT, VEC>(cbase, cend, g);
+                    bits[g] = bt;
+                    mine += __popc(bt);
+                }
+                const int incl = warp_incl_scan(mine);
+                const int wtot = __shfl_sync(FULL, incl, 31);
+                if (wtot > 0) {
+                    int base = 0;
+                    if (lane == 31) base = atomicAdd(&ncset, wtot);
+                    int pos = __shfl_sync(FULL, base, 31) + incl - mine;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        uint32_t bt = bits[g];
+                        while (bt) {
+                            const int bp = __ffs(bt) - 1;
+                            bt &= bt - 1;
+                            const int j = bp & 15, half = bp >> 4;  // register j of the group, bf16 half
+                            const uint32_t wd = select8(w, g * G, j);
+                            TopkEntry en;
+                            if constexpr (DT == DT_BF16) {
+                                en.x = half ? bf16hi(wd) : bf16lo(wd);
+                                en.idx = slot_elem<VEC>(cbase, 2 * (g * G + j) + half);
+                            } else {
+                                en.x = __uint_as_float(wd);
+                                en.idx = slot_elem<VEC>(cbase, g * G + j);
+                            }
+                            if (pos < TK_CAPC) cset[pos] = en;
+                            ++pos;
+                        }
+                    }
+                }
+            }
+            __syncthreads();  // every candidate of the chunk is in the set
+
+            // ---- warp 0: tighten the set to its exact k-th largest when it grows large or the
+            // segment ends; at the end, publish the segment's list.  The other warps go on with
+            // the next chunk meanwhile.
+            if (warp == 0) {
+                const bool last = st + 1 == nst;
+                int n = ncset;
+                const int over = sover || k > NT || n > TK_CAPC;
+                float nb = beta;
+                if (!seg_bad && !over && (last || n > max(3 * k, 128) || n > TK_CAPC / 2)) {
+                    uint32_t gk = okey(NEG_INF);
+                    if (n >= k) {
+                        if (n <= 32 * 8) gk = warp_kth_key_regs<DT, 8>(cset, n, k);
+                        else if (n <= 32 * 16) gk = warp_kth_key_regs<DT, 16>(cset, n, k);
+                        else gk = warp_kth_key<DT>(n, k, [&](int i) { return okey(cset[i].x); });
+                    }
+                    int m = 0;
+                    for (int i0 = 0; i0 < n; i0 += 32) {
+                        const int i = i0 + lane;
+                        TopkEntry e;
+                        bool keep = false;
+                        if (i < n) {
+                            e = cset[i];
+                            keep = okey(e.x) >= gk;
+                        }
+                        const unsigned bal = __ballot_sync(FULL, keep);
+                        __syncwarp();
+                        if (keep) cset[m + __popc(bal & ((1u << lane) - 1u))] = e;
+                        m += __popc(bal);
+                        __syncwarp();
+                    }
+                    n = m;
+                    nb = fmaxf(nb, key_value(gk));
+                }
+                if (last) {
+                    const int code = seg_bad ? TK_NONFINITE : (over || n > P.cap_s) ? TK_OVERFLOW : n;
+                    if (code > 0) {
+                        TopkEntry* dst = P.clist + (size_t)sg * P.cap_s;
+                        for (int i = lane; i < n; i += 32) dst[i] = cset[i];
+                    }
+                    if (lane == 0) {
+                        P.ccount[sg] = code;
+                        ncset = 0;
+                        sbeta = NEG_INF;
+                        sover = 0;
+                    }
+                } else if (lane == 0) {
+                    ncset = n;
+                    sbeta = nb;
+                    sover = over;
+                }
+                __syncwarp();
             }
         }
     }
-    __syncthreads();
-    // ---- reserve room in the row's union and copy the candidates there (coalesced)
-    if (tid == 0) {
-        const int n = sm.n;
-        int base = -1;
-        if (nonfinite) atomicOr(P.uflags + row_id, 1);
-        else if (too_many || n > CAP_C) atomicOr(P.uflags + row_id, 2);
-        else if (n > 0) {
-            base = atomicAdd(P.ucount + row_id, n);
-            if (base + n > P.cap_u) { atomicOr(P.uflags + row_id, 2); base = -1; }
+    // after a failed wait, let the copies still in flight land before the CTA leaves (bounded)
+    if constexpr (BULK) {
+        if (failed && tid == 0)
+            for (long long j = fail_it; j < nissued && j < fail_it + TK_STAGES; ++j)
+                (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u);
+    }
+}
+
+// Kernel 2, one warp per row: exact threshold g over the union of the row's segment lists, the
+// kept list sorted by index, and the normaliser over it.  u holds nsegr * cap_s entries, kept
+// cap_k.
+template <int DT>
+__device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry* kept, int row_id)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    RowStats st;
+    st.M = NEG_INF; st.MC = NEG_INF; st.S = 0.0; st.thr = NEG_INF;
+    st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
+    const int ns = P.nsegr;  // <= 4
+    const int* cnt = P.ccount + (size_t)row_id * ns;
+    const TopkEntry* lists = P.clist + (size_t)row_id * ns * P.cap_s;
+
+    int n = (lane < ns) ? min(__ldcg(cnt + lane), P.cap_s) : 0;
+    int flag = 0;
+    if (n == TK_NONFINITE) flag |= 1;
+    else if (n == TK_TIMEOUT) flag |= 4;
+    else if (n < 0) flag |= 2;
+    flag = (int)__reduce_or_sync(FULL, (unsigned)flag);
+    if (flag & 4) { st.status = ROW_TIMEOUT; return st; }
+    if (flag & 1) { st.status = ROW_NONFINITE; return st; }
+    if (flag & 2) { st.dense = 1; return st; }
+    // offsets of the segment lists in the union
+    const int incl = warp_incl_scan(n);
+    const int o1 = __shfl_sync(FULL, incl, 0), o2 = __shfl_sync(FULL, incl, 1),
+              o3 = __shfl_sync(FULL, incl, 2), total = __shfl_sync(FULL, incl, 31);
+    for (int f0 = 0; f0 < total; f0 += 32 * 8) {
+        TopkEntry e[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int f = f0 + 32 * j + lane;
+            if (f < total) {
+                const int sgi = (f >= o1) + (ns > 2 && f >= o2) + (ns > 3 && f >= o3);
+                const int off = sgi == 0 ? 0 : sgi == 1 ? o1 : sgi == 2 ? o2 : o3;
+                const TopkEntry* src = lists + (size_t)sgi * P.cap_s + (f - off);
+                e[j].x = __ldcg(&src->x);
+                e[j].idx = __ldcg(&src->idx);
+            }
         }
-        sm.base = base;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int f = f0 + 32 * j + lane;
+            if (f < total) u[f] = e[j];
+        }
+    }
+    __syncwarp();
+
+    const int k = P.top_k;
+    const uint32_t gkey = (total >= k) ? warp_kth_key<DT>(total, k, [&](int i) { return okey(u[i].x); })
+                                       : okey(NEG_INF);
+    // stable ballot compaction of the entries >= g
+    int nk = 0;
+    for (int i0 = 0; i0 < total; i0 += 32) {
+        const int i = i0 + lane;
+        const bool keep = i < total && okey(u[i].x) >= gkey;
+        const unsigned bal = __ballot_sync(FULL, keep);
+        const int pos = nk + __popc(bal & ((1u << lane) - 1u));
+        if (keep && pos < P.cap_k) kept[pos] = u[i];
+        nk += __popc(bal);
+    }
+    __syncwarp();
+    if (nk > P.cap_k) { st.dense = 1; return st; }
+    warp_sort_by_index(kept, nk);
+    float mx = NEG_INF;
+    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, kept[i].x);
+    const float M = warp_max(mx);
+    const float MC = M * P.c;
+    double acc = 0.0;
+    if (M != NEG_INF)
+        for (int i = lane; i < nk; i += 32) acc += (double)ex2(fmaf(kept[i].x, P.c, -MC));
+    const double S = warp_sum(acc);
+    TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
+    for (int i = lane; i < nk; i += 32) kl[i] = kept[i];
+    st.M = M;
+    st.MC = MC;
+    st.S = S;
+    st.thr = key_value(gkey);
+    st.klist_n = nk;
+    st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
+    return st;
+}
+
+// Kernel 2: one CTA per request.  Warps take the request's rows; then one warp scans and draws.
+template <int DT>
+__global__ void __launch_bounds__(NT) topk_finish_kernel(SpecParams P)
+{
+    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: u[nsegr*cap_s], kept[cap_k]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x;
+    const int per = P.nsegr * P.cap_s + P.cap_k;
+    TopkEntry* u = fin + (size_t)warp * per;
+    TopkEntry* kept = u + P.nsegr * P.cap_s;
+    for (int r = warp; r < P.R; r += WARPS) {
+        const int row_id = b * P.R + r;
+        const RowStats st = topk_row_finish<DT>(P, u, kept, row_id);
+        if (lane == 0) P.rstats[row_id] = st;
     }
     __syncthreads();
-    if (sm.base >= 0) {
-        TopkEntry* dst = P.ulist + (size_t)row_id * P.cap_u + sm.base;
-        for (int i = tid; i < sm.n; i += NT) dst[i] = sm.cand[i];
-    }
-    if (!arrive_last(&P.row_ctr[row_id], (unsigned)P.CT, &sm.flag)) return;
     if (warp != 0) return;
-
-    // ==== one warp of the last CTA of the row
-    const RowStats st = topk_row_epilogue<DT>(P, sm, row_id);
-    if (lane == 0) P.rstats[row_id] = st;
-    if (!warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) return;
-
-    // ==== the same warp, last row of the request
     int nd = 0;
     for (int rr = lane; rr < P.R; rr += 32) nd += __ldcg(&P.rstats[(size_t)b * P.R + rr].dense);
     nd = __reduce_add_sync(0xffffffffu, nd);
@@ -451,7 +643,7 @@ __global__ void __launch_bounds__(NT, 4) topk_stats_kernel(SpecParams P)
         if (lane == 0) P.ndense[b] = nd;
         return;
     }
-    topk_request_epilogue<DT>(P, sm, b);
+    topk_request_epilogue<DT>(P, reinterpret_cast<double*>(fin), b);
 }
 
 // ---------------------------------------------------------------- exact fallback for dense rows
@@ -595,17 +787,53 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
     emit_spec(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
 }
 
-cudaError_t launch_topk_path(const SpecParams& P, unsigned g1, unsigned g2, cudaStream_t st)
+
+// persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task
+template <auto K>
+static unsigned cta_grid(long long tasks, int sms, size_t smem)
 {
-    if (P.dtype == DT_BF16) {
-        if (P.vec == 8) topk_stats_kernel<DT_BF16, 8><<<g1, NT, 0, st>>>(P);
-        else topk_stats_kernel<DT_BF16, 1><<<g1, NT, 0, st>>>(P);
-        topk_dense_kernel<DT_BF16><<<g2, NT, 0, st>>>(P);
-    } else {
-        if (P.vec == 4) topk_stats_kernel<DT_F32, 4><<<g1, NT, 0, st>>>(P);
-        else topk_stats_kernel<DT_F32, 1><<<g1, NT, 0, st>>>(P);
-        topk_dense_kernel<DT_F32><<<g2, NT, 0, st>>>(P);
+    static int per_sm = 0;
+    if (per_sm < 1) {
+        int n = 0;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, NT, smem) != cudaSuccess || n < 1) n = 1;
+        per_sm = n;
     }
+    const long long cap = (long long)per_sm * sms;
+    return (unsigned)(tasks < 1 ? 1 : (tasks < cap ? tasks : cap));
+}
+
+template <auto K>
+static void set_smem_limit(size_t smem)
+{
+    static size_t done = 0;
+    if (smem > 48 * 1024 && smem > done) {
+        cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        done = smem;
+    }
+}
+
+template <int DT>
+static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
+{
+    const long long nsegs = (long long)P.B * P.R * P.nsegr;
+    if (P.vec > 1) {
+        constexpr auto K1 = topk_stream_kernel<DT, true>;
+        K1<<<cta_grid<K1>(nsegs, sms, TK_SMEM), NT, TK_SMEM, st>>>(P);
+    } else {
+        constexpr auto K1 = topk_stream_kernel<DT, false>;
+        K1<<<cta_grid<K1>(nsegs, sms, 0), NT, 0, st>>>(P);
+    }
+    const size_t fsm = (size_t)WARPS * (P.nsegr * P.cap_s + P.cap_k) * sizeof(TopkEntry);
+    set_smem_limit<topk_finish_kernel<DT>>(fsm);
+    topk_finish_kernel<DT><<<(unsigned)P.B, NT, fsm, st>>>(P);
+    topk_dense_kernel<DT><<<(unsigned)((long long)P.B * P.R), NT, 0, st>>>(P);
+}
+
+cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st)
+{
+    if (P.dtype == DT_BF16) launch_topk<DT_BF16>(P, sms, st);
+    else launch_topk<DT_F32>(P, sms, st);
     return cudaGetLastError();
 }
 
