@@ -45,17 +45,20 @@ constexpr double PIN_BYTES = 80e6;
 // top-k chunks are 32 KB of one row: 16384 bf16 or 8192 fp32 elements
 static long long topk_chunk_elems(int dtype) { return dtype == DT_BF16 ? 16384 : 8192; }
 static int topk_chunks(int dtype, int V) { return (int)cdiv(V, topk_chunk_elems(dtype)); }
-// Segments per row: a row is split into up to 4 runs of chunks so that the streaming kernel's
-// ~2 CTAs per SM have at least a dozen segments each (load balance at small B).
+// Candidate lists of a row hold at most TK_UNION entries in all (the finish kernel keeps them in
+// registers), one list per (segment, warp of the streaming kernel).  A row is split into up to 4
+// segments (runs of chunks) so that the streaming kernel's ~2 CTAs per SM have at least a dozen
+// segments each (load balance at small B), as far as every segment's lists can still hold a
+// generous estimate of its candidates: 64 per chunk plus 2k + 64.
 constexpr int TK_MAX_SEGR = 4;
-static int topk_segments(long long rows, int CT, int sms)
+constexpr int TK_UNION = 1024;
+static int topk_segments(long long rows, int CT, int sms, int k)
 {
     const long long want = cdiv(24LL * sms, std::max(1LL, rows));
-    const int ns = (int)std::max(1LL, std::min<long long>(want, std::min(TK_MAX_SEGR, CT)));
-    const int sps = (int)cdiv(CT, ns);
-    return (int)cdiv(CT, sps);
+    int ns = (int)std::max(1LL, std::min<long long>(want, std::min(TK_MAX_SEGR, CT)));
+    while (ns > 1 && (long long)ns * (64 * cdiv(CT, ns) + 2 * std::min(k, NT) + 64) > TK_UNION) --ns;
+    return (int)cdiv(CT, cdiv(CT, ns));
 }
-// Rows with k > NT take the dense path, so capacities are sized for min(k, NT).
 // per-chunk candidate slot: 2k + 64 entries
 static int topk_slot_cap(int k) { return (int)((2LL * std::min(k, NT) + 64 + 31) / 32 * 32); }
 // per-row kept list: the same, rounded up to a power of two (the on-chip sort pads to one)
@@ -80,6 +83,7 @@ struct SpecLayout {
 // All counters sit at the front so one memset clears them.
 static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool topk, int nsegr,
                               int cap_s, int cap_k)
+
 {
     SpecLayout L;
     size_t o = 0;
@@ -96,8 +100,8 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_plan = o; o = align_up(o + (size_t)B * sizeof(Plan));
     L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
     if (topk) {
-        L.o_clist = o; o = align_up(o + (size_t)B * R * nsegr * cap_s * sizeof(TopkEntry));
-        L.o_ccount = o; o = align_up(o + (size_t)B * R * nsegr * sizeof(int));
+        L.o_clist = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * cap_s * sizeof(TopkEntry));
+        L.o_ccount = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * sizeof(int));
         L.o_klist = o; o = align_up(o + (size_t)B * R * cap_k * sizeof(TopkEntry));
     }
     L.bytes = o;
@@ -208,14 +212,15 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.pin_pairs = (int)std::min(2.0, std::floor(PIN_BYTES / ((double)B * 2.0 * (double)V * (double)es)));
     if (topk) {
         P.CT = topk_chunks(dt, V);
-        P.nsegr = topk_segments((long long)B * R, P.CT, sms);
+        P.nsegr = topk_segments((long long)B * R, P.CT, sms, top_k);
         P.sps = (int)cdiv(P.CT, P.nsegr);
-        P.cap_s = topk_slot_cap(top_k);
+        P.cap_s = TK_UNION / (P.nsegr * WARPS);
         P.cap_k = topk_kept_cap(top_k);
     }
     const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.nsegr, P.cap_s, P.cap_k);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
-    if ((long long)B * R * (topk ? P.CT : 1) >= (1LL << 31) || P.tasks1 >= (1LL << 31))
+    if ((long long)B * R * (topk ? P.CT : 1) >= (1LL << 31) || P.tasks1 >= (1LL << 31) ||
+        (long long)B * R * TK_MAX_SEGR * WARPS >= (1LL << 31))
         return SPEC_ERR_INVALID_ARG;
 
     char* ws = static_cast<char*>(workspace);
@@ -268,10 +273,9 @@ size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
             best = std::max(best, tree_layout(B, tree_nodes, slices1(sh)).bytes);
         } else {
             const bool topk = top_k > 0 && top_k < V;
-            const int CT = topk ? std::max(topk_chunks(DT_BF16, V), topk_chunks(DT_F32, V)) : 0;
+            // lists: nsegr * WARPS * cap_s <= TK_UNION entries, at most TK_MAX_SEGR * WARPS per row
             const SpecLayout L = spec_layout(B, 2 * gamma + 1, partials_per_row(sh), nsegs(sh), topk,
-                                             std::min(TK_MAX_SEGR, std::max(CT, 1)),
-                                             topk ? topk_slot_cap(top_k) : 0,
+                                             TK_MAX_SEGR, topk ? TK_UNION / (TK_MAX_SEGR * WARPS) : 0,
                                              topk ? topk_kept_cap(top_k) : 0);
             best = std::max(best, L.bytes);
         }

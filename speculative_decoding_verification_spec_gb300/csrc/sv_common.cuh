@@ -97,7 +97,7 @@ struct SpecParams {
     // top-k chunking and capacities
     int CT;               // 32 KB chunks per row
     int nsegr, sps;       // segments per row (<= 4) and chunks per segment
-    int cap_s;            // per-segment candidate list capacity (entries)
+    int cap_s;            // capacity of one warp's candidate list for a segment (entries)
     int cap_k;            // per-row kept-list capacity
     // outputs
     int32_t* accepted_len;
@@ -115,8 +115,8 @@ struct SpecParams {
     unsigned* req_ctr;    // [B]
     unsigned* res_ctr;    // [B]
     unsigned* work;       // [2] task counters of the two streaming kernels
-    TopkEntry* clist;     // [B*R*nsegr*cap_s] each segment's entries >= its k-th largest (unordered)
-    int* ccount;          // [B*R*nsegr] entries listed, or TK_NONFINITE / TK_OVERFLOW / TK_TIMEOUT
+    TopkEntry* clist;     // [B*R*nsegr*WARPS*cap_s] per (segment, warp): candidates (unordered)
+    int* ccount;          // [B*R*nsegr*WARPS] entries listed, or TK_NONFINITE / TK_OVERFLOW / TK_TIMEOUT
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
     unsigned* dense_ctr;  // [B]
     int* ndense;          // [B]

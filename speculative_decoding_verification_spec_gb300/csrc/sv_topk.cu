@@ -201,35 +201,44 @@ __device__ __forceinline__ uint32_t valid_bits(int cbase, int cend, int g)
     return m;
 }
 
-// k-th largest key (as warp_kth_key) of e[0..n), n <= 32 * KPL, with the keys held in registers.
-template <int DT, int KPL>
-__device__ uint32_t warp_kth_key_regs(const TopkEntry* e, int n, int k)
-{
-    const int lane = threadIdx.x & 31;
-    uint32_t key[KPL];
-#pragma unroll
-    for (int j = 0; j < KPL; ++j) {
-        const int i = lane + 32 * j;
-        key[j] = i < n ? okey(e[i].x) : 0u;  // 0: below every key a value can have
-    }
-    uint32_t prefix = 0;
-    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-    for (int bit = 31; bit >= lo; --bit) {
-        const uint32_t want = prefix | (1u << bit);
-        unsigned cnt = 0;
-#pragma unroll
-        for (int j = 0; j < KPL; ++j) cnt += key[j] >= want;
-        if ((int)__reduce_add_sync(0xffffffffu, cnt) >= k) prefix = want;
-    }
-    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-    return prefix;
-}
+constexpr int TK_BINS = 256;  // histogram of candidate values above a segment's first bound
+static_assert(TK_BINS == NT, "one bin per thread to clear");
+constexpr int TK_KPL = 32;                 // union entries per lane in the finish kernel
+constexpr int TK_UNION = 32 * TK_KPL;      // entries of all candidate lists of a row
 
-constexpr int TK_CAPC = 1024;  // on-chip candidate set of the segment being streamed
+// Position in the segment sequence blockIdx.x, blockIdx.x + stride, ... with the segment's row and
+// its index within the row kept up to date without divisions.
+struct SegCursor {
+    int sg, row_id, si, drow, dsi;
+    __device__ __forceinline__ void init(int start, int stride, int nsegr)
+    {
+        sg = start;
+        row_id = start / nsegr;
+        si = start % nsegr;
+        drow = stride / nsegr;
+        dsi = stride % nsegr;
+    }
+    __device__ __forceinline__ void next(int stride, int nsegr)
+    {
+        sg += stride;
+        row_id += drow;
+        si += dsi;
+        if (si >= nsegr) {
+            si -= nsegr;
+            ++row_id;
+        }
+    }
+};
 
 // Kernel 1.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage ring; otherwise
 // element loads straight into registers.  A CTA takes segments (runs of up to P.sps chunks of one
-// row) round-robin and streams them chunk by chunk.
+// row) round-robin and streams them chunk by chunk, one CTA barrier per chunk.  Each warp appends
+// the elements of its part of a chunk that are at or above the current bound beta to its own list
+// for the segment (no atomics), and counts each in a histogram of its value above the segment's
+// first bound (bins 2^16 apart in the order-preserving key: one bf16 value per bin).  After the
+// barrier warp 1 reads the histogram -- every count in it is a real element of the segment -- and
+// the lowest bin edge with at least k counted elements above it becomes the bound for the next
+// chunk.
 template <int DT, bool BULK>
 __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
 {
@@ -239,59 +248,56 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     constexpr int VEC = BULK ? ((DT == DT_BF16) ? 8 : 4) : 1;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int G = 8, NG = NREG / G;
+    constexpr int HW = (WARPS > 1) ? 1 : 0;  // the warp that turns the histogram into a bound
     static_assert(NREG % G == 0, "register groups");
     extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
-    __shared__ float tmax[NT];
-    __shared__ TopkEntry cset[TK_CAPC];
-    __shared__ int ncset;     // candidates in cset (may exceed TK_CAPC: then the segment overflowed)
-    __shared__ float sbeta;   // running lower bound of the segment's k-th largest value
-    __shared__ int sover;     // the segment's candidates overflowed
-    __shared__ int sbad[2];   // a NaN or +inf was seen in the chunk (double-buffered by parity)
+    __shared__ float tmax[2][NT];      // thread maxima of the chunk (alternating)
+    __shared__ int hist[2][TK_BINS];   // per segment (alternating)
+    __shared__ int sbad[3];            // a NaN or +inf was seen in the chunk (cleared two chunks on)
+    __shared__ float pub_beta[2];      // bound published for segment pub_seg
+    __shared__ int pub_seg[2];         // -1: none
     __shared__ __align__(8) uint64_t full[TK_STAGES];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned FULL = 0xffffffffu;
-    const long long nsegs = (long long)P.B * P.R * P.nsegr;
-    const long long G0 = gridDim.x;
+    const int nsegs = P.B * P.R * P.nsegr;
+    const int G0 = gridDim.x;
     const int k = P.top_k;
     const uint64_t pol = policy_evict_first();
 
-    auto seg_stages = [&](long long sg) -> int {
-        const int si = (int)(sg % P.nsegr);
-        return min(P.sps, P.CT - si * P.sps);
-    };
-    // row and element range of chunk `st` of segment `sg`
-    auto chunk_of = [&](long long sg, int st, int& row_id, int& cbase, int& cend) {
-        row_id = (int)(sg / P.nsegr);
-        const int c = (int)(sg % P.nsegr) * P.sps + st;
-        cbase = c * CHUNK;
-        cend = min(cbase + CHUNK, P.V);
-    };
-
-    // producer cursor (thread 0): the next (segment, chunk) to fetch, in this CTA's consumption order
-    long long pseg = blockIdx.x;
-    int pst = 0;
+    // producer (thread 0): the next (segment, chunk) to fetch, in this CTA's consumption order
+    SegCursor pc;
+    pc.init(blockIdx.x, G0, P.nsegr);
+    int pst = 0, pnst = 0;
+    const char* prow = nullptr;
     long long nissued = 0;
+    auto pseg_setup = [&]() {
+        if (pc.sg < nsegs) {
+            pnst = min(P.sps, P.CT - pc.si * P.sps);
+            prow = spec_row_ptr(P, pc.row_id / P.R, pc.row_id % P.R);
+        }
+    };
     auto issue_next = [&](int s) {
-        if (pseg >= nsegs) return;
-        int row_id, cbase, cend;
-        chunk_of(pseg, pst, row_id, cbase, cend);
-        const char* src = spec_row_ptr(P, row_id / P.R, row_id % P.R) + (size_t)cbase * ES;
-        bulk_load(ring + (size_t)s * NT * TK_NV, src, (unsigned)(cend - cbase) * ES, &full[s], pol);
+        if (pc.sg >= nsegs) return;
+        const int cbase = (pc.si * P.sps + pst) * CHUNK;
+        const int cend = min(cbase + CHUNK, P.V);
+        bulk_load(ring + (size_t)s * NT * TK_NV, prow + (size_t)cbase * ES, (unsigned)(cend - cbase) * ES,
+                  &full[s], pol);
         ++nissued;
-        if (++pst == seg_stages(pseg)) {
+        if (++pst == pnst) {
             pst = 0;
-            pseg += G0;
+            pc.next(G0, P.nsegr);
+            pseg_setup();
         }
     };
 
+    hist[0][tid] = 0;
     if (tid == 0) {
-        ncset = 0;
-        sbeta = NEG_INF;
-        sover = 0;
-        sbad[0] = 0;
-        sbad[1] = 0;
+        sbad[0] = sbad[1] = sbad[2] = 0;
+        pub_beta[0] = pub_beta[1] = NEG_INF;
+        pub_seg[0] = pub_seg[1] = -1;
         if constexpr (BULK) {
+            pseg_setup();
             for (int s = 0; s < TK_STAGES; ++s) mbar_init(&full[s], 1);
             fence_mbar_init();
             for (int s = 0; s < TK_STAGES; ++s) issue_next(s);
@@ -299,15 +305,26 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     }
     __syncthreads();
 
+    // every warp: the current segment (uniform across the CTA) and this warp's list for it
+    int jseg = -1;               // this CTA's segment counter (selects hist)
+    int seg_bad = 0;
+    float tau_first = NEG_INF;   // the segment's first bound; histogram bins count from its key
+    uint32_t key0 = 0;
+    int wcount = 0;              // entries in this warp's list
+
     bool failed = false;  // a bulk-copy wait ran out: the remaining segments are reported, not read
     long long fail_it = 0;
     long long it = 0;
-    for (long long sg = blockIdx.x; sg < nsegs; sg += G0) {
-        const int nst = seg_stages(sg);
-        int seg_bad = 0;
+    SegCursor cc;
+    cc.init(blockIdx.x, G0, P.nsegr);
+    for (; cc.sg < nsegs; cc.next(G0, P.nsegr)) {
+        const int sg = cc.sg;
+        const int nst = min(P.sps, P.CT - cc.si * P.sps);
+        const char* row = BULK ? nullptr : spec_row_ptr(P, cc.row_id / P.R, cc.row_id % P.R);
+        TopkEntry* wlist = P.clist + ((size_t)sg * WARPS + warp) * P.cap_s;
         for (int st = 0; st < nst; ++st, ++it) {
-            int row_id, cbase, cend;
-            chunk_of(sg, st, row_id, cbase, cend);
+            const int cbase = (cc.si * P.sps + st) * CHUNK;
+            const int cend = min(cbase + CHUNK, P.V);
             const bool partial = cbase + CHUNK > cend;
 
             // ---- the chunk into registers (-inf padding past the row's end)
@@ -325,7 +342,6 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                     w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
                 }
             } else {
-                const char* row = spec_row_ptr(P, row_id / P.R, row_id % P.R);
                 if constexpr (DT == DT_BF16) {
                     const unsigned short* rp = reinterpret_cast<const unsigned short*>(row);
 #pragma unroll
@@ -368,37 +384,40 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
 #pragma unroll
                 for (int g = 1; g < NG; ++g) tm = fmax_nan_f(tm, __uint_as_float(gm[g]));
             }
-            tmax[tid] = tm;
-            if (tm != tm || tm == __int_as_float(0x7f800000)) sbad[it & 1] = 1;
-            if (tid == 0) sbad[(it + 1) & 1] = 0;  // the next chunk's flag
-            // every thread has read its part of the stage, every thread maximum is published, and
-            // warp 0 has finished with the previous chunk's candidate set
+            tmax[it & 1][tid] = tm;
+            if (tm != tm || tm == __int_as_float(0x7f800000)) sbad[it % 3] = 1;
+            // every thread has read its part of the stage and published its maximum; every warp
+            // has collected the previous chunk
             const int anyfail = __syncthreads_or(!ok);
             if (anyfail && !failed) {
                 failed = true;
                 fail_it = it;
             }
+            if (tid == 0) sbad[(it + 2) % 3] = 0;  // the previous chunk's flag, read by all by now
             if constexpr (BULK) {
-                if (tid == 0 && !failed) {
-                    fence_proxy_async_smem();
-                    issue_next((int)(it % TK_STAGES));
-                }
+                // the barrier above ordered every read of this stage before its refill
+                if (tid == 0 && !failed) issue_next((int)(it % TK_STAGES));
             }
             if (failed) {
-                if (tid == 0 && st + 1 == nst) P.ccount[sg] = TK_TIMEOUT;
+                if (lane == 0 && st + 1 == nst) P.ccount[(size_t)sg * WARPS + warp] = TK_TIMEOUT;
                 continue;
             }
 
-            // ---- the bound for this chunk.  On a segment's first chunk (or while no finite bound
-            // exists) every warp selects tau = the k-th largest thread maximum (valid for k <= NT)
-            // by itself; later chunks reuse the segment's running bound, which is already tighter.
-            const int bad = sbad[it & 1];
+            // ---- a new segment: fresh counters, and the bound tau = the k-th largest thread
+            // maximum of its first chunk (valid for k <= NT), selected by every warp by itself
+            if (st == 0) {
+                ++jseg;
+                hist[(jseg + 1) & 1][tid] = 0;  // for the segment after this one
+                seg_bad = 0;
+                tau_first = NEG_INF;
+                wcount = 0;
+            }
+            const int bad = sbad[it % 3];
             seg_bad |= bad;
-            float beta = (st == 0) ? NEG_INF : sbeta;
-            if (!bad && k <= NT && beta == NEG_INF) {
+            if (st == 0 && !bad && k <= NT) {
                 uint32_t keys[NT / 32];
 #pragma unroll
-                for (int i = 0; i < NT / 32; ++i) keys[i] = okey(tmax[lane + 32 * i]);
+                for (int i = 0; i < NT / 32; ++i) keys[i] = okey(tmax[it & 1][lane + 32 * i]);
                 uint32_t prefix = 0;
                 constexpr int lo = (DT == DT_BF16) ? 16 : 0;
                 for (int bit = 31; bit >= lo; --bit) {
@@ -409,23 +428,65 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                     if ((int)__reduce_add_sync(FULL, cnt) >= k) prefix = want;
                 }
                 if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-                // tau and the carried bound are both <= the segment's k-th largest value, hence
-                // <= the row's
-                beta = key_value(prefix);
+                tau_first = key_value(prefix);
+                key0 = prefix;
+            }
+            float beta = tau_first;
+            if (pub_seg[it & 1] == sg) beta = fmaxf(beta, pub_beta[it & 1]);
+
+            // ---- warp HW: the bound for the next chunk from the histogram (the counts of this
+            // chunk may be partly in: every count is a real element of the segment either way)
+            if (warp == HW) {
+                float nb = NEG_INF;
+                if (!seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
+                    int c8 = 0;
+                    int hb[TK_BINS / 32];
+#pragma unroll
+                    for (int i = 0; i < TK_BINS / 32; ++i) {
+                        hb[i] = hist[jseg & 1][lane * (TK_BINS / 32) + i];
+                        c8 += hb[i];
+                    }
+                    // counts in this lane's bins and above
+                    int suf = c8;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int v = __shfl_down_sync(FULL, suf, o);
+                        if (lane + o < 32) suf += v;
+                    }
+                    const unsigned reach = __ballot_sync(FULL, suf >= k);
+                    if (reach) {
+                        const int ls = 31 - __clz(reach);  // highest lane whose suffix reaches k
+                        int bin = -1;
+                        if (lane == ls) {
+                            int acc = suf - c8;  // counts above this lane's bins
+#pragma unroll
+                            for (int i = TK_BINS / 32 - 1; i >= 0; --i) {
+                                acc += hb[i];
+                                if (bin < 0 && acc >= k) bin = lane * (TK_BINS / 32) + i;
+                            }
+                        }
+                        bin = __shfl_sync(FULL, bin, ls);
+                        nb = key_value(key0 + ((uint32_t)bin << 16));
+                    }
+                }
+                if (lane == 0) {
+                    pub_beta[(it + 1) & 1] = nb;
+                    pub_seg[(it + 1) & 1] = (nb != NEG_INF) ? sg : -1;
+                }
             }
 
-            // ---- every element >= beta joins the candidate set.  A group whose maximum reaches
-            // beta yields a bitmask of its passing slots (slots past the row's end masked off);
-            // each warp reserves room for all of its candidates with one shared-memory atomic and
-            // every thread then writes its own at consecutive positions.
-            if (!seg_bad && !sover && k <= NT) {
+            // ---- this warp's elements >= beta go to its list and to the histogram.  A group whose
+            // maximum reaches beta yields a bitmask of its passing slots (slots past the row's end
+            // masked off); positions come from a prefix sum over the warp.
+            if (!seg_bad && k <= NT) {
+                // bf16: compare against beta rounded down to bf16, so no element >= beta is missed
+                const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(beta));
                 uint32_t bits[NG];
                 int mine = 0;
 #pragma unroll
                 for (int g = 0; g < NG; ++g) {
                     uint32_t bt = 0;
                     if constexpr (DT == DT_BF16) {
-                        const __nv_bfloat162 t2 = __floats2bfloat162_rn(beta, beta);
                         if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
 #pragma unroll
                             for (int j = 0; j < G; ++j) {
@@ -443,12 +504,11 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                     bits[g] = bt;
                     mine += __popc(bt);
                 }
-                const int incl = warp_incl_scan(mine);
-                const int wtot = __shfl_sync(FULL, incl, 31);
-                if (wtot > 0) {
-                    int base = 0;
-                    if (lane == 31) base = atomicAdd(&ncset, wtot);
-                    int pos = __shfl_sync(FULL, base, 31) + incl - mine;
+                if (__any_sync(FULL, mine)) {
+                    const int incl = warp_incl_scan(mine);
+                    int pos = wcount + incl - mine;
+                    wcount += __shfl_sync(FULL, incl, 31);
+                    int* h = hist[jseg & 1];
 #pragma unroll
                     for (int g = 0; g < NG; ++g) {
                         uint32_t bt = bits[g];
@@ -465,66 +525,19 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                                 en.x = __uint_as_float(wd);
                                 en.idx = slot_elem<VEC>(cbase, g * G + j);
                             }
-                            if (pos < TK_CAPC) cset[pos] = en;
+                            if (pos < P.cap_s) wlist[pos] = en;
                             ++pos;
+                            const uint32_t kx = okey(en.x);
+                            if (tau_first != NEG_INF && kx >= key0)
+                                atomicAdd(&h[min((int)((kx - key0) >> 16), TK_BINS - 1)], 1);
                         }
                     }
                 }
             }
-            __syncthreads();  // every candidate of the chunk is in the set
-
-            // ---- warp 0: tighten the set to its exact k-th largest when it grows large or the
-            // segment ends; at the end, publish the segment's list.  The other warps go on with
-            // the next chunk meanwhile.
-            if (warp == 0) {
-                const bool last = st + 1 == nst;
-                int n = ncset;
-                const int over = sover || k > NT || n > TK_CAPC;
-                float nb = beta;
-                if (!seg_bad && !over && (last || n > max(3 * k, 128) || n > TK_CAPC / 2)) {
-                    uint32_t gk = okey(NEG_INF);
-                    if (n >= k) {
-                        if (n <= 32 * 8) gk = warp_kth_key_regs<DT, 8>(cset, n, k);
-                        else if (n <= 32 * 16) gk = warp_kth_key_regs<DT, 16>(cset, n, k);
-                        else gk = warp_kth_key<DT>(n, k, [&](int i) { return okey(cset[i].x); });
-                    }
-                    int m = 0;
-                    for (int i0 = 0; i0 < n; i0 += 32) {
-                        const int i = i0 + lane;
-                        TopkEntry e;
-                        bool keep = false;
-                        if (i < n) {
-                            e = cset[i];
-                            keep = okey(e.x) >= gk;
-                        }
-                        const unsigned bal = __ballot_sync(FULL, keep);
-                        __syncwarp();
-                        if (keep) cset[m + __popc(bal & ((1u << lane) - 1u))] = e;
-                        m += __popc(bal);
-                        __syncwarp();
-                    }
-                    n = m;
-                    nb = fmaxf(nb, key_value(gk));
-                }
-                if (last) {
-                    const int code = seg_bad ? TK_NONFINITE : (over || n > P.cap_s) ? TK_OVERFLOW : n;
-                    if (code > 0) {
-                        TopkEntry* dst = P.clist + (size_t)sg * P.cap_s;
-                        for (int i = lane; i < n; i += 32) dst[i] = cset[i];
-                    }
-                    if (lane == 0) {
-                        P.ccount[sg] = code;
-                        ncset = 0;
-                        sbeta = NEG_INF;
-                        sover = 0;
-                    }
-                } else if (lane == 0) {
-                    ncset = n;
-                    sbeta = nb;
-                    sover = over;
-                }
-                __syncwarp();
-            }
+            // ---- the segment's last chunk: this warp publishes its list length
+            if (st + 1 == nst && lane == 0)
+                P.ccount[(size_t)sg * WARPS + warp] =
+                    seg_bad ? TK_NONFINITE : (k > NT || wcount > P.cap_s) ? TK_OVERFLOW : wcount;
         }
     }
     // after a failed wait, let the copies still in flight land before the CTA leaves (bounded)
@@ -535,22 +548,22 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     }
 }
 
-// Kernel 2, one warp per row: exact threshold g over the union of the row's segment lists, the
-// kept list sorted by index, and the normaliser over it.  u holds nsegr * cap_s entries, kept
-// cap_k.
+// Kernel 2, one warp per row: exact threshold g over the union of the row's lists (nsegr segments
+// x WARPS warps, up to TK_UNION entries, held in registers), the kept list sorted by index, and
+// the normaliser over it.  kept holds cap_k entries.
 template <int DT>
-__device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry* kept, int row_id)
+__device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* kept, int row_id)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
     RowStats st;
     st.M = NEG_INF; st.MC = NEG_INF; st.S = 0.0; st.thr = NEG_INF;
     st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
-    const int ns = P.nsegr;  // <= 4
-    const int* cnt = P.ccount + (size_t)row_id * ns;
-    const TopkEntry* lists = P.clist + (size_t)row_id * ns * P.cap_s;
+    const int nl = P.nsegr * WARPS;  // lists of the row, <= 32
+    const int* cnt = P.ccount + (size_t)row_id * nl;
+    const TopkEntry* lists = P.clist + (size_t)row_id * nl * P.cap_s;
 
-    int n = (lane < ns) ? min(__ldcg(cnt + lane), P.cap_s) : 0;
+    int n = (lane < nl) ? __ldcg(cnt + lane) : 0;
     int flag = 0;
     if (n == TK_NONFINITE) flag |= 1;
     else if (n == TK_TIMEOUT) flag |= 4;
@@ -559,42 +572,63 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     if (flag & 4) { st.status = ROW_TIMEOUT; return st; }
     if (flag & 1) { st.status = ROW_NONFINITE; return st; }
     if (flag & 2) { st.dense = 1; return st; }
-    // offsets of the segment lists in the union
-    const int incl = warp_incl_scan(n);
-    const int o1 = __shfl_sync(FULL, incl, 0), o2 = __shfl_sync(FULL, incl, 1),
-              o3 = __shfl_sync(FULL, incl, 2), total = __shfl_sync(FULL, incl, 31);
-    for (int f0 = 0; f0 < total; f0 += 32 * 8) {
-        TopkEntry e[8];
+    n = max(0, min(n, P.cap_s));
+    const int incl = warp_incl_scan(n);  // entries of lists 0..lane
+    const int total = __shfl_sync(FULL, incl, 31);
+    if (total > TK_UNION) { st.dense = 1; return st; }
+    // the union in registers: entry f = 32 j + lane, found in list q (the first with incl > f)
+    uint32_t key[TK_KPL];
+    int ix[TK_KPL];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int f = f0 + 32 * j + lane;
+    for (int j = 0; j < TK_KPL; ++j) {
+        const int f = 32 * j + lane;
+        key[j] = 0u;  // below every key a value can have
+        ix[j] = 0;
+        if (32 * j < total) {
+            int lo = 0, hi = 31;
+#pragma unroll
+            for (int step = 0; step < 5; ++step) {
+                const int mid = (lo + hi) >> 1;
+                if (__shfl_sync(FULL, incl, mid) > f) hi = mid;
+                else lo = mid + 1;
+            }
+            const int q = lo;
+            const int start = __shfl_sync(FULL, incl - n, q);
             if (f < total) {
-                const int sgi = (f >= o1) + (ns > 2 && f >= o2) + (ns > 3 && f >= o3);
-                const int off = sgi == 0 ? 0 : sgi == 1 ? o1 : sgi == 2 ? o2 : o3;
-                const TopkEntry* src = lists + (size_t)sgi * P.cap_s + (f - off);
-                e[j].x = __ldcg(&src->x);
-                e[j].idx = __ldcg(&src->idx);
+                const TopkEntry* src = lists + (size_t)q * P.cap_s + (f - start);
+                key[j] = okey(__ldcg(&src->x));
+                ix[j] = __ldcg(&src->idx);
             }
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int f = f0 + 32 * j + lane;
-            if (f < total) u[f] = e[j];
-        }
     }
-    __syncwarp();
-
     const int k = P.top_k;
-    const uint32_t gkey = (total >= k) ? warp_kth_key<DT>(total, k, [&](int i) { return okey(u[i].x); })
-                                       : okey(NEG_INF);
-    // stable ballot compaction of the entries >= g
+    uint32_t gkey = okey(NEG_INF);
+    if (total >= k) {
+        uint32_t prefix = 0;
+        constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+        for (int bit = 31; bit >= lo; --bit) {
+            const uint32_t want = prefix | (1u << bit);
+            unsigned c = 0;
+#pragma unroll
+            for (int j = 0; j < TK_KPL; ++j) c += key[j] >= want;
+            if ((int)__reduce_add_sync(FULL, c) >= k) prefix = want;
+        }
+        if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+        gkey = prefix;
+    }
+    // compaction of the entries >= g (any order; sorted below)
     int nk = 0;
-    for (int i0 = 0; i0 < total; i0 += 32) {
-        const int i = i0 + lane;
-        const bool keep = i < total && okey(u[i].x) >= gkey;
+#pragma unroll
+    for (int j = 0; j < TK_KPL; ++j) {
+        const bool keep = 32 * j + lane < total && key[j] >= gkey;
         const unsigned bal = __ballot_sync(FULL, keep);
         const int pos = nk + __popc(bal & ((1u << lane) - 1u));
-        if (keep && pos < P.cap_k) kept[pos] = u[i];
+        if (keep && pos < P.cap_k) {
+            TopkEntry e;
+            e.x = key_value(key[j]);
+            e.idx = ix[j];
+            kept[pos] = e;
+        }
         nk += __popc(bal);
     }
     __syncwarp();
@@ -623,15 +657,13 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
 template <int DT>
 __global__ void __launch_bounds__(NT) topk_finish_kernel(SpecParams P)
 {
-    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: u[nsegr*cap_s], kept[cap_k]
+    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: kept[cap_k]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x;
-    const int per = P.nsegr * P.cap_s + P.cap_k;
-    TopkEntry* u = fin + (size_t)warp * per;
-    TopkEntry* kept = u + P.nsegr * P.cap_s;
+    TopkEntry* kept = fin + (size_t)warp * P.cap_k;
     for (int r = warp; r < P.R; r += WARPS) {
         const int row_id = b * P.R + r;
-        const RowStats st = topk_row_finish<DT>(P, u, kept, row_id);
+        const RowStats st = topk_row_finish<DT>(P, kept, row_id);
         if (lane == 0) P.rstats[row_id] = st;
     }
     __syncthreads();
@@ -816,7 +848,7 @@ static void set_smem_limit(size_t smem)
 template <int DT>
 static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
 {
-    const long long nsegs = (long long)P.B * P.R * P.nsegr;
+    const long long nsegs = (long long)P.B * P.R * P.nsegr;  // < 2^31 (checked on the host)
     if (P.vec > 1) {
         constexpr auto K1 = topk_stream_kernel<DT, true>;
         K1<<<cta_grid<K1>(nsegs, sms, TK_SMEM), NT, TK_SMEM, st>>>(P);
@@ -824,7 +856,7 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
         constexpr auto K1 = topk_stream_kernel<DT, false>;
         K1<<<cta_grid<K1>(nsegs, sms, 0), NT, 0, st>>>(P);
     }
-    const size_t fsm = (size_t)WARPS * (P.nsegr * P.cap_s + P.cap_k) * sizeof(TopkEntry);
+    const size_t fsm = (size_t)WARPS * P.cap_k * sizeof(TopkEntry);
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
     topk_finish_kernel<DT><<<(unsigned)P.B, NT, fsm, st>>>(P);
     topk_dense_kernel<DT><<<(unsigned)((long long)P.B * P.R), NT, 0, st>>>(P);
