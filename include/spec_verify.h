@@ -187,6 +187,18 @@ spec_status spec_verify_noalloc(const void* target_logits, const void* draft_log
                                 float* aux_lse_p, float* aux_lse_q, float* aux_accept,
                                 void* stream);
 
+/*
+ * Measurement aid.  With both events non-NULL (cudaEvent_t created by the caller), every later
+ * verify call records `start` on its stream just before launching the call's dominant kernel and
+ * `stop` just after it, so that the caller can time that kernel alone with cudaEventElapsedTime:
+ *   spec_verify        the row-statistics (one-pass normaliser) kernel
+ *   spec_verify_topk   the streaming top-k kernel
+ *   tree_verify_greedy the argmax kernel
+ * spec_set_kernel_events(NULL, NULL) turns it off.  The setting is process-wide and not
+ * synchronised: set it from the thread that issues the calls.
+ */
+void spec_set_kernel_events(void* start, void* stop);
+
 /* Static description of a call-level status code. */
 const char* spec_status_string(spec_status s);
 

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     SpecVerifyError,
     Workspace,
     load,
+    set_kernel_events,
     spec_verify,
     spec_verify_noalloc,
     spec_verify_topk,

@@ -19,7 +19,7 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM = 5, 6, 7
 
 # every symbol the header declares
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
-           "spec_verify_noalloc", "spec_status_string")
+           "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -53,6 +53,8 @@ def load(path: str | None = None):
     lib.tree_verify_greedy.restype = I
     lib.spec_verify_noalloc.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P]
     lib.spec_verify_noalloc.restype = I
+    lib.spec_set_kernel_events.argtypes = [P, P]
+    lib.spec_set_kernel_events.restype = None
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -111,6 +113,18 @@ def _workspace(ws, device):
     if key not in _default_ws:
         _default_ws[key] = Workspace(device)
     return _default_ws[key]
+
+
+def set_kernel_events(start=None, stop=None):
+    """Time the dominant kernel of later calls: torch.cuda.Event pair (recorded around it on the
+    call's stream), or None to stop."""
+    if start is None or stop is None:
+        load().spec_set_kernel_events(None, None)
+        return
+    for e in (start, stop):
+        if not e.cuda_event:
+            e.record()  # creates the underlying CUDA event
+    load().spec_set_kernel_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
 
 
 def workspace_bytes(B, gamma, V, top_k=0, tree_nodes=0) -> int:

@@ -10,6 +10,8 @@
 
 namespace sv {
 
+KernelEvents g_kernel_events;
+
 constexpr size_t ALIGN = 256;
 static inline size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 static inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
@@ -359,6 +361,12 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
     const cudaError_t err = launch_tree_path(P, sm_count(), st);
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+void spec_set_kernel_events(void* start, void* stop)
+{
+    g_kernel_events.start = static_cast<cudaEvent_t>(start);
+    g_kernel_events.stop = static_cast<cudaEvent_t>(stop);
 }
 
 const char* spec_status_string(spec_status s)

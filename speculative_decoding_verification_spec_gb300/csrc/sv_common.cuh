@@ -582,6 +582,21 @@ inline unsigned persistent_grid(long long tasks, int sms, int threads = NT, size
     return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
+// Measurement aid (spec_set_kernel_events): events recorded on the call's stream around the
+// call's dominant kernel, or none.
+struct KernelEvents {
+    cudaEvent_t start = nullptr, stop = nullptr;
+};
+extern KernelEvents g_kernel_events;
+inline void mark_kernel_start(cudaStream_t st)
+{
+    if (g_kernel_events.start && g_kernel_events.stop) cudaEventRecord(g_kernel_events.start, st);
+}
+inline void mark_kernel_stop(cudaStream_t st)
+{
+    if (g_kernel_events.start && g_kernel_events.stop) cudaEventRecord(g_kernel_events.stop, st);
+}
+
 // spec_stats_kernel + spec_resample_kernel for the dtype / vector width in P
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st);
 // topk_stream_kernel + topk_finish_kernel + topk_dense_kernel

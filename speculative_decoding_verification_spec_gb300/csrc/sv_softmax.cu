@@ -543,14 +543,18 @@ __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
 template <int DT, int VEC>
 static void launch_softmax_plain(const SpecParams& P, int sms, cudaStream_t st)
 {
+    mark_kernel_start(st);
     spec_stats_kernel<DT, VEC><<<persistent_grid<spec_stats_kernel<DT, VEC>>(P.tasks1, sms), NT, 0, st>>>(P);
+    mark_kernel_stop(st);
     spec_resample_kernel<DT, VEC><<<persistent_grid<spec_resample_kernel<DT, VEC>>(P.tasks2, sms), NT, 0, st>>>(P);
 }
 
 template <int DT>
 static void launch_softmax_chunk(const SpecParams& P, cudaStream_t st)
 {
+    mark_kernel_start(st);
     spec_stats_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.R * P.S1), NT, 0, st>>>(P);
+    mark_kernel_stop(st);
     spec_resample_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.S2), NT, 0, st>>>(P);
 }
 

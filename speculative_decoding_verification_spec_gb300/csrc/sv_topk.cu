@@ -203,6 +203,7 @@ __device__ __forceinline__ uint32_t valid_bits(int cbase, int cend, int g)
 
 constexpr int TK_BINS = 256;  // histogram of candidate values above a segment's first bound
 static_assert(TK_BINS == NT, "one bin per thread to clear");
+constexpr int TK_HIST_CHUNKS = 4;          // chunks of a segment that refine its bound
 constexpr int TK_KPL = 32;                 // union entries per lane in the finish kernel
 constexpr int TK_UNION = 32 * TK_KPL;      // entries of all candidate lists of a row
 
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
             // chunk may be partly in: every count is a real element of the segment either way)
             if (warp == HW) {
                 float nb = NEG_INF;
-                if (!seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
+                if (!seg_bad && k <= NT && st + 1 < nst && st < TK_HIST_CHUNKS && tau_first != NEG_INF) {
                     int c8 = 0;
                     int hb[TK_BINS / 32];
 #pragma unroll
@@ -469,6 +470,8 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                         nb = key_value(key0 + ((uint32_t)bin << 16));
                     }
                 }
+                // past the first chunks the bound is left as it is (carried to the next slot)
+                if (st >= TK_HIST_CHUNKS && pub_seg[it & 1] == sg) nb = pub_beta[it & 1];
                 if (lane == 0) {
                     pub_beta[(it + 1) & 1] = nb;
                     pub_seg[(it + 1) & 1] = (nb != NEG_INF) ? sg : -1;
@@ -527,9 +530,10 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                             }
                             if (pos < P.cap_s) wlist[pos] = en;
                             ++pos;
-                            const uint32_t kx = okey(en.x);
-                            if (tau_first != NEG_INF && kx >= key0)
-                                atomicAdd(&h[min((int)((kx - key0) >> 16), TK_BINS - 1)], 1);
+                            if (st < TK_HIST_CHUNKS - 1 && tau_first != NEG_INF) {
+                                const uint32_t kx = okey(en.x);
+                                if (kx >= key0) atomicAdd(&h[min((int)((kx - key0) >> 16), TK_BINS - 1)], 1);
+                            }
                         }
                     }
                 }
@@ -849,6 +853,7 @@ template <int DT>
 static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
 {
     const long long nsegs = (long long)P.B * P.R * P.nsegr;  // < 2^31 (checked on the host)
+    mark_kernel_start(st);
     if (P.vec > 1) {
         constexpr auto K1 = topk_stream_kernel<DT, true>;
         K1<<<cta_grid<K1>(nsegs, sms, TK_SMEM), NT, TK_SMEM, st>>>(P);
@@ -856,6 +861,7 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
         constexpr auto K1 = topk_stream_kernel<DT, false>;
         K1<<<cta_grid<K1>(nsegs, sms, 0), NT, 0, st>>>(P);
     }
+    mark_kernel_stop(st);
     const size_t fsm = (size_t)WARPS * P.cap_k * sizeof(TopkEntry);
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
     topk_finish_kernel<DT><<<(unsigned)P.B, NT, fsm, st>>>(P);

@@ -305,13 +305,17 @@ __global__ void __launch_bounds__(NT) tree_argmax_chunk_kernel(TreeParams P)
 template <int DT, int VEC>
 static void launch_tree_plain(const TreeParams& P, int sms, cudaStream_t st)
 {
+    mark_kernel_start(st);
     tree_argmax_kernel<DT, VEC><<<persistent_grid<tree_argmax_kernel<DT, VEC>>(P.tasks, sms), NT, 0, st>>>(P);
+    mark_kernel_stop(st);
 }
 
 template <int DT>
 static void launch_tree_chunk(const TreeParams& P, cudaStream_t st)
 {
+    mark_kernel_start(st);
     tree_argmax_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.R * P.S1), NT, 0, st>>>(P);
+    mark_kernel_stop(st);
 }
 
 cudaError_t launch_tree_path(const TreeParams& P, int sms, cudaStream_t st)
