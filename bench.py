@@ -56,12 +56,35 @@ def workload_batches(names, rank, requests=None):
     out = {}
     for n in names:
         cfg = S.CONFIGS[n] if n in S.CONFIGS else S.TREE_CONFIGS[n]
-        kw = dict(seed=cfg.seed + 7919 * rank)
+        kw = dict(seed=rank_seed(cfg, rank))
         if requests:
             kw["B"] = requests
         cfg = S.scaled(cfg, **kw)
         out[n] = S.make_spec_batch(cfg) if n in S.CONFIGS else S.make_tree_batch(cfg)
     return out
+
+
+# ------------------------------------------------------------------ ranks
+
+def rank_seed(cfg, rank: int) -> int:
+    """Each rank verifies its own requests: the configuration's seed offset by the rank."""
+    return cfg.seed + 7919 * rank
+
+
+def dist_max(x: float, world: int, device) -> float:
+    """The maximum of x over all ranks (x itself on one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step_per_rank: float, world: int, steps: int, elapsed_max: float) -> float:
+    """Units all ranks processed per second of the slowest rank (weak scaling)."""
+    return units_per_step_per_rank * world * steps / elapsed_max
 
 
 def describe(names):
@@ -288,11 +311,7 @@ def run_ours(args, rank, world, local_rank):
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    elapsed = start.elapsed_time(end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = dist_max(start.elapsed_time(end) / 1e3, world, dev)
     call_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
 
@@ -326,13 +345,9 @@ def run_ours(args, rank, world, local_rank):
         s1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e_el = s0.elapsed_time(s1) / 1e3
-        if world > 1:
-            t = torch.tensor([e_el], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_el = float(t.item())
+        e_el = dist_max(s0.elapsed_time(s1) / 1e3, world, dev)
         rows_step = sum(batches[n].rows for n in names)
-        e2e = {"value": rows_step * world * e2e_steps / e_el, "unit": "rows/s",
+        e2e = {"value": whole_job_rate(rows_step, world, e2e_steps, e_el), "unit": "rows/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": e2e_steps}
 
@@ -356,7 +371,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = batches[dom_cfg].logit_bytes / (kernel_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
-        "value": rows_step * world * args.steps / elapsed,
+        "value": whole_job_rate(rows_step, world, args.steps, elapsed),
         "unit": "rows/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -400,17 +415,18 @@ def run_reference(args, rank, world):
     from oracle import oracle as O
     O.build()
     batches = workload_batches(names, 0)
-    # each step verifies a bounded sample of every workload: one request each
+    # each step verifies a bounded sample: one request of one workload, the workloads in turn, so
+    # that the default --steps run ends within a few minutes on one host core
     def step(i):
         rows = 0
-        for n in names:
+        for n in (names[i % len(names)],):
             b = batches[n]
             if hasattr(b, "parents"):
-                j = i % b.logits.shape[0]
+                j = (i // len(names)) % b.logits.shape[0]
                 O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
                 rows += b.logits.shape[1]
             else:
-                j = i % b.cfg.B
+                j = (i // len(names)) % b.cfg.B
                 O.spec_verify(b.target[j:j + 1], b.draft[j:j + 1], b.draft_tokens[j:j + 1],
                               b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.top_k)
                 rows += 2 * b.cfg.gamma + 1
@@ -429,9 +445,9 @@ def run_reference(args, rank, world):
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": describe(names), "input_dtype": "bf16",
-                       "sample_per_step": "one request of each workload"},
+                       "sample_per_step": "one request of one workload, the workloads in turn"},
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": "one request of each workload per step, single thread"},
+                             "sample": "one request of one workload per step (in turn), single thread"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
