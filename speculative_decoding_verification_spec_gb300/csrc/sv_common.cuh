@@ -48,6 +48,10 @@ struct RowStats {     // one logit row after its chunks are combined
     int status;       // ROW_OK or ROW_NONFINITE
     int klist_n;      // top-k: number of kept (index, value) pairs listed, -1 if not listed
     int dense;        // top-k: row needs the exact fallback path
+    // filled in advance by the top-k finish kernel (the plan reads them when `pre` is set)
+    float lse;        // natural-log normaliser of logits / T over the kept tokens
+    float invS;       // fp32(1 / S)
+    double lx;        // log2 p(x) of the token this row scores (NaN: none, or out of range)
 };
 
 struct Plan {         // one request, after the acceptance scan

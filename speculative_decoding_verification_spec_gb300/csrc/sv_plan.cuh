@@ -25,6 +25,9 @@ __device__ __forceinline__ RowStats ld_rowstats(const RowStats* p)
     r.status = __ldcg(&p->status);
     r.klist_n = __ldcg(&p->klist_n);
     r.dense = __ldcg(&p->dense);
+    r.lse = __ldcg(&p->lse);
+    r.invS = __ldcg(&p->invS);
+    r.lx = __ldcg(&p->lx);
     return r;
 }
 
@@ -62,8 +65,10 @@ __device__ __forceinline__ float row_lse(const RowStats& rs, float c, double T)
 }
 
 // Computes the plan of request b.  Must be called by all 32 lanes of one warp; every lane gets the
-// plan.  Writes the aux outputs (lse per row, accept ratio per position).
-template <int DT>
+// plan.  Writes the aux outputs (lse per row, accept ratio per position).  With PRE the rows' lse,
+// 1/S and log2 p(x) of their scoring tokens come from RowStats (filled by whoever finished the
+// rows) instead of being computed here.
+template <int DT, bool PRE = false>
 __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
 {
     const int g = P.gamma, R = P.R, lane = threadIdx.x & 31;
@@ -74,7 +79,8 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
         RowStats rs = ld_rowstats(P.rstats + (size_t)b * R + r);
         if (rs.status != ROW_OK) bad = 1;
         if (rs.status == ROW_TIMEOUT) tmo = 1;
-        const float lse = row_lse(rs, P.c, P.T);
+        const float lse = PRE ? (rs.status == ROW_OK ? rs.lse : __int_as_float(0x7fc00000))
+                              : row_lse(rs, P.c, P.T);
         if (r <= g) {
             if (P.aux_lse_p) P.aux_lse_p[(size_t)b * (g + 1) + r] = lse;
         } else if (P.aux_lse_q) {
@@ -91,15 +97,26 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
     for (int i = lane; i < g; i += 32) {
         const int x = P.tokens[(size_t)b * g + i];
         double a = __longlong_as_double(0x7ff8000000000000ll);
+        double plp = 0.0, plq = 0.0;
+        if constexpr (PRE) {
+            plp = __ldcg(&P.rstats[(size_t)b * R + i].lx);
+            plq = __ldcg(&P.rstats[(size_t)b * R + g + 1 + i].lx);
+        }
         if (x < 0 || x >= P.V) {
             badtok = 1;
         } else if (!nonfinite) {
-            const RowStats rp = ld_rowstats(P.rstats + (size_t)b * R + i);
-            const RowStats rq = ld_rowstats(P.rstats + (size_t)b * R + g + 1 + i);
-            const float xp = load_logit(spec_row_ptr(P, b, i), DT, x);
-            const float xq = load_logit(spec_row_ptr(P, b, g + 1 + i), DT, x);
-            const double lp = row_log2prob(xp, rp, P.c, topk);
-            const double lq = row_log2prob(xq, rq, P.c, topk);
+            double lp, lq;
+            if constexpr (PRE) {
+                lp = plp;
+                lq = plq;
+            } else {
+                const RowStats rp = ld_rowstats(P.rstats + (size_t)b * R + i);
+                const RowStats rq = ld_rowstats(P.rstats + (size_t)b * R + g + 1 + i);
+                const float xp = load_logit(spec_row_ptr(P, b, i), DT, x);
+                const float xq = load_logit(spec_row_ptr(P, b, g + 1 + i), DT, x);
+                lp = row_log2prob(xp, rp, P.c, topk);
+                lq = row_log2prob(xq, rq, P.c, topk);
+            }
             if (lq == -INFINITY) {
                 badtok = 1;  // q(x) = 0: the draft cannot have proposed x
             } else {
@@ -124,12 +141,12 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
     pl.rq = (pl.A < g) ? g + 1 + pl.A : -1;
     const RowStats sp = ld_rowstats(P.rstats + (size_t)b * R + pl.rp);
     pl.MCp = sp.MC;
-    pl.invSp = (float)(1.0 / sp.S);
+    pl.invSp = PRE ? sp.invS : (float)(1.0 / sp.S);
     pl.thrp = sp.thr;
     if (pl.rq >= 0) {
         const RowStats sq = ld_rowstats(P.rstats + (size_t)b * R + pl.rq);
         pl.MCq = sq.MC;
-        pl.invSq = (float)(1.0 / sq.S);
+        pl.invSq = PRE ? sq.invS : (float)(1.0 / sq.S);
         pl.thrq = sq.thr;
     } else {
         pl.MCq = 0.f;

@@ -19,11 +19,11 @@
 // what remains.  Every bound is <= the row's k-th largest value g, so the lists hold every
 // element >= g.
 //
-// Kernel 2 (topk_finish_kernel), one CTA per request: one warp per row selects g exactly from the
-// union of the row's segment lists, keeps the entries >= g sorted by index and forms the
-// normaliser (M, S).  Then one warp runs the acceptance scan and draws the correction or bonus
-// token directly from the kept list of the p row: the residual vanishes outside K_p, so no second
-// pass over V is needed.
+// Kernel 2 (topk_finish_kernel), one warp per row, selects g exactly from the union of the row's
+// candidate lists, keeps the entries >= g sorted by index and forms the normaliser (M, S).  The
+// last warp to finish a row of a request runs the acceptance scan and draws the correction or
+// bonus token directly from the kept list of the p row: the residual vanishes outside K_p, so no
+// second pass over V is needed.
 //
 // Rows whose candidates overflow the capacities (massive ties, k > NT, ...) are marked dense and
 // finished exactly by kernel 3 (topk_dense_kernel) with full-row passes.
@@ -116,12 +116,12 @@ __device__ void warp_sort_by_index(TopkEntry* e, int n)
 
 // One warp: acceptance scan of request b and the correction / bonus draw from the kept list of
 // the p row (index order); the residual is zero outside K_p.
-template <int DT>
+template <int DT, bool PRE = false>
 __device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
-    const Plan pl = compute_plan_warp<DT>(P, b, true);
+    const Plan pl = compute_plan_warp<DT, PRE>(P, b, true);
     if (pl.status != ROW_OK) {
         emit_spec_warp(P, b, pl.status, 0, -1);
         return;
@@ -134,18 +134,36 @@ __device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
     const int per = (nk + 31) / 32;
     const int i0 = min(lane * per, nk), i1 = min(i0 + per, nk);
     double mine = 0.0;
-    for (int i = i0; i < i1; ++i) {
-        const float xp = __ldcg(&kl[i].x);
-        const int v = __ldcg(&kl[i].idx);
-        const float pp = __fmul_rn(ex2(fmaf(xp, P.c, -pl.MCp)), pl.invSp);
-        float res = pp;
-        if (rowq) {
-            const float xq = load_logit(rowq, DT, v);
-            const float qq = (xq >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq, P.c, -pl.MCq)), pl.invSq) : 0.f;
-            res = fmaxf(__fsub_rn(pp, qq), 0.f);
+    for (int b0 = i0; b0 < i1; b0 += 8) {
+        // eight entries at a time: their list loads, then their q gathers, each batch in flight
+        // together, then the residual in list order
+        float xp[8], xq[8];
+        int v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (b0 + t < i1) {
+                xp[t] = __ldcg(&kl[b0 + t].x);
+                v[t] = __ldcg(&kl[b0 + t].idx);
+            }
         }
-        rr[i] = (double)res;
-        mine += (double)res;
+        if (rowq) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (b0 + t < i1) xq[t] = load_logit(rowq, DT, v[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (b0 + t < i1) {
+                const float pp = __fmul_rn(ex2(fmaf(xp[t], P.c, -pl.MCp)), pl.invSp);
+                float res = pp;
+                if (rowq) {
+                    const float qq = (xq[t] >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq[t], P.c, -pl.MCq)), pl.invSq) : 0.f;
+                    res = fmaxf(__fsub_rn(pp, qq), 0.f);
+                }
+                rr[b0 + t] = (double)res;
+                mine += (double)res;
+            }
+        }
     }
     const double incl = warp_incl_scan(mine);
     const double Z = __shfl_sync(FULL, incl, 31);
@@ -199,6 +217,83 @@ __device__ __forceinline__ uint32_t valid_bits(int cbase, int cend, int g)
         for (int h = 0; h < PER; ++h)
             if (slot_elem<VEC>(cbase, PER * (8 * g + j) + h) < cend) m |= 1u << (j + 16 * h);
     return m;
+}
+
+// The k-th largest (with multiplicity) of the keys key[j] (slots j < J, lanes with 32 j + lane <
+// total), by one warp: a radix select over 8-bit digits, each digit resolved by a 256-bin histogram
+// in shared memory (hist: 256 ints of this warp) and a suffix sum over it.  The digits start at
+// the highest bit in which the keys differ (the bits above are common to all of them), so values
+// spread over a narrow range take one pass.  Bits below 16 of bf16-valued keys never differ.
+template <int DT, int KPL>
+__device__ uint32_t warp_kth_key_hist(const uint32_t (&key)[KPL], int J, int total, int k, int* hist)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j)
+        if (j < J && 32 * j + lane < total) {
+            kmin = min(kmin, key[j]);
+            kmax = max(kmax, key[j]);
+        }
+    kmin = __reduce_min_sync(FULL, kmin);
+    kmax = __reduce_max_sync(FULL, kmax);
+    const uint32_t diff = kmin ^ kmax;
+    if (diff == 0u) return kmax;
+    const int hd = 31 - __clz(diff);  // highest differing bit
+    const uint32_t common = (hd == 31) ? 0u : ~((2u << hd) - 1u);
+    uint32_t prefix = kmax & common, mask = common;
+    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+    int kk = k;  // rank sought among the keys that match the prefix
+#pragma unroll 1
+    for (int shift = hd - 7; shift + 8 > lo; shift -= 8) {
+        const uint32_t dmask = shift >= 0 ? (255u << shift) : (255u >> -shift);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0;
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < KPL; ++j)
+            if (j < J && 32 * j + lane < total && (key[j] & mask) == prefix) {
+                const uint32_t dg = shift >= 0 ? (key[j] >> shift) & 255u : (key[j] << -shift) & 255u;
+                atomicAdd(&hist[dg], 1);
+            }
+        __syncwarp();
+        int h8[8], c8 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            h8[i] = hist[lane * 8 + i];
+            c8 += h8[i];
+        }
+        int suf = c8;  // counts in this lane's bins and above
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_down_sync(FULL, suf, o);
+            if (lane + o < 32) suf += v;
+        }
+        const unsigned reach = __ballot_sync(FULL, suf >= kk);
+        const int ls = reach ? 31 - __clz(reach) : 0;
+        int bin = 0, above = 0;
+        if (lane == ls) {
+            int acc = suf - c8;
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                if (acc + h8[i] >= kk) {
+                    bin = lane * 8 + i;
+                    above = acc;
+                    break;
+                }
+                acc += h8[i];
+            }
+        }
+        bin = __shfl_sync(FULL, bin, ls);
+        above = __shfl_sync(FULL, above, ls);
+        kk -= above;
+        prefix |= shift >= 0 ? ((uint32_t)bin << shift) : ((uint32_t)bin >> -shift);
+        mask |= dmask;
+        __syncwarp();
+    }
+    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+    return prefix;
 }
 
 constexpr int TK_BINS = 256;  // histogram of candidate values above a segment's first bound
@@ -553,19 +648,29 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
 }
 
 // Kernel 2, one warp per row: exact threshold g over the union of the row's lists (nsegr segments
-// x WARPS warps, up to TK_UNION entries, held in registers), the kept list sorted by index, and
-// the normaliser over it.  kept holds cap_k entries.
+// x WARPS warps of kernel 1, up to TK_UNION entries), the kept list sorted by index, and the
+// normaliser over it.  u holds TK_UNION entries, kept cap_k.
 template <int DT>
-__device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* kept, int row_id)
+__device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry* kept, int row_id)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
     RowStats st;
     st.M = NEG_INF; st.MC = NEG_INF; st.S = 0.0; st.thr = NEG_INF;
     st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
+    st.lse = __int_as_float(0x7fc00000);
+    st.invS = 0.f;
+    st.lx = __longlong_as_double(0x7ff8000000000000ll);
     const int nl = P.nsegr * WARPS;  // lists of the row, <= 32
     const int* cnt = P.ccount + (size_t)row_id * nl;
     const TopkEntry* lists = P.clist + (size_t)row_id * nl * P.cap_s;
+    // the token this row scores (target row i and draft row i score draft token i; the last target
+    // row scores none) and its logit, fetched now so that they arrive while the lists are read
+    const int b = row_id / P.R, r = row_id - b * P.R, g = P.gamma;
+    const int pos = (r < g) ? r : (r > g) ? r - g - 1 : -1;
+    const int tok = (pos >= 0) ? __ldg(P.tokens + (size_t)b * g + pos) : -1;
+    const bool tok_ok = tok >= 0 && tok < P.V;
+    const float xtok = tok_ok ? load_logit(spec_row_ptr(P, b, r), DT, tok) : 0.f;
 
     int n = (lane < nl) ? __ldcg(cnt + lane) : 0;
     int flag = 0;
@@ -577,101 +682,120 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* kept, int ro
     if (flag & 1) { st.status = ROW_NONFINITE; return st; }
     if (flag & 2) { st.dense = 1; return st; }
     n = max(0, min(n, P.cap_s));
-    const int incl = warp_incl_scan(n);  // entries of lists 0..lane
+    const int incl = warp_incl_scan(n);
+    const int excl = incl - n;
     const int total = __shfl_sync(FULL, incl, 31);
+    const int nmax = (int)__reduce_max_sync(FULL, (unsigned)n);
     if (total > TK_UNION) { st.dense = 1; return st; }
-    // the union in registers: entry f = 32 j + lane, found in list q (the first with incl > f)
-    uint32_t key[TK_KPL];
-    int ix[TK_KPL];
+
+    // the lists, packed into u: four lists at a time, every load of a batch issued before any store
+    for (int l0 = 0; l0 < nl; l0 += 4) {
+        for (int i0 = 0; i0 < nmax; i0 += 64) {
+            TopkEntry e[8];
+            bool v[8];
 #pragma unroll
-    for (int j = 0; j < TK_KPL; ++j) {
-        const int f = 32 * j + lane;
-        key[j] = 0u;  // below every key a value can have
-        ix[j] = 0;
-        if (32 * j < total) {
-            int lo = 0, hi = 31;
-#pragma unroll
-            for (int step = 0; step < 5; ++step) {
-                const int mid = (lo + hi) >> 1;
-                if (__shfl_sync(FULL, incl, mid) > f) hi = mid;
-                else lo = mid + 1;
+            for (int t = 0; t < 8; ++t) {
+                const int l = l0 + (t >> 1), i = i0 + 32 * (t & 1) + lane;
+                const int nn = __shfl_sync(FULL, n, l & 31);
+                v[t] = l < nl && i < nn;
+                if (v[t]) {
+                    const TopkEntry* src = lists + (size_t)l * P.cap_s + i;
+                    e[t].x = __ldcg(&src->x);
+                    e[t].idx = __ldcg(&src->idx);
+                }
             }
-            const int q = lo;
-            const int start = __shfl_sync(FULL, incl - n, q);
-            if (f < total) {
-                const TopkEntry* src = lists + (size_t)q * P.cap_s + (f - start);
-                key[j] = okey(__ldcg(&src->x));
-                ix[j] = __ldcg(&src->idx);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int l = l0 + (t >> 1), i = i0 + 32 * (t & 1) + lane;
+                const int off = __shfl_sync(FULL, excl, l & 31);
+                if (v[t]) u[off + i] = e[t];
             }
         }
+    }
+    __syncwarp();
+
+    // exact k-th largest key over the packed union, keys in registers (occupied slots only)
+    const int J = (total + 31) >> 5;
+    uint32_t key[TK_KPL];
+#pragma unroll
+    for (int j = 0; j < TK_KPL; ++j) {
+        key[j] = 0u;  // below every key a value can have
+        if (j < J && 32 * j + lane < total) key[j] = okey(u[32 * j + lane].x);
     }
     const int k = P.top_k;
     uint32_t gkey = okey(NEG_INF);
-    if (total >= k) {
-        uint32_t prefix = 0;
-        constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-        for (int bit = 31; bit >= lo; --bit) {
-            const uint32_t want = prefix | (1u << bit);
-            unsigned c = 0;
-#pragma unroll
-            for (int j = 0; j < TK_KPL; ++j) c += key[j] >= want;
-            if ((int)__reduce_add_sync(FULL, c) >= k) prefix = want;
-        }
-        if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-        gkey = prefix;
-    }
-    // compaction of the entries >= g (any order; sorted below)
+    if (total >= k) gkey = warp_kth_key_hist<DT, TK_KPL>(key, J, total, k, reinterpret_cast<int*>(kept));
+    // the entries >= g, in union order
     int nk = 0;
 #pragma unroll
     for (int j = 0; j < TK_KPL; ++j) {
-        const bool keep = 32 * j + lane < total && key[j] >= gkey;
-        const unsigned bal = __ballot_sync(FULL, keep);
-        const int pos = nk + __popc(bal & ((1u << lane) - 1u));
-        if (keep && pos < P.cap_k) {
-            TopkEntry e;
-            e.x = key_value(key[j]);
-            e.idx = ix[j];
-            kept[pos] = e;
+        if (j < J) {
+            const bool keep = 32 * j + lane < total && key[j] >= gkey;
+            const unsigned bal = __ballot_sync(FULL, keep);
+            const int pos = nk + __popc(bal & ((1u << lane) - 1u));
+            if (keep && pos < P.cap_k) kept[pos] = u[32 * j + lane];
+            nk += __popc(bal);
         }
-        nk += __popc(bal);
     }
     __syncwarp();
     if (nk > P.cap_k) { st.dense = 1; return st; }
-    warp_sort_by_index(kept, nk);
+    // sorted by index (the indices are distinct): each entry's rank is the number of smaller ones;
+    // the sorted list goes back into u
+    for (int i0 = 0; i0 < nk; i0 += 32) {
+        const int i = i0 + lane;
+        TopkEntry e;
+        e.idx = 0x7fffffff;
+        e.x = NEG_INF;
+        if (i < nk) e = kept[i];
+        int rank = 0;
+        for (int j = 0; j < nk; ++j) rank += kept[j].idx < e.idx;
+        if (i < nk) u[rank] = e;
+    }
+    __syncwarp();
     float mx = NEG_INF;
-    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, kept[i].x);
+    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, u[i].x);
     const float M = warp_max(mx);
     const float MC = M * P.c;
     double acc = 0.0;
     if (M != NEG_INF)
-        for (int i = lane; i < nk; i += 32) acc += (double)ex2(fmaf(kept[i].x, P.c, -MC));
+        for (int i = lane; i < nk; i += 32) acc += (double)ex2(fmaf(u[i].x, P.c, -MC));
     const double S = warp_sum(acc);
     TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
-    for (int i = lane; i < nk; i += 32) kl[i] = kept[i];
+    for (int i = lane; i < nk; i += 32) kl[i] = u[i];
     st.M = M;
     st.MC = MC;
     st.S = S;
     st.thr = key_value(gkey);
     st.klist_n = nk;
     st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
+    if (st.status == ROW_OK) {
+        // log2 S from S = m 2^e, m in [0.5, 1): an fp32 log2 of m (absolute error ~1e-7) plus e,
+        // which keeps the fp64 pipe (slow on this part) out of the per-row work
+        int e;
+        const double m = frexp(S, &e);
+        const double l2S = (double)log2f((float)m) + (double)e;
+        const double exact = (double)M * (double)P.c;
+        st.lse = (float)((double)M / P.T + LN2 * (l2S - (exact - (double)MC)));
+        st.invS = __frcp_rn(__double2float_rn(S));
+        if (tok_ok) st.lx = (xtok >= st.thr) ? (double)fmaf(xtok, P.c, -MC) - l2S : -INFINITY;
+    }
     return st;
 }
 
-// Kernel 2: one CTA per request.  Warps take the request's rows; then one warp scans and draws.
+// Kernel 2: one warp per row; the last warp to finish a row of a request scans it and draws.
 template <int DT>
 __global__ void __launch_bounds__(NT) topk_finish_kernel(SpecParams P)
 {
-    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: kept[cap_k]
+    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: u[TK_UNION], kept[cap_k]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x;
-    TopkEntry* kept = fin + (size_t)warp * P.cap_k;
-    for (int r = warp; r < P.R; r += WARPS) {
-        const int row_id = b * P.R + r;
-        const RowStats st = topk_row_finish<DT>(P, kept, row_id);
-        if (lane == 0) P.rstats[row_id] = st;
-    }
-    __syncthreads();
-    if (warp != 0) return;
+    const int row_id = blockIdx.x * WARPS + warp;
+    if (row_id >= P.B * P.R) return;
+    const int b = row_id / P.R;
+    TopkEntry* u = fin + (size_t)warp * (TK_UNION + P.cap_k);
+    TopkEntry* kept = u + TK_UNION;
+    const RowStats st = topk_row_finish<DT>(P, u, kept, row_id);
+    if (lane == 0) P.rstats[row_id] = st;
+    if (!warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) return;
     int nd = 0;
     for (int rr = lane; rr < P.R; rr += 32) nd += __ldcg(&P.rstats[(size_t)b * P.R + rr].dense);
     nd = __reduce_add_sync(0xffffffffu, nd);
@@ -679,7 +803,7 @@ __global__ void __launch_bounds__(NT) topk_finish_kernel(SpecParams P)
         if (lane == 0) P.ndense[b] = nd;
         return;
     }
-    topk_request_epilogue<DT>(P, reinterpret_cast<double*>(fin), b);
+    topk_request_epilogue<DT, true>(P, reinterpret_cast<double*>(u), b);
 }
 
 // ---------------------------------------------------------------- exact fallback for dense rows
@@ -862,9 +986,9 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
         K1<<<cta_grid<K1>(nsegs, sms, 0), NT, 0, st>>>(P);
     }
     mark_kernel_stop(st);
-    const size_t fsm = (size_t)WARPS * P.cap_k * sizeof(TopkEntry);
+    const size_t fsm = (size_t)WARPS * (TK_UNION + P.cap_k) * sizeof(TopkEntry);
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
-    topk_finish_kernel<DT><<<(unsigned)P.B, NT, fsm, st>>>(P);
+    topk_finish_kernel<DT><<<(unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, fsm, st>>>(P);
     topk_dense_kernel<DT><<<(unsigned)((long long)P.B * P.R), NT, 0, st>>>(P);
 }
 
