@@ -41,8 +41,8 @@ SUITE = ("c3", "c4", "c5")
 # the sources it is built from
 KERNEL_OF = {
     "c1": ("spec_stats_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
-    "c2": ("spec_stats_chunk_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
-    "c3": ("spec_stats_chunk_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c2": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c3": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c4": ("topk_stream_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c5": ("tree_argmax_chunk_kernel", ["sv_tree.cu", "sv_common.cuh"]),
 }

@@ -33,10 +33,12 @@ static Shape row_shape(int V, int vec)
 
 static long long slices1(const Shape& s) { return std::max(1LL, cdiv(s.nvec, TV1)); }
 static long long chunks1(const Shape& s) { return std::max(1LL, cdiv(s.nvec, CHUNK_VECS)); }
-// softmax partials per row: one per warp task (scalar path) or one per warp of each chunk CTA
+// 32 KB chunks of a row of 16-byte vectors (the streaming kernels)
+static long long stream_chunks(const Shape& s) { return std::max(1LL, cdiv(s.nvec, (long long)NT * STREAM_NV)); }
+// softmax partials per row: one per warp task (scalar path) or one per warp of each stream chunk
 static long long partials_per_row(const Shape& s)
 {
-    return s.vec > 1 ? chunks1(s) * WARPS : slices1(s);
+    return s.vec > 1 ? stream_chunks(s) * WARPS : slices1(s);
 }
 static long long slices2(const Shape& s) { return std::max(1LL, cdiv(s.nvec, TV2)); }
 static long long nsegs(const Shape& s) { return std::max(1LL, cdiv(s.nvec, SEGV)); }
@@ -204,9 +206,9 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.B = B; P.gamma = gamma; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
     P.c = c; P.T = T; P.top_k = top_k;
-    // chunk kernels (16-byte vectors) take CHUNK_VECS / 2048 vectors per CTA; the scalar path's
-    // persistent warps take TV1 / TV2 vectors per task
-    P.S1 = (int)(vec > 1 ? chunks1(sh) : slices1(sh));
+    // 16-byte vectors: 32 KB stream chunks (statistics) and 2048-vector residual chunks; the
+    // scalar path's persistent warps take TV1 / TV2 vectors per task
+    P.S1 = (int)(vec > 1 ? stream_chunks(sh) : slices1(sh));
     P.S2 = (int)(vec > 1 ? std::max(1LL, cdiv(sh.nvec, NT * 8)) : slices2(sh));
     P.nseg = (int)nsegs(sh);
     P.tasks1 = (long long)B * R * P.S1;
@@ -222,6 +224,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.nsegr, P.cap_s, P.cap_k);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
     if ((long long)B * R * (topk ? P.CT : 1) >= (1LL << 31) || P.tasks1 >= (1LL << 31) ||
+        (long long)B * R * P.S1 >= (1LL << 31) ||
         (long long)B * R * TK_MAX_SEGR * WARPS >= (1LL << 31))
         return SPEC_ERR_INVALID_ARG;
 

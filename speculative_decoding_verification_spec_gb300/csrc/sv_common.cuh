@@ -12,6 +12,8 @@
 //     fp64, always in a fixed order, so results do not depend on CTA scheduling.
 #pragma once
 
+#include <utility>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -284,24 +286,6 @@ __device__ __forceinline__ void load_vec_pol(const char* row, long long v, uint6
     }
 }
 
-// ---------------------------------------------------------------- per-warp cp.async ring
-//
-// Each lane copies its own 16-byte vectors global -> shared with cp.async (L1 bypassed, L2 policy
-// hint) and later reads back exactly the vectors it copied, so a lane waits only on its own copy
-// groups (cp.async.wait_group): no cross-thread synchronisation and no flag waits.  PS stages of
-// U vectors per lane keep (PS-1) * U * 512 bytes per warp in flight while one stage is consumed.
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint64_t pol)
-{
-    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 :: "r"(d), "l"(gsrc), "l"(pol) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 __device__ __forceinline__ uint4 lds128(const uint4* p)
 {
     uint4 r;
@@ -355,29 +339,69 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
     return false;
 }
 
-// Chunk kernels: one CTA of NT threads per chunk of CHUNK_VECS vectors.  Thread t copies vectors
-// t + i*NT (i < CV) into shared slot i*NT + t with cp.async, CG commit groups of CV/CG vectors,
-// all issued before the first is consumed (64 KB per CTA in flight; three CTAs per SM).
+// Chunk kernels: one CTA of NT threads per chunk of CHUNK_VECS contiguous vectors; thread t reads
+// vectors t + i*NT (i < CV) into registers.
 constexpr int CV = 16;
-constexpr int CG = 4;
-constexpr int CVG = CV / CG;
 constexpr int CHUNK_VECS = NT * CV;
-constexpr size_t CHUNK_SMEM = (size_t)CHUNK_VECS * sizeof(uint4);
 
-// Ring kernels: CTAs of 8 warps; each warp owns PS stages of RU vectors per lane (2 KB per stage),
-// so three CTAs (24 warps, 192 KB) fit on an SM with ~144 KB of copies in flight.  A ring task is
-// RST steps of RU vectors per lane: the same TV1 = 1024 vectors as the plain kernels' tasks.
-constexpr int NT_RING = 256;
-constexpr int WARPS_RING = NT_RING / 32;
-constexpr int PS = 4;
-constexpr int RU = 4;
-constexpr int RST = TV1 / (32 * RU);
-constexpr int RING_VECS_PER_WARP = PS * RU * 32;  // uint4 per warp ring
-constexpr size_t RING_SMEM = (size_t)WARPS_RING * RING_VECS_PER_WARP * sizeof(uint4);
-static_assert(RST * 32 * RU == TV1, "ring task geometry");
-constexpr int RU2 = RU / 2;               // residual ring: RU2 vectors of p and of q per step
-constexpr int RST2 = TV2 / (32 * RU2);
-static_assert(RST2 * 32 * RU2 == TV2, "residual ring task geometry");
+// Streaming kernels: persistent CTAs (two per SM) fetch 32 KB chunks of one row with bulk copies
+// into a ring of STREAM_STAGES shared-memory stages; thread t reads vectors t + j*NT (j <
+// STREAM_NV) of a stage into registers.
+constexpr int STREAM_CHUNK_BYTES = 32768;
+constexpr int STREAM_NV = STREAM_CHUNK_BYTES / (NT * 16);  // 16-byte vectors per thread (8)
+constexpr int STREAM_STAGES = 3;
+constexpr int STREAM_SMEM = STREAM_STAGES * STREAM_CHUNK_BYTES;
+
+// persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task (the occupancy query
+// runs once per kernel)
+template <auto K>
+inline unsigned cta_grid(long long tasks, int sms, size_t smem)
+{
+    static int per_sm = 0;
+    if (per_sm < 1) {
+        int n = 0;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, NT, smem) != cudaSuccess || n < 1) n = 1;
+        per_sm = n;
+    }
+    const long long cap = (long long)per_sm * sms;
+    return (unsigned)(tasks < 1 ? 1 : (tasks < cap ? tasks : cap));
+}
+
+// Programmatic dependent launch: a kernel launched with launch_dependent may start while the
+// previous kernel on the stream is still running; before it reads anything that kernel wrote it
+// calls pdl_wait(), which returns once the previous grid has completed and its writes are visible
+// (a no-op for an ordinary launch).  pdl_trigger() lets the next grid launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t st, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// raises a kernel's dynamic shared-memory limit to `smem` when above the default
+template <auto K>
+inline void set_smem_limit(size_t smem)
+{
+    static size_t done = 0;
+    if (smem > 48 * 1024 && smem > done) {
+        cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        done = smem;
+    }
+}
 
 // One vector of a row kept as raw bits until it is used: 16 bytes (8 bf16 or 4 fp32) or a single
 // element for the unaligned path.

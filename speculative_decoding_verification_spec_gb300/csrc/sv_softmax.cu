@@ -1,13 +1,12 @@
 // sv_softmax.cu -- exact speculative sampling without top-k: one-pass row normalisers and the
 // residual / bonus inverse-CDF draw.
 //
-// Kernel 1 (row statistics): each lane keeps an online (max, sum of 2^(x*c - max*c)) pair -- the
-// online (m, l) merge over vocabulary blocks of M7.1 section 0x04J.  For rows of 16-byte vectors
-// one CTA takes a contiguous chunk of CHUNK_VECS vectors, loaded straight into registers, and each
-// warp writes one partial.  The last CTA of a row merges the row's partials (fp64, chunk order) and
-// the last row of a request runs the acceptance scan (sv_plan.cuh).  Completion is counted with
-// atomics; nothing waits.  Rows that are not 16-byte aligned use persistent warps with plain loads
-// instead.
+// Kernel 1 (row statistics).  Rows of 16-byte vectors: spec_stream_kernel, persistent CTAs that
+// fetch 32 KB chunks with bulk copies into a shared-memory ring and write one (max, sum of
+// 2^(x c - max c)) partial per (chunk, warp) -- the (m, l) pairs of M7.1 section 0x04J; then
+// spec_rowplan_kernel merges each row's partials (fp64, chunk order) with one warp per row, and
+// the last warp of a request runs the acceptance scan (sv_plan.cuh).  Rows that are not 16-byte
+// aligned use persistent warps with plain loads and do the same merge through completion counters.
 //
 // Kernel 2 (residual draw): r = max(p - q, 0) (M7.1 section 0x03C; p alone for the bonus, 0x03H)
 // over the selected row pair, summed per segment of 32 vectors; the last CTA of a request scans the
@@ -261,51 +260,212 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
     }
 }
 
-// Chunk kernel for 16-byte vectors: one CTA per (request, row, chunk of CHUNK_VECS contiguous
-// vectors).  Thread t loads vectors t + i*NT (i < CV), U1 at a time straight into registers, and
-// keeps its online (max, sum) pair; each warp writes its own partial (no block-wide reduction), and
-// the last CTA of a row merges the row's WARPS * S1 partials.
+// Streaming kernel for rows of 16-byte vectors: persistent CTAs take 32 KB chunks round-robin,
+// fetched by bulk copies (TMA engine) into a ring of STREAM_STAGES shared-memory stages, so the
+// next chunks are in flight while one is reduced.  Each warp reduces its part of a chunk -- the
+// maximum first, then the sum of 2^(x c - MC) with MC = fp32(M c) -- and writes one partial per
+// (chunk, warp).  The only synchronisation is the CTA barrier per chunk that frees the stage.
+// NaN or +inf anywhere makes the partial's sum NaN, so the row merge reports the row non-finite.
 template <int DT>
-__global__ void __launch_bounds__(NT) spec_stats_chunk_kernel(SpecParams P)
+__global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
 {
-    __shared__ int sh_flag;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = blockIdx.x % P.S1;
-    const int rr = blockIdx.x / P.S1;
-    const int r = rr % P.R, b = rr / P.R;
-    const char* row = spec_row_ptr(P, b, r);
-    const int c0 = c * CHUNK_VECS;
-    const int c1 = (int)min((long long)c0 + CHUNK_VECS, P.nvec);
-    const uint64_t pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
-    const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-    float m = NEG_INF, mc = NEG_INF, acc = 0.f;
+    constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
+    constexpr int ES = (DT == DT_BF16) ? 2 : 4;
+    constexpr int CHUNK = NT * STREAM_NV * VEC;  // elements per chunk
+    extern __shared__ __align__(128) uint4 ring[];  // STREAM_STAGES x (NT * STREAM_NV) vectors
+    __shared__ __align__(8) uint64_t full[STREAM_STAGES];
+
+    pdl_trigger();  // the row-merge kernel may be scheduled as SMs free up; it waits for this grid
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = P.B * P.R * P.S1;  // < 2^31 (checked on the host)
+    const int G0 = gridDim.x;
+    const float c = P.c;
+
+    // producer (thread 0): chunks blockIdx.x, + G0, ... in this CTA's consumption order
+    int pid = blockIdx.x;
+    long long nissued = 0;
+    auto issue_next = [&](int s) {
+        if (pid >= nch) return;
+        const int row_id = pid / P.S1, ci = pid - row_id * P.S1;
+        const int b = row_id / P.R, r = row_id - b * P.R;
+        const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+        const uint64_t pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
+        bulk_load(ring + (size_t)s * NT * STREAM_NV, spec_row_ptr(P, b, r) + (size_t)cbase * ES,
+                  (unsigned)(cend - cbase) * ES, &full[s], pol);
+        ++nissued;
+        pid += G0;
+    };
+    if (tid == 0) {
+        for (int s = 0; s < STREAM_STAGES; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+        for (int s = 0; s < STREAM_STAGES; ++s) issue_next(s);
+    }
+    __syncthreads();
+
+    bool failed = false;  // a bulk-copy wait ran out: the remaining chunks are reported, not read
+    long long fail_it = 0;
+    long long it = 0;
+    for (int id = blockIdx.x; id < nch; id += G0, ++it) {
+        const int row_id = id / P.S1, ci = id - row_id * P.S1;
+        const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+        const bool partial = cbase + CHUNK > cend;
+        const int s = (int)(it % STREAM_STAGES);
+        bool ok = !failed;
+        if (ok) ok = mbar_wait(&full[s], (unsigned)(it / STREAM_STAGES) & 1u);
+        uint4 w[STREAM_NV];
+        const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+        const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
 #pragma unroll
-    for (int it = 0; it < CV / U1; ++it) {
-        const int vb = c0 + it * U1 * NT + tid;
-        if (vb >= c1) break;
-        uint4 w[U1];
-#pragma unroll
-        for (int u = 0; u < U1; ++u) {
-            const int v = vb + u * NT;
-            w[u] = v < c1 ? ld_stream_v4_pol(row + (size_t)v * 16, pol) : make_uint4(pad, pad, pad, pad);
+        for (int j = 0; j < STREAM_NV; ++j) {
+            w[j] = make_uint4(pad, pad, pad, pad);
+            if (ok && (!partial || cbase + (j * NT + tid) * VEC < cend)) w[j] = lds128(sb + j * NT + tid);
         }
-        stats_step<DT, U1>(w, P.c, m, mc, acc);
-    }
-    // per-warp partial
-    const float M = warp_max(m);
-    const float MC = M * P.c;
-    const float sc = (mc == NEG_INF) ? 0.f : acc * ex2(mc - MC);
-    const float S = warp_sum(sc);
-    const int row_id = b * P.R + r;
-    if (lane == 0) {
+        // every thread has read its part of the stage: it can be refilled
+        const int anyfail = __syncthreads_or(!ok);
+        if (anyfail && !failed) {
+            failed = true;
+            fail_it = it;
+        }
+        if (tid == 0 && !failed) issue_next(s);
         Partial pt;
-        pt.M = M;
-        pt.MC = MC;
-        pt.S = (double)S;
-        P.partials[((size_t)row_id * P.S1 + c) * WARPS + warp] = pt;
+        if (failed) {
+            pt.M = __int_as_float(0x7fc00000);  // the chunk was not read: S < 0 marks a timeout
+            pt.MC = pt.M;
+            pt.S = -1.0;
+        } else {
+            // maximum of the thread's elements, then of the warp
+            float m;
+            if constexpr (DT == DT_BF16) {
+                uint32_t pm = w[0].x;
+#pragma unroll
+                for (int j = 0; j < STREAM_NV; ++j) {
+                    pm = bmax2(pm, w[j].x); pm = bmax2(pm, w[j].y);
+                    pm = bmax2(pm, w[j].z); pm = bmax2(pm, w[j].w);
+                }
+                m = fmaxf(bf16lo(pm), bf16hi(pm));
+            } else {
+                m = NEG_INF;
+#pragma unroll
+                for (int j = 0; j < STREAM_NV; ++j)
+                    m = fmaxf(fmaxf(m, __uint_as_float(w[j].x)), fmaxf(fmaxf(__uint_as_float(w[j].y),
+                            __uint_as_float(w[j].z)), __uint_as_float(w[j].w)));
+            }
+            const float M = warp_max(m);
+            const float MC = M * c;
+            // sum of 2^(x c - MC) in four fp32 accumulators, combined in a fixed order
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            if (M != NEG_INF) {
+#pragma unroll
+                for (int j = 0; j < STREAM_NV; ++j) {
+                    if constexpr (DT == DT_BF16) {
+                        a0 += ex2(fmaf(bf16lo(w[j].x), c, -MC)); a1 += ex2(fmaf(bf16hi(w[j].x), c, -MC));
+                        a2 += ex2(fmaf(bf16lo(w[j].y), c, -MC)); a3 += ex2(fmaf(bf16hi(w[j].y), c, -MC));
+                        a0 += ex2(fmaf(bf16lo(w[j].z), c, -MC)); a1 += ex2(fmaf(bf16hi(w[j].z), c, -MC));
+                        a2 += ex2(fmaf(bf16lo(w[j].w), c, -MC)); a3 += ex2(fmaf(bf16hi(w[j].w), c, -MC));
+                    } else {
+                        a0 += ex2(fmaf(__uint_as_float(w[j].x), c, -MC));
+                        a1 += ex2(fmaf(__uint_as_float(w[j].y), c, -MC));
+                        a2 += ex2(fmaf(__uint_as_float(w[j].z), c, -MC));
+                        a3 += ex2(fmaf(__uint_as_float(w[j].w), c, -MC));
+                    }
+                }
+            }
+            pt.M = M;
+            pt.MC = MC;
+            pt.S = (double)warp_sum((a0 + a1) + (a2 + a3));  // fp32: the fp64 pipe is slow here
+        }
+        if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
     }
-    if (!arrive_last(&P.row_ctr[row_id], (unsigned)P.S1, &sh_flag)) return;
-    if (tid < 32) row_merge_and_plan<DT>(P, b, row_id, P.S1 * WARPS);
+    // after a failed wait, let the copies still in flight land before the CTA leaves (bounded)
+    if (failed && tid == 0)
+        for (long long j = fail_it; j < nissued && j < fail_it + STREAM_STAGES; ++j)
+            (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
+}
+
+// Row merge and plan, one warp per row: the row's S1 x WARPS partials merged in order into
+// RowStats, with the lse, 1/S and log2 p(x) of the token the row scores filled in advance; the
+// last warp to finish a row of a request runs the acceptance scan and writes the plan.
+template <int DT>
+__global__ void __launch_bounds__(NT) spec_rowplan_kernel(SpecParams P)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_id = blockIdx.x * WARPS + warp;
+    if (row_id >= P.B * P.R) return;
+    const int b = row_id / P.R, r = row_id - b * P.R, g = P.gamma;
+    // the token this row scores and its logit, fetched first so that they arrive meanwhile
+    const int pos = (r < g) ? r : (r > g) ? r - g - 1 : -1;
+    const int tok = (pos >= 0) ? __ldg(P.tokens + (size_t)b * g + pos) : -1;
+    const bool tok_ok = tok >= 0 && tok < P.V;
+    const float xtok = tok_ok ? load_logit(spec_row_ptr(P, b, r), DT, tok) : 0.f;
+    pdl_trigger();
+    pdl_wait();  // the partials of the streaming kernel
+
+    const int nparts = P.S1 * WARPS;
+    const Partial* pp = P.partials + (size_t)row_id * nparts;
+    float Mr = NEG_INF;
+    double Sr = 0.0;
+    int tmo = 0;
+    if (nparts <= 128) {
+        // every partial of the row in flight at once: four per lane
+        Partial q[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int k = lane + 32 * t;
+            q[t].M = NEG_INF;
+            q[t].MC = NEG_INF;
+            q[t].S = 0.0;
+            if (k < nparts) q[t] = ld_partial(pp + k);
+            Mr = fmaxf(Mr, q[t].M);
+        }
+        Mr = warp_max(Mr);
+        const float MCr = Mr * P.c;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (q[t].S < 0.0) tmo = 1;  // a chunk the streaming kernel could not read
+            if (q[t].S != 0.0) Sr += q[t].S * (double)ex2(q[t].MC - MCr);
+        }
+    } else {
+        for (int k = lane; k < nparts; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
+        Mr = warp_max(Mr);
+        const float MCr = Mr * P.c;
+        for (int k = lane; k < nparts; k += 32) {
+            const Partial q = ld_partial(pp + k);
+            if (q.S < 0.0) tmo = 1;
+            if (q.S != 0.0) Sr += q.S * (double)ex2(q.MC - MCr);
+        }
+    }
+    const float MCr = Mr * P.c;
+    Sr = warp_sum(Sr);
+    tmo = __any_sync(0xffffffffu, tmo);
+    if (lane == 0) {
+        RowStats st;
+        st.M = Mr;
+        st.MC = MCr;
+        st.S = Sr;
+        st.thr = NEG_INF;
+        st.klist_n = -1;
+        st.dense = 0;
+        const bool ok = !tmo && isfinite(Sr) && Sr > 0.0 && Mr != NEG_INF && isfinite(Mr);
+        st.status = tmo ? ROW_TIMEOUT : ok ? ROW_OK : ROW_NONFINITE;
+        st.lse = __int_as_float(0x7fc00000);
+        st.invS = 0.f;
+        st.lx = __longlong_as_double(0x7ff8000000000000ll);
+        if (ok) {
+            // log2 S from S = m 2^e, m in [0.5, 1): an fp32 log2 of m (absolute error ~1e-7) plus e
+            int e;
+            const double mm = frexp(Sr, &e);
+            const double l2S = (double)log2f((float)mm) + (double)e;
+            const double exact = (double)Mr * (double)P.c;
+            st.lse = (float)((double)Mr / P.T + LN2 * (l2S - (exact - (double)MCr)));
+            st.invS = __frcp_rn(__double2float_rn(Sr));
+            if (tok_ok) st.lx = (double)fmaf(xtok, P.c, -MCr) - l2S;
+        }
+        P.rstats[row_id] = st;
+    }
+    if (warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) {
+        const Plan pl = compute_plan_warp<DT, true>(P, b, false);
+        if (lane == 0) P.plan[b] = pl;
+    }
 }
 
 // ---------------------------------------------------------------- kernel 2: residual draw
@@ -385,8 +545,16 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
     const float* segs = P.segs + (size_t)b * P.nseg;
     const int per = (P.nseg + 31) / 32;
     const int s0 = min(lane * per, P.nseg), s1 = min(s0 + per, P.nseg);
+    // each lane's contiguous block of segment sums, eight independent loads in flight at a time
     double mine = 0.0;
-    for (int s = s0; s < s1; ++s) mine += (double)__ldcg(segs + s);
+    for (int q0 = s0; q0 < s1; q0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = (q0 + t < s1) ? __ldcg(segs + q0 + t) : 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (q0 + t < s1) mine += (double)v[t];
+    }
     const double incl = warp_incl_scan(mine);
     const double Z = __shfl_sync(0xffffffffu, incl, 31);
     if (!(Z > 0.0) || !isfinite(Z)) return -1;
@@ -404,11 +572,20 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
     if (lane == owner) {
         double run = 0.0, lastbase = excl;
         int lastpos = -1;
-        for (int s = s0; s < s1; ++s) {
-            const double sv = (double)__ldcg(segs + s);
-            if (sv > 0.0) { lastpos = s; lastbase = excl + run; }
-            if (sv > 0.0 && t < excl + run + sv) { seg = s; base = excl + run; break; }
-            run += sv;
+        for (int q0 = s0; q0 < s1 && seg < 0; q0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = (q0 + k < s1) ? __ldcg(segs + q0 + k) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int s = q0 + k;
+                if (s < s1 && seg < 0) {
+                    const double sv = (double)v[k];
+                    if (sv > 0.0) { lastpos = s; lastbase = excl + run; }
+                    if (sv > 0.0 && t < excl + run + sv) { seg = s; base = excl + run; }
+                    else run += sv;
+                }
+            }
         }
         if (seg < 0) { seg = lastpos; base = lastbase; }
     }
@@ -491,6 +668,7 @@ __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
     __shared__ int sh_flag;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x / P.S2, c = blockIdx.x % P.S2;
+    pdl_wait();  // the plan of the row-merge kernel
     const Plan pl = ld_plan(P.plan + b);
     const char* rowp = spec_row_ptr(P, b, pl.rp);
     const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
@@ -550,19 +728,22 @@ static void launch_softmax_plain(const SpecParams& P, int sms, cudaStream_t st)
 }
 
 template <int DT>
-static void launch_softmax_chunk(const SpecParams& P, cudaStream_t st)
+static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
 {
+    constexpr auto K1 = spec_stream_kernel<DT>;
     mark_kernel_start(st);
-    spec_stats_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.R * P.S1), NT, 0, st>>>(P);
+    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM), NT, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
-    spec_resample_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.S2), NT, 0, st>>>(P);
+    launch_dependent(spec_rowplan_kernel<DT>, (unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, 0,
+                     st, P);
+    launch_dependent(spec_resample_chunk_kernel<DT>, (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
 }
 
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st)
 {
-    if (P.dtype == DT_BF16 && P.vec == 8) launch_softmax_chunk<DT_BF16>(P, st);
+    if (P.dtype == DT_BF16 && P.vec == 8) launch_softmax_chunk<DT_BF16>(P, sms, st);
     else if (P.dtype == DT_BF16) launch_softmax_plain<DT_BF16, 1>(P, sms, st);
-    else if (P.vec == 4) launch_softmax_chunk<DT_F32>(P, st);
+    else if (P.vec == 4) launch_softmax_chunk<DT_F32>(P, sms, st);
     else launch_softmax_plain<DT_F32, 1>(P, sms, st);
     return cudaGetLastError();
 }

@@ -33,11 +33,10 @@
 
 namespace sv {
 
-constexpr int TK_CHUNK_BYTES = 32768;                 // bytes of one row per chunk
-constexpr int TK_NREG = TK_CHUNK_BYTES / (NT * 4);    // 32-bit words per thread (32)
-constexpr int TK_NV = TK_NREG / 4;                    // 16-byte vectors per thread (8)
-constexpr int TK_STAGES = 3;                          // bulk-copy ring depth
-constexpr int TK_SMEM = TK_STAGES * TK_CHUNK_BYTES;   // dynamic shared memory of kernel 1
+constexpr int TK_NREG = STREAM_CHUNK_BYTES / (NT * 4);  // 32-bit words per thread (32)
+constexpr int TK_NV = STREAM_NV;                        // 16-byte vectors per thread (8)
+constexpr int TK_STAGES = STREAM_STAGES;                // bulk-copy ring depth
+constexpr int TK_SMEM = STREAM_SMEM;                    // dynamic shared memory of kernel 1
 // per-chunk candidate count codes
 constexpr int TK_OVERFLOW = -1, TK_NONFINITE = -2, TK_TIMEOUT = -3;
 
@@ -354,6 +353,7 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     __shared__ int pub_seg[2];         // -1: none
     __shared__ __align__(8) uint64_t full[TK_STAGES];
 
+    pdl_trigger();  // the finish kernel may be scheduled as SMs free up; it waits for this grid
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned FULL = 0xffffffffu;
     const int nsegs = P.B * P.R * P.nsegr;
@@ -671,6 +671,8 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     const int tok = (pos >= 0) ? __ldg(P.tokens + (size_t)b * g + pos) : -1;
     const bool tok_ok = tok >= 0 && tok < P.V;
     const float xtok = tok_ok ? load_logit(spec_row_ptr(P, b, r), DT, tok) : 0.f;
+    pdl_trigger();
+    pdl_wait();  // the candidate lists of the streaming kernel
 
     int n = (lane < nl) ? __ldcg(cnt + lane) : 0;
     int flag = 0;
@@ -842,6 +844,7 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
 
     const int row_id = blockIdx.x;
     const int b = row_id / P.R, r = row_id % P.R;
+    pdl_wait();  // the row statistics of the finish kernel
     if (!__ldcg(&P.rstats[row_id].dense)) return;
     const char* row = spec_row_ptr(P, b, r);
     const int V = P.V, k = P.top_k;
@@ -948,31 +951,6 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
 }
 
 
-// persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task
-template <auto K>
-static unsigned cta_grid(long long tasks, int sms, size_t smem)
-{
-    static int per_sm = 0;
-    if (per_sm < 1) {
-        int n = 0;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, NT, smem) != cudaSuccess || n < 1) n = 1;
-        per_sm = n;
-    }
-    const long long cap = (long long)per_sm * sms;
-    return (unsigned)(tasks < 1 ? 1 : (tasks < cap ? tasks : cap));
-}
-
-template <auto K>
-static void set_smem_limit(size_t smem)
-{
-    static size_t done = 0;
-    if (smem > 48 * 1024 && smem > done) {
-        cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        done = smem;
-    }
-}
-
 template <int DT>
 static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
 {
@@ -988,8 +966,9 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
     mark_kernel_stop(st);
     const size_t fsm = (size_t)WARPS * (TK_UNION + P.cap_k) * sizeof(TopkEntry);
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
-    topk_finish_kernel<DT><<<(unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, fsm, st>>>(P);
-    topk_dense_kernel<DT><<<(unsigned)((long long)P.B * P.R), NT, 0, st>>>(P);
+    launch_dependent(topk_finish_kernel<DT>, (unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, fsm,
+                     st, P);
+    launch_dependent(topk_dense_kernel<DT>, (unsigned)((long long)P.B * P.R), NT, 0, st, P);
 }
 
 cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st)
