@@ -44,7 +44,7 @@ KERNEL_OF = {
     "c2": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c3": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c4": ("topk_stream_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.cuh"]),
-    "c5": ("tree_argmax_chunk_kernel", ["sv_tree.cu", "sv_common.cuh"]),
+    "c5": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
 }
 DOMINANT_CFG = "c4"
 

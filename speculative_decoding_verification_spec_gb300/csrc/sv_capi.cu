@@ -32,7 +32,6 @@ static Shape row_shape(int V, int vec)
 }
 
 static long long slices1(const Shape& s) { return std::max(1LL, cdiv(s.nvec, TV1)); }
-static long long chunks1(const Shape& s) { return std::max(1LL, cdiv(s.nvec, CHUNK_VECS)); }
 // 32 KB chunks of a row of 16-byte vectors (the streaming kernels)
 static long long stream_chunks(const Shape& s) { return std::max(1LL, cdiv(s.nvec, (long long)NT * STREAM_NV)); }
 // softmax partials per row: one per warp task (scalar path) or one per warp of each stream chunk
@@ -275,7 +274,8 @@ size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
     for (int vec : {1, 4, 8}) {
         const Shape sh = row_shape(V, vec);
         if (tree_nodes > 0) {
-            best = std::max(best, tree_layout(B, tree_nodes, slices1(sh)).bytes);
+            best = std::max(best, tree_layout(B, tree_nodes, sh.vec > 1 ? stream_chunks(sh) * WARPS
+                                                                           : slices1(sh)).bytes);
         } else {
             const bool topk = top_k > 0 && top_k < V;
             // lists: nsegr * WARPS * cap_s <= TK_UNION entries, at most TK_MAX_SEGR * WARPS per row
@@ -343,11 +343,12 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     P.tokens = tokens;
     P.B = B; P.N = N; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
-    P.S1 = (int)(vec > 1 ? chunks1(sh) : slices1(sh));
+    // 16-byte vectors: 32 KB stream chunks (a partial per chunk and warp); scalar path: slices
+    P.S1 = (int)(vec > 1 ? stream_chunks(sh) : slices1(sh));
     P.tasks = (long long)B * R * P.S1;
     P.max_out = max_out;
     if (P.tasks >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
-    const TreeLayout L = tree_layout(B, N, P.S1);
+    const TreeLayout L = tree_layout(B, N, vec > 1 ? (long long)P.S1 * WARPS : P.S1);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
     char* ws = static_cast<char*>(workspace);
     P.accepted_len = accepted_len;

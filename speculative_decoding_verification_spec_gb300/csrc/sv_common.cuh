@@ -75,6 +75,7 @@ struct ArgmaxPartial {
     int nan;
     int pad;
 };
+static_assert(sizeof(ArgmaxPartial) == 16, "argmax partials are read as one 16-byte vector");
 
 // ---------------------------------------------------------------- parameter blocks
 
@@ -338,11 +339,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
     }
     return false;
 }
-
-// Chunk kernels: one CTA of NT threads per chunk of CHUNK_VECS contiguous vectors; thread t reads
-// vectors t + i*NT (i < CV) into registers.
-constexpr int CV = 16;
-constexpr int CHUNK_VECS = NT * CV;
 
 // Streaming kernels: persistent CTAs (two per SM) fetch 32 KB chunks of one row with bulk copies
 // into a ring of STREAM_STAGES shared-memory stages; thread t reads vectors t + j*NT (j <

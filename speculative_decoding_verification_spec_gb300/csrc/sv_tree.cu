@@ -83,6 +83,10 @@ __device__ __forceinline__ int step_find(const char* row, long long base, long l
     return found;
 }
 
+__device__ void tree_walk_and_emit(const TreeParams& P, int b, int bad, const int32_t* par,
+                                   const int32_t* tok, const int32_t* am, int32_t* depth,
+                                   int32_t* valid);
+
 // The warp that completed request b: per-row argmax in slice order, the walk, the outputs.
 __device__ void tree_finish_request(const TreeParams& P, int b)
 {
@@ -105,40 +109,87 @@ __device__ void tree_finish_request(const TreeParams& P, int b)
     }
     bad = __any_sync(0xffffffffu, bad);
     __syncwarp();
-    // ---- walk (lane 0; parents precede children)
+    int32_t* depth = P.scratch + (size_t)b * P.N * 2;
+    tree_walk_and_emit(P, b, bad, P.parents + (size_t)b * P.N, P.tokens + (size_t)b * P.N,
+                       P.amax + (size_t)b * P.R, depth, depth + P.N);
+}
+
+// One warp: validates the request's tree, finds every node's validity and depth, picks the deepest
+// valid node (lowest index on ties) and writes the outputs.  par / tok are the request's parent
+// and token arrays, am its rows' argmaxes, depth / valid N-int scratch (global or shared memory).
+// bad: 0, 1 (a row is non-finite) or 2 (a row could not be read).
+//
+// Nodes are taken 32 at a time in index order, one per lane.  A node whose parent lies in an
+// earlier group reads the parent's final validity and depth; within a group the values move from
+// parent to child by ballot / shuffle until nothing changes (parents precede children, so this
+// settles after as many rounds as the group's longest chain).
+__device__ void tree_walk_and_emit(const TreeParams& P, int b, int bad, const int32_t* par,
+                                   const int32_t* tok, const int32_t* am, int32_t* depth,
+                                   int32_t* valid)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
     const int N = P.N, mo = P.max_out;
     int32_t* out = P.out_tokens + (size_t)b * mo;
     int32_t* onodes = P.out_nodes ? P.out_nodes + (size_t)b * (mo - 1) : nullptr;
-    int st = bad ? ROW_NONFINITE : ROW_OK, bestd = 0;
+    int st = (bad == 2) ? ROW_TIMEOUT : bad ? ROW_NONFINITE : ROW_OK;
+    if (st == ROW_OK) {
+        int badp = 0, badt = 0;
+        for (int i = lane; i < N; i += 32) {
+            const int p = par[i];
+            if (p < -1 || p >= i) badp = 1;
+            const int tk = tok[i];
+            if (tk < 0 || tk >= P.V) badt = 1;
+        }
+        badp = __any_sync(FULL, badp);
+        badt = __any_sync(FULL, badt);
+        st = badp ? ROW_BAD_PARENT : (badt ? ROW_BAD_TOKEN : ROW_OK);
+    }
+    int bestd = 0, bestn = -1;
+    if (st == ROW_OK) {
+        for (int i0 = 0; i0 < N; i0 += 32) {
+            const int i = i0 + lane;
+            const bool in = i < N;
+            const int p = in ? par[i] : -1;
+            const bool local = p >= i0;  // the parent is in this group
+            const int m = in && tok[i] == am[p < 0 ? 0 : p + 1];
+            int v = 0, dd = 0;
+            if (in && !local) {
+                v = m && (p < 0 || valid[p]);
+                dd = p < 0 ? 1 : depth[p] + 1;
+            }
+            for (int round = 0; round < 32; ++round) {
+                const unsigned vm = __ballot_sync(FULL, v);
+                const int pd = __shfl_sync(FULL, dd, local ? p - i0 : lane);
+                int nv = v, nd = dd;
+                if (in && local) {
+                    nv = m && ((vm >> (p - i0)) & 1u);
+                    nd = pd > 0 ? pd + 1 : 0;
+                }
+                if (!__any_sync(FULL, nv != v || nd != dd)) break;
+                v = nv;
+                dd = nd;
+            }
+            if (in) {
+                valid[i] = v;
+                depth[i] = dd;
+                if (v && dd > bestd) { bestd = dd; bestn = i; }
+            }
+            __syncwarp();
+        }
+        // deepest valid node, lowest index on ties
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const int od = __shfl_xor_sync(FULL, bestd, o);
+            const int on = __shfl_xor_sync(FULL, bestn, o);
+            if (od > bestd || (od == bestd && on >= 0 && (bestn < 0 || on < bestn))) {
+                bestd = od;
+                bestn = on;
+            }
+        }
+        if (bestd + 1 > mo) st = ROW_OVERFLOW;
+    }
     if (lane == 0) {
-        const int32_t* par = P.parents + (size_t)b * N;
-        const int32_t* tok = P.tokens + (size_t)b * N;
-        const int32_t* am = P.amax + (size_t)b * P.R;
-        int32_t* depth = P.scratch + (size_t)b * N * 2;
-        int32_t* valid = depth + N;
-        if (st == ROW_OK) {
-            int badp = 0, badt = 0;
-            for (int i = 0; i < N; ++i) {
-                const int p = par[i];
-                if (p < -1 || p >= i) badp = 1;
-                const int tk = tok[i];
-                if (tk < 0 || tk >= P.V) badt = 1;
-            }
-            st = badp ? ROW_BAD_PARENT : (badt ? ROW_BAD_TOKEN : ROW_OK);
-        }
-        int bestn = -1;
-        if (st == ROW_OK) {
-            for (int i = 0; i < N; ++i) {
-                const int p = par[i];
-                const int predictor = p < 0 ? 0 : p + 1;
-                const int vi = (tok[i] == am[predictor]) && (p < 0 || valid[p]);
-                const int d = p < 0 ? 1 : depth[p] + 1;
-                valid[i] = vi;
-                depth[i] = d;
-                if (vi && d > bestd) { bestd = d; bestn = i; }
-            }
-            if (bestd + 1 > mo) st = ROW_OVERFLOW;
-        }
         P.accepted_len[b] = (st == ROW_OK) ? bestd : -1;
         if (P.row_status) P.row_status[b] = st;
         if (st == ROW_OK) {  // path written back to front, then the bonus
@@ -151,14 +202,11 @@ __device__ void tree_finish_request(const TreeParams& P, int b)
             }
         }
     }
-    st = __shfl_sync(0xffffffffu, st, 0);
-    bestd = __shfl_sync(0xffffffffu, bestd, 0);
     const int A = (st == ROW_OK) ? bestd : -1;
     for (int i = lane; i < mo; i += 32) {
         if (st != ROW_OK || i > A) out[i] = -1;
         if (onodes && i < mo - 1 && (st != ROW_OK || i >= A)) onodes[i] = -1;
     }
-
 }
 
 // End of an argmax task: the lanes holding the warp maximum locate its first index (ties to the
@@ -229,77 +277,206 @@ __global__ void __launch_bounds__(NT) tree_argmax_kernel(TreeParams P)
     }
 }
 
-// Chunk kernel for 16-byte vectors: one CTA per (request, row, chunk of CHUNK_VECS contiguous
-// vectors), U1 vectors per thread loaded at a time into registers.  Each thread keeps its running
-// maximum and the first vector where it was reached (strictly greater replaces, and a thread sees
-// its vectors in index order); after the CTA maximum is known, the threads holding it re-read that
-// one vector to locate the element, and the lowest such index is the chunk's argmax.
+// Streaming argmax for rows of 16-byte vectors: persistent CTAs take 32 KB chunks round-robin,
+// fetched by bulk copies into a ring of shared-memory stages.  Each thread finds its maximum (via
+// the maxima of its vectors) and the first of its elements equal to it -- its vectors and their
+// elements are in index order -- and each warp reduces (value, index) with ties to the lower
+// index into one partial per (chunk, warp).  A NaN anywhere marks the partial.
 template <int DT>
-__global__ void __launch_bounds__(NT) tree_argmax_chunk_kernel(TreeParams P)
+__global__ void __launch_bounds__(NT, 2) tree_stream_kernel(TreeParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
-    __shared__ float sh_f[WARPS];
-    __shared__ int sh_i[WARPS], sh_flag;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = blockIdx.x % P.S1;
-    const int rr = blockIdx.x / P.S1;
-    const int b = rr / P.R, r = rr % P.R;
-    const char* row = tree_row(P, b, r);
-    const int c0 = c * CHUNK_VECS;
-    const int c1 = (int)min((long long)c0 + CHUNK_VECS, P.nvec);
+    constexpr int ES = (DT == DT_BF16) ? 2 : 4;
+    constexpr int CHUNK = NT * STREAM_NV * VEC;
+    extern __shared__ __align__(128) uint4 ring[];
+    __shared__ __align__(8) uint64_t full[STREAM_STAGES];
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = P.B * P.R * P.S1;
+    const int G0 = gridDim.x;
     const uint64_t pol = policy_evict_first();
-    float best = NEG_INF;
-    int bvec = -1, nan = 0;
-#pragma unroll
-    for (int it = 0; it < CV / U1; ++it) {
-        const int vb = c0 + it * U1 * NT + tid;
-        if (vb >= c1) break;
-        uint4 w[U1];
-#pragma unroll
-        for (int u = 0; u < U1; ++u) {
-            const int v = vb + u * NT;
-            const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;  // -inf
-            w[u] = v < c1 ? ld_stream_v4_pol(row + (size_t)v * 16, pol) : make_uint4(pad, pad, pad, pad);
-        }
-#pragma unroll
-        for (int u = 0; u < U1; ++u) {
-            float vm;
-            if constexpr (DT == DT_BF16) {
-                const uint32_t pm = bmax2_nan(bmax2_nan(w[u].x, w[u].y), bmax2_nan(w[u].z, w[u].w));
-                vm = fmax_nan(bf16lo(pm), bf16hi(pm));
-            } else {
-                vm = fmax_nan(fmax_nan(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
-                              fmax_nan(__uint_as_float(w[u].z), __uint_as_float(w[u].w)));
-            }
-            if (vm != vm) nan = 1;
-            else if (vm > best) { best = vm; bvec = vb + u * NT; }
-        }
-    }
-    const float W = block_max(best, sh_f);
-    const int anynan = __syncthreads_or(nan);
-    int idx = 0x7fffffff;
-    if (best == W && bvec >= 0) {  // re-read the vector where this thread first reached W
-        RawVec<DT, VEC> x;
-        x.load(row, bvec, pol);
-#pragma unroll
-        for (int e = VEC - 1; e >= 0; --e)
-            if (x.get(e) == W) idx = bvec * VEC + e;
-    }
-    idx = __reduce_min_sync(0xffffffffu, idx);
-    if (lane == 0) sh_i[warp] = idx;
-    __syncthreads();
+
+    int pid = blockIdx.x;
+    long long nissued = 0;
+    auto issue_next = [&](int s) {
+        if (pid >= nch) return;
+        const int row_id = pid / P.S1, ci = pid - row_id * P.S1;
+        const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+        const char* row = reinterpret_cast<const char*>(P.logits) + (size_t)row_id * P.V * ES;
+        bulk_load(ring + (size_t)s * NT * STREAM_NV, row + (size_t)cbase * ES, (unsigned)(cend - cbase) * ES,
+                  &full[s], pol);
+        ++nissued;
+        pid += G0;
+    };
     if (tid == 0) {
-        int bi = sh_i[0];
-        for (int w = 1; w < WARPS; ++w) bi = min(bi, sh_i[w]);
-        ArgmaxPartial pt;
-        pt.best = W;
-        pt.idx = bi;
-        pt.nan = anynan;
-        pt.pad = 0;
-        P.partials[((size_t)b * P.R + r) * P.S1 + c] = pt;
+        for (int s = 0; s < STREAM_STAGES; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+        for (int s = 0; s < STREAM_STAGES; ++s) issue_next(s);
     }
-    if (!arrive_last(&P.req_ctr[b], (unsigned)(P.R * P.S1), &sh_flag)) return;
-    if (warp == 0) tree_finish_request(P, b);
+    __syncthreads();
+
+    bool failed = false;
+    long long fail_it = 0;
+    long long it = 0;
+    for (int id = blockIdx.x; id < nch; id += G0, ++it) {
+        const int row_id = id / P.S1, ci = id - row_id * P.S1;
+        const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+        const int s = (int)(it % STREAM_STAGES);
+        bool ok = !failed;
+        if (ok) ok = mbar_wait(&full[s], (unsigned)(it / STREAM_STAGES) & 1u);
+        const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+        const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
+        uint4 w[STREAM_NV];
+        float vmax[STREAM_NV];
+        int nin = 0;  // vectors of this thread inside the row
+#pragma unroll
+        for (int j = 0; j < STREAM_NV; ++j) {
+            const bool in = cbase + (j * NT + tid) * VEC < cend;
+            nin += in;
+            w[j] = make_uint4(pad, pad, pad, pad);
+            if (ok && in) w[j] = lds128(sb + j * NT + tid);
+        }
+        const int anyfail = __syncthreads_or(!ok);
+        if (anyfail && !failed) {
+            failed = true;
+            fail_it = it;
+        }
+        if (tid == 0 && !failed) issue_next(s);
+        ArgmaxPartial pt;
+        pt.pad = 0;
+        if (failed) {
+            pt.best = NEG_INF;
+            pt.idx = 0x7fffffff;
+            pt.nan = 2;  // the chunk was not read
+        } else {
+            float tm = NEG_INF;
+#pragma unroll
+            for (int j = 0; j < STREAM_NV; ++j) {
+                if constexpr (DT == DT_BF16) {
+                    const uint32_t pm = bmax2_nan(bmax2_nan(w[j].x, w[j].y), bmax2_nan(w[j].z, w[j].w));
+                    vmax[j] = fmax_nan(bf16lo(pm), bf16hi(pm));
+                } else {
+                    vmax[j] = fmax_nan(fmax_nan(__uint_as_float(w[j].x), __uint_as_float(w[j].y)),
+                                       fmax_nan(__uint_as_float(w[j].z), __uint_as_float(w[j].w)));
+                }
+                tm = fmax_nan(tm, vmax[j]);
+            }
+            const int nan = tm != tm;
+            int idx = 0x7fffffff;
+            if (!nan && nin > 0) {
+                int jf = 0;
+#pragma unroll
+                for (int j = STREAM_NV - 1; j >= 0; --j)
+                    if (vmax[j] == tm) jf = j;
+                uint4 v = w[0];
+#pragma unroll
+                for (int j = 1; j < STREAM_NV; ++j)
+                    if (j == jf) v = w[j];
+                int ef = 0;
+                if constexpr (DT == DT_BF16) {
+                    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 7; e >= 0; --e) {
+                        const float x = (e & 1) ? bf16hi(q[e >> 1]) : bf16lo(q[e >> 1]);
+                        if (x == tm) ef = e;
+                    }
+                } else {
+                    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 3; e >= 0; --e)
+                        if (__uint_as_float(q[e]) == tm) ef = e;
+                }
+                idx = cbase + (jf * NT + tid) * VEC + ef;
+            }
+            // warp: maximum value, then the lowest index holding it
+            float bv = nan ? NEG_INF : tm;
+            int bi = idx;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            pt.best = bv;
+            pt.idx = bi;
+            pt.nan = __any_sync(0xffffffffu, nan);
+        }
+        if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
+    }
+    if (failed && tid == 0)
+        for (long long j = fail_it; j < nissued && j < fail_it + STREAM_STAGES; ++j)
+            (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
+}
+
+// One CTA per request: the warps merge the rows' partials (rows round-robin, every partial of a
+// warp's rows in flight together), then warp 0 walks the tree.  When the tree fits
+// (N <= TREE_SMEM_NODES) the walk runs entirely in shared memory -- parents, tokens, the rows'
+// argmaxes, depth and validity: dynamic shared memory of 4 N + R ints.
+constexpr int TREE_SMEM_NODES = 4096;
+
+template <int DT>
+__global__ void __launch_bounds__(NT) tree_finish_kernel(TreeParams P)
+{
+    extern __shared__ int32_t tsm[];  // par[N], tok[N], depth[N], valid[N], am[R]
+    __shared__ int sh_bad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x, N = P.N, R = P.R;
+    const bool staged = N <= TREE_SMEM_NODES;
+    const int32_t* par = staged ? tsm : P.parents + (size_t)b * N;
+    const int32_t* tok = staged ? tsm + N : P.tokens + (size_t)b * N;
+    int32_t* depth = staged ? tsm + 2 * N : P.scratch + (size_t)b * N * 2;
+    int32_t* valid = staged ? tsm + 3 * N : P.scratch + (size_t)b * N * 2 + N;
+    int32_t* am = staged ? tsm + 4 * N : P.amax + (size_t)b * R;
+    if (staged)
+        for (int i = tid; i < N; i += NT) {
+            tsm[i] = __ldg(P.parents + (size_t)b * N + i);
+            tsm[N + i] = __ldg(P.tokens + (size_t)b * N + i);
+        }
+    if (tid == 0) sh_bad = 0;
+    pdl_wait();  // the partials of the streaming kernel
+    __syncthreads();
+    const int np = P.S1 * WARPS;  // partials per row
+    int bad = 0;
+    constexpr int RPW = 9;  // rows of a warp in flight together (one round trip for R <= 72)
+    for (int j0 = warp; j0 < R; j0 += WARPS * RPW) {
+        int4 q[RPW][2];  // (best, idx, nan, pad) of two partials per lane for each row
+#pragma unroll
+        for (int t = 0; t < RPW; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = j0 + t * WARPS, k = lane + 32 * h;
+                q[t][h] = make_int4(__float_as_int(NEG_INF), 0x7fffffff, 0, 0);
+                if (j < R && k < np)
+                    q[t][h] = __ldcg(reinterpret_cast<const int4*>(P.partials + ((size_t)b * R + j) * np + k));
+            }
+#pragma unroll
+        for (int t = 0; t < RPW; ++t) {
+            const int j = j0 + t * WARPS;
+            if (j >= R) break;  // j is the same for every lane
+            float bv = __int_as_float(q[t][0].x);
+            int bi = q[t][0].y, bn = max(q[t][0].z, q[t][1].z);
+            if (better(__int_as_float(q[t][1].x), q[t][1].y, bv, bi)) { bv = __int_as_float(q[t][1].x); bi = q[t][1].y; }
+            for (int k = lane + 64; k < np; k += 32) {  // rows with more than 64 partials
+                const int4 e = __ldcg(reinterpret_cast<const int4*>(P.partials + ((size_t)b * R + j) * np + k));
+                bn = max(bn, e.z);
+                if (better(__int_as_float(e.x), e.y, bv, bi)) { bv = __int_as_float(e.x); bi = e.y; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            const int btmo = __any_sync(0xffffffffu, bn == 2);
+            bn = __any_sync(0xffffffffu, bn);
+            const bool ok = !bn && bi != 0x7fffffff;
+            if (!ok) bad = btmo ? 2 : max(bad, 1);
+            if (lane == 0) am[j] = ok ? bi : -1;
+        }
+    }
+    if (bad && lane == 0) atomicMax(&sh_bad, bad);
+    __syncthreads();
+    if (warp == 0) tree_walk_and_emit(P, b, sh_bad, par, tok, am, depth, valid);
 }
 
 template <int DT, int VEC>
@@ -311,20 +488,24 @@ static void launch_tree_plain(const TreeParams& P, int sms, cudaStream_t st)
 }
 
 template <int DT>
-static void launch_tree_chunk(const TreeParams& P, cudaStream_t st)
+static void launch_tree_chunk(const TreeParams& P, int sms, cudaStream_t st)
 {
+    constexpr auto K1 = tree_stream_kernel<DT>;
     mark_kernel_start(st);
-    tree_argmax_chunk_kernel<DT><<<(unsigned)((long long)P.B * P.R * P.S1), NT, 0, st>>>(P);
+    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM), NT, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
+    const size_t smem = P.N <= TREE_SMEM_NODES ? (size_t)(4 * P.N + P.R) * sizeof(int32_t) : 0;
+    set_smem_limit<tree_finish_kernel<DT>>(smem);
+    launch_dependent(tree_finish_kernel<DT>, (unsigned)P.B, NT, smem, st, P);
 }
 
 cudaError_t launch_tree_path(const TreeParams& P, int sms, cudaStream_t st)
 {
     if (P.dtype == DT_BF16) {
-        if (P.vec == 8) launch_tree_chunk<DT_BF16>(P, st);
+        if (P.vec == 8) launch_tree_chunk<DT_BF16>(P, sms, st);
         else launch_tree_plain<DT_BF16, 1>(P, sms, st);
     } else {
-        if (P.vec == 4) launch_tree_chunk<DT_F32>(P, st);
+        if (P.vec == 4) launch_tree_chunk<DT_F32>(P, sms, st);
         else launch_tree_plain<DT_F32, 1>(P, sms, st);
     }
     return cudaGetLastError();
