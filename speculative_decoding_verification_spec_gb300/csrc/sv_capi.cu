@@ -251,7 +251,14 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+    // streaming paths (16-byte vectors) clear the counters in their first kernel; the scalar
+    // paths' persistent kernels claim work from counters, so those are cleared beforehand
+    if (vec > 1) {
+        P.ctr_clear = reinterpret_cast<unsigned*>(ws);
+        P.ctr_words = (int)(L.ctr_bytes / sizeof(unsigned));
+    } else if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) {
+        return SPEC_ERR_CUDA;
+    }
     cudaError_t err;
     if (!topk) {
         err = launch_softmax_path(P, sms, st);
@@ -362,7 +369,8 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     P.scratch = reinterpret_cast<int32_t*>(ws + L.o_scratch);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+    // the streaming path (16-byte vectors) uses no counters; the scalar path claims work from them
+    if (vec == 1 && cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
     const cudaError_t err = launch_tree_path(P, sm_count(), st);
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -127,6 +127,9 @@ struct SpecParams {
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
     unsigned* dense_ctr;  // [B]
     int* ndense;          // [B]
+    // counters the first kernel clears itself (streaming paths; otherwise a memset does): words
+    unsigned* ctr_clear;
+    int ctr_words;
 };
 
 struct TreeParams {
@@ -362,6 +365,14 @@ inline unsigned cta_grid(long long tasks, int sms, size_t smem)
     }
     const long long cap = (long long)per_sm * sms;
     return (unsigned)(tasks < 1 ? 1 : (tasks < cap ? tasks : cap));
+}
+
+// Called at the start of a streaming kernel: its first CTA zeroes the call's completion counters,
+// which no kernel touches before that grid has completed (the later kernels wait for it).
+__device__ __forceinline__ void clear_counters(unsigned* ctr, int words)
+{
+    if (blockIdx.x == 0 && ctr)
+        for (int i = threadIdx.x; i < words; i += blockDim.x) ctr[i] = 0u;
 }
 
 // Programmatic dependent launch: a kernel launched with launch_dependent may start while the

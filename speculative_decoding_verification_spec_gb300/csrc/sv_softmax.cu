@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
     __shared__ __align__(8) uint64_t full[STREAM_STAGES];
 
     pdl_trigger();  // the row-merge kernel may be scheduled as SMs free up; it waits for this grid
+    clear_counters(P.ctr_clear, P.ctr_words);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nch = P.B * P.R * P.S1;  // < 2^31 (checked on the host)
     const int G0 = gridDim.x;

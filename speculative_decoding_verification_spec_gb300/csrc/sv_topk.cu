@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     __shared__ __align__(8) uint64_t full[TK_STAGES];
 
     pdl_trigger();  // the finish kernel may be scheduled as SMs free up; it waits for this grid
+    clear_counters(P.ctr_clear, P.ctr_words);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned FULL = 0xffffffffu;
     const int nsegs = P.B * P.R * P.nsegr;
