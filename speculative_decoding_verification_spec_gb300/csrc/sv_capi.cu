@@ -204,7 +204,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.uniforms = uniforms;
     P.B = B; P.gamma = gamma; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
-    P.c = c; P.T = T; P.top_k = top_k;
+    P.c = c; P.T = T; P.invT = 1.0 / T; P.top_k = top_k;
     // 16-byte vectors: 32 KB stream chunks (statistics) and 2048-vector residual chunks; the
     // scalar path's persistent warps take TV1 / TV2 vectors per task
     P.S1 = (int)(vec > 1 ? stream_chunks(sh) : slices1(sh));

@@ -96,6 +96,7 @@ struct SpecParams {
     long long nvec;       // vectors per row
     float c;              // log2(e)/T
     double T;
+    double invT;          // 1/T
     int top_k;
     int pin_pairs;        // row pairs 0..pin_pairs-1 are read with L2 evict_last
     // softmax path: stats tasks (row, slice) and residual tasks (request, slice)

@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(NT) spec_rowplan_kernel(SpecParams P)
             const double mm = frexp(Sr, &e);
             const double l2S = (double)log2f((float)mm) + (double)e;
             const double exact = (double)Mr * (double)P.c;
-            st.lse = (float)((double)Mr / P.T + LN2 * (l2S - (exact - (double)MCr)));
+            st.lse = (float)((double)Mr * P.invT + LN2 * (l2S - (exact - (double)MCr)));
             st.invS = __frcp_rn(__double2float_rn(Sr));
             if (tok_ok) st.lx = (double)fmaf(xtok, P.c, -MCr) - l2S;
         }

@@ -771,14 +771,14 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     st.thr = key_value(gkey);
     st.klist_n = nk;
     st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
-    if (st.status == ROW_OK) {
+    if (st.status == ROW_OK && lane == 0) {  // only lane 0's RowStats is stored
         // log2 S from S = m 2^e, m in [0.5, 1): an fp32 log2 of m (absolute error ~1e-7) plus e,
         // which keeps the fp64 pipe (slow on this part) out of the per-row work
         int e;
         const double m = frexp(S, &e);
         const double l2S = (double)log2f((float)m) + (double)e;
         const double exact = (double)M * (double)P.c;
-        st.lse = (float)((double)M / P.T + LN2 * (l2S - (exact - (double)MC)));
+        st.lse = (float)((double)M * P.invT + LN2 * (l2S - (exact - (double)MC)));
         st.invS = __frcp_rn(__double2float_rn(S));
         if (tok_ok) st.lx = (xtok >= st.thr) ? (double)fmaf(xtok, P.c, -MC) - l2S : -INFINITY;
     }
@@ -841,51 +841,52 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
     __shared__ int sh_red[WARPS];
     __shared__ double sh_d[WARPS];
     __shared__ float sh_f[WARPS];
-    __shared__ int sh_flag, sh_tok;
+    __shared__ int sh_tok;
 
-    const int row_id = blockIdx.x;
-    const int b = row_id / P.R, r = row_id % P.R;
+    // one CTA per request: it finishes the request's dense rows one after another, then scans
+    const int b = blockIdx.x;
     pdl_wait();  // the row statistics of the finish kernel
-    if (!__ldcg(&P.rstats[row_id].dense)) return;
-    const char* row = spec_row_ptr(P, b, r);
+    if (__ldcg(&P.ndense[b]) == 0) return;
     const int V = P.V, k = P.top_k;
-
-    // exact k-th largest key by bitwise search over full-row counts
-    uint32_t prefix = 0;
-    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-    for (int bit = 31; bit >= lo; --bit) {
-        const uint32_t want = prefix | (1u << bit);
-        int cnt = 0;
-        for (int v = threadIdx.x; v < V; v += NT) cnt += okey(load_logit(row, DT, v)) >= want;
-        if (block_sum_int(cnt, sh_red) >= k) prefix = want;
-    }
-    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-    const float g = key_value(prefix);
-    float mx = NEG_INF;
-    for (int v = threadIdx.x; v < V; v += NT) {
-        const float x = load_logit(row, DT, v);
-        if (x >= g) mx = fmaxf(mx, x);
-    }
-    const float M = block_max(mx, sh_f);
-    const float MC = M * P.c;
-    float s = 0.f;
-    if (M != NEG_INF)
+    for (int r = 0; r < P.R; ++r) {
+        const int row_id = b * P.R + r;
+        if (!__ldcg(&P.rstats[row_id].dense)) continue;  // the same for every thread
+        const char* row = spec_row_ptr(P, b, r);
+        // exact k-th largest key by bitwise search over full-row counts
+        uint32_t prefix = 0;
+        constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+        for (int bit = 31; bit >= lo; --bit) {
+            const uint32_t want = prefix | (1u << bit);
+            int cnt = 0;
+            for (int v = threadIdx.x; v < V; v += NT) cnt += okey(load_logit(row, DT, v)) >= want;
+            if (block_sum_int(cnt, sh_red) >= k) prefix = want;
+        }
+        if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+        const float g = key_value(prefix);
+        float mx = NEG_INF;
         for (int v = threadIdx.x; v < V; v += NT) {
             const float x = load_logit(row, DT, v);
-            if (x >= g) s += ex2(fmaf(x, P.c, -MC));
+            if (x >= g) mx = fmaxf(mx, x);
         }
-    const double S = block_sum_f32(s, sh_d);
-    if (threadIdx.x == 0) {
-        RowStats st;
-        st.M = M; st.MC = MC; st.S = S; st.thr = g;
-        st.status = (M != NEG_INF && isfinite(M) && S > 0.0) ? ROW_OK : ROW_NONFINITE;
-        st.klist_n = -1;
-        st.dense = 1;
-        P.rstats[row_id] = st;
+        const float M = block_max(mx, sh_f);
+        const float MC = M * P.c;
+        float s = 0.f;
+        if (M != NEG_INF)
+            for (int v = threadIdx.x; v < V; v += NT) {
+                const float x = load_logit(row, DT, v);
+                if (x >= g) s += ex2(fmaf(x, P.c, -MC));
+            }
+        const double S = block_sum_f32(s, sh_d);
+        if (threadIdx.x == 0) {
+            RowStats st;
+            st.M = M; st.MC = MC; st.S = S; st.thr = g;
+            st.status = (M != NEG_INF && isfinite(M) && S > 0.0) ? ROW_OK : ROW_NONFINITE;
+            st.klist_n = -1;
+            st.dense = 1;
+            P.rstats[row_id] = st;
+        }
+        __syncthreads();
     }
-    const unsigned nd = (unsigned)__ldcg(&P.ndense[b]);
-    if (!arrive_last(&P.dense_ctr[b], nd, &sh_flag)) return;
-    if (threadIdx.x == 0) P.ndense[b] = 0;
 
     __shared__ Plan sh_plan;
     if (threadIdx.x < 32) {
@@ -969,7 +970,7 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
     launch_dependent(topk_finish_kernel<DT>, (unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, fsm,
                      st, P);
-    launch_dependent(topk_dense_kernel<DT>, (unsigned)((long long)P.B * P.R), NT, 0, st, P);
+    launch_dependent(topk_dense_kernel<DT>, (unsigned)P.B, NT, 0, st, P);
 }
 
 cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st)
