@@ -331,6 +331,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
                  :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol) : "memory");
 }
 
+// One arrival on `bar` (release: this thread's earlier shared-memory reads are ordered before it).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
 // Bounded wait for the phase with parity `parity` of `bar` to complete; false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
 {
@@ -355,13 +361,13 @@ constexpr int STREAM_SMEM = STREAM_STAGES * STREAM_CHUNK_BYTES;
 // persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task (the occupancy query
 // runs once per kernel)
 template <auto K>
-inline unsigned cta_grid(long long tasks, int sms, size_t smem)
+inline unsigned cta_grid(long long tasks, int sms, size_t smem, int threads = NT)
 {
     static int per_sm = 0;
     if (per_sm < 1) {
         int n = 0;
         if (smem > 48 * 1024) cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, NT, smem) != cudaSuccess || n < 1) n = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, threads, smem) != cudaSuccess || n < 1) n = 1;
         per_sm = n;
     }
     const long long cap = (long long)per_sm * sms;

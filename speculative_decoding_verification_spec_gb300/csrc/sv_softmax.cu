@@ -306,20 +306,41 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
     bool failed = false;  // a bulk-copy wait ran out: the remaining chunks are reported, not read
     long long fail_it = 0;
     long long it = 0;
+    int stg = 0;          // it % STREAM_STAGES
+    unsigned phase = 0;   // (it / STREAM_STAGES) & 1
+    // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
+    int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
+    const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
     for (int id = blockIdx.x; id < nch; id += G0, ++it) {
-        const int row_id = id / P.S1, ci = id - row_id * P.S1;
+        if (id != blockIdx.x) {
+            row_id += drow;
+            ci += dci;
+            if (ci >= P.S1) {
+                ci -= P.S1;
+                ++row_id;
+            }
+            if (++stg == STREAM_STAGES) {
+                stg = 0;
+                phase ^= 1u;
+            }
+        }
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
         const bool partial = cbase + CHUNK > cend;
-        const int s = (int)(it % STREAM_STAGES);
+        const int s = stg;
         bool ok = !failed;
-        if (ok) ok = mbar_wait(&full[s], (unsigned)(it / STREAM_STAGES) & 1u);
+        if (ok) ok = mbar_wait(&full[s], phase);
         uint4 w[STREAM_NV];
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-        const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
+        const uint4* sb = ring + (size_t)s * NT * STREAM_NV + tid;
+        if (ok && !partial) {
 #pragma unroll
-        for (int j = 0; j < STREAM_NV; ++j) {
-            w[j] = make_uint4(pad, pad, pad, pad);
-            if (ok && (!partial || cbase + (j * NT + tid) * VEC < cend)) w[j] = lds128(sb + j * NT + tid);
+            for (int j = 0; j < STREAM_NV; ++j) w[j] = lds128(sb + j * NT);
+        } else {
+#pragma unroll
+            for (int j = 0; j < STREAM_NV; ++j) {
+                w[j] = make_uint4(pad, pad, pad, pad);
+                if (ok && cbase + (j * NT + tid) * VEC < cend) w[j] = lds128(sb + j * NT);
+            }
         }
         // every thread has read its part of the stage: it can be refilled
         const int anyfail = __syncthreads_or(!ok);

@@ -6,18 +6,16 @@
 // at the threshold are all kept.
 //
 // Kernel 1 (topk_stream_kernel) streams every logit row once.  Rows are cut into 32 KB chunks and
-// runs of chunks (segments, at most 4 per row); persistent CTAs take segments round-robin and, for
-// 16-byte aligned rows, fetch their chunks with bulk copies (TMA engine) into a ring of TK_STAGES
-// shared-memory stages, so the next chunks are in flight while one is filtered.  Each thread holds
-// its 64 (bf16) or 32 (fp32) elements of a chunk in registers.  The k-th largest of the NT
-// per-thread maxima (NT disjoint groups, so at least k chunk elements are >= it) bounds the chunk's
-// k-th largest value from below; every warp selects it from shared memory by itself, so no warp
-// waits for another.  With the bound carried over from the segment's earlier chunks it forms beta,
-// and only elements >= beta -- a few dozen per chunk at k = 50 -- join the segment's candidate set
-// in shared memory.  When the set grows large, and at the end of the segment, one warp cuts it to
-// the entries >= its exact k-th largest value, which becomes the new bound; the segment's list is
-// what remains.  Every bound is <= the row's k-th largest value g, so the lists hold every
-// element >= g.
+// runs of chunks (segments, at most 4 per row); persistent CTAs take segments round-robin.  For
+// 16-byte aligned rows a producer warp fetches the chunks with bulk copies (TMA engine) into a ring
+// of TK_STAGES shared-memory stages, so the next chunks are in flight while one is filtered.  Each
+// consumer thread holds its 64 (bf16) or 32 (fp32) elements of a chunk in registers; the consumer
+// warps run independently of one another and meet once per segment.  The k-th largest of the NT
+// per-thread maxima of a segment's first chunk (NT disjoint groups, so at least k elements are >=
+// it) bounds the segment's k-th largest value from below; a histogram of the candidates found so
+// far tightens the bound as the segment proceeds.  Only elements >= the bound -- a few dozen per
+// chunk at k = 50 -- join the warp's candidate list for the segment.  Every bound is <= the row's
+// k-th largest value g, so the lists hold every element >= g.
 //
 // Kernel 2 (topk_finish_kernel), one warp per row, selects g exactly from the union of the row's
 // candidate lists, keeps the entries >= g sorted by index and forms the normaliser (M, S).  The
@@ -39,6 +37,10 @@ constexpr int TK_STAGES = STREAM_STAGES;                // bulk-copy ring depth
 constexpr int TK_SMEM = STREAM_SMEM;                    // dynamic shared memory of kernel 1
 // per-chunk candidate count codes
 constexpr int TK_OVERFLOW = -1, TK_NONFINITE = -2, TK_TIMEOUT = -3;
+constexpr int TK_PRODUCER = WARPS;         // kernel 1: the bulk-copy producer warp
+constexpr int TK_THREADS = NT + 32;        // kernel 1: WARPS consumer warps + the producer warp
+// the consumer warps of kernel 1 meet at named barrier 1 (the producer warp never waits there)
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory"); }
 
 // order-preserving 32-bit key of a float; -0 and +0 map to the same key
 __device__ __forceinline__ uint32_t okey(float x)
@@ -325,17 +327,26 @@ struct SegCursor {
     }
 };
 
-// Kernel 1.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage ring; otherwise
-// element loads straight into registers.  A CTA takes segments (runs of up to P.sps chunks of one
-// row) round-robin and streams them chunk by chunk, one CTA barrier per chunk.  Each warp appends
-// the elements of its part of a chunk that are at or above the current bound beta to its own list
-// for the segment (no atomics), and counts each in a histogram of its value above the segment's
-// first bound (bins 2^16 apart in the order-preserving key: one bf16 value per bin).  After the
-// barrier warp 1 reads the histogram -- every count in it is a real element of the segment -- and
-// the lowest bin edge with at least k counted elements above it becomes the bound for the next
-// chunk.
+// Kernel 1: warp-specialised.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage
+// ring by a producer warp; otherwise the consumer warps load their elements straight into
+// registers.  A CTA takes segments (runs of up to P.sps chunks of one row) round-robin.
+//
+// Producer (warp WARPS, one lane): for every chunk in the CTA's order it waits until all consumer
+// warps have released the stage (an "empty" mbarrier per stage) and refills it with one bulk copy
+// (a "full" mbarrier per stage completes when the bytes land).
+//
+// Consumers (warps 0..WARPS-1): each waits on its chunk's full barrier, reads its 64 (bf16) or 32
+// (fp32) elements into registers, releases the stage and filters them on its own: warps meet only
+// at the start of each segment (a named barrier of the consumer warps), where the k-th largest of
+// the NT thread maxima of the segment's first chunk gives the segment's first bound tau.  Each warp
+// appends its elements at or above the current bound beta to its own list for the segment (no
+// atomics) and counts each in a histogram of its value above tau (bins 2^16 apart in the
+// order-preserving key: one bf16 value per bin).  Warp 1 turns the histogram -- every count in it
+// is a real element of the segment, whichever chunks the other warps have reached -- into a
+// tighter bound: the lowest bin edge with at least k counted elements above it, published as one
+// 64-bit word (segment, key) that every warp reads before its next chunk.
 template <int DT, bool BULK>
-__global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
+__global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P)
 {
     constexpr int NREG = TK_NREG;
     constexpr int EPT = (DT == DT_BF16) ? 2 * NREG : NREG;  // elements per thread
@@ -346,12 +357,12 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     constexpr int HW = (WARPS > 1) ? 1 : 0;  // the warp that turns the histogram into a bound
     static_assert(NREG % G == 0, "register groups");
     extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
-    __shared__ float tmax[2][NT];      // thread maxima of the chunk (alternating)
-    __shared__ int hist[2][TK_BINS];   // per segment (alternating)
-    __shared__ int sbad[3];            // a NaN or +inf was seen in the chunk (cleared two chunks on)
-    __shared__ float pub_beta[2];      // bound published for segment pub_seg
-    __shared__ int pub_seg[2];         // -1: none
+    __shared__ float tmax[2][NT];      // thread maxima of a segment's first chunk (by segment parity)
+    __shared__ int hist[2][TK_BINS];   // by segment parity
+    __shared__ unsigned long long pub; // (segment << 32) | key of the latest bound published for it
+    __shared__ int sfail;              // a wait ran out in this CTA: nothing more is read
     __shared__ __align__(8) uint64_t full[TK_STAGES];
+    __shared__ __align__(8) uint64_t empty[TK_STAGES];
 
     pdl_trigger();  // the finish kernel may be scheduled as SMs free up; it waits for this grid
     clear_counters(P.ctr_clear, P.ctr_words);
@@ -360,83 +371,117 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
     const int nsegs = P.B * P.R * P.nsegr;
     const int G0 = gridDim.x;
     const int k = P.top_k;
-    const uint64_t pol = policy_evict_first();
 
-    // producer (thread 0): the next (segment, chunk) to fetch, in this CTA's consumption order
-    SegCursor pc;
-    pc.init(blockIdx.x, G0, P.nsegr);
-    int pst = 0, pnst = 0;
-    const char* prow = nullptr;
-    long long nissued = 0;
-    auto pseg_setup = [&]() {
-        if (pc.sg < nsegs) {
-            pnst = min(P.sps, P.CT - pc.si * P.sps);
-            prow = spec_row_ptr(P, pc.row_id / P.R, pc.row_id % P.R);
-        }
-    };
-    auto issue_next = [&](int s) {
-        if (pc.sg >= nsegs) return;
-        const int cbase = (pc.si * P.sps + pst) * CHUNK;
-        const int cend = min(cbase + CHUNK, P.V);
-        bulk_load(ring + (size_t)s * NT * TK_NV, prow + (size_t)cbase * ES, (unsigned)(cend - cbase) * ES,
-                  &full[s], pol);
-        ++nissued;
-        if (++pst == pnst) {
-            pst = 0;
-            pc.next(G0, P.nsegr);
-            pseg_setup();
-        }
-    };
-
-    hist[0][tid] = 0;
+    if (tid < NT) hist[0][tid] = 0;
     if (tid == 0) {
-        sbad[0] = sbad[1] = sbad[2] = 0;
-        pub_beta[0] = pub_beta[1] = NEG_INF;
-        pub_seg[0] = pub_seg[1] = -1;
+        pub = ~0ull;  // segment field 0xffffffff: no bound yet
+        sfail = 0;
         if constexpr (BULK) {
-            pseg_setup();
-            for (int s = 0; s < TK_STAGES; ++s) mbar_init(&full[s], 1);
+            for (int s = 0; s < TK_STAGES; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], WARPS);
+            }
             fence_mbar_init();
-            for (int s = 0; s < TK_STAGES; ++s) issue_next(s);
         }
     }
     __syncthreads();
 
-    // every warp: the current segment (uniform across the CTA) and this warp's list for it
-    int jseg = -1;               // this CTA's segment counter (selects hist)
-    int seg_bad = 0;
-    float tau_first = NEG_INF;   // the segment's first bound; histogram bins count from its key
-    uint32_t key0 = 0;
-    int wcount = 0;              // entries in this warp's list
+    // ------------------------------------------------------------------ producer warp
+    if (warp == TK_PRODUCER) {
+        if constexpr (BULK) {
+            if (lane == 0) {
+                const uint64_t pol = policy_evict_first();
+                SegCursor pc;
+                pc.init(blockIdx.x, G0, P.nsegr);
+                int stg = 0;
+                unsigned ph = 0;
+                long long n = 0;  // copies issued
+                bool ok = true;
+                for (; ok && pc.sg < nsegs; pc.next(G0, P.nsegr)) {
+                    const int nst = min(P.sps, P.CT - pc.si * P.sps);
+                    const char* row = spec_row_ptr(P, pc.row_id / P.R, pc.row_id % P.R);
+                    for (int st = 0; st < nst; ++st) {
+                        // the stage's previous fill released by every consumer warp (bounded)
+                        if (n >= TK_STAGES && !mbar_wait(&empty[stg], ph ^ 1u)) ok = false;
+                        if (ok && *reinterpret_cast<volatile int*>(&sfail)) ok = false;
+                        if (!ok) break;
+                        const int cbase = (pc.si * P.sps + st) * CHUNK;
+                        const int cend = min(cbase + CHUNK, P.V);
+                        bulk_load(ring + (size_t)stg * NT * TK_NV, row + (size_t)cbase * ES,
+                                  (unsigned)(cend - cbase) * ES, &full[stg], pol);
+                        ++n;
+                        if (++stg == TK_STAGES) {
+                            stg = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) *reinterpret_cast<volatile int*>(&sfail) = 1;
+                // the CTA may not leave while a copy is in flight: wait (bounded) for the last fill
+                // of every stage -- no later fill of that stage exists, so its phase is unambiguous
+                for (long long j = (n > TK_STAGES ? n - TK_STAGES : 0); j < n; ++j)
+                    (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u);
+            }
+        }
+        return;
+    }
 
-    bool failed = false;  // a bulk-copy wait ran out: the remaining segments are reported, not read
-    long long fail_it = 0;
-    long long it = 0;
+    // ------------------------------------------------------------------ consumer warps
+    int stg = 0;          // ring stage of the next chunk
+    unsigned ph = 0;      // its fill parity
+    int jseg = -1;        // this CTA's segment counter (selects tmax and hist)
+    bool failed = false;  // a bulk-copy wait ran out: the remaining lists are marked, not filled
     SegCursor cc;
     cc.init(blockIdx.x, G0, P.nsegr);
     for (; cc.sg < nsegs; cc.next(G0, P.nsegr)) {
         const int sg = cc.sg;
+        ++jseg;
         const int nst = min(P.sps, P.CT - cc.si * P.sps);
         const char* row = BULK ? nullptr : spec_row_ptr(P, cc.row_id / P.R, cc.row_id % P.R);
         TopkEntry* wlist = P.clist + ((size_t)sg * WARPS + warp) * P.cap_s;
-        for (int st = 0; st < nst; ++st, ++it) {
+        int wcount = 0;              // entries in this warp's list
+        int seg_bad = 0;             // this warp saw a NaN or +inf in the segment
+        float tau_first = NEG_INF;   // the segment's first bound; histogram bins count from its key
+        uint32_t key0 = 0;
+        for (int st = 0; st < nst; ++st) {
             const int cbase = (cc.si * P.sps + st) * CHUNK;
             const int cend = min(cbase + CHUNK, P.V);
             const bool partial = cbase + CHUNK > cend;
 
             // ---- the chunk into registers (-inf padding past the row's end)
             uint32_t w[NREG];
-            bool ok = !failed;
+            if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
             if constexpr (BULK) {
-                const int s = (int)(it % TK_STAGES);
-                if (ok) ok = mbar_wait(&full[s], (unsigned)(it / TK_STAGES) & 1u);
-                const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-                const uint4* sb = ring + (size_t)s * NT * TK_NV;
+                bool ok = !failed && mbar_wait(&full[stg], ph);
+                const uint4* sb = ring + (size_t)stg * NT * TK_NV + tid;
+                if (ok && !partial) {
 #pragma unroll
-                for (int j = 0; j < TK_NV; ++j) {
-                    uint4 q = make_uint4(pad, pad, pad, pad);
-                    if (ok && (!partial || cbase + (j * NT + tid) * VEC < cend)) q = lds128(sb + j * NT + tid);
-                    w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
+                    for (int j = 0; j < TK_NV; ++j) {
+                        const uint4 q = lds128(sb + j * NT);
+                        w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
+                    }
+                } else {
+                    const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+                    for (int j = 0; j < TK_NV; ++j) {
+                        uint4 q = make_uint4(pad, pad, pad, pad);
+                        if (ok && cbase + (j * NT + tid) * VEC < cend) q = lds128(sb + j * NT);
+                        w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
+                    }
+                }
+                // release the stage once every lane has read it; a warp whose wait ran out never
+                // releases it (its copy may still land), which stops the producer
+                ok = __all_sync(FULL, ok);
+                if (ok) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stg]);
+                } else if (!failed) {
+                    failed = true;
+                    if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
+                }
+                if (++stg == TK_STAGES) {
+                    stg = 0;
+                    ph ^= 1u;
                 }
             } else {
                 if constexpr (DT == DT_BF16) {
@@ -481,96 +526,79 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
 #pragma unroll
                 for (int g = 1; g < NG; ++g) tm = fmax_nan_f(tm, __uint_as_float(gm[g]));
             }
-            tmax[it & 1][tid] = tm;
-            if (tm != tm || tm == __int_as_float(0x7f800000)) sbad[it % 3] = 1;
-            // every thread has read its part of the stage and published its maximum; every warp
-            // has collected the previous chunk
-            const int anyfail = __syncthreads_or(!ok);
-            if (anyfail && !failed) {
-                failed = true;
-                fail_it = it;
-            }
-            if (tid == 0) sbad[(it + 2) % 3] = 0;  // the previous chunk's flag, read by all by now
-            if constexpr (BULK) {
-                // the barrier above ordered every read of this stage before its refill
-                if (tid == 0 && !failed) issue_next((int)(it % TK_STAGES));
+            seg_bad |= __any_sync(FULL, tm != tm || tm == __int_as_float(0x7f800000));
+
+            // ---- a segment's first chunk: every consumer warp meets here once per segment (failed
+            // or not), after which the thread maxima are complete and the previous segment is done
+            // by all, so its histogram can be cleared for the segment after this one
+            if (st == 0) {
+                tmax[jseg & 1][tid] = tm;
+                consumer_sync();
+                hist[(jseg + 1) & 1][tid] = 0;
+                // tau = the k-th largest thread maximum (valid for k <= NT), selected by every
+                // warp by itself
+                if (k <= NT) {
+                    uint32_t keys[NT / 32];
+#pragma unroll
+                    for (int i = 0; i < NT / 32; ++i) keys[i] = okey(tmax[jseg & 1][lane + 32 * i]);
+                    uint32_t prefix = 0;
+                    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+                    for (int bit = 31; bit >= lo; --bit) {
+                        const uint32_t want = prefix | (1u << bit);
+                        unsigned cnt = 0;
+#pragma unroll
+                        for (int i = 0; i < NT / 32; ++i) cnt += keys[i] >= want;
+                        if ((int)__reduce_add_sync(FULL, cnt) >= k) prefix = want;
+                    }
+                    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+                    tau_first = key_value(prefix);
+                    key0 = prefix;
+                }
             }
             if (failed) {
                 if (lane == 0 && st + 1 == nst) P.ccount[(size_t)sg * WARPS + warp] = TK_TIMEOUT;
                 continue;
             }
-
-            // ---- a new segment: fresh counters, and the bound tau = the k-th largest thread
-            // maximum of its first chunk (valid for k <= NT), selected by every warp by itself
-            if (st == 0) {
-                ++jseg;
-                hist[(jseg + 1) & 1][tid] = 0;  // for the segment after this one
-                seg_bad = 0;
-                tau_first = NEG_INF;
-                wcount = 0;
-            }
-            const int bad = sbad[it % 3];
-            seg_bad |= bad;
-            if (st == 0 && !bad && k <= NT) {
-                uint32_t keys[NT / 32];
-#pragma unroll
-                for (int i = 0; i < NT / 32; ++i) keys[i] = okey(tmax[it & 1][lane + 32 * i]);
-                uint32_t prefix = 0;
-                constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-                for (int bit = 31; bit >= lo; --bit) {
-                    const uint32_t want = prefix | (1u << bit);
-                    unsigned cnt = 0;
-#pragma unroll
-                    for (int i = 0; i < NT / 32; ++i) cnt += keys[i] >= want;
-                    if ((int)__reduce_add_sync(FULL, cnt) >= k) prefix = want;
-                }
-                if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-                tau_first = key_value(prefix);
-                key0 = prefix;
-            }
             float beta = tau_first;
-            if (pub_seg[it & 1] == sg) beta = fmaxf(beta, pub_beta[it & 1]);
+            {
+                const unsigned long long pb = *reinterpret_cast<volatile unsigned long long*>(&pub);
+                if ((int)(pb >> 32) == sg) beta = fmaxf(beta, key_value((uint32_t)pb));
+            }
 
-            // ---- warp HW: the bound for the next chunk from the histogram (the counts of this
-            // chunk may be partly in: every count is a real element of the segment either way)
-            if (warp == HW) {
-                float nb = NEG_INF;
-                if (!seg_bad && k <= NT && st + 1 < nst && st < TK_HIST_CHUNKS && tau_first != NEG_INF) {
-                    int c8 = 0;
-                    int hb[TK_BINS / 32];
+            // ---- warp HW: a tighter bound from the histogram (counts of every warp so far)
+            if (warp == HW && !seg_bad && k <= NT && st + 1 < nst && st < TK_HIST_CHUNKS &&
+                tau_first != NEG_INF) {
+                int c8 = 0;
+                int hb[TK_BINS / 32];
 #pragma unroll
-                    for (int i = 0; i < TK_BINS / 32; ++i) {
-                        hb[i] = hist[jseg & 1][lane * (TK_BINS / 32) + i];
-                        c8 += hb[i];
-                    }
-                    // counts in this lane's bins and above
-                    int suf = c8;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int v = __shfl_down_sync(FULL, suf, o);
-                        if (lane + o < 32) suf += v;
-                    }
-                    const unsigned reach = __ballot_sync(FULL, suf >= k);
-                    if (reach) {
-                        const int ls = 31 - __clz(reach);  // highest lane whose suffix reaches k
-                        int bin = -1;
-                        if (lane == ls) {
-                            int acc = suf - c8;  // counts above this lane's bins
-#pragma unroll
-                            for (int i = TK_BINS / 32 - 1; i >= 0; --i) {
-                                acc += hb[i];
-                                if (bin < 0 && acc >= k) bin = lane * (TK_BINS / 32) + i;
-                            }
-                        }
-                        bin = __shfl_sync(FULL, bin, ls);
-                        nb = key_value(key0 + ((uint32_t)bin << 16));
-                    }
+                for (int i = 0; i < TK_BINS / 32; ++i) {
+                    hb[i] = hist[jseg & 1][lane * (TK_BINS / 32) + i];
+                    c8 += hb[i];
                 }
-                // past the first chunks the bound is left as it is (carried to the next slot)
-                if (st >= TK_HIST_CHUNKS && pub_seg[it & 1] == sg) nb = pub_beta[it & 1];
-                if (lane == 0) {
-                    pub_beta[(it + 1) & 1] = nb;
-                    pub_seg[(it + 1) & 1] = (nb != NEG_INF) ? sg : -1;
+                // counts in this lane's bins and above
+                int suf = c8;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_down_sync(FULL, suf, o);
+                    if (lane + o < 32) suf += v;
+                }
+                const unsigned reach = __ballot_sync(FULL, suf >= k);
+                if (reach) {
+                    const int ls = 31 - __clz(reach);  // highest lane whose suffix reaches k
+                    int bin = -1;
+                    if (lane == ls) {
+                        int acc = suf - c8;  // counts above this lane's bins
+#pragma unroll
+                        for (int i = TK_BINS / 32 - 1; i >= 0; --i) {
+                            acc += hb[i];
+                            if (bin < 0 && acc >= k) bin = lane * (TK_BINS / 32) + i;
+                        }
+                    }
+                    bin = __shfl_sync(FULL, bin, ls);
+                    const uint32_t nk = key0 + ((uint32_t)bin << 16);
+                    if (lane == 0 && key_value(nk) > beta)
+                        *reinterpret_cast<volatile unsigned long long*>(&pub) =
+                            ((unsigned long long)(unsigned)sg << 32) | nk;
                 }
             }
 
@@ -639,12 +667,6 @@ __global__ void __launch_bounds__(NT, 2) topk_stream_kernel(SpecParams P)
                 P.ccount[(size_t)sg * WARPS + warp] =
                     seg_bad ? TK_NONFINITE : (k > NT || wcount > P.cap_s) ? TK_OVERFLOW : wcount;
         }
-    }
-    // after a failed wait, let the copies still in flight land before the CTA leaves (bounded)
-    if constexpr (BULK) {
-        if (failed && tid == 0)
-            for (long long j = fail_it; j < nissued && j < fail_it + TK_STAGES; ++j)
-                (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u);
     }
 }
 
@@ -960,10 +982,10 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
     mark_kernel_start(st);
     if (P.vec > 1) {
         constexpr auto K1 = topk_stream_kernel<DT, true>;
-        K1<<<cta_grid<K1>(nsegs, sms, TK_SMEM), NT, TK_SMEM, st>>>(P);
+        K1<<<cta_grid<K1>(nsegs, sms, TK_SMEM, TK_THREADS), TK_THREADS, TK_SMEM, st>>>(P);
     } else {
         constexpr auto K1 = topk_stream_kernel<DT, false>;
-        K1<<<cta_grid<K1>(nsegs, sms, 0), NT, 0, st>>>(P);
+        K1<<<cta_grid<K1>(nsegs, sms, 0, TK_THREADS), TK_THREADS, 0, st>>>(P);
     }
     mark_kernel_stop(st);
     const size_t fsm = (size_t)WARPS * (TK_UNION + P.cap_k) * sizeof(TopkEntry);

@@ -318,12 +318,28 @@ __global__ void __launch_bounds__(NT, 2) tree_stream_kernel(TreeParams P)
     bool failed = false;
     long long fail_it = 0;
     long long it = 0;
+    int stg = 0;          // it % STREAM_STAGES
+    unsigned phase = 0;   // (it / STREAM_STAGES) & 1
+    // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
+    int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
+    const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
     for (int id = blockIdx.x; id < nch; id += G0, ++it) {
-        const int row_id = id / P.S1, ci = id - row_id * P.S1;
+        if (id != blockIdx.x) {
+            row_id += drow;
+            ci += dci;
+            if (ci >= P.S1) {
+                ci -= P.S1;
+                ++row_id;
+            }
+            if (++stg == STREAM_STAGES) {
+                stg = 0;
+                phase ^= 1u;
+            }
+        }
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
-        const int s = (int)(it % STREAM_STAGES);
+        const int s = stg;
         bool ok = !failed;
-        if (ok) ok = mbar_wait(&full[s], (unsigned)(it / STREAM_STAGES) & 1u);
+        if (ok) ok = mbar_wait(&full[s], phase);
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
         const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
         uint4 w[STREAM_NV];
