@@ -78,7 +78,7 @@ struct SpecLayout {
     size_t ctr_bytes = 0, bytes = 0;
     size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0, o_work = 0;
     size_t o_partials = 0, o_rstats = 0, o_plan = 0, o_segs = 0;
-    size_t o_clist = 0, o_ccount = 0, o_klist = 0;
+    size_t o_clist = 0, o_cdata = 0, o_ccount = 0, o_klist = 0;
 };
 
 // Byte layout for `ppr` softmax partials per row, nseg residual segments per request and (top-k)
@@ -104,6 +104,7 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
     if (topk) {
         L.o_clist = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * cap_s * sizeof(TopkEntry));
+        L.o_cdata = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * cap_s * sizeof(uint4));
         L.o_ccount = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * sizeof(int));
         L.o_klist = o; o = align_up(o + (size_t)B * R * cap_k * sizeof(TopkEntry));
     }
@@ -246,6 +247,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.segs = reinterpret_cast<float*>(ws + L.o_segs);
     if (topk) {
         P.clist = reinterpret_cast<TopkEntry*>(ws + L.o_clist);
+        P.cdata = reinterpret_cast<uint4*>(ws + L.o_cdata);
         P.ccount = reinterpret_cast<int*>(ws + L.o_ccount);
         P.klist = reinterpret_cast<TopkEntry*>(ws + L.o_klist);
     }

@@ -123,7 +123,9 @@ struct SpecParams {
     unsigned* req_ctr;    // [B]
     unsigned* res_ctr;    // [B]
     unsigned* work;       // [2] task counters of the two streaming kernels
-    TopkEntry* clist;     // [B*R*nsegr*WARPS*cap_s] per (segment, warp): candidates (unordered)
+    TopkEntry* clist;     // [B*R*nsegr*WARPS*cap_s] per (segment, warp): candidate groups (unordered):
+                          // the group's maximum and the index of its first element
+    uint4* cdata;         // [same] the candidate group's raw 16 bytes (8 bf16 or 4 fp32 logits)
     int* ccount;          // [B*R*nsegr*WARPS] entries listed, or TK_NONFINITE / TK_OVERFLOW / TK_TIMEOUT
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
     unsigned* dense_ctr;  // [B]

@@ -79,19 +79,6 @@ __device__ uint32_t warp_kth_key(int n, int k, KeyAt key_at)
     return prefix;
 }
 
-// w[base + j] for a run-time j in [0, 8) and a compile-time base, by a select tree (no local memory)
-template <int N>
-__device__ __forceinline__ uint32_t select8(const uint32_t (&w)[N], int base, int j)
-{
-    const uint32_t a0 = (j & 1) ? w[base + 1] : w[base];
-    const uint32_t a1 = (j & 1) ? w[base + 3] : w[base + 2];
-    const uint32_t a2 = (j & 1) ? w[base + 5] : w[base + 4];
-    const uint32_t a3 = (j & 1) ? w[base + 7] : w[base + 6];
-    const uint32_t c0 = (j & 2) ? a1 : a0;
-    const uint32_t c1 = (j & 2) ? a3 : a2;
-    return (j & 4) ? c1 : c0;
-}
-
 // Warp-level bitonic sort of e[0..n) by index (ascending), padding to a power of two.
 __device__ void warp_sort_by_index(TopkEntry* e, int n)
 {
@@ -202,22 +189,6 @@ __device__ __forceinline__ int slot_elem(int cbase, int s)
 {
     if constexpr (VEC == 1) return cbase + s * NT + (int)threadIdx.x;
     else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
-}
-
-// Bits of a group's passing-slot mask (as built in topk_stream_kernel) whose elements lie before
-// cend.  Group g holds registers 8g..8g+7 of the thread: for bf16 bit j is the low half of register
-// 8g+j and bit 16+j its high half; for fp32 bit j is register 8g+j.
-template <int DT, int VEC>
-__device__ __forceinline__ uint32_t valid_bits(int cbase, int cend, int g)
-{
-    uint32_t m = 0;
-    constexpr int PER = (DT == DT_BF16) ? 2 : 1;  // elements per register
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int h = 0; h < PER; ++h)
-            if (slot_elem<VEC>(cbase, PER * (8 * g + j) + h) < cend) m |= 1u << (j + 16 * h);
-    return m;
 }
 
 // The k-th largest (with multiplicity) of the keys key[j] (slots j < J, lanes with 32 j + lane <
@@ -353,7 +324,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     constexpr int CHUNK = NT * EPT;                          // elements per chunk
     constexpr int VEC = BULK ? ((DT == DT_BF16) ? 8 : 4) : 1;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
-    constexpr int G = 8, NG = NREG / G;
+    constexpr int G = 4, NG = NREG / G;        // groups of 4 registers: one 16-byte vector each
+    constexpr int EPG = (DT == DT_BF16) ? 2 * G : G;  // elements per group
     constexpr int HW = (WARPS > 1) ? 1 : 0;  // the warp that turns the histogram into a bound
     static_assert(NREG % G == 0, "register groups");
     extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
@@ -439,6 +411,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
         const int nst = min(P.sps, P.CT - cc.si * P.sps);
         const char* row = BULK ? nullptr : spec_row_ptr(P, cc.row_id / P.R, cc.row_id % P.R);
         TopkEntry* wlist = P.clist + ((size_t)sg * WARPS + warp) * P.cap_s;
+        uint4* wdata = P.cdata + ((size_t)sg * WARPS + warp) * P.cap_s;
         int wcount = 0;              // entries in this warp's list
         int seg_bad = 0;             // this warp saw a NaN or +inf in the segment
         float tau_first = NEG_INF;   // the segment's first bound; histogram bins count from its key
@@ -602,59 +575,46 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 }
             }
 
-            // ---- this warp's elements >= beta go to its list and to the histogram.  A group whose
-            // maximum reaches beta yields a bitmask of its passing slots (slots past the row's end
-            // masked off); positions come from a prefix sum over the warp.
+            // ---- this warp's groups whose maximum reaches beta go to its list: the maximum and
+            // the first element's index, and the group's 16 raw bytes; the maximum is counted in
+            // the histogram (maxima of distinct groups are distinct elements).  Positions come from
+            // a prefix sum over the warp.
             if (!seg_bad && k <= NT) {
                 // bf16: compare against beta rounded down to bf16, so no element >= beta is missed
                 const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(beta));
-                uint32_t bits[NG];
-                int mine = 0;
+                unsigned pass = 0;
 #pragma unroll
                 for (int g = 0; g < NG; ++g) {
-                    uint32_t bt = 0;
-                    if constexpr (DT == DT_BF16) {
-                        if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2)) {
-#pragma unroll
-                            for (int j = 0; j < G; ++j) {
-                                const uint32_t wd = w[g * G + j];
-                                bt |= (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd), t2) & 0x00010001u) << j;
-                            }
-                        }
-                    } else {
-                        if (__uint_as_float(gm[g]) >= beta) {
-#pragma unroll
-                            for (int j = 0; j < G; ++j) bt |= (uint32_t)(__uint_as_float(w[g * G + j]) >= beta) << j;
-                        }
-                    }
-                    if (partial && bt) bt &= valid_bits<DT, VEC>(cbase, cend, g);
-                    bits[g] = bt;
-                    mine += __popc(bt);
+                    bool ge;
+                    if constexpr (DT == DT_BF16) ge = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2) != 0u;
+                    else ge = __uint_as_float(gm[g]) >= beta;
+                    pass |= (unsigned)ge << g;
                 }
+                if (partial && pass) {  // groups that start past the row's end hold padding only
+#pragma unroll
+                    for (int g = 0; g < NG; ++g)
+                        if (slot_elem<VEC>(cbase, EPG * g) >= cend) pass &= ~(1u << g);
+                }
+                const int mine = __popc(pass);
                 if (__any_sync(FULL, mine)) {
                     const int incl = warp_incl_scan(mine);
                     int pos = wcount + incl - mine;
                     wcount += __shfl_sync(FULL, incl, 31);
                     int* h = hist[jseg & 1];
+                    const bool count = st < TK_HIST_CHUNKS - 1 && tau_first != NEG_INF;
 #pragma unroll
                     for (int g = 0; g < NG; ++g) {
-                        uint32_t bt = bits[g];
-                        while (bt) {
-                            const int bp = __ffs(bt) - 1;
-                            bt &= bt - 1;
-                            const int j = bp & 15, half = bp >> 4;  // register j of the group, bf16 half
-                            const uint32_t wd = select8(w, g * G, j);
+                        if (pass & (1u << g)) {
                             TopkEntry en;
-                            if constexpr (DT == DT_BF16) {
-                                en.x = half ? bf16hi(wd) : bf16lo(wd);
-                                en.idx = slot_elem<VEC>(cbase, 2 * (g * G + j) + half);
-                            } else {
-                                en.x = __uint_as_float(wd);
-                                en.idx = slot_elem<VEC>(cbase, g * G + j);
+                            if constexpr (DT == DT_BF16) en.x = fmaxf(bf16lo(gm[g]), bf16hi(gm[g]));
+                            else en.x = __uint_as_float(gm[g]);
+                            en.idx = slot_elem<VEC>(cbase, EPG * g);
+                            if (pos < P.cap_s) {
+                                wlist[pos] = en;
+                                wdata[pos] = make_uint4(w[G * g], w[G * g + 1], w[G * g + 2], w[G * g + 3]);
                             }
-                            if (pos < P.cap_s) wlist[pos] = en;
                             ++pos;
-                            if (st < TK_HIST_CHUNKS - 1 && tau_first != NEG_INF) {
+                            if (count) {
                                 const uint32_t kx = okey(en.x);
                                 if (kx >= key0) atomicAdd(&h[min((int)((kx - key0) >> 16), TK_BINS - 1)], 1);
                             }
@@ -670,9 +630,12 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     }
 }
 
-// Kernel 2, one warp per row: exact threshold g over the union of the row's lists (nsegr segments
-// x WARPS warps of kernel 1, up to TK_UNION entries), the kept list sorted by index, and the
-// normaliser over it.  u holds TK_UNION entries, kept cap_k.
+// Kernel 2, one warp per row: exact threshold g from the row's candidate groups (nsegr segments x
+// WARPS lists of kernel 1, up to TK_UNION groups), the kept list sorted by index, and the
+// normaliser over it.  The k-th largest group maximum tau_g is a lower bound of g (the maxima of
+// distinct groups are distinct elements), so only the groups whose maximum reaches tau_g can hold
+// an element >= g; their elements >= tau_g are the candidates from which g is selected exactly.
+// u holds TK_UNION entries, kept cap_k.
 template <int DT>
 __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry* kept, int row_id)
 {
@@ -724,9 +687,8 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
                 const int nn = __shfl_sync(FULL, n, l & 31);
                 v[t] = l < nl && i < nn;
                 if (v[t]) {
-                    const TopkEntry* src = lists + (size_t)l * P.cap_s + i;
-                    e[t].x = __ldcg(&src->x);
-                    e[t].idx = __ldcg(&src->idx);
+                    e[t].x = __ldcg(&lists[(size_t)l * P.cap_s + i].x);  // the group's maximum
+                    e[t].idx = l * P.cap_s + i;                          // its slot in the row's lists
                 }
             }
 #pragma unroll
@@ -739,8 +701,9 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     }
     __syncwarp();
 
-    // exact k-th largest key over the packed union, keys in registers (occupied slots only)
-    const int J = (total + 31) >> 5;
+    // tau_g: the k-th largest group maximum, keys in registers (occupied slots only); with fewer
+    // than k groups every group is expanded
+    int J = (total + 31) >> 5;
     uint32_t key[TK_KPL];
 #pragma unroll
     for (int j = 0; j < TK_KPL; ++j) {
@@ -748,14 +711,88 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
         if (j < J && 32 * j + lane < total) key[j] = okey(u[32 * j + lane].x);
     }
     const int k = P.top_k;
+    uint32_t gk = okey(NEG_INF);
+    if (total >= k) gk = warp_kth_key_hist<DT, TK_KPL>(key, J, total, k, reinterpret_cast<int*>(kept));
+    // the slots of the groups whose maximum reaches tau_g, compacted into kept
+    int ng = 0;
+#pragma unroll
+    for (int j = 0; j < TK_KPL; ++j) {
+        if (j < J) {
+            const bool keep = 32 * j + lane < total && key[j] >= gk;
+            const unsigned bal = __ballot_sync(FULL, keep);
+            const int pos = ng + __popc(bal & ((1u << lane) - 1u));
+            if (keep && pos < P.cap_k) kept[pos].idx = u[32 * j + lane].idx;
+            ng += __popc(bal);
+        }
+    }
+    __syncwarp();
+    if (ng > P.cap_k) { st.dense = 1; return st; }
+    // their elements >= tau_g inside the row are the candidates, packed into u (groups of 32 x 8
+    // at a time, every load of a batch issued before any is used)
+    constexpr int EPG = (DT == DT_BF16) ? 8 : 4;  // elements per group (one 16-byte vector)
+    const uint4* gdata = P.cdata + (size_t)row_id * nl * P.cap_s;
+    const int estride = (P.vec > 1) ? 1 : NT;     // index step between a group's elements
+    int ne = 0;
+    for (int r0 = 0; r0 < ng; r0 += 256) {
+        uint4 d[8];
+        int base[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int i = r0 + 32 * t + lane;
+            base[t] = P.V;  // nothing inside the row
+            if (i < ng) {
+                const int slot = kept[i].idx;
+                d[t] = __ldcg(gdata + slot);
+                base[t] = __ldcg(&lists[slot].idx);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (r0 + 32 * t >= ng) break;  // the same for every lane
+            const uint32_t wd[4] = {d[t].x, d[t].y, d[t].z, d[t].w};
+            float xe[EPG];
+            unsigned m = 0;
+#pragma unroll
+            for (int e = 0; e < EPG; ++e) {
+                if constexpr (DT == DT_BF16) xe[e] = (e & 1) ? bf16hi(wd[e >> 1]) : bf16lo(wd[e >> 1]);
+                else xe[e] = __uint_as_float(wd[e]);
+                if (base[t] + e * estride < P.V && okey(xe[e]) >= gk) m |= 1u << e;
+            }
+            const int c = __popc(m);
+            const int incl = warp_incl_scan(c);
+            int p = ne + incl - c;
+            ne += __shfl_sync(FULL, incl, 31);
+#pragma unroll
+            for (int e = 0; e < EPG; ++e) {
+                if (m & (1u << e)) {
+                    if (p < TK_UNION) {
+                        TopkEntry en;
+                        en.x = xe[e];
+                        en.idx = base[t] + e * estride;
+                        u[p] = en;
+                    }
+                    ++p;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (ne > TK_UNION) { st.dense = 1; return st; }
+    // g: the exact k-th largest candidate
+    J = (ne + 31) >> 5;
+#pragma unroll
+    for (int j = 0; j < TK_KPL; ++j) {
+        key[j] = 0u;
+        if (j < J && 32 * j + lane < ne) key[j] = okey(u[32 * j + lane].x);
+    }
     uint32_t gkey = okey(NEG_INF);
-    if (total >= k) gkey = warp_kth_key_hist<DT, TK_KPL>(key, J, total, k, reinterpret_cast<int*>(kept));
-    // the entries >= g, in union order
+    if (ne >= k) gkey = warp_kth_key_hist<DT, TK_KPL>(key, J, ne, k, reinterpret_cast<int*>(kept));
+    // the candidates >= g, in candidate order
     int nk = 0;
 #pragma unroll
     for (int j = 0; j < TK_KPL; ++j) {
         if (j < J) {
-            const bool keep = 32 * j + lane < total && key[j] >= gkey;
+            const bool keep = 32 * j + lane < ne && key[j] >= gkey;
             const unsigned bal = __ballot_sync(FULL, keep);
             const int pos = nk + __popc(bal & ((1u << lane) - 1u));
             if (keep && pos < P.cap_k) kept[pos] = u[32 * j + lane];
