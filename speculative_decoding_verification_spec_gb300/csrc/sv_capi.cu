@@ -78,7 +78,7 @@ struct SpecLayout {
     size_t ctr_bytes = 0, bytes = 0;
     size_t o_row_ctr = 0, o_req_ctr = 0, o_res_ctr = 0, o_dense_ctr = 0, o_ndense = 0, o_work = 0;
     size_t o_partials = 0, o_rstats = 0, o_plan = 0, o_segs = 0;
-    size_t o_clist = 0, o_cdata = 0, o_ccount = 0, o_klist = 0;
+    size_t o_clist = 0, o_cdata = 0, o_ccount = 0, o_cbound = 0, o_klist = 0;
 };
 
 // Byte layout for `ppr` softmax partials per row, nseg residual segments per request and (top-k)
@@ -103,9 +103,10 @@ static SpecLayout spec_layout(int B, int R, long long ppr, long long nseg, bool 
     L.o_plan = o; o = align_up(o + (size_t)B * sizeof(Plan));
     L.o_segs = o; o = align_up(o + (size_t)B * nseg * sizeof(float));
     if (topk) {
-        L.o_clist = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * cap_s * sizeof(TopkEntry));
-        L.o_cdata = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * cap_s * sizeof(uint4));
-        L.o_ccount = o; o = align_up(o + (size_t)B * R * nsegr * WARPS * sizeof(int));
+        L.o_clist = o; o = align_up(o + (size_t)B * R * nsegr * cap_s * sizeof(TopkEntry));
+        L.o_cdata = o; o = align_up(o + (size_t)B * R * nsegr * cap_s * sizeof(uint4));
+        L.o_ccount = o; o = align_up(o + (size_t)B * R * nsegr * sizeof(int));
+        L.o_cbound = o; o = align_up(o + (size_t)B * R * nsegr * sizeof(float));
         L.o_klist = o; o = align_up(o + (size_t)B * R * cap_k * sizeof(TopkEntry));
     }
     L.bytes = o;
@@ -218,7 +219,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
         P.CT = topk_chunks(dt, V);
         P.nsegr = topk_segments((long long)B * R, P.CT, sms, top_k);
         P.sps = (int)cdiv(P.CT, P.nsegr);
-        P.cap_s = TK_UNION / (P.nsegr * WARPS);
+        P.cap_s = TK_UNION / P.nsegr;
         P.cap_k = topk_kept_cap(top_k);
     }
     const SpecLayout L = spec_layout(B, R, partials_per_row(sh), P.nseg, topk, P.nsegr, P.cap_s, P.cap_k);
@@ -249,6 +250,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
         P.clist = reinterpret_cast<TopkEntry*>(ws + L.o_clist);
         P.cdata = reinterpret_cast<uint4*>(ws + L.o_cdata);
         P.ccount = reinterpret_cast<int*>(ws + L.o_ccount);
+        P.cbound = reinterpret_cast<float*>(ws + L.o_cbound);
         P.klist = reinterpret_cast<TopkEntry*>(ws + L.o_klist);
     }
 
@@ -287,9 +289,9 @@ size_t spec_workspace_bytes(int B, int gamma, int V, int top_k, int tree_nodes)
                                                                            : slices1(sh)).bytes);
         } else {
             const bool topk = top_k > 0 && top_k < V;
-            // lists: nsegr * WARPS * cap_s <= TK_UNION entries, at most TK_MAX_SEGR * WARPS per row
+            // lists: nsegr * cap_s = TK_UNION groups per row, at most TK_MAX_SEGR lists
             const SpecLayout L = spec_layout(B, 2 * gamma + 1, partials_per_row(sh), nsegs(sh), topk,
-                                             TK_MAX_SEGR, topk ? TK_UNION / (TK_MAX_SEGR * WARPS) : 0,
+                                             TK_MAX_SEGR, topk ? TK_UNION / TK_MAX_SEGR : 0,
                                              topk ? topk_kept_cap(top_k) : 0);
             best = std::max(best, L.bytes);
         }

@@ -64,7 +64,7 @@ struct Plan {         // one request, after the acceptance scan
     double u;         // correction or bonus uniform
 };
 
-struct TopkEntry {    // one kept top-k candidate
+struct __align__(8) TopkEntry {  // one kept top-k candidate
     float x;
     int idx;
 };
@@ -123,10 +123,11 @@ struct SpecParams {
     unsigned* req_ctr;    // [B]
     unsigned* res_ctr;    // [B]
     unsigned* work;       // [2] task counters of the two streaming kernels
-    TopkEntry* clist;     // [B*R*nsegr*WARPS*cap_s] per (segment, warp): candidate groups (unordered):
-                          // the group's maximum and the index of its first element
+    TopkEntry* clist;     // [B*R*nsegr*cap_s] per segment: candidate groups (unordered): the
+                          // group's maximum and the index of its first element
     uint4* cdata;         // [same] the candidate group's raw 16 bytes (8 bf16 or 4 fp32 logits)
-    int* ccount;          // [B*R*nsegr*WARPS] entries listed, or TK_NONFINITE / TK_OVERFLOW / TK_TIMEOUT
+    int* ccount;          // [B*R*nsegr] groups listed, or TK_NONFINITE / TK_OVERFLOW / TK_TIMEOUT
+    float* cbound;        // [B*R*nsegr] the segment's final bound: >= k of its elements reach it
     TopkEntry* klist;     // [B*R*cap_k] per-row kept list, sorted by index
     unsigned* dense_ctr;  // [B]
     int* ndense;          // [B]

@@ -53,6 +53,16 @@ __device__ __forceinline__ float key_value(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// one candidate entry through L2 (written by the previous kernel)
+__device__ __forceinline__ TopkEntry ld_entry(const TopkEntry* p)
+{
+    const int2 v = __ldcg(reinterpret_cast<const int2*>(p));
+    TopkEntry e;
+    e.x = __int_as_float(v.x);
+    e.idx = v.y;
+    return e;
+}
+
 __device__ __forceinline__ float fmax_nan_f(float a, float b)
 {
     float r;
@@ -191,23 +201,22 @@ __device__ __forceinline__ int slot_elem(int cbase, int s)
     else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
 }
 
-// The k-th largest (with multiplicity) of the keys key[j] (slots j < J, lanes with 32 j + lane <
-// total), by one warp: a radix select over 8-bit digits, each digit resolved by a 256-bin histogram
-// in shared memory (hist: 256 ints of this warp) and a suffix sum over it.  The digits start at
-// the highest bit in which the keys differ (the bits above are common to all of them), so values
-// spread over a narrow range take one pass.  Bits below 16 of bf16-valued keys never differ.
-template <int DT, int KPL>
-__device__ uint32_t warp_kth_key_hist(const uint32_t (&key)[KPL], int J, int total, int k, int* hist)
+// The k-th largest (with multiplicity) of the n keys key_at(0..n), by one warp: a radix select
+// over 8-bit digits, each digit resolved by a 256-bin histogram in shared memory (hist: 256 ints of
+// this warp) and a suffix sum over it.  The digits start at the highest bit in which the keys differ
+// (the bits above are common to all of them), so values spread over a narrow range take one pass.
+// Bits below 16 of bf16-valued keys never differ.
+template <int DT, class KeyAt>
+__device__ uint32_t warp_kth_key_hist(int n, int k, int* hist, KeyAt key_at)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-    for (int j = 0; j < KPL; ++j)
-        if (j < J && 32 * j + lane < total) {
-            kmin = min(kmin, key[j]);
-            kmax = max(kmax, key[j]);
-        }
+    for (int i = lane; i < n; i += 32) {
+        const uint32_t kx = key_at(i);
+        kmin = min(kmin, kx);
+        kmax = max(kmax, kx);
+    }
     kmin = __reduce_min_sync(FULL, kmin);
     kmax = __reduce_max_sync(FULL, kmax);
     const uint32_t diff = kmin ^ kmax;
@@ -223,12 +232,13 @@ __device__ uint32_t warp_kth_key_hist(const uint32_t (&key)[KPL], int J, int tot
 #pragma unroll
         for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0;
         __syncwarp();
-#pragma unroll
-        for (int j = 0; j < KPL; ++j)
-            if (j < J && 32 * j + lane < total && (key[j] & mask) == prefix) {
-                const uint32_t dg = shift >= 0 ? (key[j] >> shift) & 255u : (key[j] << -shift) & 255u;
+        for (int i = lane; i < n; i += 32) {
+            const uint32_t kx = key_at(i);
+            if ((kx & mask) == prefix) {
+                const uint32_t dg = shift >= 0 ? (kx >> shift) & 255u : (kx << -shift) & 255u;
                 atomicAdd(&hist[dg], 1);
             }
+        }
         __syncwarp();
         int h8[8], c8 = 0;
 #pragma unroll
@@ -270,9 +280,10 @@ __device__ uint32_t warp_kth_key_hist(const uint32_t (&key)[KPL], int J, int tot
 
 constexpr int TK_BINS = 256;  // histogram of candidate values above a segment's first bound
 static_assert(TK_BINS == NT, "one bin per thread to clear");
-constexpr int TK_HIST_CHUNKS = 4;          // chunks of a segment that refine its bound
-constexpr int TK_KPL = 32;                 // union entries per lane in the finish kernel
-constexpr int TK_UNION = 32 * TK_KPL;      // entries of all candidate lists of a row
+constexpr int TK_CAND_MIN = 512;           // finish kernel: candidate elements of a row (at least)
+constexpr int FIN_WARPS = 4;               // finish kernel: warps (rows) per CTA
+// finish kernel: candidate capacity of a row, which also holds the kept list and the draw scratch
+__device__ __host__ __forceinline__ int topk_cand_cap(int cap_k) { return cap_k > TK_CAND_MIN ? cap_k : TK_CAND_MIN; }
 
 // Position in the segment sequence blockIdx.x, blockIdx.x + stride, ... with the segment's row and
 // its index within the row kept up to date without divisions.
@@ -298,6 +309,44 @@ struct SegCursor {
     }
 };
 
+// The bound a segment's histogram gives (one warp): the lowest bin edge with at least k counted
+// group maxima at or above it, or -inf if fewer than k were counted.  Bin b counts the maxima whose
+// order-preserving key lies in [key0 + (b << 16), key0 + ((b + 1) << 16)), the last bin everything
+// above.  Every counted maximum is a distinct element of the segment, so at least k of its elements
+// reach the bound.
+__device__ __forceinline__ float hist_bound(const int* h, int k, uint32_t key0)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    int c8 = 0;
+    int hb[TK_BINS / 32];
+#pragma unroll
+    for (int i = 0; i < TK_BINS / 32; ++i) {
+        hb[i] = h[lane * (TK_BINS / 32) + i];
+        c8 += hb[i];
+    }
+    int suf = c8;  // counts in this lane's bins and above
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_down_sync(FULL, suf, o);
+        if (lane + o < 32) suf += v;
+    }
+    const unsigned reach = __ballot_sync(FULL, suf >= k);
+    if (!reach) return NEG_INF;
+    const int ls = 31 - __clz(reach);  // highest lane whose suffix reaches k
+    int bin = -1;
+    if (lane == ls) {
+        int acc = suf - c8;  // counts above this lane's bins
+#pragma unroll
+        for (int i = TK_BINS / 32 - 1; i >= 0; --i) {
+            acc += hb[i];
+            if (bin < 0 && acc >= k) bin = lane * (TK_BINS / 32) + i;
+        }
+    }
+    bin = __shfl_sync(FULL, bin, ls);
+    return key_value(key0 + ((uint32_t)bin << 16));
+}
+
 // Kernel 1: warp-specialised.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage
 // ring by a producer warp; otherwise the consumer warps load their elements straight into
 // registers.  A CTA takes segments (runs of up to P.sps chunks of one row) round-robin.
@@ -309,13 +358,15 @@ struct SegCursor {
 // Consumers (warps 0..WARPS-1): each waits on its chunk's full barrier, reads its 64 (bf16) or 32
 // (fp32) elements into registers, releases the stage and filters them on its own: warps meet only
 // at the start of each segment (a named barrier of the consumer warps), where the k-th largest of
-// the NT thread maxima of the segment's first chunk gives the segment's first bound tau.  Each warp
-// appends its elements at or above the current bound beta to its own list for the segment (no
-// atomics) and counts each in a histogram of its value above tau (bins 2^16 apart in the
-// order-preserving key: one bf16 value per bin).  Warp 1 turns the histogram -- every count in it
-// is a real element of the segment, whichever chunks the other warps have reached -- into a
-// tighter bound: the lowest bin edge with at least k counted elements above it, published as one
-// 64-bit word (segment, key) that every warp reads before its next chunk.
+// the NT thread maxima of the segment's first chunk gives the segment's first bound tau.  Elements
+// sit in groups of 4 registers (one 16-byte vector); a group whose maximum reaches the current bound
+// beta goes to the segment's list (positions reserved with one shared-memory atomic per warp and
+// chunk), and its maximum is counted in a histogram above tau (bins 2^16 apart in the
+// order-preserving key: one bf16 value per bin).  Every count in the histogram is a distinct
+// element of the segment, whichever chunks the other warps have reached, so the warps take turns
+// turning it into a tighter bound for the chunks still to come, published as one 64-bit word
+// (segment, key).  At the next segment's start (and after the last segment) warp 0 publishes the
+// finished segment: its list length (or a status) and its final bound from the complete histogram.
 template <int DT, bool BULK>
 __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P)
 {
@@ -326,11 +377,13 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int G = 4, NG = NREG / G;        // groups of 4 registers: one 16-byte vector each
     constexpr int EPG = (DT == DT_BF16) ? 2 * G : G;  // elements per group
-    constexpr int HW = (WARPS > 1) ? 1 : 0;  // the warp that turns the histogram into a bound
     static_assert(NREG % G == 0, "register groups");
+    static_assert((WARPS & (WARPS - 1)) == 0, "warps take turns by chunk index");
     extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
     __shared__ float tmax[2][NT];      // thread maxima of a segment's first chunk (by segment parity)
-    __shared__ int hist[2][TK_BINS];   // by segment parity
+    __shared__ int hist[3][TK_BINS];   // by segment mod 3: in use, being published, being cleared
+    __shared__ int scount[2];          // groups listed in the segment (by segment parity)
+    __shared__ int sflag[2];           // 1: a NaN or +inf in the segment; 4: a wait ran out
     __shared__ unsigned long long pub; // (segment << 32) | key of the latest bound published for it
     __shared__ int sfail;              // a wait ran out in this CTA: nothing more is read
     __shared__ __align__(8) uint64_t full[TK_STAGES];
@@ -346,6 +399,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
 
     if (tid < NT) hist[0][tid] = 0;
     if (tid == 0) {
+        scount[0] = 0;
+        sflag[0] = 0;
         pub = ~0ull;  // segment field 0xffffffff: no bound yet
         sfail = 0;
         if constexpr (BULK) {
@@ -401,8 +456,23 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     // ------------------------------------------------------------------ consumer warps
     int stg = 0;          // ring stage of the next chunk
     unsigned ph = 0;      // its fill parity
-    int jseg = -1;        // this CTA's segment counter (selects tmax and hist)
+    int jseg = -1;        // this CTA's segment counter (selects tmax, hist, scount, sflag)
     bool failed = false;  // a bulk-copy wait ran out: the remaining lists are marked, not filled
+    // the segment before the current one, published by warp 0 at the current one's start
+    int prev_sg = -1;
+    float prev_tau = NEG_INF;
+    uint32_t prev_key0 = 0;
+    // warp 0, after a consumer barrier: the segment's list length (or status) and final bound
+    auto publish = [&](int psg, int pj, float ptau, uint32_t pkey0) {
+        float bnd = ptau;
+        if (k <= NT && ptau != NEG_INF) bnd = fmaxf(bnd, hist_bound(hist[pj % 3], k, pkey0));
+        if (lane == 0) {
+            const int c = scount[pj & 1], f = sflag[pj & 1];
+            P.ccount[psg] = (f & 4) ? TK_TIMEOUT : (f & 1) ? TK_NONFINITE
+                          : (k > NT || c > P.cap_s) ? TK_OVERFLOW : c;
+            P.cbound[psg] = bnd;
+        }
+    };
     SegCursor cc;
     cc.init(blockIdx.x, G0, P.nsegr);
     for (; cc.sg < nsegs; cc.next(G0, P.nsegr)) {
@@ -410,9 +480,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
         ++jseg;
         const int nst = min(P.sps, P.CT - cc.si * P.sps);
         const char* row = BULK ? nullptr : spec_row_ptr(P, cc.row_id / P.R, cc.row_id % P.R);
-        TopkEntry* wlist = P.clist + ((size_t)sg * WARPS + warp) * P.cap_s;
-        uint4* wdata = P.cdata + ((size_t)sg * WARPS + warp) * P.cap_s;
-        int wcount = 0;              // entries in this warp's list
+        TopkEntry* slist = P.clist + (size_t)sg * P.cap_s;
+        uint4* sdata = P.cdata + (size_t)sg * P.cap_s;
         int seg_bad = 0;             // this warp saw a NaN or +inf in the segment
         float tau_first = NEG_INF;   // the segment's first bound; histogram bins count from its key
         uint32_t key0 = 0;
@@ -476,7 +545,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 }
             }
 
-            // ---- group maxima (G registers each) and the thread maximum, NaN-propagating
+            // ---- group maxima and the thread maximum, NaN-propagating
             uint32_t gm[NG];
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
@@ -499,15 +568,26 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
 #pragma unroll
                 for (int g = 1; g < NG; ++g) tm = fmax_nan_f(tm, __uint_as_float(gm[g]));
             }
-            seg_bad |= __any_sync(FULL, tm != tm || tm == __int_as_float(0x7f800000));
+            const bool bad_now = __any_sync(FULL, tm != tm || tm == __int_as_float(0x7f800000));
 
             // ---- a segment's first chunk: every consumer warp meets here once per segment (failed
             // or not), after which the thread maxima are complete and the previous segment is done
-            // by all, so its histogram can be cleared for the segment after this one
+            // by all: warp 0 publishes it, and the histogram of the segment before it is cleared
+            // for the segment after this one
             if (st == 0) {
                 tmax[jseg & 1][tid] = tm;
                 consumer_sync();
-                hist[(jseg + 1) & 1][tid] = 0;
+                hist[(jseg + 1) % 3][tid] = 0;
+                if (warp == 0 && prev_sg >= 0) {
+                    publish(prev_sg, jseg - 1, prev_tau, prev_key0);
+                    if (lane == 0) {  // the slots of the published segment serve the next one
+                        scount[(jseg + 1) & 1] = 0;
+                        sflag[(jseg + 1) & 1] = 0;
+                    }
+                } else if (warp == 0 && lane == 0) {
+                    scount[(jseg + 1) & 1] = 0;
+                    sflag[(jseg + 1) & 1] = 0;
+                }
                 // tau = the k-th largest thread maximum (valid for k <= NT), selected by every
                 // warp by itself
                 if (k <= NT) {
@@ -527,9 +607,17 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     tau_first = key_value(prefix);
                     key0 = prefix;
                 }
+                prev_sg = sg;
+                prev_tau = tau_first;
+                prev_key0 = key0;
+            }
+            // flags of this segment are set only after its barrier, once its slot has been cleared
+            if (bad_now && !seg_bad) {
+                seg_bad = 1;
+                if (lane == 0) atomicOr(&sflag[jseg & 1], 1);
             }
             if (failed) {
-                if (lane == 0 && st + 1 == nst) P.ccount[(size_t)sg * WARPS + warp] = TK_TIMEOUT;
+                if (lane == 0) atomicOr(&sflag[jseg & 1], 4);
                 continue;
             }
             float beta = tau_first;
@@ -538,47 +626,18 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 if ((int)(pb >> 32) == sg) beta = fmaxf(beta, key_value((uint32_t)pb));
             }
 
-            // ---- warp HW: a tighter bound from the histogram (counts of every warp so far)
-            if (warp == HW && !seg_bad && k <= NT && st + 1 < nst && st < TK_HIST_CHUNKS &&
-                tau_first != NEG_INF) {
-                int c8 = 0;
-                int hb[TK_BINS / 32];
-#pragma unroll
-                for (int i = 0; i < TK_BINS / 32; ++i) {
-                    hb[i] = hist[jseg & 1][lane * (TK_BINS / 32) + i];
-                    c8 += hb[i];
-                }
-                // counts in this lane's bins and above
-                int suf = c8;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_down_sync(FULL, suf, o);
-                    if (lane + o < 32) suf += v;
-                }
-                const unsigned reach = __ballot_sync(FULL, suf >= k);
-                if (reach) {
-                    const int ls = 31 - __clz(reach);  // highest lane whose suffix reaches k
-                    int bin = -1;
-                    if (lane == ls) {
-                        int acc = suf - c8;  // counts above this lane's bins
-#pragma unroll
-                        for (int i = TK_BINS / 32 - 1; i >= 0; --i) {
-                            acc += hb[i];
-                            if (bin < 0 && acc >= k) bin = lane * (TK_BINS / 32) + i;
-                        }
-                    }
-                    bin = __shfl_sync(FULL, bin, ls);
-                    const uint32_t nk = key0 + ((uint32_t)bin << 16);
-                    if (lane == 0 && key_value(nk) > beta)
-                        *reinterpret_cast<volatile unsigned long long*>(&pub) =
-                            ((unsigned long long)(unsigned)sg << 32) | nk;
-                }
+            // ---- the warps take turns: a tighter bound from the histogram (counts of every warp
+            // so far), for the chunks still to come
+            if (warp == (st & (WARPS - 1)) && !seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
+                const float nb = hist_bound(hist[jseg % 3], k, key0);
+                if (lane == 0 && nb > beta)
+                    *reinterpret_cast<volatile unsigned long long*>(&pub) =
+                        ((unsigned long long)(unsigned)sg << 32) | okey(nb);
             }
 
-            // ---- this warp's groups whose maximum reaches beta go to its list: the maximum and
-            // the first element's index, and the group's 16 raw bytes; the maximum is counted in
-            // the histogram (maxima of distinct groups are distinct elements).  Positions come from
-            // a prefix sum over the warp.
+            // ---- this warp's groups whose maximum reaches beta go to the segment's list: the
+            // maximum and the first element's index, and the group's 16 raw bytes; the maximum is
+            // counted in the histogram
             if (!seg_bad && k <= NT) {
                 // bf16: compare against beta rounded down to bf16, so no element >= beta is missed
                 const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(beta));
@@ -598,10 +657,11 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 const int mine = __popc(pass);
                 if (__any_sync(FULL, mine)) {
                     const int incl = warp_incl_scan(mine);
-                    int pos = wcount + incl - mine;
-                    wcount += __shfl_sync(FULL, incl, 31);
-                    int* h = hist[jseg & 1];
-                    const bool count = st < TK_HIST_CHUNKS - 1 && tau_first != NEG_INF;
+                    int pos = 0;
+                    if (lane == 31) pos = atomicAdd(&scount[jseg & 1], incl);
+                    pos = __shfl_sync(FULL, pos, 31) + incl - mine;
+                    int* h = hist[jseg % 3];
+                    const bool count = tau_first != NEG_INF;
 #pragma unroll
                     for (int g = 0; g < NG; ++g) {
                         if (pass & (1u << g)) {
@@ -610,8 +670,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                             else en.x = __uint_as_float(gm[g]);
                             en.idx = slot_elem<VEC>(cbase, EPG * g);
                             if (pos < P.cap_s) {
-                                wlist[pos] = en;
-                                wdata[pos] = make_uint4(w[G * g], w[G * g + 1], w[G * g + 2], w[G * g + 3]);
+                                slist[pos] = en;
+                                sdata[pos] = make_uint4(w[G * g], w[G * g + 1], w[G * g + 2], w[G * g + 3]);
                             }
                             ++pos;
                             if (count) {
@@ -622,20 +682,19 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     }
                 }
             }
-            // ---- the segment's last chunk: this warp publishes its list length
-            if (st + 1 == nst && lane == 0)
-                P.ccount[(size_t)sg * WARPS + warp] =
-                    seg_bad ? TK_NONFINITE : (k > NT || wcount > P.cap_s) ? TK_OVERFLOW : wcount;
         }
     }
+    // the CTA's last segment: published once every consumer warp is done with it
+    consumer_sync();
+    if (warp == 0 && prev_sg >= 0) publish(prev_sg, jseg, prev_tau, prev_key0);
 }
 
-// Kernel 2, one warp per row: exact threshold g from the row's candidate groups (nsegr segments x
-// WARPS lists of kernel 1, up to TK_UNION groups), the kept list sorted by index, and the
-// normaliser over it.  The k-th largest group maximum tau_g is a lower bound of g (the maxima of
-// distinct groups are distinct elements), so only the groups whose maximum reaches tau_g can hold
-// an element >= g; their elements >= tau_g are the candidates from which g is selected exactly.
-// u holds TK_UNION entries, kept cap_k.
+// Kernel 2, one warp per row: exact threshold g from the row's candidate groups (nsegr segment
+// lists of kernel 1, up to 1024 groups in all), the kept list sorted by index, and the
+// normaliser over it.  Each segment's final bound reaches at most g (at least k of the row's
+// elements reach it), so only the listed groups whose maximum reaches the largest of them, beta,
+// can hold an element >= g; their elements >= beta are the candidates from which g is selected
+// exactly.  u holds topk_cand_cap(cap_k) entries, kept cap_k.
 template <int DT>
 __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry* kept, int row_id)
 {
@@ -647,9 +706,8 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     st.lse = __int_as_float(0x7fc00000);
     st.invS = 0.f;
     st.lx = __longlong_as_double(0x7ff8000000000000ll);
-    const int nl = P.nsegr * WARPS;  // lists of the row, <= 32
-    const int* cnt = P.ccount + (size_t)row_id * nl;
-    const TopkEntry* lists = P.clist + (size_t)row_id * nl * P.cap_s;
+    const int nl = P.nsegr;  // lists of the row, <= 4
+    const size_t sg0 = (size_t)row_id * nl;
     // the token this row scores (target row i and draft row i score draft token i; the last target
     // row scores none) and its logit, fetched now so that they arrive while the lists are read
     const int b = row_id / P.R, r = row_id - b * P.R, g = P.gamma;
@@ -660,7 +718,12 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     pdl_trigger();
     pdl_wait();  // the candidate lists of the streaming kernel
 
-    int n = (lane < nl) ? __ldcg(cnt + lane) : 0;
+    int n = 0;
+    float bd = NEG_INF;
+    if (lane < nl) {
+        n = __ldcg(P.ccount + sg0 + lane);
+        bd = __ldcg(P.cbound + sg0 + lane);
+    }
     int flag = 0;
     if (n == TK_NONFINITE) flag |= 1;
     else if (n == TK_TIMEOUT) flag |= 4;
@@ -671,83 +734,73 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     if (flag & 2) { st.dense = 1; return st; }
     n = max(0, min(n, P.cap_s));
     const int incl = warp_incl_scan(n);
-    const int excl = incl - n;
     const int total = __shfl_sync(FULL, incl, 31);
-    const int nmax = (int)__reduce_max_sync(FULL, (unsigned)n);
-    if (total > TK_UNION) { st.dense = 1; return st; }
+    const float beta = warp_max(bd);
+    // list starts in the packed order (lists 1..3; nl <= 4)
+    const int ls1 = __shfl_sync(FULL, incl, 0), ls2 = __shfl_sync(FULL, incl, 1), ls3 = __shfl_sync(FULL, incl, 2);
 
-    // the lists, packed into u: four lists at a time, every load of a batch issued before any store
-    for (int l0 = 0; l0 < nl; l0 += 4) {
-        for (int i0 = 0; i0 < nmax; i0 += 64) {
-            TopkEntry e[8];
-            bool v[8];
+    // the groups whose maximum reaches beta: (first element's index, slot), compacted into kept;
+    // entries in batches of 8 per lane, every load of a batch issued before any is used
+    const TopkEntry* lists = P.clist + sg0 * P.cap_s;
+    const uint4* gdata = P.cdata + sg0 * P.cap_s;
+    constexpr int EB = 8;
+    int ng = 0;
+    for (int p0 = 0; p0 < total; p0 += 32 * EB) {
+        TopkEntry e[EB];
+        int slot[EB];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int l = l0 + (t >> 1), i = i0 + 32 * (t & 1) + lane;
-                const int nn = __shfl_sync(FULL, n, l & 31);
-                v[t] = l < nl && i < nn;
-                if (v[t]) {
-                    e[t].x = __ldcg(&lists[(size_t)l * P.cap_s + i].x);  // the group's maximum
-                    e[t].idx = l * P.cap_s + i;                          // its slot in the row's lists
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int l = l0 + (t >> 1), i = i0 + 32 * (t & 1) + lane;
-                const int off = __shfl_sync(FULL, excl, l & 31);
-                if (v[t]) u[off + i] = e[t];
+        for (int t = 0; t < EB; ++t) {
+            const int p = p0 + 32 * t + lane;
+            e[t].x = NEG_INF;
+            e[t].idx = 0;
+            slot[t] = -1;
+            if (p < total) {
+                const int l = (nl > 1 && p >= ls1) + (nl > 2 && p >= ls2) + (nl > 3 && p >= ls3);
+                const int start = (l == 0) ? 0 : (l == 1) ? ls1 : (l == 2) ? ls2 : ls3;
+                slot[t] = l * P.cap_s + (p - start);
+                e[t] = ld_entry(lists + slot[t]);
             }
         }
-    }
-    __syncwarp();
-
-    // tau_g: the k-th largest group maximum, keys in registers (occupied slots only); with fewer
-    // than k groups every group is expanded
-    int J = (total + 31) >> 5;
-    uint32_t key[TK_KPL];
 #pragma unroll
-    for (int j = 0; j < TK_KPL; ++j) {
-        key[j] = 0u;  // below every key a value can have
-        if (j < J && 32 * j + lane < total) key[j] = okey(u[32 * j + lane].x);
-    }
-    const int k = P.top_k;
-    uint32_t gk = okey(NEG_INF);
-    if (total >= k) gk = warp_kth_key_hist<DT, TK_KPL>(key, J, total, k, reinterpret_cast<int*>(kept));
-    // the slots of the groups whose maximum reaches tau_g, compacted into kept
-    int ng = 0;
-#pragma unroll
-    for (int j = 0; j < TK_KPL; ++j) {
-        if (j < J) {
-            const bool keep = 32 * j + lane < total && key[j] >= gk;
+        for (int t = 0; t < EB; ++t) {
+            if (p0 + 32 * t >= total) break;  // the same for every lane
+            const bool keep = slot[t] >= 0 && e[t].x >= beta;
             const unsigned bal = __ballot_sync(FULL, keep);
-            const int pos = ng + __popc(bal & ((1u << lane) - 1u));
-            if (keep && pos < P.cap_k) kept[pos].idx = u[32 * j + lane].idx;
+            const int q = ng + __popc(bal & ((1u << lane) - 1u));
+            if (keep && q < P.cap_k) {
+                TopkEntry ge;
+                ge.x = __int_as_float(slot[t]);
+                ge.idx = e[t].idx;
+                kept[q] = ge;
+            }
             ng += __popc(bal);
         }
     }
     __syncwarp();
     if (ng > P.cap_k) { st.dense = 1; return st; }
-    // their elements >= tau_g inside the row are the candidates, packed into u (groups of 32 x 8
-    // at a time, every load of a batch issued before any is used)
+    // their elements >= beta inside the row are the candidates, packed into u (32 x GB groups at a
+    // time, every load of a batch issued before any is used)
     constexpr int EPG = (DT == DT_BF16) ? 8 : 4;  // elements per group (one 16-byte vector)
-    const uint4* gdata = P.cdata + (size_t)row_id * nl * P.cap_s;
     const int estride = (P.vec > 1) ? 1 : NT;     // index step between a group's elements
+    const int cand = topk_cand_cap(P.cap_k);
+    const uint32_t bkey = okey(beta);
     int ne = 0;
-    for (int r0 = 0; r0 < ng; r0 += 256) {
-        uint4 d[8];
-        int base[8];
+    constexpr int GB = 4;
+    for (int r0 = 0; r0 < ng; r0 += 32 * GB) {
+        uint4 d[GB];
+        int base[GB];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < GB; ++t) {
             const int i = r0 + 32 * t + lane;
             base[t] = P.V;  // nothing inside the row
             if (i < ng) {
-                const int slot = kept[i].idx;
-                d[t] = __ldcg(gdata + slot);
-                base[t] = __ldcg(&lists[slot].idx);
+                const TopkEntry ge = kept[i];
+                d[t] = __ldcg(gdata + __float_as_int(ge.x));
+                base[t] = ge.idx;
             }
         }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < GB; ++t) {
             if (r0 + 32 * t >= ng) break;  // the same for every lane
             const uint32_t wd[4] = {d[t].x, d[t].y, d[t].z, d[t].w};
             float xe[EPG];
@@ -756,16 +809,16 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
             for (int e = 0; e < EPG; ++e) {
                 if constexpr (DT == DT_BF16) xe[e] = (e & 1) ? bf16hi(wd[e >> 1]) : bf16lo(wd[e >> 1]);
                 else xe[e] = __uint_as_float(wd[e]);
-                if (base[t] + e * estride < P.V && okey(xe[e]) >= gk) m |= 1u << e;
+                if (base[t] + e * estride < P.V && okey(xe[e]) >= bkey) m |= 1u << e;
             }
             const int c = __popc(m);
-            const int incl = warp_incl_scan(c);
-            int p = ne + incl - c;
-            ne += __shfl_sync(FULL, incl, 31);
+            const int ci = warp_incl_scan(c);
+            int p = ne + ci - c;
+            ne += __shfl_sync(FULL, ci, 31);
 #pragma unroll
             for (int e = 0; e < EPG; ++e) {
                 if (m & (1u << e)) {
-                    if (p < TK_UNION) {
+                    if (p < cand) {
                         TopkEntry en;
                         en.x = xe[e];
                         en.idx = base[t] + e * estride;
@@ -777,27 +830,27 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
         }
     }
     __syncwarp();
-    if (ne > TK_UNION) { st.dense = 1; return st; }
-    // g: the exact k-th largest candidate
-    J = (ne + 31) >> 5;
-#pragma unroll
-    for (int j = 0; j < TK_KPL; ++j) {
-        key[j] = 0u;
-        if (j < J && 32 * j + lane < ne) key[j] = okey(u[32 * j + lane].x);
-    }
+    if (ne > cand) { st.dense = 1; return st; }
+    // g: the exact k-th largest candidate (kept serves as the histogram)
+    const int k = P.top_k;
     uint32_t gkey = okey(NEG_INF);
-    if (ne >= k) gkey = warp_kth_key_hist<DT, TK_KPL>(key, J, ne, k, reinterpret_cast<int*>(kept));
+    if (ne >= k)
+        gkey = warp_kth_key_hist<DT>(ne, k, reinterpret_cast<int*>(kept),
+                                     [&](int i) { return okey(u[i].x); });
+    __syncwarp();
     // the candidates >= g, in candidate order
     int nk = 0;
-#pragma unroll
-    for (int j = 0; j < TK_KPL; ++j) {
-        if (j < J) {
-            const bool keep = 32 * j + lane < ne && key[j] >= gkey;
-            const unsigned bal = __ballot_sync(FULL, keep);
-            const int pos = nk + __popc(bal & ((1u << lane) - 1u));
-            if (keep && pos < P.cap_k) kept[pos] = u[32 * j + lane];
-            nk += __popc(bal);
-        }
+    for (int i0 = 0; i0 < ne; i0 += 32) {
+        const int i = i0 + lane;
+        TopkEntry en;
+        en.x = NEG_INF;
+        en.idx = 0;
+        if (i < ne) en = u[i];
+        const bool keep = i < ne && okey(en.x) >= gkey;
+        const unsigned bal = __ballot_sync(FULL, keep);
+        const int q = nk + __popc(bal & ((1u << lane) - 1u));
+        if (keep && q < P.cap_k) kept[q] = en;
+        nk += __popc(bal);
     }
     __syncwarp();
     if (nk > P.cap_k) { st.dense = 1; return st; }
@@ -844,17 +897,20 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     return st;
 }
 
-// Kernel 2: one warp per row; the last warp to finish a row of a request scans it and draws.
+// Kernel 2: one warp per row, FIN_WARPS rows per CTA (small CTAs with few registers, so that every
+// row of a large batch is resident at once); the last warp to finish a row of a request scans it
+// and draws.
 template <int DT>
-__global__ void __launch_bounds__(NT) topk_finish_kernel(SpecParams P)
+__global__ void __launch_bounds__(FIN_WARPS * 32, 7) topk_finish_kernel(SpecParams P)
 {
-    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: u[TK_UNION], kept[cap_k]
+    extern __shared__ __align__(16) TopkEntry fin[];  // per warp: u[cand], kept[cap_k]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row_id = blockIdx.x * WARPS + warp;
+    const int row_id = blockIdx.x * FIN_WARPS + warp;
     if (row_id >= P.B * P.R) return;
     const int b = row_id / P.R;
-    TopkEntry* u = fin + (size_t)warp * (TK_UNION + P.cap_k);
-    TopkEntry* kept = u + TK_UNION;
+    const int cand = topk_cand_cap(P.cap_k);
+    TopkEntry* u = fin + (size_t)warp * (cand + P.cap_k);
+    TopkEntry* kept = u + cand;
     const RowStats st = topk_row_finish<DT>(P, u, kept, row_id);
     if (lane == 0) P.rstats[row_id] = st;
     if (!warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) return;
@@ -1025,9 +1081,10 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
         K1<<<cta_grid<K1>(nsegs, sms, 0, TK_THREADS), TK_THREADS, 0, st>>>(P);
     }
     mark_kernel_stop(st);
-    const size_t fsm = (size_t)WARPS * (TK_UNION + P.cap_k) * sizeof(TopkEntry);
+    const size_t fsm = (size_t)FIN_WARPS * (topk_cand_cap(P.cap_k) + P.cap_k) * sizeof(TopkEntry);
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
-    launch_dependent(topk_finish_kernel<DT>, (unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, fsm,
+    launch_dependent(topk_finish_kernel<DT>, (unsigned)(((long long)P.B * P.R + FIN_WARPS - 1) / FIN_WARPS),
+                     FIN_WARPS * 32, fsm,
                      st, P);
     launch_dependent(topk_dense_kernel<DT>, (unsigned)P.B, NT, 0, st, P);
 }
