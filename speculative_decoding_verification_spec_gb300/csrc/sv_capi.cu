@@ -207,6 +207,8 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.B = B; P.gamma = gamma; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
     P.c = c; P.T = T; P.invT = 1.0 / T; P.top_k = top_k;
+    P.invT_hi = (float)P.invT;
+    P.invT_lo = (float)(P.invT - (double)P.invT_hi);
     // 16-byte vectors: 32 KB stream chunks (statistics) and 2048-vector residual chunks; the
     // scalar path's persistent warps take TV1 / TV2 vectors per task
     P.S1 = (int)(vec > 1 ? stream_chunks(sh) : slices1(sh));

@@ -37,10 +37,11 @@ enum {
 
 // ---------------------------------------------------------------- workspace records
 
-struct Partial {      // one (row, chunk) of the softmax statistics
+struct __align__(16) Partial {  // one (row, chunk) of the softmax statistics
     float M;          // chunk maximum of the raw logits (-inf if none)
     float MC;         // fp32(M * c)
-    double S;         // sum over the chunk of 2^(fma(x, c, -MC))
+    float S;          // sum over the chunk of 2^(fma(x, c, -MC)); < 0: the chunk was not read
+    float pad;
 };
 
 struct RowStats {     // one logit row after its chunks are combined
@@ -97,6 +98,7 @@ struct SpecParams {
     float c;              // log2(e)/T
     double T;
     double invT;          // 1/T
+    float invT_hi, invT_lo;  // 1/T as an unevaluated pair of floats
     int top_k;
     int pin_pairs;        // row pairs 0..pin_pairs-1 are read with L2 evict_last
     // softmax path: stats tasks (row, slice) and residual tasks (request, slice)
@@ -479,6 +481,55 @@ __device__ __forceinline__ T warp_sum(T v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Error-free transformation (Knuth's TwoSum) in fp32: a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// A value carried as an unevaluated pair hi + lo of floats (|lo| <= ulp(hi) / 2): about 48
+// significant bits from fp32 operations only (the fp64 pipe is very slow on this part).
+struct DFloat {
+    float hi, lo;
+};
+__device__ __forceinline__ DFloat df_make(float hi, float lo)
+{
+    DFloat r;
+    r.hi = __fadd_rn(hi, lo);
+    r.lo = __fsub_rn(lo, __fsub_rn(r.hi, hi));  // Dekker's FastTwoSum (|hi| >= |lo|)
+    return r;
+}
+__device__ __forceinline__ DFloat df_add(DFloat x, DFloat y)
+{
+    float s, e;
+    two_sum(x.hi, y.hi, s, e);
+    return df_make(s, __fadd_rn(e, __fadd_rn(x.lo, y.lo)));
+}
+// x * (c_hi + c_lo) for a constant given as a pair
+__device__ __forceinline__ DFloat df_mul(DFloat x, float c_hi, float c_lo)
+{
+    const float p = __fmul_rn(x.hi, c_hi);
+    const float e = fmaf(x.hi, c_hi, -p);  // the product's rounding error, exact
+    return df_make(p, fmaf(x.hi, c_lo, fmaf(x.lo, c_hi, e)));
+}
+__device__ __forceinline__ double df_to_double(DFloat x) { return (double)x.hi + (double)x.lo; }
+
+// Sum over the warp of pairs; every lane gets the same pair (the butterfly adds the same two
+// operands in each pair of lanes, and the pair sum is symmetric).
+__device__ __forceinline__ DFloat warp_sum_df(DFloat v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        DFloat w;
+        w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = df_add(v, w);
+    }
     return v;
 }
 

@@ -14,6 +14,48 @@
 namespace sv {
 
 constexpr double LN2 = 0.69314718055994530942;
+constexpr float LN2_HI = 0.693147182464599609375f;   // fp32(ln 2)
+constexpr float LN2_LO = -1.904654299957768e-09f;    // ln 2 - LN2_HI
+constexpr float LOG2E_F = 1.44269504088896340736f;
+
+// The normaliser fields of a row (one thread): from its maximum M, MC = fp32(M c), the sum
+// S = hi + lo of 2^(fma(x, c, -MC)) over its (kept) tokens, and the logit xtok of the token it
+// scores (tok_ok), kept when xtok >= thr:
+//   lse = M / T + ln S - ln 2 (M c - MC)       natural log, over logits / T
+//   lx  = fma(xtok, c, -MC) - log2 S           log2 p(xtok)
+// log2 S = e + log2 m + log2(1 + lo / hi) with hi = m 2^e, m in [0.5, 1): the fp32 log2 of m has an
+// absolute error of about 1e-7, and the integer e joins it exactly.  M c - MC, the rounding error
+// of MC, is exact as fma(M, c, -MC).  Everything is carried in pairs of floats; only lx and S are
+// widened to fp64 at the end.
+__device__ __forceinline__ void row_norm(RowStats& st, float M, float MC, DFloat S, const SpecParams& P,
+                                         bool tok_ok, float xtok, float thr)
+{
+    int e;
+    const float m = frexpf(S.hi, &e);
+    const float l2m = __fadd_rn(log2f(m), __fmul_rn(__fdiv_rn(S.lo, S.hi), LOG2E_F));
+    DFloat l2S;
+    two_sum((float)e, l2m, l2S.hi, l2S.lo);
+    const float err = fmaf(M, P.c, -MC);
+    const float a_hi = __fmul_rn(M, P.invT_hi);
+    const DFloat a = df_make(a_hi, fmaf(M, P.invT_lo, fmaf(M, P.invT_hi, -a_hi)));
+    DFloat d;
+    d.hi = -err;
+    d.lo = 0.f;
+    const DFloat lse = df_add(a, df_mul(df_add(l2S, d), LN2_HI, LN2_LO));
+    st.lse = __fadd_rn(lse.hi, lse.lo);
+    st.invS = __frcp_rn(__fadd_rn(S.hi, S.lo));
+    st.S = df_to_double(S);
+    if (tok_ok) {
+        const float t0 = fmaf(xtok, P.c, -MC);
+        if (xtok >= thr && isfinite(t0)) {
+            DFloat t;
+            two_sum(t0, -l2S.hi, t.hi, t.lo);
+            st.lx = df_to_double(df_make(t.hi, __fsub_rn(t.lo, l2S.lo)));
+        } else {
+            st.lx = (xtok >= thr) ? (double)t0 : -INFINITY;  // a -inf logit: p(x) = 0
+        }
+    }
+}
 
 __device__ __forceinline__ RowStats ld_rowstats(const RowStats* p)
 {
@@ -55,6 +97,110 @@ __device__ __forceinline__ double row_log2prob(float x, const RowStats& rs, floa
     return (double)fmaf(x, c, -rs.MC) - log2(rs.S);
 }
 
+// The accept ratio a = min(1, 2^(lp - lq)) of log2 probabilities lp <= 0 and a finite lq.  The
+// exponent's integer part n is applied as an exact power-of-two scale and 2^f of its fraction f in
+// [0, 1) comes from the fp32 ex2 unit: relative error a few 1e-7, well inside the 1e-6 decision
+// margin of the matching rules, with four fp64 operations (the fp64 pipe is very slow on this
+// part).  a stays > 0 whenever p(x) > 0, so a uniform of exactly 0 is still accepted.
+__device__ __forceinline__ double accept_ratio(double lp, double lq)
+{
+    if (!(lp < lq)) return 1.0;
+    if (lp == -INFINITY) return 0.0;
+    const double d = lp - lq;  // < 0
+    const double n = floor(d);
+    const float f = (float)(d - n);
+    const int ni = (n < -1100.0) ? -1100 : (int)n;
+    const double scale = (ni >= -1022) ? __longlong_as_double((long long)(ni + 1023) << 52)
+                                       : 4.9406564584124654e-324;  // the smallest positive double
+    return (double)ex2(f) * scale;
+}
+
+__device__ __forceinline__ RowStats blank_rowstats()
+{
+    RowStats r;
+    r.M = NEG_INF; r.MC = NEG_INF; r.S = 0.0; r.thr = NEG_INF;
+    r.status = ROW_OK; r.klist_n = -1; r.dense = 0;
+    r.lse = 0.f; r.invS = 0.f; r.lx = 0.0;
+    return r;
+}
+
+__device__ __forceinline__ RowStats shfl_rowstats(const RowStats& r, int src)
+{
+    const unsigned FULL = 0xffffffffu;
+    RowStats o;
+    o.M = __shfl_sync(FULL, r.M, src);
+    o.MC = __shfl_sync(FULL, r.MC, src);
+    o.S = __shfl_sync(FULL, r.S, src);
+    o.thr = __shfl_sync(FULL, r.thr, src);
+    o.status = __shfl_sync(FULL, r.status, src);
+    o.klist_n = __shfl_sync(FULL, r.klist_n, src);
+    o.dense = __shfl_sync(FULL, r.dense, src);
+    o.lse = __shfl_sync(FULL, r.lse, src);
+    o.invS = __shfl_sync(FULL, r.invS, src);
+    o.lx = __shfl_sync(FULL, r.lx, src);
+    return o;
+}
+
+// The plan of request b from its rows' statistics held one row per lane (row r in lane r; R =
+// 2 gamma + 1 <= 32), with the lse, 1/S and log2 p(x) of the scoring tokens filled in by whoever
+// finished the rows.  One warp, every lane gets the plan; writes the aux outputs.  The request's
+// tokens and uniforms are read here; everything else comes by shuffles.
+__device__ __forceinline__ Plan plan_from_lanes(const SpecParams& P, int b, const RowStats& rs)
+{
+    const int g = P.gamma, R = P.R, lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    const int x = (lane < g) ? __ldg(P.tokens + (size_t)b * g + lane) : 0;
+    const float uu = (lane < g + 2) ? __ldg(P.uniforms + (size_t)b * (g + 2) + lane) : 0.f;
+    const bool row = lane < R;
+    const int nonfinite = __any_sync(FULL, row && rs.status != ROW_OK);
+    const int timeout = __any_sync(FULL, row && rs.status == ROW_TIMEOUT);
+    if (row) {
+        const float lse = (rs.status == ROW_OK) ? rs.lse : __int_as_float(0x7fc00000);
+        if (lane <= g) {
+            if (P.aux_lse_p) P.aux_lse_p[(size_t)b * (g + 1) + lane] = lse;
+        } else if (P.aux_lse_q) {
+            P.aux_lse_q[(size_t)b * g + (lane - g - 1)] = lse;
+        }
+    }
+    // position i = lane < g: log2 p_i(x_i) is this lane's row, log2 q_i(x_i) row g + 1 + i's
+    const double lq = __shfl_sync(FULL, rs.lx, (lane + g + 1) & 31);
+    int badtok = 0;
+    bool reject = false;
+    if (lane < g) {
+        double a = __longlong_as_double(0x7ff8000000000000ll);
+        if (x < 0 || x >= P.V) {
+            badtok = 1;
+        } else if (!nonfinite) {
+            if (lq == -INFINITY) {
+                badtok = 1;  // q(x) = 0: the draft cannot have proposed x
+            } else {
+                a = accept_ratio(rs.lx, lq);
+                reject = !((double)uu < a);
+            }
+        }
+        if (P.aux_accept) P.aux_accept[(size_t)b * g + lane] = (float)a;
+    }
+    badtok = __any_sync(FULL, badtok);
+    const int badu = __any_sync(FULL, lane < g + 2 && !(uu >= 0.0f && uu < 1.0f));
+    const unsigned rej = __ballot_sync(FULL, reject);
+
+    Plan pl;
+    pl.status = timeout ? ROW_TIMEOUT : nonfinite ? ROW_NONFINITE : badtok ? ROW_BAD_TOKEN : badu ? ROW_BAD_UNIFORM : ROW_OK;
+    pl.A = rej ? __ffs(rej) - 1 : g;
+    pl.rp = (pl.A < g) ? pl.A : g;
+    pl.rq = (pl.A < g) ? g + 1 + pl.A : -1;
+    const RowStats sp = shfl_rowstats(rs, pl.rp);
+    const RowStats sq = shfl_rowstats(rs, pl.rq >= 0 ? pl.rq : 0);
+    pl.MCp = sp.MC;
+    pl.invSp = sp.invS;
+    pl.thrp = sp.thr;
+    pl.MCq = (pl.rq >= 0) ? sq.MC : 0.f;
+    pl.invSq = (pl.rq >= 0) ? sq.invS : 0.f;
+    pl.thrq = (pl.rq >= 0) ? sq.thr : 0.f;
+    pl.u = (double)__shfl_sync(FULL, uu, (pl.A < g) ? g : g + 1);
+    return pl;
+}
+
 // Natural-log normaliser of logits/T over the kept tokens.  S is relative to MC = fp32(M*c); the
 // exact product M*c (fp64) recovers the normaliser relative to M/T.
 __device__ __forceinline__ float row_lse(const RowStats& rs, float c, double T)
@@ -73,6 +219,13 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
 {
     const int g = P.gamma, R = P.R, lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
+    if constexpr (PRE) {
+        if (R <= 32) {  // every row's statistics in one round of loads, one row per lane
+            RowStats rs = blank_rowstats();
+            if (lane < R) rs = ld_rowstats(P.rstats + (size_t)b * R + lane);
+            return plan_from_lanes(P, b, rs);
+        }
+    }
 
     int bad = 0, tmo = 0;
     for (int r = lane; r < R; r += 32) {
@@ -120,7 +273,7 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
             if (lq == -INFINITY) {
                 badtok = 1;  // q(x) = 0: the draft cannot have proposed x
             } else {
-                a = (lp >= lq) ? 1.0 : exp2(lp - lq);
+                a = accept_ratio(lp, lq);
                 if (!((double)u[i] < a) && i < rej_first) rej_first = i;
             }
         }

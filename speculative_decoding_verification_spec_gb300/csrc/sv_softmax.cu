@@ -107,10 +107,12 @@ __device__ __forceinline__ void task_softmax_stats(const char* row, long long t0
 
 __device__ __forceinline__ Partial ld_partial(const Partial* p)
 {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
     Partial r;
-    r.M = __ldcg(&p->M);
-    r.MC = __ldcg(&p->MC);
-    r.S = __ldcg(&p->S);
+    r.M = v.x;
+    r.MC = v.y;
+    r.S = v.z;
+    r.pad = 0.f;
     return r;
 }
 
@@ -151,7 +153,8 @@ __device__ __forceinline__ void stats_finalize(const SpecParams& P, int b, int r
         Partial pt;
         pt.M = M;
         pt.MC = MC;
-        pt.S = (double)S;
+        pt.S = S;
+        pt.pad = 0.f;
         P.partials[(size_t)row_id * P.S1 + s] = pt;
     }
     if (warp_arrive_last(&P.row_ctr[row_id], (unsigned)P.S1)) row_merge_and_plan<DT>(P, b, row_id, P.S1);
@@ -350,10 +353,11 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
         }
         if (tid == 0 && !failed) issue_next(s);
         Partial pt;
+        pt.pad = 0.f;
         if (failed) {
             pt.M = __int_as_float(0x7fc00000);  // the chunk was not read: S < 0 marks a timeout
             pt.MC = pt.M;
-            pt.S = -1.0;
+            pt.S = -1.f;
         } else {
             // maximum of the thread's elements, then of the warp
             float m;
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
             }
             pt.M = M;
             pt.MC = MC;
-            pt.S = (double)warp_sum((a0 + a1) + (a2 + a3));  // fp32: the fp64 pipe is slow here
+            pt.S = warp_sum((a0 + a1) + (a2 + a3));
         }
         if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
     }
@@ -404,90 +408,128 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
             (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
 }
 
-// Row merge and plan, one warp per row: the row's S1 x WARPS partials merged in order into
-// RowStats, with the lse, 1/S and log2 p(x) of the token the row scores filled in advance; the
-// last warp to finish a row of a request runs the acceptance scan and writes the plan.
+// Row merge and plan, one CTA per request.  Warp w merges rows w, w + WARPS, ... (two at a time,
+// the partial loads of both in flight together): each row's S1 x WARPS partials in order into
+// RowStats, with the lse, 1/S and log2 p(x) of the token the row scores, kept in shared memory.
+// After one CTA barrier warp 0 runs the acceptance scan over them and writes the plan.
 template <int DT>
 __global__ void __launch_bounds__(NT) spec_rowplan_kernel(SpecParams P)
 {
+    __shared__ RowStats srs[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row_id = blockIdx.x * WARPS + warp;
-    if (row_id >= P.B * P.R) return;
-    const int b = row_id / P.R, r = row_id - b * P.R, g = P.gamma;
-    // the token this row scores and its logit, fetched first so that they arrive meanwhile
-    const int pos = (r < g) ? r : (r > g) ? r - g - 1 : -1;
-    const int tok = (pos >= 0) ? __ldg(P.tokens + (size_t)b * g + pos) : -1;
-    const bool tok_ok = tok >= 0 && tok < P.V;
-    const float xtok = tok_ok ? load_logit(spec_row_ptr(P, b, r), DT, tok) : 0.f;
-    pdl_trigger();
-    pdl_wait();  // the partials of the streaming kernel
-
+    const int b = blockIdx.x, g = P.gamma, R = P.R;
+    const unsigned FULL = 0xffffffffu;
     const int nparts = P.S1 * WARPS;
-    const Partial* pp = P.partials + (size_t)row_id * nparts;
-    float Mr = NEG_INF;
-    double Sr = 0.0;
-    int tmo = 0;
-    if (nparts <= 128) {
-        // every partial of the row in flight at once: four per lane
-        Partial q[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int k = lane + 32 * t;
-            q[t].M = NEG_INF;
-            q[t].MC = NEG_INF;
-            q[t].S = 0.0;
-            if (k < nparts) q[t] = ld_partial(pp + k);
-            Mr = fmaxf(Mr, q[t].M);
-        }
-        Mr = warp_max(Mr);
+
+    // the token row r scores and its logit (inputs: fetched before waiting for the partials)
+    auto token_logit = [&](int r, bool& ok) -> float {
+        const int pos = (r < g) ? r : (r > g) ? r - g - 1 : -1;
+        const int tok = (r < R && pos >= 0) ? __ldg(P.tokens + (size_t)b * g + pos) : -1;
+        ok = tok >= 0 && tok < P.V;
+        return ok ? load_logit(spec_row_ptr(P, b, r), DT, tok) : 0.f;
+    };
+    // lane 0: the row's statistics from its merged maximum and sum
+    auto row_stats = [&](float Mr, DFloat Sr, int tmo, bool tok_ok, float xtok) {
         const float MCr = Mr * P.c;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            if (q[t].S < 0.0) tmo = 1;  // a chunk the streaming kernel could not read
-            if (q[t].S != 0.0) Sr += q[t].S * (double)ex2(q[t].MC - MCr);
-        }
-    } else {
-        for (int k = lane; k < nparts; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
-        Mr = warp_max(Mr);
-        const float MCr = Mr * P.c;
-        for (int k = lane; k < nparts; k += 32) {
-            const Partial q = ld_partial(pp + k);
-            if (q.S < 0.0) tmo = 1;
-            if (q.S != 0.0) Sr += q.S * (double)ex2(q.MC - MCr);
-        }
-    }
-    const float MCr = Mr * P.c;
-    Sr = warp_sum(Sr);
-    tmo = __any_sync(0xffffffffu, tmo);
-    if (lane == 0) {
-        RowStats st;
+        RowStats st = blank_rowstats();
         st.M = Mr;
         st.MC = MCr;
-        st.S = Sr;
-        st.thr = NEG_INF;
-        st.klist_n = -1;
-        st.dense = 0;
-        const bool ok = !tmo && isfinite(Sr) && Sr > 0.0 && Mr != NEG_INF && isfinite(Mr);
+        st.S = (double)Sr.hi;
+        const bool ok = !tmo && isfinite(Sr.hi) && Sr.hi > 0.f && Mr != NEG_INF && isfinite(Mr);
         st.status = tmo ? ROW_TIMEOUT : ok ? ROW_OK : ROW_NONFINITE;
         st.lse = __int_as_float(0x7fc00000);
-        st.invS = 0.f;
         st.lx = __longlong_as_double(0x7ff8000000000000ll);
-        if (ok) {
-            // log2 S from S = m 2^e, m in [0.5, 1): an fp32 log2 of m (absolute error ~1e-7) plus e
-            int e;
-            const double mm = frexp(Sr, &e);
-            const double l2S = (double)log2f((float)mm) + (double)e;
-            const double exact = (double)Mr * (double)P.c;
-            st.lse = (float)((double)Mr * P.invT + LN2 * (l2S - (exact - (double)MCr)));
-            st.invS = __frcp_rn(__double2float_rn(Sr));
-            if (tok_ok) st.lx = (double)fmaf(xtok, P.c, -MCr) - l2S;
+        if (ok) row_norm(st, Mr, MCr, Sr, P, tok_ok, xtok, NEG_INF);
+        return st;
+    };
+    auto publish_row = [&](int r, const RowStats& st) {
+        if (lane == 0) {
+            P.rstats[(size_t)b * R + r] = st;
+            if (r < 32) srs[r] = st;
+            else __threadfence();  // read back by warp 0 from global memory
         }
-        P.rstats[row_id] = st;
+    };
+
+    // rows r0 = warp + 2 WARPS j and r1 = r0 + WARPS, prefetched before the wait
+    for (int r0 = warp; r0 < R; r0 += 2 * WARPS) {
+        const int r1 = r0 + WARPS;
+        bool ok0, ok1;
+        const float x0 = token_logit(r0, ok0);
+        const float x1 = token_logit(r1, ok1);
+        if (r0 == warp) {
+            pdl_trigger();
+            pdl_wait();  // the partials of the streaming kernel
+        }
+        if (nparts <= 64) {
+            // both rows' partials in flight at once: two per lane and row
+            Partial q[2][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int rr = h ? r1 : r0, k = lane + 32 * t;
+                    q[h][t].M = NEG_INF;
+                    q[h][t].MC = NEG_INF;
+                    q[h][t].S = 0.f;
+                    if (rr < R && k < nparts) q[h][t] = ld_partial(P.partials + ((size_t)b * R + rr) * nparts + k);
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rr = h ? r1 : r0;
+                if (rr >= R) break;  // the same for the whole warp
+                const float Mr = warp_max(fmaxf(q[h][0].M, q[h][1].M));
+                const float MCr = Mr * P.c;
+                // the chunk sums rescaled to MCr, added as pairs of floats
+                DFloat Sr = df_make(0.f, 0.f);
+                int tmo = 0;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (q[h][t].S < 0.f) tmo = 1;  // a chunk the streaming kernel could not read
+                    if (q[h][t].S != 0.f) Sr = df_add(Sr, df_make(__fmul_rn(q[h][t].S, ex2(q[h][t].MC - MCr)), 0.f));  // NaN and inf propagate
+                }
+                Sr = warp_sum_df(Sr);
+                tmo = __any_sync(FULL, tmo);
+                publish_row(rr, row_stats(Mr, Sr, tmo, h ? ok1 : ok0, h ? x1 : x0));
+            }
+        } else {
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int rr = h ? r1 : r0;
+                if (rr >= R) break;
+                const Partial* pp = P.partials + ((size_t)b * R + rr) * nparts;
+                float Mr = NEG_INF;
+                for (int k = lane; k < nparts; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
+                Mr = warp_max(Mr);
+                const float MCr = Mr * P.c;
+                DFloat Sr = df_make(0.f, 0.f);
+                int tmo = 0;
+                for (int k = lane; k < nparts; k += 32) {
+                    const Partial q = ld_partial(pp + k);
+                    if (q.S < 0.f) tmo = 1;
+                    if (q.S != 0.f) Sr = df_add(Sr, df_make(__fmul_rn(q.S, ex2(q.MC - MCr)), 0.f));
+                }
+                Sr = warp_sum_df(Sr);
+                tmo = __any_sync(FULL, tmo);
+                publish_row(rr, row_stats(Mr, Sr, tmo, h ? ok1 : ok0, h ? x1 : x0));
+            }
+        }
     }
-    if (warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) {
-        const Plan pl = compute_plan_warp<DT, true>(P, b, false);
-        if (lane == 0) P.plan[b] = pl;
+    if (warp >= R) {  // a warp without rows still lets the next grid launch and waits like the rest
+        pdl_trigger();
+        pdl_wait();
     }
+    __syncthreads();
+    if (warp != 0) return;
+    Plan pl;
+    if (R <= 32) {
+        RowStats rs = blank_rowstats();
+        if (lane < R) rs = srs[lane];
+        pl = plan_from_lanes(P, b, rs);
+    } else {
+        __threadfence_block();
+        pl = compute_plan_warp<DT, true>(P, b, false);
+    }
+    if (lane == 0) P.plan[b] = pl;
 }
 
 // ---------------------------------------------------------------- kernel 2: residual draw
@@ -510,7 +552,9 @@ __device__ __forceinline__ void residual_from(const float (&xp)[VEC], const floa
 }
 
 // Resolve the token inside the segment of 32 vectors starting at vbase (one per lane), given the
-// mass t_local still to pass within it.  Runs in one warp; returns the token in every lane.
+// mass t_local still to pass within it.  Runs in one warp; returns the token in every lane.  The
+// scans inside the segment are fp32: the segment's mass is a small part of the total, so their
+// rounding stays far below the 1e-6 decision margin.
 template <int DT, int VEC>
 __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const char* rowq,
                                   const Plan& pl, long long vbase, double t_local)
@@ -531,11 +575,11 @@ __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const c
         }
         residual_from<VEC>(xp, xq, rowq != nullptr, pl, P.c, r);
     }
+    const float tl = (float)t_local;
     const float ls = tree_sum(r);
-    const double incl = warp_incl_scan((double)ls);
-    const double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    const double start = lane ? excl : 0.0;
-    const unsigned hit = __ballot_sync(0xffffffffu, t_local < incl && ls > 0.f);
+    const float incl = warp_incl_scan(ls);
+    const float start = incl - ls;
+    const unsigned hit = __ballot_sync(0xffffffffu, tl < incl && ls > 0.f);
     int owner;
     if (hit) {
         owner = __ffs(hit) - 1;
@@ -545,12 +589,13 @@ __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const c
     }
     int tok = -1;
     if (lane == owner) {
-        double run = start;
+        float run = start;
         int last_pos = -1;
+#pragma unroll
         for (int e = 0; e < VEC; ++e) {
             if (r[e] > 0.f) last_pos = e;
-            run += (double)r[e];
-            if (hit && t_local < run && r[e] > 0.f) { tok = e; break; }
+            run += r[e];
+            if (tok < 0 && hit && tl < run && r[e] > 0.f) tok = e;
         }
         if (tok < 0) tok = last_pos;
         tok = (tok < 0) ? -1 : (int)(v * VEC + tok);
@@ -558,7 +603,10 @@ __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const c
     return __shfl_sync(0xffffffffu, tok, owner);
 }
 
-// Request b's draw from its segment sums (one warp).  Returns the token, -1 if degenerate.
+// Request b's draw from its segment sums (one warp).  Returns the token, -1 if degenerate.  With up
+// to 32 x DPL segments every lane holds its block of sums in registers (one round of loads), adds
+// them pairwise in fp32 and the lane totals are scanned in fp64.
+constexpr int DPL = 16;
 template <int DT, int VEC>
 __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, const char* rowp,
                                   const char* rowq)
@@ -567,15 +615,61 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
     const float* segs = P.segs + (size_t)b * P.nseg;
     const int per = (P.nseg + 31) / 32;
     const int s0 = min(lane * per, P.nseg), s1 = min(s0 + per, P.nseg);
-    // each lane's contiguous block of segment sums, eight independent loads in flight at a time
+    if (per <= DPL) {
+        float v[DPL];
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) v[k] = (s0 + k < s1) ? __ldcg(segs + s0 + k) : 0.f;
+        const float lsum = tree_sum(v);
+        const double mine = (double)lsum;
+        const double incl = warp_incl_scan(mine);
+        const double Z = __shfl_sync(0xffffffffu, incl, 31);
+        if (!(Z > 0.0) || !isfinite(Z)) return -1;
+        const double excl = incl - mine;
+        const double t = pl.u * Z;
+        unsigned own = __ballot_sync(0xffffffffu, mine > 0.0 && t < excl + mine);
+        if (!own) {  // rounding: the last lane holding positive mass
+            const unsigned pos = __ballot_sync(0xffffffffu, mine > 0.0);
+            own = pos ? (1u << (31 - __clz(pos))) : 0u;
+            if (!own) return -1;
+        }
+        const int owner = __ffs(own) - 1;
+        int seg = -1;
+        double base = 0.0;
+        if (lane == owner) {
+            const float tr = (float)(t - excl);  // mass still to pass inside this lane's block
+            float run = 0.f, lastrun = 0.f;
+            int lastpos = -1;
+            float before = 0.f;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) {
+                if (seg < 0 && v[k] > 0.f) {
+                    lastpos = s0 + k;
+                    lastrun = run;
+                    if (tr < run + v[k]) {
+                        seg = s0 + k;
+                        before = run;
+                    }
+                }
+                run += v[k];
+            }
+            if (seg < 0) {
+                seg = lastpos;
+                before = lastrun;
+            }
+            base = excl + (double)before;
+        }
+        seg = __shfl_sync(0xffffffffu, seg, owner);
+        base = __shfl_sync(0xffffffffu, base, owner);
+        if (seg < 0) return -1;
+        return resolve_in_segment<DT, VEC>(P, rowp, rowq, pl, (long long)seg * SEGV, t - base);
+    }
+    // more segments than the registers hold: each lane's block in batches of eight
     double mine = 0.0;
     for (int q0 = s0; q0 < s1; q0 += 8) {
         float v[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) v[t] = (q0 + t < s1) ? __ldcg(segs + q0 + t) : 0.f;
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-            if (q0 + t < s1) mine += (double)v[t];
+        mine += (double)tree_sum(v);
     }
     const double incl = warp_incl_scan(mine);
     const double Z = __shfl_sync(0xffffffffu, incl, 31);
@@ -583,7 +677,7 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
     const double excl = incl - mine;
     const double t = pl.u * Z;
     unsigned own = __ballot_sync(0xffffffffu, mine > 0.0 && t < excl + mine);
-    if (!own) {  // rounding: the last lane holding positive mass
+    if (!own) {
         const unsigned pos = __ballot_sync(0xffffffffu, mine > 0.0);
         own = pos ? (1u << (31 - __clz(pos))) : 0u;
         if (!own) return -1;
@@ -594,20 +688,11 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
     if (lane == owner) {
         double run = 0.0, lastbase = excl;
         int lastpos = -1;
-        for (int q0 = s0; q0 < s1 && seg < 0; q0 += 8) {
-            float v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = (q0 + k < s1) ? __ldcg(segs + q0 + k) : 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int s = q0 + k;
-                if (s < s1 && seg < 0) {
-                    const double sv = (double)v[k];
-                    if (sv > 0.0) { lastpos = s; lastbase = excl + run; }
-                    if (sv > 0.0 && t < excl + run + sv) { seg = s; base = excl + run; }
-                    else run += sv;
-                }
-            }
+        for (int q = s0; q < s1 && seg < 0; ++q) {
+            const double sv = (double)__ldcg(segs + q);
+            if (sv > 0.0) { lastpos = q; lastbase = excl + run; }
+            if (sv > 0.0 && t < excl + run + sv) { seg = q; base = excl + run; }
+            else run += sv;
         }
         if (seg < 0) { seg = lastpos; base = lastbase; }
     }
@@ -756,8 +841,7 @@ static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
     mark_kernel_start(st);
     K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM), NT, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
-    launch_dependent(spec_rowplan_kernel<DT>, (unsigned)(((long long)P.B * P.R + WARPS - 1) / WARPS), NT, 0,
-                     st, P);
+    launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, NT, 0, st, P);
     launch_dependent(spec_resample_chunk_kernel<DT>, (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
 }
 

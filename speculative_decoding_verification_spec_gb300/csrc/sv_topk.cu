@@ -871,29 +871,21 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, u[i].x);
     const float M = warp_max(mx);
     const float MC = M * P.c;
-    double acc = 0.0;
+    // the sum of 2^(fma(x, c, -MC)) over the kept tokens, as a pair of floats
+    DFloat acc = df_make(0.f, 0.f);
     if (M != NEG_INF)
-        for (int i = lane; i < nk; i += 32) acc += (double)ex2(fmaf(u[i].x, P.c, -MC));
-    const double S = warp_sum(acc);
+        for (int i = lane; i < nk; i += 32) acc = df_add(acc, df_make(ex2(fmaf(u[i].x, P.c, -MC)), 0.f));
+    const DFloat S = warp_sum_df(acc);
     TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
     for (int i = lane; i < nk; i += 32) kl[i] = u[i];
     st.M = M;
     st.MC = MC;
-    st.S = S;
+    st.S = (double)S.hi;
     st.thr = key_value(gkey);
     st.klist_n = nk;
     st.status = (M != NEG_INF && isfinite(M)) ? ROW_OK : ROW_NONFINITE;
-    if (st.status == ROW_OK && lane == 0) {  // only lane 0's RowStats is stored
-        // log2 S from S = m 2^e, m in [0.5, 1): an fp32 log2 of m (absolute error ~1e-7) plus e,
-        // which keeps the fp64 pipe (slow on this part) out of the per-row work
-        int e;
-        const double m = frexp(S, &e);
-        const double l2S = (double)log2f((float)m) + (double)e;
-        const double exact = (double)M * (double)P.c;
-        st.lse = (float)((double)M * P.invT + LN2 * (l2S - (exact - (double)MC)));
-        st.invS = __frcp_rn(__double2float_rn(S));
-        if (tok_ok) st.lx = (xtok >= st.thr) ? (double)fmaf(xtok, P.c, -MC) - l2S : -INFINITY;
-    }
+    if (st.status == ROW_OK && lane == 0)  // only lane 0's RowStats is stored
+        row_norm(st, M, MC, S, P, tok_ok, xtok, st.thr);
     return st;
 }
 
