@@ -54,7 +54,8 @@ struct RowStats {     // one logit row after its chunks are combined
     // filled in advance by the top-k finish kernel (the plan reads them when `pre` is set)
     float lse;        // natural-log normaliser of logits / T over the kept tokens
     float invS;       // fp32(1 / S)
-    double lx;        // log2 p(x) of the token this row scores (NaN: none, or out of range)
+    float lx_hi, lx_lo;  // log2 p(x) of the token this row scores as a pair of floats (hi NaN:
+                         // none or out of range; -inf: p(x) = 0)
 };
 
 struct Plan {         // one request, after the acceptance scan

@@ -50,9 +50,12 @@ __device__ __forceinline__ void row_norm(RowStats& st, float M, float MC, DFloat
         if (xtok >= thr && isfinite(t0)) {
             DFloat t;
             two_sum(t0, -l2S.hi, t.hi, t.lo);
-            st.lx = df_to_double(df_make(t.hi, __fsub_rn(t.lo, l2S.lo)));
+            const DFloat lx = df_make(t.hi, __fsub_rn(t.lo, l2S.lo));
+            st.lx_hi = lx.hi;
+            st.lx_lo = lx.lo;
         } else {
-            st.lx = (xtok >= thr) ? (double)t0 : -INFINITY;  // a -inf logit: p(x) = 0
+            st.lx_hi = (xtok >= thr) ? t0 : NEG_INF;  // a -inf logit: p(x) = 0
+            st.lx_lo = 0.f;
         }
     }
 }
@@ -69,7 +72,8 @@ __device__ __forceinline__ RowStats ld_rowstats(const RowStats* p)
     r.dense = __ldcg(&p->dense);
     r.lse = __ldcg(&p->lse);
     r.invS = __ldcg(&p->invS);
-    r.lx = __ldcg(&p->lx);
+    r.lx_hi = __ldcg(&p->lx_hi);
+    r.lx_lo = __ldcg(&p->lx_lo);
     return r;
 }
 
@@ -115,12 +119,30 @@ __device__ __forceinline__ double accept_ratio(double lp, double lq)
     return (double)ex2(f) * scale;
 }
 
+// The same ratio from log2 probabilities held as pairs of floats (no fp64 at all): the difference
+// is formed exactly as a pair, its integer part n becomes an fp32 power of two and ex2 takes the
+// fraction.  Returns a float > 0 whenever p(x) > 0.
+__device__ __forceinline__ float accept_ratio_df(DFloat lp, DFloat lq)
+{
+    if (!(lp.hi < lq.hi || (lp.hi == lq.hi && lp.lo < lq.lo))) return 1.f;
+    if (lp.hi == NEG_INF) return 0.f;
+    float s, e;
+    two_sum(lp.hi, -lq.hi, s, e);
+    const DFloat d = df_make(s, __fadd_rn(e, __fsub_rn(lp.lo, lq.lo)));  // < 0
+    const float n = floorf(d.hi);
+    const float m = ex2(__fadd_rn(__fsub_rn(d.hi, n), d.lo));
+    const int ni = (n < -200.f) ? -200 : (int)n;
+    if (ni >= -126) return __fmul_rn(m, __int_as_float((ni + 127) << 23));
+    if (ni >= -150) return __fmul_rn(__fmul_rn(m, __int_as_float((ni + 24 + 127) << 23)), 5.9604644775390625e-8f);
+    return 1.40129846e-45f;  // the smallest positive float
+}
+
 __device__ __forceinline__ RowStats blank_rowstats()
 {
     RowStats r;
     r.M = NEG_INF; r.MC = NEG_INF; r.S = 0.0; r.thr = NEG_INF;
     r.status = ROW_OK; r.klist_n = -1; r.dense = 0;
-    r.lse = 0.f; r.invS = 0.f; r.lx = 0.0;
+    r.lse = 0.f; r.invS = 0.f; r.lx_hi = 0.f; r.lx_lo = 0.f;
     return r;
 }
 
@@ -137,7 +159,8 @@ __device__ __forceinline__ RowStats shfl_rowstats(const RowStats& r, int src)
     o.dense = __shfl_sync(FULL, r.dense, src);
     o.lse = __shfl_sync(FULL, r.lse, src);
     o.invS = __shfl_sync(FULL, r.invS, src);
-    o.lx = __shfl_sync(FULL, r.lx, src);
+    o.lx_hi = __shfl_sync(FULL, r.lx_hi, src);
+    o.lx_lo = __shfl_sync(FULL, r.lx_lo, src);
     return o;
 }
 
@@ -163,22 +186,26 @@ __device__ __forceinline__ Plan plan_from_lanes(const SpecParams& P, int b, cons
         }
     }
     // position i = lane < g: log2 p_i(x_i) is this lane's row, log2 q_i(x_i) row g + 1 + i's
-    const double lq = __shfl_sync(FULL, rs.lx, (lane + g + 1) & 31);
+    DFloat lp, lq;
+    lp.hi = rs.lx_hi;
+    lp.lo = rs.lx_lo;
+    lq.hi = __shfl_sync(FULL, rs.lx_hi, (lane + g + 1) & 31);
+    lq.lo = __shfl_sync(FULL, rs.lx_lo, (lane + g + 1) & 31);
     int badtok = 0;
     bool reject = false;
     if (lane < g) {
-        double a = __longlong_as_double(0x7ff8000000000000ll);
+        float a = __int_as_float(0x7fc00000);
         if (x < 0 || x >= P.V) {
             badtok = 1;
         } else if (!nonfinite) {
-            if (lq == -INFINITY) {
+            if (lq.hi == NEG_INF) {
                 badtok = 1;  // q(x) = 0: the draft cannot have proposed x
             } else {
-                a = accept_ratio(rs.lx, lq);
-                reject = !((double)uu < a);
+                a = accept_ratio_df(lp, lq);
+                reject = !(uu < a);
             }
         }
-        if (P.aux_accept) P.aux_accept[(size_t)b * g + lane] = (float)a;
+        if (P.aux_accept) P.aux_accept[(size_t)b * g + lane] = a;
     }
     badtok = __any_sync(FULL, badtok);
     const int badu = __any_sync(FULL, lane < g + 2 && !(uu >= 0.0f && uu < 1.0f));
@@ -252,8 +279,10 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
         double a = __longlong_as_double(0x7ff8000000000000ll);
         double plp = 0.0, plq = 0.0;
         if constexpr (PRE) {
-            plp = __ldcg(&P.rstats[(size_t)b * R + i].lx);
-            plq = __ldcg(&P.rstats[(size_t)b * R + g + 1 + i].lx);
+            const RowStats* rp = P.rstats + (size_t)b * R + i;
+            const RowStats* rq = P.rstats + (size_t)b * R + g + 1 + i;
+            plp = (double)__ldcg(&rp->lx_hi) + (double)__ldcg(&rp->lx_lo);
+            plq = (double)__ldcg(&rq->lx_hi) + (double)__ldcg(&rq->lx_lo);
         }
         if (x < 0 || x >= P.V) {
             badtok = 1;

@@ -408,15 +408,17 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
             (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
 }
 
-// Row merge and plan, one CTA per request.  Warp w merges rows w, w + WARPS, ... (two at a time,
-// the partial loads of both in flight together): each row's S1 x WARPS partials in order into
-// RowStats, with the lse, 1/S and log2 p(x) of the token the row scores, kept in shared memory.
-// After one CTA barrier warp 0 runs the acceptance scan over them and writes the plan.
+// Row merge and plan, one CTA per request of nw = min(R, PLAN_WARPS) warps (8 when R > 32).  Warp
+// w merges rows w, w + nw, ... (two at a time, the partial loads of both in flight together): each
+// row's S1 x WARPS partials in order into RowStats, with the lse, 1/S and log2 p(x) of the token the
+// row scores, kept in shared memory.  After one CTA barrier warp 0 runs the acceptance scan over
+// them and writes the plan.
+constexpr int PLAN_WARPS = 16;
 template <int DT>
-__global__ void __launch_bounds__(NT) spec_rowplan_kernel(SpecParams P)
+__global__ void __launch_bounds__(PLAN_WARPS * 32) spec_rowplan_kernel(SpecParams P)
 {
     __shared__ RowStats srs[32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int b = blockIdx.x, g = P.gamma, R = P.R;
     const unsigned FULL = 0xffffffffu;
     const int nparts = P.S1 * WARPS;
@@ -438,7 +440,8 @@ __global__ void __launch_bounds__(NT) spec_rowplan_kernel(SpecParams P)
         const bool ok = !tmo && isfinite(Sr.hi) && Sr.hi > 0.f && Mr != NEG_INF && isfinite(Mr);
         st.status = tmo ? ROW_TIMEOUT : ok ? ROW_OK : ROW_NONFINITE;
         st.lse = __int_as_float(0x7fc00000);
-        st.lx = __longlong_as_double(0x7ff8000000000000ll);
+        st.lx_hi = __int_as_float(0x7fc00000);
+        st.lx_lo = 0.f;
         if (ok) row_norm(st, Mr, MCr, Sr, P, tok_ok, xtok, NEG_INF);
         return st;
     };
@@ -450,9 +453,9 @@ __global__ void __launch_bounds__(NT) spec_rowplan_kernel(SpecParams P)
         }
     };
 
-    // rows r0 = warp + 2 WARPS j and r1 = r0 + WARPS, prefetched before the wait
-    for (int r0 = warp; r0 < R; r0 += 2 * WARPS) {
-        const int r1 = r0 + WARPS;
+    // rows r0 = warp + 2 nw j and r1 = r0 + nw, prefetched before the wait
+    for (int r0 = warp; r0 < R; r0 += 2 * nw) {
+        const int r1 = r0 + nw;
         bool ok0, ok1;
         const float x0 = token_logit(r0, ok0);
         const float x1 = token_logit(r1, ok1);
@@ -841,7 +844,8 @@ static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
     mark_kernel_start(st);
     K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM), NT, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
-    launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, NT, 0, st, P);
+    const int pw = (P.R <= 32) ? std::min(P.R, PLAN_WARPS) : WARPS;
+    launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, (unsigned)(32 * pw), 0, st, P);
     launch_dependent(spec_resample_chunk_kernel<DT>, (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
 }
 

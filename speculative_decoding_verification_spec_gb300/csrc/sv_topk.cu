@@ -705,7 +705,8 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     st.status = ROW_OK; st.klist_n = -1; st.dense = 0;
     st.lse = __int_as_float(0x7fc00000);
     st.invS = 0.f;
-    st.lx = __longlong_as_double(0x7ff8000000000000ll);
+    st.lx_hi = __int_as_float(0x7fc00000);
+    st.lx_lo = 0.f;
     const int nl = P.nsegr;  // lists of the row, <= 4
     const size_t sg0 = (size_t)row_id * nl;
     // the token this row scores (target row i and draft row i score draft token i; the last target
