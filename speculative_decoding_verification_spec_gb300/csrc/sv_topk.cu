@@ -38,9 +38,8 @@ constexpr int TK_SMEM = STREAM_SMEM;                    // dynamic shared memory
 // per-chunk candidate count codes
 constexpr int TK_OVERFLOW = -1, TK_NONFINITE = -2, TK_TIMEOUT = -3;
 constexpr int TK_PRODUCER = WARPS;         // kernel 1: the bulk-copy producer warp
+constexpr int TK_SLOTS = 4;                // kernel 1: per-segment shared state, by segment mod 4
 constexpr int TK_THREADS = NT + 32;        // kernel 1: WARPS consumer warps + the producer warp
-// the consumer warps of kernel 1 meet at named barrier 1 (the producer warp never waits there)
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory"); }
 
 // order-preserving 32-bit key of a float; -0 and +0 map to the same key
 __device__ __forceinline__ uint32_t okey(float x)
@@ -347,26 +346,81 @@ __device__ __forceinline__ float hist_bound(const int* h, int k, uint32_t key0)
     return key_value(key0 + ((uint32_t)bin << 16));
 }
 
+// The bound tau of a segment from its first chunk: the k-th largest of the NT thread maxima of the
+// chunk (valid for k <= NT: NT disjoint groups, so at least k elements reach it), as an
+// order-preserving key.  Group g is the set of elements consumer thread g holds -- vectors g + NT i
+// of the chunk -- so the value is the one the consumer warps would select themselves.  Computed by
+// one warp (the producer): lane l takes groups l + 32 j, from the stage (BULK) or from the row.
+template <int DT, bool BULK>
+__device__ uint32_t chunk_tau_key(const uint4* stage, const char* row, int cbase, int cend, int k)
+{
+    constexpr int VEC = BULK ? ((DT == DT_BF16) ? 8 : 4) : 1;
+    constexpr int EPT = (DT == DT_BF16) ? 2 * TK_NREG : TK_NREG;
+    const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
+    uint32_t keys[NT / 32];
+#pragma unroll
+    for (int j = 0; j < NT / 32; ++j) {
+        const int g = lane + 32 * j;
+        float tm = NEG_INF;
+        if constexpr (BULK) {
+            uint32_t pm = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+            for (int i = 0; i < TK_NV; ++i) {
+                if (cbase + (g + NT * i) * VEC < cend) {
+                    const uint4 q = lds128(stage + g + NT * i);
+                    if constexpr (DT == DT_BF16) {
+                        pm = bmax2_nan(pm, bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w)));
+                    } else {
+                        tm = fmax_nan_f(tm, fmax_nan_f(fmax_nan_f(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                                       fmax_nan_f(__uint_as_float(q.z), __uint_as_float(q.w))));
+                    }
+                }
+            }
+            if constexpr (DT == DT_BF16) tm = fmax_nan_f(bf16lo(pm), bf16hi(pm));
+        } else {
+            for (int s = 0; s < EPT; ++s) {
+                const int e = cbase + s * NT + g;
+                if (e < cend) tm = fmax_nan_f(tm, load_logit(row, DT, e));
+            }
+        }
+        keys[j] = okey(tm);
+    }
+    uint32_t prefix = 0;
+    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
+    for (int bit = 31; bit >= lo; --bit) {
+        const uint32_t want = prefix | (1u << bit);
+        unsigned cnt = 0;
+#pragma unroll
+        for (int j = 0; j < NT / 32; ++j) cnt += keys[j] >= want;
+        if ((int)__reduce_add_sync(FULL, cnt) >= k) prefix = want;
+    }
+    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
+    return prefix;
+}
+
 // Kernel 1: warp-specialised.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage
-// ring by a producer warp; otherwise the consumer warps load their elements straight into
-// registers.  A CTA takes segments (runs of up to P.sps chunks of one row) round-robin.
+// ring; otherwise the consumer warps load their elements straight into registers.  A CTA takes
+// segments (runs of up to P.sps chunks of one row) round-robin; segment j of the CTA uses slot
+// j % TK_SLOTS of the per-segment shared state (histogram, list length, flags, tau).
 //
-// Producer (warp WARPS, one lane): for every chunk in the CTA's order it waits until all consumer
-// warps have released the stage (an "empty" mbarrier per stage) and refills it with one bulk copy
-// (a "full" mbarrier per stage completes when the bytes land).
+// Producer (warp WARPS): lane 0 issues one bulk copy per chunk once every consumer warp has
+// released the stage (an "empty" mbarrier per stage; a "full" mbarrier completes when the bytes
+// land).  The whole warp also keeps the books of the segments: before segment j starts it waits
+// until segment j - TK_SLOTS is done by every consumer warp (a "done" mbarrier per slot), publishes
+// that segment -- its list length (or a status) and its final bound from the complete histogram --
+// and clears the slot; once the first chunk of segment j has landed it selects the segment's first
+// bound tau from it and publishes it through a "tau" mbarrier.  So the consumer warps never wait
+// for one another, and they are at most TK_SLOTS - 1 segments apart from the producer.
 //
 // Consumers (warps 0..WARPS-1): each waits on its chunk's full barrier, reads its 64 (bf16) or 32
-// (fp32) elements into registers, releases the stage and filters them on its own: warps meet only
-// at the start of each segment (a named barrier of the consumer warps), where the k-th largest of
-// the NT thread maxima of the segment's first chunk gives the segment's first bound tau.  Elements
-// sit in groups of 4 registers (one 16-byte vector); a group whose maximum reaches the current bound
-// beta goes to the segment's list (positions reserved with one shared-memory atomic per warp and
-// chunk), and its maximum is counted in a histogram above tau (bins 2^16 apart in the
-// order-preserving key: one bf16 value per bin).  Every count in the histogram is a distinct
-// element of the segment, whichever chunks the other warps have reached, so the warps take turns
-// turning it into a tighter bound for the chunks still to come, published as one 64-bit word
-// (segment, key).  At the next segment's start (and after the last segment) warp 0 publishes the
-// finished segment: its list length (or a status) and its final bound from the complete histogram.
+// (fp32) elements into registers and releases the stage.  Elements sit in groups of 4 registers
+// (one 16-byte vector); a group whose maximum reaches the current bound beta goes to the segment's
+// list (positions reserved with one shared-memory atomic per warp and chunk), and its maximum is
+// counted in a histogram above tau (bins 2^16 apart in the order-preserving key: one bf16 value per
+// bin).  Every count is a distinct element of the segment, whichever chunks the other warps have
+// reached, so the warps take turns turning the histogram into a tighter bound for the chunks still
+// to come, published as one 64-bit word (segment, key).
 template <int DT, bool BULK>
 __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P)
 {
@@ -380,14 +434,17 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     static_assert(NREG % G == 0, "register groups");
     static_assert((WARPS & (WARPS - 1)) == 0, "warps take turns by chunk index");
     extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
-    __shared__ float tmax[2][NT];      // thread maxima of a segment's first chunk (by segment parity)
-    __shared__ int hist[3][TK_BINS];   // by segment mod 3: in use, being published, being cleared
-    __shared__ int scount[2];          // groups listed in the segment (by segment parity)
-    __shared__ int sflag[2];           // 1: a NaN or +inf in the segment; 4: a wait ran out
-    __shared__ unsigned long long pub; // (segment << 32) | key of the latest bound published for it
-    __shared__ int sfail;              // a wait ran out in this CTA: nothing more is read
+    __shared__ int hist[TK_SLOTS][TK_BINS];
+    __shared__ int scount[TK_SLOTS];        // groups listed in the segment
+    __shared__ int sflag[TK_SLOTS];         // 1: a NaN or +inf in the segment; 4: a wait ran out
+    __shared__ uint32_t tau_key[TK_SLOTS];  // the segment's tau, published by the producer
+    __shared__ int seg_id[TK_SLOTS];        // the segment in the slot (producer's books)
+    __shared__ unsigned long long pub;      // (segment << 32) | key of the latest running bound
+    __shared__ int sfail;                   // a wait ran out in this CTA: nothing more is read
     __shared__ __align__(8) uint64_t full[TK_STAGES];
     __shared__ __align__(8) uint64_t empty[TK_STAGES];
+    __shared__ __align__(8) uint64_t tau_bar[TK_SLOTS];
+    __shared__ __align__(8) uint64_t done_bar[TK_SLOTS];
 
     pdl_trigger();  // the finish kernel may be scheduled as SMs free up; it waits for this grid
     clear_counters(P.ctr_clear, P.ctr_words);
@@ -397,45 +454,115 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     const int G0 = gridDim.x;
     const int k = P.top_k;
 
-    if (tid < NT) hist[0][tid] = 0;
+    for (int i = tid; i < TK_SLOTS * TK_BINS; i += TK_THREADS) (&hist[0][0])[i] = 0;
+    if (tid < TK_SLOTS) {
+        scount[tid] = 0;
+        sflag[tid] = 0;
+    }
     if (tid == 0) {
-        scount[0] = 0;
-        sflag[0] = 0;
         pub = ~0ull;  // segment field 0xffffffff: no bound yet
         sfail = 0;
-        if constexpr (BULK) {
-            for (int s = 0; s < TK_STAGES; ++s) {
-                mbar_init(&full[s], 1);
-                mbar_init(&empty[s], WARPS);
-            }
-            fence_mbar_init();
+        for (int s = 0; s < TK_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], WARPS);
         }
+        for (int s = 0; s < TK_SLOTS; ++s) {
+            mbar_init(&tau_bar[s], 1);
+            mbar_init(&done_bar[s], WARPS);
+        }
+        fence_mbar_init();
     }
     __syncthreads();
 
     // ------------------------------------------------------------------ producer warp
     if (warp == TK_PRODUCER) {
-        if constexpr (BULK) {
+        const uint64_t pol = policy_evict_first();
+        // the list length (or status) and final bound of the segment in slot `slot`, done or not
+        auto publish = [&](int slot, bool done) {
+            const int psg = seg_id[slot];
+            const uint32_t key0 = tau_key[slot];
+            const float tau = (k <= NT) ? key_value(key0) : NEG_INF;
+            float bnd = tau;
+            if (done && k <= NT && tau != NEG_INF) bnd = fmaxf(bnd, hist_bound(hist[slot], k, key0));
             if (lane == 0) {
-                const uint64_t pol = policy_evict_first();
-                SegCursor pc;
-                pc.init(blockIdx.x, G0, P.nsegr);
-                int stg = 0;
-                unsigned ph = 0;
-                long long n = 0;  // copies issued
-                bool ok = true;
-                for (; ok && pc.sg < nsegs; pc.next(G0, P.nsegr)) {
-                    const int nst = min(P.sps, P.CT - pc.si * P.sps);
-                    const char* row = spec_row_ptr(P, pc.row_id / P.R, pc.row_id % P.R);
-                    for (int st = 0; st < nst; ++st) {
-                        // the stage's previous fill released by every consumer warp (bounded)
-                        if (n >= TK_STAGES && !mbar_wait(&empty[stg], ph ^ 1u)) ok = false;
-                        if (ok && *reinterpret_cast<volatile int*>(&sfail)) ok = false;
-                        if (!ok) break;
-                        const int cbase = (pc.si * P.sps + st) * CHUNK;
-                        const int cend = min(cbase + CHUNK, P.V);
-                        bulk_load(ring + (size_t)stg * NT * TK_NV, row + (size_t)cbase * ES,
-                                  (unsigned)(cend - cbase) * ES, &full[stg], pol);
+                const int c = scount[slot], f = sflag[slot];
+                P.ccount[psg] = (!done || (f & 4)) ? TK_TIMEOUT : (f & 1) ? TK_NONFINITE
+                              : (k > NT || c > P.cap_s) ? TK_OVERFLOW : c;
+                P.cbound[psg] = bnd;
+            }
+        };
+        SegCursor pc;
+        pc.init(blockIdx.x, G0, P.nsegr);
+        int stg = 0;
+        unsigned ph = 0;
+        long long n = 0;  // copies issued
+        bool ok = true;
+        int m = 0;        // this CTA's segment counter
+        for (; pc.sg < nsegs; pc.next(G0, P.nsegr), ++m) {
+            const int slot = m % TK_SLOTS;
+            // the slot's previous segment: done by every consumer warp, published, cleared
+            if (m >= TK_SLOTS) {
+                const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)((m - TK_SLOTS) / TK_SLOTS) & 1u));
+                publish(slot, done);
+                if (!done) ok = false;
+#pragma unroll
+                for (int i = 0; i < TK_BINS / 32; ++i) hist[slot][lane + 32 * i] = 0;
+                if (lane == 0) {
+                    scount[slot] = 0;
+                    sflag[slot] = 0;
+                }
+            }
+            if (lane == 0) seg_id[slot] = pc.sg;
+            const int nst = min(P.sps, P.CT - pc.si * P.sps);
+            const char* row = spec_row_ptr(P, pc.row_id / P.R, pc.row_id % P.R);
+            // tau from the segment's first chunk, selected once the next copy is on its way (or at
+            // the segment's end), so that the ring keeps filling meanwhile
+            int t_stg = -1;
+            unsigned t_ph = 0;
+            int t_cbase = 0, t_cend = 0;
+            auto publish_tau = [&]() {
+                uint32_t key = 0;
+                if (k <= NT) {
+                    if constexpr (BULK) {
+                        if (t_stg >= 0 && __all_sync(FULL, mbar_wait(&full[t_stg], t_ph))) {
+                            key = chunk_tau_key<DT, true>(ring + (size_t)t_stg * NT * TK_NV, nullptr, t_cbase, t_cend, k);
+                            fence_proxy_async_smem();  // these reads come before the stage's refill
+                        } else {
+                            ok = false;
+                        }
+                    } else {
+                        key = chunk_tau_key<DT, false>(nullptr, row, t_cbase, t_cend, k);
+                    }
+                }
+                __syncwarp();  // the slot is clear before the consumers see this segment
+                if (lane == 0) {
+                    tau_key[slot] = key;
+                    if (!ok) *reinterpret_cast<volatile int*>(&sfail) = 1;
+                    mbar_arrive(&tau_bar[slot]);
+                }
+            };
+            for (int st = 0; st < nst; ++st) {
+                const int cbase = (pc.si * P.sps + st) * CHUNK;
+                const int cend = min(cbase + CHUNK, P.V);
+                if constexpr (BULK) {
+                    // lane 0: the stage's previous fill released by every consumer warp (bounded)
+                    int go = 0;
+                    if (lane == 0 && ok && !*reinterpret_cast<volatile int*>(&sfail)) {
+                        if (n < TK_STAGES || mbar_wait(&empty[stg], ph ^ 1u)) {
+                            bulk_load(ring + (size_t)stg * NT * TK_NV, row + (size_t)cbase * ES,
+                                      (unsigned)(cend - cbase) * ES, &full[stg], pol);
+                            go = 1;
+                        } else {
+                            *reinterpret_cast<volatile int*>(&sfail) = 1;
+                        }
+                    }
+                    go = __shfl_sync(FULL, go, 0);
+                    if (!go) ok = false;
+                    if (go && st == 0) {
+                        t_stg = stg;
+                        t_ph = ph;
+                    }
+                    if (go) {
                         ++n;
                         if (++stg == TK_STAGES) {
                             stg = 0;
@@ -443,12 +570,26 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                         }
                     }
                 }
-                if (!ok) *reinterpret_cast<volatile int*>(&sfail) = 1;
-                // the CTA may not leave while a copy is in flight: wait (bounded) for the last fill
-                // of every stage -- no later fill of that stage exists, so its phase is unambiguous
+                if (st == 0) {
+                    t_cbase = cbase;
+                    t_cend = cend;
+                }
+                if (st == 1) publish_tau();
+            }
+            if (nst == 1) publish_tau();
+        }
+        // the last segments: published once every consumer warp is done with them
+        for (int j = (m > TK_SLOTS ? m - TK_SLOTS : 0); j < m; ++j) {
+            const int slot = j % TK_SLOTS;
+            const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)(j / TK_SLOTS) & 1u));
+            publish(slot, done);
+        }
+        // the CTA may not leave while a copy is in flight: wait (bounded) for the last fill of
+        // every stage -- no later fill of that stage exists, so its phase is unambiguous
+        if constexpr (BULK) {
+            if (lane == 0)
                 for (long long j = (n > TK_STAGES ? n - TK_STAGES : 0); j < n; ++j)
                     (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u);
-            }
         }
         return;
     }
@@ -456,28 +597,14 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     // ------------------------------------------------------------------ consumer warps
     int stg = 0;          // ring stage of the next chunk
     unsigned ph = 0;      // its fill parity
-    int jseg = -1;        // this CTA's segment counter (selects tmax, hist, scount, sflag)
-    bool failed = false;  // a bulk-copy wait ran out: the remaining lists are marked, not filled
-    // the segment before the current one, published by warp 0 at the current one's start
-    int prev_sg = -1;
-    float prev_tau = NEG_INF;
-    uint32_t prev_key0 = 0;
-    // warp 0, after a consumer barrier: the segment's list length (or status) and final bound
-    auto publish = [&](int psg, int pj, float ptau, uint32_t pkey0) {
-        float bnd = ptau;
-        if (k <= NT && ptau != NEG_INF) bnd = fmaxf(bnd, hist_bound(hist[pj % 3], k, pkey0));
-        if (lane == 0) {
-            const int c = scount[pj & 1], f = sflag[pj & 1];
-            P.ccount[psg] = (f & 4) ? TK_TIMEOUT : (f & 1) ? TK_NONFINITE
-                          : (k > NT || c > P.cap_s) ? TK_OVERFLOW : c;
-            P.cbound[psg] = bnd;
-        }
-    };
+    int jseg = -1;        // this CTA's segment counter
+    bool failed = false;  // a wait ran out: the remaining segments are marked, not read
     SegCursor cc;
     cc.init(blockIdx.x, G0, P.nsegr);
     for (; cc.sg < nsegs; cc.next(G0, P.nsegr)) {
         const int sg = cc.sg;
         ++jseg;
+        const int slot = jseg % TK_SLOTS;
         const int nst = min(P.sps, P.CT - cc.si * P.sps);
         const char* row = BULK ? nullptr : spec_row_ptr(P, cc.row_id / P.R, cc.row_id % P.R);
         TopkEntry* slist = P.clist + (size_t)sg * P.cap_s;
@@ -570,123 +697,98 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             }
             const bool bad_now = __any_sync(FULL, tm != tm || tm == __int_as_float(0x7f800000));
 
-            // ---- a segment's first chunk: every consumer warp meets here once per segment (failed
-            // or not), after which the thread maxima are complete and the previous segment is done
-            // by all: warp 0 publishes it, and the histogram of the segment before it is cleared
-            // for the segment after this one
+            // ---- a segment's first chunk: tau from the producer (bounded wait); only after this
+            // does the warp touch the segment's slot, which the producer has cleared by then
             if (st == 0) {
-                tmax[jseg & 1][tid] = tm;
-                consumer_sync();
-                hist[(jseg + 1) % 3][tid] = 0;
-                if (warp == 0 && prev_sg >= 0) {
-                    publish(prev_sg, jseg - 1, prev_tau, prev_key0);
-                    if (lane == 0) {  // the slots of the published segment serve the next one
-                        scount[(jseg + 1) & 1] = 0;
-                        sflag[(jseg + 1) & 1] = 0;
+                if (!failed) {
+                    const bool got = __all_sync(FULL, mbar_wait(&tau_bar[slot], (unsigned)(jseg / TK_SLOTS) & 1u));
+                    if (!got) {
+                        failed = true;
+                        if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
                     }
-                } else if (warp == 0 && lane == 0) {
-                    scount[(jseg + 1) & 1] = 0;
-                    sflag[(jseg + 1) & 1] = 0;
                 }
-                // tau = the k-th largest thread maximum (valid for k <= NT), selected by every
-                // warp by itself
-                if (k <= NT) {
-                    uint32_t keys[NT / 32];
-#pragma unroll
-                    for (int i = 0; i < NT / 32; ++i) keys[i] = okey(tmax[jseg & 1][lane + 32 * i]);
-                    uint32_t prefix = 0;
-                    constexpr int lo = (DT == DT_BF16) ? 16 : 0;
-                    for (int bit = 31; bit >= lo; --bit) {
-                        const uint32_t want = prefix | (1u << bit);
-                        unsigned cnt = 0;
-#pragma unroll
-                        for (int i = 0; i < NT / 32; ++i) cnt += keys[i] >= want;
-                        if ((int)__reduce_add_sync(FULL, cnt) >= k) prefix = want;
-                    }
-                    if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
-                    tau_first = key_value(prefix);
-                    key0 = prefix;
+                if (!failed && k <= NT) {
+                    key0 = tau_key[slot];
+                    tau_first = key_value(key0);
                 }
-                prev_sg = sg;
-                prev_tau = tau_first;
-                prev_key0 = key0;
             }
-            // flags of this segment are set only after its barrier, once its slot has been cleared
-            if (bad_now && !seg_bad) {
-                seg_bad = 1;
-                if (lane == 0) atomicOr(&sflag[jseg & 1], 1);
-            }
-            if (failed) {
-                if (lane == 0) atomicOr(&sflag[jseg & 1], 4);
-                continue;
-            }
-            float beta = tau_first;
-            {
-                const unsigned long long pb = *reinterpret_cast<volatile unsigned long long*>(&pub);
-                if ((int)(pb >> 32) == sg) beta = fmaxf(beta, key_value((uint32_t)pb));
-            }
+            if (!failed) {
+                if (bad_now && !seg_bad) {
+                    seg_bad = 1;
+                    if (lane == 0) atomicOr(&sflag[slot], 1);
+                }
+                float beta = tau_first;
+                {
+                    const unsigned long long pb = *reinterpret_cast<volatile unsigned long long*>(&pub);
+                    if ((int)(pb >> 32) == sg) beta = fmaxf(beta, key_value((uint32_t)pb));
+                }
 
-            // ---- the warps take turns: a tighter bound from the histogram (counts of every warp
-            // so far), for the chunks still to come
-            if (warp == (st & (WARPS - 1)) && !seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
-                const float nb = hist_bound(hist[jseg % 3], k, key0);
-                if (lane == 0 && nb > beta)
-                    *reinterpret_cast<volatile unsigned long long*>(&pub) =
-                        ((unsigned long long)(unsigned)sg << 32) | okey(nb);
-            }
+                // ---- the warps take turns: a tighter bound from the histogram (counts of every
+                // warp so far), for the chunks still to come
+                if (warp == (st & (WARPS - 1)) && !seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
+                    const float nb = hist_bound(hist[slot], k, key0);
+                    if (lane == 0 && nb > beta)
+                        *reinterpret_cast<volatile unsigned long long*>(&pub) =
+                            ((unsigned long long)(unsigned)sg << 32) | okey(nb);
+                }
 
-            // ---- this warp's groups whose maximum reaches beta go to the segment's list: the
-            // maximum and the first element's index, and the group's 16 raw bytes; the maximum is
-            // counted in the histogram
-            if (!seg_bad && k <= NT) {
-                // bf16: compare against beta rounded down to bf16, so no element >= beta is missed
-                const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(beta));
-                unsigned pass = 0;
-#pragma unroll
-                for (int g = 0; g < NG; ++g) {
-                    bool ge;
-                    if constexpr (DT == DT_BF16) ge = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2) != 0u;
-                    else ge = __uint_as_float(gm[g]) >= beta;
-                    pass |= (unsigned)ge << g;
-                }
-                if (partial && pass) {  // groups that start past the row's end hold padding only
-#pragma unroll
-                    for (int g = 0; g < NG; ++g)
-                        if (slot_elem<VEC>(cbase, EPG * g) >= cend) pass &= ~(1u << g);
-                }
-                const int mine = __popc(pass);
-                if (__any_sync(FULL, mine)) {
-                    const int incl = warp_incl_scan(mine);
-                    int pos = 0;
-                    if (lane == 31) pos = atomicAdd(&scount[jseg & 1], incl);
-                    pos = __shfl_sync(FULL, pos, 31) + incl - mine;
-                    int* h = hist[jseg % 3];
-                    const bool count = tau_first != NEG_INF;
+                // ---- this warp's groups whose maximum reaches beta go to the segment's list: the
+                // maximum and the first element's index, and the group's 16 raw bytes; the maximum
+                // is counted in the histogram
+                if (!seg_bad && k <= NT) {
+                    // bf16: compare against beta rounded down to bf16, so no element >= beta is missed
+                    const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(beta));
+                    unsigned pass = 0;
 #pragma unroll
                     for (int g = 0; g < NG; ++g) {
-                        if (pass & (1u << g)) {
-                            TopkEntry en;
-                            if constexpr (DT == DT_BF16) en.x = fmaxf(bf16lo(gm[g]), bf16hi(gm[g]));
-                            else en.x = __uint_as_float(gm[g]);
-                            en.idx = slot_elem<VEC>(cbase, EPG * g);
-                            if (pos < P.cap_s) {
-                                slist[pos] = en;
-                                sdata[pos] = make_uint4(w[G * g], w[G * g + 1], w[G * g + 2], w[G * g + 3]);
-                            }
-                            ++pos;
-                            if (count) {
-                                const uint32_t kx = okey(en.x);
-                                if (kx >= key0) atomicAdd(&h[min((int)((kx - key0) >> 16), TK_BINS - 1)], 1);
+                        bool ge;
+                        if constexpr (DT == DT_BF16) ge = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&gm[g]), t2) != 0u;
+                        else ge = __uint_as_float(gm[g]) >= beta;
+                        pass |= (unsigned)ge << g;
+                    }
+                    if (partial && pass) {  // groups that start past the row's end hold padding only
+#pragma unroll
+                        for (int g = 0; g < NG; ++g)
+                            if (slot_elem<VEC>(cbase, EPG * g) >= cend) pass &= ~(1u << g);
+                    }
+                    const int mine = __popc(pass);
+                    if (__any_sync(FULL, mine)) {
+                        const int incl = warp_incl_scan(mine);
+                        int pos = 0;
+                        if (lane == 31) pos = atomicAdd(&scount[slot], incl);
+                        pos = __shfl_sync(FULL, pos, 31) + incl - mine;
+                        int* h = hist[slot];
+                        const bool count = tau_first != NEG_INF;
+#pragma unroll
+                        for (int g = 0; g < NG; ++g) {
+                            if (pass & (1u << g)) {
+                                TopkEntry en;
+                                if constexpr (DT == DT_BF16) en.x = fmaxf(bf16lo(gm[g]), bf16hi(gm[g]));
+                                else en.x = __uint_as_float(gm[g]);
+                                en.idx = slot_elem<VEC>(cbase, EPG * g);
+                                if (pos < P.cap_s) {
+                                    slist[pos] = en;
+                                    sdata[pos] = make_uint4(w[G * g], w[G * g + 1], w[G * g + 2], w[G * g + 3]);
+                                }
+                                ++pos;
+                                if (count) {
+                                    const uint32_t kx = okey(en.x);
+                                    if (kx >= key0) atomicAdd(&h[min((int)((kx - key0) >> 16), TK_BINS - 1)], 1);
+                                }
                             }
                         }
                     }
                 }
+            } else if (lane == 0) {
+                atomicOr(&sflag[slot], 4);
+            }
+            // ---- the segment's last chunk: this warp is done with the segment
+            if (st + 1 == nst) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&done_bar[slot]);
             }
         }
     }
-    // the CTA's last segment: published once every consumer warp is done with it
-    consumer_sync();
-    if (warp == 0 && prev_sg >= 0) publish(prev_sg, jseg, prev_tau, prev_key0);
 }
 
 // Kernel 2, one warp per row: exact threshold g from the row's candidate groups (nsegr segment
