@@ -111,26 +111,23 @@ __device__ void warp_sort_by_index(TopkEntry* e, int n)
     }
 }
 
-// One warp: acceptance scan of request b and the correction / bonus draw from the kept list of
-// the p row (index order); the residual is zero outside K_p.
-template <int DT, bool PRE = false>
-__device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
+// One warp: the correction / bonus draw of request b, planned as pl, from the kept list of the p
+// row (index order, nk entries); the residual is zero outside K_p.  Sums in pairs of floats.
+template <int DT>
+__device__ void topk_request_draw(const SpecParams& P, const Plan& pl, int nk, float* rr, int b)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
-    const Plan pl = compute_plan_warp<DT, PRE>(P, b, true);
     if (pl.status != ROW_OK) {
         emit_spec_warp(P, b, pl.status, 0, -1);
         return;
     }
-    const RowStats sp = ld_rowstats(P.rstats + (size_t)b * P.R + pl.rp);
-    const int nk = sp.klist_n;
     const TopkEntry* kl = P.klist + ((size_t)b * P.R + pl.rp) * P.cap_k;
     const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
     // each lane owns a contiguous block of the kept list
     const int per = (nk + 31) / 32;
     const int i0 = min(lane * per, nk), i1 = min(i0 + per, nk);
-    double mine = 0.0;
+    DFloat mine = df_make(0.f, 0.f);
     for (int b0 = i0; b0 < i1; b0 += 8) {
         // eight entries at a time: their list loads, then their q gathers, each batch in flight
         // together, then the residual in list order
@@ -139,8 +136,9 @@ __device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             if (b0 + t < i1) {
-                xp[t] = __ldcg(&kl[b0 + t].x);
-                v[t] = __ldcg(&kl[b0 + t].idx);
+                const TopkEntry e = ld_entry(kl + b0 + t);
+                xp[t] = e.x;
+                v[t] = e.idx;
             }
         }
         if (rowq) {
@@ -157,30 +155,40 @@ __device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
                     const float qq = (xq[t] >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq[t], P.c, -pl.MCq)), pl.invSq) : 0.f;
                     res = fmaxf(__fsub_rn(pp, qq), 0.f);
                 }
-                rr[b0 + t] = (double)res;
-                mine += (double)res;
+                rr[b0 + t] = res;
+                mine = df_add(mine, df_make(res, 0.f));
             }
         }
     }
-    const double incl = warp_incl_scan(mine);
-    const double Z = __shfl_sync(FULL, incl, 31);
+    // inclusive scan of the lane blocks' masses, in pairs of floats
+    DFloat incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        DFloat n;
+        n.hi = __shfl_up_sync(FULL, incl.hi, o);
+        n.lo = __shfl_up_sync(FULL, incl.lo, o);
+        if (lane >= o) incl = df_add(n, incl);
+    }
+    const double Z = df_to_double(DFloat{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)});
     int tok = -1;
     if (Z > 0.0 && isfinite(Z)) {
-        const double t = pl.u * Z, excl = incl - mine;
-        unsigned own = __ballot_sync(FULL, mine > 0.0 && t < excl + mine);
+        const double t = pl.u * Z;
+        const double inc = df_to_double(incl), m = df_to_double(mine), excl = inc - m;
+        unsigned own = __ballot_sync(FULL, m > 0.0 && t < inc);
         if (!own) {
-            const unsigned pos = __ballot_sync(FULL, mine > 0.0);
+            const unsigned pos = __ballot_sync(FULL, m > 0.0);
             own = pos ? (1u << (31 - __clz(pos))) : 0u;
         }
         if (own) {
             const int owner = __ffs(own) - 1;
             if (lane == owner) {
-                double run = excl;
+                const float tr = (float)(t - excl);  // mass still to pass inside this lane's block
+                float run = 0.f;
                 int lastpos = -1;
                 for (int i = i0; i < i1; ++i) {
-                    if (rr[i] > 0.0) lastpos = i;
+                    if (rr[i] > 0.f) lastpos = i;
                     run += rr[i];
-                    if (t < run && rr[i] > 0.0) { tok = __ldcg(&kl[i].idx); break; }
+                    if (tr < run && rr[i] > 0.f) { tok = __ldcg(&kl[i].idx); break; }
                 }
                 if (tok < 0 && lastpos >= 0) tok = __ldcg(&kl[lastpos].idx);
             }
@@ -189,7 +197,6 @@ __device__ void topk_request_epilogue(const SpecParams& P, double* rr, int b)
     }
     emit_spec_warp(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
 }
-
 
 // element index (within the row) of register slot s of this thread: vector j = s / VEC, element
 // e = s % VEC of it; vectors of a thread are NT apart
@@ -280,7 +287,6 @@ __device__ uint32_t warp_kth_key_hist(int n, int k, int* hist, KeyAt key_at)
 constexpr int TK_BINS = 256;  // histogram of candidate values above a segment's first bound
 static_assert(TK_BINS == NT, "one bin per thread to clear");
 constexpr int TK_CAND_MIN = 512;           // finish kernel: candidate elements of a row (at least)
-constexpr int FIN_WARPS = 4;               // finish kernel: warps (rows) per CTA
 // finish kernel: candidate capacity of a row, which also holds the kept list and the draw scratch
 __device__ __host__ __forceinline__ int topk_cand_cap(int cap_k) { return cap_k > TK_CAND_MIN ? cap_k : TK_CAND_MIN; }
 
@@ -843,10 +849,10 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     const int ls1 = __shfl_sync(FULL, incl, 0), ls2 = __shfl_sync(FULL, incl, 1), ls3 = __shfl_sync(FULL, incl, 2);
 
     // the groups whose maximum reaches beta: (first element's index, slot), compacted into kept;
-    // entries in batches of 8 per lane, every load of a batch issued before any is used
+    // entries in batches of 6 per lane, every load of a batch issued before any is used
     const TopkEntry* lists = P.clist + sg0 * P.cap_s;
     const uint4* gdata = P.cdata + sg0 * P.cap_s;
-    constexpr int EB = 8;
+    constexpr int EB = 6;
     int ng = 0;
     for (int p0 = 0; p0 < total; p0 += 32 * EB) {
         TopkEntry e[EB];
@@ -992,31 +998,54 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     return st;
 }
 
-// Kernel 2: one warp per row, FIN_WARPS rows per CTA (small CTAs with few registers, so that every
-// row of a large batch is resident at once); the last warp to finish a row of a request scans it
-// and draws.
+// Kernel 2: one CTA per request, one warp per row (nw = min(R, FIN_MAX_WARPS) warps, rows w, w +
+// nw, ...): each warp finishes its row into shared memory; after one CTA barrier warp 0 runs the
+// acceptance scan over them and draws from the kept list of the p row.  A request with a dense row
+// is left to kernel 3.
+constexpr int FIN_MAX_WARPS = 16;
+constexpr size_t FIN_MAX_SMEM = 200 * 1024;  // dynamic shared memory of one finish CTA, at most
 template <int DT>
-__global__ void __launch_bounds__(FIN_WARPS * 32, 7) topk_finish_kernel(SpecParams P)
+__global__ void __launch_bounds__(FIN_MAX_WARPS * 32, 2) topk_finish_kernel(SpecParams P)
 {
     extern __shared__ __align__(16) TopkEntry fin[];  // per warp: u[cand], kept[cap_k]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row_id = blockIdx.x * FIN_WARPS + warp;
-    if (row_id >= P.B * P.R) return;
-    const int b = row_id / P.R;
+    __shared__ RowStats srs[32];
+    __shared__ int sdense;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    const int b = blockIdx.x, R = P.R;
     const int cand = topk_cand_cap(P.cap_k);
     TopkEntry* u = fin + (size_t)warp * (cand + P.cap_k);
     TopkEntry* kept = u + cand;
-    const RowStats st = topk_row_finish<DT>(P, u, kept, row_id);
-    if (lane == 0) P.rstats[row_id] = st;
-    if (!warp_arrive_last(&P.req_ctr[b], (unsigned)P.R)) return;
-    int nd = 0;
-    for (int rr = lane; rr < P.R; rr += 32) nd += __ldcg(&P.rstats[(size_t)b * P.R + rr].dense);
-    nd = __reduce_add_sync(0xffffffffu, nd);
+    if (tid == 0) sdense = 0;
+    __syncthreads();
+    for (int r = warp; r < R; r += nw) {
+        const RowStats st = topk_row_finish<DT>(P, u, kept, b * R + r);
+        if (lane == 0) {
+            P.rstats[(size_t)b * R + r] = st;
+            if (r < 32) srs[r] = st;
+            else __threadfence();  // read back from global memory below
+            if (st.dense) atomicAdd(&sdense, 1);
+        }
+        __syncwarp();  // u and kept serve the next row
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int nd = sdense;
     if (nd > 0) {  // finished by topk_dense_kernel
         if (lane == 0) P.ndense[b] = nd;
         return;
     }
-    topk_request_epilogue<DT, true>(P, reinterpret_cast<double*>(u), b);
+    Plan pl;
+    int nk;
+    if (R <= 32) {
+        RowStats rs = blank_rowstats();
+        if (lane < R) rs = srs[lane];
+        pl = plan_from_lanes(P, b, rs);
+        nk = __shfl_sync(0xffffffffu, rs.klist_n, pl.rp);
+    } else {
+        pl = compute_plan_warp<DT, true>(P, b, true);
+        nk = __ldcg(&P.rstats[(size_t)b * R + pl.rp].klist_n);
+    }
+    topk_request_draw<DT>(P, pl, nk, reinterpret_cast<float*>(u), b);
 }
 
 // ---------------------------------------------------------------- exact fallback for dense rows
@@ -1176,11 +1205,12 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
         K1<<<cta_grid<K1>(nsegs, sms, 0, TK_THREADS), TK_THREADS, 0, st>>>(P);
     }
     mark_kernel_stop(st);
-    const size_t fsm = (size_t)FIN_WARPS * (topk_cand_cap(P.cap_k) + P.cap_k) * sizeof(TopkEntry);
+    // one warp per row, as many as the shared memory of one CTA holds (the rest loop over rows)
+    const size_t per_warp = (size_t)(topk_cand_cap(P.cap_k) + P.cap_k) * sizeof(TopkEntry);
+    const int fw = std::max(1, std::min(std::min(P.R, FIN_MAX_WARPS), (int)(FIN_MAX_SMEM / per_warp)));
+    const size_t fsm = (size_t)fw * per_warp;
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
-    launch_dependent(topk_finish_kernel<DT>, (unsigned)(((long long)P.B * P.R + FIN_WARPS - 1) / FIN_WARPS),
-                     FIN_WARPS * 32, fsm,
-                     st, P);
+    launch_dependent(topk_finish_kernel<DT>, (unsigned)P.B, (unsigned)(32 * fw), fsm, st, P);
     launch_dependent(topk_dense_kernel<DT>, (unsigned)P.B, NT, 0, st, P);
 }
 
