@@ -312,8 +312,22 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
     barrier()
     elapsed = dist_max(start.elapsed_time(end) / 1e3, world, dev)
-    call_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
+    call_ms_timed = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+
+    # per-call times once more without the dominant kernel's own events: an event recorded between
+    # two launches of a call breaks their dependent-launch overlap
+    clean = {n: [] for n in names}
+    for i in range(min(args.steps, 200)):
+        for n in names:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(n, devin[n], outs[n])
+            e1.record(stream)
+            clean[n].append((e0, e1))
+    torch.cuda.synchronize()
+    call_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in clean[n]) for n in names}
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -362,7 +376,8 @@ def run_ours(args, rank, world, local_rank):
     per_cfg = {}
     for n in names:
         gbs = batches[n].logit_bytes / (call_ms[n] / 1e3) / 1e9
-        per_cfg[n] = {"call_ms": round(call_ms[n], 5), "rows_per_s": batches[n].rows / (call_ms[n] / 1e3),
+        per_cfg[n] = {"call_ms": round(call_ms[n], 5), "call_ms_timed_region": round(call_ms_timed[n], 5),
+                      "rows_per_s": batches[n].rows / (call_ms[n] / 1e3),
                       "calls_per_s": 1e3 / call_ms[n], "logit_bytes": batches[n].logit_bytes,
                       "hbm_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
                       "frac_of_8tbs": round(gbs / 8000.0, 4)}
