@@ -212,7 +212,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     // 16-byte vectors: 32 KB stream chunks (statistics) and 2048-vector residual chunks; the
     // scalar path's persistent warps take TV1 / TV2 vectors per task
     P.S1 = (int)(vec > 1 ? stream_chunks(sh) : slices1(sh));
-    P.S2 = (int)(vec > 1 ? std::max(1LL, cdiv(sh.nvec, NT * 8)) : slices2(sh));
+    P.S2 = (int)(vec > 1 ? std::max(1LL, cdiv(sh.nvec, NT * RCV)) : slices2(sh));
     P.nseg = (int)nsegs(sh);
     P.tasks1 = (long long)B * R * P.S1;
     P.tasks2 = (long long)B * P.S2;

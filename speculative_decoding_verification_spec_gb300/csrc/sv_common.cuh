@@ -86,6 +86,7 @@ static_assert(sizeof(ArgmaxPartial) == 16, "argmax partials are read as one 16-b
 // base + j*32*U + u*32 + l, so every load instruction of a warp covers 32 consecutive vectors.
 constexpr int U1 = 8, ST1 = 4, TV1 = 32 * U1 * ST1;  // row statistics / argmax: 1024 vectors
 constexpr int U2 = 4, ST2 = 4, TV2 = 32 * U2 * ST2;  // residual pass over a row pair: 512 vectors
+constexpr int RCV = 8;  // residual pass over 16-byte vectors: vectors per row and thread of one CTA
 constexpr int SEGV = 32;                             // vectors per residual segment
 
 struct SpecParams {

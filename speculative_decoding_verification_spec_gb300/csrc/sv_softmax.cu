@@ -768,7 +768,6 @@ __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
 // selected row pair).  Thread t loads vectors t + i*NT (i < RCV) of both rows, U2 of each at a time
 // into registers.  Each warp's 32 vectors of one i form one segment; the last CTA of a request draws
 // the token.
-constexpr int RCV = 8;                 // vectors per row per thread
 constexpr int RCHUNK = NT * RCV;
 
 template <int DT>
