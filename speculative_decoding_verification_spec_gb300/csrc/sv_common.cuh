@@ -365,6 +365,40 @@ constexpr int STREAM_NV = STREAM_CHUNK_BYTES / (NT * 16);  // 16-byte vectors pe
 constexpr int STREAM_STAGES = 3;
 constexpr int STREAM_SMEM = STREAM_STAGES * STREAM_CHUNK_BYTES;
 
+// Warp-specialised streaming (the plain and tree kernels): one producer lane issues the CTA's chunks
+// ids blockIdx.x, + gridDim.x, ... (< nch) into the STREAM_STAGES-stage ring, refilling a stage once
+// all WARPS consumer warps have arrived on its "empty" mbarrier; the stage's "full" mbarrier completes
+// when the bytes land.  src(id, ptr, bytes, policy) describes chunk id.  A wait that runs out, or a
+// consumer's (sfail), stops the issue; the copies in flight are then waited for (bounded), so the
+// CTA never leaves while one could still land.
+template <class Src>
+__device__ void ring_produce(uint4* ring, uint64_t* full, uint64_t* empty, int* sfail, int nch, Src src)
+{
+    int stg = 0;
+    unsigned ph = 0;
+    long long n = 0;
+    for (int id = blockIdx.x; id < nch; id += gridDim.x) {
+        if (*reinterpret_cast<volatile int*>(sfail)) break;
+        if (n >= STREAM_STAGES && !mbar_wait(&empty[stg], ph ^ 1u)) {
+            *reinterpret_cast<volatile int*>(sfail) = 1;
+            break;
+        }
+        const char* ptr;
+        unsigned bytes;
+        uint64_t pol;
+        src(id, ptr, bytes, pol);
+        bulk_load(ring + (size_t)stg * NT * STREAM_NV, ptr, bytes, &full[stg], pol);
+        ++n;
+        if (++stg == STREAM_STAGES) {
+            stg = 0;
+            ph ^= 1u;
+        }
+    }
+    // the last fill of every stage: no later fill of that stage exists, so its phase is unambiguous
+    for (long long j = (n > STREAM_STAGES ? n - STREAM_STAGES : 0); j < n; ++j)
+        (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
+}
+
 // persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task (the occupancy query
 // runs once per kernel)
 template <auto K>

@@ -267,54 +267,57 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
 // fetched by bulk copies (TMA engine) into a ring of STREAM_STAGES shared-memory stages, so the
 // next chunks are in flight while one is reduced.  Each warp reduces its part of a chunk -- the
 // maximum first, then the sum of 2^(x c - MC) with MC = fp32(M c) -- and writes one partial per
-// (chunk, warp).  The only synchronisation is the CTA barrier per chunk that frees the stage.
+// (chunk, warp).  Warp-specialised: a producer warp fills the ring (ring_produce) and the consumer
+// warps release each stage on its "empty" mbarrier, so they never wait for one another.
 // NaN or +inf anywhere makes the partial's sum NaN, so the row merge reports the row non-finite.
 template <int DT>
-__global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
+__global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int CHUNK = NT * STREAM_NV * VEC;  // elements per chunk
     extern __shared__ __align__(128) uint4 ring[];  // STREAM_STAGES x (NT * STREAM_NV) vectors
     __shared__ __align__(8) uint64_t full[STREAM_STAGES];
+    __shared__ __align__(8) uint64_t empty[STREAM_STAGES];
+    __shared__ int sfail;  // a wait ran out in this CTA: nothing more is read
 
     pdl_trigger();  // the row-merge kernel may be scheduled as SMs free up; it waits for this grid
     clear_counters(P.ctr_clear, P.ctr_words);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned FULL = 0xffffffffu;
     const int nch = P.B * P.R * P.S1;  // < 2^31 (checked on the host)
     const int G0 = gridDim.x;
     const float c = P.c;
-
-    // producer (thread 0): chunks blockIdx.x, + G0, ... in this CTA's consumption order
-    int pid = blockIdx.x;
-    long long nissued = 0;
-    auto issue_next = [&](int s) {
-        if (pid >= nch) return;
-        const int row_id = pid / P.S1, ci = pid - row_id * P.S1;
-        const int b = row_id / P.R, r = row_id - b * P.R;
-        const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
-        const uint64_t pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
-        bulk_load(ring + (size_t)s * NT * STREAM_NV, spec_row_ptr(P, b, r) + (size_t)cbase * ES,
-                  (unsigned)(cend - cbase) * ES, &full[s], pol);
-        ++nissued;
-        pid += G0;
-    };
     if (tid == 0) {
-        for (int s = 0; s < STREAM_STAGES; ++s) mbar_init(&full[s], 1);
+        sfail = 0;
+        for (int s = 0; s < STREAM_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], WARPS);
+        }
         fence_mbar_init();
-        for (int s = 0; s < STREAM_STAGES; ++s) issue_next(s);
     }
     __syncthreads();
+    if (warp == WARPS) {  // the producer: the rows of the likely correction pairs stay in L2
+        if (lane == 0)
+            ring_produce(ring, full, empty, &sfail, nch,
+                         [&](int id, const char*& ptr, unsigned& bytes, uint64_t& pol) {
+                             const int row_id = id / P.S1, ci = id - row_id * P.S1;
+                             const int b = row_id / P.R, r = row_id - b * P.R;
+                             const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+                             ptr = spec_row_ptr(P, b, r) + (size_t)cbase * ES;
+                             bytes = (unsigned)(cend - cbase) * ES;
+                             pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
+                         });
+        return;
+    }
 
-    bool failed = false;  // a bulk-copy wait ran out: the remaining chunks are reported, not read
-    long long fail_it = 0;
-    long long it = 0;
+    bool failed = false;  // a wait ran out: the remaining chunks are reported, not read
     int stg = 0;          // it % STREAM_STAGES
     unsigned phase = 0;   // (it / STREAM_STAGES) & 1
     // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
     int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
     const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
-    for (int id = blockIdx.x; id < nch; id += G0, ++it) {
+    for (int id = blockIdx.x; id < nch; id += G0) {
         if (id != blockIdx.x) {
             row_id += drow;
             ci += dci;
@@ -330,8 +333,8 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
         const bool partial = cbase + CHUNK > cend;
         const int s = stg;
-        bool ok = !failed;
-        if (ok) ok = mbar_wait(&full[s], phase);
+        if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
+        bool ok = !failed && mbar_wait(&full[s], phase);
         uint4 w[STREAM_NV];
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
         const uint4* sb = ring + (size_t)s * NT * STREAM_NV + tid;
@@ -345,13 +348,16 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
                 if (ok && cbase + (j * NT + tid) * VEC < cend) w[j] = lds128(sb + j * NT);
             }
         }
-        // every thread has read its part of the stage: it can be refilled
-        const int anyfail = __syncthreads_or(!ok);
-        if (anyfail && !failed) {
+        // release the stage once every lane has read it; a warp whose wait ran out never releases
+        // it (its copy may still land), which stops the producer
+        ok = __all_sync(FULL, ok);
+        if (ok) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        } else if (!failed) {
             failed = true;
-            fail_it = it;
+            if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
         }
-        if (tid == 0 && !failed) issue_next(s);
         Partial pt;
         pt.pad = 0.f;
         if (failed) {
@@ -402,10 +408,6 @@ __global__ void __launch_bounds__(NT, 2) spec_stream_kernel(SpecParams P)
         }
         if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
     }
-    // after a failed wait, let the copies still in flight land before the CTA leaves (bounded)
-    if (failed && tid == 0)
-        for (long long j = fail_it; j < nissued && j < fail_it + STREAM_STAGES; ++j)
-            (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
 }
 
 // Row merge and plan, one CTA per request of nw = min(R, PLAN_WARPS) warps (8 when R > 32).  Warp
@@ -841,7 +843,7 @@ static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
 {
     constexpr auto K1 = spec_stream_kernel<DT>;
     mark_kernel_start(st);
-    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM), NT, STREAM_SMEM, st>>>(P);
+    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
     const int pw = (P.R <= 32) ? std::min(P.R, PLAN_WARPS) : WARPS;
     launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, (unsigned)(32 * pw), 0, st, P);

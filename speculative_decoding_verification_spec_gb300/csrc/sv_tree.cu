@@ -281,49 +281,55 @@ __global__ void __launch_bounds__(NT) tree_argmax_kernel(TreeParams P)
 // fetched by bulk copies into a ring of shared-memory stages.  Each thread finds its maximum (via
 // the maxima of its vectors) and the first of its elements equal to it -- its vectors and their
 // elements are in index order -- and each warp reduces (value, index) with ties to the lower
-// index into one partial per (chunk, warp).  A NaN anywhere marks the partial.
+// index into one partial per (chunk, warp).  A NaN anywhere marks the partial.  Warp-specialised:
+// a producer warp fills the ring (ring_produce) and the consumer warps release each stage on its
+// "empty" mbarrier, so they never wait for one another.
 template <int DT>
-__global__ void __launch_bounds__(NT, 2) tree_stream_kernel(TreeParams P)
+__global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int CHUNK = NT * STREAM_NV * VEC;
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) uint64_t full[STREAM_STAGES];
+    __shared__ __align__(8) uint64_t empty[STREAM_STAGES];
+    __shared__ int sfail;  // a wait ran out in this CTA: nothing more is read
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned FULL = 0xffffffffu;
     const int nch = P.B * P.R * P.S1;
     const int G0 = gridDim.x;
-    const uint64_t pol = policy_evict_first();
-
-    int pid = blockIdx.x;
-    long long nissued = 0;
-    auto issue_next = [&](int s) {
-        if (pid >= nch) return;
-        const int row_id = pid / P.S1, ci = pid - row_id * P.S1;
-        const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
-        const char* row = reinterpret_cast<const char*>(P.logits) + (size_t)row_id * P.V * ES;
-        bulk_load(ring + (size_t)s * NT * STREAM_NV, row + (size_t)cbase * ES, (unsigned)(cend - cbase) * ES,
-                  &full[s], pol);
-        ++nissued;
-        pid += G0;
-    };
     if (tid == 0) {
-        for (int s = 0; s < STREAM_STAGES; ++s) mbar_init(&full[s], 1);
+        sfail = 0;
+        for (int s = 0; s < STREAM_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], WARPS);
+        }
         fence_mbar_init();
-        for (int s = 0; s < STREAM_STAGES; ++s) issue_next(s);
     }
     __syncthreads();
+    if (warp == WARPS) {  // the producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            ring_produce(ring, full, empty, &sfail, nch,
+                         [&](int id, const char*& ptr, unsigned& bytes, uint64_t& cp) {
+                             const int row_id = id / P.S1, ci = id - row_id * P.S1;
+                             const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+                             ptr = reinterpret_cast<const char*>(P.logits) + ((size_t)row_id * P.V + cbase) * ES;
+                             bytes = (unsigned)(cend - cbase) * ES;
+                             cp = pol;
+                         });
+        }
+        return;
+    }
 
     bool failed = false;
-    long long fail_it = 0;
-    long long it = 0;
     int stg = 0;          // it % STREAM_STAGES
     unsigned phase = 0;   // (it / STREAM_STAGES) & 1
     // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
     int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
     const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
-    for (int id = blockIdx.x; id < nch; id += G0, ++it) {
+    for (int id = blockIdx.x; id < nch; id += G0) {
         if (id != blockIdx.x) {
             row_id += drow;
             ci += dci;
@@ -338,8 +344,8 @@ __global__ void __launch_bounds__(NT, 2) tree_stream_kernel(TreeParams P)
         }
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
         const int s = stg;
-        bool ok = !failed;
-        if (ok) ok = mbar_wait(&full[s], phase);
+        if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
+        bool ok = !failed && mbar_wait(&full[s], phase);
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
         const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
         uint4 w[STREAM_NV];
@@ -352,12 +358,16 @@ __global__ void __launch_bounds__(NT, 2) tree_stream_kernel(TreeParams P)
             w[j] = make_uint4(pad, pad, pad, pad);
             if (ok && in) w[j] = lds128(sb + j * NT + tid);
         }
-        const int anyfail = __syncthreads_or(!ok);
-        if (anyfail && !failed) {
+        // release the stage once every lane has read it; a warp whose wait ran out never releases
+        // it (its copy may still land), which stops the producer
+        ok = __all_sync(FULL, ok);
+        if (ok) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        } else if (!failed) {
             failed = true;
-            fail_it = it;
+            if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
         }
-        if (tid == 0 && !failed) issue_next(s);
         ArgmaxPartial pt;
         pt.pad = 0;
         if (failed) {
@@ -419,9 +429,6 @@ __global__ void __launch_bounds__(NT, 2) tree_stream_kernel(TreeParams P)
         }
         if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
     }
-    if (failed && tid == 0)
-        for (long long j = fail_it; j < nissued && j < fail_it + STREAM_STAGES; ++j)
-            (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
 }
 
 // One CTA per request: the warps merge the rows' partials (rows round-robin, every partial of a
@@ -508,7 +515,7 @@ static void launch_tree_chunk(const TreeParams& P, int sms, cudaStream_t st)
 {
     constexpr auto K1 = tree_stream_kernel<DT>;
     mark_kernel_start(st);
-    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM), NT, STREAM_SMEM, st>>>(P);
+    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
     const size_t smem = P.N <= TREE_SMEM_NODES ? (size_t)(4 * P.N + P.R) * sizeof(int32_t) : 0;
     set_smem_limit<tree_finish_kernel<DT>>(smem);
