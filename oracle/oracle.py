@@ -21,7 +21,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 F32, BF16, F64 = 0, 1, 2
 ROW_OK, ROW_NONFINITE, ROW_DEGENERATE, ROW_BAD_TOKEN = 0, 1, 2, 3
-ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM = 5, 6, 7
+ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 
 _lib = None
 
@@ -39,14 +39,41 @@ def build(force: bool = False) -> str:
 
 def _load():
     global _lib
-    if _lib is not None:
-        return _lib
-    lib = ctypes.CDLL(build())
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def build_planted(replacements, workdir: str):
+    """Compile a copy of ``spec_oracle.c`` with a mistake planted by text replacement.
+
+    ``replacements`` is a list of (old, new) pairs; each ``old`` must occur exactly once.  The copy
+    is built in ``workdir`` and returned bound like the real oracle, so that a test can show that a
+    pin fails when the arithmetic is wrong.  The real oracle is untouched.
+    """
+    with open(_SRC) as f:
+        src = f.read()
+    for old, new in replacements:
+        if src.count(old) != 1:
+            raise ValueError(f"planted replacement target must occur once: {old!r}")
+        src = src.replace(old, new)
+    path_c = os.path.join(workdir, "planted_oracle.c")
+    path_so = os.path.join(workdir, "libplanted_oracle.so")
+    with open(path_c, "w") as f:
+        f.write(src)
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", path_so, path_c, "-lm"])
+    return _bind(ctypes.CDLL(path_so))
+
+
+def _bind(lib):
     P, I, D, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
     lib.oracle_spec_verify.argtypes = [P, P, I, P, P, I, I, I, D, I, P, P, P, P, P, P, P]
     lib.oracle_spec_verify.restype = I
     lib.oracle_tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P]
     lib.oracle_tree_verify_greedy.restype = I
+    lib.oracle_tree_verify_sample.argtypes = [P, P, I, P, P, P, P, I, I, I, I, D, I,
+                                              P, P, P, P, P, P, P, P]
+    lib.oracle_tree_verify_sample.restype = I
     lib.oracle_row_probs.argtypes = [P, I, Z, I, D, I, P, P, P]
     lib.oracle_row_probs.restype = I
     lib.oracle_lse_online.argtypes = [P, I, I]
@@ -61,7 +88,6 @@ def _load():
     lib.oracle_inverse_cdf.restype = I
     lib.oracle_kth_largest.argtypes = [P, I, I]
     lib.oracle_kth_largest.restype = D
-    _lib = lib
     return lib
 
 
@@ -142,6 +168,50 @@ def tree_verify_greedy(logits, parents, tokens, max_out: int | None = None):
     )
     if rc != 0:
         raise ValueError("oracle_tree_verify_greedy rejected its arguments")
+    return out
+
+
+def tree_verify_sample(target, draft, parents, tokens, qrow, uniforms, temperature: float,
+                       max_out: int | None = None, lib=None):
+    """Stochastic tree verify by the residual update over children (fp64).
+
+    target [B, N+1, V], draft [B, Nq, V] (same dtype), parents / tokens / qrow [B, N] int32,
+    uniforms [B, N+1] float32.  Returns a dict with accepted_len, out_tokens, out_nodes,
+    row_status, accept (NaN where a node was not tested), margin, draw_lo, draw_hi.  ``lib`` selects
+    a planted copy (``build_planted``) instead of the oracle.
+    """
+    lib = lib or _load()
+    t, dt = _logits(target)
+    B, n1, V = t.shape
+    N = n1 - 1
+    d, dd = _logits(draft)
+    assert dd == dt and d.shape[0] == B and d.shape[2] == V
+    Nq = d.shape[1]
+    if max_out is None:
+        max_out = N + 1
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    qr = np.ascontiguousarray(qrow, dtype=np.int32).reshape(B, N)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, N + 1)
+    out = dict(
+        accepted_len=np.empty(B, np.int32),
+        out_tokens=np.empty((B, max_out), np.int32),
+        out_nodes=np.empty((B, max(max_out - 1, 0)), np.int32),
+        row_status=np.empty(B, np.int32),
+        accept=np.empty((B, N)),
+        margin=np.empty(B),
+        draw_lo=np.empty(B),
+        draw_hi=np.empty(B),
+    )
+    rc = lib.oracle_tree_verify_sample(
+        _ptr(t), _ptr(d), dt, _ptr(par), _ptr(tok), _ptr(qr), _ptr(u), B, N, Nq, V,
+        float(temperature), int(max_out),
+        _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
+        _ptr(out["out_nodes"]) if max_out > 1 else None, _ptr(out["row_status"]),
+        _ptr(out["accept"]), _ptr(out["margin"]), _ptr(out["draw_lo"]), _ptr(out["draw_hi"]),
+    )
+    if rc != 0:
+        raise ValueError("oracle_tree_verify_sample rejected its arguments")
     return out
 
 

@@ -11,7 +11,8 @@
  *   [M16]   "Module 16" speculative-decoding lesson (learnllm.pages.dev), "The Math: Speculative
  *           Sampling", "The Candidate Tree", "Verify the Tree -- and Why It's Exact".
  *   [M7.7]  "M7.7 - Draft Sources, Dependent Heads, Hardware-Aware Trees", section 0x07E
- *           (candidate row / predictor row convention).
+ *           (candidate row / predictor row convention), 0x08B (re-testing k candidates against the
+ *           same target is wrong), 0x09A (stochastic residual update over a node's children).
  *   [TRLM]  "Exact speculative and assisted decoding for TinyRustLM" (mikekappel.com),
  *           "Normative stochastic pseudocode", "Normative edge-case behavior".
  *
@@ -28,6 +29,9 @@
  *     uniforms outside [0,1) are a bad uniform; such requests emit nothing (-1).
  *   - tree argmax ties go to the lowest token index; the deepest valid node wins, ties to the
  *     lowest node index.
+ *   - stochastic tree: a node's children are tested in ascending node index; node i's accept test
+ *     uses uniform slot i and the one final draw (correction or bonus) uses slot N; only the rows
+ *     the walk visits are read, so a bad value in a row it never reaches goes unseen.
  */
 #include <math.h>
 #include <stdint.h>
@@ -42,7 +46,8 @@ enum {
     OR_ROW_BAD_TOKEN = 3,
     OR_ROW_BAD_PARENT = 5,
     OR_ROW_OVERFLOW = 6,
-    OR_ROW_BAD_UNIFORM = 7
+    OR_ROW_BAD_UNIFORM = 7,
+    OR_ROW_BAD_QROW = 8
 };
 
 /* ---------------------------------------------------------------- element access */
@@ -383,6 +388,131 @@ int oracle_tree_verify_greedy(const void* logits, int dtype, const int32_t* pare
     free(amax);
     free(valid);
     free(depth);
+    free(path);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- stochastic tree verify */
+
+/*
+ * Stochastic verification of a candidate tree by the residual update over children
+ * ([M7.7] 0x09A; [M7.7] 0x07E row convention; [M16] accept rule and inverse-CDF draw):
+ *   target   [B, N+1, V]  row 0 = prefix frontier, row i+1 = produced at node i
+ *   draft    [B, Nq, V]   proposal rows; node i's token was drawn from row qrow[b,i]
+ *   parents  [B, N]       -1 for a depth-1 node, else in [0, i)
+ *   tokens   [B, N], qrow [B, N]
+ *   uniforms [B, N+1]     slot i = the accept test of node i, slot N = the final draw
+ * The walk starts at the frontier.  At the current node it sets r = p (the processed target row of
+ * the node) and tests the children in ascending index: child s with token x is accepted when
+ * u[s] < min(1, r(x)/q_s(x)); the walk then moves to s.  On rejection r becomes the normalised
+ * positive part of r - q_s.  When every child is rejected the final token is drawn from r; when the
+ * node has no children it is the bonus, drawn from p.  Either way the draw uses u[N].
+ * Outputs: accepted_len[B] (path length, or -1), out_tokens[B, max_out] (path tokens, final token,
+ * then -1), out_nodes[B, max_out-1] (path node ids, then -1; may be NULL), row_status[B], and, each
+ * nullable: accept[B, N] (the ratio of every tested node, NaN for the rest), margin[B] (smallest
+ * distance between a used uniform and a boundary it was compared with), draw_lo / draw_hi [B] (the
+ * normalised CDF interval [C(y-1), C(y)) of the final token).
+ */
+int oracle_tree_verify_sample(const void* target, const void* draft, int dtype,
+                              const int32_t* parents, const int32_t* tokens, const int32_t* qrow,
+                              const float* uniforms, int B, int N, int Nq, int V, double T,
+                              int max_out, int32_t* accepted_len, int32_t* out_tokens,
+                              int32_t* out_nodes, int32_t* row_status, double* accept,
+                              double* margin, double* draw_lo, double* draw_hi)
+{
+    if (B < 0 || N < 0 || Nq < 0 || V < 1 || !(T > 0.0) || max_out < 1) return 1;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    int32_t* path = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N + 1));
+    for (int b = 0; b < B; ++b) {
+        const int32_t* par = parents + (size_t)b * N;
+        const int32_t* tok = tokens + (size_t)b * N;
+        const int32_t* qr = qrow + (size_t)b * N;
+        const float* u = uniforms + (size_t)b * (N + 1);
+        int st = OR_ROW_OK;
+        /* what the host-side description fixes, before any row is read */
+        for (int i = 0; i < N && st == OR_ROW_OK; ++i)
+            if (par[i] < -1 || par[i] >= i) st = OR_ROW_BAD_PARENT;
+        for (int i = 0; i < N && st == OR_ROW_OK; ++i)
+            if (qr[i] < 0 || qr[i] >= Nq) st = OR_ROW_BAD_QROW;
+        for (int i = 0; i < N && st == OR_ROW_OK; ++i)
+            if (tok[i] < 0 || tok[i] >= V) st = OR_ROW_BAD_TOKEN;
+        for (int i = 0; i <= N && st == OR_ROW_OK; ++i)
+            if (!(u[i] >= 0.0f && u[i] < 1.0f)) st = OR_ROW_BAD_UNIFORM;
+        if (accept)
+            for (int i = 0; i < N; ++i) accept[(size_t)b * N + i] = NAN;
+
+        double mg = INFINITY, lo = NAN, hi = NAN;
+        int n = 0, y = -1;
+        int cur = -1; /* the frontier */
+        while (st == OR_ROW_OK) {
+            double l, thr;
+            size_t off = ((size_t)b * (size_t)(N + 1) + (size_t)(cur + 1)) * (size_t)V;
+            if (oracle_row_probs(target, dtype, off, V, T, 0, p, &l, &thr) != OR_ROW_OK) {
+                st = OR_ROW_NONFINITE;
+                break;
+            }
+            for (int v = 0; v < V; ++v) r[v] = p[v];
+            int next = -1;
+            for (int s = cur + 1; s < N && next < 0; ++s) {
+                if (par[s] != cur) continue;
+                size_t qoff = ((size_t)b * (size_t)Nq + (size_t)qr[s]) * (size_t)V;
+                if (oracle_row_probs(draft, dtype, qoff, V, T, 0, q, &l, &thr) != OR_ROW_OK) {
+                    st = OR_ROW_NONFINITE;
+                    break;
+                }
+                int x = tok[s];
+                if (q[x] == 0.0) { st = OR_ROW_BAD_TOKEN; break; } /* q never proposes x */
+                double ratio = r[x] / q[x];
+                double a = ratio < 1.0 ? ratio : 1.0;
+                if (accept) accept[(size_t)b * N + s] = a;
+                double d = fabs((double)u[s] - a);
+                if (d < mg) mg = d;
+                if ((double)u[s] < a) { next = s; break; }
+                /* rejected: the remaining target mass is the positive residual ([M7.7] 0x09A) */
+                double Z = oracle_residual(r, q, V, r);
+                if (!(Z > 0.0)) { st = OR_ROW_DEGENERATE; break; }
+            }
+            if (st != OR_ROW_OK) break;
+            if (next >= 0) {
+                path[n++] = next;
+                cur = next;
+                if (n + 1 > max_out) { st = OR_ROW_OVERFLOW; break; }
+                continue;
+            }
+            /* every child rejected (correction from r), or a leaf (bonus from p = r) */
+            y = oracle_inverse_cdf(r, V, (double)u[N], &lo, &hi);
+            if (y < 0) { st = OR_ROW_DEGENERATE; break; }
+            double d1 = fabs((double)u[N] - lo), d2 = fabs((double)u[N] - hi);
+            if (d1 < mg) mg = d1;
+            if (d2 < mg) mg = d2;
+            break;
+        }
+
+        int32_t* out = out_tokens + (size_t)b * max_out;
+        int32_t* on = out_nodes ? out_nodes + (size_t)b * (max_out - 1) : NULL;
+        for (int i = 0; i < max_out; ++i) out[i] = -1;
+        if (on) for (int i = 0; i < max_out - 1; ++i) on[i] = -1;
+        if (st == OR_ROW_OK) {
+            for (int j = 0; j < n; ++j) {
+                out[j] = tok[path[j]];
+                if (on) on[j] = path[j];
+            }
+            out[n] = y;
+            accepted_len[b] = n;
+        } else {
+            accepted_len[b] = -1;
+            lo = hi = NAN;
+        }
+        if (row_status) row_status[b] = st;
+        if (margin) margin[b] = mg;
+        if (draw_lo) draw_lo[b] = lo;
+        if (draw_hi) draw_hi[b] = hi;
+    }
+    free(p);
+    free(q);
+    free(r);
     free(path);
     return 0;
 }
