@@ -7,6 +7,7 @@
  *   spec_verify        exact speculative sampling with temperature
  *   spec_verify_topk   the same with a top-k processor applied identically to target and draft
  *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
+ *   tree_verify_sample stochastic verification of a candidate tree (residual update over children)
  *
  * Sources (page title + section):
  *   "M7.1 - Speculative Decoding: Draft, Verify, Accept, Reject": 0x03 (accept probability and
@@ -17,7 +18,8 @@
  *     u < min(1, p(x)/q(x))), "Verify the Tree -- and Why It's Exact" (greedy tree walk).
  *   "M7.7 - Draft Sources, Dependent Heads, Hardware-Aware Trees": 0x07E (candidate row vs
  *     predictor row: a depth-1 node is scored by the frontier row, any other node by its
- *     parent's row).
+ *     parent's row), 0x08B-0x09A (several candidates at one node: test them in turn against the
+ *     running residual, never against the original target row).
  *   "Exact speculative and assisted decoding for TinyRustLM": "Normative stochastic pseudocode"
  *     (separate accept / correction / extra-token random streams, abort without emitting on
  *     non-finite rows or a non-positive residual), "Minimum target API" (row i predicts proposal
@@ -71,7 +73,8 @@ enum {
     SPEC_ROW_TIMEOUT = 4,              /* reserved: no kernel of this library waits on a flag */
     SPEC_ROW_BAD_PARENT = 5,           /* tree: parents[b,i] is not in [-1, i) */
     SPEC_ROW_OUTPUT_OVERFLOW = 6,      /* tree: accepted path + bonus does not fit in max_out */
-    SPEC_ROW_BAD_UNIFORM = 7           /* a uniform of the request is not in [0, 1) */
+    SPEC_ROW_BAD_UNIFORM = 7,          /* a uniform of the request is not in [0, 1) */
+    SPEC_ROW_BAD_PROPOSAL_ROW = 8      /* tree_verify_sample: qrow[b,i] is not in [0, Nq) */
 };
 
 /*
@@ -154,6 +157,48 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype,
                                void* stream);
 
 /*
+ * Stochastic tree verify (M7.7 0x09A residual update over a node's children; 0x07E row
+ * convention; Module 16 accept rule and inverse-CDF draw).  Exact: the emitted tokens, continued
+ * by target draws, follow the target distribution.
+ *
+ *   target_logits [B, N+1, V]  row 0 = prefix frontier, row i+1 = target logits at node i
+ *   draft_logits  [B, Nq, V]   proposal rows (may be NULL when N == 0)
+ *   parents       [B, N]       int32 in [-1, i): -1 for a depth-1 node
+ *   tokens        [B, N]       int32 token of node i
+ *   qrow          [B, N]       int32 in [0, Nq): node i's token was drawn from draft row qrow[b,i]
+ *                              (i.i.d. siblings share a row; e.g. qrow = parent + 1 with the draft
+ *                              rows laid out like the target rows)
+ *   uniforms      [B, N+1]     fp32 in [0, 1): slot i = the accept test of node i, slot N = the
+ *                              final draw.  Every slot is validated, tested or not.
+ *   temperature   > 0, finite; p = softmax(target/T), q = softmax(draft/T)
+ *   max_out >= 1               length of an out_tokens row; must hold the path plus one token
+ *
+ * The walk starts at the frontier with r = p of the current node's row and tests the node's
+ * children in ascending index: child s with token x is accepted when u[s] < min(1, r(x)/q_s(x)),
+ * and the walk moves to s (r is reset to p of s's row).  On rejection r becomes the normalised
+ * positive part of r - q_s.  When every child is rejected the final token is drawn from r; at a
+ * node without children it is the bonus, drawn from p.  The draw uses u[N] and picks the smallest
+ * token whose running mass (ascending index) exceeds u * (total mass).
+ *   accepted_len[b]          = path length (0 if the first node's children were all rejected)
+ *   out_tokens[b, 0..A-1]    = tokens on the path; out_tokens[b, A] = the final token; rest -1
+ *   out_nodes [B, max_out-1] = node ids on the path, then -1 (nullable)
+ *   row_status [B] (nullable); aux_accept [B, N] (nullable): the ratio of every tested node, NaN
+ *   for nodes the walk never tested.
+ * Only the rows the walk visits are read: a NaN or +inf there gives SPEC_ROW_NONFINITE, one in a
+ * row the walk never reaches goes unseen.  q_s(x) = 0 (a -inf draft logit at x) gives
+ * SPEC_ROW_BAD_TOKEN when node s is tested; a path plus final token longer than max_out gives
+ * SPEC_ROW_OUTPUT_OVERFLOW.  Limits: N <= 4096; V <= 262144 for bf16 and 131072 for fp32 (larger
+ * sizes return SPEC_ERR_INVALID_ARG).  No workspace: each request is one thread-block cluster
+ * whose state lives in shared memory.
+ */
+spec_status tree_verify_sample(const void* target_logits, const void* draft_logits,
+                               spec_dtype dtype, const int32_t* parents, const int32_t* tokens,
+                               const int32_t* qrow, const float* uniforms, int B, int N, int Nq,
+                               int V, float temperature, int max_out, int32_t* accepted_len,
+                               int32_t* out_tokens, int32_t* out_nodes, int32_t* row_status,
+                               float* aux_accept, void* stream);
+
+/*
  * spec_verify for callers that cannot allocate device memory.  The paper has no counterpart: this
  * call only changes where spec_verify's scratch lives.
  *
@@ -194,6 +239,7 @@ spec_status spec_verify_noalloc(const void* target_logits, const void* draft_log
  *   spec_verify        the row-statistics (one-pass normaliser) kernel
  *   spec_verify_topk   the streaming top-k kernel
  *   tree_verify_greedy the argmax kernel
+ *   tree_verify_sample its only kernel
  * spec_set_kernel_events(NULL, NULL) turns it off.  The setting is process-wide and not
  * synchronised: set it from the thread that issues the calls.
  */

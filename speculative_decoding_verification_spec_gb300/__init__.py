@@ -1,5 +1,5 @@
 """GB300 (sm_103a) speculative-decoding verify step: exact speculative sampling, its top-k
-variant, and greedy tree verify, as hand-written CUDA behind a C ABI (include/spec_verify.h).
+variant, greedy tree verify and stochastic tree verify, as hand-written CUDA behind a C ABI (include/spec_verify.h).
 
 The binding functions load the compiled library on first use and raise if it is missing: there is
 no CPU fallback.
@@ -15,5 +15,6 @@ from .binding import (  # noqa: F401
     spec_verify_noalloc,
     spec_verify_topk,
     tree_verify_greedy,
+    tree_verify_sample,
     workspace_bytes,
 )

@@ -15,11 +15,11 @@ from . import build_ext
 
 SPEC_F32, SPEC_BF16 = 0, 1
 ROW_OK, ROW_NONFINITE, ROW_DEGENERATE, ROW_BAD_TOKEN, ROW_TIMEOUT = 0, 1, 2, 3, 4
-ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM = 5, 6, 7
+ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 
 # every symbol the header declares
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
-           "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
+           "tree_verify_sample", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -51,6 +51,8 @@ def load(path: str | None = None):
     lib.spec_verify_topk.restype = I
     lib.tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
     lib.tree_verify_greedy.restype = I
+    lib.tree_verify_sample.argtypes = [P, P, I, P, P, P, P, I, I, I, I, F, I, P, P, P, P, P, P]
+    lib.tree_verify_sample.restype = I
     lib.spec_verify_noalloc.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P]
     lib.spec_verify_noalloc.restype = I
     lib.spec_set_kernel_events.argtypes = [P, P]
@@ -232,5 +234,42 @@ def tree_verify_greedy(logits, parents, tokens, *, max_out: int | None = None, o
                                 B, N, V, max_out, _ptr(out["accepted_len"]),
                                 _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")),
                                 _ptr(out.get("row_status")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc)
+    return out
+
+
+def tree_verify_sample(target, draft, parents, tokens, qrow, uniforms, temperature: float, *,
+                       max_out: int | None = None, aux: bool = False, out=None, stream=None):
+    """Stochastic tree verify on the GPU (residual update over each node's children).
+
+    target [B, N+1, V], draft [B, Nq, V] (same dtype), parents / tokens / qrow [B, N] int32,
+    uniforms [B, N+1] float32; all CUDA tensors.  Returns accepted_len, out_tokens, out_nodes,
+    row_status and, with ``aux``, accept [B, N] (NaN where a node was not tested).
+    """
+    lib = load()
+    _need_cuda(target, draft, parents, tokens, qrow, uniforms)
+    B, n1, V = target.shape
+    N = n1 - 1
+    Nq = draft.shape[1] if draft is not None and draft.dim() == 3 else 0
+    if draft is not None and N > 0 and (draft.shape[0] != B or draft.shape[2] != V or
+                                        _dtype_code(draft) != _dtype_code(target)):
+        raise ValueError("draft must be [B, Nq, V] with the target's dtype")
+    max_out = N + 1 if max_out is None else int(max_out)
+    dev = target.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, max_out, dtype=torch.int32, device=dev),
+            out_nodes=torch.empty(B, max(max_out - 1, 1), dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+        if aux:
+            out["accept"] = torch.empty(B, max(N, 1), dtype=torch.float32, device=dev)
+    rc = lib.tree_verify_sample(_ptr(target), _ptr(draft) if Nq > 0 else None, _dtype_code(target),
+                                _ptr(parents), _ptr(tokens), _ptr(qrow), _ptr(uniforms), B, N, Nq,
+                                V, float(temperature), max_out, _ptr(out["accepted_len"]),
+                                _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")),
+                                _ptr(out.get("row_status")), _ptr(out.get("accept")),
+                                _stream(stream))
     _check(rc)
     return out

@@ -381,6 +381,72 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+spec_status tree_verify_sample(const void* target_logits, const void* draft_logits,
+                               spec_dtype dtype, const int32_t* parents, const int32_t* tokens,
+                               const int32_t* qrow, const float* uniforms, int B, int N, int Nq,
+                               int V, float temperature, int max_out, int32_t* accepted_len,
+                               int32_t* out_tokens, int32_t* out_nodes, int32_t* row_status,
+                               float* aux_accept, void* stream)
+{
+    if (B < 0 || N < 0 || Nq < 0 || V < 1 || max_out < 1) return SPEC_ERR_INVALID_ARG;
+    if (N > TS_MAX_NODES) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    const size_t es = dtype == SPEC_BF16 ? 2 : 4;
+    if (!target_logits || !aligned(target_logits, es)) return SPEC_ERR_INVALID_ARG;
+    if (N > 0) {
+        if (Nq < 1 || !draft_logits || !aligned(draft_logits, es)) return SPEC_ERR_INVALID_ARG;
+        if (!parents || !tokens || !qrow || !aligned(parents, 4) || !aligned(tokens, 4) ||
+            !aligned(qrow, 4))
+            return SPEC_ERR_INVALID_ARG;
+    }
+    if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_INVALID_ARG;
+    if (!accepted_len || !out_tokens || !aligned(accepted_len, 4) || !aligned(out_tokens, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if ((out_nodes && !aligned(out_nodes, 4)) || (row_status && !aligned(row_status, 4)) ||
+        (aux_accept && !aligned(aux_accept, 4)))
+        return SPEC_ERR_INVALID_ARG;
+
+    const int dt = (dtype == SPEC_BF16) ? DT_BF16 : DT_F32;
+    const int EPV = dt == DT_BF16 ? 8 : 4;
+    const long long nvec = cdiv(V, EPV);
+    // the smallest cluster whose slices fit TS_VPT vectors per thread ...
+    int CL = 1;
+    while (CL <= TS_MAX_CLUSTER && cdiv(nvec, (long long)CL * TS_NT) > TS_VPT) CL *= 2;
+    if (CL > TS_MAX_CLUSTER) return SPEC_ERR_INVALID_ARG;  // V above the cluster's capacity
+    // ... widened, up to the portable 8, while the doubled cluster still leaves every CTA an SM of
+    // its own and each thread at least one vector (a wider cluster shares a row among more SMs, but
+    // every exchange between them then costs more)
+    const int sms = sm_count();
+    while (CL < 8 && 2LL * B * CL <= sms && nvec >= 2LL * CL * TS_NT) CL *= 2;
+    if ((long long)B * CL > 0x7fffffffLL) return SPEC_ERR_INVALID_ARG;
+
+    TreeSampleParams P;
+    std::memset(&P, 0, sizeof P);
+    P.target = target_logits;
+    P.draft = draft_logits;
+    P.parents = parents;
+    P.tokens = tokens;
+    P.qrow = qrow;
+    P.uniforms = uniforms;
+    P.B = B; P.N = N; P.Nq = Nq; P.V = V; P.max_out = max_out;
+    P.dtype = dt;
+    P.invT = 1.0f / temperature;
+    P.nvec = nvec;
+    P.vpt = (int)cdiv(nvec, (long long)CL * TS_NT);
+    P.accepted_len = accepted_len;
+    P.out_tokens = out_tokens;
+    P.out_nodes = (max_out > 1) ? out_nodes : nullptr;
+    P.row_status = row_status;
+    P.aux_accept = aux_accept;
+    // 16-byte loads when every row starts on a 16-byte boundary
+    const bool vec16 = ((size_t)V * es) % 16 == 0 && aligned(target_logits, 16) &&
+                       (N == 0 || aligned(draft_logits, 16));
+    const cudaError_t err = launch_tree_sample(P, CL, vec16, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 void spec_set_kernel_events(void* start, void* stop)
 {
     g_kernel_events.start = static_cast<cudaEvent_t>(start);

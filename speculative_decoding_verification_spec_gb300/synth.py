@@ -18,6 +18,11 @@ Workload recipes (five named configurations):
   c5  B=32  N=64    V=128256 bf16         tree logits as c3's target, Medusa tree 4/4/2/2 in BFS
                                           order truncated to 64 nodes; a node's token is its
                                           predictor row's argmax with prob 0.6, else uniform
+  c6  B=32  N=64    V=128256 bf16  T=0.7  stochastic tree verify: c5's tree; target rows as c3's
+                                          target, draft rows = 0.8*target + N(0,1.5^2) laid out
+                                          like the target rows (row 0 frontier, row i+1 at node i);
+                                          the children of a node are i.i.d. draws from the draft
+                                          row at their parent (qrow = parent + 1)
 
 Streams: SeedSequence(seed).spawn(3) gives (logits, draft sampling, uniforms); each is spawned again
 per request, so a request's inputs do not depend on B or on how many threads generate them.
@@ -70,6 +75,23 @@ CONFIGS = {
     "c4": SpecConfig("c4", 256, 7, 152064, "bf16", 0.8, 50, "peaks", 1.0, 2.0, 1004),
 }
 TREE_CONFIGS = {"c5": TreeConfig("c5", 32, 128256)}
+
+
+@dataclass(frozen=True)
+class SampleTreeConfig:
+    name: str
+    B: int
+    V: int
+    branching: tuple = (4, 4, 2, 2)
+    max_nodes: int = 64
+    dtype: str = "bf16"
+    temperature: float = 0.7
+    draft_scale: float = 0.8
+    draft_noise: float = 1.5
+    seed: int = 1006
+
+
+SAMPLE_TREE_CONFIGS = {"c6": SampleTreeConfig("c6", 32, 128256)}
 
 
 def scaled(cfg, **kw):
@@ -314,3 +336,62 @@ def make_tree_batch(cfg: TreeConfig, *, threads: int | None = None) -> TreeBatch
         for b in range(B):
             one(b)
     return TreeBatch(cfg, logits, np.broadcast_to(par, (B, N)).copy(), tokens)
+
+
+# ------------------------------------------------------------------ sampled trees
+
+@dataclass
+class SampleTreeBatch:
+    cfg: SampleTreeConfig
+    target: np.ndarray    # [B, N+1, V]
+    draft: np.ndarray     # [B, N+1, V]: row 0 frontier, row i+1 at node i
+    parents: np.ndarray   # [B, N] int32
+    tokens: np.ndarray    # [B, N] int32
+    qrow: np.ndarray      # [B, N] int32 = parent + 1
+    uniforms: np.ndarray  # [B, N+1] float32
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def rows(self) -> int:
+        return self.target.shape[0] * self.target.shape[1]
+
+
+def make_sample_tree_batch(cfg: SampleTreeConfig, *, parents=None,
+                           threads: int | None = None) -> SampleTreeBatch:
+    """Target rows as c3's target, draft rows 0.8 * target + noise; each node's token a Gumbel-max
+    draw from softmax(draft row at its parent / T) (the drafter's own sampler, outside the verify
+    step), so the children of one node are i.i.d. given their parent."""
+    par = medusa_tree_parents(cfg.branching, cfg.max_nodes) if parents is None else \
+        np.asarray(parents, dtype=np.int32)
+    N, B, V = len(par), cfg.B, cfg.V
+    ss_logit, ss_draw, ss_unif = np.random.SeedSequence(cfg.seed).spawn(3)
+    req_logit, req_draw, req_unif = ss_logit.spawn(B), ss_draw.spawn(B), ss_unif.spawn(B)
+    bias = _zipf_bias(V, cfg.seed)
+    sdt = np.uint16 if cfg.dtype == "bf16" else np.float32
+    target = np.empty((B, N + 1, V), dtype=sdt)
+    draft = np.empty((B, N + 1, V), dtype=sdt)
+    tokens = np.empty((B, N), dtype=np.int32)
+    uniforms = np.empty((B, N + 1), dtype=np.float32)
+    qrow = (par + 1).astype(np.int32)
+
+    def one(b):
+        rng = np.random.Generator(np.random.PCG64(req_logit[b]))
+        t32 = _target_rows(rng, "zipf", N + 1, V, bias)
+        d32 = (cfg.draft_scale * t32.astype(np.float64)
+               + rng.standard_normal((N + 1, V)) * cfg.draft_noise).astype(np.float32)
+        target[b] = _store(t32, cfg.dtype)
+        draft[b] = _store(d32, cfg.dtype)
+        if N:
+            z = stored_to_f64(draft[b][qrow]) / cfg.temperature
+            tokens[b] = gumbel_max_tokens(np.random.Generator(np.random.PCG64(req_draw[b])), z)
+        uniforms[b] = uniforms_from(np.random.Generator(np.random.PCG64(req_unif[b])), N + 1)
+
+    n = threads or _nthreads()
+    if n > 1 and B > 1:
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(one, range(B)))
+    else:
+        for b in range(B):
+            one(b)
+    return SampleTreeBatch(cfg, target, draft, np.broadcast_to(par, (B, N)).copy(), tokens,
+                           np.broadcast_to(qrow, (B, N)).copy(), uniforms)

@@ -92,6 +92,21 @@ def test_host_validation_without_gpu(lib):
                                   1 << 30, None) == INVALID
     assert lib.tree_verify_greedy(fake, 1, fake, fake, 2, 4, 10, 5, fake, fake, None, None, ws,
                                   64, None) == WORKSPACE
+    # tree_verify_sample: sizes, temperature, pointers and capacity, before any CUDA call
+    F = ctypes.c_float
+
+    def ts_call(B=2, N=4, Nq=5, V=1000, T=1.0, dtype=1, target=fake, draft=fake, par=fake,
+                tok=fake, qr=fake, u=fake, max_out=5, acc=fake, out=fake):
+        return lib.tree_verify_sample(target, draft, dtype, par, tok, qr, u, B, N, Nq, V, F(T),
+                                      max_out, acc, out, None, None, None, None)
+
+    assert ts_call(B=0) == 0
+    for bad in (dict(B=-1), dict(N=-1), dict(Nq=-1), dict(V=0), dict(max_out=0), dict(T=0.0),
+                dict(T=float("nan")), dict(dtype=3), dict(target=None), dict(draft=None),
+                dict(Nq=0), dict(par=None), dict(tok=None), dict(qr=None), dict(u=None),
+                dict(acc=None), dict(out=None), dict(target=P(0x10001)), dict(N=4097),
+                dict(V=262145), dict(dtype=0, V=131073), dict(u=P(0x10002))):
+        assert ts_call(**bad) == INVALID, bad
     assert lib.spec_status_string(0) == b"ok"
     # the no-allocation entry point refuses oversized or invalid sizes before any CUDA call
     TOO_LARGE = 4
