@@ -7,6 +7,7 @@
 
 #include "../../include/spec_verify.h"
 #include "sv_common.cuh"
+#include "sv_tree_sample.cuh"
 
 namespace sv {
 

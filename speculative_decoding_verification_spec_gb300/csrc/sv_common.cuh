@@ -32,8 +32,7 @@ enum {
     ROW_TIMEOUT = 4,
     ROW_BAD_PARENT = 5,
     ROW_OVERFLOW = 6,
-    ROW_BAD_UNIFORM = 7,
-    ROW_BAD_QROW = 8
+    ROW_BAD_UNIFORM = 7
 };
 
 // ---------------------------------------------------------------- workspace records
@@ -160,33 +159,6 @@ struct TreeParams {
     unsigned* work;           // [1]
     int32_t* amax;            // [B*R]
     int32_t* scratch;         // [B*N*2] depth / valid of each node
-};
-
-// Stochastic tree verify: one cluster of CL CTAs per request, each CTA one slice of the vocabulary
-constexpr int TS_NT = 512;               // threads per CTA
-constexpr int TS_WARPS = TS_NT / 32;
-constexpr int TS_VPT = 4;                // 16-byte vectors of a row per thread (registers)
-constexpr int TS_MAX_CLUSTER = 16;
-constexpr int TS_MAX_NODES = 4096;       // the tree description is kept in shared memory
-
-struct TreeSampleParams {
-    const void* target;       // [B, N+1, V]
-    const void* draft;        // [B, Nq, V]
-    const int32_t* parents;   // [B, N]
-    const int32_t* tokens;    // [B, N]
-    const int32_t* qrow;      // [B, N]
-    const float* uniforms;    // [B, N+1]
-    int B, N, Nq, V, max_out;
-    int dtype;
-    float invT;
-    long long nvec;           // vectors of EPV elements per row (the last may be partial)
-    int vpt;                  // vectors per thread: a CTA's slice is vpt * TS_NT vectors, a warp's
-                              // a contiguous run of vpt * 32 of them
-    int32_t* accepted_len;
-    int32_t* out_tokens;
-    int32_t* out_nodes;
-    int32_t* row_status;
-    float* aux_accept;        // [B, N] or null
 };
 
 // ---------------------------------------------------------------- small device helpers
@@ -763,8 +735,5 @@ cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st);
 cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st);
 // tree_argmax_kernel
 cudaError_t launch_tree_path(const TreeParams& P, int sms, cudaStream_t st);
-// tree_sample_kernel: dynamic shared memory of one CTA, and the clustered launch
-size_t tree_sample_smem(int vpt, int dtype, int N);
-cudaError_t launch_tree_sample(const TreeSampleParams& P, int CL, bool vec16, cudaStream_t st);
 
 }  // namespace sv

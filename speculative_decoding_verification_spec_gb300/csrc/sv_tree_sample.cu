@@ -21,7 +21,7 @@
 //     warp whose run holds the uniform's mass, scanning its elements in index order.
 #include <cooperative_groups.h>
 
-#include "sv_common.cuh"
+#include "sv_tree_sample.cuh"
 
 namespace cg = cooperative_groups;
 
