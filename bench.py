@@ -4,7 +4,10 @@ One step = one pass of the whole hot path over one batch of synthetic inputs per
   c3  spec_verify       B=64  gamma=5 V=128256 bf16 T=0.7         (temperature softmax, residual)
   c4  spec_verify_topk  B=256 gamma=7 V=152064 bf16 T=0.8 k=50    (top-k processor)
   c5  tree_verify_greedy B=32 N=64(+1) V=128256 bf16              (greedy tree walk)
-issued back to back on one stream.  ``--workload`` selects a single configuration instead.
+issued back to back on one stream.  ``--workload`` selects a single configuration instead, among
+them c6 (tree_verify_sample, B=32 N=64(+1) V=128256 bf16 T=0.7: the stochastic tree walk).  c6
+reads only the rows its walk visits (about 31 MB per call, inside L2), so each of its timed calls
+follows an L2 flush outside the call's events and its rates come from the per-call event times.
 
 value     logit rows per second, inputs resident in HBM (whole job, all ranks)
 e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
@@ -45,6 +48,7 @@ KERNEL_OF = {
     "c3": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c4": ("topk_stream_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c5": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
+    "c6": ("tree_sample_kernel", ["sv_tree_sample.cu", "sv_tree_sample.cuh", "sv_common.cuh"]),
 }
 DOMINANT_CFG = "c4"
 
@@ -55,13 +59,38 @@ def workload_batches(names, rank, requests=None):
     from speculative_decoding_verification_spec_gb300 import synth as S
     out = {}
     for n in names:
-        cfg = S.CONFIGS[n] if n in S.CONFIGS else S.TREE_CONFIGS[n]
+        cfg = (S.CONFIGS.get(n) or S.TREE_CONFIGS.get(n) or S.SAMPLE_TREE_CONFIGS[n])
         kw = dict(seed=rank_seed(cfg, rank))
         if requests:
             kw["B"] = requests
         cfg = S.scaled(cfg, **kw)
-        out[n] = S.make_spec_batch(cfg) if n in S.CONFIGS else S.make_tree_batch(cfg)
+        if n in S.CONFIGS:
+            out[n] = S.make_spec_batch(cfg)
+        elif n in S.TREE_CONFIGS:
+            out[n] = S.make_tree_batch(cfg)
+        else:
+            out[n] = S.make_sample_tree_batch(cfg)
     return out
+
+
+def is_sample_tree(b) -> bool:
+    return hasattr(b, "qrow")
+
+
+def is_greedy_tree(b) -> bool:
+    return hasattr(b, "logits")
+
+
+def sample_tree_rows_read(b, accepted_len, accept) -> int:
+    """Rows one tree_verify_sample call reads: the target row of every node its walk arrives at,
+    and one proposal row for each of those nodes whose children it tested (the children of a node
+    share the proposal row at their parent)."""
+    rows = 0
+    for i in range(b.parents.shape[0]):
+        rows += int(accepted_len[i]) + 1
+        tested = np.flatnonzero(~np.isnan(accept[i]))
+        rows += len(set(zip(b.parents[i, tested].tolist(), b.qrow[i, tested].tolist())))
+    return rows
 
 
 # ------------------------------------------------------------------ ranks
@@ -96,16 +125,23 @@ def describe(names):
             op = "spec_verify_topk" if c.top_k else "spec_verify"
             parts.append(f"{n} {op} B={c.B} gamma={c.gamma} V={c.V} {c.dtype} T={c.temperature}"
                          + (f" top_k={c.top_k}" if c.top_k else ""))
-        else:
+        elif n in S.TREE_CONFIGS:
             c = S.TREE_CONFIGS[n]
             parts.append(f"{n} tree_verify_greedy B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
                          f"{c.dtype} tree {'/'.join(map(str, c.branching))}")
+        else:
+            c = S.SAMPLE_TREE_CONFIGS[n]
+            parts.append(f"{n} tree_verify_sample B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
+                         f"{c.dtype} T={c.temperature} tree {'/'.join(map(str, c.branching))}, "
+                         f"children i.i.d. from the draft row at their parent")
     return " + ".join(parts)
 
 
 def kernels_per_call(batch):
     """Kernels one verify call launches on the 16-byte-vector (streaming) paths the suite uses."""
-    if hasattr(batch, "parents"):
+    if is_sample_tree(batch):
+        return 1                              # the clustered walk
+    if is_greedy_tree(batch):
         return 2                              # argmax stream + tree finish
     return 3                                  # stream + finish + dense / stream + row plan + residual
 
@@ -209,10 +245,15 @@ def cpu_baseline(names, budget_s=15.0):
     share = budget_s / len(names)
     for n, b in batches.items():
         rows_done, t_used, i = 0, 0.0, 0
-        B = b.logits.shape[0] if hasattr(b, "parents") else b.cfg.B
+        B = b.cfg.B
         while t_used < share and i < B:
             t0 = time.perf_counter()
-            if hasattr(b, "parents"):
+            if is_sample_tree(b):
+                O.tree_verify_sample(b.target[i:i + 1], b.draft[i:i + 1], b.parents[i:i + 1],
+                                     b.tokens[i:i + 1], b.qrow[i:i + 1], b.uniforms[i:i + 1],
+                                     b.cfg.temperature)
+                rows_done += b.target.shape[1]
+            elif is_greedy_tree(b):
                 O.tree_verify_greedy(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1])
                 rows_done += b.logits.shape[1]
             else:
@@ -251,7 +292,10 @@ def run_ours(args, rank, world, local_rank):
 
     host, devin, outs, wss = {}, {}, {}, {}
     for n, b in batches.items():
-        if hasattr(b, "parents"):
+        if is_sample_tree(b):
+            arrs = dict(target=b.target, draft=b.draft, parents=b.parents, tokens=b.tokens,
+                        qrow=b.qrow, uniforms=b.uniforms)
+        elif is_greedy_tree(b):
             arrs = dict(logits=b.logits, parents=b.parents, tokens=b.tokens)
         else:
             arrs = dict(target=b.target, draft=b.draft, tokens=b.draft_tokens, uniforms=b.uniforms)
@@ -263,7 +307,11 @@ def run_ours(args, rank, world, local_rank):
 
     def call(n, ins, out=None):
         b = batches[n]
-        if hasattr(b, "parents"):
+        if is_sample_tree(b):
+            return sv.tree_verify_sample(ins["target"], ins["draft"], ins["parents"], ins["tokens"],
+                                         ins["qrow"], ins["uniforms"], b.cfg.temperature, out=out,
+                                         aux=True, stream=stream)
+        if is_greedy_tree(b):
             return sv.tree_verify_greedy(ins["logits"], ins["parents"], ins["tokens"], out=out,
                                          workspace=wss[n], stream=stream)
         return sv.spec_verify(ins["target"], ins["draft"], ins["tokens"], ins["uniforms"],
@@ -273,6 +321,21 @@ def run_ours(args, rank, world, local_rank):
     for n in names:  # allocate outputs once
         outs[n] = call(n, devin[n])
     torch.cuda.synchronize()
+    # algorithmic bytes of one call: the logits it reads (all of them, except on the sampled tree,
+    # whose walk reads only the rows it visits)
+    read_bytes = {}
+    for n in names:
+        b = batches[n]
+        if is_sample_tree(b):
+            rows = sample_tree_rows_read(b, outs[n]["accepted_len"].cpu().numpy(),
+                                         outs[n]["accept"].cpu().numpy())
+            read_bytes[n] = rows * b.cfg.V * b.target.itemsize
+        else:
+            read_bytes[n] = b.logit_bytes
+    # calls whose reads fit in L2 are timed after an L2 flush (a 256 MB write), outside their events
+    flush = None
+    if any(read_bytes[n] < L2_BYTES for n in names):
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def barrier():
         if world > 1:
@@ -298,6 +361,8 @@ def run_ours(args, rank, world, local_rank):
         start.record(stream)
         for i in range(args.steps):
             for n in names:
+                if flush is not None:
+                    flush.zero_()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -311,7 +376,10 @@ def run_ours(args, rank, world, local_rank):
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    elapsed = dist_max(start.elapsed_time(end) / 1e3, world, dev)
+    if flush is None:
+        elapsed = dist_max(start.elapsed_time(end) / 1e3, world, dev)
+    else:  # the flushes are not verify work: the step time is the sum of the calls' event times
+        elapsed = dist_max(sum(a.elapsed_time(b) for n in names for a, b in ev[n]) / 1e3, world, dev)
     call_ms_timed = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
 
@@ -320,6 +388,8 @@ def run_ours(args, rank, world, local_rank):
     clean = {n: [] for n in names}
     for i in range(min(args.steps, 200)):
         for n in names:
+            if flush is not None:
+                flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -372,18 +442,19 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = measured_peak()
     rows_step = sum(batches[n].rows for n in names)
-    bytes_step = sum(batches[n].logit_bytes for n in names)
+    bytes_step = sum(read_bytes[n] for n in names)
     per_cfg = {}
     for n in names:
-        gbs = batches[n].logit_bytes / (call_ms[n] / 1e3) / 1e9
+        gbs = read_bytes[n] / (call_ms[n] / 1e3) / 1e9
         per_cfg[n] = {"call_ms": round(call_ms[n], 5), "call_ms_timed_region": round(call_ms_timed[n], 5),
                       "rows_per_s": batches[n].rows / (call_ms[n] / 1e3),
-                      "calls_per_s": 1e3 / call_ms[n], "logit_bytes": batches[n].logit_bytes,
+                      "requests_per_s": batches[n].cfg.B / (call_ms[n] / 1e3),
+                      "calls_per_s": 1e3 / call_ms[n], "logit_bytes": read_bytes[n],
                       "hbm_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
                       "frac_of_8tbs": round(gbs / 8000.0, 4)}
     dom_kernel, dom_files = KERNEL_OF[dom_cfg]
     sha = source_sha(dom_files)
-    achieved = batches[dom_cfg].logit_bytes / (kernel_ms / 1e3) / 1e9
+    achieved = read_bytes[dom_cfg] / (kernel_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": whole_job_rate(rows_step, world, args.steps, elapsed),
@@ -399,7 +470,10 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": describe(names), "input_dtype": "bf16",
                    "logit_rows_per_step": rows_step, "logit_bytes_per_step": bytes_step,
-                   "l2": f"inputs larger than L2 ({bytes_step / 1e6:.0f} MB per step > 129 MB); no flush",
+                   "l2": (f"inputs larger than L2 ({bytes_step / 1e6:.0f} MB per step > 129 MB); no flush"
+                          if flush is None else
+                          f"L2 flushed (256 MB write) before every call, outside its events; the "
+                          f"calls read {bytes_step / 1e6:.0f} MB per step"),
                    "parallelism": f"replicas x{world} (independent requests per rank)",
                    **({"requests_override": args.requests} if args.requests else {})},
         "hbm_gbs": bytes_step * world * args.steps / elapsed / 1e9,
@@ -411,7 +485,9 @@ def run_ours(args, rank, world, local_rank):
                      "kernel_ms": round(kernel_ms, 5),
                      "timing": "CUDA events recorded on the call's stream around this kernel's "
                                "launch (spec_set_kernel_events), mean over the timed steps; "
-                               "algorithmic bytes = the workload's logit bytes, read once"},
+                               "algorithmic bytes = the logit bytes the call reads, once"
+                               + (" (the sampled tree: the rows its walk visits)"
+                                  if is_sample_tree(batches[dom_cfg]) else "")},
         "clocks": clocks.summary(),
         "gpu_launches": args.steps * sum(kernels_per_call(batches[n]) for n in names),
         "e2e": e2e,
@@ -436,7 +512,13 @@ def run_reference(args, rank, world):
         rows = 0
         for n in (names[i % len(names)],):
             b = batches[n]
-            if hasattr(b, "parents"):
+            if is_sample_tree(b):
+                j = (i // len(names)) % b.cfg.B
+                O.tree_verify_sample(b.target[j:j + 1], b.draft[j:j + 1], b.parents[j:j + 1],
+                                     b.tokens[j:j + 1], b.qrow[j:j + 1], b.uniforms[j:j + 1],
+                                     b.cfg.temperature)
+                rows += b.target.shape[1]
+            elif is_greedy_tree(b):
                 j = (i // len(names)) % b.logits.shape[0]
                 O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
                 rows += b.logits.shape[1]
@@ -474,7 +556,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5"], default="suite")
+    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6"],
+                    default="suite")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
