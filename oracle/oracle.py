@@ -74,6 +74,11 @@ def _bind(lib):
     lib.oracle_tree_verify_sample.argtypes = [P, P, I, P, P, P, P, I, I, I, I, D, I,
                                               P, P, P, P, P, P, P, P]
     lib.oracle_tree_verify_sample.restype = I
+    lib.oracle_smc_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, D, I, D,
+                                      P, P, P, P, P, P, P, P, P]
+    lib.oracle_smc_verify.restype = I
+    lib.oracle_ess.argtypes = [P, I]
+    lib.oracle_ess.restype = D
     lib.oracle_row_probs.argtypes = [P, I, Z, I, D, I, P, P, P]
     lib.oracle_row_probs.restype = I
     lib.oracle_lse_online.argtypes = [P, I, I]
@@ -213,6 +218,56 @@ def tree_verify_sample(target, draft, parents, tokens, qrow, uniforms, temperatu
     if rc != 0:
         raise ValueError("oracle_tree_verify_sample rejected its arguments")
     return out
+
+
+def smc_verify(target, draft, draft_tokens, logw_in, uniforms, groups: int, temperature: float,
+               eta: float, top_k: int = 0):
+    """One SMC-SD verify round over ``groups`` groups of particles (fp64).
+
+    target [B, K+1, V], draft [B, K, V], draft_tokens [B, K], logw_in [B] (natural-log weights),
+    uniforms [B, 2] (extension draw, ancestor draw); B = groups * particles.  Returns a dict with
+    out_tokens, row_status, log_ratio, logw_out, ess, resampled, ancestors, margin, ess_margin.
+    """
+    lib = _load()
+    t, dt = _logits(target)
+    B, k1, V = t.shape
+    K = k1 - 1
+    if K > 0:
+        d, dd = _logits(draft)
+        assert dd == dt and d.shape == (B, K, V)
+    else:
+        d = np.zeros((B, 0, V), dtype=t.dtype)
+    assert B % groups == 0
+    Np = B // groups
+    tok = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
+    lw = np.ascontiguousarray(logw_in, dtype=np.float64).reshape(B)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, 2)
+    out = dict(
+        out_tokens=np.empty((B, K + 1), np.int32),
+        row_status=np.empty(B, np.int32),
+        log_ratio=np.empty(B),
+        logw_out=np.empty(B),
+        ess=np.empty(groups),
+        resampled=np.empty(groups, np.int32),
+        ancestors=np.empty(B, np.int32),
+        margin=np.empty(B),
+        ess_margin=np.empty(groups),
+    )
+    rc = lib.oracle_smc_verify(
+        _ptr(t), _ptr(d), dt, _ptr(tok), _ptr(lw), _ptr(u), groups, Np, K, V, float(temperature),
+        int(top_k), float(eta), _ptr(out["out_tokens"]), _ptr(out["row_status"]),
+        _ptr(out["log_ratio"]), _ptr(out["logw_out"]), _ptr(out["ess"]), _ptr(out["resampled"]),
+        _ptr(out["ancestors"]), _ptr(out["margin"]), _ptr(out["ess_margin"]),
+    )
+    if rc != 0:
+        raise ValueError("oracle_smc_verify rejected its arguments")
+    return out
+
+
+def ess(weights) -> float:
+    """Effective sample size of positive weights (given as weights, not logs)."""
+    lw = np.log(np.ascontiguousarray(weights, dtype=np.float64))
+    return _load().oracle_ess(_ptr(lw), lw.shape[0])
 
 
 def row_probs(logits_row, temperature: float, top_k: int = 0):

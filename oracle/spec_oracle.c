@@ -15,6 +15,8 @@
  *           same target is wrong), 0x09A (stochastic residual update over a node's children).
  *   [TRLM]  "Exact speculative and assisted decoding for TinyRustLM" (mikekappel.com),
  *           "Normative stochastic pseudocode", "Normative edge-case behavior".
+ *   [SMC]   the same Module 16 lesson, "SMC Speculative Decoding: Resample, Don't Reject":
+ *           "The Math: Reweight, Don't Reject" (block weight, ESS, Algorithm 1), "Two Exact Anchors".
  *
  * Readings taken where the pages are silent (each is listed in the design notes):
  *   - accept iff u < a with u in [0,1)                            ([M16] accept rule)
@@ -29,6 +31,9 @@
  *     uniforms outside [0,1) are a bad uniform; such requests emit nothing (-1).
  *   - tree argmax ties go to the lowest token index; the deepest valid node wins, ties to the
  *     lowest node index.
+ *   - SMC-SD round: uniform slot 0 draws the extension token from row K, slot 1 the particle's
+ *     ancestor; ancestors are drawn by inverse CDF over the group's normalised weights in particle
+ *     order; a particle with a bad status leaves its group's ESS and resampling undefined (NaN, -1)
  *   - stochastic tree: a node's children are tested in ascending node index; node i's accept test
  *     uses uniform slot i and the one final draw (correction or bonus) uses slot N; only the rows
  *     the walk visits are read, so a bad value in a row it never reaches goes unseen.
@@ -514,5 +519,147 @@ int oracle_tree_verify_sample(const void* target, const void* draft, int dtype,
     free(q);
     free(r);
     free(path);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- SMC-SD verify round */
+
+/*
+ * Effective sample size of n weights given as logs ([SMC] "The Math"): (sum w)^2 / sum w^2, with the
+ * weights scaled by their largest (the ratio does not change).  Returns NaN if a weight is NaN.
+ */
+double oracle_ess(const double* logw, int n)
+{
+    double m = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+        if (isnan(logw[i])) return NAN;
+        if (logw[i] > m) m = logw[i];
+    }
+    if (m == -INFINITY) return NAN;
+    double s1 = 0.0, s2 = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double w = exp(logw[i] - m);
+        s1 += w;
+        s2 += w * w;
+    }
+    return s1 * s1 / s2;
+}
+
+/*
+ * One SMC-SD round on the verify side for G groups of Np particles, B = G * Np requests, particle n
+ * of group g at request g * Np + n ([SMC] Algorithm 1, steps 2-5):
+ *   target [B, K+1, V], draft [B, K, V], tokens [B, K], logw_in [B] (natural-log weights before the
+ *   round), uniforms [B, 2] (slot 0: the extension draw, slot 1: the ancestor draw), eta.
+ * Per particle (processed rows as oracle_spec_verify, with temperature T and optional top-k):
+ *   log W = sum_j log p_j(d_j) - log q_j(d_j)                   (step 3, in log space)
+ *   x+ = inverse-CDF draw from p_K with slot 0                   (step 4)
+ *   out_tokens = d_1 .. d_K, x+
+ * Per group, when every particle is OK:
+ *   logw_mid = logw_in + log W; ESS over logw_mid                (step 5)
+ *   ESS < eta: ancestor of n = inverse-CDF draw over the normalised weights (particle order) with
+ *              slot 1 of particle n; logw_out = log(1/Np); resampled = 1
+ *   otherwise: ancestor of n = n; logw_out = logw_mid; resampled = 0
+ * A group with a particle whose status is not OK: ess NaN, resampled -1, ancestors -1, logw_out NaN
+ * (its OK particles still report their block ratio and tokens).
+ * Outputs (out_tokens, row_status and logw_out required, the rest nullable): log_ratio [B], logw_out [B], ess [G],
+ * resampled [G], ancestors [B], margin [B] (smallest distance of a used uniform to a boundary it was
+ * compared with, over the extension and ancestor draws), ess_margin [G] (|ESS - eta| / eta).
+ */
+int oracle_smc_verify(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                      const double* logw_in, const float* uniforms, int G, int Np, int K, int V,
+                      double T, int top_k, double eta, int32_t* out_tokens, int32_t* row_status,
+                      double* log_ratio, double* logw_out, double* ess, int32_t* resampled,
+                      int32_t* ancestors, double* margin, double* ess_margin)
+{
+    if (G < 0 || Np < 1 || K < 0 || V < 1 || !(T > 0.0) || !logw_out) return 1;
+    const int B = G * Np;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    double* lw = (double*)malloc(sizeof(double) * (size_t)Np);
+    double* w = (double*)malloc(sizeof(double) * (size_t)Np);
+    for (int b = 0; b < B; ++b) {
+        int st = OR_ROW_OK;
+        double lr = 0.0, l, thr;
+        const int32_t* tok = tokens + (size_t)b * (K > 0 ? K : 0);
+        const float* u = uniforms + (size_t)b * 2;
+        double mg = INFINITY;
+        for (int j = 0; j < K && st == OR_ROW_OK; ++j) {
+            size_t off_p = ((size_t)b * (size_t)(K + 1) + (size_t)j) * (size_t)V;
+            size_t off_q = ((size_t)b * (size_t)K + (size_t)j) * (size_t)V;
+            int sp = oracle_row_probs(target, dtype, off_p, V, T, top_k, p, &l, &thr);
+            int sq = oracle_row_probs(draft, dtype, off_q, V, T, top_k, q, &l, &thr);
+            if (sp != OR_ROW_OK || sq != OR_ROW_OK) { st = OR_ROW_NONFINITE; break; }
+            if (tok[j] < 0 || tok[j] >= V) { st = OR_ROW_BAD_TOKEN; break; }
+            if (q[tok[j]] == 0.0) { st = OR_ROW_BAD_TOKEN; break; } /* q never proposes d_j */
+            lr += log(p[tok[j]]) - log(q[tok[j]]);
+        }
+        size_t off_b = ((size_t)b * (size_t)(K + 1) + (size_t)K) * (size_t)V;
+        if (oracle_row_probs(target, dtype, off_b, V, T, top_k, p, &l, &thr) != OR_ROW_OK)
+            st = OR_ROW_NONFINITE; /* the row the extension token is drawn from */
+        if (st == OR_ROW_OK && !(u[0] >= 0.0f && u[0] < 1.0f && u[1] >= 0.0f && u[1] < 1.0f))
+            st = OR_ROW_BAD_UNIFORM;
+        int32_t* out = out_tokens + (size_t)b * (K + 1);
+        for (int j = 0; j <= K; ++j) out[j] = -1;
+        if (st == OR_ROW_OK) {
+            double lo, hi;
+            int y = oracle_inverse_cdf(p, V, (double)u[0], &lo, &hi);
+            if (y < 0) {
+                st = OR_ROW_DEGENERATE;
+            } else {
+                for (int j = 0; j < K; ++j) out[j] = tok[j];
+                out[K] = y;
+                mg = fmin(fabs((double)u[0] - lo), fabs((double)u[0] - hi));
+            }
+        }
+        row_status[b] = st;
+        if (log_ratio) log_ratio[b] = (st == OR_ROW_OK) ? lr : NAN;
+        logw_out[b] = (st == OR_ROW_OK) ? logw_in[b] + lr : NAN;
+        if (margin) margin[b] = mg;
+    }
+    /* groups: ESS and resampling (step 5) */
+    for (int g = 0; g < G; ++g) {
+        int ok = 1;
+        for (int n = 0; n < Np; ++n) {
+            const int b = g * Np + n;
+            if (row_status[b] != OR_ROW_OK) ok = 0;
+        }
+        if (!ok) {
+            if (ess) ess[g] = NAN;
+            if (resampled) resampled[g] = -1;
+            if (ess_margin) ess_margin[g] = INFINITY;
+            for (int n = 0; n < Np; ++n) {
+                if (ancestors) ancestors[g * Np + n] = -1;
+                logw_out[g * Np + n] = NAN;
+            }
+            continue;
+        }
+        for (int n = 0; n < Np; ++n) lw[n] = logw_out[g * Np + n]; /* logw_in + log W */
+        const double e = oracle_ess(lw, Np);
+        if (ess) ess[g] = e;
+        if (ess_margin) ess_margin[g] = fabs(e - eta) / eta;
+        const int rs = e < eta;
+        if (resampled) resampled[g] = rs;
+        if (rs) {
+            double m = -INFINITY;
+            for (int n = 0; n < Np; ++n) if (lw[n] > m) m = lw[n];
+            for (int n = 0; n < Np; ++n) w[n] = exp(lw[n] - m);
+            for (int n = 0; n < Np; ++n) {
+                const int b = g * Np + n;
+                double lo, hi;
+                const double un = (double)uniforms[(size_t)b * 2 + 1];
+                const int a = oracle_inverse_cdf(w, Np, un, &lo, &hi);
+                if (ancestors) ancestors[b] = a;
+                if (margin) margin[b] = fmin(margin[b], fmin(fabs(un - lo), fabs(un - hi)));
+            }
+            for (int n = 0; n < Np; ++n) logw_out[g * Np + n] = -log((double)Np);
+        } else {
+            for (int n = 0; n < Np; ++n)
+                if (ancestors) ancestors[g * Np + n] = n;
+        }
+    }
+    free(p);
+    free(q);
+    free(lw);
+    free(w);
     return 0;
 }
