@@ -578,24 +578,27 @@ int oracle_smc_verify(const void* target, const void* draft, int dtype, const in
     double* lw = (double*)malloc(sizeof(double) * (size_t)Np);
     double* w = (double*)malloc(sizeof(double) * (size_t)Np);
     for (int b = 0; b < B; ++b) {
-        int st = OR_ROW_OK;
+        /* statuses in the order of the plain round (a non-finite row anywhere, then the tokens,
+         * then the uniforms), the log ratios gathered on the way */
+        int st = OR_ROW_OK, badtok = 0;
         double lr = 0.0, l, thr;
         const int32_t* tok = tokens + (size_t)b * (K > 0 ? K : 0);
         const float* u = uniforms + (size_t)b * 2;
         double mg = INFINITY;
-        for (int j = 0; j < K && st == OR_ROW_OK; ++j) {
+        for (int j = 0; j < K; ++j) {
             size_t off_p = ((size_t)b * (size_t)(K + 1) + (size_t)j) * (size_t)V;
             size_t off_q = ((size_t)b * (size_t)K + (size_t)j) * (size_t)V;
             int sp = oracle_row_probs(target, dtype, off_p, V, T, top_k, p, &l, &thr);
             int sq = oracle_row_probs(draft, dtype, off_q, V, T, top_k, q, &l, &thr);
-            if (sp != OR_ROW_OK || sq != OR_ROW_OK) { st = OR_ROW_NONFINITE; break; }
-            if (tok[j] < 0 || tok[j] >= V) { st = OR_ROW_BAD_TOKEN; break; }
-            if (q[tok[j]] == 0.0) { st = OR_ROW_BAD_TOKEN; break; } /* q never proposes d_j */
+            if (sp != OR_ROW_OK || sq != OR_ROW_OK) { st = OR_ROW_NONFINITE; continue; }
+            if (tok[j] < 0 || tok[j] >= V) { badtok = 1; continue; }
+            if (q[tok[j]] == 0.0) { badtok = 1; continue; } /* q never proposes d_j */
             lr += log(p[tok[j]]) - log(q[tok[j]]);
         }
         size_t off_b = ((size_t)b * (size_t)(K + 1) + (size_t)K) * (size_t)V;
         if (oracle_row_probs(target, dtype, off_b, V, T, top_k, p, &l, &thr) != OR_ROW_OK)
             st = OR_ROW_NONFINITE; /* the row the extension token is drawn from */
+        if (st == OR_ROW_OK && badtok) st = OR_ROW_BAD_TOKEN;
         if (st == OR_ROW_OK && !(u[0] >= 0.0f && u[0] < 1.0f && u[1] >= 0.0f && u[1] < 1.0f))
             st = OR_ROW_BAD_UNIFORM;
         int32_t* out = out_tokens + (size_t)b * (K + 1);

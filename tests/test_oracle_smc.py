@@ -162,3 +162,18 @@ def test_q_zero_is_a_bad_token():
     d[0, 0, 3] = -np.inf
     o = O.smc_verify(t, d, [[3]], np.zeros(1), np.full((1, 2), 0.5, np.float32), 1, 1.0, 0.5)
     assert o["row_status"][0] == O.ROW_BAD_TOKEN
+
+
+def test_status_precedence_matches_the_plain_round():
+    """A non-finite row anywhere outranks a bad token, which outranks a bad uniform (as in the
+    plain round's statuses)."""
+    V = 6
+    t = np.zeros((3, 3, V))
+    d = np.zeros((3, 2, V))
+    tok = np.array([[9, 1], [9, 1], [1, 1]])   # position 0 out of range in requests 0 and 1
+    t[0, 2, 4] = np.nan                          # request 0: also a NaN in the extension row
+    u = np.full((3, 2), 0.5, np.float32)
+    u[1, 1] = 1.5                                # request 1: also a bad uniform
+    u[2, 0] = -0.1                               # request 2: a bad uniform alone
+    o = O.smc_verify(t, d, tok, np.zeros(3), u, 3, 1.0, 0.5)
+    assert list(o["row_status"]) == [O.ROW_NONFINITE, O.ROW_BAD_TOKEN, O.ROW_BAD_UNIFORM]
