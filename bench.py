@@ -8,6 +8,7 @@ issued back to back on one stream.  ``--workload`` selects a single configuratio
 them c6 (tree_verify_sample, B=32 N=64(+1) V=128256 bf16 T=0.7: the stochastic tree walk).  c6
 reads only the rows its walk visits (about 31 MB per call, inside L2), so each of its timed calls
 follows an L2 flush outside the call's events and its rates come from the per-call event times.
+c7 is one SMC-SD round through smc_verify (8 groups x 8 particles, K=5, V=128256 bf16, T=0.7).
 
 value     logit rows per second, inputs resident in HBM (whole job, all ranks)
 e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
@@ -49,6 +50,7 @@ KERNEL_OF = {
     "c4": ("topk_stream_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c5": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
     "c6": ("tree_sample_kernel", ["sv_tree_sample.cu", "sv_tree_sample.cuh", "sv_common.cuh"]),
+    "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
 }
 DOMINANT_CFG = "c4"
 
@@ -59,17 +61,20 @@ def workload_batches(names, rank, requests=None):
     from speculative_decoding_verification_spec_gb300 import synth as S
     out = {}
     for n in names:
-        cfg = (S.CONFIGS.get(n) or S.TREE_CONFIGS.get(n) or S.SAMPLE_TREE_CONFIGS[n])
+        cfg = (S.CONFIGS.get(n) or S.TREE_CONFIGS.get(n) or S.SAMPLE_TREE_CONFIGS.get(n)
+               or S.SMC_CONFIGS[n])
         kw = dict(seed=rank_seed(cfg, rank))
         if requests:
-            kw["B"] = requests
+            kw["groups" if n in S.SMC_CONFIGS else "B"] = requests
         cfg = S.scaled(cfg, **kw)
         if n in S.CONFIGS:
             out[n] = S.make_spec_batch(cfg)
         elif n in S.TREE_CONFIGS:
             out[n] = S.make_tree_batch(cfg)
-        else:
+        elif n in S.SAMPLE_TREE_CONFIGS:
             out[n] = S.make_sample_tree_batch(cfg)
+        else:
+            out[n] = S.make_smc_batch(cfg)
     return out
 
 
@@ -79,6 +84,10 @@ def is_sample_tree(b) -> bool:
 
 def is_greedy_tree(b) -> bool:
     return hasattr(b, "logits")
+
+
+def is_smc(b) -> bool:
+    return hasattr(b, "log_weights")
 
 
 def sample_tree_rows_read(b, accepted_len, accept) -> int:
@@ -129,6 +138,10 @@ def describe(names):
             c = S.TREE_CONFIGS[n]
             parts.append(f"{n} tree_verify_greedy B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
                          f"{c.dtype} tree {'/'.join(map(str, c.branching))}")
+        elif n in S.SMC_CONFIGS:
+            c = S.SMC_CONFIGS[n]
+            parts.append(f"{n} smc_verify {c.groups} groups x {c.particles} particles K={c.K} "
+                         f"V={c.V} {c.dtype} T={c.temperature} eta={c.eta}")
         else:
             c = S.SAMPLE_TREE_CONFIGS[n]
             parts.append(f"{n} tree_verify_sample B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
@@ -143,6 +156,8 @@ def kernels_per_call(batch):
         return 1                              # the clustered walk
     if is_greedy_tree(batch):
         return 2                              # argmax stream + tree finish
+    if is_smc(batch):
+        return 4                              # stream + row plan + extension draw + group step
     return 3                                  # stream + finish + dense / stream + row plan + residual
 
 
@@ -256,6 +271,15 @@ def cpu_baseline(names, budget_s=15.0):
             elif is_greedy_tree(b):
                 O.tree_verify_greedy(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1])
                 rows_done += b.logits.shape[1]
+            elif is_smc(b):  # one group of particles per sample
+                Np = b.cfg.particles
+                if i >= b.cfg.groups:
+                    break
+                sl = slice(i * Np, (i + 1) * Np)
+                O.smc_verify(b.target[sl], b.draft[sl], b.draft_tokens[sl],
+                             b.log_weights[sl].astype(np.float64), b.uniforms[sl], 1,
+                             b.cfg.temperature, b.cfg.eta)
+                rows_done += Np * (2 * b.cfg.K + 1)
             else:
                 O.spec_verify(b.target[i:i + 1], b.draft[i:i + 1], b.draft_tokens[i:i + 1],
                               b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k)
@@ -263,7 +287,8 @@ def cpu_baseline(names, budget_s=15.0):
             t_used += time.perf_counter() - t0
             i += 1
         per_row_s[n] = t_used / rows_done
-        sample.append(f"{n}: {i} requests ({rows_done} rows)")
+        sample.append(f"{n}: {i} {'groups of particles' if is_smc(b) else 'requests'} "
+                      f"({rows_done} rows)")
     rows = {n: batches[n].rows for n in names}
     step_s = sum(per_row_s[n] * rows[n] for n in names)
     return {"value": sum(rows.values()) / step_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
@@ -297,6 +322,9 @@ def run_ours(args, rank, world, local_rank):
                         qrow=b.qrow, uniforms=b.uniforms)
         elif is_greedy_tree(b):
             arrs = dict(logits=b.logits, parents=b.parents, tokens=b.tokens)
+        elif is_smc(b):
+            arrs = dict(target=b.target, draft=b.draft, tokens=b.draft_tokens,
+                        log_weights=b.log_weights, uniforms=b.uniforms)
         else:
             arrs = dict(target=b.target, draft=b.draft, tokens=b.draft_tokens, uniforms=b.uniforms)
         host[n] = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16
@@ -311,6 +339,10 @@ def run_ours(args, rank, world, local_rank):
             return sv.tree_verify_sample(ins["target"], ins["draft"], ins["parents"], ins["tokens"],
                                          ins["qrow"], ins["uniforms"], b.cfg.temperature, out=out,
                                          aux=True, stream=stream)
+        if is_smc(b):
+            return sv.smc_verify(ins["target"], ins["draft"], ins["tokens"], ins["log_weights"],
+                                 ins["uniforms"], b.cfg.groups, b.cfg.temperature, b.cfg.eta,
+                                 out=out, workspace=wss[n], stream=stream)
         if is_greedy_tree(b):
             return sv.tree_verify_greedy(ins["logits"], ins["parents"], ins["tokens"], out=out,
                                          workspace=wss[n], stream=stream)
@@ -518,6 +550,14 @@ def run_reference(args, rank, world):
                                      b.tokens[j:j + 1], b.qrow[j:j + 1], b.uniforms[j:j + 1],
                                      b.cfg.temperature)
                 rows += b.target.shape[1]
+            elif is_smc(b):
+                Np = b.cfg.particles
+                j = (i // len(names)) % b.cfg.groups
+                sl = slice(j * Np, (j + 1) * Np)
+                O.smc_verify(b.target[sl], b.draft[sl], b.draft_tokens[sl],
+                             b.log_weights[sl].astype(np.float64), b.uniforms[sl], 1,
+                             b.cfg.temperature, b.cfg.eta)
+                rows += Np * (2 * b.cfg.K + 1)
             elif is_greedy_tree(b):
                 j = (i // len(names)) % b.logits.shape[0]
                 O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
@@ -556,7 +596,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6"],
+    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7"],
                     default="suite")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

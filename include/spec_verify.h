@@ -8,6 +8,7 @@
  *   spec_verify_topk   the same with a top-k processor applied identically to target and draft
  *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
  *   tree_verify_sample stochastic verification of a candidate tree (residual update over children)
+ *   smc_verify         the verify side of one SMC-SD round: block weights, extension, resampling
  *
  * Sources (page title + section):
  *   "M7.1 - Speculative Decoding: Draft, Verify, Accept, Reject": 0x03 (accept probability and
@@ -20,6 +21,8 @@
  *     predictor row: a depth-1 node is scored by the frontier row, any other node by its
  *     parent's row), 0x08B-0x09A (several candidates at one node: test them in turn against the
  *     running residual, never against the original target row).
+ *   Module 16 lesson, "SMC Speculative Decoding: Resample, Don't Reject": "The Math: Reweight, Don't
+ *     Reject" (block weight, effective sample size, Algorithm 1), "Two Exact Anchors".
  *   "Exact speculative and assisted decoding for TinyRustLM": "Normative stochastic pseudocode"
  *     (separate accept / correction / extra-token random streams, abort without emitting on
  *     non-finite rows or a non-positive residual), "Minimum target API" (row i predicts proposal
@@ -199,6 +202,42 @@ spec_status tree_verify_sample(const void* target_logits, const void* draft_logi
                                float* aux_accept, void* stream);
 
 /*
+ * The verify side of one SMC-SD round (Module 16 lesson, "SMC Speculative Decoding: Resample, Don't
+ * Reject", Algorithm 1 steps 2-5) for `groups` groups of `particles` particles; B = groups *
+ * particles requests, particle n of group g at request g * particles + n.  Not exact: the method
+ * trades exactness for a fixed K+1 tokens per particle and round.
+ *
+ *   target_logits [B, K+1, V], draft_logits [B, K, V] (NULL when K == 0), draft_tokens [B, K]:
+ *                              as spec_verify with gamma = K
+ *   log_weights_in [B]         fp32 natural-log weight of each particle before the round
+ *   uniforms      [B, 2]       fp32 in [0, 1): slot 0 draws the extension token, slot 1 the
+ *                              particle's ancestor
+ *   temperature                as spec_verify (no top-k)
+ *   ess_threshold              eta: a group resamples when its ESS < eta (N/2 is the usual choice)
+ *
+ * Per particle, with p and q processed as in spec_verify and every draft position kept:
+ *   block_log_ratio[b] = sum_j log p_j(d_j) - log q_j(d_j)                     (nullable)
+ *   out_tokens[b, 0..K-1] = d_1 .. d_K; out_tokens[b, K] = the extension token, an inverse-CDF
+ *   draw from p_K with slot 0; accepted_len[b] = K; row_status[b] (nullable) as spec_verify.
+ * Per group, with w = exp(log_weights_in + block_log_ratio):
+ *   ess[g] = (sum w)^2 / sum w^2                                                (nullable)
+ *   ESS < eta: resampled[g] = 1; ancestors[b] = the inverse-CDF draw over the group's normalised
+ *              weights (particle order) with slot 1 of particle b; log_weights_out = log(1/particles)
+ *   otherwise: resampled[g] = 0; ancestors[b] = n; log_weights_out[b] = log w
+ *   A group holding a particle whose status is not OK: ess NaN, resampled -1, ancestors -1 and
+ *   log_weights_out NaN for all its particles (its OK particles keep their tokens and block ratio).
+ * The caller copies the resampled particles (tokens, caches) from their ancestors.  Workspace:
+ * spec_workspace_bytes(B, K, V, 0, 0).  particles <= 4096.
+ */
+spec_status smc_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                       const int32_t* draft_tokens, const float* log_weights_in,
+                       const float* uniforms, int groups, int particles, int K, int V,
+                       float temperature, float ess_threshold, int32_t* accepted_len,
+                       int32_t* out_tokens, float* log_weights_out, float* block_log_ratio,
+                       float* ess, int32_t* resampled, int32_t* ancestors, int32_t* row_status,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * spec_verify for callers that cannot allocate device memory.  The paper has no counterpart: this
  * call only changes where spec_verify's scratch lives.
  *
@@ -240,6 +279,7 @@ spec_status spec_verify_noalloc(const void* target_logits, const void* draft_log
  *   spec_verify_topk   the streaming top-k kernel
  *   tree_verify_greedy the argmax kernel
  *   tree_verify_sample its only kernel
+ *   smc_verify         the row-statistics kernel, as spec_verify
  * spec_set_kernel_events(NULL, NULL) turns it off.  The setting is process-wide and not
  * synchronised: set it from the thread that issues the calls.
  */

@@ -19,7 +19,7 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 
 # every symbol the header declares
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
-           "tree_verify_sample", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
+           "tree_verify_sample", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -53,6 +53,8 @@ def load(path: str | None = None):
     lib.tree_verify_greedy.restype = I
     lib.tree_verify_sample.argtypes = [P, P, I, P, P, P, P, I, I, I, I, F, I, P, P, P, P, P, P]
     lib.tree_verify_sample.restype = I
+    lib.smc_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, F, F, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.smc_verify.restype = I
     lib.spec_verify_noalloc.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P]
     lib.spec_verify_noalloc.restype = I
     lib.spec_set_kernel_events.argtypes = [P, P]
@@ -271,5 +273,45 @@ def tree_verify_sample(target, draft, parents, tokens, qrow, uniforms, temperatu
                                 _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")),
                                 _ptr(out.get("row_status")), _ptr(out.get("accept")),
                                 _stream(stream))
+    _check(rc)
+    return out
+
+
+def smc_verify(target, draft, draft_tokens, log_weights, uniforms, groups: int, temperature: float,
+               ess_threshold: float, *, out=None, workspace: Workspace | None = None, stream=None):
+    """The verify side of one SMC-SD round on the GPU.
+
+    target [B, K+1, V], draft [B, K, V], draft_tokens [B, K] int32, log_weights [B] float32,
+    uniforms [B, 2] float32, B = groups * particles.  Returns out_tokens, accepted_len, row_status,
+    log_weights (after the round), block_log_ratio, ess, resampled and ancestors.
+    """
+    lib = load()
+    _need_cuda(target, draft, draft_tokens, log_weights, uniforms)
+    B, k1, V = target.shape
+    K = k1 - 1
+    if groups < 1 or B % groups:
+        raise ValueError("the batch must split into equal groups of particles")
+    Np = B // groups
+    dev = target.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+            log_weights=torch.empty(B, dtype=torch.float32, device=dev),
+            block_log_ratio=torch.empty(B, dtype=torch.float32, device=dev),
+            ess=torch.empty(groups, dtype=torch.float32, device=dev),
+            resampled=torch.empty(groups, dtype=torch.int32, device=dev),
+            ancestors=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+    nbytes = workspace_bytes(B, K, V)
+    ws = _workspace(workspace, dev).get(nbytes)
+    rc = lib.smc_verify(_ptr(target), _ptr(draft) if K > 0 else None, _dtype_code(target),
+                        _ptr(draft_tokens), _ptr(log_weights), _ptr(uniforms), groups, Np, K, V,
+                        float(temperature), float(ess_threshold), _ptr(out["accepted_len"]),
+                        _ptr(out["out_tokens"]), _ptr(out["log_weights"]),
+                        _ptr(out.get("block_log_ratio")), _ptr(out.get("ess")),
+                        _ptr(out.get("resampled")), _ptr(out.get("ancestors")),
+                        _ptr(out.get("row_status")), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc)
     return out

@@ -7,6 +7,7 @@
 
 #include "../../include/spec_verify.h"
 #include "sv_common.cuh"
+#include "sv_smc.cuh"
 #include "sv_tree_sample.cuh"
 
 namespace sv {
@@ -164,12 +165,24 @@ static int pick_vec(int dtype, int V, const void* a, const void* b)
 
 // --------------------------------------------------------------------------- the calls
 
+// the SMC-SD group step of smc_verify (null for the speculative-sampling calls)
+struct SmcArgs {
+    const float* logw_in;
+    float* logw_out;
+    float* log_ratio;
+    int groups, particles;
+    float eta;
+    float* ess;
+    int32_t* resampled;
+    int32_t* ancestors;
+};
+
 static spec_status spec_common(const void* target, const void* draft, spec_dtype dtype,
                                const int32_t* tokens, const float* uniforms, int B, int gamma,
                                int V, float temperature, int top_k, int32_t* accepted_len,
                                int32_t* out_tokens, int32_t* row_status, float* aux_lse_p,
                                float* aux_lse_q, float* aux_accept, void* workspace,
-                               size_t workspace_bytes, void* stream)
+                               size_t workspace_bytes, void* stream, const SmcArgs* smc = nullptr)
 {
     if (B < 0 || gamma < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
@@ -239,6 +252,12 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.aux_lse_p = aux_lse_p;
     P.aux_lse_q = aux_lse_q;
     P.aux_accept = aux_accept;
+    if (smc) {
+        P.smc = 1;
+        P.smc_logw_in = smc->logw_in;
+        P.smc_log_ratio = smc->log_ratio;
+        P.smc_logw = smc->logw_out;
+    }
     P.row_ctr = reinterpret_cast<unsigned*>(ws + L.o_row_ctr);
     P.req_ctr = reinterpret_cast<unsigned*>(ws + L.o_req_ctr);
     P.res_ctr = reinterpret_cast<unsigned*>(ws + L.o_res_ctr);
@@ -271,6 +290,19 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
         err = launch_softmax_path(P, sms, st);
     } else {
         err = launch_topk_path(P, sms, st);
+    }
+    if (err == cudaSuccess && smc) {
+        SmcGroupParams S;
+        S.plan = P.plan;
+        S.uniforms = uniforms;
+        S.logw = smc->logw_out;
+        S.G = smc->groups;
+        S.Np = smc->particles;
+        S.eta = smc->eta;
+        S.ess = smc->ess;
+        S.resampled = smc->resampled;
+        S.ancestors = smc->ancestors;
+        err = launch_smc_groups(S, st);
     }
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -324,6 +356,38 @@ spec_status spec_verify_topk(const void* target_logits, const void* draft_logits
     return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
                        temperature, top_k, accepted_len, out_tokens, row_status, aux_lse_p,
                        aux_lse_q, aux_accept, workspace, workspace_bytes, stream);
+}
+
+spec_status smc_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                       const int32_t* draft_tokens, const float* log_weights_in,
+                       const float* uniforms, int groups, int particles, int K, int V,
+                       float temperature, float ess_threshold, int32_t* accepted_len,
+                       int32_t* out_tokens, float* log_weights_out, float* block_log_ratio,
+                       float* ess, int32_t* resampled, int32_t* ancestors, int32_t* row_status,
+                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (groups < 0 || particles < 1 || particles > SMC_MAX_PARTICLES) return SPEC_ERR_INVALID_ARG;
+    if ((long long)groups * particles > 0x7fffffffLL) return SPEC_ERR_INVALID_ARG;
+    if (!std::isfinite(ess_threshold)) return SPEC_ERR_INVALID_ARG;
+    if (groups > 0 && (!log_weights_in || !aligned(log_weights_in, 4) || !log_weights_out ||
+                       !aligned(log_weights_out, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if ((block_log_ratio && !aligned(block_log_ratio, 4)) || (ess && !aligned(ess, 4)) ||
+        (resampled && !aligned(resampled, 4)) || (ancestors && !aligned(ancestors, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    SmcArgs a;
+    a.logw_in = log_weights_in;
+    a.logw_out = log_weights_out;
+    a.log_ratio = block_log_ratio;
+    a.groups = groups;
+    a.particles = particles;
+    a.eta = ess_threshold;
+    a.ess = ess;
+    a.resampled = resampled;
+    a.ancestors = ancestors;
+    return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                       groups * particles, K, V, temperature, 0, accepted_len, out_tokens,
+                       row_status, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream, &a);
 }
 
 spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32_t* parents,

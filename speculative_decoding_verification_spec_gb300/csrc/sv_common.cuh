@@ -138,6 +138,12 @@ struct SpecParams {
     // counters the first kernel clears itself (streaming paths; otherwise a memset does): words
     unsigned* ctr_clear;
     int ctr_words;
+    // SMC-SD round (smc_verify): no acceptance test, every draft position is kept; uniforms are
+    // [B, 2]: slot 0 draws the extension token from row gamma, slot 1 is the particle's ancestor draw
+    int smc;
+    const float* smc_logw_in;  // [B] log weight before the round
+    float* smc_log_ratio;      // [B] or null: sum over the draft positions of log p - log q
+    float* smc_logw;           // [B] logw_in + log ratio (the group step may reset it)
 };
 
 struct TreeParams {

@@ -173,7 +173,8 @@ __device__ __forceinline__ Plan plan_from_lanes(const SpecParams& P, int b, cons
     const int g = P.gamma, R = P.R, lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
     const int x = (lane < g) ? __ldg(P.tokens + (size_t)b * g + lane) : 0;
-    const float uu = (lane < g + 2) ? __ldg(P.uniforms + (size_t)b * (g + 2) + lane) : 0.f;
+    const int nu = P.smc ? 2 : g + 2;  // uniforms per request
+    const float uu = (lane < nu) ? __ldg(P.uniforms + (size_t)b * nu + lane) : 0.f;
     const bool row = lane < R;
     const int nonfinite = __any_sync(FULL, row && rs.status != ROW_OK);
     const int timeout = __any_sync(FULL, row && rs.status == ROW_TIMEOUT);
@@ -193,6 +194,7 @@ __device__ __forceinline__ Plan plan_from_lanes(const SpecParams& P, int b, cons
     lq.lo = __shfl_sync(FULL, rs.lx_lo, (lane + g + 1) & 31);
     int badtok = 0;
     bool reject = false;
+    DFloat lr = df_make(0.f, 0.f);  // SMC: log2 p(x) - log2 q(x) of this position
     if (lane < g) {
         float a = __int_as_float(0x7fc00000);
         if (x < 0 || x >= P.V) {
@@ -202,14 +204,25 @@ __device__ __forceinline__ Plan plan_from_lanes(const SpecParams& P, int b, cons
                 badtok = 1;  // q(x) = 0: the draft cannot have proposed x
             } else {
                 a = accept_ratio_df(lp, lq);
-                reject = !(uu < a);
+                reject = !P.smc && !(uu < a);
+                lr = df_add(lp, df_make(-lq.hi, -lq.lo));
             }
         }
         if (P.aux_accept) P.aux_accept[(size_t)b * g + lane] = a;
     }
     badtok = __any_sync(FULL, badtok);
-    const int badu = __any_sync(FULL, lane < g + 2 && !(uu >= 0.0f && uu < 1.0f));
+    const int badu = __any_sync(FULL, lane < nu && !(uu >= 0.0f && uu < 1.0f));
     const unsigned rej = __ballot_sync(FULL, reject);
+    if (P.smc) {  // the block log-ratio, natural log (M16 "The Math: Reweight, Don't Reject")
+        const DFloat l2 = warp_sum_df(lr);
+        const DFloat ln = df_mul(l2, LN2_HI, LN2_LO);
+        const bool okr = !nonfinite && !badtok && !badu;
+        if (lane == 0) {
+            const float v = okr ? ln.hi + ln.lo : __int_as_float(0x7fc00000);
+            if (P.smc_log_ratio) P.smc_log_ratio[b] = v;
+            P.smc_logw[b] = okr ? __ldg(P.smc_logw_in + b) + v : __int_as_float(0x7fc00000);
+        }
+    }
 
     Plan pl;
     pl.status = timeout ? ROW_TIMEOUT : nonfinite ? ROW_NONFINITE : badtok ? ROW_BAD_TOKEN : badu ? ROW_BAD_UNIFORM : ROW_OK;
@@ -224,7 +237,7 @@ __device__ __forceinline__ Plan plan_from_lanes(const SpecParams& P, int b, cons
     pl.MCq = (pl.rq >= 0) ? sq.MC : 0.f;
     pl.invSq = (pl.rq >= 0) ? sq.invS : 0.f;
     pl.thrq = (pl.rq >= 0) ? sq.thr : 0.f;
-    pl.u = (double)__shfl_sync(FULL, uu, (pl.A < g) ? g : g + 1);
+    pl.u = (double)__shfl_sync(FULL, uu, P.smc ? 0 : (pl.A < g) ? g : g + 1);
     return pl;
 }
 
@@ -273,7 +286,9 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
     // acceptance ratios at every position
     int badtok = 0;
     int rej_first = g;
-    const float* u = P.uniforms + (size_t)b * (g + 2);
+    const int nu = P.smc ? 2 : g + 2;  // uniforms per request
+    const float* u = P.uniforms + (size_t)b * nu;
+    double lrsum = 0.0;  // SMC: sum of log2 p(x) - log2 q(x) over this lane's positions
     for (int i = lane; i < g; i += 32) {
         const int x = P.tokens[(size_t)b * g + i];
         double a = __longlong_as_double(0x7ff8000000000000ll);
@@ -303,18 +318,29 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
                 badtok = 1;  // q(x) = 0: the draft cannot have proposed x
             } else {
                 a = accept_ratio(lp, lq);
-                if (!((double)u[i] < a) && i < rej_first) rej_first = i;
+                if (!P.smc && !((double)u[i] < a) && i < rej_first) rej_first = i;
+                lrsum += lp - lq;
             }
         }
         if (P.aux_accept) P.aux_accept[(size_t)b * g + i] = (float)a;
     }
     badtok = __any_sync(FULL, badtok);
     int badu = 0;
-    for (int i = lane; i < g + 2; i += 32) {
+    for (int i = lane; i < nu; i += 32) {
         const float v = u[i];
         if (!(v >= 0.0f && v < 1.0f)) badu = 1;
     }
     badu = __any_sync(FULL, badu);
+    if (P.smc) {  // the block log-ratio, natural log (M16 "The Math: Reweight, Don't Reject")
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lrsum += __shfl_xor_sync(FULL, lrsum, o);
+        const bool okr = !nonfinite && !badtok && !badu;
+        if (lane == 0) {
+            const float v = okr ? (float)(lrsum * LN2) : __int_as_float(0x7fc00000);
+            if (P.smc_log_ratio) P.smc_log_ratio[b] = v;
+            P.smc_logw[b] = okr ? P.smc_logw_in[b] + v : __int_as_float(0x7fc00000);
+        }
+    }
 
     Plan pl;
     pl.status = timeout ? ROW_TIMEOUT : nonfinite ? ROW_NONFINITE : badtok ? ROW_BAD_TOKEN : badu ? ROW_BAD_UNIFORM : ROW_OK;
@@ -335,7 +361,7 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
         pl.invSq = 0.f;
         pl.thrq = 0.f;
     }
-    pl.u = (double)u[(pl.A < g) ? g : g + 1];
+    pl.u = (double)u[P.smc ? 0 : (pl.A < g) ? g : g + 1];
     return pl;
 }
 

@@ -23,6 +23,10 @@ Workload recipes (five named configurations):
                                           like the target rows (row 0 frontier, row i+1 at node i);
                                           the children of a node are i.i.d. draws from the draft
                                           row at their parent (qrow = parent + 1)
+  c7  G=8 x N=8 particles, K=5, V=128256 bf16, T=0.7, eta = N/2: one SMC-SD round; logits as
+                                          c3 (target, draft = 0.8*target + N(0,1.5^2)), draft
+                                          tokens from q, incoming log weights N(0, 0.5^2),
+                                          uniforms [B, 2] (extension, ancestor)
 
 Streams: SeedSequence(seed).spawn(3) gives (logits, draft sampling, uniforms); each is spawned again
 per request, so a request's inputs do not depend on B or on how many threads generate them.
@@ -92,6 +96,29 @@ class SampleTreeConfig:
 
 
 SAMPLE_TREE_CONFIGS = {"c6": SampleTreeConfig("c6", 32, 128256)}
+
+
+@dataclass(frozen=True)
+class SmcConfig:
+    name: str
+    groups: int
+    particles: int
+    K: int
+    V: int
+    dtype: str = "bf16"
+    temperature: float = 0.7
+    eta: float = 4.0
+    draft_scale: float = 0.8
+    draft_noise: float = 1.5
+    logw_sd: float = 0.5
+    seed: int = 1007
+
+    @property
+    def B(self) -> int:
+        return self.groups * self.particles
+
+
+SMC_CONFIGS = {"c7": SmcConfig("c7", 8, 8, 5, 128256)}
 
 
 def scaled(cfg, **kw):
@@ -395,3 +422,62 @@ def make_sample_tree_batch(cfg: SampleTreeConfig, *, parents=None,
             one(b)
     return SampleTreeBatch(cfg, target, draft, np.broadcast_to(par, (B, N)).copy(), tokens,
                            np.broadcast_to(qrow, (B, N)).copy(), uniforms)
+
+
+# ------------------------------------------------------------------ SMC-SD rounds
+
+@dataclass
+class SmcBatch:
+    cfg: SmcConfig
+    target: np.ndarray    # [B, K+1, V]
+    draft: np.ndarray     # [B, K, V]
+    draft_tokens: np.ndarray  # [B, K] int32
+    log_weights: np.ndarray   # [B] float32
+    uniforms: np.ndarray  # [B, 2] float32
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def rows(self) -> int:
+        return self.cfg.B * (2 * self.cfg.K + 1)
+
+    @property
+    def logit_bytes(self) -> int:
+        return self.target.nbytes + self.draft.nbytes
+
+
+def make_smc_batch(cfg: SmcConfig, *, threads: int | None = None) -> SmcBatch:
+    """Particles drawn like c3's requests: target rows N(0,3^2) + Zipf bias, draft rows
+    0.8 * target + noise, draft tokens Gumbel-max draws from q (the drafter's sampler, outside the
+    verify step); incoming log weights N(0, logw_sd^2); uniforms for the extension and the ancestor."""
+    B, K, V = cfg.B, cfg.K, cfg.V
+    ss_logit, ss_draw, ss_unif = np.random.SeedSequence(cfg.seed).spawn(3)
+    req_logit, req_draw, req_unif = ss_logit.spawn(B), ss_draw.spawn(B), ss_unif.spawn(B)
+    bias = _zipf_bias(V, cfg.seed)
+    sdt = np.uint16 if cfg.dtype == "bf16" else np.float32
+    target = np.empty((B, K + 1, V), dtype=sdt)
+    draft = np.empty((B, K, V), dtype=sdt)
+    tokens = np.empty((B, K), dtype=np.int32)
+    uniforms = np.empty((B, 2), dtype=np.float32)
+    logw = np.empty(B, dtype=np.float32)
+
+    def one(b):
+        rng = np.random.Generator(np.random.PCG64(req_logit[b]))
+        t32 = _target_rows(rng, "zipf", K + 1, V, bias)
+        d32 = (cfg.draft_scale * t32[:K].astype(np.float64)
+               + rng.standard_normal((K, V)) * cfg.draft_noise).astype(np.float32)
+        target[b] = _store(t32, cfg.dtype)
+        draft[b] = _store(d32, cfg.dtype)
+        r2 = np.random.Generator(np.random.PCG64(req_draw[b]))
+        if K:
+            tokens[b] = gumbel_max_tokens(r2, stored_to_f64(draft[b]) / cfg.temperature)
+        logw[b] = np.float32(r2.standard_normal() * cfg.logw_sd)
+        uniforms[b] = uniforms_from(np.random.Generator(np.random.PCG64(req_unif[b])), 2)
+
+    n = threads or _nthreads()
+    if n > 1 and B > 1:
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(one, range(B)))
+    else:
+        for b in range(B):
+            one(b)
+    return SmcBatch(cfg, target, draft, tokens, logw, uniforms)

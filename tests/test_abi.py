@@ -107,6 +107,18 @@ def test_host_validation_without_gpu(lib):
                 dict(acc=None), dict(out=None), dict(target=P(0x10001)), dict(N=4097),
                 dict(V=262145), dict(dtype=0, V=131073), dict(u=P(0x10002))):
         assert ts_call(**bad) == INVALID, bad
+    # smc_verify: groups, particles, threshold and pointers, before any CUDA call
+    def smc_call(G=2, Np=4, K=3, V=1000, T=1.0, eta=2.0, lw=fake, lwo=fake, u=fake, acc=fake,
+                 out=fake, wsp=ws):
+        return lib.smc_verify(fake, fake, 1, fake, lw, u, G, Np, K, V, F(T), F(eta), acc, out, lwo,
+                              None, None, None, None, None, wsp, 1 << 30, None)
+
+    assert smc_call(G=0) == 0
+    for bad in (dict(G=-1), dict(Np=0), dict(Np=4097), dict(eta=float("nan")), dict(lw=None),
+                dict(lwo=None), dict(T=0.0), dict(V=0), dict(K=-1), dict(u=None), dict(acc=None),
+                dict(out=None), dict(lw=P(0x10002))):
+        assert smc_call(**bad) == INVALID, bad
+    assert smc_call(wsp=None) == WORKSPACE
     assert lib.spec_status_string(0) == b"ok"
     # the no-allocation entry point refuses oversized or invalid sizes before any CUDA call
     TOO_LARGE = 4
