@@ -8,7 +8,8 @@ issued back to back on one stream.  ``--workload`` selects a single configuratio
 them c6 (tree_verify_sample, B=32 N=64(+1) V=128256 bf16 T=0.7: the stochastic tree walk).  c6
 reads only the rows its walk visits (about 31 MB per call, inside L2), so each of its timed calls
 follows an L2 flush outside the call's events and its rates come from the per-call event times.
-c7 is one SMC-SD round through smc_verify (8 groups x 8 particles, K=5, V=128256 bf16, T=0.7).
+c7 is one SMC-SD round through smc_verify (8 groups x 8 particles, K=5, V=128256 bf16, T=0.7);
+c8 linear greedy verify through spec_verify_greedy (B=64 gamma=5 V=128256 bf16).
 
 value     logit rows per second, inputs resident in HBM (whole job, all ranks)
 e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
@@ -51,6 +52,7 @@ KERNEL_OF = {
     "c5": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
     "c6": ("tree_sample_kernel", ["sv_tree_sample.cu", "sv_tree_sample.cuh", "sv_common.cuh"]),
     "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c8": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
 }
 DOMINANT_CFG = "c4"
 
@@ -134,6 +136,9 @@ def describe(names):
             op = "spec_verify_topk" if c.top_k else "spec_verify"
             parts.append(f"{n} {op} B={c.B} gamma={c.gamma} V={c.V} {c.dtype} T={c.temperature}"
                          + (f" top_k={c.top_k}" if c.top_k else ""))
+        elif n in S.TREE_CONFIGS and S.TREE_CONFIGS[n].chain:
+            c = S.TREE_CONFIGS[n]
+            parts.append(f"{n} spec_verify_greedy B={c.B} gamma={c.max_nodes} V={c.V} {c.dtype}")
         elif n in S.TREE_CONFIGS:
             c = S.TREE_CONFIGS[n]
             parts.append(f"{n} tree_verify_greedy B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
@@ -343,6 +348,9 @@ def run_ours(args, rank, world, local_rank):
             return sv.smc_verify(ins["target"], ins["draft"], ins["tokens"], ins["log_weights"],
                                  ins["uniforms"], b.cfg.groups, b.cfg.temperature, b.cfg.eta,
                                  out=out, workspace=wss[n], stream=stream)
+        if is_greedy_tree(b) and b.cfg.chain:
+            return sv.spec_verify_greedy(ins["logits"], ins["tokens"], out=out, workspace=wss[n],
+                                         stream=stream)
         if is_greedy_tree(b):
             return sv.tree_verify_greedy(ins["logits"], ins["parents"], ins["tokens"], out=out,
                                          workspace=wss[n], stream=stream)
@@ -596,7 +604,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7"],
+    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7", "c8"],
                     default="suite")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

@@ -7,6 +7,7 @@
  *   spec_verify        exact speculative sampling with temperature
  *   spec_verify_topk   the same with a top-k processor applied identically to target and draft
  *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
+ *   spec_verify_greedy linear greedy verification of a draft (the greedy tree on a chain)
  *   tree_verify_sample stochastic verification of a candidate tree (residual update over children)
  *   smc_verify         the verify side of one SMC-SD round: block weights, extension, resampling
  *
@@ -160,6 +161,24 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype,
                                void* stream);
 
 /*
+ * Linear greedy verify (temperature -> 0; M7.1 "greedy = the p/q rule with one-hot p"; Module 16
+ * "Verify the Tree": a chain is the degenerate tree): tree_verify_greedy on the chain
+ * node i -> parent i - 1, with the target rows as the tree's rows.
+ *
+ *   target_logits [B, gamma+1, V]  row i scores draft token i; row gamma the position after the draft
+ *   draft_tokens  [B, gamma]       int32
+ *
+ *   accepted_len[b] = A, the length of the longest prefix with draft_tokens[b, i] = argmax(row i)
+ *   out_tokens[b, 0..A-1] = that prefix; out_tokens[b, A] = argmax(row A) (the correction, or the
+ *   bonus when A = gamma); rest -1.  Ties go to the lowest index.  row_status as tree_verify_greedy.
+ * Workspace: spec_workspace_bytes(B, 0, V, 0, max(gamma, 1)).
+ */
+spec_status spec_verify_greedy(const void* target_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, int B, int gamma, int V,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Stochastic tree verify (M7.7 0x09A residual update over a node's children; 0x07E row
  * convention; Module 16 accept rule and inverse-CDF draw).  Exact: the emitted tokens, continued
  * by target draws, follow the target distribution.
@@ -278,6 +297,7 @@ spec_status spec_verify_noalloc(const void* target_logits, const void* draft_log
  *   spec_verify        the row-statistics (one-pass normaliser) kernel
  *   spec_verify_topk   the streaming top-k kernel
  *   tree_verify_greedy the argmax kernel
+ *   spec_verify_greedy the argmax kernel, as tree_verify_greedy
  *   tree_verify_sample its only kernel
  *   smc_verify         the row-statistics kernel, as spec_verify
  * spec_set_kernel_events(NULL, NULL) turns it off.  The setting is process-wide and not

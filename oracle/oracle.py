@@ -176,6 +176,15 @@ def tree_verify_greedy(logits, parents, tokens, max_out: int | None = None):
     return out
 
 
+def spec_verify_greedy(target, draft_tokens):
+    """Linear greedy verify: the greedy tree verify on the chain node i -> parent i - 1."""
+    t = np.asarray(target)
+    B, g1, _ = t.shape
+    gamma = g1 - 1
+    parents = np.tile(np.arange(-1, gamma - 1, dtype=np.int32), (B, 1))
+    return tree_verify_greedy(t, parents, draft_tokens, max_out=gamma + 1)
+
+
 def tree_verify_sample(target, draft, parents, tokens, qrow, uniforms, temperature: float,
                        max_out: int | None = None, lib=None):
     """Stochastic tree verify by the residual update over children (fp64).

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     set_kernel_events,
     smc_verify,
     spec_verify,
+    spec_verify_greedy,
     spec_verify_noalloc,
     spec_verify_topk,
     tree_verify_greedy,

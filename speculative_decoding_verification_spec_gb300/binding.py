@@ -19,6 +19,7 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 
 # every symbol the header declares
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
+           "spec_verify_greedy",
            "tree_verify_sample", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
@@ -51,6 +52,8 @@ def load(path: str | None = None):
     lib.spec_verify_topk.restype = I
     lib.tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
     lib.tree_verify_greedy.restype = I
+    lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, Z, P]
+    lib.spec_verify_greedy.restype = I
     lib.tree_verify_sample.argtypes = [P, P, I, P, P, P, P, I, I, I, I, F, I, P, P, P, P, P, P]
     lib.tree_verify_sample.restype = I
     lib.smc_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, F, F, P, P, P, P, P, P, P, P, P, Z, P]
@@ -313,5 +316,28 @@ def smc_verify(target, draft, draft_tokens, log_weights, uniforms, groups: int, 
                         _ptr(out.get("block_log_ratio")), _ptr(out.get("ess")),
                         _ptr(out.get("resampled")), _ptr(out.get("ancestors")),
                         _ptr(out.get("row_status")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc)
+    return out
+
+
+def spec_verify_greedy(target, draft_tokens, *, out=None, workspace: Workspace | None = None,
+                       stream=None):
+    """Linear greedy verify on the GPU.  target [B, gamma+1, V]; draft_tokens [B, gamma] int32."""
+    lib = load()
+    _need_cuda(target, draft_tokens)
+    B, g1, V = target.shape
+    gamma = g1 - 1
+    dev = target.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, gamma + 1, dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+    nbytes = workspace_bytes(B, 0, V, 0, max(gamma, 1))
+    ws = _workspace(workspace, dev).get(nbytes)
+    rc = lib.spec_verify_greedy(_ptr(target), _dtype_code(target), _ptr(draft_tokens), B, gamma, V,
+                                _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
+                                _ptr(out.get("row_status")), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc)
     return out

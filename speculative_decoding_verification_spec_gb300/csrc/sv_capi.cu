@@ -390,11 +390,12 @@ spec_status smc_verify(const void* target_logits, const void* draft_logits, spec
                        row_status, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream, &a);
 }
 
-spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32_t* parents,
+// greedy tree verify; chain: parents is ignored and node i's parent is i - 1 (spec_verify_greedy)
+static spec_status tree_common(const void* logits, spec_dtype dtype, const int32_t* parents,
                                const int32_t* tokens, int B, int N, int V, int max_out,
                                int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
                                int32_t* row_status, void* workspace, size_t workspace_bytes,
-                               void* stream)
+                               void* stream, bool chain)
 {
     if (B < 0 || N < 0 || V < 1 || max_out < 1) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
@@ -403,7 +404,8 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     if ((long long)B * R > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
     const size_t es = dtype == SPEC_BF16 ? 2 : 4;
     if (!logits || !aligned(logits, es)) return SPEC_ERR_INVALID_ARG;
-    if (N > 0 && (!parents || !tokens || !aligned(parents, 4) || !aligned(tokens, 4)))
+    if (chain) parents = nullptr;
+    if (N > 0 && ((!chain && (!parents || !aligned(parents, 4))) || !tokens || !aligned(tokens, 4)))
         return SPEC_ERR_INVALID_ARG;
     if (!accepted_len || !out_tokens || !aligned(accepted_len, 4) || !aligned(out_tokens, 4))
         return SPEC_ERR_INVALID_ARG;
@@ -444,6 +446,27 @@ spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32
     if (vec == 1 && cudaMemsetAsync(ws, 0, L.ctr_bytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
     const cudaError_t err = launch_tree_path(P, sm_count(), st);
     return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status tree_verify_greedy(const void* logits, spec_dtype dtype, const int32_t* parents,
+                               const int32_t* tokens, int B, int N, int V, int max_out,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                               int32_t* row_status, void* workspace, size_t workspace_bytes,
+                               void* stream)
+{
+    return tree_common(logits, dtype, parents, tokens, B, N, V, max_out, accepted_len, out_tokens,
+                       out_nodes, row_status, workspace, workspace_bytes, stream, false);
+}
+
+spec_status spec_verify_greedy(const void* target_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, int B, int gamma, int V,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                               void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (gamma < 0) return SPEC_ERR_INVALID_ARG;
+    return tree_common(target_logits, dtype, nullptr, draft_tokens, B, gamma, V, gamma + 1,
+                       accepted_len, out_tokens, nullptr, row_status, workspace, workspace_bytes,
+                       stream, true);
 }
 
 spec_status tree_verify_sample(const void* target_logits, const void* draft_logits,

@@ -103,20 +103,22 @@ __device__ void tree_finish_request(const TreeParams& P, int b)
             bn |= __ldcg(&pp[k].nan);
             if (better(v, i, bv, bi)) { bv = v; bi = i; }
         }
-        const bool ok = !bn && bi != 0x7fffffff;
+        const bool ok = !bn && bi != 0x7fffffff && bv != NEG_INF;  // all -inf: no token
         if (!ok) bad = 1;
         P.amax[(size_t)b * P.R + j] = ok ? bi : -1;
     }
     bad = __any_sync(0xffffffffu, bad);
     __syncwarp();
     int32_t* depth = P.scratch + (size_t)b * P.N * 2;
-    tree_walk_and_emit(P, b, bad, P.parents + (size_t)b * P.N, P.tokens + (size_t)b * P.N,
+    tree_walk_and_emit(P, b, bad, P.parents ? P.parents + (size_t)b * P.N : nullptr,
+                       P.tokens + (size_t)b * P.N,
                        P.amax + (size_t)b * P.R, depth, depth + P.N);
 }
 
 // One warp: validates the request's tree, finds every node's validity and depth, picks the deepest
 // valid node (lowest index on ties) and writes the outputs.  par / tok are the request's parent
-// and token arrays, am its rows' argmaxes, depth / valid N-int scratch (global or shared memory).
+// and token arrays (par null: a chain, node i's parent is i - 1), am its rows' argmaxes, depth /
+// valid N-int scratch (global or shared memory).
 // bad: 0, 1 (a row is non-finite) or 2 (a row could not be read).
 //
 // Nodes are taken 32 at a time in index order, one per lane.  A node whose parent lies in an
@@ -136,7 +138,7 @@ __device__ void tree_walk_and_emit(const TreeParams& P, int b, int bad, const in
     if (st == ROW_OK) {
         int badp = 0, badt = 0;
         for (int i = lane; i < N; i += 32) {
-            const int p = par[i];
+            const int p = par ? par[i] : i - 1;
             if (p < -1 || p >= i) badp = 1;
             const int tk = tok[i];
             if (tk < 0 || tk >= P.V) badt = 1;
@@ -150,7 +152,7 @@ __device__ void tree_walk_and_emit(const TreeParams& P, int b, int bad, const in
         for (int i0 = 0; i0 < N; i0 += 32) {
             const int i = i0 + lane;
             const bool in = i < N;
-            const int p = in ? par[i] : -1;
+            const int p = !in ? -1 : par ? par[i] : i - 1;
             const bool local = p >= i0;  // the parent is in this group
             const int m = in && tok[i] == am[p < 0 ? 0 : p + 1];
             int v = 0, dd = 0;
@@ -195,7 +197,7 @@ __device__ void tree_walk_and_emit(const TreeParams& P, int b, int bad, const in
         if (st == ROW_OK) {  // path written back to front, then the bonus
             int n = bestd;
             out[n] = am[bestn < 0 ? 0 : bestn + 1];
-            for (int i = bestn; i >= 0; i = par[i]) {
+            for (int i = bestn; i >= 0; i = par ? par[i] : i - 1) {
                 --n;
                 out[n] = tok[i];
                 if (onodes) onodes[n] = i;
@@ -445,14 +447,14 @@ __global__ void __launch_bounds__(NT) tree_finish_kernel(TreeParams P)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x, N = P.N, R = P.R;
     const bool staged = N <= TREE_SMEM_NODES;
-    const int32_t* par = staged ? tsm : P.parents + (size_t)b * N;
+    const int32_t* par = staged ? tsm : P.parents ? P.parents + (size_t)b * N : nullptr;
     const int32_t* tok = staged ? tsm + N : P.tokens + (size_t)b * N;
     int32_t* depth = staged ? tsm + 2 * N : P.scratch + (size_t)b * N * 2;
     int32_t* valid = staged ? tsm + 3 * N : P.scratch + (size_t)b * N * 2 + N;
     int32_t* am = staged ? tsm + 4 * N : P.amax + (size_t)b * R;
     if (staged)
         for (int i = tid; i < N; i += NT) {
-            tsm[i] = __ldg(P.parents + (size_t)b * N + i);
+            tsm[i] = P.parents ? __ldg(P.parents + (size_t)b * N + i) : i - 1;  // null: a chain
             tsm[N + i] = __ldg(P.tokens + (size_t)b * N + i);
         }
     if (tid == 0) sh_bad = 0;
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(NT) tree_finish_kernel(TreeParams P)
             }
             const int btmo = __any_sync(0xffffffffu, bn == 2);
             bn = __any_sync(0xffffffffu, bn);
-            const bool ok = !bn && bi != 0x7fffffff;
+            const bool ok = !bn && bi != 0x7fffffff && bv != NEG_INF;  // all -inf: no token
             if (!ok) bad = btmo ? 2 : max(bad, 1);
             if (lane == 0) am[j] = ok ? bi : -1;
         }

@@ -23,6 +23,9 @@ Workload recipes (five named configurations):
                                           like the target rows (row 0 frontier, row i+1 at node i);
                                           the children of a node are i.i.d. draws from the draft
                                           row at their parent (qrow = parent + 1)
+  c8  B=64  gamma=5 V=128256 bf16         linear greedy verify: c5's recipe on a chain of 5 drafted
+                                          tokens (target rows as c3's target; a token is its row's
+                                          argmax with prob 0.6, else uniform)
   c7  G=8 x N=8 particles, K=5, V=128256 bf16, T=0.7, eta = N/2: one SMC-SD round; logits as
                                           c3 (target, draft = 0.8*target + N(0,1.5^2)), draft
                                           tokens from q, incoming log weights N(0, 0.5^2),
@@ -70,6 +73,7 @@ class TreeConfig:
     dtype: str = "bf16"
     p_match: float = 0.6
     seed: int = 1005
+    chain: bool = False    # verified as a linear draft (spec_verify_greedy), not as a tree
 
 
 CONFIGS = {
@@ -78,7 +82,9 @@ CONFIGS = {
     "c3": SpecConfig("c3", 64, 5, 128256, "bf16", 0.7, 0, "zipf", 0.8, 1.5, 1003),
     "c4": SpecConfig("c4", 256, 7, 152064, "bf16", 0.8, 50, "peaks", 1.0, 2.0, 1004),
 }
-TREE_CONFIGS = {"c5": TreeConfig("c5", 32, 128256)}
+TREE_CONFIGS = {"c5": TreeConfig("c5", 32, 128256),
+                "c8": TreeConfig("c8", 64, 128256, branching=(1, 1, 1, 1, 1), max_nodes=5,
+                                 seed=1008, chain=True)}
 
 
 @dataclass(frozen=True)

@@ -119,6 +119,12 @@ def test_host_validation_without_gpu(lib):
                 dict(out=None), dict(lw=P(0x10002))):
         assert smc_call(**bad) == INVALID, bad
     assert smc_call(wsp=None) == WORKSPACE
+    # spec_verify_greedy: sizes and pointers
+    assert lib.spec_verify_greedy(fake, 1, fake, 0, 5, 100, fake, fake, None, ws, 1 << 30, None) == 0
+    assert lib.spec_verify_greedy(fake, 1, fake, 2, -1, 100, fake, fake, None, ws, 1 << 30, None) == INVALID
+    assert lib.spec_verify_greedy(fake, 1, None, 2, 3, 100, fake, fake, None, ws, 1 << 30, None) == INVALID
+    assert lib.spec_verify_greedy(fake, 9, fake, 2, 3, 100, fake, fake, None, ws, 1 << 30, None) == INVALID
+    assert lib.spec_verify_greedy(fake, 1, fake, 2, 3, 100, fake, fake, None, ws, 16, None) == WORKSPACE
     assert lib.spec_status_string(0) == b"ok"
     # the no-allocation entry point refuses oversized or invalid sizes before any CUDA call
     TOO_LARGE = 4

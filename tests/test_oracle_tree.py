@@ -162,3 +162,26 @@ def test_synthetic_tree_shape():
         assert -1 <= p < i
         depth[i] = 1 if p < 0 else depth[p] + 1
     assert np.bincount(depth).tolist() == [0, 4, 16, 32, 12]
+
+
+def test_linear_greedy_is_greedy_decoding():
+    """A chain verified greedily emits what greedy decoding does: the drafted prefix that agrees
+    with the target's greedy next tokens, then the target's next token ([M16] "Verify the Tree";
+    greedy is the p/q rule with one-hot p, M7.1)."""
+    rng = np.random.default_rng(21)
+    V, gamma = 12, 6
+    nxt = rng.integers(0, V, V)  # a context-free next-token table: the target's greedy step
+    for trial in range(200):
+        start = int(rng.integers(0, V))
+        greedy = [start]
+        for _ in range(gamma + 1):
+            greedy.append(int(nxt[greedy[-1]]))
+        m = int(rng.integers(0, gamma + 1))          # the draft follows greedy decoding m steps
+        draft = greedy[1:1 + m] + [int((greedy[1 + j] + 1 + rng.integers(0, V - 1)) % V)
+                                   for j in range(m, gamma)]
+        prefix = [start] + draft
+        rows = one_hot_rows([nxt[t] for t in prefix], V)  # row i: the greedy step after token i
+        o = O.spec_verify_greedy(rows[None], np.array([draft], np.int32))
+        assert o["accepted_len"][0] == m
+        assert list(o["out_tokens"][0, : m + 1]) == greedy[1:m + 2]
+        assert np.all(o["out_tokens"][0, m + 1:] == -1)
