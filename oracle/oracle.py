@@ -79,8 +79,12 @@ def _bind(lib):
     lib.oracle_smc_verify.restype = I
     lib.oracle_ess.argtypes = [P, I]
     lib.oracle_ess.restype = D
+    lib.oracle_spec_verify_masked.argtypes = [P, P, I, P, P, I, I, I, D, P, P, P, P, P, P, P, P]
+    lib.oracle_spec_verify_masked.restype = I
     lib.oracle_row_probs.argtypes = [P, I, Z, I, D, I, P, P, P]
     lib.oracle_row_probs.restype = I
+    lib.oracle_row_probs_masked.argtypes = [P, I, Z, I, D, I, P, P, P, P]
+    lib.oracle_row_probs_masked.restype = I
     lib.oracle_lse_online.argtypes = [P, I, I]
     lib.oracle_lse_online.restype = D
     lib.oracle_lse_maxshift.argtypes = [P, I]
@@ -112,12 +116,20 @@ def _logits(a: np.ndarray):
     raise TypeError(f"unsupported logits dtype {a.dtype}")
 
 
-def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k: int = 0):
+def mask_words(V: int) -> int:
+    """32-bit words of one grammar-mask row over a vocabulary of V tokens."""
+    return (V + 31) // 32
+
+
+def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k: int = 0,
+                allowed=None):
     """Exact speculative-sampling verify over B requests (fp64).
 
     target [B, gamma+1, V], draft [B, gamma, V] (float64, float32, or bf16 bits as uint16),
-    draft_tokens [B, gamma] int32, uniforms [B, gamma+2] float32.  Returns a dict with
-    accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin.
+    draft_tokens [B, gamma] int32, uniforms [B, gamma+2] float32.  ``allowed`` (optional, no
+    top-k with it) is the grammar mask [B, gamma+1, ceil(V/32)] uint32: bit v % 32 of word v // 32
+    set when token v is valid at that position.  Returns a dict with accepted_len, out_tokens,
+    row_status, lse_p, lse_q, accept, margin.
     """
     lib = _load()
     t, dt = _logits(target)
@@ -139,11 +151,17 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k
         accept=np.empty((B, gamma)),
         margin=np.empty(B),
     )
-    rc = lib.oracle_spec_verify(
-        _ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V, float(temperature), int(top_k),
-        _ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["row_status"]),
-        _ptr(out["lse_p"]), _ptr(out["lse_q"]), _ptr(out["accept"]), _ptr(out["margin"]),
-    )
+    outs = (_ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["row_status"]),
+            _ptr(out["lse_p"]), _ptr(out["lse_q"]), _ptr(out["accept"]), _ptr(out["margin"]))
+    if allowed is None:
+        rc = lib.oracle_spec_verify(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V,
+                                    float(temperature), int(top_k), *outs)
+    else:
+        if top_k:
+            raise ValueError("the masked oracle takes no top-k")
+        m = np.ascontiguousarray(allowed, dtype=np.uint32).reshape(B, gamma + 1, mask_words(V))
+        rc = lib.oracle_spec_verify_masked(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V,
+                                           float(temperature), _ptr(m), *outs)
     if rc != 0:
         raise ValueError("oracle_spec_verify rejected its arguments")
     return out
@@ -279,16 +297,22 @@ def ess(weights) -> float:
     return _load().oracle_ess(_ptr(lw), lw.shape[0])
 
 
-def row_probs(logits_row, temperature: float, top_k: int = 0):
-    """Processed probability row p = softmax(topk(logits)/T).  Returns (status, p, lse, thr)."""
+def row_probs(logits_row, temperature: float, top_k: int = 0, allowed=None):
+    """Processed probability row p = softmax(topk(mask(logits))/T).  ``allowed``: the row's
+    grammar-mask words (ceil(V/32) uint32) or None.  Returns (status, p, lse, thr)."""
     lib = _load()
     x, dt = _logits(np.asarray(logits_row).reshape(-1))
     V = x.shape[0]
     p = np.zeros(V)
     lse = ctypes.c_double(0.0)
     thr = ctypes.c_double(0.0)
-    st = lib.oracle_row_probs(_ptr(x), dt, 0, V, float(temperature), int(top_k), _ptr(p),
-                              ctypes.byref(lse), ctypes.byref(thr))
+    if allowed is None:
+        st = lib.oracle_row_probs(_ptr(x), dt, 0, V, float(temperature), int(top_k), _ptr(p),
+                                  ctypes.byref(lse), ctypes.byref(thr))
+    else:
+        m = np.ascontiguousarray(allowed, dtype=np.uint32).reshape(mask_words(V))
+        st = lib.oracle_row_probs_masked(_ptr(x), dt, 0, V, float(temperature), int(top_k), _ptr(m),
+                                         _ptr(p), ctypes.byref(lse), ctypes.byref(thr))
     return st, p, lse.value, thr.value
 
 

@@ -90,20 +90,34 @@ double oracle_kth_largest(const double* x, int n, int k)
 
 /* ---------------------------------------------------------------- processors + softmax */
 
+/* Grammar mask bit of token v: bit (v mod 32) of 32-bit word v / 32 of the row's words. */
+static int token_allowed(const uint32_t* allowed, int v)
+{
+    return (int)((allowed[v / 32] >> (v % 32)) & 1u);
+}
+
 /*
  * One probability row after the declared processors ([M7.1] 0x02A: p_i = Pi_T(logits)):
- *   optional top-k on the stored logits, then z = logit / T, then max-shift softmax
- *   ([M7.1] 0x04J backend 1).  Returns a row status; fills p[0..V) and *lse (natural log of the
- *   normaliser of z over the kept tokens) and *thr (the top-k threshold, -inf without top-k).
+ *   optional grammar mask, optional top-k on the stored logits, then z = logit / T, then max-shift
+ *   softmax ([M7.1] 0x04J backend 1).  Returns a row status; fills p[0..V) and *lse (natural log
+ *   of the normaliser of z over the kept tokens) and *thr (the top-k threshold, -inf without
+ *   top-k).
+ *
+ * The grammar mask ([TRLM] "Grammar and deterministic opportunities") replaces q by
+ *   q_G(x) = q(x) 1[x in A_G] / sum_v q(v) 1[v in A_G]:
+ * `allowed` (NULL = every token) holds one bit per token of the valid set A_G.  A token outside
+ * A_G is removed before anything else reads the row: its stored logit becomes -inf, so a NaN or
+ * +inf there is never seen.  The normalisation over A_G is then the softmax's own.
  */
-int oracle_row_probs(const void* base, int dtype, size_t off, int V, double T, int top_k,
-                     double* p, double* lse, double* thr)
+int oracle_row_probs_masked(const void* base, int dtype, size_t off, int V, double T, int top_k,
+                            const uint32_t* allowed, double* p, double* lse, double* thr)
 {
     if (V < 1) return OR_ROW_NONFINITE;
     double* x = (double*)malloc(sizeof(double) * (size_t)V);
     int v;
     for (v = 0; v < V; ++v) {
-        x[v] = load_logit(base, dtype, off + (size_t)v);
+        x[v] = (allowed && !token_allowed(allowed, v)) ? -INFINITY
+                                                       : load_logit(base, dtype, off + (size_t)v);
         if (isnan(x[v]) || (isinf(x[v]) && x[v] > 0)) { free(x); return OR_ROW_NONFINITE; }
     }
     double t = -INFINITY;
@@ -128,6 +142,13 @@ int oracle_row_probs(const void* base, int dtype, size_t off, int V, double T, i
     *lse = m + log(S);
     free(x);
     return OR_ROW_OK;
+}
+
+/* The same row without a grammar mask. */
+int oracle_row_probs(const void* base, int dtype, size_t off, int V, double T, int top_k,
+                     double* p, double* lse, double* thr)
+{
+    return oracle_row_probs_masked(base, dtype, off, V, T, top_k, NULL, p, lse, thr);
 }
 
 /* Backend 2 of [M7.1] 0x04J: an online (m, l) merge over vocabulary blocks of width `block`.
@@ -219,12 +240,14 @@ int oracle_inverse_cdf(const double* r, int V, double u, double* lo, double* hi)
  * accept test and |u - C(v-1)/Z|, |u - C(v)/Z| for the drawn token).
  * Any output pointer except the first two may be NULL.
  */
-int oracle_spec_verify(const void* target, const void* draft, int dtype, const int32_t* tokens,
-                       const float* uniforms, int B, int gamma, int V, double T, int top_k,
-                       int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
-                       double* lse_p, double* lse_q, double* accept, double* margin)
+static int spec_verify_impl(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                            const float* uniforms, int B, int gamma, int V, double T, int top_k,
+                            const uint32_t* allowed, int32_t* accepted_len, int32_t* out_tokens,
+                            int32_t* row_status, double* lse_p, double* lse_q, double* accept,
+                            double* margin)
 {
     if (B < 0 || gamma < 0 || V < 1 || !(T > 0.0)) return 1;
+    const size_t W = (size_t)(V + 31) / 32; /* mask words per position */
     double* p = (double*)malloc(sizeof(double) * (size_t)(gamma + 1) * (size_t)V);
     double* q = (double*)malloc(sizeof(double) * (size_t)(gamma > 0 ? gamma : 1) * (size_t)V);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -234,14 +257,17 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, const i
         for (int i = 0; i <= gamma; ++i) {
             double l = NAN;
             size_t off = ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * (size_t)V;
-            int s = oracle_row_probs(target, dtype, off, V, T, top_k, p + (size_t)i * V, &l, &thr);
+            const uint32_t* m = allowed ? allowed + ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * W : NULL;
+            int s = oracle_row_probs_masked(target, dtype, off, V, T, top_k, m, p + (size_t)i * V, &l, &thr);
             if (s != OR_ROW_OK) st = OR_ROW_NONFINITE;
             if (lse_p) lse_p[(size_t)b * (gamma + 1) + i] = l;
         }
         for (int i = 0; i < gamma; ++i) {
             double l = NAN;
             size_t off = ((size_t)b * (size_t)gamma + (size_t)i) * (size_t)V;
-            int s = oracle_row_probs(draft, dtype, off, V, T, top_k, q + (size_t)i * V, &l, &thr);
+            /* the draft row of position i sampled under the same grammar state as target row i */
+            const uint32_t* m = allowed ? allowed + ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * W : NULL;
+            int s = oracle_row_probs_masked(draft, dtype, off, V, T, top_k, m, q + (size_t)i * V, &l, &thr);
             if (s != OR_ROW_OK) st = OR_ROW_NONFINITE;
             if (lse_q) lse_q[(size_t)b * gamma + i] = l;
         }
@@ -312,6 +338,34 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, const i
     free(q);
     free(r);
     return 0;
+}
+
+int oracle_spec_verify(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                       const float* uniforms, int B, int gamma, int V, double T, int top_k,
+                       int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                       double* lse_p, double* lse_q, double* accept, double* margin)
+{
+    return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, top_k, NULL,
+                            accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
+}
+
+/*
+ * The verify round under a grammar mask ([TRLM] "Grammar and deterministic opportunities": exact
+ * speculation is exact relative to q_G when baseline and speculative execution mask alike).
+ *   allowed [B, gamma+1, ceil(V/32)] uint32: the valid-token set of position i, one bit per token
+ *           (bit v mod 32 of word v / 32).  Position i masks target row i and draft row i (the
+ *           draft sampled token i in the same grammar state); position gamma masks the bonus row.
+ * Temperature only (no top-k); everything else as oracle_spec_verify.
+ */
+int oracle_spec_verify_masked(const void* target, const void* draft, int dtype,
+                              const int32_t* tokens, const float* uniforms, int B, int gamma,
+                              int V, double T, const uint32_t* allowed, int32_t* accepted_len,
+                              int32_t* out_tokens, int32_t* row_status, double* lse_p,
+                              double* lse_q, double* accept, double* margin)
+{
+    if (!allowed) return 1;
+    return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, 0, allowed,
+                            accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
 }
 
 /* ---------------------------------------------------------------- greedy tree verify */

@@ -26,6 +26,11 @@ Workload recipes (five named configurations):
   c8  B=64  gamma=5 V=128256 bf16         linear greedy verify: c5's recipe on a chain of 5 drafted
                                           tokens (target rows as c3's target; a token is its row's
                                           argmax with prob 0.6, else uniform)
+  c9  B=64  gamma=5 V=128256 bf16  T=0.7  grammar-masked verify: c3's logits; every position has its
+                                          own valid-token set, one of three kinds with equal odds:
+                                          narrow (64 random tokens), half (each token with
+                                          probability 1/2), wide (each token blocked with
+                                          probability 1/100); draft tokens from the masked q
   c7  G=8 x N=8 particles, K=5, V=128256 bf16, T=0.7, eta = N/2: one SMC-SD round; logits as
                                           c3 (target, draft = 0.8*target + N(0,1.5^2)), draft
                                           tokens from q, incoming log weights N(0, 0.5^2),
@@ -61,6 +66,7 @@ class SpecConfig:
     draft_scale: float  # draft = draft_scale * target + N(0, draft_noise^2)
     draft_noise: float
     seed: int
+    mask: str = ""      # "" = no grammar mask; "grammar" = the mixed valid-set recipe (c9)
 
 
 @dataclass(frozen=True)
@@ -81,6 +87,9 @@ CONFIGS = {
     "c2": SpecConfig("c2", 8, 4, 32000, "bf16", 1.0, 0, "peaks", 1.0, 1.0, 1002),
     "c3": SpecConfig("c3", 64, 5, 128256, "bf16", 0.7, 0, "zipf", 0.8, 1.5, 1003),
     "c4": SpecConfig("c4", 256, 7, 152064, "bf16", 0.8, 50, "peaks", 1.0, 2.0, 1004),
+}
+MASK_CONFIGS = {
+    "c9": SpecConfig("c9", 64, 5, 128256, "bf16", 0.7, 0, "zipf", 0.8, 1.5, 1009, mask="grammar"),
 }
 TREE_CONFIGS = {"c5": TreeConfig("c5", 32, 128256),
                 "c8": TreeConfig("c8", 64, 128256, branching=(1, 1, 1, 1, 1), max_nodes=5,
@@ -201,6 +210,43 @@ def draft_keep_mask(x: np.ndarray, top_k: int) -> np.ndarray | None:
     return x >= kth
 
 
+def grammar_valid_sets(rng: np.random.Generator, positions: int, V: int) -> np.ndarray:
+    """Valid-token sets of ``positions`` grammar states, bool [positions, V].
+
+    Each state is one of three kinds with equal odds: narrow (64 distinct random tokens, or all of
+    them when V <= 64), half (each token valid with probability 1/2) or wide (each token blocked
+    with probability 1/100).  A state with no valid token is given one random token.
+    """
+    kinds = rng.integers(0, 3, size=positions)
+    out = np.zeros((positions, V), dtype=bool)
+    for i, k in enumerate(kinds):
+        if k == 0:
+            out[i, rng.choice(V, size=min(64, V), replace=False)] = True
+        elif k == 1:
+            out[i] = rng.random(V) < 0.5
+        else:
+            out[i] = rng.random(V) >= 0.01
+        if not out[i].any():
+            out[i, rng.integers(0, V)] = True
+    return out
+
+
+def pack_valid_sets(valid: np.ndarray) -> np.ndarray:
+    """bool [..., V] -> uint32 words [..., ceil(V/32)]: bit v % 32 of word v // 32 = valid[..., v]."""
+    V = valid.shape[-1]
+    W = (V + 31) // 32
+    pad = np.zeros(valid.shape[:-1] + (W * 32,), dtype=bool)
+    pad[..., :V] = valid
+    by = np.packbits(pad, axis=-1, bitorder="little")
+    return np.ascontiguousarray(by).view("<u4").astype(np.uint32)
+
+
+def unpack_valid_sets(words: np.ndarray, V: int) -> np.ndarray:
+    """Inverse of pack_valid_sets."""
+    by = np.ascontiguousarray(words, dtype="<u4").view(np.uint8)
+    return np.unpackbits(by, axis=-1, bitorder="little")[..., :V].astype(bool)
+
+
 def _nthreads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
@@ -215,6 +261,7 @@ class SpecBatch:
     draft_tokens: np.ndarray  # [B, gamma] int32
     uniforms: np.ndarray     # [B, gamma+2] float32
     meta: dict = field(default_factory=dict)
+    allowed: np.ndarray | None = None  # grammar mask words [B, gamma+1, ceil(V/32)] uint32
 
     @property
     def rows(self) -> int:
@@ -237,6 +284,8 @@ def make_spec_batch(cfg: SpecConfig, *, threads: int | None = None) -> SpecBatch
     draft = np.empty((B, g, V), dtype=sdt)
     tokens = np.empty((B, g), dtype=np.int32)
     uniforms = np.empty((B, g + 2), dtype=np.float32)
+    allowed = np.empty((B, g + 1, (V + 31) // 32), dtype=np.uint32) if cfg.mask else None
+    req_mask = np.random.SeedSequence([cfg.seed, 11]).spawn(B) if cfg.mask else None
 
     def one(b):
         rng = np.random.Generator(np.random.PCG64(req_logit[b]))
@@ -247,6 +296,10 @@ def make_spec_batch(cfg: SpecConfig, *, threads: int | None = None) -> SpecBatch
         draft[b] = _store(d32, cfg.dtype)
         xd = stored_to_f64(draft[b])
         keep = draft_keep_mask(xd, cfg.top_k)
+        if cfg.mask:
+            valid = grammar_valid_sets(np.random.Generator(np.random.PCG64(req_mask[b])), g + 1, V)
+            allowed[b] = pack_valid_sets(valid)
+            keep = valid[:g] if keep is None else keep & valid[:g]
         tokens[b] = gumbel_max_tokens(np.random.Generator(np.random.PCG64(req_draw[b])),
                                       xd / cfg.temperature, keep)
         uniforms[b] = uniforms_from(np.random.Generator(np.random.PCG64(req_unif[b])), g + 2)
@@ -258,7 +311,7 @@ def make_spec_batch(cfg: SpecConfig, *, threads: int | None = None) -> SpecBatch
     else:
         for b in range(B):
             one(b)
-    return SpecBatch(cfg, target, draft, tokens, uniforms)
+    return SpecBatch(cfg, target, draft, tokens, uniforms, allowed=allowed)
 
 
 def redraw(batch: SpecBatch, trial_seed: int) -> SpecBatch:
