@@ -9,7 +9,8 @@ them c6 (tree_verify_sample, B=32 N=64(+1) V=128256 bf16 T=0.7: the stochastic t
 reads only the rows its walk visits (about 31 MB per call, inside L2), so each of its timed calls
 follows an L2 flush outside the call's events and its rates come from the per-call event times.
 c7 is one SMC-SD round through smc_verify (8 groups x 8 particles, K=5, V=128256 bf16, T=0.7);
-c8 linear greedy verify through spec_verify_greedy (B=64 gamma=5 V=128256 bf16).
+c8 linear greedy verify through spec_verify_greedy (B=64 gamma=5 V=128256 bf16); c9 grammar-masked
+verify through spec_verify_masked (c3's logits with a valid-token set per position).
 
 value     logit rows per second, inputs resident in HBM (whole job, all ranks)
 e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
@@ -53,6 +54,7 @@ KERNEL_OF = {
     "c6": ("tree_sample_kernel", ["sv_tree_sample.cu", "sv_tree_sample.cuh", "sv_common.cuh"]),
     "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c8": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
+    "c9": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
 }
 DOMINANT_CFG = "c4"
 
@@ -63,13 +65,13 @@ def workload_batches(names, rank, requests=None):
     from speculative_decoding_verification_spec_gb300 import synth as S
     out = {}
     for n in names:
-        cfg = (S.CONFIGS.get(n) or S.TREE_CONFIGS.get(n) or S.SAMPLE_TREE_CONFIGS.get(n)
-               or S.SMC_CONFIGS[n])
+        cfg = (S.CONFIGS.get(n) or S.MASK_CONFIGS.get(n) or S.TREE_CONFIGS.get(n)
+               or S.SAMPLE_TREE_CONFIGS.get(n) or S.SMC_CONFIGS[n])
         kw = dict(seed=rank_seed(cfg, rank))
         if requests:
             kw["groups" if n in S.SMC_CONFIGS else "B"] = requests
         cfg = S.scaled(cfg, **kw)
-        if n in S.CONFIGS:
+        if n in S.CONFIGS or n in S.MASK_CONFIGS:
             out[n] = S.make_spec_batch(cfg)
         elif n in S.TREE_CONFIGS:
             out[n] = S.make_tree_batch(cfg)
@@ -131,7 +133,12 @@ def describe(names):
     from speculative_decoding_verification_spec_gb300 import synth as S
     parts = []
     for n in names:
-        if n in S.CONFIGS:
+        if n in S.MASK_CONFIGS:
+            c = S.MASK_CONFIGS[n]
+            parts.append(f"{n} spec_verify_masked B={c.B} gamma={c.gamma} V={c.V} {c.dtype} "
+                         f"T={c.temperature} grammar valid sets per position (narrow 64 tokens / "
+                         f"half / wide 99%, equal odds)")
+        elif n in S.CONFIGS:
             c = S.CONFIGS[n]
             op = "spec_verify_topk" if c.top_k else "spec_verify"
             parts.append(f"{n} {op} B={c.B} gamma={c.gamma} V={c.V} {c.dtype} T={c.temperature}"
@@ -287,7 +294,8 @@ def cpu_baseline(names, budget_s=15.0):
                 rows_done += Np * (2 * b.cfg.K + 1)
             else:
                 O.spec_verify(b.target[i:i + 1], b.draft[i:i + 1], b.draft_tokens[i:i + 1],
-                              b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k)
+                              b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k,
+                              allowed=None if b.allowed is None else b.allowed[i:i + 1])
                 rows_done += 2 * b.cfg.gamma + 1
             t_used += time.perf_counter() - t0
             i += 1
@@ -332,6 +340,8 @@ def run_ours(args, rank, world, local_rank):
                         log_weights=b.log_weights, uniforms=b.uniforms)
         else:
             arrs = dict(target=b.target, draft=b.draft, tokens=b.draft_tokens, uniforms=b.uniforms)
+            if b.allowed is not None:
+                arrs["allowed"] = b.allowed.view(np.int32)
         host[n] = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16
                                        else np.ascontiguousarray(v)).pin_memory()
                    for k, v in arrs.items()}
@@ -355,8 +365,8 @@ def run_ours(args, rank, world, local_rank):
             return sv.tree_verify_greedy(ins["logits"], ins["parents"], ins["tokens"], out=out,
                                          workspace=wss[n], stream=stream)
         return sv.spec_verify(ins["target"], ins["draft"], ins["tokens"], ins["uniforms"],
-                              b.cfg.temperature, top_k=b.cfg.top_k, out=out, workspace=wss[n],
-                              stream=stream)
+                              b.cfg.temperature, top_k=b.cfg.top_k, allowed=ins.get("allowed"),
+                              out=out, workspace=wss[n], stream=stream)
 
     for n in names:  # allocate outputs once
         outs[n] = call(n, devin[n])
@@ -370,8 +380,8 @@ def run_ours(args, rank, world, local_rank):
             rows = sample_tree_rows_read(b, outs[n]["accepted_len"].cpu().numpy(),
                                          outs[n]["accept"].cpu().numpy())
             read_bytes[n] = rows * b.cfg.V * b.target.itemsize
-        else:
-            read_bytes[n] = b.logit_bytes
+        else:  # plus the grammar mask's words, once
+            read_bytes[n] = b.logit_bytes + (b.allowed.nbytes if getattr(b, "allowed", None) is not None else 0)
     # calls whose reads fit in L2 are timed after an L2 flush (a 256 MB write), outside their events
     flush = None
     if any(read_bytes[n] < L2_BYTES for n in names):
@@ -573,7 +583,8 @@ def run_reference(args, rank, world):
             else:
                 j = (i // len(names)) % b.cfg.B
                 O.spec_verify(b.target[j:j + 1], b.draft[j:j + 1], b.draft_tokens[j:j + 1],
-                              b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.top_k)
+                              b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.top_k,
+                              allowed=None if b.allowed is None else b.allowed[j:j + 1])
                 rows += 2 * b.cfg.gamma + 1
         return rows
 
@@ -604,7 +615,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7", "c8"],
+    ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7", "c8",
+                                           "c9"],
                     default="suite")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

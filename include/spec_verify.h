@@ -6,6 +6,7 @@
  *
  *   spec_verify        exact speculative sampling with temperature
  *   spec_verify_topk   the same with a top-k processor applied identically to target and draft
+ *   spec_verify_masked the same with a grammar mask (a valid-token set per position)
  *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
  *   spec_verify_greedy linear greedy verification of a draft (the greedy tree on a chain)
  *   tree_verify_sample stochastic verification of a candidate tree (residual update over children)
@@ -85,6 +86,7 @@ enum {
  * Bytes of workspace needed by one call.
  *   spec_verify:        spec_workspace_bytes(B, gamma, V, 0, 0)
  *   spec_verify_topk:   spec_workspace_bytes(B, gamma, V, top_k, 0)
+ *   spec_verify_masked: spec_workspace_bytes(B, gamma, V, 0, 0)   (as spec_verify)
  *   tree_verify_greedy: spec_workspace_bytes(B, 0, V, 0, N)   (tree_nodes = N > 0)
  * The value is an upper bound valid for both dtypes, any alignment and any GPU.
  * Returns 0 for invalid sizes.
@@ -135,6 +137,30 @@ spec_status spec_verify_topk(const void* target_logits, const void* draft_logits
                              int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
                              float* aux_lse_p, float* aux_lse_q, float* aux_accept,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify under a grammar mask ("Exact speculative and assisted decoding for TinyRustLM",
+ * "Grammar and deterministic opportunities"): with A_G the valid-token set of the grammar state at
+ * a position, both distributions of that position become
+ *   p_G(x) = p(x) 1[x in A_G] / sum_v p(v) 1[v in A_G]      (q_G likewise),
+ * and the round is exact relative to p_G when the draft sampled from q_G.
+ *
+ *   allowed [B, gamma+1, ceil(V/32)] uint32, device, 4-byte aligned: bit (v mod 32) of word v/32 of
+ *           position i is set when token v is in A_G at position i.  Position i < gamma masks
+ *           target row i and draft row i (the draft sampled token i in the same grammar state);
+ *           position gamma masks the bonus row.  Bits of tokens >= V are ignored.
+ *
+ * A disallowed token is removed before its logit is read, so a NaN or +inf there is not seen.  A
+ * drafted token outside A_G has q_G(x) = 0: SPEC_ROW_BAD_TOKEN.  A position whose A_G is empty
+ * leaves its rows without mass: SPEC_ROW_NONFINITE.  Temperature only (no top-k); every other
+ * argument, output and status as spec_verify.  allowed == NULL is SPEC_ERR_INVALID_ARG (B > 0).
+ */
+spec_status spec_verify_masked(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const float* uniforms,
+                               const uint32_t* allowed, int B, int gamma, int V, float temperature,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                               float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Greedy tree verify (Module 16 "Verify the Tree"; M7.7 0x07E row convention).

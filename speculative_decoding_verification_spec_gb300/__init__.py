@@ -1,5 +1,5 @@
-"""GB300 (sm_103a) speculative-decoding verify step: exact speculative sampling, its top-k
-variant, greedy tree verify, stochastic tree verify and the verify side of an SMC-SD round, as hand-written CUDA behind a C ABI (include/spec_verify.h).
+"""GB300 (sm_103a) speculative-decoding verify step: exact speculative sampling, its top-k and
+grammar-mask variants, greedy tree verify, stochastic tree verify and the verify side of an SMC-SD round, as hand-written CUDA behind a C ABI (include/spec_verify.h).
 
 The binding functions load the compiled library on first use and raise if it is missing: there is
 no CPU fallback.
@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     smc_verify,
     spec_verify,
     spec_verify_greedy,
+    spec_verify_masked,
     spec_verify_noalloc,
     spec_verify_topk,
     tree_verify_greedy,

@@ -18,8 +18,8 @@ ROW_OK, ROW_NONFINITE, ROW_DEGENERATE, ROW_BAD_TOKEN, ROW_TIMEOUT = 0, 1, 2, 3, 
 ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 
 # every symbol the header declares
-EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "tree_verify_greedy",
-           "spec_verify_greedy",
+EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "spec_verify_masked",
+           "tree_verify_greedy", "spec_verify_greedy",
            "tree_verify_sample", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
@@ -50,6 +50,8 @@ def load(path: str | None = None):
     lib.spec_verify.restype = I
     lib.spec_verify_topk.argtypes = [P, P, I, P, P, I, I, I, F, I, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_topk.restype = I
+    lib.spec_verify_masked.argtypes = [P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_masked.restype = I
     lib.tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
     lib.tree_verify_greedy.restype = I
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, Z, P]
@@ -139,13 +141,15 @@ def workspace_bytes(B, gamma, V, top_k=0, tree_nodes=0) -> int:
 
 
 def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, top_k: int = 0,
-                aux: bool = False, out=None, workspace: Workspace | None = None, stream=None):
+                allowed=None, aux: bool = False, out=None, workspace: Workspace | None = None,
+                stream=None):
     """Exact speculative-sampling verify on the GPU.
 
     target [B, gamma+1, V], draft [B, gamma, V] (bf16 / int16 bf16 bits / fp32, CUDA),
     draft_tokens [B, gamma] int32, uniforms [B, gamma+2] fp32.  ``top_k`` > 0 applies the top-k
-    processor (spec_verify_topk).  Returns a dict of CUDA tensors: accepted_len, out_tokens,
-    row_status (and lse_p, lse_q, accept when ``aux``).
+    processor (spec_verify_topk).  ``allowed`` (CUDA int32/uint32 [B, gamma+1, ceil(V/32)]) is a
+    grammar mask (spec_verify_masked; not with top_k).  Returns a dict of CUDA tensors:
+    accepted_len, out_tokens, row_status (and lse_p, lse_q, accept when ``aux``).
     """
     lib = load()
     _need_cuda(target, draft, draft_tokens, uniforms)
@@ -169,12 +173,26 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, to
     tail = [_ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out.get("row_status")),
             _ptr(out.get("lse_p")), _ptr(out.get("lse_q")), _ptr(out.get("accept")),
             _ptr(ws), ws.numel(), _stream(stream)]
-    if top_k:
+    if allowed is not None:
+        if top_k:
+            raise ValueError("spec_verify_masked takes no top_k")
+        _need_cuda(allowed)
+        W = (V + 31) // 32
+        if tuple(allowed.shape) != (B, gamma + 1, W) or allowed.element_size() != 4 \
+                or not allowed.is_contiguous():
+            raise ValueError(f"allowed must be a contiguous 32-bit [B, gamma+1, {W}] tensor")
+        rc = lib.spec_verify_masked(*common[:5], _ptr(allowed), *common[5:], *tail)
+    elif top_k:
         rc = lib.spec_verify_topk(*common, int(top_k), *tail)
     else:
         rc = lib.spec_verify(*common, *tail)
     _check(rc)
     return out
+
+
+def spec_verify_masked(target, draft, draft_tokens, uniforms, allowed, temperature: float, **kw):
+    """spec_verify under a grammar mask ``allowed`` [B, gamma+1, ceil(V/32)] (32-bit words)."""
+    return spec_verify(target, draft, draft_tokens, uniforms, temperature, allowed=allowed, **kw)
 
 
 def spec_verify_noalloc(target, draft, draft_tokens, uniforms, temperature: float, *,

@@ -182,7 +182,8 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
                                int V, float temperature, int top_k, int32_t* accepted_len,
                                int32_t* out_tokens, int32_t* row_status, float* aux_lse_p,
                                float* aux_lse_q, float* aux_accept, void* workspace,
-                               size_t workspace_bytes, void* stream, const SmcArgs* smc = nullptr)
+                               size_t workspace_bytes, void* stream, const SmcArgs* smc = nullptr,
+                               const uint32_t* allowed = nullptr)
 {
     if (B < 0 || gamma < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
@@ -205,6 +206,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
         (aux_lse_q && !aligned(aux_lse_q, 4)) || (aux_accept && !aligned(aux_accept, 4)))
         return SPEC_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 16)) return SPEC_ERR_WORKSPACE;
+    if (allowed && (!aligned(allowed, 4) || top_k != 0 || smc)) return SPEC_ERR_INVALID_ARG;
 
     const bool topk = top_k > 0 && top_k < V;
     const int dt = (dtype == SPEC_BF16) ? DT_BF16 : DT_F32;
@@ -252,6 +254,8 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.aux_lse_p = aux_lse_p;
     P.aux_lse_q = aux_lse_q;
     P.aux_accept = aux_accept;
+    P.mask = allowed;
+    P.mwords = (int)cdiv(V, 32);
     if (smc) {
         P.smc = 1;
         P.smc_logw_in = smc->logw_in;
@@ -356,6 +360,19 @@ spec_status spec_verify_topk(const void* target_logits, const void* draft_logits
     return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
                        temperature, top_k, accepted_len, out_tokens, row_status, aux_lse_p,
                        aux_lse_q, aux_accept, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_verify_masked(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const float* uniforms,
+                               const uint32_t* allowed, int B, int gamma, int V, float temperature,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                               float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                               void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (B > 0 && !allowed) return SPEC_ERR_INVALID_ARG;
+    return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
+                       temperature, 0, accepted_len, out_tokens, row_status, aux_lse_p, aux_lse_q,
+                       aux_accept, workspace, workspace_bytes, stream, nullptr, allowed);
 }
 
 spec_status smc_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,

@@ -144,6 +144,10 @@ struct SpecParams {
     const float* smc_logw_in;  // [B] log weight before the round
     float* smc_log_ratio;      // [B] or null: sum over the draft positions of log p - log q
     float* smc_logw;           // [B] logw_in + log ratio (the group step may reset it)
+    // grammar mask (spec_verify_masked): [B, gamma+1, mwords] allowed-token bits, one 32-bit word
+    // per 32 tokens (bit v % 32 of word v / 32); position i masks target row i and draft row i
+    const uint32_t* mask;
+    int mwords;
 };
 
 struct TreeParams {
@@ -495,6 +499,75 @@ struct RawVec {
         }
     }
 };
+
+// ---------------------------------------------------------------- grammar mask
+//
+// "Exact speculative and assisted decoding for TinyRustLM", "Grammar and deterministic
+// opportunities": a grammar mask replaces q by q_G(x) = q(x) 1[x in A_G] / sum over A_G, the same
+// for p.  A token outside A_G is turned into a -inf logit the moment it is loaded, so every later
+// step (maximum, sum, gathered token, residual, draw) sees only A_G and the renormalisation is the
+// softmax's own.
+
+// the mask words of request b's row r (target row r <= gamma, else draft row r - gamma - 1): both
+// rows of position i share position i's valid set
+__device__ __forceinline__ const uint32_t* spec_mask_row(const SpecParams& P, int b, int r)
+{
+    const int pos = (r <= P.gamma) ? r : r - P.gamma - 1;
+    return P.mask + ((size_t)b * (P.gamma + 1) + pos) * (size_t)P.mwords;
+}
+
+// allowed bits of the VEC elements of vector v (VEC = 1, 4 or 8 divides 32): bit e = element e
+template <int VEC>
+__device__ __forceinline__ uint32_t allowed_bits(const uint32_t* mrow, long long v)
+{
+    const long long e0 = v * VEC;
+    const uint32_t w = __ldg(mrow + (e0 >> 5));
+    return (w >> (unsigned)(e0 & 31)) & ((VEC == 32) ? 0xffffffffu : ((1u << VEC) - 1u));
+}
+
+// one vector of raw logits with its disallowed elements replaced by -inf bit patterns (RawVec layout:
+// VEC == 1 holds one fp32 pattern in .x, bf16 as its high half)
+template <int DT, int VEC>
+__device__ __forceinline__ void mask_raw(uint4& w, uint32_t bits)
+{
+    if constexpr (VEC == 1) {
+        if (!(bits & 1u)) w.x = 0xff800000u;
+    } else if constexpr (DT == DT_BF16) {
+        // element 2k is the low half of word k, element 2k + 1 the high half.  The keep mask of word
+        // k comes from one byte permute in sign-replicate mode: bit 2k moved to the top of byte 0
+        // fills bytes 0-1, bit 2k + 1 moved to the top of the second operand's byte 0 fills bytes 2-3.
+        auto sel = [bits](uint32_t x, int k) {
+            uint32_t keep;
+            asm("prmt.b32 %0, %1, %2, 0xCC88;" : "=r"(keep) : "r"(bits << (7 - 2 * k)), "r"(bits << (6 - 2 * k)));
+            return (x & keep) | (0xff80ff80u & ~keep);
+        };
+        w.x = sel(w.x, 0);
+        w.y = sel(w.y, 1);
+        w.z = sel(w.z, 2);
+        w.w = sel(w.w, 3);
+    } else {
+        if (!(bits & 1u)) w.x = 0xff800000u;
+        if (!(bits & 2u)) w.y = 0xff800000u;
+        if (!(bits & 4u)) w.z = 0xff800000u;
+        if (!(bits & 8u)) w.w = 0xff800000u;
+    }
+}
+
+// the same on values already converted to fp32
+template <int VEC>
+__device__ __forceinline__ void mask_vals(float (&x)[VEC], uint32_t bits)
+{
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+        if (!((bits >> e) & 1u)) x[e] = NEG_INF;
+}
+
+// the stored logit of token tok in request b's row r, -inf when the grammar mask removes it
+__device__ __forceinline__ float masked_logit(const SpecParams& P, int b, int r, int dtype, int tok)
+{
+    if (P.mask && !((__ldg(spec_mask_row(P, b, r) + (tok >> 5)) >> (tok & 31)) & 1u)) return NEG_INF;
+    return load_logit(spec_row_ptr(P, b, r), dtype, tok);
+}
 
 // warp-wide claim of the next task index from a global counter (lane 0 increments)
 __device__ __forceinline__ long long claim_task(unsigned* ctr)

@@ -309,8 +309,8 @@ __device__ Plan compute_plan_warp(const SpecParams& P, int b, bool topk)
             } else {
                 const RowStats rp = ld_rowstats(P.rstats + (size_t)b * R + i);
                 const RowStats rq = ld_rowstats(P.rstats + (size_t)b * R + g + 1 + i);
-                const float xp = load_logit(spec_row_ptr(P, b, i), DT, x);
-                const float xq = load_logit(spec_row_ptr(P, b, g + 1 + i), DT, x);
+                const float xp = masked_logit(P, b, i, DT, x);
+                const float xq = masked_logit(P, b, g + 1 + i, DT, x);
                 lp = row_log2prob(xp, rp, P.c, topk);
                 lq = row_log2prob(xq, rq, P.c, topk);
             }

@@ -24,9 +24,9 @@ namespace sv {
 // Online softmax statistics of one task: lane accumulators (m, mc, s), mc = fp32(m*c),
 // s = sum 2^(fma(x, c, -mc)).
 template <int DT, int VEC>
-__device__ __forceinline__ void task_softmax_stats(const char* row, long long t0, long long t1,
-                                                   float c, uint64_t pol, float& m, float& mc,
-                                                   float& s)
+__device__ __forceinline__ void task_softmax_stats(const char* row, const uint32_t* mrow, long long t0,
+                                                   long long t1, float c, uint64_t pol, float& m,
+                                                   float& mc, float& s)
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -38,8 +38,12 @@ __device__ __forceinline__ void task_softmax_stats(const char* row, long long t0
 #pragma unroll
             for (int u = 0; u < U1; ++u) {
                 const long long v = base + u * 32;
-                if (v < t1) w[u] = ld_stream_v4_pol(row + v * 16, pol);
-                else w[u] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                if (v < t1) {
+                    w[u] = ld_stream_v4_pol(row + v * 16, pol);
+                    if (mrow) mask_raw<DT, 8>(w[u], allowed_bits<8>(mrow, v));
+                } else {
+                    w[u] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                }
             }
             uint32_t pm = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
 #pragma unroll
@@ -74,6 +78,7 @@ __device__ __forceinline__ void task_softmax_stats(const char* row, long long t0
                 const long long v = base + u * 32;
                 if (v < t1) {
                     load_vec_pol<DT, VEC>(row, v, pol, x[u]);
+                    if (mrow) mask_vals<VEC>(x[u], allowed_bits<VEC>(mrow, v));
                 } else {
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) x[u][e] = NEG_INF;
@@ -256,8 +261,8 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
         const long long t0 = (long long)s * TV1;
         const long long t1 = min(t0 + TV1, P.nvec);
         float m = NEG_INF, mc = NEG_INF, acc = 0.f;
-        task_softmax_stats<DT, VEC>(row, t0, t1, P.c, pinned_row(P, r) ? pol_keep : pol_first,
-                                    m, mc, acc);
+        task_softmax_stats<DT, VEC>(row, P.mask ? spec_mask_row(P, b, r) : nullptr, t0, t1, P.c,
+                                    pinned_row(P, r) ? pol_keep : pol_first, m, mc, acc);
         stats_finalize<DT>(P, b, r, s, m, mc, acc);
         t = next;
     }
@@ -270,7 +275,10 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
 // (chunk, warp).  Warp-specialised: a producer warp fills the ring (ring_produce) and the consumer
 // warps release each stage on its "empty" mbarrier, so they never wait for one another.
 // NaN or +inf anywhere makes the partial's sum NaN, so the row merge reports the row non-finite.
-template <int DT>
+// MASK: the grammar mask's bits of the thread's vectors are applied to the raw vectors as they leave
+// shared memory.  They are loaded two chunks ahead into one of two register sets used in turn, so
+// their latency (a DRAM miss under full load) hides behind the chunks in between.
+template <int DT, bool MASK>
 __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
@@ -317,14 +325,34 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
     // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
     int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
     const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
-    for (int id = blockIdx.x; id < nch; id += G0) {
+    // the mask bits of chunk (rid, cix) for this thread's vectors: vector j * NT + tid of the chunk
+    // sits in word (j * NT + tid) * VEC / 32 of the chunk's CHUNK / 32 words, at a fixed shift
+    auto load_mask = [&](int rid, int cix, uint32_t (&out)[STREAM_NV]) {
+        const int b = rid / P.R;
+        const uint32_t* mw = spec_mask_row(P, b, rid - b * P.R) + (size_t)cix * (CHUNK / 32) + (tid * VEC) / 32;
+        const unsigned sh = (unsigned)(tid * VEC) & 31u;
+        const int left = P.V - cix * CHUNK - tid * VEC;  // elements from this thread's first vector on
+#pragma unroll
+        for (int j = 0; j < STREAM_NV; ++j) {
+            uint32_t wv = 0u;
+            if (j * NT * VEC < left)
+                asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(wv) : "l"(mw + j * (NT * VEC / 32)));
+            out[j] = (wv >> sh) & ((1u << VEC) - 1u);
+        }
+    };
+    auto advance = [&](int& r, int& c) {
+        r += drow;
+        c += dci;
+        if (c >= P.S1) {
+            c -= P.S1;
+            ++r;
+        }
+    };
+    int pr = row_id, pc = ci;  // MASK: the chunk whose bits are loaded next
+    // one chunk; with MASK, mreg holds its bits (loaded two chunks earlier) and is refilled
+    auto process = [&](int id, uint32_t (&mreg)[STREAM_NV]) {
         if (id != blockIdx.x) {
-            row_id += drow;
-            ci += dci;
-            if (ci >= P.S1) {
-                ci -= P.S1;
-                ++row_id;
-            }
+            advance(row_id, ci);
             if (++stg == STREAM_STAGES) {
                 stg = 0;
                 phase ^= 1u;
@@ -347,6 +375,13 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
                 w[j] = make_uint4(pad, pad, pad, pad);
                 if (ok && cbase + (j * NT + tid) * VEC < cend) w[j] = lds128(sb + j * NT);
             }
+        }
+        if constexpr (MASK) {
+#pragma unroll
+            for (int j = 0; j < STREAM_NV; ++j) mask_raw<DT, VEC>(w[j], mreg[j]);
+            // this register set is free again: the bits of the chunk two ahead
+            if ((long long)id + 2 * G0 < nch) load_mask(pr, pc, mreg);
+            advance(pr, pc);
         }
         // release the stage once every lane has read it; a warp whose wait ran out never releases
         // it (its copy may still land), which stops the producer
@@ -407,6 +442,21 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
             pt.S = warp_sum((a0 + a1) + (a2 + a3));
         }
         if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
+    };
+    if constexpr (MASK) {
+        // two register sets in turn, so that no register move waits for a load still in flight
+        uint32_t mA[STREAM_NV], mB[STREAM_NV];
+        if (blockIdx.x < nch) load_mask(pr, pc, mA);
+        advance(pr, pc);
+        if ((long long)blockIdx.x + G0 < nch) load_mask(pr, pc, mB);
+        advance(pr, pc);
+        for (int id = blockIdx.x; id < nch; id += 2 * G0) {
+            process(id, mA);
+            if ((long long)id + G0 < nch) process(id + G0, mB);
+        }
+    } else {
+        uint32_t none[STREAM_NV];
+        for (int id = blockIdx.x; id < nch; id += G0) process(id, none);
     }
 }
 
@@ -430,7 +480,7 @@ __global__ void __launch_bounds__(PLAN_WARPS * 32) spec_rowplan_kernel(SpecParam
         const int pos = (r < g) ? r : (r > g) ? r - g - 1 : -1;
         const int tok = (r < R && pos >= 0) ? __ldg(P.tokens + (size_t)b * g + pos) : -1;
         ok = tok >= 0 && tok < P.V;
-        return ok ? load_logit(spec_row_ptr(P, b, r), DT, tok) : 0.f;
+        return ok ? masked_logit(P, b, r, DT, tok) : 0.f;
     };
     // lane 0: the row's statistics from its merged maximum and sum
     auto row_stats = [&](float Mr, DFloat Sr, int tmo, bool tok_ok, float xtok) {
@@ -562,7 +612,8 @@ __device__ __forceinline__ void residual_from(const float (&xp)[VEC], const floa
 // rounding stays far below the 1e-6 decision margin.
 template <int DT, int VEC>
 __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const char* rowq,
-                                  const Plan& pl, long long vbase, double t_local)
+                                  const uint32_t* mrow, const Plan& pl, long long vbase,
+                                  double t_local)
 {
     const int lane = threadIdx.x & 31;
     const long long v = vbase + lane;
@@ -577,6 +628,11 @@ __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const c
         } else {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) xq[e] = 0.f;
+        }
+        if (mrow) {
+            const uint32_t bits = allowed_bits<VEC>(mrow, v);
+            mask_vals<VEC>(xp, bits);
+            mask_vals<VEC>(xq, bits);
         }
         residual_from<VEC>(xp, xq, rowq != nullptr, pl, P.c, r);
     }
@@ -618,6 +674,7 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
 {
     const int lane = threadIdx.x & 31;
     const float* segs = P.segs + (size_t)b * P.nseg;
+    const uint32_t* mrow = P.mask ? spec_mask_row(P, b, pl.rp) : nullptr;
     const int per = (P.nseg + 31) / 32;
     const int s0 = min(lane * per, P.nseg), s1 = min(s0 + per, P.nseg);
     if (per <= DPL) {
@@ -666,7 +723,7 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
         seg = __shfl_sync(0xffffffffu, seg, owner);
         base = __shfl_sync(0xffffffffu, base, owner);
         if (seg < 0) return -1;
-        return resolve_in_segment<DT, VEC>(P, rowp, rowq, pl, (long long)seg * SEGV, t - base);
+        return resolve_in_segment<DT, VEC>(P, rowp, rowq, mrow, pl, (long long)seg * SEGV, t - base);
     }
     // more segments than the registers hold: each lane's block in batches of eight
     double mine = 0.0;
@@ -704,7 +761,7 @@ __device__ int draw_from_segments(const SpecParams& P, int b, const Plan& pl, co
     seg = __shfl_sync(0xffffffffu, seg, owner);
     base = __shfl_sync(0xffffffffu, base, owner);
     if (seg < 0) return -1;
-    return resolve_in_segment<DT, VEC>(P, rowp, rowq, pl, (long long)seg * SEGV, t - base);
+    return resolve_in_segment<DT, VEC>(P, rowp, rowq, mrow, pl, (long long)seg * SEGV, t - base);
 }
 
 template <int DT, int VEC>
@@ -719,6 +776,7 @@ __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
         const Plan pl = ld_plan(P.plan + b);
         const char* rowp = spec_row_ptr(P, b, pl.rp);
         const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
+        const uint32_t* mrow = P.mask ? spec_mask_row(P, b, pl.rp) : nullptr;
         if (pl.status == ROW_OK) {
             const long long t0 = (long long)s * TV2;
             const long long t1 = min(t0 + TV2, P.nvec);
@@ -736,6 +794,11 @@ __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
                     if (v < t1) {
                         xp[u].load(rowp, v, pol);
                         if (rowq) xq[u].load(rowq, v, pol);
+                        if (mrow) {
+                            const uint32_t bits = allowed_bits<VEC>(mrow, v);
+                            mask_raw<DT, VEC>(xp[u].w, bits);
+                            mask_raw<DT, VEC>(xq[u].w, bits);
+                        }
                     }
                 }
 #pragma unroll
@@ -772,7 +835,7 @@ __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
 // the token.
 constexpr int RCHUNK = NT * RCV;
 
-template <int DT>
+template <int DT, bool MASK>
 __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
@@ -799,6 +862,11 @@ __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
                 if (v < c1) {
                     a[u].load(rowp, v, pol);
                     if (rowq) q[u].load(rowq, v, pol);
+                    if constexpr (MASK) {
+                        const uint32_t bits = allowed_bits<VEC>(spec_mask_row(P, b, pl.rp), v);
+                        mask_raw<DT, VEC>(a[u].w, bits);
+                        mask_raw<DT, VEC>(q[u].w, bits);
+                    }
                 }
             }
 #pragma unroll
@@ -838,24 +906,32 @@ static void launch_softmax_plain(const SpecParams& P, int sms, cudaStream_t st)
     spec_resample_kernel<DT, VEC><<<persistent_grid<spec_resample_kernel<DT, VEC>>(P.tasks2, sms), NT, 0, st>>>(P);
 }
 
-template <int DT>
+template <int DT, bool MASK>
 static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
 {
-    constexpr auto K1 = spec_stream_kernel<DT>;
+    constexpr auto K1 = spec_stream_kernel<DT, MASK>;
     mark_kernel_start(st);
     K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
     mark_kernel_stop(st);
     const int pw = (P.R <= 32) ? std::min(P.R, PLAN_WARPS) : WARPS;
     launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, (unsigned)(32 * pw), 0, st, P);
-    launch_dependent(spec_resample_chunk_kernel<DT>, (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
+    launch_dependent(spec_resample_chunk_kernel<DT, MASK>, (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
 }
 
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st)
 {
-    if (P.dtype == DT_BF16 && P.vec == 8) launch_softmax_chunk<DT_BF16>(P, sms, st);
-    else if (P.dtype == DT_BF16) launch_softmax_plain<DT_BF16, 1>(P, sms, st);
-    else if (P.vec == 4) launch_softmax_chunk<DT_F32>(P, sms, st);
-    else launch_softmax_plain<DT_F32, 1>(P, sms, st);
+    const bool mask = P.mask != nullptr;
+    if (P.dtype == DT_BF16 && P.vec == 8) {
+        if (mask) launch_softmax_chunk<DT_BF16, true>(P, sms, st);
+        else launch_softmax_chunk<DT_BF16, false>(P, sms, st);
+    } else if (P.dtype == DT_BF16) {
+        launch_softmax_plain<DT_BF16, 1>(P, sms, st);
+    } else if (P.vec == 4) {
+        if (mask) launch_softmax_chunk<DT_F32, true>(P, sms, st);
+        else launch_softmax_chunk<DT_F32, false>(P, sms, st);
+    } else {
+        launch_softmax_plain<DT_F32, 1>(P, sms, st);
+    }
     return cudaGetLastError();
 }
 

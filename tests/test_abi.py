@@ -126,6 +126,15 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_verify_greedy(fake, 9, fake, 2, 3, 100, fake, fake, None, ws, 1 << 30, None) == INVALID
     assert lib.spec_verify_greedy(fake, 1, fake, 2, 3, 100, fake, fake, None, ws, 16, None) == WORKSPACE
     assert lib.spec_status_string(0) == b"ok"
+    # spec_verify_masked: the mask is required (B > 0) and 4-byte aligned
+    def mk_call(B=2, mask=fake):
+        return lib.spec_verify_masked(fake, fake, 1, fake, fake, mask, B, 3, 100, F(1.0), fake, fake,
+                                      None, None, None, None, ws, 1 << 30, None)
+
+    assert mk_call(B=0, mask=None) == 0
+    assert mk_call(mask=None) == INVALID
+    assert mk_call(mask=P(0x10002)) == INVALID
+    assert mk_call(B=-1) == INVALID
     # the no-allocation entry point refuses oversized or invalid sizes before any CUDA call
     TOO_LARGE = 4
     assert lib.spec_verify_noalloc(fake, fake, 1, fake, fake, 1024, 7, 152064, 1.0, fake, fake,
