@@ -77,6 +77,9 @@ def _bind(lib):
     lib.oracle_smc_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, D, I, D,
                                       P, P, P, P, P, P, P, P, P]
     lib.oracle_smc_verify.restype = I
+    lib.oracle_tree_verify_typical.argtypes = [P, I, P, P, P, I, I, I, D, D, D, I,
+                                               P, P, P, P, P, P, P]
+    lib.oracle_tree_verify_typical.restype = I
     lib.oracle_ess.argtypes = [P, I]
     lib.oracle_ess.restype = D
     lib.oracle_spec_verify_masked.argtypes = [P, P, I, P, P, I, I, I, D, P, P, P, P, P, P, P, P]
@@ -295,6 +298,39 @@ def ess(weights) -> float:
     """Effective sample size of positive weights (given as weights, not logs)."""
     lw = np.log(np.ascontiguousarray(weights, dtype=np.float64))
     return _load().oracle_ess(_ptr(lw), lw.shape[0])
+
+
+def tree_verify_typical(logits, parents, tokens, uniforms, temperature: float, eps: float,
+                        delta: float, max_out: int | None = None):
+    """Tree verify with typical acceptance (fp64).  logits [B, N+1, V]; parents, tokens [B, N];
+    uniforms [B].  Returns accepted_len, out_tokens, out_nodes, row_status, entropy [B, N+1],
+    logp [B, N], margin [B]."""
+    lib = _load()
+    lg, dt = _logits(logits)
+    B, n1, V = lg.shape
+    N = n1 - 1
+    if max_out is None:
+        max_out = N + 1
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B)
+    out = dict(
+        accepted_len=np.empty(B, np.int32),
+        out_tokens=np.empty((B, max_out), np.int32),
+        out_nodes=np.empty((B, max(max_out - 1, 0)), np.int32),
+        row_status=np.empty(B, np.int32),
+        entropy=np.empty((B, N + 1)),
+        logp=np.empty((B, N)),
+        margin=np.empty(B),
+    )
+    rc = lib.oracle_tree_verify_typical(
+        _ptr(lg), dt, _ptr(par), _ptr(tok), _ptr(u), B, N, V, float(temperature), float(eps),
+        float(delta), int(max_out), _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
+        _ptr(out["out_nodes"]) if max_out > 1 else None, _ptr(out["row_status"]),
+        _ptr(out["entropy"]), _ptr(out["logp"]), _ptr(out["margin"]))
+    if rc != 0:
+        raise ValueError("oracle_tree_verify_typical rejected its arguments")
+    return out
 
 
 def row_probs(logits_row, temperature: float, top_k: int = 0, allowed=None):

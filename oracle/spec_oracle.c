@@ -31,6 +31,9 @@
  *     uniforms outside [0,1) are a bad uniform; such requests emit nothing (-1).
  *   - tree argmax ties go to the lowest token index; the deepest valid node wins, ties to the
  *     lowest node index.
+ *   - typical acceptance (tree): a node passes when p(x) > min(eps, delta exp(-H)) strictly, H the
+ *     natural-log entropy of its predictor row after temperature; the token after the accepted
+ *     path is drawn from p of the accepted node's own row with the request's one uniform
  *   - SMC-SD round: uniform slot 0 draws the extension token from row K, slot 1 the particle's
  *     ancestor; ancestors are drawn by inverse CDF over the group's normalised weights in particle
  *     order; a particle with a bad status leaves its group's ESS and resampling undefined (NaN, -1)
@@ -445,6 +448,127 @@ int oracle_tree_verify_greedy(const void* logits, int dtype, const int32_t* pare
         if (row_status) row_status[b] = st;
     }
     free(amax);
+    free(valid);
+    free(depth);
+    free(path);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- typical-acceptance tree verify */
+
+/*
+ * Medusa-style tree verify with typical acceptance ([M16] "Verify the Tree": Medusa's sampling
+ * mode swaps the greedy check for typical acceptance, accepting a token when the target's
+ * probability clears min(eps, delta * exp(-H))):
+ *   logits   [B, N+1, V]  row 0 = prefix frontier, row i+1 = produced at candidate node i
+ *   parents  [B, N]       -1 for a depth-1 node, else in [0, i)
+ *   tokens   [B, N]
+ *   uniforms [B]          the final draw
+ * Row j's distribution is p_j = softmax(logits[b][j] / T) and its entropy H_j = -sum p_j ln p_j.
+ * Node i is typical when p_r(tok_i) > min(eps, delta * exp(-H_r)), r its predictor row (0 for a
+ * depth-1 node, parent + 1 otherwise), and valid when it is typical and its parent is valid.  The
+ * deepest valid node (lowest index on ties) is accepted with its root path.  The token after the
+ * path is drawn from p of the accepted node's own row (the frontier row when no node is valid) by
+ * inverse CDF with uniforms[b]: in sampling mode the next token comes from the target there.
+ * Statuses: a row with NaN, +inf or no finite entry -> non-finite; then a bad parent, a token
+ * outside [0, V), a uniform outside [0, 1); a path and final token longer than max_out -> overflow.
+ * Outputs: accepted_len[B] (path length or -1), out_tokens[B, max_out] (path tokens, the drawn
+ * token, then -1), out_nodes[B, max_out-1] (nullable), row_status[B], and, each nullable:
+ * entropy[B, N+1] (H of every row), logp[B, N] (ln p_r(tok_i) of every node), margin[B] (the
+ * smallest |ln p_r(tok_i) - ln threshold| over the nodes whose parent is valid, and |u - C| for the
+ * two CDF boundaries of the drawn token).
+ */
+int oracle_tree_verify_typical(const void* logits, int dtype, const int32_t* parents,
+                               const int32_t* tokens, const float* uniforms, int B, int N, int V,
+                               double T, double eps, double delta, int max_out,
+                               int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                               int32_t* row_status, double* entropy, double* logp, double* margin)
+{
+    if (B < 0 || N < 0 || V < 1 || max_out < 1 || !(T > 0.0) || !(eps >= 0.0) || !(delta >= 0.0) ||
+        !isfinite(eps) || !isfinite(delta))
+        return 1;
+    const size_t R = (size_t)N + 1;
+    double* p = (double*)malloc(sizeof(double) * R * (size_t)V);
+    double* H = (double*)malloc(sizeof(double) * R);
+    int32_t* valid = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    int32_t* depth = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    int32_t* path = (int32_t*)malloc(sizeof(int32_t) * R);
+    for (int b = 0; b < B; ++b) {
+        int st = OR_ROW_OK;
+        for (size_t j = 0; j < R; ++j) {
+            double lse, thr;
+            double* pj = p + j * (size_t)V;
+            int s = oracle_row_probs(logits, dtype, ((size_t)b * R + j) * (size_t)V, V, T, 0, pj,
+                                     &lse, &thr);
+            H[j] = NAN;
+            if (s != OR_ROW_OK) {
+                st = OR_ROW_NONFINITE;
+            } else {
+                double h = 0.0;
+                for (int v = 0; v < V; ++v)
+                    if (pj[v] > 0.0) h -= pj[v] * log(pj[v]);
+                H[j] = h;
+            }
+            if (entropy) entropy[(size_t)b * R + j] = H[j];
+        }
+        const int32_t* par = parents + (size_t)b * N;
+        const int32_t* tok = tokens + (size_t)b * N;
+        const double u = (double)uniforms[b];
+        if (st == OR_ROW_OK)
+            for (int i = 0; i < N; ++i) {
+                if (par[i] < -1 || par[i] >= i) { st = OR_ROW_BAD_PARENT; break; }
+                if (tok[i] < 0 || tok[i] >= V) st = OR_ROW_BAD_TOKEN;
+            }
+        if (st == OR_ROW_OK && !(u >= 0.0 && u < 1.0)) st = OR_ROW_BAD_UNIFORM;
+        double mg = INFINITY;
+        int best = -1, bestd = 0;
+        for (int i = 0; i < N; ++i)
+            if (logp) logp[(size_t)b * N + i] = NAN;
+        if (st == OR_ROW_OK) {
+            for (int i = 0; i < N; ++i) {
+                const int pr = par[i];
+                const int row = pr < 0 ? 0 : pr + 1;
+                const double px = p[(size_t)row * V + tok[i]];
+                const double thr = fmin(eps, delta * exp(-H[row]));
+                const int typical = px > thr;
+                if (logp) logp[(size_t)b * N + i] = log(px);
+                if (pr < 0 || valid[pr]) { /* a test that decides the outcome */
+                    double d = fabs(log(px) - log(thr));
+                    if (d < mg) mg = d;
+                }
+                valid[i] = typical && (pr < 0 || valid[pr]);
+                depth[i] = pr < 0 ? 1 : depth[pr] + 1;
+                if (valid[i] && depth[i] > bestd) { bestd = depth[i]; best = i; }
+            }
+            if (bestd + 1 > max_out) st = OR_ROW_OVERFLOW;
+        }
+        int32_t* out = out_tokens + (size_t)b * max_out;
+        int32_t* on = out_nodes ? out_nodes + (size_t)b * (max_out - 1) : NULL;
+        for (int i = 0; i < max_out; ++i) out[i] = -1;
+        if (on) for (int i = 0; i < max_out - 1; ++i) on[i] = -1;
+        if (st == OR_ROW_OK) {
+            const int row = best < 0 ? 0 : best + 1;
+            double lo = 0.0, hi = 0.0;
+            const int y = oracle_inverse_cdf(p + (size_t)row * V, V, u, &lo, &hi);
+            double d1 = fabs(u - lo), d2 = fabs(u - hi);
+            if (d1 < mg) mg = d1;
+            if (d2 < mg) mg = d2;
+            int n = 0;
+            for (int i = best; i >= 0; i = par[i]) path[n++] = i;
+            for (int j = 0; j < n; ++j) {
+                out[j] = tok[path[n - 1 - j]];
+                if (on) on[j] = path[n - 1 - j];
+            }
+            out[n] = y;
+            accepted_len[b] = n;
+        } else {
+            accepted_len[b] = -1;
+        }
+        if (row_status) row_status[b] = st;
+        if (margin) margin[b] = mg;
+    }
+    free(p);
+    free(H);
     free(valid);
     free(depth);
     free(path);

@@ -31,6 +31,9 @@ Workload recipes (five named configurations):
                                           narrow (64 random tokens), half (each token with
                                           probability 1/2), wide (each token blocked with
                                           probability 1/100); draft tokens from the masked q
+  c10 B=32  N=64    V=128256 bf16  T=0.7  typical-acceptance tree verify: c5's recipe (tree, logits,
+                                          tokens); eps = 0.09, delta = 0.3; one uniform per
+                                          request for the token after the path
   c7  G=8 x N=8 particles, K=5, V=128256 bf16, T=0.7, eta = N/2: one SMC-SD round; logits as
                                           c3 (target, draft = 0.8*target + N(0,1.5^2)), draft
                                           tokens from q, incoming log weights N(0, 0.5^2),
@@ -80,6 +83,10 @@ class TreeConfig:
     p_match: float = 0.6
     seed: int = 1005
     chain: bool = False    # verified as a linear draft (spec_verify_greedy), not as a tree
+    typical: bool = False  # verified by typical acceptance (tree_verify_typical)
+    temperature: float = 0.7
+    eps: float = 0.09      # typical acceptance: p(x) > min(eps, delta exp(-H))
+    delta: float = 0.3
 
 
 CONFIGS = {
@@ -93,7 +100,8 @@ MASK_CONFIGS = {
 }
 TREE_CONFIGS = {"c5": TreeConfig("c5", 32, 128256),
                 "c8": TreeConfig("c8", 64, 128256, branching=(1, 1, 1, 1, 1), max_nodes=5,
-                                 seed=1008, chain=True)}
+                                 seed=1008, chain=True),
+                "c10": TreeConfig("c10", 32, 128256, seed=1010, typical=True)}
 
 
 @dataclass(frozen=True)
@@ -382,6 +390,7 @@ class TreeBatch:
     parents: np.ndarray   # [B, N] int32
     tokens: np.ndarray    # [B, N] int32
     meta: dict = field(default_factory=dict)
+    uniforms: np.ndarray | None = None  # [B] float32: typical acceptance's final draw
 
     @property
     def rows(self) -> int:
@@ -421,7 +430,11 @@ def make_tree_batch(cfg: TreeConfig, *, threads: int | None = None) -> TreeBatch
     else:
         for b in range(B):
             one(b)
-    return TreeBatch(cfg, logits, np.broadcast_to(par, (B, N)).copy(), tokens)
+    unif = None
+    if cfg.typical:
+        unif = uniforms_from(np.random.Generator(np.random.PCG64(
+            np.random.SeedSequence([cfg.seed, 13]))), B)
+    return TreeBatch(cfg, logits, np.broadcast_to(par, (B, N)).copy(), tokens, uniforms=unif)
 
 
 # ------------------------------------------------------------------ sampled trees
