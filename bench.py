@@ -10,7 +10,8 @@ reads only the rows its walk visits (about 31 MB per call, inside L2), so each o
 follows an L2 flush outside the call's events and its rates come from the per-call event times.
 c7 is one SMC-SD round through smc_verify (8 groups x 8 particles, K=5, V=128256 bf16, T=0.7);
 c8 linear greedy verify through spec_verify_greedy (B=64 gamma=5 V=128256 bf16); c9 grammar-masked
-verify through spec_verify_masked (c3's logits with a valid-token set per position).
+verify through spec_verify_masked (c3's logits with a valid-token set per position); c10 tree verify
+by typical acceptance through tree_verify_typical (c5's tree and logits, T=0.7, eps=0.09, delta=0.3).
 
 value     logit rows per second, inputs resident in HBM (whole job, all ranks)
 e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
@@ -55,6 +56,8 @@ KERNEL_OF = {
     "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c8": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
     "c9": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c10": ("typical_stream_kernel", ["sv_typical.cu", "sv_typical.cuh", "sv_tree_walk.cuh",
+                                      "sv_common.cuh", "sv_plan.cuh"]),
 }
 DOMINANT_CFG = "c4"
 
@@ -143,6 +146,11 @@ def describe(names):
             op = "spec_verify_topk" if c.top_k else "spec_verify"
             parts.append(f"{n} {op} B={c.B} gamma={c.gamma} V={c.V} {c.dtype} T={c.temperature}"
                          + (f" top_k={c.top_k}" if c.top_k else ""))
+        elif n in S.TREE_CONFIGS and S.TREE_CONFIGS[n].typical:
+            c = S.TREE_CONFIGS[n]
+            parts.append(f"{n} tree_verify_typical B={c.B} N={c.max_nodes}(+1 frontier row) V={c.V} "
+                         f"{c.dtype} T={c.temperature} eps={c.eps} delta={c.delta} tree "
+                         f"{'/'.join(map(str, c.branching))}")
         elif n in S.TREE_CONFIGS and S.TREE_CONFIGS[n].chain:
             c = S.TREE_CONFIGS[n]
             parts.append(f"{n} spec_verify_greedy B={c.B} gamma={c.max_nodes} V={c.V} {c.dtype}")
@@ -280,6 +288,10 @@ def cpu_baseline(names, budget_s=15.0):
                                      b.tokens[i:i + 1], b.qrow[i:i + 1], b.uniforms[i:i + 1],
                                      b.cfg.temperature)
                 rows_done += b.target.shape[1]
+            elif is_greedy_tree(b) and b.cfg.typical:
+                O.tree_verify_typical(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1],
+                                      b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.eps, b.cfg.delta)
+                rows_done += b.logits.shape[1]
             elif is_greedy_tree(b):
                 O.tree_verify_greedy(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1])
                 rows_done += b.logits.shape[1]
@@ -335,6 +347,8 @@ def run_ours(args, rank, world, local_rank):
                         qrow=b.qrow, uniforms=b.uniforms)
         elif is_greedy_tree(b):
             arrs = dict(logits=b.logits, parents=b.parents, tokens=b.tokens)
+            if b.uniforms is not None:
+                arrs["uniforms"] = b.uniforms
         elif is_smc(b):
             arrs = dict(target=b.target, draft=b.draft, tokens=b.draft_tokens,
                         log_weights=b.log_weights, uniforms=b.uniforms)
@@ -358,6 +372,10 @@ def run_ours(args, rank, world, local_rank):
             return sv.smc_verify(ins["target"], ins["draft"], ins["tokens"], ins["log_weights"],
                                  ins["uniforms"], b.cfg.groups, b.cfg.temperature, b.cfg.eta,
                                  out=out, workspace=wss[n], stream=stream)
+        if is_greedy_tree(b) and b.cfg.typical:
+            return sv.tree_verify_typical(ins["logits"], ins["parents"], ins["tokens"],
+                                          ins["uniforms"], b.cfg.temperature, b.cfg.eps,
+                                          b.cfg.delta, out=out, workspace=wss[n], stream=stream)
         if is_greedy_tree(b) and b.cfg.chain:
             return sv.spec_verify_greedy(ins["logits"], ins["tokens"], out=out, workspace=wss[n],
                                          stream=stream)
@@ -578,7 +596,12 @@ def run_reference(args, rank, world):
                 rows += Np * (2 * b.cfg.K + 1)
             elif is_greedy_tree(b):
                 j = (i // len(names)) % b.logits.shape[0]
-                O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
+                if b.cfg.typical:
+                    O.tree_verify_typical(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1],
+                                          b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.eps,
+                                          b.cfg.delta)
+                else:
+                    O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
                 rows += b.logits.shape[1]
             else:
                 j = (i // len(names)) % b.cfg.B
@@ -616,7 +639,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7", "c8",
-                                           "c9"],
+                                           "c9", "c10"],
                     default="suite")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

@@ -10,6 +10,7 @@
  *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
  *   spec_verify_greedy linear greedy verification of a draft (the greedy tree on a chain)
  *   tree_verify_sample stochastic verification of a candidate tree (residual update over children)
+ *   tree_verify_typical Medusa-style tree verification by typical acceptance (entropy threshold)
  *   smc_verify         the verify side of one SMC-SD round: block weights, extension, resampling
  *
  * Sources (page title + section):
@@ -88,6 +89,7 @@ enum {
  *   spec_verify_topk:   spec_workspace_bytes(B, gamma, V, top_k, 0)
  *   spec_verify_masked: spec_workspace_bytes(B, gamma, V, 0, 0)   (as spec_verify)
  *   tree_verify_greedy: spec_workspace_bytes(B, 0, V, 0, N)   (tree_nodes = N > 0)
+ *   tree_verify_typical: spec_workspace_bytes(B, 0, V, 0, N)  (as tree_verify_greedy)
  * The value is an upper bound valid for both dtypes, any alignment and any GPU.
  * Returns 0 for invalid sizes.
  */
@@ -203,6 +205,37 @@ spec_status spec_verify_greedy(const void* target_logits, spec_dtype dtype,
                                const int32_t* draft_tokens, int B, int gamma, int V,
                                int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Tree verify with typical acceptance (Module 16 "Verify the Tree": Medusa's sampling mode swaps
+ * the greedy check for typical acceptance, which accepts a token when the target's probability
+ * clears min(eps, delta exp(-H))).  Same tree layout as tree_verify_greedy:
+ *   logits   [B, N+1, V]  row 0 = prefix frontier, row i+1 = produced at candidate node i
+ *   parents  [B, N]       int32, -1 for a depth-1 node, else in [0, i)
+ *   tokens   [B, N]       int32
+ *   uniforms [B]          fp32 in [0, 1): the draw of the token after the accepted path
+ * Row j's distribution is p_j = softmax(logits[b,j] / temperature), its entropy
+ * H_j = -sum p_j ln p_j.  Node i passes when p_r(tokens[b,i]) > min(epsilon, delta exp(-H_r)),
+ * strictly, r its predictor row (0 at depth 1, parents[b,i] + 1 otherwise); it is valid when it
+ * passes and its parent is valid.  The deepest valid node (lowest index on ties) is accepted:
+ *   accepted_len[b] = its depth (0 when no node is valid)
+ *   out_tokens[b, 0..A-1] = the tokens on its root path, out_tokens[b, A] = a draw from p of the
+ *   accepted node's own row (the frontier row when A = 0) by inverse CDF with uniforms[b] (the
+ *   smallest token whose running mass exceeds u * total, ascending index), then -1 up to max_out.
+ * out_nodes [B, max_out-1] (nullable): the path's node ids, then -1.  Optional (nullable):
+ * row_status [B]; aux_entropy [B, N+1] (H_j); aux_logp [B, N] (ln p_r(tokens[b,i]), NaN when the
+ * request has a bad row, parent or token).  temperature > 0; epsilon, delta >= 0 and finite
+ * (epsilon = 0 passes every token with p > 0); N <= 2048; V <= 16384 * 32 * w, w = 8 (bf16) or
+ * 4 (fp32) elements per 16-byte vector, 1 when rows are not 16-byte aligned.
+ * Statuses: SPEC_ROW_NONFINITE (a row with NaN, +inf or no finite entry), then BAD_PARENT,
+ * BAD_TOKEN, BAD_UNIFORM, OUTPUT_OVERFLOW (path + 1 > max_out).
+ */
+spec_status tree_verify_typical(const void* logits, spec_dtype dtype, const int32_t* parents,
+                                const int32_t* tokens, const float* uniforms, int B, int N, int V,
+                                float temperature, float epsilon, float delta, int max_out,
+                                int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                                int32_t* row_status, float* aux_entropy, float* aux_logp,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Stochastic tree verify (M7.7 0x09A residual update over a node's children; 0x07E row

@@ -20,7 +20,7 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 # every symbol the header declares
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "spec_verify_masked",
            "tree_verify_greedy", "spec_verify_greedy",
-           "tree_verify_sample", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
+           "tree_verify_sample", "tree_verify_typical", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -58,6 +58,8 @@ def load(path: str | None = None):
     lib.spec_verify_greedy.restype = I
     lib.tree_verify_sample.argtypes = [P, P, I, P, P, P, P, I, I, I, I, F, I, P, P, P, P, P, P]
     lib.tree_verify_sample.restype = I
+    lib.tree_verify_typical.argtypes = [P, I, P, P, P, I, I, I, F, F, F, I, P, P, P, P, P, P, P, Z, P]
+    lib.tree_verify_typical.restype = I
     lib.smc_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, F, F, P, P, P, P, P, P, P, P, P, Z, P]
     lib.smc_verify.restype = I
     lib.spec_verify_noalloc.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, P, P, P, P]
@@ -257,6 +259,40 @@ def tree_verify_greedy(logits, parents, tokens, *, max_out: int | None = None, o
                                 B, N, V, max_out, _ptr(out["accepted_len"]),
                                 _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")),
                                 _ptr(out.get("row_status")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc)
+    return out
+
+
+def tree_verify_typical(logits, parents, tokens, uniforms, temperature: float, epsilon: float,
+                        delta: float, *, max_out: int | None = None, aux: bool = False, out=None,
+                        workspace: Workspace | None = None, stream=None):
+    """Tree verify with typical acceptance on the GPU.  logits [B, N+1, V] (bf16 / int16 bf16
+    bits / fp32, CUDA), parents and tokens [B, N] int32, uniforms [B] fp32.  Returns a dict of CUDA
+    tensors: accepted_len, out_tokens [B, max_out], out_nodes, row_status (and entropy [B, N+1],
+    logp [B, N] when ``aux``)."""
+    lib = load()
+    _need_cuda(logits, parents, tokens, uniforms)
+    B, R, V = logits.shape
+    N = R - 1
+    mo = N + 1 if max_out is None else int(max_out)
+    dev = logits.device
+    if out is None:
+        out = dict(
+            accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_tokens=torch.empty(B, mo, dtype=torch.int32, device=dev),
+            out_nodes=torch.empty(B, max(mo - 1, 1), dtype=torch.int32, device=dev),
+            row_status=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+        if aux:
+            out["entropy"] = torch.empty(B, R, dtype=torch.float32, device=dev)
+            out["logp"] = torch.empty(B, max(N, 1), dtype=torch.float32, device=dev)
+    nbytes = workspace_bytes(B, 0, V, 0, max(N, 1))
+    ws = _workspace(workspace, dev).get(nbytes)
+    rc = lib.tree_verify_typical(
+        _ptr(logits), _dtype_code(logits), _ptr(parents), _ptr(tokens), _ptr(uniforms), B, N, V,
+        float(temperature), float(epsilon), float(delta), mo, _ptr(out["accepted_len"]),
+        _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")), _ptr(out.get("row_status")),
+        _ptr(out.get("entropy")), _ptr(out.get("logp")), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc)
     return out
 

@@ -9,6 +9,7 @@
 #include "sv_common.cuh"
 #include "sv_smc.cuh"
 #include "sv_tree_sample.cuh"
+#include "sv_typical.cuh"
 
 namespace sv {
 
@@ -484,6 +485,71 @@ spec_status spec_verify_greedy(const void* target_logits, spec_dtype dtype,
     return tree_common(target_logits, dtype, nullptr, draft_tokens, B, gamma, V, gamma + 1,
                        accepted_len, out_tokens, nullptr, row_status, workspace, workspace_bytes,
                        stream, true);
+}
+
+spec_status tree_verify_typical(const void* logits, spec_dtype dtype, const int32_t* parents,
+                                const int32_t* tokens, const float* uniforms, int B, int N, int V,
+                                float temperature, float epsilon, float delta, int max_out,
+                                int32_t* accepted_len, int32_t* out_tokens, int32_t* out_nodes,
+                                int32_t* row_status, float* aux_entropy, float* aux_logp,
+                                void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (B < 0 || N < 0 || N > TYP_MAX_NODES || V < 1 || max_out < 1) return SPEC_ERR_INVALID_ARG;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+    const double T = (double)temperature;
+    const float c = (float)(1.4426950408889634 / T);
+    if (!std::isfinite(c) || !(c > 0.0f)) return SPEC_ERR_INVALID_ARG;
+    if (!(epsilon >= 0.f) || !std::isfinite(epsilon) || !(delta >= 0.f) || !std::isfinite(delta))
+        return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    const int R = N + 1;
+    if ((long long)B * R > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+    const size_t es = dtype == SPEC_BF16 ? 2 : 4;
+    if (!logits || !aligned(logits, es)) return SPEC_ERR_INVALID_ARG;
+    if (N > 0 && (!parents || !aligned(parents, 4) || !tokens || !aligned(tokens, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_INVALID_ARG;
+    if (!accepted_len || !out_tokens || !aligned(accepted_len, 4) || !aligned(out_tokens, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if ((out_nodes && !aligned(out_nodes, 4)) || (row_status && !aligned(row_status, 4)) ||
+        (aux_entropy && !aligned(aux_entropy, 4)) || (aux_logp && !aligned(aux_logp, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16)) return SPEC_ERR_WORKSPACE;
+
+    const int dt = (dtype == SPEC_BF16) ? DT_BF16 : DT_F32;
+    const int vec = pick_vec(dt, V, logits, nullptr);
+    const Shape sh = row_shape(V, vec);
+    TypicalParams P;
+    std::memset(&P, 0, sizeof P);
+    P.t.logits = logits;
+    P.t.parents = parents;
+    P.t.tokens = tokens;
+    P.t.B = B; P.t.N = N; P.t.V = V; P.t.R = R;
+    P.t.dtype = dt; P.t.vec = vec; P.t.nvec = sh.nvec;
+    P.t.max_out = max_out;
+    P.t.accepted_len = accepted_len;
+    P.t.out_tokens = out_tokens;
+    P.t.out_nodes = (max_out > 1) ? out_nodes : nullptr;
+    P.t.row_status = row_status;
+    P.uniforms = uniforms;
+    P.c = c;
+    P.ln_eps = epsilon > 0.f ? (float)std::log((double)epsilon) : -INFINITY;
+    P.ln_delta = delta > 0.f ? (float)std::log((double)delta) : -INFINITY;
+    P.aux_entropy = aux_entropy;
+    P.aux_logp = aux_logp;
+    // 16-byte vectors: 32 KB stream chunks, a partial per chunk and warp; scalar path: slices of
+    // TYP_SLICE elements (as many as slices1, so the tree workspace size holds them)
+    P.S1 = (int)(vec > 1 ? stream_chunks(sh) : cdiv(V, TYP_SLICE));
+    P.np = vec > 1 ? P.S1 * WARPS : P.S1;
+    P.nseg = (int)cdiv(sh.nvec, 32);
+    if (P.nseg > TYP_MAX_SEGS) return SPEC_ERR_INVALID_ARG;
+    if ((long long)B * R * P.S1 >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+    const TreeLayout L = tree_layout(B, N, P.np);
+    if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+    P.partials = reinterpret_cast<TypPartial*>(static_cast<char*>(workspace) + L.o_partials);
+    const cudaError_t err = launch_typical_path(P, sm_count(), static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status tree_verify_sample(const void* target_logits, const void* draft_logits,

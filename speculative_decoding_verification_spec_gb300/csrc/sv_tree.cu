@@ -8,7 +8,7 @@
 // re-read that one step to find the first index of the maximum, so ties go to the lowest index.  The warp that completes a
 // request merges the partials of every row in slice order, walks the tree in node order (a node's
 // parent always precedes it), picks the deepest valid node and writes the path and the bonus.
-#include "sv_common.cuh"
+#include "sv_tree_walk.cuh"
 
 namespace sv {
 
@@ -115,100 +115,16 @@ __device__ void tree_finish_request(const TreeParams& P, int b)
                        P.amax + (size_t)b * P.R, depth, depth + P.N);
 }
 
-// One warp: validates the request's tree, finds every node's validity and depth, picks the deepest
-// valid node (lowest index on ties) and writes the outputs.  par / tok are the request's parent
-// and token arrays (par null: a chain, node i's parent is i - 1), am its rows' argmaxes, depth /
-// valid N-int scratch (global or shared memory).
-// bad: 0, 1 (a row is non-finite) or 2 (a row could not be read).
-//
-// Nodes are taken 32 at a time in index order, one per lane.  A node whose parent lies in an
-// earlier group reads the parent's final validity and depth; within a group the values move from
-// parent to child by ballot / shuffle until nothing changes (parents precede children, so this
-// settles after as many rounds as the group's longest chain).
+// One warp: the greedy walk (a node passes when its token is its predictor row's argmax, am[row])
+// and the outputs, with the argmax of the accepted node's own row as the token after the path.
 __device__ void tree_walk_and_emit(const TreeParams& P, int b, int bad, const int32_t* par,
                                    const int32_t* tok, const int32_t* am, int32_t* depth,
                                    int32_t* valid)
 {
-    const int lane = threadIdx.x & 31;
-    const unsigned FULL = 0xffffffffu;
-    const int N = P.N, mo = P.max_out;
-    int32_t* out = P.out_tokens + (size_t)b * mo;
-    int32_t* onodes = P.out_nodes ? P.out_nodes + (size_t)b * (mo - 1) : nullptr;
-    int st = (bad == 2) ? ROW_TIMEOUT : bad ? ROW_NONFINITE : ROW_OK;
-    if (st == ROW_OK) {
-        int badp = 0, badt = 0;
-        for (int i = lane; i < N; i += 32) {
-            const int p = par ? par[i] : i - 1;
-            if (p < -1 || p >= i) badp = 1;
-            const int tk = tok[i];
-            if (tk < 0 || tk >= P.V) badt = 1;
-        }
-        badp = __any_sync(FULL, badp);
-        badt = __any_sync(FULL, badt);
-        st = badp ? ROW_BAD_PARENT : (badt ? ROW_BAD_TOKEN : ROW_OK);
-    }
-    int bestd = 0, bestn = -1;
-    if (st == ROW_OK) {
-        for (int i0 = 0; i0 < N; i0 += 32) {
-            const int i = i0 + lane;
-            const bool in = i < N;
-            const int p = !in ? -1 : par ? par[i] : i - 1;
-            const bool local = p >= i0;  // the parent is in this group
-            const int m = in && tok[i] == am[p < 0 ? 0 : p + 1];
-            int v = 0, dd = 0;
-            if (in && !local) {
-                v = m && (p < 0 || valid[p]);
-                dd = p < 0 ? 1 : depth[p] + 1;
-            }
-            for (int round = 0; round < 32; ++round) {
-                const unsigned vm = __ballot_sync(FULL, v);
-                const int pd = __shfl_sync(FULL, dd, local ? p - i0 : lane);
-                int nv = v, nd = dd;
-                if (in && local) {
-                    nv = m && ((vm >> (p - i0)) & 1u);
-                    nd = pd > 0 ? pd + 1 : 0;
-                }
-                if (!__any_sync(FULL, nv != v || nd != dd)) break;
-                v = nv;
-                dd = nd;
-            }
-            if (in) {
-                valid[i] = v;
-                depth[i] = dd;
-                if (v && dd > bestd) { bestd = dd; bestn = i; }
-            }
-            __syncwarp();
-        }
-        // deepest valid node, lowest index on ties
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const int od = __shfl_xor_sync(FULL, bestd, o);
-            const int on = __shfl_xor_sync(FULL, bestn, o);
-            if (od > bestd || (od == bestd && on >= 0 && (bestn < 0 || on < bestn))) {
-                bestd = od;
-                bestn = on;
-            }
-        }
-        if (bestd + 1 > mo) st = ROW_OVERFLOW;
-    }
-    if (lane == 0) {
-        P.accepted_len[b] = (st == ROW_OK) ? bestd : -1;
-        if (P.row_status) P.row_status[b] = st;
-        if (st == ROW_OK) {  // path written back to front, then the bonus
-            int n = bestd;
-            out[n] = am[bestn < 0 ? 0 : bestn + 1];
-            for (int i = bestn; i >= 0; i = par ? par[i] : i - 1) {
-                --n;
-                out[n] = tok[i];
-                if (onodes) onodes[n] = i;
-            }
-        }
-    }
-    const int A = (st == ROW_OK) ? bestd : -1;
-    for (int i = lane; i < mo; i += 32) {
-        if (st != ROW_OK || i > A) out[i] = -1;
-        if (onodes && i < mo - 1 && (st != ROW_OK || i >= A)) onodes[i] = -1;
-    }
+    const TreeWalk w = tree_walk(P.N, P.V, P.max_out, bad, 0, par, tok,
+                                 [&](int i, int p) { return tok[i] == am[p < 0 ? 0 : p + 1]; },
+                                 depth, valid);
+    tree_emit(P, b, w, par, tok, w.st == ROW_OK ? am[w.node < 0 ? 0 : w.node + 1] : -1);
 }
 
 // End of an argmax task: the lanes holding the warp maximum locate its first index (ties to the

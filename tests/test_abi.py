@@ -126,6 +126,18 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_verify_greedy(fake, 9, fake, 2, 3, 100, fake, fake, None, ws, 1 << 30, None) == INVALID
     assert lib.spec_verify_greedy(fake, 1, fake, 2, 3, 100, fake, fake, None, ws, 16, None) == WORKSPACE
     assert lib.spec_status_string(0) == b"ok"
+    # tree_verify_typical: sizes, temperature, thresholds and pointers
+    def ty_call(B=2, N=4, V=1000, T=1.0, eps=0.09, delta=0.3, par=fake, tok=fake, u=fake, wsp=ws,
+                mo=5):
+        return lib.tree_verify_typical(fake, 1, par, tok, u, B, N, V, F(T), F(eps), F(delta), mo,
+                                       fake, fake, None, None, None, None, wsp, 1 << 30, None)
+
+    assert ty_call(B=0) == 0
+    for bad in (dict(B=-1), dict(N=-1), dict(N=2049), dict(V=0), dict(T=0.0), dict(eps=-1.0),
+                dict(delta=float("inf")), dict(eps=float("nan")), dict(par=None), dict(tok=None),
+                dict(u=None), dict(mo=0), dict(u=P(0x10002))):
+        assert ty_call(**bad) == INVALID, bad
+    assert ty_call(wsp=None) == WORKSPACE
     # spec_verify_masked: the mask is required (B > 0) and 4-byte aligned
     def mk_call(B=2, mask=fake):
         return lib.spec_verify_masked(fake, fake, 1, fake, fake, mask, B, 3, 100, F(1.0), fake, fake,
