@@ -84,6 +84,10 @@ def _bind(lib):
     lib.oracle_ess.restype = D
     lib.oracle_spec_verify_masked.argtypes = [P, P, I, P, P, I, I, I, D, P, P, P, P, P, P, P, P]
     lib.oracle_spec_verify_masked.restype = I
+    lib.oracle_spec_verify_topp.argtypes = [P, P, I, P, P, I, I, I, D, D, P, P, P, P, P, P, P]
+    lib.oracle_spec_verify_topp.restype = I
+    lib.oracle_row_probs_topp.argtypes = [P, I, Z, I, D, D, P, P, P, P]
+    lib.oracle_row_probs_topp.restype = I
     lib.oracle_row_probs.argtypes = [P, I, Z, I, D, I, P, P, P]
     lib.oracle_row_probs.restype = I
     lib.oracle_row_probs_masked.argtypes = [P, I, Z, I, D, I, P, P, P, P]
@@ -125,14 +129,15 @@ def mask_words(V: int) -> int:
 
 
 def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k: int = 0,
-                allowed=None):
+                allowed=None, top_p: float | None = None):
     """Exact speculative-sampling verify over B requests (fp64).
 
     target [B, gamma+1, V], draft [B, gamma, V] (float64, float32, or bf16 bits as uint16),
     draft_tokens [B, gamma] int32, uniforms [B, gamma+2] float32.  ``allowed`` (optional, no
     top-k with it) is the grammar mask [B, gamma+1, ceil(V/32)] uint32: bit v % 32 of word v // 32
-    set when token v is valid at that position.  Returns a dict with accepted_len, out_tokens,
-    row_status, lse_p, lse_q, accept, margin.
+    set when token v is valid at that position.  ``top_p`` (optional, alone) applies the top-p
+    processor to every row.  Returns a dict with accepted_len, out_tokens, row_status, lse_p, lse_q,
+    accept, margin.
     """
     lib = _load()
     t, dt = _logits(target)
@@ -156,7 +161,12 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k
     )
     outs = (_ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["row_status"]),
             _ptr(out["lse_p"]), _ptr(out["lse_q"]), _ptr(out["accept"]), _ptr(out["margin"]))
-    if allowed is None:
+    if top_p is not None:
+        if top_k or allowed is not None:
+            raise ValueError("the top-p oracle takes no top-k or mask")
+        rc = lib.oracle_spec_verify_topp(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V,
+                                         float(temperature), float(top_p), *outs)
+    elif allowed is None:
         rc = lib.oracle_spec_verify(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V,
                                     float(temperature), int(top_k), *outs)
     else:
@@ -350,6 +360,19 @@ def row_probs(logits_row, temperature: float, top_k: int = 0, allowed=None):
         st = lib.oracle_row_probs_masked(_ptr(x), dt, 0, V, float(temperature), int(top_k), _ptr(m),
                                          _ptr(p), ctypes.byref(lse), ctypes.byref(thr))
     return st, p, lse.value, thr.value
+
+
+def row_probs_topp(logits_row, temperature: float, top_p: float):
+    """Processed probability row under temperature and top-p.  Returns (status, p, lse, thr,
+    margin)."""
+    lib = _load()
+    x, dt = _logits(np.asarray(logits_row).reshape(-1))
+    V = x.shape[0]
+    p = np.zeros(V)
+    lse, thr, mg = ctypes.c_double(0.0), ctypes.c_double(0.0), ctypes.c_double(0.0)
+    st = lib.oracle_row_probs_topp(_ptr(x), dt, 0, V, float(temperature), float(top_p), _ptr(p),
+                                   ctypes.byref(lse), ctypes.byref(thr), ctypes.byref(mg))
+    return st, p, lse.value, thr.value, mg.value
 
 
 def lse_online(z, block: int) -> float:

@@ -31,6 +31,8 @@
  *     uniforms outside [0,1) are a bad uniform; such requests emit nothing (-1).
  *   - tree argmax ties go to the lowest token index; the deepest valid node wins, ties to the
  *     lowest node index.
+ *   - top-p keeps whole groups of equal stored logit in descending order until the kept mass (after
+ *     temperature) first reaches top_p, ties with the last group kept included
  *   - typical acceptance (tree): a node passes when p(x) > min(eps, delta exp(-H)) strictly, H the
  *     natural-log entropy of its predictor row after temperature; the token after the accepted
  *     path is drawn from p of the accepted node's own row with the request's one uniform
@@ -154,6 +156,72 @@ int oracle_row_probs(const void* base, int dtype, size_t off, int V, double T, i
     return oracle_row_probs_masked(base, dtype, off, V, T, top_k, NULL, p, lse, thr);
 }
 
+/* (stored logit, probability) pairs, ordered by descending logit */
+typedef struct {
+    double x, p;
+} xp_pair;
+
+static int cmp_pair_desc(const void* a, const void* b)
+{
+    double x = ((const xp_pair*)a)->x, y = ((const xp_pair*)b)->x;
+    return (x < y) - (x > y);
+}
+
+/*
+ * One probability row after temperature and a top-p (nucleus) processor: with p = softmax(x / T),
+ * keep the tokens of largest probability, whole groups of equal stored logit at a time in
+ * descending order, until the kept mass first reaches top_p; every token tied with the last group
+ * kept stays in.  The kept set is {v : x_v >= g}, g that group's logit; p is then renormalised over
+ * it.  top_p >= 1 keeps every token.  *thr receives g (-inf when all are kept) and *margin the
+ * distance between top_p and the two cumulative masses around the chosen group (the decision's
+ * rounding exposure).
+ */
+int oracle_row_probs_topp(const void* base, int dtype, size_t off, int V, double T, double top_p,
+                          double* p, double* lse, double* thr, double* margin)
+{
+    double t = -INFINITY, mg = INFINITY;
+    int st = oracle_row_probs(base, dtype, off, V, T, 0, p, lse, thr);
+    if (st != OR_ROW_OK || !(top_p < 1.0)) {
+        *thr = -INFINITY;
+        *margin = mg;
+        return st;
+    }
+    xp_pair* srt = (xp_pair*)malloc(sizeof(xp_pair) * (size_t)V);
+    for (int v = 0; v < V; ++v) {
+        srt[v].x = load_logit(base, dtype, off + (size_t)v);
+        srt[v].p = p[v];
+    }
+    qsort(srt, (size_t)V, sizeof(xp_pair), cmp_pair_desc);
+    double cum = 0.0;
+    for (int i = 0; i < V;) {
+        const double g = srt[i].x;
+        const double before = cum;
+        while (i < V && srt[i].x == g) cum += srt[i++].p; /* the whole group of equal logits */
+        if (cum >= top_p) {
+            t = g;
+            mg = fmin(fabs(before - top_p), fabs(cum - top_p));
+            break;
+        }
+    }
+    free(srt);
+    /* renormalise over the kept set {x >= t} */
+    double m = -INFINITY, S = 0.0;
+    for (int v = 0; v < V; ++v) {
+        const double x = load_logit(base, dtype, off + (size_t)v);
+        if (x >= t && x / T > m) m = x / T;
+    }
+    for (int v = 0; v < V; ++v) {
+        const double x = load_logit(base, dtype, off + (size_t)v);
+        p[v] = (x >= t && x > -INFINITY) ? exp(x / T - m) : 0.0;
+        S += p[v];
+    }
+    for (int v = 0; v < V; ++v) p[v] /= S;
+    *lse = m + log(S);
+    *thr = t;
+    *margin = mg;
+    return OR_ROW_OK;
+}
+
 /* Backend 2 of [M7.1] 0x04J: an online (m, l) merge over vocabulary blocks of width `block`.
  * Returns the log-normaliser of z[0..n). */
 double oracle_lse_online(const double* z, int n, int block)
@@ -245,9 +313,9 @@ int oracle_inverse_cdf(const double* r, int V, double u, double* lo, double* hi)
  */
 static int spec_verify_impl(const void* target, const void* draft, int dtype, const int32_t* tokens,
                             const float* uniforms, int B, int gamma, int V, double T, int top_k,
-                            const uint32_t* allowed, int32_t* accepted_len, int32_t* out_tokens,
-                            int32_t* row_status, double* lse_p, double* lse_q, double* accept,
-                            double* margin)
+                            const uint32_t* allowed, double top_p, int32_t* accepted_len,
+                            int32_t* out_tokens, int32_t* row_status, double* lse_p,
+                            double* lse_q, double* accept, double* margin)
 {
     if (B < 0 || gamma < 0 || V < 1 || !(T > 0.0)) return 1;
     const size_t W = (size_t)(V + 31) / 32; /* mask words per position */
@@ -256,12 +324,15 @@ static int spec_verify_impl(const void* target, const void* draft, int dtype, co
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     for (int b = 0; b < B; ++b) {
         int st = OR_ROW_OK;
-        double thr;
+        double thr, rmg = INFINITY, rm;
         for (int i = 0; i <= gamma; ++i) {
             double l = NAN;
             size_t off = ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * (size_t)V;
             const uint32_t* m = allowed ? allowed + ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * W : NULL;
-            int s = oracle_row_probs_masked(target, dtype, off, V, T, top_k, m, p + (size_t)i * V, &l, &thr);
+            int s = top_p < 1.0
+                        ? oracle_row_probs_topp(target, dtype, off, V, T, top_p, p + (size_t)i * V, &l, &thr, &rm)
+                        : oracle_row_probs_masked(target, dtype, off, V, T, top_k, m, p + (size_t)i * V, &l, &thr);
+            if (top_p < 1.0 && rm < rmg) rmg = rm;
             if (s != OR_ROW_OK) st = OR_ROW_NONFINITE;
             if (lse_p) lse_p[(size_t)b * (gamma + 1) + i] = l;
         }
@@ -270,7 +341,10 @@ static int spec_verify_impl(const void* target, const void* draft, int dtype, co
             size_t off = ((size_t)b * (size_t)gamma + (size_t)i) * (size_t)V;
             /* the draft row of position i sampled under the same grammar state as target row i */
             const uint32_t* m = allowed ? allowed + ((size_t)b * (size_t)(gamma + 1) + (size_t)i) * W : NULL;
-            int s = oracle_row_probs_masked(draft, dtype, off, V, T, top_k, m, q + (size_t)i * V, &l, &thr);
+            int s = top_p < 1.0
+                        ? oracle_row_probs_topp(draft, dtype, off, V, T, top_p, q + (size_t)i * V, &l, &thr, &rm)
+                        : oracle_row_probs_masked(draft, dtype, off, V, T, top_k, m, q + (size_t)i * V, &l, &thr);
+            if (top_p < 1.0 && rm < rmg) rmg = rm;
             if (s != OR_ROW_OK) st = OR_ROW_NONFINITE;
             if (lse_q) lse_q[(size_t)b * gamma + i] = l;
         }
@@ -297,7 +371,7 @@ static int spec_verify_impl(const void* target, const void* draft, int dtype, co
 
         int32_t* out = out_tokens + (size_t)b * (gamma + 1);
         for (int i = 0; i <= gamma; ++i) out[i] = -1;
-        double mg = INFINITY;
+        double mg = rmg; /* top-p: how close a row's kept set came to changing */
         int A = -1;
         if (st == OR_ROW_OK) {
             /* first rejection ([M7.1] 0x03G) */
@@ -349,6 +423,23 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, const i
                        double* lse_p, double* lse_q, double* accept, double* margin)
 {
     return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, top_k, NULL,
+                            2.0, accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
+}
+
+/*
+ * The verify round with a top-p (nucleus) processor on every target and draft row after temperature
+ * (oracle_row_probs_topp; "Exact speculative and assisted decoding for TinyRustLM": top-p is one of
+ * the declared processors both distributions pass through; M7.1 0x03D: truncation keeps exactness
+ * when q is the truncated distribution that sampled the draft).  0 < top_p; top_p >= 1 is the plain
+ * round.  margin[b] also covers each row's kept-set decision.  Everything else as oracle_spec_verify.
+ */
+int oracle_spec_verify_topp(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                            const float* uniforms, int B, int gamma, int V, double T, double top_p,
+                            int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                            double* lse_p, double* lse_q, double* accept, double* margin)
+{
+    if (!(top_p > 0.0)) return 1;
+    return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, 0, NULL, top_p,
                             accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
 }
 
@@ -367,7 +458,7 @@ int oracle_spec_verify_masked(const void* target, const void* draft, int dtype,
                               double* lse_q, double* accept, double* margin)
 {
     if (!allowed) return 1;
-    return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, 0, allowed,
+    return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, 0, allowed, 2.0,
                             accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
 }
 

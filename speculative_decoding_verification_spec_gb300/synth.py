@@ -34,6 +34,9 @@ Workload recipes (five named configurations):
   c10 B=32  N=64    V=128256 bf16  T=0.7  typical-acceptance tree verify: c5's recipe (tree, logits,
                                           tokens); eps = 0.09, delta = 0.3; one uniform per
                                           request for the token after the path
+  c11 B=64  gamma=5 V=128256 bf16 T=0.8  top-p verify, top_p = 0.9 on every row: c2's target recipe
+                                          (20 peak tokens per row +8) at c3's sizes, draft noise
+                                          N(0,1^2); draft tokens from the draft's own nucleus
   c7  G=8 x N=8 particles, K=5, V=128256 bf16, T=0.7, eta = N/2: one SMC-SD round; logits as
                                           c3 (target, draft = 0.8*target + N(0,1.5^2)), draft
                                           tokens from q, incoming log weights N(0, 0.5^2),
@@ -70,6 +73,7 @@ class SpecConfig:
     draft_noise: float
     seed: int
     mask: str = ""      # "" = no grammar mask; "grammar" = the mixed valid-set recipe (c9)
+    top_p: float = 1.0  # < 1: the top-p processor on every row (c11)
 
 
 @dataclass(frozen=True)
@@ -94,6 +98,9 @@ CONFIGS = {
     "c2": SpecConfig("c2", 8, 4, 32000, "bf16", 1.0, 0, "peaks", 1.0, 1.0, 1002),
     "c3": SpecConfig("c3", 64, 5, 128256, "bf16", 0.7, 0, "zipf", 0.8, 1.5, 1003),
     "c4": SpecConfig("c4", 256, 7, 152064, "bf16", 0.8, 50, "peaks", 1.0, 2.0, 1004),
+}
+TOPP_CONFIGS = {
+    "c11": SpecConfig("c11", 64, 5, 128256, "bf16", 0.8, 0, "peaks", 1.0, 1.0, 1011, top_p=0.9),
 }
 MASK_CONFIGS = {
     "c9": SpecConfig("c9", 64, 5, 128256, "bf16", 0.7, 0, "zipf", 0.8, 1.5, 1009, mask="grammar"),
@@ -255,6 +262,27 @@ def unpack_valid_sets(words: np.ndarray, V: int) -> np.ndarray:
     return np.unpackbits(by, axis=-1, bitorder="little")[..., :V].astype(bool)
 
 
+def draft_nucleus_mask(x: np.ndarray, temperature: float, top_p: float) -> np.ndarray | None:
+    """The draft sampler's own top-p set per row of stored logits x [..., V]: the tokens of largest
+    logit, whole groups of equal logit at a time, until the mass of softmax(x / T) they hold first
+    reaches top_p (the proposal side's processor, so that draft tokens are draws from it)."""
+    if not top_p < 1.0:
+        return None
+    flat = x.reshape(-1, x.shape[-1])
+    keep = np.zeros(flat.shape, dtype=bool)
+    for r, row in enumerate(flat):
+        z = row / temperature
+        w = np.exp(z - z.max())
+        w /= w.sum()
+        vals, inv = np.unique(row, return_inverse=True)       # ascending distinct logits
+        mass = np.bincount(inv, weights=w, minlength=vals.size)[::-1]  # descending
+        cum = np.cumsum(mass)
+        j = int(np.searchsorted(cum, top_p, side="left"))
+        g = vals[::-1][min(j, vals.size - 1)]
+        keep[r] = row >= g
+    return keep.reshape(x.shape)
+
+
 def _nthreads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
@@ -304,6 +332,8 @@ def make_spec_batch(cfg: SpecConfig, *, threads: int | None = None) -> SpecBatch
         draft[b] = _store(d32, cfg.dtype)
         xd = stored_to_f64(draft[b])
         keep = draft_keep_mask(xd, cfg.top_k)
+        if cfg.top_p < 1.0:
+            keep = draft_nucleus_mask(xd, cfg.temperature, cfg.top_p)
         if cfg.mask:
             valid = grammar_valid_sets(np.random.Generator(np.random.PCG64(req_mask[b])), g + 1, V)
             allowed[b] = pack_valid_sets(valid)
