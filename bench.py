@@ -11,7 +11,8 @@ follows an L2 flush outside the call's events and its rates come from the per-ca
 c7 is one SMC-SD round through smc_verify (8 groups x 8 particles, K=5, V=128256 bf16, T=0.7);
 c8 linear greedy verify through spec_verify_greedy (B=64 gamma=5 V=128256 bf16); c9 grammar-masked
 verify through spec_verify_masked (c3's logits with a valid-token set per position); c10 tree verify
-by typical acceptance through tree_verify_typical (c5's tree and logits, T=0.7, eps=0.09, delta=0.3).
+by typical acceptance through tree_verify_typical (c5's tree and logits, T=0.7, eps=0.09, delta=0.3);
+c11 top-p verify through spec_verify_topp (B=64 gamma=5 V=128256 bf16, T=0.8, top_p=0.9).
 
 value     logit rows per second, inputs resident in HBM (whole job, all ranks)
 e2e       the same metric through the C ABI with host buffers: pinned host -> device copies of
@@ -56,6 +57,7 @@ KERNEL_OF = {
     "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c8": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
     "c9": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c11": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c10": ("typical_stream_kernel", ["sv_typical.cu", "sv_typical.cuh", "sv_tree_walk.cuh",
                                       "sv_common.cuh", "sv_plan.cuh"]),
 }
@@ -68,13 +70,13 @@ def workload_batches(names, rank, requests=None):
     from speculative_decoding_verification_spec_gb300 import synth as S
     out = {}
     for n in names:
-        cfg = (S.CONFIGS.get(n) or S.MASK_CONFIGS.get(n) or S.TREE_CONFIGS.get(n)
-               or S.SAMPLE_TREE_CONFIGS.get(n) or S.SMC_CONFIGS[n])
+        cfg = (S.CONFIGS.get(n) or S.MASK_CONFIGS.get(n) or S.TOPP_CONFIGS.get(n)
+               or S.TREE_CONFIGS.get(n) or S.SAMPLE_TREE_CONFIGS.get(n) or S.SMC_CONFIGS[n])
         kw = dict(seed=rank_seed(cfg, rank))
         if requests:
             kw["groups" if n in S.SMC_CONFIGS else "B"] = requests
         cfg = S.scaled(cfg, **kw)
-        if n in S.CONFIGS or n in S.MASK_CONFIGS:
+        if n in S.CONFIGS or n in S.MASK_CONFIGS or n in S.TOPP_CONFIGS:
             out[n] = S.make_spec_batch(cfg)
         elif n in S.TREE_CONFIGS:
             out[n] = S.make_tree_batch(cfg)
@@ -136,7 +138,11 @@ def describe(names):
     from speculative_decoding_verification_spec_gb300 import synth as S
     parts = []
     for n in names:
-        if n in S.MASK_CONFIGS:
+        if n in S.TOPP_CONFIGS:
+            c = S.TOPP_CONFIGS[n]
+            parts.append(f"{n} spec_verify_topp B={c.B} gamma={c.gamma} V={c.V} {c.dtype} "
+                         f"T={c.temperature} top_p={c.top_p}")
+        elif n in S.MASK_CONFIGS:
             c = S.MASK_CONFIGS[n]
             parts.append(f"{n} spec_verify_masked B={c.B} gamma={c.gamma} V={c.V} {c.dtype} "
                          f"T={c.temperature} grammar valid sets per position (narrow 64 tokens / "
@@ -307,7 +313,8 @@ def cpu_baseline(names, budget_s=15.0):
             else:
                 O.spec_verify(b.target[i:i + 1], b.draft[i:i + 1], b.draft_tokens[i:i + 1],
                               b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k,
-                              allowed=None if b.allowed is None else b.allowed[i:i + 1])
+                              allowed=None if b.allowed is None else b.allowed[i:i + 1],
+                              top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None)
                 rows_done += 2 * b.cfg.gamma + 1
             t_used += time.perf_counter() - t0
             i += 1
@@ -384,6 +391,7 @@ def run_ours(args, rank, world, local_rank):
                                          workspace=wss[n], stream=stream)
         return sv.spec_verify(ins["target"], ins["draft"], ins["tokens"], ins["uniforms"],
                               b.cfg.temperature, top_k=b.cfg.top_k, allowed=ins.get("allowed"),
+                              top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None,
                               out=out, workspace=wss[n], stream=stream)
 
     for n in names:  # allocate outputs once
@@ -607,7 +615,8 @@ def run_reference(args, rank, world):
                 j = (i // len(names)) % b.cfg.B
                 O.spec_verify(b.target[j:j + 1], b.draft[j:j + 1], b.draft_tokens[j:j + 1],
                               b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.top_k,
-                              allowed=None if b.allowed is None else b.allowed[j:j + 1])
+                              allowed=None if b.allowed is None else b.allowed[j:j + 1],
+                              top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None)
                 rows += 2 * b.cfg.gamma + 1
         return rows
 
@@ -639,7 +648,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["suite", "c1", "c2", "c3", "c4", "c5", "c6", "c7", "c8",
-                                           "c9", "c10"],
+                                           "c9", "c10", "c11"],
                     default="suite")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

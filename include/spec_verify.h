@@ -7,6 +7,7 @@
  *   spec_verify        exact speculative sampling with temperature
  *   spec_verify_topk   the same with a top-k processor applied identically to target and draft
  *   spec_verify_masked the same with a grammar mask (a valid-token set per position)
+ *   spec_verify_topp   the same with a top-p (nucleus) processor applied identically to target and draft
  *   tree_verify_greedy Medusa-style greedy verification of a candidate tree
  *   spec_verify_greedy linear greedy verification of a draft (the greedy tree on a chain)
  *   tree_verify_sample stochastic verification of a candidate tree (residual update over children)
@@ -88,6 +89,7 @@ enum {
  *   spec_verify:        spec_workspace_bytes(B, gamma, V, 0, 0)
  *   spec_verify_topk:   spec_workspace_bytes(B, gamma, V, top_k, 0)
  *   spec_verify_masked: spec_workspace_bytes(B, gamma, V, 0, 0)   (as spec_verify)
+ *   spec_verify_topp:   spec_workspace_bytes(B, gamma, V, 0, 0)   (as spec_verify)
  *   tree_verify_greedy: spec_workspace_bytes(B, 0, V, 0, N)   (tree_nodes = N > 0)
  *   tree_verify_typical: spec_workspace_bytes(B, 0, V, 0, N)  (as tree_verify_greedy)
  * The value is an upper bound valid for both dtypes, any alignment and any GPU.
@@ -136,6 +138,27 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits, spe
 spec_status spec_verify_topk(const void* target_logits, const void* draft_logits, spec_dtype dtype,
                              const int32_t* draft_tokens, const float* uniforms,
                              int B, int gamma, int V, float temperature, int top_k,
+                             int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
+                             float* aux_lse_p, float* aux_lse_q, float* aux_accept,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify with a top-p (nucleus) processor on every target and draft row ("Exact speculative
+ * and assisted decoding for TinyRustLM": top-p is one of the declared processors both distributions
+ * pass through before the ratio is formed; M7.1 0x03D: truncation keeps the round exact when q is
+ * the truncated distribution that sampled the draft).  With p = softmax(logits / temperature), a row
+ * keeps the tokens of largest probability, whole groups of equal stored logit at a time in
+ * descending order, until the kept mass first reaches top_p; every token tied with the last group
+ * kept stays in.  The kept set is {v : logit_v >= g} and p is renormalised over it; the same rule
+ * applies to each draft row.  top_p > 0; top_p >= 1 is exactly spec_verify.  The kept mass is
+ * summed in fixed point (2^-40 of the row maximum's mass per unit), so a row whose cumulative mass
+ * lies within about 1e-7 of top_p may keep one group more or less than an exact computation would.
+ * A drafted token outside its draft row's kept set is SPEC_ROW_BAD_TOKEN.  Other arguments, outputs
+ * and statuses as spec_verify.
+ */
+spec_status spec_verify_topp(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                             const int32_t* draft_tokens, const float* uniforms,
+                             int B, int gamma, int V, float temperature, float top_p,
                              int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
                              float* aux_lse_p, float* aux_lse_q, float* aux_accept,
                              void* workspace, size_t workspace_bytes, void* stream);

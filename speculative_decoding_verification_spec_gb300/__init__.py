@@ -1,5 +1,5 @@
-"""GB300 (sm_103a) speculative-decoding verify step: exact speculative sampling, its top-k and
-grammar-mask variants, greedy and typical-acceptance tree verify, stochastic tree verify and the verify side of an SMC-SD round, as hand-written CUDA behind a C ABI (include/spec_verify.h).
+"""GB300 (sm_103a) speculative-decoding verify step: exact speculative sampling, its top-k, top-p
+and grammar-mask variants, greedy and typical-acceptance tree verify, stochastic tree verify and the verify side of an SMC-SD round, as hand-written CUDA behind a C ABI (include/spec_verify.h).
 
 The binding functions load the compiled library on first use and raise if it is missing: there is
 no CPU fallback.
@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     spec_verify_masked,
     spec_verify_noalloc,
     spec_verify_topk,
+    spec_verify_topp,
     tree_verify_greedy,
     tree_verify_sample,
     tree_verify_typical,

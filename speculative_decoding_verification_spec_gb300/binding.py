@@ -18,7 +18,8 @@ ROW_OK, ROW_NONFINITE, ROW_DEGENERATE, ROW_BAD_TOKEN, ROW_TIMEOUT = 0, 1, 2, 3, 
 ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 
 # every symbol the header declares
-EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "spec_verify_masked",
+EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "spec_verify_topp",
+           "spec_verify_masked",
            "tree_verify_greedy", "spec_verify_greedy",
            "tree_verify_sample", "tree_verify_typical", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
 
@@ -50,6 +51,8 @@ def load(path: str | None = None):
     lib.spec_verify.restype = I
     lib.spec_verify_topk.argtypes = [P, P, I, P, P, I, I, I, F, I, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_topk.restype = I
+    lib.spec_verify_topp.argtypes = [P, P, I, P, P, I, I, I, F, F, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_topp.restype = I
     lib.spec_verify_masked.argtypes = [P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_masked.restype = I
     lib.tree_verify_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
@@ -143,14 +146,15 @@ def workspace_bytes(B, gamma, V, top_k=0, tree_nodes=0) -> int:
 
 
 def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, top_k: int = 0,
-                allowed=None, aux: bool = False, out=None, workspace: Workspace | None = None,
-                stream=None):
+                allowed=None, top_p: float | None = None, aux: bool = False, out=None,
+                workspace: Workspace | None = None, stream=None):
     """Exact speculative-sampling verify on the GPU.
 
     target [B, gamma+1, V], draft [B, gamma, V] (bf16 / int16 bf16 bits / fp32, CUDA),
     draft_tokens [B, gamma] int32, uniforms [B, gamma+2] fp32.  ``top_k`` > 0 applies the top-k
     processor (spec_verify_topk).  ``allowed`` (CUDA int32/uint32 [B, gamma+1, ceil(V/32)]) is a
-    grammar mask (spec_verify_masked; not with top_k).  Returns a dict of CUDA tensors:
+    grammar mask (spec_verify_masked; not with top_k); ``top_p`` applies the top-p processor
+    (spec_verify_topp; alone).  Returns a dict of CUDA tensors:
     accepted_len, out_tokens, row_status (and lse_p, lse_q, accept when ``aux``).
     """
     lib = load()
@@ -175,7 +179,11 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, to
     tail = [_ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out.get("row_status")),
             _ptr(out.get("lse_p")), _ptr(out.get("lse_q")), _ptr(out.get("accept")),
             _ptr(ws), ws.numel(), _stream(stream)]
-    if allowed is not None:
+    if top_p is not None:
+        if top_k or allowed is not None:
+            raise ValueError("spec_verify_topp takes no top_k or mask")
+        rc = lib.spec_verify_topp(*common, float(top_p), *tail)
+    elif allowed is not None:
         if top_k:
             raise ValueError("spec_verify_masked takes no top_k")
         _need_cuda(allowed)
@@ -190,6 +198,11 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, *, to
         rc = lib.spec_verify(*common, *tail)
     _check(rc)
     return out
+
+
+def spec_verify_topp(target, draft, draft_tokens, uniforms, temperature: float, top_p: float, **kw):
+    """spec_verify with the top-p (nucleus) processor on every row."""
+    return spec_verify(target, draft, draft_tokens, uniforms, temperature, top_p=top_p, **kw)
 
 
 def spec_verify_masked(target, draft, draft_tokens, uniforms, allowed, temperature: float, **kw):

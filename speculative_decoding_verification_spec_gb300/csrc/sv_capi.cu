@@ -184,7 +184,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
                                int32_t* out_tokens, int32_t* row_status, float* aux_lse_p,
                                float* aux_lse_q, float* aux_accept, void* workspace,
                                size_t workspace_bytes, void* stream, const SmcArgs* smc = nullptr,
-                               const uint32_t* allowed = nullptr)
+                               const uint32_t* allowed = nullptr, float top_p = 1.0f)
 {
     if (B < 0 || gamma < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
@@ -208,6 +208,9 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
         return SPEC_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 16)) return SPEC_ERR_WORKSPACE;
     if (allowed && (!aligned(allowed, 4) || top_k != 0 || smc)) return SPEC_ERR_INVALID_ARG;
+    if (!(top_p > 0.0f) || std::isnan(top_p)) return SPEC_ERR_INVALID_ARG;
+    const bool topp = top_p < 1.0f;
+    if (topp && (top_k != 0 || allowed || smc)) return SPEC_ERR_INVALID_ARG;
 
     const bool topk = top_k > 0 && top_k < V;
     const int dt = (dtype == SPEC_BF16) ? DT_BF16 : DT_F32;
@@ -257,6 +260,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.aux_accept = aux_accept;
     P.mask = allowed;
     P.mwords = (int)cdiv(V, 32);
+    P.top_p = topp ? top_p : 1.0f;
     if (smc) {
         P.smc = 1;
         P.smc_logw_in = smc->logw_in;
@@ -291,7 +295,9 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
         return SPEC_ERR_CUDA;
     }
     cudaError_t err;
-    if (!topk) {
+    if (topp) {
+        err = launch_topp_path(P, sms, st);
+    } else if (!topk) {
         err = launch_softmax_path(P, sms, st);
     } else {
         err = launch_topk_path(P, sms, st);
@@ -361,6 +367,20 @@ spec_status spec_verify_topk(const void* target_logits, const void* draft_logits
     return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
                        temperature, top_k, accepted_len, out_tokens, row_status, aux_lse_p,
                        aux_lse_q, aux_accept, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_verify_topp(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                             const int32_t* draft_tokens, const float* uniforms, int B, int gamma,
+                             int V, float temperature, float top_p, int32_t* accepted_len,
+                             int32_t* out_tokens, int32_t* row_status, float* aux_lse_p,
+                             float* aux_lse_q, float* aux_accept, void* workspace,
+                             size_t workspace_bytes, void* stream)
+{
+    if (!(top_p > 0.0f) || std::isnan(top_p)) return SPEC_ERR_INVALID_ARG;
+    if ((long long)B * (2 * (long long)gamma + 1) >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+    return spec_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma, V,
+                       temperature, 0, accepted_len, out_tokens, row_status, aux_lse_p, aux_lse_q,
+                       aux_accept, workspace, workspace_bytes, stream, nullptr, nullptr, top_p);
 }
 
 spec_status spec_verify_masked(const void* target_logits, const void* draft_logits, spec_dtype dtype,

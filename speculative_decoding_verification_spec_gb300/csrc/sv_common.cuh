@@ -88,6 +88,7 @@ constexpr int U1 = 8, ST1 = 4, TV1 = 32 * U1 * ST1;  // row statistics / argmax:
 constexpr int U2 = 4, ST2 = 4, TV2 = 32 * U2 * ST2;  // residual pass over a row pair: 512 vectors
 constexpr int RCV = 8;  // residual pass over 16-byte vectors: vectors per row and thread of one CTA
 constexpr int SEGV = 32;                             // vectors per residual segment
+enum { RES_PLAIN = 0, RES_MASK = 1, RES_THR = 2 };   // residual pass variants
 
 struct SpecParams {
     const void* target;   // [B, gamma+1, V]
@@ -148,6 +149,7 @@ struct SpecParams {
     // per 32 tokens (bit v % 32 of word v / 32); position i masks target row i and draft row i
     const uint32_t* mask;
     int mwords;
+    float top_p;          // top-p processor (spec_verify_topp): < 1 keeps each row's nucleus
 };
 
 struct TreeParams {
@@ -810,6 +812,11 @@ inline void mark_kernel_stop(cudaStream_t st)
 
 // spec_stats_kernel + spec_resample_kernel for the dtype / vector width in P
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st);
+// the plain path's row statistics alone, and its correction draw with top-p thresholds
+cudaError_t launch_softmax_stats(const SpecParams& P, int sms, cudaStream_t st);
+cudaError_t launch_softmax_resample_thr(const SpecParams& P, int sms, cudaStream_t st);
+// top-p: statistics, per-row threshold select and plan, thresholded draw
+cudaError_t launch_topp_path(const SpecParams& P, int sms, cudaStream_t st);
 // topk_stream_kernel + topk_finish_kernel + topk_dense_kernel
 cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st);
 // tree_argmax_kernel

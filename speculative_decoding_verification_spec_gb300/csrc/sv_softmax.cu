@@ -589,6 +589,20 @@ __global__ void __launch_bounds__(PLAN_WARPS * 32) spec_rowplan_kernel(SpecParam
 
 // ---------------------------------------------------------------- kernel 2: residual draw
 
+// Top-p: a row keeps the tokens whose stored logit is >= its threshold (pl.thrp for the p row,
+// pl.thrq for the q row); the rest become -inf.  The plain and masked paths carry -inf thresholds,
+// for which this changes nothing.
+template <int VEC>
+__device__ __forceinline__ void apply_thresholds(float (&xp)[VEC], float (&xq)[VEC], bool has_q,
+                                                 const Plan& pl)
+{
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        if (!(xp[e] >= pl.thrp)) xp[e] = NEG_INF;
+        if (has_q && !(xq[e] >= pl.thrq)) xq[e] = NEG_INF;
+    }
+}
+
 // residual mass of one vector from already-loaded values (bit-identical wherever recomputed)
 template <int VEC>
 __device__ __forceinline__ void residual_from(const float (&xp)[VEC], const float (&xq)[VEC],
@@ -634,6 +648,7 @@ __device__ int resolve_in_segment(const SpecParams& P, const char* rowp, const c
             mask_vals<VEC>(xp, bits);
             mask_vals<VEC>(xq, bits);
         }
+        apply_thresholds<VEC>(xp, xq, rowq != nullptr, pl);
         residual_from<VEC>(xp, xq, rowq != nullptr, pl, P.c, r);
     }
     const float tl = (float)t_local;
@@ -809,6 +824,7 @@ __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
                         float a[VEC], q[VEC], r[VEC];
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) { a[e] = xp[u].get(e); q[e] = xq[u].get(e); }
+                        apply_thresholds<VEC>(a, q, rowq != nullptr, pl);
                         residual_from<VEC>(a, q, rowq != nullptr, pl, P.c, r);
                         ls = tree_sum(r);
                     }
@@ -835,7 +851,8 @@ __global__ void __launch_bounds__(NT) spec_resample_kernel(SpecParams P)
 // the token.
 constexpr int RCHUNK = NT * RCV;
 
-template <int DT, bool MASK>
+// MODE: RES_PLAIN, RES_MASK (grammar mask applied to both rows) or RES_THR (top-p thresholds)
+template <int DT, int MODE>
 __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
@@ -862,7 +879,7 @@ __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
                 if (v < c1) {
                     a[u].load(rowp, v, pol);
                     if (rowq) q[u].load(rowq, v, pol);
-                    if constexpr (MASK) {
+                    if constexpr (MODE == RES_MASK) {
                         const uint32_t bits = allowed_bits<VEC>(spec_mask_row(P, b, pl.rp), v);
                         mask_raw<DT, VEC>(a[u].w, bits);
                         mask_raw<DT, VEC>(q[u].w, bits);
@@ -878,6 +895,7 @@ __global__ void __launch_bounds__(NT) spec_resample_chunk_kernel(SpecParams P)
                     float xp[VEC], xq[VEC], rv[VEC];
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) { xp[e] = a[u].get(e); xq[e] = q[u].get(e); }
+                    if constexpr (MODE == RES_THR) apply_thresholds<VEC>(xp, xq, rowq != nullptr, pl);
                     residual_from<VEC>(xp, xq, rowq != nullptr, pl, P.c, rv);
                     ls = tree_sum(rv);
                 }
@@ -915,7 +933,47 @@ static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
     mark_kernel_stop(st);
     const int pw = (P.R <= 32) ? std::min(P.R, PLAN_WARPS) : WARPS;
     launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, (unsigned)(32 * pw), 0, st, P);
-    launch_dependent(spec_resample_chunk_kernel<DT, MASK>, (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
+    launch_dependent(spec_resample_chunk_kernel<DT, MASK ? RES_MASK : RES_PLAIN>,
+                     (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
+}
+
+// Kernel 1 alone (the row statistics): the top-p path's first step.  The scalar variant also forms a
+// plan, which the top-p kernels replace.
+cudaError_t launch_softmax_stats(const SpecParams& P, int sms, cudaStream_t st)
+{
+    mark_kernel_start(st);
+    if (P.vec > 1) {
+        if (P.dtype == DT_BF16) {
+            constexpr auto K1 = spec_stream_kernel<DT_BF16, false>;
+            K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
+        } else {
+            constexpr auto K1 = spec_stream_kernel<DT_F32, false>;
+            K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
+        }
+    } else if (P.dtype == DT_BF16) {
+        spec_stats_kernel<DT_BF16, 1><<<persistent_grid<spec_stats_kernel<DT_BF16, 1>>(P.tasks1, sms), NT, 0, st>>>(P);
+    } else {
+        spec_stats_kernel<DT_F32, 1><<<persistent_grid<spec_stats_kernel<DT_F32, 1>>(P.tasks1, sms), NT, 0, st>>>(P);
+    }
+    mark_kernel_stop(st);
+    return cudaGetLastError();
+}
+
+// Kernel 2 with the plan's top-p thresholds: the correction or bonus draw of the top-p path.
+cudaError_t launch_softmax_resample_thr(const SpecParams& P, int sms, cudaStream_t st)
+{
+    if (P.vec > 1) {
+        if (P.dtype == DT_BF16)
+            return launch_dependent(spec_resample_chunk_kernel<DT_BF16, RES_THR>,
+                                    (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
+        return launch_dependent(spec_resample_chunk_kernel<DT_F32, RES_THR>,
+                                (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
+    }
+    if (P.dtype == DT_BF16)
+        spec_resample_kernel<DT_BF16, 1><<<persistent_grid<spec_resample_kernel<DT_BF16, 1>>(P.tasks2, sms), NT, 0, st>>>(P);
+    else
+        spec_resample_kernel<DT_F32, 1><<<persistent_grid<spec_resample_kernel<DT_F32, 1>>(P.tasks2, sms), NT, 0, st>>>(P);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st)

@@ -138,6 +138,14 @@ def test_host_validation_without_gpu(lib):
                 dict(u=None), dict(mo=0), dict(u=P(0x10002))):
         assert ty_call(**bad) == INVALID, bad
     assert ty_call(wsp=None) == WORKSPACE
+    # spec_verify_topp: top_p > 0 and not NaN
+    def tp_call(B=2, top_p=0.9):
+        return lib.spec_verify_topp(fake, fake, 1, fake, fake, B, 3, 100, F(1.0), F(top_p), fake,
+                                    fake, None, None, None, None, ws, 1 << 30, None)
+
+    assert tp_call(B=0) == 0
+    for bad in (dict(top_p=0.0), dict(top_p=-0.5), dict(top_p=float("nan")), dict(B=-1)):
+        assert tp_call(**bad) == INVALID, bad
     # spec_verify_masked: the mask is required (B > 0) and 4-byte aligned
     def mk_call(B=2, mask=fake):
         return lib.spec_verify_masked(fake, fake, 1, fake, fake, mask, B, 3, 100, F(1.0), fake, fake,
