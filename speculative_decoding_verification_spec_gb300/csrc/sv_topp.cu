@@ -11,11 +11,12 @@
 // Kernel 2 (topp_row_kernel), one CTA per row: the row's M, MC and full mass, then g by a
 // mass-weighted radix select over the order-preserving key of the stored logits (16-bit for bf16,
 // 32-bit for fp32), four bits per pass over the row.  Each pass adds the fixed-point mass
-// round(2^40 * 2^y), y = x c - MC, of every element whose key matches the digits chosen so far to
-// the thread's own bin of its next digit (integer sums: exact and order-free, so g does not depend
-// on scheduling); the digit is where the mass above it first reaches top_p * (total).  The kept
-// mass is the select's own sum above g.  The row's lse, 1/S and log2 p(x) of the token it scores
-// are then formed as on the plain path; the last CTA of a request runs the acceptance scan.
+// 2^40 * 2^y (rounded toward zero), y = x c - MC, of every element whose key matches the digits
+// chosen so far to the thread's own bin of its next digit (integer sums: exact and order-free, so
+// g does not depend on scheduling); the digit is where the mass above it first reaches
+// top_p * (total).  The kept mass is the select's own sum above g.  The row's lse, 1/S and
+// log2 p(x) of the token it scores are then formed as on the plain path; the last CTA of a request
+// runs the acceptance scan.
 // Kernel 3: the plain path's residual pass with each row's threshold applied.
 #include "sv_plan.cuh"
 
@@ -34,7 +35,17 @@ __device__ __forceinline__ float key_float(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
-constexpr float TOPP_FIX = 1099511627776.0f;  // 2^40: fixed-point scale of one element's mass
+// The fixed-point mass 2^40 w (rounded toward zero) of w in [0, 1], from the float's bits with
+// integer operations only (a conversion to a 64-bit integer is not a fast-pipe instruction).
+__device__ __forceinline__ unsigned long long fixed_mass(float w)
+{
+    const uint32_t u = __float_as_uint(w);
+    const int e = (int)(u >> 23);  // biased exponent; w >= 0
+    if (e == 0) return 0ull;       // zero (the exponential flushes subnormals)
+    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
+    const int sh = e - 127 - 23 + 40;  // 2^40 w = m 2^sh, sh <= 17
+    return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0ull);
+}
 
 template <int DT, int VEC>
 __global__ void __launch_bounds__(NT) topp_row_kernel(SpecParams P)
@@ -99,6 +110,10 @@ __global__ void __launch_bounds__(NT) topp_row_kernel(SpecParams P)
             const uint32_t prefix = sh_prefix;
 #pragma unroll
             for (int d = 0; d < 16; ++d) hist[d * NT + tid] = 0ull;
+            // consecutive elements of a thread mostly share a digit: their masses are added in a
+            // register and reach the thread's bin when the digit changes
+            unsigned long long run = 0ull;
+            int cur = 0;
             for (long long v = tid; v < P.nvec; v += NT) {
                 float x[VEC];
                 load_vec<DT, VEC>(row, v, x);
@@ -106,11 +121,19 @@ __global__ void __launch_bounds__(NT) topp_row_kernel(SpecParams P)
                 for (int e = 0; e < VEC; ++e) {
                     const uint32_t key = order_key(x[e]);
                     if (lvl == 0 || (key >> (shift + 4)) == prefix) {
-                        const float w = ex2(fmaf(x[e], P.c, -MC));
-                        hist[((key >> shift) & 15u) * NT + tid] += __float2ull_rn(__fmul_rn(w, TOPP_FIX));
+                        const int d = (int)((key >> shift) & 15u);
+                        const unsigned long long fx = fixed_mass(ex2(fmaf(x[e], P.c, -MC)));
+                        if (d != cur) {
+                            hist[cur * NT + tid] += run;
+                            cur = d;
+                            run = fx;
+                        } else {
+                            run += fx;
+                        }
                     }
                 }
             }
+            hist[cur * NT + tid] += run;
             __syncthreads();
             // digit totals: warp w adds the columns of digits 2w and 2w + 1
             for (int d = 2 * warp; d < 2 * warp + 2; ++d) {
