@@ -84,7 +84,7 @@ def _bind(lib):
     lib.oracle_ess.restype = D
     lib.oracle_spec_verify_masked.argtypes = [P, P, I, P, P, I, I, I, D, P, P, P, P, P, P, P, P]
     lib.oracle_spec_verify_masked.restype = I
-    lib.oracle_spec_verify_topp.argtypes = [P, P, I, P, P, I, I, I, D, D, P, P, P, P, P, P, P]
+    lib.oracle_spec_verify_topp.argtypes = [P, P, I, P, P, I, I, I, D, D, P, P, P, P, P, P, P, P]
     lib.oracle_spec_verify_topp.restype = I
     lib.oracle_row_probs_topp.argtypes = [P, I, Z, I, D, D, P, P, P, P]
     lib.oracle_row_probs_topp.restype = I
@@ -137,7 +137,7 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k
     top-k with it) is the grammar mask [B, gamma+1, ceil(V/32)] uint32: bit v % 32 of word v // 32
     set when token v is valid at that position.  ``top_p`` (optional, alone) applies the top-p
     processor to every row.  Returns a dict with accepted_len, out_tokens, row_status, lse_p, lse_q,
-    accept, margin.
+    accept, margin and set_margin (top-p: the rows' kept-set margin alone; +inf otherwise).
     """
     lib = _load()
     t, dt = _logits(target)
@@ -158,6 +158,7 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k
         lse_q=np.empty((B, gamma)),
         accept=np.empty((B, gamma)),
         margin=np.empty(B),
+        set_margin=np.full(B, np.inf),
     )
     outs = (_ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["row_status"]),
             _ptr(out["lse_p"]), _ptr(out["lse_q"]), _ptr(out["accept"]), _ptr(out["margin"]))
@@ -165,7 +166,8 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature: float, top_k
         if top_k or allowed is not None:
             raise ValueError("the top-p oracle takes no top-k or mask")
         rc = lib.oracle_spec_verify_topp(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V,
-                                         float(temperature), float(top_p), *outs)
+                                         float(temperature), float(top_p), *outs,
+                                         _ptr(out["set_margin"]))
     elif allowed is None:
         rc = lib.oracle_spec_verify(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(u), B, gamma, V,
                                     float(temperature), int(top_k), *outs)

@@ -308,14 +308,16 @@ int oracle_inverse_cdf(const double* r, int V, double u, double* lo, double* hi)
  * bonus, then -1), row_status[B], lse_p[B, gamma+1], lse_q[B, gamma], accept[B, gamma]
  * (a_i = min(1, p_i(x_i)/q_i(x_i)) at every position), margin[B] (smallest distance between a
  * used uniform and a decision boundary it was compared with: |u_i - a_i| for every reached
- * accept test and |u - C(v-1)/Z|, |u - C(v)/Z| for the drawn token).
- * Any output pointer except the first two may be NULL.
+ * accept test and |u - C(v-1)/Z|, |u - C(v)/Z| for the drawn token; under top-p it also covers
+ * every row's kept-set decision), set_margin[B] (top-p only: the smallest distance between top_p
+ * and the cumulative masses around a row's last kept group, over the request's rows; +inf when no
+ * kept set was chosen by mass).  Any output pointer except the first two may be NULL.
  */
 static int spec_verify_impl(const void* target, const void* draft, int dtype, const int32_t* tokens,
                             const float* uniforms, int B, int gamma, int V, double T, int top_k,
                             const uint32_t* allowed, double top_p, int32_t* accepted_len,
                             int32_t* out_tokens, int32_t* row_status, double* lse_p,
-                            double* lse_q, double* accept, double* margin)
+                            double* lse_q, double* accept, double* margin, double* set_margin)
 {
     if (B < 0 || gamma < 0 || V < 1 || !(T > 0.0)) return 1;
     const size_t W = (size_t)(V + 31) / 32; /* mask words per position */
@@ -409,6 +411,7 @@ static int spec_verify_impl(const void* target, const void* draft, int dtype, co
         accepted_len[b] = A;
         if (row_status) row_status[b] = st;
         if (margin) margin[b] = mg;
+        if (set_margin) set_margin[b] = rmg;
         free(a);
     }
     free(p);
@@ -423,7 +426,8 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, const i
                        double* lse_p, double* lse_q, double* accept, double* margin)
 {
     return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, top_k, NULL,
-                            2.0, accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
+                            2.0, accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin,
+                            NULL);
 }
 
 /*
@@ -431,16 +435,20 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, const i
  * (oracle_row_probs_topp; "Exact speculative and assisted decoding for TinyRustLM": top-p is one of
  * the declared processors both distributions pass through; M7.1 0x03D: truncation keeps exactness
  * when q is the truncated distribution that sampled the draft).  0 < top_p; top_p >= 1 is the plain
- * round.  margin[b] also covers each row's kept-set decision.  Everything else as oracle_spec_verify.
+ * round.  margin[b] also covers each row's kept-set decision; set_margin[b] is that decision's part
+ * alone (the normalisers and accept ratios depend on it, not on the uniforms).  Everything else as
+ * oracle_spec_verify.
  */
 int oracle_spec_verify_topp(const void* target, const void* draft, int dtype, const int32_t* tokens,
                             const float* uniforms, int B, int gamma, int V, double T, double top_p,
                             int32_t* accepted_len, int32_t* out_tokens, int32_t* row_status,
-                            double* lse_p, double* lse_q, double* accept, double* margin)
+                            double* lse_p, double* lse_q, double* accept, double* margin,
+                            double* set_margin)
 {
     if (!(top_p > 0.0)) return 1;
     return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, 0, NULL, top_p,
-                            accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
+                            accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin,
+                            set_margin);
 }
 
 /*
@@ -459,7 +467,7 @@ int oracle_spec_verify_masked(const void* target, const void* draft, int dtype,
 {
     if (!allowed) return 1;
     return spec_verify_impl(target, draft, dtype, tokens, uniforms, B, gamma, V, T, 0, allowed, 2.0,
-                            accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin);
+                            accepted_len, out_tokens, row_status, lse_p, lse_q, accept, margin, NULL);
 }
 
 /* ---------------------------------------------------------------- greedy tree verify */

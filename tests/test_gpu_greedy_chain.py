@@ -8,7 +8,7 @@ import speculative_decoding_verification_spec_gb300 as sv
 from oracle import oracle as O
 from speculative_decoding_verification_spec_gb300 import synth as S
 
-from parity import dev
+from parity import dev, guarded_call
 
 pytestmark = pytest.mark.gpu
 
@@ -16,9 +16,7 @@ C8 = S.TREE_CONFIGS["c8"]
 
 
 def run(tb):
-    out = sv.spec_verify_greedy(dev(tb.logits), dev(tb.tokens))
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+    return guarded_call(sv.spec_verify_greedy, dev(tb.logits), dev(tb.tokens))
 
 
 def check(tb):

@@ -12,7 +12,7 @@ import speculative_decoding_verification_spec_gb300 as sv
 from oracle import oracle as O
 from speculative_decoding_verification_spec_gb300 import synth as S
 
-from parity import compare_spec, dev
+from parity import compare_spec, dev, guarded_call
 
 pytestmark = pytest.mark.gpu
 
@@ -23,12 +23,10 @@ def words_dev(words):
 
 def run_gpu(b, allowed=None, target=None, draft=None):
     a = b.allowed if allowed is None else allowed
-    out = sv.spec_verify_masked(dev(b.target) if target is None else target,
-                                dev(b.draft) if draft is None else draft,
-                                dev(b.draft_tokens), dev(b.uniforms), words_dev(a),
-                                b.cfg.temperature, aux=True)
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+    return guarded_call(sv.spec_verify_masked, dev(b.target) if target is None else target,
+                        dev(b.draft) if draft is None else draft,
+                        dev(b.draft_tokens), dev(b.uniforms), words_dev(a),
+                        b.cfg.temperature, aux=True)
 
 
 def run_oracle(b, allowed=None, idx=None):
@@ -77,11 +75,10 @@ def test_full_mask_equals_spec_verify():
     b = masked(B=16, V=20000, seed=9400)
     full = np.full_like(b.allowed, 0xFFFFFFFF)
     g = run_gpu(b, allowed=full)
-    out = sv.spec_verify(dev(b.target), dev(b.draft), dev(b.draft_tokens), dev(b.uniforms),
-                         b.cfg.temperature, aux=True)
-    torch.cuda.synchronize()
+    out = guarded_call(sv.spec_verify, dev(b.target), dev(b.draft), dev(b.draft_tokens),
+                       dev(b.uniforms), b.cfg.temperature, aux=True)
     for k, v in out.items():
-        np.testing.assert_array_equal(g[k], v.cpu().numpy(), err_msg=k)
+        np.testing.assert_array_equal(g[k], v, err_msg=k)
 
 
 def test_single_valid_token_is_forced():

@@ -13,7 +13,7 @@ import speculative_decoding_verification_spec_gb300 as sv
 from oracle import oracle as O
 from speculative_decoding_verification_spec_gb300 import synth as S
 
-from parity import BOUNDARY, TOL, dev
+from parity import BOUNDARY, TOL, dev, guarded_call
 
 pytestmark = pytest.mark.gpu
 
@@ -22,11 +22,9 @@ C7 = S.SMC_CONFIGS["c7"]
 
 def run_gpu(b, groups=None, eta=None, T=None):
     cfg = b.cfg
-    out = sv.smc_verify(dev(b.target), dev(b.draft), dev(b.draft_tokens), dev(b.log_weights),
-                        dev(b.uniforms), groups or cfg.groups, T or cfg.temperature,
-                        cfg.eta if eta is None else eta)
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+    return guarded_call(sv.smc_verify, dev(b.target), dev(b.draft), dev(b.draft_tokens),
+                        dev(b.log_weights), dev(b.uniforms), groups or cfg.groups,
+                        T or cfg.temperature, cfg.eta if eta is None else eta)
 
 
 def run_oracle(b, groups=None, eta=None, T=None):

@@ -14,18 +14,16 @@ import speculative_decoding_verification_spec_gb300 as sv
 from oracle import oracle as O
 from speculative_decoding_verification_spec_gb300 import synth as S
 
-from parity import compare_spec, dev
+from parity import compare_spec, dev, guarded_call
 
 pytestmark = pytest.mark.gpu
 
 
 def run_gpu(b, top_p=None, target=None, draft=None):
-    out = sv.spec_verify_topp(dev(b.target) if target is None else target,
-                              dev(b.draft) if draft is None else draft,
-                              dev(b.draft_tokens), dev(b.uniforms), b.cfg.temperature,
-                              b.cfg.top_p if top_p is None else top_p, aux=True)
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+    return guarded_call(sv.spec_verify_topp, dev(b.target) if target is None else target,
+                        dev(b.draft) if draft is None else draft,
+                        dev(b.draft_tokens), dev(b.uniforms), b.cfg.temperature,
+                        b.cfg.top_p if top_p is None else top_p, aux=True)
 
 
 def run_oracle(b, top_p=None):
@@ -88,11 +86,10 @@ def test_topp_ties_at_the_threshold():
 def test_topp_one_is_spec_verify():
     b = topp(B=8, V=20000, seed=11600)
     g = run_gpu(b, top_p=1.0)
-    out = sv.spec_verify(dev(b.target), dev(b.draft), dev(b.draft_tokens), dev(b.uniforms),
-                         b.cfg.temperature, aux=True)
-    torch.cuda.synchronize()
+    out = guarded_call(sv.spec_verify, dev(b.target), dev(b.draft), dev(b.draft_tokens),
+                       dev(b.uniforms), b.cfg.temperature, aux=True)
     for k, v in out.items():
-        np.testing.assert_array_equal(g[k], v.cpu().numpy(), err_msg=k)
+        np.testing.assert_array_equal(g[k], v, err_msg=k)
 
 
 def test_topp_statuses():

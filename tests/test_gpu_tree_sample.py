@@ -14,7 +14,7 @@ import speculative_decoding_verification_spec_gb300 as sv
 from oracle import oracle as O
 from speculative_decoding_verification_spec_gb300 import synth as S
 
-from parity import BOUNDARY, TOL, dev
+from parity import BOUNDARY, TOL, dev, guarded_call
 
 pytestmark = pytest.mark.gpu
 
@@ -22,11 +22,10 @@ C6 = S.SAMPLE_TREE_CONFIGS["c6"]
 
 
 def run_gpu(tb, T=None, max_out=None):
-    out = sv.tree_verify_sample(dev(tb.target), dev(tb.draft), dev(tb.parents), dev(tb.tokens),
-                                dev(tb.qrow), dev(tb.uniforms), tb.cfg.temperature if T is None else T,
-                                max_out=max_out, aux=True)
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+    return guarded_call(sv.tree_verify_sample, dev(tb.target), dev(tb.draft), dev(tb.parents),
+                        dev(tb.tokens), dev(tb.qrow), dev(tb.uniforms),
+                        tb.cfg.temperature if T is None else T, max_out=max_out, aux=True,
+                        guard_ws=False)
 
 
 def run_oracle(tb, T=None, max_out=None):
@@ -186,9 +185,8 @@ def test_unaligned_rows_take_the_element_path():
         setattr(tb, name + "_shifted", flat)
     t = dev(tb.target_shifted)[1:].view(tb.target.shape)
     d = dev(tb.draft_shifted)[1:].view(tb.draft.shape)
-    out = sv.tree_verify_sample(t, d, dev(tb.parents), dev(tb.tokens), dev(tb.qrow),
-                                dev(tb.uniforms), cfg.temperature, aux=True)
-    torch.cuda.synchronize()
+    out = guarded_call(sv.tree_verify_sample, t, d, dev(tb.parents), dev(tb.tokens), dev(tb.qrow),
+                       dev(tb.uniforms), cfg.temperature, aux=True, guard_ws=False)
     for k in out:
-        np.testing.assert_array_equal(out[k].cpu().numpy(), g_ref[k])
+        np.testing.assert_array_equal(out[k], g_ref[k])
     compare(g_ref, run_oracle(tb))

@@ -17,7 +17,7 @@ import speculative_decoding_verification_spec_gb300 as sv
 from oracle import oracle as O
 from speculative_decoding_verification_spec_gb300 import synth as S
 
-from parity import dev
+from parity import dev, guarded_call
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +27,10 @@ TOL = 1e-5
 
 def run_gpu(tb, logits=None, eps=None, delta=None, max_out=None):
     c = tb.cfg
-    out = sv.tree_verify_typical(dev(tb.logits) if logits is None else logits, dev(tb.parents),
-                                 dev(tb.tokens), dev(tb.uniforms), c.temperature,
-                                 c.eps if eps is None else eps, c.delta if delta is None else delta,
-                                 max_out=max_out, aux=True)
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+    return guarded_call(sv.tree_verify_typical, dev(tb.logits) if logits is None else logits,
+                        dev(tb.parents), dev(tb.tokens), dev(tb.uniforms), c.temperature,
+                        c.eps if eps is None else eps, c.delta if delta is None else delta,
+                        max_out=max_out, aux=True)
 
 
 def run_oracle(tb, eps=None, delta=None, max_out=None):

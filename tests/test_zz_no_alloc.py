@@ -19,6 +19,8 @@ import speculative_decoding_verification_spec_gb300 as sv
 from speculative_decoding_verification_spec_gb300 import binding
 from speculative_decoding_verification_spec_gb300 import synth as S
 
+from parity import Guarded
+
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5  # absolute, on normalisers and accept ratios (the parity tests' bound)
@@ -40,6 +42,23 @@ def _host(out):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
+def _noalloc(x):
+    """One spec_verify_noalloc call with every output inside sentinel guard bands (checked after
+    the call: nothing outside the caller's buffers may be written)."""
+    B, g1, _ = x[0].shape
+    g = Guarded()
+    out = dict(accepted_len=g.empty((B,), torch.int32, "accepted_len"),
+               out_tokens=g.empty((B, g1), torch.int32, "out_tokens"),
+               row_status=g.empty((B,), torch.int32, "row_status"),
+               lse_p=g.empty((B, g1), torch.float32, "lse_p"),
+               lse_q=g.empty((B, g1 - 1), torch.float32, "lse_q"),
+               accept=g.empty((B, g1 - 1), torch.float32, "accept"))
+    sv.spec_verify_noalloc(*x, out=out)
+    torch.cuda.synchronize()
+    g.check()
+    return _host(out)
+
+
 def _same(got, want):
     for key in ("row_status", "accepted_len", "out_tokens"):
         np.testing.assert_array_equal(got[key], want[key], err_msg=key)
@@ -58,15 +77,14 @@ def test_noalloc_matches_spec_verify_on_two_calls_in_a_row():
     for b in (b1, b2):
         assert sv.workspace_bytes(b.cfg.B, b.cfg.gamma, b.cfg.V) <= sv.NOALLOC_SCRATCH_BYTES
     x1, x2 = _inputs(b1), _inputs(b2)
-    g1 = _host(sv.spec_verify_noalloc(*x1, aux=True))
-    g2 = _host(sv.spec_verify_noalloc(*x2, aux=True))
-    torch.cuda.synchronize()
+    g1 = _noalloc(x1)
+    g2 = _noalloc(x2)
     w1 = _host(sv.spec_verify(*x1, aux=True))
     w2 = _host(sv.spec_verify(*x2, aux=True))
     _same(g1, w1)
     _same(g2, w2)
     # and once more on the first inputs, after the second shape used the array
-    _same(_host(sv.spec_verify_noalloc(*x1, aux=True)), w1)
+    _same(_noalloc(x1), w1)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
