@@ -77,7 +77,10 @@ enum {
     SPEC_ROW_DEGENERATE_RESIDUAL = 2,  /* the correction residual mass is not positive */
     SPEC_ROW_BAD_TOKEN = 3,            /* a draft / node token is outside [0, V), or a drafted
                                           token has q(x) = 0 (it cannot have been sampled) */
-    SPEC_ROW_TIMEOUT = 4,              /* reserved: no kernel of this library waits on a flag */
+    SPEC_ROW_TIMEOUT = 4,              /* a bounded wait inside a streaming kernel ran out (a
+                                          bulk copy or a peer warp of the same CTA did not arrive
+                                          within its limit of polls, see spec_set_wait_limit): the
+                                          request is abandoned and emits nothing */
     SPEC_ROW_BAD_PARENT = 5,           /* tree: parents[b,i] is not in [-1, i) */
     SPEC_ROW_OUTPUT_OVERFLOW = 6,      /* tree: accepted path + bonus does not fit in max_out */
     SPEC_ROW_BAD_UNIFORM = 7,          /* a uniform of the request is not in [0, 1) */
@@ -386,6 +389,29 @@ spec_status spec_verify_noalloc(const void* target_logits, const void* draft_log
  * synchronised: set it from the thread that issues the calls.
  */
 void spec_set_kernel_events(void* start, void* stop);
+
+/*
+ * Test aid: the number of polls after which a bounded wait of the streaming kernels gives up.
+ *
+ * The streaming kernels (spec_verify and its processors, spec_verify_topk, tree_verify_greedy,
+ * spec_verify_greedy, tree_verify_typical, smc_verify) wait only inside one CTA, on mbarriers:
+ * for a bulk copy of a chunk to land, for the CTA's consumer warps to free a ring stage, and
+ * (top-k) for a segment's first bound and its completion.  Each such wait is bounded.  When one
+ * runs out, the CTA stops reading, marks every chunk it has not read, still waits for its copies
+ * in flight (always with the full default limit, so no CTA leaves while a copy could land) and
+ * every request with an unread chunk reports SPEC_ROW_TIMEOUT with accepted_len = -1 and
+ * out_tokens = -1: the request is abandoned without emitting ("Exact speculative and assisted
+ * decoding for TinyRustLM", "Normative edge-case behavior").
+ *
+ *   polls  < 0: back to the default (2^22 polls, far beyond any healthy wait);
+ *          0: every such wait gives up at once, so every request of a streaming call reports
+ *             SPEC_ROW_TIMEOUT (how the tests reach this path without a fault);
+ *          otherwise min(polls, 2^22).
+ * Returns the previous limit.  Process-wide, read when a call is issued; not synchronised: set it
+ * from the thread that issues the calls.  The scalar paths (rows not 16-byte aligned) and
+ * tree_verify_sample do not wait and ignore it.
+ */
+int spec_set_wait_limit(int polls);
 
 /* Static description of a call-level status code. */
 const char* spec_status_string(spec_status s);

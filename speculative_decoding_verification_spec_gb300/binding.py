@@ -21,7 +21,7 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "spec_verify_topp",
            "spec_verify_masked",
            "tree_verify_greedy", "spec_verify_greedy",
-           "tree_verify_sample", "tree_verify_typical", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_status_string")
+           "tree_verify_sample", "tree_verify_typical", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_set_wait_limit", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -69,6 +69,8 @@ def load(path: str | None = None):
     lib.spec_verify_noalloc.restype = I
     lib.spec_set_kernel_events.argtypes = [P, P]
     lib.spec_set_kernel_events.restype = None
+    lib.spec_set_wait_limit.argtypes = [I]
+    lib.spec_set_wait_limit.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -139,6 +141,13 @@ def set_kernel_events(start=None, stop=None):
         if not e.cuda_event:
             e.record()  # creates the underlying CUDA event
     load().spec_set_kernel_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
+
+
+def set_wait_limit(polls: int) -> int:
+    """Test aid: polls after which a bounded wait of the streaming kernels gives up (0: at once,
+    so every request of a streaming call reports ROW_TIMEOUT; negative: the default).  Returns
+    the previous limit."""
+    return int(load().spec_set_wait_limit(int(polls)))
 
 
 def workspace_bytes(B, gamma, V, top_k=0, tree_nodes=0) -> int:
@@ -263,7 +272,7 @@ def tree_verify_greedy(logits, parents, tokens, *, max_out: int | None = None, o
         out = dict(
             accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
             out_tokens=torch.empty(B, max_out, dtype=torch.int32, device=dev),
-            out_nodes=torch.empty(B, max(max_out - 1, 1), dtype=torch.int32, device=dev),
+            out_nodes=torch.empty(B, max(max_out - 1, 0), dtype=torch.int32, device=dev),
             row_status=torch.empty(B, dtype=torch.int32, device=dev),
         )
     nbytes = workspace_bytes(B, 0, V, 0, max(N, 1))
@@ -293,12 +302,12 @@ def tree_verify_typical(logits, parents, tokens, uniforms, temperature: float, e
         out = dict(
             accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
             out_tokens=torch.empty(B, mo, dtype=torch.int32, device=dev),
-            out_nodes=torch.empty(B, max(mo - 1, 1), dtype=torch.int32, device=dev),
+            out_nodes=torch.empty(B, max(mo - 1, 0), dtype=torch.int32, device=dev),
             row_status=torch.empty(B, dtype=torch.int32, device=dev),
         )
         if aux:
             out["entropy"] = torch.empty(B, R, dtype=torch.float32, device=dev)
-            out["logp"] = torch.empty(B, max(N, 1), dtype=torch.float32, device=dev)
+            out["logp"] = torch.empty(B, N, dtype=torch.float32, device=dev)
     nbytes = workspace_bytes(B, 0, V, 0, max(N, 1))
     ws = _workspace(workspace, dev).get(nbytes)
     rc = lib.tree_verify_typical(
@@ -332,11 +341,11 @@ def tree_verify_sample(target, draft, parents, tokens, qrow, uniforms, temperatu
         out = dict(
             accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
             out_tokens=torch.empty(B, max_out, dtype=torch.int32, device=dev),
-            out_nodes=torch.empty(B, max(max_out - 1, 1), dtype=torch.int32, device=dev),
+            out_nodes=torch.empty(B, max(max_out - 1, 0), dtype=torch.int32, device=dev),
             row_status=torch.empty(B, dtype=torch.int32, device=dev),
         )
         if aux:
-            out["accept"] = torch.empty(B, max(N, 1), dtype=torch.float32, device=dev)
+            out["accept"] = torch.empty(B, N, dtype=torch.float32, device=dev)
     rc = lib.tree_verify_sample(_ptr(target), _ptr(draft) if Nq > 0 else None, _dtype_code(target),
                                 _ptr(parents), _ptr(tokens), _ptr(qrow), _ptr(uniforms), B, N, Nq,
                                 V, float(temperature), max_out, _ptr(out["accepted_len"]),

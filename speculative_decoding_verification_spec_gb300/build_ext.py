@@ -17,7 +17,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["sv_softmax.cu", "sv_topk.cu", "sv_tree.cu", "sv_tree_sample.cu", "sv_smc.cu",
            "sv_typical.cu", "sv_topp.cu", "sv_capi.cu", "sv_noalloc.cu"]
-HEADERS = ["sv_common.cuh", "sv_plan.cuh", "sv_tree_sample.cuh", "sv_smc.cuh", "sv_tree_walk.cuh",
+HEADERS = ["sv_common.cuh", "sv_plan.cuh", "sv_draw.cuh", "sv_tree_sample.cuh", "sv_smc.cuh", "sv_tree_walk.cuh",
            "sv_typical.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

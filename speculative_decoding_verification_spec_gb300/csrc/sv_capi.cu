@@ -14,6 +14,8 @@
 namespace sv {
 
 KernelEvents g_kernel_events;
+// polls of a ring or segment wait before it gives up (spec_set_wait_limit); read at every call
+static int g_wait_limit = MBAR_SPIN_LIMIT;
 
 constexpr size_t ALIGN = 256;
 static inline size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
@@ -227,6 +229,7 @@ static spec_status spec_common(const void* target, const void* draft, spec_dtype
     P.B = B; P.gamma = gamma; P.V = V; P.R = R;
     P.dtype = dt; P.vec = vec; P.nvec = sh.nvec;
     P.c = c; P.T = T; P.invT = 1.0 / T; P.top_k = top_k;
+    P.wait_limit = g_wait_limit;
     P.invT_hi = (float)P.invT;
     P.invT_lo = (float)(P.invT - (double)P.invT_hi);
     // 16-byte vectors: 32 KB stream chunks (statistics) and 2048-vector residual chunks; the
@@ -465,6 +468,7 @@ static spec_status tree_common(const void* logits, spec_dtype dtype, const int32
     P.S1 = (int)(vec > 1 ? stream_chunks(sh) : slices1(sh));
     P.tasks = (long long)B * R * P.S1;
     P.max_out = max_out;
+    P.wait_limit = g_wait_limit;
     if (P.tasks >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
     const TreeLayout L = tree_layout(B, N, vec > 1 ? (long long)P.S1 * WARPS : P.S1);
     if (workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
@@ -548,6 +552,7 @@ spec_status tree_verify_typical(const void* logits, spec_dtype dtype, const int3
     P.t.B = B; P.t.N = N; P.t.V = V; P.t.R = R;
     P.t.dtype = dt; P.t.vec = vec; P.t.nvec = sh.nvec;
     P.t.max_out = max_out;
+    P.t.wait_limit = g_wait_limit;
     P.t.accepted_len = accepted_len;
     P.t.out_tokens = out_tokens;
     P.t.out_nodes = (max_out > 1) ? out_nodes : nullptr;
@@ -642,6 +647,13 @@ void spec_set_kernel_events(void* start, void* stop)
 {
     g_kernel_events.start = static_cast<cudaEvent_t>(start);
     g_kernel_events.stop = static_cast<cudaEvent_t>(stop);
+}
+
+int spec_set_wait_limit(int polls)
+{
+    const int prev = g_wait_limit;
+    g_wait_limit = polls < 0 ? MBAR_SPIN_LIMIT : std::min(polls, MBAR_SPIN_LIMIT);
+    return prev;
 }
 
 const char* spec_status_string(spec_status s)

@@ -150,6 +150,7 @@ struct SpecParams {
     const uint32_t* mask;
     int mwords;
     float top_p;          // top-p processor (spec_verify_topp): < 1 keeps each row's nucleus
+    int wait_limit;       // polls of a ring or segment wait before it gives up (ROW_TIMEOUT)
 };
 
 struct TreeParams {
@@ -171,6 +172,7 @@ struct TreeParams {
     unsigned* work;           // [1]
     int32_t* amax;            // [B*R]
     int32_t* scratch;         // [B*N*2] depth / valid of each node
+    int wait_limit;           // polls of a ring wait before it gives up (ROW_TIMEOUT)
 };
 
 // ---------------------------------------------------------------- small device helpers
@@ -322,8 +324,11 @@ __device__ __forceinline__ uint4 lds128(const uint4* p)
 // ---------------------------------------------------------------- bulk copies (TMA engine)
 //
 // One thread arms an mbarrier with the byte count and issues cp.async.bulk global -> shared; the
-// consumers poll the barrier's phase.  Every wait is bounded: after MBAR_SPIN_LIMIT polls it gives
-// up and reports failure, and the caller turns that into a status instead of hanging.
+// consumers poll the barrier's phase.  Every wait is bounded: after a limit of polls it gives up and
+// reports failure, and the caller turns that into a status instead of hanging.  The ring and segment
+// waits take the call's limit (the parameter block's wait_limit: MBAR_SPIN_LIMIT unless a test set
+// a smaller one through spec_set_wait_limit); the final wait for the copies still in flight before
+// a CTA leaves always takes MBAR_SPIN_LIMIT, so no CTA exits while a copy could still land.
 
 constexpr int MBAR_SPIN_LIMIT = 1 << 22;
 
@@ -356,11 +361,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 
-// Bounded wait for the phase with parity `parity` of `bar` to complete; false if the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
+// Bounded wait for the phase with parity `parity` of `bar` to complete: at most `limit` polls
+// (none when limit <= 0); false if they ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int limit)
 {
     const unsigned a = smem_addr(bar);
-    for (int i = 0; i < MBAR_SPIN_LIMIT; ++i) {
+    for (int i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
                      : "=r"(done) : "r"(a), "r"(parity) : "memory");
@@ -380,18 +386,19 @@ constexpr int STREAM_SMEM = STREAM_STAGES * STREAM_CHUNK_BYTES;
 // Warp-specialised streaming (the plain and tree kernels): one producer lane issues the CTA's chunks
 // ids blockIdx.x, + gridDim.x, ... (< nch) into the STREAM_STAGES-stage ring, refilling a stage once
 // all WARPS consumer warps have arrived on its "empty" mbarrier; the stage's "full" mbarrier completes
-// when the bytes land.  src(id, ptr, bytes, policy) describes chunk id.  A wait that runs out, or a
-// consumer's (sfail), stops the issue; the copies in flight are then waited for (bounded), so the
-// CTA never leaves while one could still land.
+// when the bytes land.  src(id, ptr, bytes, policy) describes chunk id.  A wait that runs out (after
+// `limit` polls), or a consumer's (sfail), stops the issue; the copies in flight are then waited for
+// with the full MBAR_SPIN_LIMIT, so the CTA never leaves while one could still land.
 template <class Src>
-__device__ void ring_produce(uint4* ring, uint64_t* full, uint64_t* empty, int* sfail, int nch, Src src)
+__device__ void ring_produce(uint4* ring, uint64_t* full, uint64_t* empty, int* sfail, int nch,
+                             int limit, Src src)
 {
     int stg = 0;
     unsigned ph = 0;
     long long n = 0;
     for (int id = blockIdx.x; id < nch; id += gridDim.x) {
         if (*reinterpret_cast<volatile int*>(sfail)) break;
-        if (n >= STREAM_STAGES && !mbar_wait(&empty[stg], ph ^ 1u)) {
+        if (n >= STREAM_STAGES && !mbar_wait(&empty[stg], ph ^ 1u, limit)) {
             *reinterpret_cast<volatile int*>(sfail) = 1;
             break;
         }
@@ -408,7 +415,7 @@ __device__ void ring_produce(uint4* ring, uint64_t* full, uint64_t* empty, int* 
     }
     // the last fill of every stage: no later fill of that stage exists, so its phase is unambiguous
     for (long long j = (n > STREAM_STAGES ? n - STREAM_STAGES : 0); j < n; ++j)
-        (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u);
+        (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u, MBAR_SPIN_LIMIT);
 }
 
 // persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task (the occupancy query

@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             const int slot = m % TK_SLOTS;
             // the slot's previous segment: done by every consumer warp, published, cleared
             if (m >= TK_SLOTS) {
-                const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)((m - TK_SLOTS) / TK_SLOTS) & 1u));
+                const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)((m - TK_SLOTS) / TK_SLOTS) & 1u, P.wait_limit));
                 publish(slot, done);
                 if (!done) ok = false;
 #pragma unroll
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 uint32_t key = 0;
                 if (k <= NT) {
                     if constexpr (BULK) {
-                        if (t_stg >= 0 && __all_sync(FULL, mbar_wait(&full[t_stg], t_ph))) {
+                        if (t_stg >= 0 && __all_sync(FULL, mbar_wait(&full[t_stg], t_ph, P.wait_limit))) {
                             key = chunk_tau_key<DT, true>(ring + (size_t)t_stg * NT * TK_NV, nullptr, t_cbase, t_cend, k);
                             fence_proxy_async_smem();  // these reads come before the stage's refill
                         } else {
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     // lane 0: the stage's previous fill released by every consumer warp (bounded)
                     int go = 0;
                     if (lane == 0 && ok && !*reinterpret_cast<volatile int*>(&sfail)) {
-                        if (n < TK_STAGES || mbar_wait(&empty[stg], ph ^ 1u)) {
+                        if (n < TK_STAGES || mbar_wait(&empty[stg], ph ^ 1u, P.wait_limit)) {
                             bulk_load(ring + (size_t)stg * NT * TK_NV, row + (size_t)cbase * ES,
                                       (unsigned)(cend - cbase) * ES, &full[stg], pol);
                             go = 1;
@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
         // the last segments: published once every consumer warp is done with them
         for (int j = (m > TK_SLOTS ? m - TK_SLOTS : 0); j < m; ++j) {
             const int slot = j % TK_SLOTS;
-            const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)(j / TK_SLOTS) & 1u));
+            const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)(j / TK_SLOTS) & 1u, P.wait_limit));
             publish(slot, done);
         }
         // the CTA may not leave while a copy is in flight: wait (bounded) for the last fill of
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
         if constexpr (BULK) {
             if (lane == 0)
                 for (long long j = (n > TK_STAGES ? n - TK_STAGES : 0); j < n; ++j)
-                    (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u);
+                    (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u, MBAR_SPIN_LIMIT);
         }
         return;
     }
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             uint32_t w[NREG];
             if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
             if constexpr (BULK) {
-                bool ok = !failed && mbar_wait(&full[stg], ph);
+                bool ok = !failed && mbar_wait(&full[stg], ph, P.wait_limit);
                 const uint4* sb = ring + (size_t)stg * NT * TK_NV + tid;
                 if (ok && !partial) {
 #pragma unroll
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             // does the warp touch the segment's slot, which the producer has cleared by then
             if (st == 0) {
                 if (!failed) {
-                    const bool got = __all_sync(FULL, mbar_wait(&tau_bar[slot], (unsigned)(jseg / TK_SLOTS) & 1u));
+                    const bool got = __all_sync(FULL, mbar_wait(&tau_bar[slot], (unsigned)(jseg / TK_SLOTS) & 1u, P.wait_limit));
                     if (!got) {
                         failed = true;
                         if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
@@ -979,7 +979,7 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     float mx = NEG_INF;
     for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, u[i].x);
     const float M = warp_max(mx);
-    const float MC = M * P.c;
+    const float MC = __fmul_rn(M, P.c);
     // the sum of 2^(fma(x, c, -MC)) over the kept tokens, as a pair of floats
     DFloat acc = df_make(0.f, 0.f);
     if (M != NEG_INF)
@@ -1108,7 +1108,7 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
             if (x >= g) mx = fmaxf(mx, x);
         }
         const float M = block_max(mx, sh_f);
-        const float MC = M * P.c;
+        const float MC = __fmul_rn(M, P.c);
         float s = 0.f;
         if (M != NEG_INF)
             for (int v = threadIdx.x; v < V; v += NT) {

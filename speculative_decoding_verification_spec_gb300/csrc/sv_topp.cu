@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(NT) topp_row_kernel(SpecParams P)
         float Mr = NEG_INF;
         for (int k = lane; k < np; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
         Mr = warp_max(Mr);
-        const float MCr = Mr * P.c;
+        const float MCr = __fmul_rn(Mr, P.c);
         DFloat S = df_make(0.f, 0.f);
         int tmo = 0;
         for (int k = lane; k < np; k += 32) {
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(NT) topp_row_kernel(SpecParams P)
         }
     }
     __syncthreads();
-    const float M = sh_M, MC = M * P.c;
+    const float M = sh_M, MC = __fmul_rn(M, P.c);
     float thr = NEG_INF;
     DFloat S = sh_S;
 

@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
     if (warp == WARPS) {  // the producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            ring_produce(ring, full, empty, &sfail, nch,
+            ring_produce(ring, full, empty, &sfail, nch, P.wait_limit,
                          [&](int id, const char*& ptr, unsigned& bytes, uint64_t& cp) {
                              const int row_id = id / P.S1, ci = id - row_id * P.S1;
                              const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
         const int s = stg;
         if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
-        bool ok = !failed && mbar_wait(&full[s], phase);
+        bool ok = !failed && mbar_wait(&full[s], phase, P.wait_limit);
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
         const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
         uint4 w[STREAM_NV];

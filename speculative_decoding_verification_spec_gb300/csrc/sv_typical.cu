@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
     __syncthreads();
     if (warp == WARPS) {
         if (lane == 0)
-            ring_produce(ring, full, empty, &sfail, nch,
+            ring_produce(ring, full, empty, &sfail, nch, P.t.wait_limit,
                          [&](int id, const char*& ptr, unsigned& bytes, uint64_t& pol) {
                              const int row = id / S1, ci = id - row * S1;
                              const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, V);
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
         const int row = id / S1, ci = id - row * S1;
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, V);
         if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
-        bool ok = !failed && mbar_wait(&full[stg], phase);
+        bool ok = !failed && mbar_wait(&full[stg], phase, P.t.wait_limit);
         uint4 w[STREAM_NV];
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
         const uint4* sb = ring + (size_t)stg * NT * STREAM_NV + tid;
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
                             __uint_as_float(w[j].z)), __uint_as_float(w[j].w)));
             }
             const float M = warp_max(m);
-            const float MC = M * c;
+            const float MC = __fmul_rn(M, c);
             float s0 = 0.f, s1 = 0.f, e0 = 0.f, e1 = 0.f;
             if (M != NEG_INF) {
 #pragma unroll
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(NT) typical_stats_kernel(TypicalParams P)
             m = fmaxf(m, x);
         }
         const float M = warp_max(m);
-        const float MC = M * P.c;
+        const float MC = __fmul_rn(M, P.c);
         float s = 0.f, e = 0.f;
         if (M != NEG_INF)
             for (int v = v0 + lane; v < v1; v += 32) typ_acc(load_logit(rp, DT, v), P.c, MC, s, e);
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
             float Mr = fmaxf(q[t][0].x, q[t][1].x);
             for (int k = lane + 64; k < P.np; k += 32) Mr = fmaxf(Mr, __ldcg(&pp[k].M));
             Mr = warp_max(Mr);
-            const float MCr = Mr * P.c;
+            const float MCr = __fmul_rn(Mr, P.c);
             DFloat S = df_make(0.f, 0.f), E = df_make(0.f, 0.f);
             int tmo = 0;
             auto merge = [&](const float4& e) {
