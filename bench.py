@@ -45,19 +45,21 @@ if ROOT not in sys.path:
 METRIC = "verify rows/sec and achieved HBM GB/s (fraction of GB300 peak) per config"
 L2_BYTES = 129 * 10**6
 SUITE = ("c3", "c4", "c5")
+SMALL = ("c1", "c2")   # timed per call beside the suite
+PER_CALL = 300         # back-to-back calls per configuration for the per-call times
 # the dominant kernel of each workload's call (timed alone through spec_set_kernel_events) and
 # the sources it is built from
 KERNEL_OF = {
-    "c1": ("spec_stats_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
-    "c2": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
-    "c3": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c1": ("spec_stream_kernel", ["sv_softmax.cu", "sv_draw.cuh", "sv_common.cuh", "sv_plan.cuh"]),
+    "c2": ("spec_stream_kernel", ["sv_softmax.cu", "sv_draw.cuh", "sv_common.cuh", "sv_plan.cuh"]),
+    "c3": ("spec_stream_kernel", ["sv_softmax.cu", "sv_draw.cuh", "sv_common.cuh", "sv_plan.cuh"]),
     "c4": ("topk_stream_kernel", ["sv_topk.cu", "sv_common.cuh", "sv_plan.cuh"]),
     "c5": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
     "c6": ("tree_sample_kernel", ["sv_tree_sample.cu", "sv_tree_sample.cuh", "sv_common.cuh"]),
-    "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c7": ("spec_stream_kernel", ["sv_softmax.cu", "sv_draw.cuh", "sv_common.cuh", "sv_plan.cuh"]),
     "c8": ("tree_stream_kernel", ["sv_tree.cu", "sv_common.cuh"]),
-    "c9": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
-    "c11": ("spec_stream_kernel", ["sv_softmax.cu", "sv_common.cuh", "sv_plan.cuh"]),
+    "c9": ("spec_stream_kernel", ["sv_softmax.cu", "sv_draw.cuh", "sv_common.cuh", "sv_plan.cuh"]),
+    "c11": ("spec_stream_kernel", ["sv_softmax.cu", "sv_draw.cuh", "sv_common.cuh", "sv_plan.cuh"]),
     "c10": ("typical_stream_kernel", ["sv_typical.cu", "sv_typical.cuh", "sv_tree_walk.cuh",
                                       "sv_common.cuh", "sv_plan.cuh"]),
 }
@@ -245,6 +247,63 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ acceptance diagnostics
+
+def acceptance_diagnostics(accepted_len, row_status, K: int) -> dict:
+    """The per-round measurements M7.1 ("0x05A/0x05B": the accepted-prefix law and round progress)
+    lists for diagnosis, from one call's outputs: over the requests whose status is OK,
+    Pr(A = a) for a = 0..K, the tails s_j = Pr(A >= j) for j = 1..K, the reach-conditioned rates
+    alpha_j^reach = Pr(A >= j | A >= j-1) (averaged only over requests that reach position j), and
+    the expected round progress E[G] = 1 + sum_j s_j (the accepted drafts plus the correction or
+    bonus token).  For a tree, A is the depth of the accepted node and K the deepest level."""
+    a = np.asarray(accepted_len)[np.asarray(row_status) == 0].astype(np.int64)
+    n = int(a.size)
+    out = {"requests": n, "K": int(K)}
+    if n == 0:
+        return out
+    pa = np.bincount(np.clip(a, 0, K), minlength=K + 1)[:K + 1] / n
+    tail = [float((a >= j).mean()) for j in range(0, K + 1)]  # tail[0] = 1
+    alpha = [tail[j] / tail[j - 1] if tail[j - 1] > 0 else None for j in range(1, K + 1)]
+    out.update({
+        "pr_A": [round(float(x), 6) for x in pa],
+        "pr_A_ge": [round(x, 6) for x in tail[1:]],
+        "alpha_reach": [None if x is None else round(x, 6) for x in alpha],
+        "mean_A": round(float(a.mean()), 6),
+        "E_G": round(1.0 + float(sum(tail[1:])), 6),
+    })
+    return out
+
+
+def read_bytes_nominal(b) -> int:
+    """Bytes of the inputs one call is handed: every logit, plus the grammar mask's words.  This is
+    the algorithmic byte count of every call except the sampled tree, whose walk reads only the
+    rows it visits (counted after its first call)."""
+    if is_sample_tree(b):
+        return b.target.nbytes + b.draft.nbytes
+    return b.logit_bytes + (b.allowed.nbytes if getattr(b, "allowed", None) is not None else 0)
+
+
+def needs_flush(b) -> bool:
+    """Calls whose reads fit in L2 are timed after an L2 flush: the sampled tree always (its walk
+    reads a few rows), the others when all their inputs fit."""
+    return is_sample_tree(b) or read_bytes_nominal(b) < L2_BYTES
+
+
+def run_config(names, batches, world: int, requests=None) -> dict:
+    """The ``config`` object of the JSON line, the same in both arms: it depends only on the
+    workload's inputs."""
+    rows_step = sum(batches[n].rows for n in names)
+    bytes_step = sum(read_bytes_nominal(batches[n]) for n in names)
+    if any(needs_flush(batches[n]) for n in names):
+        l2 = "L2 flushed (256 MB write) before every call, outside its events"
+    else:
+        l2 = f"inputs larger than L2 ({bytes_step / 1e6:.0f} MB per step > 129 MB); no flush"
+    return {"workload": describe(names), "input_dtype": "bf16",
+            "logit_rows_per_step": rows_step, "input_bytes_per_step": bytes_step,
+            "l2": l2, "parallelism": f"replicas x{world} (independent requests per rank)",
+            **({"requests_override": requests} if requests else {})}
+
+
 # ------------------------------------------------------------------ helpers
 
 def source_sha(files):
@@ -278,56 +337,119 @@ def recorded_traffic(kernel, sha):
     return None
 
 
-def cpu_baseline(names, budget_s=15.0):
-    """The oracle as it stands, single thread, on a bounded sample of each workload."""
+def _oracle_one(O, b, i):
+    """The oracle on request i (for SMC: group i) of batch b; returns (rows verified, outputs)."""
+    if is_sample_tree(b):
+        o = O.tree_verify_sample(b.target[i:i + 1], b.draft[i:i + 1], b.parents[i:i + 1],
+                                 b.tokens[i:i + 1], b.qrow[i:i + 1], b.uniforms[i:i + 1],
+                                 b.cfg.temperature)
+        return b.target.shape[1], o
+    if is_greedy_tree(b) and b.cfg.typical:
+        o = O.tree_verify_typical(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1],
+                                  b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.eps, b.cfg.delta)
+        return b.logits.shape[1], o
+    if is_greedy_tree(b):
+        return b.logits.shape[1], O.tree_verify_greedy(b.logits[i:i + 1], b.parents[i:i + 1],
+                                                       b.tokens[i:i + 1])
+    if is_smc(b):
+        Np = b.cfg.particles
+        sl = slice(i * Np, (i + 1) * Np)
+        o = O.smc_verify(b.target[sl], b.draft[sl], b.draft_tokens[sl],
+                         b.log_weights[sl].astype(np.float64), b.uniforms[sl], 1,
+                         b.cfg.temperature, b.cfg.eta)
+        return Np * (2 * b.cfg.K + 1), o
+    o = O.spec_verify(b.target[i:i + 1], b.draft[i:i + 1], b.draft_tokens[i:i + 1],
+                      b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k,
+                      allowed=None if b.allowed is None else b.allowed[i:i + 1],
+                      top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None)
+    return 2 * b.cfg.gamma + 1, o
+
+
+def _units(b) -> int:
+    return b.cfg.groups if is_smc(b) else b.cfg.B
+
+
+def _parity_counts(b, gpu, idx, outs):
+    """{requests, flagged, mismatched} of the matching rules over the requests in idx: the GPU's
+    accepted lengths and tokens against the oracle's, a request flagged when its oracle margin
+    (a used uniform's distance to a decision boundary) is below the rule's bound."""
+    if gpu is None or not idx or is_smc(b):
+        return None
+    bound = 1e-5 if (is_greedy_tree(b) and b.cfg.typical) else 1e-6
+    n = f = m = 0
+    for i, o in zip(idx, outs):
+        same = (int(gpu["accepted_len"][i]) == int(o["accepted_len"][0])
+                and np.array_equal(gpu["out_tokens"][i][:o["out_tokens"].shape[1]], o["out_tokens"][0])
+                and int(gpu["row_status"][i]) == int(o["row_status"][0]))
+        flag = bool(o.get("margin", np.array([np.inf]))[0] < bound)
+        n, f, m = n + 1, f + flag, m + (not same)
+    return {"requests": n, "flagged": f, "mismatched": m,
+            "rule": f"bit-exact tokens, lengths and statuses except draws within {bound:g} of a "
+                    "boundary (flagged)" + ("; trees bit-exact" if is_greedy_tree(b) and not b.cfg.typical else "")}
+
+
+def cpu_baseline(names, budget_s=15.0, gpu_outs=None, all_cores=True):
+    """The oracle as it stands on a bounded sample of each workload: single-threaded (the line's
+    value), and over every host core with a process pool over whole requests.  With ``gpu_outs``
+    (the bench's first call of each configuration, same inputs) the sampled requests also give the
+    matching rules' counts.  Returns (cpu_baseline, parity)."""
     from oracle import oracle as O
+    from oracle import pool as OP
     batches = workload_batches(names, 0)
-    per_row_s, sample = {}, []
+    per_row_s, sample, parity = {}, [], {}
     share = budget_s / len(names)
     for n, b in batches.items():
         rows_done, t_used, i = 0, 0.0, 0
-        B = b.cfg.B
-        while t_used < share and i < B:
+        idx, outs = [], []
+        while t_used < share and i < _units(b):
             t0 = time.perf_counter()
-            if is_sample_tree(b):
-                O.tree_verify_sample(b.target[i:i + 1], b.draft[i:i + 1], b.parents[i:i + 1],
-                                     b.tokens[i:i + 1], b.qrow[i:i + 1], b.uniforms[i:i + 1],
-                                     b.cfg.temperature)
-                rows_done += b.target.shape[1]
-            elif is_greedy_tree(b) and b.cfg.typical:
-                O.tree_verify_typical(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1],
-                                      b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.eps, b.cfg.delta)
-                rows_done += b.logits.shape[1]
-            elif is_greedy_tree(b):
-                O.tree_verify_greedy(b.logits[i:i + 1], b.parents[i:i + 1], b.tokens[i:i + 1])
-                rows_done += b.logits.shape[1]
-            elif is_smc(b):  # one group of particles per sample
-                Np = b.cfg.particles
-                if i >= b.cfg.groups:
-                    break
-                sl = slice(i * Np, (i + 1) * Np)
-                O.smc_verify(b.target[sl], b.draft[sl], b.draft_tokens[sl],
-                             b.log_weights[sl].astype(np.float64), b.uniforms[sl], 1,
-                             b.cfg.temperature, b.cfg.eta)
-                rows_done += Np * (2 * b.cfg.K + 1)
-            else:
-                O.spec_verify(b.target[i:i + 1], b.draft[i:i + 1], b.draft_tokens[i:i + 1],
-                              b.uniforms[i:i + 1], b.cfg.temperature, b.cfg.top_k,
-                              allowed=None if b.allowed is None else b.allowed[i:i + 1],
-                              top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None)
-                rows_done += 2 * b.cfg.gamma + 1
+            r, o = _oracle_one(O, b, i)
             t_used += time.perf_counter() - t0
+            rows_done += r
+            idx.append(i)
+            outs.append(o)
             i += 1
         per_row_s[n] = t_used / rows_done
         sample.append(f"{n}: {i} {'groups of particles' if is_smc(b) else 'requests'} "
                       f"({rows_done} rows)")
+        parity[n] = _parity_counts(b, (gpu_outs or {}).get(n), idx, outs)
     rows = {n: batches[n].rows for n in names}
     step_s = sum(per_row_s[n] * rows[n] for n in names)
-    return {"value": sum(rows.values()) / step_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": "; ".join(sample) + "; single-threaded fp64 C oracle, scaled to one step"}
+    base = {"value": sum(rows.values()) / step_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": "; ".join(sample) + "; single-threaded fp64 C oracle, scaled to one step",
+            "host": {"nproc": os.cpu_count(), "cpu_model": OP.cpu_model()}}
+    # every host core: whole configurations through a pool of worker processes (spawn), one block
+    # of requests per task; only calls the pool covers (plain, processors, top-k, greedy tree)
+    pooled = [n for n in names if not is_sample_tree(batches[n]) and not is_smc(batches[n])
+              and not (is_greedy_tree(batches[n]) and batches[n].cfg.typical)]
+    if all_cores and pooled:
+        procs = OP.cores()
+        t0 = time.perf_counter()
+        for n in pooled:
+            b = batches[n]
+            if is_greedy_tree(b):
+                OP.tree_verify_greedy(b.logits, b.parents, b.tokens, procs=procs)
+            else:
+                OP.spec_verify(b.target, b.draft, b.draft_tokens, b.uniforms, b.cfg.temperature,
+                               b.cfg.top_k, allowed=b.allowed,
+                               top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None, procs=procs)
+        el = time.perf_counter() - t0
+        done = sum(rows[n] for n in pooled)
+        base["all_cores"] = {"value": done / el, "unit": "rows/s", "cores": procs,
+                             "cpu_model": base["host"]["cpu_model"],
+                             "sample": f"every request of {', '.join(pooled)} ({done} rows) in "
+                                       f"{el:.2f} s, worker start-up included"}
+    return base, parity
 
 
 # ------------------------------------------------------------------ our arm
+
+def percentiles(ms):
+    """median and p10 / p90 of per-call times (ms)."""
+    q = np.percentile(np.asarray(ms, dtype=np.float64), [10, 50, 90])
+    return {"p10": round(float(q[0]), 5), "median": round(float(q[1]), 5), "p90": round(float(q[2]), 5),
+            "mean": round(float(np.mean(ms)), 5), "calls": len(ms)}
+
 
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -339,13 +461,12 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     names = SUITE if args.workload == "suite" else (args.workload,)
-    batches = workload_batches(names, rank, args.requests)
+    # the suite's step is the large configurations; the small ones (c1, c2) are timed per call
+    # beside it, since each is a few microseconds of launch-bound work
+    extra = tuple(n for n in SMALL if n not in names) if args.workload == "suite" else ()
+    batches = workload_batches(names + extra, rank, args.requests)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
-
-    def to_dev(a):
-        a = np.ascontiguousarray(a)
-        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
 
     host, devin, outs, wss = {}, {}, {}, {}
     for n, b in batches.items():
@@ -369,49 +490,53 @@ def run_ours(args, rank, world, local_rank):
         devin[n] = {k: v.to(dev) for k, v in host[n].items()}
         wss[n] = sv.Workspace(dev)
 
-    def call(n, ins, out=None):
+    def call(n, ins, out=None, st=stream):
         b = batches[n]
         if is_sample_tree(b):
             return sv.tree_verify_sample(ins["target"], ins["draft"], ins["parents"], ins["tokens"],
                                          ins["qrow"], ins["uniforms"], b.cfg.temperature, out=out,
-                                         aux=True, stream=stream)
+                                         aux=True, stream=st)
         if is_smc(b):
             return sv.smc_verify(ins["target"], ins["draft"], ins["tokens"], ins["log_weights"],
                                  ins["uniforms"], b.cfg.groups, b.cfg.temperature, b.cfg.eta,
-                                 out=out, workspace=wss[n], stream=stream)
+                                 out=out, workspace=wss[n], stream=st)
         if is_greedy_tree(b) and b.cfg.typical:
             return sv.tree_verify_typical(ins["logits"], ins["parents"], ins["tokens"],
                                           ins["uniforms"], b.cfg.temperature, b.cfg.eps,
-                                          b.cfg.delta, out=out, workspace=wss[n], stream=stream)
+                                          b.cfg.delta, out=out, workspace=wss[n], stream=st)
         if is_greedy_tree(b) and b.cfg.chain:
             return sv.spec_verify_greedy(ins["logits"], ins["tokens"], out=out, workspace=wss[n],
-                                         stream=stream)
+                                         stream=st)
         if is_greedy_tree(b):
             return sv.tree_verify_greedy(ins["logits"], ins["parents"], ins["tokens"], out=out,
-                                         workspace=wss[n], stream=stream)
+                                         workspace=wss[n], stream=st)
         return sv.spec_verify(ins["target"], ins["draft"], ins["tokens"], ins["uniforms"],
                               b.cfg.temperature, top_k=b.cfg.top_k, allowed=ins.get("allowed"),
                               top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None,
-                              out=out, workspace=wss[n], stream=stream)
+                              out=out, workspace=wss[n], stream=st)
 
-    for n in names:  # allocate outputs once
+    for n in batches:  # allocate outputs once
         outs[n] = call(n, devin[n])
     torch.cuda.synchronize()
+    first = {n: {k: v.cpu().numpy() for k, v in outs[n].items()} for n in batches}
     # algorithmic bytes of one call: the logits it reads (all of them, except on the sampled tree,
     # whose walk reads only the rows it visits)
     read_bytes = {}
-    for n in names:
-        b = batches[n]
+    for n, b in batches.items():
         if is_sample_tree(b):
-            rows = sample_tree_rows_read(b, outs[n]["accepted_len"].cpu().numpy(),
-                                         outs[n]["accept"].cpu().numpy())
+            rows = sample_tree_rows_read(b, first[n]["accepted_len"], first[n]["accept"])
             read_bytes[n] = rows * b.cfg.V * b.target.itemsize
-        else:  # plus the grammar mask's words, once
-            read_bytes[n] = b.logit_bytes + (b.allowed.nbytes if getattr(b, "allowed", None) is not None else 0)
+        else:
+            read_bytes[n] = read_bytes_nominal(b)
     # calls whose reads fit in L2 are timed after an L2 flush (a 256 MB write), outside their events
-    flush = None
-    if any(read_bytes[n] < L2_BYTES for n in names):
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_buf = None
+    if any(needs_flush(b) for b in batches.values()):
+        flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_step = any(needs_flush(batches[n]) for n in names)
+
+    def flush(n):
+        if needs_flush(batches[n]):
+            flush_buf.zero_()
 
     def barrier():
         if world > 1:
@@ -437,8 +562,8 @@ def run_ours(args, rank, world, local_rank):
         start.record(stream)
         for i in range(args.steps):
             for n in names:
-                if flush is not None:
-                    flush.zero_()
+                if flush_step:
+                    flush(n)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -452,28 +577,76 @@ def run_ours(args, rank, world, local_rank):
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    if flush is None:
+    if not flush_step:
         elapsed = dist_max(start.elapsed_time(end) / 1e3, world, dev)
     else:  # the flushes are not verify work: the step time is the sum of the calls' event times
         elapsed = dist_max(sum(a.elapsed_time(b) for n in names for a, b in ev[n]) / 1e3, world, dev)
     call_ms_timed = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
 
-    # per-call times once more without the dominant kernel's own events: an event recorded between
-    # two launches of a call breaks their dependent-launch overlap
-    clean = {n: [] for n in names}
-    for i in range(min(args.steps, 200)):
-        for n in names:
-            if flush is not None:
-                flush.zero_()
+    # ---- per-configuration call times: PER_CALL back-to-back calls of each configuration alone,
+    # each bracketed by events on the call's stream (no event inside a call, so its dependent
+    # launches overlap as in use); configurations that fit in L2 are flushed before every call
+    per_ms = {n: [] for n in batches}
+    for n in batches:
+        for _ in range(3):
+            call(n, devin[n], outs[n])
+        pairs = []
+        for i in range(PER_CALL):
+            if flush_buf is not None:
+                flush(n)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             call(n, devin[n], outs[n])
             e1.record(stream)
-            clean[n].append((e0, e1))
-    torch.cuda.synchronize()
-    call_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in clean[n]) for n in names}
+            pairs.append((e0, e1))
+        torch.cuda.synchronize()
+        per_ms[n] = [a.elapsed_time(b) for a, b in pairs]
+
+    # the small configurations once more as CUDA-graph replays: one captured call, replayed, so
+    # the host's launch cost is out of the time (how a serving loop would issue them)
+    graph_ms = {}
+    for n in extra:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for _ in range(2):
+                    call(n, devin[n], outs[n], st=side)
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call(n, devin[n], outs[n], st=torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            pairs = []
+            for i in range(PER_CALL):
+                flush(n)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                pairs.append((e0, e1))
+            torch.cuda.synchronize()
+            graph_ms[n] = [a.elapsed_time(b) for a, b in pairs]
+            del g
+        except Exception as exc:  # reported, not fatal: the direct calls are timed above
+            graph_ms[n] = f"capture failed: {type(exc).__name__}: {exc}"[:200]
+
+    # c1 is one request: its acceptance law is read from its 10,000 seeded trials in one call
+    diag_outs = {}
+    if "c1" in batches and not args.requests:
+        from speculative_decoding_verification_spec_gb300 import synth as S
+        tb = S.trial_batches(S.scaled(batches["c1"].cfg), 10000)
+        t = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev)
+             for k, v in dict(target=tb.target, draft=tb.draft, tokens=tb.draft_tokens,
+                              uniforms=tb.uniforms).items()}
+        o = sv.spec_verify(t["target"], t["draft"], t["tokens"], t["uniforms"], tb.cfg.temperature,
+                           stream=stream)
+        torch.cuda.synchronize()
+        diag_outs["c1"] = {k: v.cpu().numpy() for k, v in o.items()}
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -520,14 +693,37 @@ def run_ours(args, rank, world, local_rank):
     rows_step = sum(batches[n].rows for n in names)
     bytes_step = sum(read_bytes[n] for n in names)
     per_cfg = {}
-    for n in names:
-        gbs = read_bytes[n] / (call_ms[n] / 1e3) / 1e9
-        per_cfg[n] = {"call_ms": round(call_ms[n], 5), "call_ms_timed_region": round(call_ms_timed[n], 5),
-                      "rows_per_s": batches[n].rows / (call_ms[n] / 1e3),
-                      "requests_per_s": batches[n].cfg.B / (call_ms[n] / 1e3),
-                      "calls_per_s": 1e3 / call_ms[n], "logit_bytes": read_bytes[n],
-                      "hbm_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
-                      "frac_of_8tbs": round(gbs / 8000.0, 4)}
+    for n, b in batches.items():
+        pc = percentiles(per_ms[n])
+        med = pc["median"]
+        gbs = read_bytes[n] / (med / 1e3) / 1e9
+        per_cfg[n] = {"call_ms": pc, "rows_per_s": b.rows / (med / 1e3),
+                      "requests_per_s": _units(b) / (med / 1e3), "calls_per_s": 1e3 / med,
+                      "logit_bytes": read_bytes[n], "hbm_gbs": round(gbs, 1),
+                      "frac_of_measured_peak": round(gbs / peak, 4),
+                      "frac_of_8tbs": round(gbs / 8000.0, 4),
+                      "l2": "flushed before every call (its reads fit in L2)" if needs_flush(b)
+                            else "inputs larger than L2, no flush"}
+        if n in call_ms_timed:
+            per_cfg[n]["call_ms_timed_region"] = round(call_ms_timed[n], 5)
+        if n in graph_ms:
+            gm = graph_ms[n]
+            per_cfg[n]["graph_replay"] = (gm if isinstance(gm, str) else
+                                          {"call_ms": percentiles(gm),
+                                           "calls_per_s": 1e3 / percentiles(gm)["median"]})
+        if not is_sample_tree(b) and not is_smc(b):
+            K = b.cfg.max_nodes if is_greedy_tree(b) and b.cfg.chain else (
+                int(S_tree_depth(b)) if is_greedy_tree(b) else b.cfg.gamma)
+            acc = diag_outs.get(n, first[n])
+            per_cfg[n]["acceptance"] = acceptance_diagnostics(acc["accepted_len"],
+                                                              acc["row_status"], K)
+            if n in diag_outs:
+                per_cfg[n]["acceptance"]["sample"] = (f"{len(acc['accepted_len'])} seeded trials "
+                                                      "of the configuration (one call)")
+            eg = per_cfg[n]["acceptance"].get("E_G")
+            if eg:
+                per_cfg[n]["acceptance"]["bytes_per_committed_token"] = round(
+                    read_bytes[n] / (eg * _units(b)), 1)
     dom_kernel, dom_files = KERNEL_OF[dom_cfg]
     sha = source_sha(dom_files)
     achieved = read_bytes[dom_cfg] / (kernel_ms / 1e3) / 1e9
@@ -544,14 +740,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": describe(names), "input_dtype": "bf16",
-                   "logit_rows_per_step": rows_step, "logit_bytes_per_step": bytes_step,
-                   "l2": (f"inputs larger than L2 ({bytes_step / 1e6:.0f} MB per step > 129 MB); no flush"
-                          if flush is None else
-                          f"L2 flushed (256 MB write) before every call, outside its events; the "
-                          f"calls read {bytes_step / 1e6:.0f} MB per step"),
-                   "parallelism": f"replicas x{world} (independent requests per rank)",
-                   **({"requests_override": args.requests} if args.requests else {})},
+        "config": run_config(names, batches, world, args.requests),
         "hbm_gbs": bytes_step * world * args.steps / elapsed / 1e9,
         "per_config": per_cfg,
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "workload": dom_cfg,
@@ -569,8 +758,19 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(names, args.cpu_budget)
+        cb, parity = cpu_baseline(names + extra, args.cpu_budget, first)
+        line["cpu_baseline"] = cb
+        line["parity"] = parity
     print(json.dumps(line), flush=True)
+
+
+def S_tree_depth(b) -> int:
+    """The deepest level of a greedy tree batch (depth of a node = 1 + its parent's)."""
+    par = b.parents[0]
+    depth = np.zeros(len(par), np.int64)
+    for i, p in enumerate(par):
+        depth[i] = 1 if p < 0 else depth[p] + 1
+    return int(depth.max()) if len(depth) else 0
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -581,43 +781,12 @@ def run_reference(args, rank, world):
     names = SUITE if args.workload == "suite" else (args.workload,)
     from oracle import oracle as O
     O.build()
-    batches = workload_batches(names, 0)
+    batches = workload_batches(names, 0, args.requests)
     # each step verifies a bounded sample: one request of one workload, the workloads in turn, so
     # that the default --steps run ends within a few minutes on one host core
     def step(i):
-        rows = 0
-        for n in (names[i % len(names)],):
-            b = batches[n]
-            if is_sample_tree(b):
-                j = (i // len(names)) % b.cfg.B
-                O.tree_verify_sample(b.target[j:j + 1], b.draft[j:j + 1], b.parents[j:j + 1],
-                                     b.tokens[j:j + 1], b.qrow[j:j + 1], b.uniforms[j:j + 1],
-                                     b.cfg.temperature)
-                rows += b.target.shape[1]
-            elif is_smc(b):
-                Np = b.cfg.particles
-                j = (i // len(names)) % b.cfg.groups
-                sl = slice(j * Np, (j + 1) * Np)
-                O.smc_verify(b.target[sl], b.draft[sl], b.draft_tokens[sl],
-                             b.log_weights[sl].astype(np.float64), b.uniforms[sl], 1,
-                             b.cfg.temperature, b.cfg.eta)
-                rows += Np * (2 * b.cfg.K + 1)
-            elif is_greedy_tree(b):
-                j = (i // len(names)) % b.logits.shape[0]
-                if b.cfg.typical:
-                    O.tree_verify_typical(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1],
-                                          b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.eps,
-                                          b.cfg.delta)
-                else:
-                    O.tree_verify_greedy(b.logits[j:j + 1], b.parents[j:j + 1], b.tokens[j:j + 1])
-                rows += b.logits.shape[1]
-            else:
-                j = (i // len(names)) % b.cfg.B
-                O.spec_verify(b.target[j:j + 1], b.draft[j:j + 1], b.draft_tokens[j:j + 1],
-                              b.uniforms[j:j + 1], b.cfg.temperature, b.cfg.top_k,
-                              allowed=None if b.allowed is None else b.allowed[j:j + 1],
-                              top_p=b.cfg.top_p if b.cfg.top_p < 1.0 else None)
-                rows += 2 * b.cfg.gamma + 1
+        b = batches[names[i % len(names)]]
+        rows, _ = _oracle_one(O, b, (i // len(names)) % _units(b))
         return rows
 
     for i in range(args.warmup):
@@ -632,10 +801,11 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(names), "input_dtype": "bf16",
-                       "sample_per_step": "one request of one workload, the workloads in turn"},
+            "config": run_config(names, batches, world, args.requests),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": "one request of one workload per step (in turn), single thread"},
+                             "sample": "each step verifies one request (a group of particles for "
+                                       "SMC) of one workload, the workloads in turn, single "
+                                       "thread; value = rows verified / time"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
