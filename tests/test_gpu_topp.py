@@ -107,3 +107,86 @@ def test_topp_repeat_calls_are_deterministic():
     a1, a2 = run_gpu(b), run_gpu(b)
     for k in a1:
         np.testing.assert_array_equal(a1[k], a2[k])
+
+
+def with_rows(b, xt, xd, seed=5):
+    """b with its logits replaced by xt / xd (stored in b's dtype) and each draft token redrawn
+    from its draft row's nucleus."""
+    if b.target.dtype == np.uint16:
+        b.target[:] = S.f32_to_bf16_bits(xt.astype(np.float32))
+        b.draft[:] = S.f32_to_bf16_bits(xd.astype(np.float32))
+    else:
+        b.target[:] = xt.astype(np.float32)
+        b.draft[:] = xd.astype(np.float32)
+    keep = S.draft_nucleus_mask(S.stored_to_f64(b.draft), b.cfg.temperature, b.cfg.top_p)
+    rng = np.random.default_rng(seed)
+    for r in range(b.draft.shape[0]):
+        for i in range(b.draft.shape[1]):
+            b.draft_tokens[r, i] = rng.choice(np.flatnonzero(keep[r, i]))
+    return b
+
+
+def _rows(rng, b, f):
+    xt = f(rng, b.target.shape)
+    return xt, f(rng, b.draft.shape)
+
+
+def _negative(rng, shape):
+    return -3.0 + 0.3 * rng.standard_normal(shape)
+
+
+def _zero_max(rng, shape):
+    x = -np.abs(2.0 * rng.standard_normal(shape))
+    flat = x.reshape(-1, shape[-1])
+    for row in flat:
+        at = rng.choice(shape[-1], 10, replace=False)
+        row[at[:5]] = 0.0
+        row[at[5:]] = -0.0
+    return x
+
+
+def _flat(rng, shape):
+    return 0.05 * rng.standard_normal(shape)
+
+
+def _deep(rng, shape):
+    # one token at 20 and the rest about 15 bits of mass below it: the kept mass crosses top_p far
+    # below the cut, where no candidate is
+    x = 9.6 + 0.05 * rng.standard_normal(shape)
+    x.reshape(-1, shape[-1])[:, 0] = 20.0
+    return x
+
+
+def _cluster(rng, shape):
+    # a tight cluster of 1000 distinct values holds nearly all the mass: the bin where it crosses
+    # top_p is crowded
+    x = -5.0 + rng.standard_normal(shape)
+    flat = x.reshape(-1, shape[-1])
+    for row in flat:
+        at = rng.choice(shape[-1], 1000, replace=False)
+        row[at] = 2.0 + 1e-6 * np.arange(1000)
+    return x
+
+
+@pytest.mark.parametrize("case, dtype, V, T", [
+    ("negative", "bf16", 20000, 0.5),   # per-value bins over negative keys
+    ("zero_max", "bf16", 4096, 1.0),    # +0 and -0 at the maximum; the keys span zero: the list path
+    ("flat", "bf16", 40000, 1.0),       # every element a candidate: the list overflows
+    ("deep", "bf16", 40000, 1.0),       # per-value bins, but the crossing lies below the cut
+    ("deep", "f32", 20000, 1.0),        # the list, and the crossing below the cut
+    ("flat", "f32", 20000, 1.0),        # fp32 list overflow
+    ("cluster", "f32", 4096, 1.0),      # a crowded crossing bin
+    ("zero_max", "f32", 4096, 1.0),     # fp32 list path with +0 and -0
+])
+def test_topp_select_paths(case, dtype, V, T):
+    """Rows built to take each branch of the threshold select: per-value bins, the candidate list
+    with its crossing bin resolved, and the radix select when the list overflows, the crossing lies
+    below the cut or the crossing bin is crowded."""
+    b = topp(B=4, gamma=3, V=V, dtype=dtype, temperature=T, seed=11900)
+    f = {"negative": _negative, "zero_max": _zero_max, "flat": _flat, "deep": _deep,
+         "cluster": _cluster}[case]
+    xt, xd = _rows(np.random.default_rng(11901), b, f)
+    b = with_rows(b, xt, xd)
+    g, o = run_gpu(b), run_oracle(b)
+    compare_spec(g, o, label=f"top-p {case} {dtype}")
+    assert np.all(g["row_status"] == O.ROW_OK)
