@@ -186,7 +186,9 @@ def kernels_per_call(batch):
         return 2                              # argmax stream + tree finish
     if is_smc(batch):
         return 4                              # stream + row plan + extension draw + group step
-    return 3                                  # stream + finish + dense / stream + row plan + residual
+    if batch.cfg.top_k:
+        return 2                              # stream + finish (dense rows inside the finish)
+    return 3                                  # stream + row plan + residual
 
 
 # ------------------------------------------------------------------ clocks

@@ -643,6 +643,29 @@ __device__ __forceinline__ DFloat df_mul(DFloat x, float c_hi, float c_lo)
 }
 __device__ __forceinline__ double df_to_double(DFloat x) { return (double)x.hi + (double)x.lo; }
 
+// Fixed-point masses: 2^40 w rounded toward zero for a mass w in [0, 1], from the float's bits
+// with integer operations only (a conversion to a 64-bit integer is not a fast-pipe instruction).
+// Sums of them are exact and independent of order, so a kept set's mass does not depend on
+// scheduling.
+constexpr double FIXED_ONE = 1099511627776.0;  // 2^40
+__device__ __forceinline__ unsigned long long fixed_mass(float w)
+{
+    const uint32_t u = __float_as_uint(w);
+    const int e = (int)(u >> 23);     // biased exponent; w >= 0
+    if (e == 0 || e > 127) return 0ull;  // zero (the exponential flushes subnormals); NaN or inf
+    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
+    const int sh = e - 127 - 23 + 40;  // 2^40 w = m 2^sh, sh <= 17
+    return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0ull);
+}
+
+// a fixed-point sum as a pair of floats (exact in fp64 up to 2^53)
+__device__ __forceinline__ DFloat fixed_to_df(unsigned long long f)
+{
+    const double d = (double)f * (1.0 / FIXED_ONE);
+    const float hi = (float)d;
+    return df_make(hi, (float)(d - (double)hi));
+}
+
 // Sum over the warp of pairs; every lane gets the same pair (the butterfly adds the same two
 // operands in each pair of lanes, and the pair sum is symmetric).
 __device__ __forceinline__ DFloat warp_sum_df(DFloat v)

@@ -18,13 +18,14 @@
 // k-th largest value g, so the lists hold every element >= g.
 //
 // Kernel 2 (topk_finish_kernel), one warp per row, selects g exactly from the union of the row's
-// candidate lists, keeps the entries >= g sorted by index and forms the normaliser (M, S).  The
-// last warp to finish a row of a request runs the acceptance scan and draws the correction or
-// bonus token directly from the kept list of the p row: the residual vanishes outside K_p, so no
-// second pass over V is needed.
+// candidate lists, keeps the entries >= g and forms the normaliser (M, and S as a fixed-point sum,
+// which does not depend on the order the lists deliver the entries in).  After a CTA barrier one
+// warp runs the request's acceptance scan and draws the correction or bonus token directly from the
+// kept list of the p row, sorted by index first: the residual vanishes outside K_p, so no second
+// pass over V is needed.
 //
-// Rows whose candidates overflow the capacities (massive ties, k > NT, ...) are marked dense and
-// finished exactly by kernel 3 (topk_dense_kernel) with full-row passes.
+// Rows whose candidates overflow the capacities (massive ties, k > NT, ...) are marked dense; the
+// finish CTA of their request then completes it exactly with full-row passes (topk_dense_request).
 #include <cuda_bf16.h>
 
 #include "sv_plan.cuh"
@@ -112,9 +113,12 @@ __device__ void warp_sort_by_index(TopkEntry* e, int n)
 }
 
 // One warp: the correction / bonus draw of request b, planned as pl, from the kept list of the p
-// row (index order, nk entries); the residual is zero outside K_p.  Sums in pairs of floats.
+// row (nk entries of the workspace, in the order the lists gave them); the residual is zero outside
+// K_p.  Each entry's residual is formed (with the draft row's logit at its token), and the entries
+// are sorted by index into se (room for 2 * cap_k entries), since the draw walks the tokens in
+// index order.  Sums in pairs of floats.
 template <int DT>
-__device__ void topk_request_draw(const SpecParams& P, const Plan& pl, int nk, float* rr, int b)
+__device__ void topk_request_draw(const SpecParams& P, const Plan& pl, int nk, TopkEntry* se, int b)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
@@ -124,42 +128,59 @@ __device__ void topk_request_draw(const SpecParams& P, const Plan& pl, int nk, f
     }
     const TopkEntry* kl = P.klist + ((size_t)b * P.R + pl.rp) * P.cap_k;
     const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
-    // each lane owns a contiguous block of the kept list
-    const int per = (nk + 31) / 32;
-    const int i0 = min(lane * per, nk), i1 = min(i0 + per, nk);
-    DFloat mine = df_make(0.f, 0.f);
-    for (int b0 = i0; b0 < i1; b0 += 8) {
-        // eight entries at a time: their list loads, then their q gathers, each batch in flight
-        // together, then the residual in list order
-        float xp[8], xq[8];
-        int v[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (b0 + t < i1) {
-                const TopkEntry e = ld_entry(kl + b0 + t);
-                xp[t] = e.x;
-                v[t] = e.idx;
-            }
-        }
+    auto residual = [&](float xp, float xq) {
+        const float pp = __fmul_rn(ex2(fmaf(xp, P.c, -pl.MCp)), pl.invSp);
+        if (!rowq) return pp;
+        const float qq = (xq >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq, P.c, -pl.MCq)), pl.invSq) : 0.f;
+        return fmaxf(__fsub_rn(pp, qq), 0.f);
+    };
+    if (nk <= 64) {
+        // entries lane and lane + 32 in registers with their residuals; each goes to its rank, the
+        // number of smaller indices (the indices are distinct), counted by shuffles
+        TopkEntry a, c;
+        a.idx = c.idx = 0x7fffffff;
+        a.x = c.x = 0.f;
+        float qa = 0.f, qc = 0.f;
+        if (lane < nk) a = ld_entry(kl + lane);
+        if (lane + 32 < nk) c = ld_entry(kl + lane + 32);
         if (rowq) {
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-                if (b0 + t < i1) xq[t] = load_logit(rowq, DT, v[t]);
+            if (lane < nk) qa = load_logit(rowq, DT, a.idx);
+            if (lane + 32 < nk) qc = load_logit(rowq, DT, c.idx);
         }
+        int ra = 0, rc = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const int ia = __shfl_sync(FULL, a.idx, j), ic = __shfl_sync(FULL, c.idx, j);
+            ra += (ia < a.idx) + (ic < a.idx);
+            rc += (ia < c.idx) + (ic < c.idx);
+        }
+        if (lane < nk) se[ra] = TopkEntry{residual(a.x, qa), a.idx};
+        if (lane + 32 < nk) se[rc] = TopkEntry{residual(c.x, qc), c.idx};
+    } else {
+        for (int i = lane; i < nk; i += 32) se[i] = ld_entry(kl + i);
+        __syncwarp();
+        warp_sort_by_index(se, nk);
+        // the draft row's logits at the sorted tokens, eight per lane in flight, then residuals
+        for (int i0 = 0; i0 < nk; i0 += 32 * 8) {
+            float xq[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (b0 + t < i1) {
-                const float pp = __fmul_rn(ex2(fmaf(xp[t], P.c, -pl.MCp)), pl.invSp);
-                float res = pp;
-                if (rowq) {
-                    const float qq = (xq[t] >= pl.thrq) ? __fmul_rn(ex2(fmaf(xq[t], P.c, -pl.MCq)), pl.invSq) : 0.f;
-                    res = fmaxf(__fsub_rn(pp, qq), 0.f);
-                }
-                rr[b0 + t] = res;
-                mine = df_add(mine, df_make(res, 0.f));
+            for (int t = 0; t < 8; ++t) {
+                const int i = i0 + 32 * t + lane;
+                xq[t] = (rowq && i < nk) ? load_logit(rowq, DT, se[i].idx) : 0.f;
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int i = i0 + 32 * t + lane;
+                if (i < nk) se[i].x = residual(se[i].x, xq[t]);
             }
         }
     }
+    __syncwarp();
+    // each lane owns a contiguous block of the sorted list
+    const int per = (nk + 31) / 32;
+    const int i0 = min(lane * per, nk), i1 = min(i0 + per, nk);
+    DFloat mine = df_make(0.f, 0.f);
+    for (int i = i0; i < i1; ++i) mine = df_add(mine, df_make(se[i].x, 0.f));
     // inclusive scan of the lane blocks' masses, in pairs of floats
     DFloat incl = mine;
 #pragma unroll
@@ -186,11 +207,12 @@ __device__ void topk_request_draw(const SpecParams& P, const Plan& pl, int nk, f
                 float run = 0.f;
                 int lastpos = -1;
                 for (int i = i0; i < i1; ++i) {
-                    if (rr[i] > 0.f) lastpos = i;
-                    run += rr[i];
-                    if (tr < run && rr[i] > 0.f) { tok = __ldcg(&kl[i].idx); break; }
+                    const float ri = se[i].x;
+                    if (ri > 0.f) lastpos = i;
+                    run += ri;
+                    if (tr < run && ri > 0.f) { tok = se[i].idx; break; }
                 }
-                if (tok < 0 && lastpos >= 0) tok = __ldcg(&kl[lastpos].idx);
+                if (tok < 0 && lastpos >= 0) tok = se[lastpos].idx;
             }
             tok = __shfl_sync(FULL, tok, owner);
         }
@@ -798,7 +820,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
 }
 
 // Kernel 2, one warp per row: exact threshold g from the row's candidate groups (nsegr segment
-// lists of kernel 1, up to 1024 groups in all), the kept list sorted by index, and the
+// lists of kernel 1, up to 1024 groups in all), the kept list (in list order), and the
 // normaliser over it.  Each segment's final bound reaches at most g (at least k of the row's
 // elements reach it), so only the listed groups whose maximum reaches the largest of them, beta,
 // can hold an element >= g; their elements >= beta are the candidates from which g is selected
@@ -963,30 +985,19 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
     }
     __syncwarp();
     if (nk > P.cap_k) { st.dense = 1; return st; }
-    // sorted by index (the indices are distinct): each entry's rank is the number of smaller ones;
-    // the sorted list goes back into u
-    for (int i0 = 0; i0 < nk; i0 += 32) {
-        const int i = i0 + lane;
-        TopkEntry e;
-        e.idx = 0x7fffffff;
-        e.x = NEG_INF;
-        if (i < nk) e = kept[i];
-        int rank = 0;
-        for (int j = 0; j < nk; ++j) rank += kept[j].idx < e.idx;
-        if (i < nk) u[rank] = e;
-    }
-    __syncwarp();
+    // the normaliser over the kept entries: their maximum, and their mass in fixed point (an
+    // integer sum, exact whatever the order the lists delivered them in); the kept list is stored
+    // in that order and sorted by index only where a draw uses it
     float mx = NEG_INF;
-    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, u[i].x);
+    for (int i = lane; i < nk; i += 32) mx = fmaxf(mx, kept[i].x);
     const float M = warp_max(mx);
     const float MC = __fmul_rn(M, P.c);
-    // the sum of 2^(fma(x, c, -MC)) over the kept tokens, as a pair of floats
-    DFloat acc = df_make(0.f, 0.f);
+    unsigned long long fs = 0ull;
     if (M != NEG_INF)
-        for (int i = lane; i < nk; i += 32) acc = df_add(acc, df_make(ex2(fmaf(u[i].x, P.c, -MC)), 0.f));
-    const DFloat S = warp_sum_df(acc);
+        for (int i = lane; i < nk; i += 32) fs += fixed_mass(ex2(fmaf(kept[i].x, P.c, -MC)));
+    const DFloat S = fixed_to_df(warp_sum(fs));
     TopkEntry* kl = P.klist + (size_t)row_id * P.cap_k;
-    for (int i = lane; i < nk; i += 32) kl[i] = u[i];
+    for (int i = lane; i < nk; i += 32) kl[i] = kept[i];
     st.M = M;
     st.MC = MC;
     st.S = (double)S.hi;
@@ -1001,7 +1012,10 @@ __device__ RowStats topk_row_finish(const SpecParams& P, TopkEntry* u, TopkEntry
 // Kernel 2: one CTA per request, one warp per row (nw = min(R, FIN_MAX_WARPS) warps, rows w, w +
 // nw, ...): each warp finishes its row into shared memory; after one CTA barrier warp 0 runs the
 // acceptance scan over them and draws from the kept list of the p row.  A request with a dense row
-// is left to kernel 3.
+// is completed by the whole CTA with full-row passes instead.
+template <int DT>
+__device__ __noinline__ void topk_dense_request(const SpecParams& P, int b);
+
 constexpr int FIN_MAX_WARPS = 16;
 constexpr size_t FIN_MAX_SMEM = 200 * 1024;  // dynamic shared memory of one finish CTA, at most
 template <int DT>
@@ -1028,12 +1042,11 @@ __global__ void __launch_bounds__(FIN_MAX_WARPS * 32, 2) topk_finish_kernel(Spec
         __syncwarp();  // u and kept serve the next row
     }
     __syncthreads();
-    if (warp != 0) return;
-    const int nd = sdense;
-    if (nd > 0) {  // finished by topk_dense_kernel
-        if (lane == 0) P.ndense[b] = nd;
+    if (sdense > 0) {  // the whole CTA finishes the request exactly (rare)
+        topk_dense_request<DT>(P, b);
         return;
     }
+    if (warp != 0) return;
     Plan pl;
     int nk;
     if (R <= 32) {
@@ -1045,7 +1058,7 @@ __global__ void __launch_bounds__(FIN_MAX_WARPS * 32, 2) topk_finish_kernel(Spec
         pl = compute_plan_warp<DT, true>(P, b, true);
         nk = __ldcg(&P.rstats[(size_t)b * R + pl.rp].klist_n);
     }
-    topk_request_draw<DT>(P, pl, nk, reinterpret_cast<float*>(u), b);
+    topk_request_draw<DT>(P, pl, nk, u, b);
 }
 
 // ---------------------------------------------------------------- exact fallback for dense rows
@@ -1062,30 +1075,68 @@ __device__ __forceinline__ double topk_residual_at(const char* rowp, const char*
     return (double)fmaxf(__fsub_rn(pp, qq), 0.f);
 }
 
-__device__ __forceinline__ double block_sum_f64(double v, double* sh)
+// Block-wide reductions over the CTA's blockDim.x threads (a whole number of warps, at most 32):
+// warp partials in shared memory, combined in warp order.  Every thread receives the result.
+template <class T, class Op>
+__device__ __forceinline__ T cta_reduce(T v, T* sh /* >= 32 */, Op op)
 {
-    v = warp_sum(v);
+    const int nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
     __syncthreads();
     if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
     __syncthreads();
-    double r = 0.0;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) r += sh[w];
+    T r = sh[0];
+    for (int w = 1; w < nw; ++w) r = op(r, sh[w]);
     return r;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
+// sum over the CTA: fp32 within warps, fp64 across warps in warp order
+__device__ __forceinline__ double cta_sum_f32(float v, double* sh /* >= 32 */)
 {
-    __shared__ int sh_red[WARPS];
-    __shared__ double sh_d[WARPS];
-    __shared__ float sh_f[WARPS];
-    __shared__ int sh_tok;
+    const int nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = (double)v;
+    __syncthreads();
+    double r = 0.0;
+    for (int w = 0; w < nw; ++w) r += sh[w];
+    return r;
+}
 
-    // one CTA per request: it finishes the request's dense rows one after another, then scans
-    const int b = blockIdx.x;
-    pdl_wait();  // the row statistics of the finish kernel
-    if (__ldcg(&P.ndense[b]) == 0) return;
+// exclusive prefix sum in fp64 over the CTA (thread order); the total goes to *total
+__device__ __forceinline__ double cta_excl_scan_f64(double v, double* sh, double* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const double incl = warp_incl_scan(v);
+    __syncthreads();
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    double before = 0.0, tot = 0.0;
+    for (int w = 0; w < nw; ++w) {
+        if (w < warp) before += sh[w];
+        tot += sh[w];
+    }
+    *total = tot;
+    return before + (incl - v);
+}
+
+// The exact fallback for a request with a dense row (candidates that overflowed the lists: mass
+// ties, k > NT, ...), run by the whole finish CTA: each dense row's threshold by a bitwise search
+// over full-row counts and its normaliser by full-row passes; then the acceptance scan and the
+// correction / bonus draw by two passes of the residual over V (fp64 sums, tile by tile).
+template <int DT>
+__device__ __noinline__ void topk_dense_request(const SpecParams& P, int b)
+{
+    __shared__ int sh_i[32];
+    __shared__ float sh_f[32];
+    __shared__ double sh_d[32];
+    __shared__ int sh_tok;
+    __shared__ Plan sh_plan;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const auto add_i = [](int x, int y) { return x + y; };
+    const auto add_d = [](double x, double y) { return x + y; };
+    const auto max_f = [](float x, float y) { return fmaxf(x, y); };
     const int V = P.V, k = P.top_k;
     for (int r = 0; r < P.R; ++r) {
         const int row_id = b * P.R + r;
@@ -1097,27 +1148,27 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
         for (int bit = 31; bit >= lo; --bit) {
             const uint32_t want = prefix | (1u << bit);
             int cnt = 0;
-            for (int v = threadIdx.x; v < V; v += NT) cnt += okey(load_logit(row, DT, v)) >= want;
-            if (block_sum_int(cnt, sh_red) >= k) prefix = want;
+            for (int v = tid; v < V; v += nth) cnt += okey(load_logit(row, DT, v)) >= want;
+            if (cta_reduce(cnt, sh_i, add_i) >= k) prefix = want;
         }
         if (DT == DT_BF16 && prefix < 0x80000000u) prefix |= 0xffffu;
         const float g = key_value(prefix);
         float mx = NEG_INF;
-        for (int v = threadIdx.x; v < V; v += NT) {
+        for (int v = tid; v < V; v += nth) {
             const float x = load_logit(row, DT, v);
             if (x >= g) mx = fmaxf(mx, x);
         }
-        const float M = block_max(mx, sh_f);
+        const float M = cta_reduce(mx, sh_f, max_f);
         const float MC = __fmul_rn(M, P.c);
         float s = 0.f;
         if (M != NEG_INF)
-            for (int v = threadIdx.x; v < V; v += NT) {
+            for (int v = tid; v < V; v += nth) {
                 const float x = load_logit(row, DT, v);
                 if (x >= g) s += ex2(fmaf(x, P.c, -MC));
             }
-        const double S = block_sum_f32(s, sh_d);
-        if (threadIdx.x == 0) {
-            RowStats st;
+        const double S = cta_sum_f32(s, sh_d);
+        if (tid == 0) {
+            RowStats st = blank_rowstats();
             st.M = M; st.MC = MC; st.S = S; st.thr = g;
             st.status = (M != NEG_INF && isfinite(M) && S > 0.0) ? ROW_OK : ROW_NONFINITE;
             st.klist_n = -1;
@@ -1126,50 +1177,48 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
         }
         __syncthreads();
     }
-
-    __shared__ Plan sh_plan;
-    if (threadIdx.x < 32) {
+    if (tid < 32) {
         const Plan p0 = compute_plan_warp<DT>(P, b, true);
-        if (threadIdx.x == 0) sh_plan = p0;
+        if (tid == 0) sh_plan = p0;
     }
     __syncthreads();
     const Plan pl = sh_plan;
     if (pl.status != ROW_OK) {
-        emit_spec(P, b, pl.status, 0, -1);
+        if (tid < 32) emit_spec_n(P, b, pl.status, 0, -1, tid, 32);
         return;
     }
     const char* rowp = spec_row_ptr(P, b, pl.rp);
     const char* rowq = pl.rq >= 0 ? spec_row_ptr(P, b, pl.rq) : nullptr;
     // pass 1: total residual mass, tile by tile in index order (fp64)
     double Z = 0.0;
-    for (int t0 = 0; t0 < V; t0 += NT) {
-        const int v = t0 + threadIdx.x;
+    for (int t0 = 0; t0 < V; t0 += nth) {
+        const int v = t0 + tid;
         const double rv = v < V ? topk_residual_at<DT>(rowp, rowq, v, pl, P.c) : 0.0;
-        Z += block_sum_f64(rv, sh_d);
+        Z += cta_reduce(rv, sh_d, add_d);
     }
     if (!(Z > 0.0) || !isfinite(Z)) {
-        emit_spec(P, b, ROW_DEGENERATE, 0, -1);
+        if (tid < 32) emit_spec_n(P, b, ROW_DEGENERATE, 0, -1, tid, 32);
         return;
     }
     // pass 2: the tile where the running mass passes u*Z, then the element inside it
     const double t = pl.u * Z;
     double run = 0.0;
     int tok = -1;
-    for (int t0 = 0; t0 < V; t0 += NT) {
-        const int v = t0 + threadIdx.x;
+    for (int t0 = 0; t0 < V; t0 += nth) {
+        const int v = t0 + tid;
         const double rv = v < V ? topk_residual_at<DT>(rowp, rowq, v, pl, P.c) : 0.0;
-        const double ts = block_sum_f64(rv, sh_d);
+        const double ts = cta_reduce(rv, sh_d, add_d);
         if (t < run + ts) {  // uniform across the CTA
             double tot;
-            const double excl = block_excl_scan_f64(rv, sh_d, &tot);
-            if (threadIdx.x == 0) sh_tok = 0x7fffffff;
+            const double excl = cta_excl_scan_f64(rv, sh_d, &tot);
+            if (tid == 0) sh_tok = 0x7fffffff;
             __syncthreads();
             if (rv > 0.0 && t < run + excl + rv) atomicMin(&sh_tok, v);
             __syncthreads();
             tok = sh_tok;
             if (tok == 0x7fffffff) {  // rounding: last positive entry of the tile
                 __syncthreads();
-                if (threadIdx.x == 0) sh_tok = -1;
+                if (tid == 0) sh_tok = -1;
                 __syncthreads();
                 if (rv > 0.0) atomicMax(&sh_tok, v);
                 __syncthreads();
@@ -1181,16 +1230,15 @@ __global__ void __launch_bounds__(NT) topk_dense_kernel(SpecParams P)
     }
     if (tok < 0) {  // rounding ran past the end: last token with positive mass
         __syncthreads();
-        if (threadIdx.x == 0) sh_tok = -1;
+        if (tid == 0) sh_tok = -1;
         __syncthreads();
-        for (int v = threadIdx.x; v < V; v += NT)
+        for (int v = tid; v < V; v += nth)
             if (topk_residual_at<DT>(rowp, rowq, v, pl, P.c) > 0.0) atomicMax(&sh_tok, v);
         __syncthreads();
         tok = sh_tok;
     }
-    emit_spec(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok);
+    if (tid < 32) emit_spec_n(P, b, tok >= 0 ? ROW_OK : ROW_DEGENERATE, pl.A, tok, tid, 32);
 }
-
 
 template <int DT>
 static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
@@ -1211,7 +1259,6 @@ static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
     const size_t fsm = (size_t)fw * per_warp;
     set_smem_limit<topk_finish_kernel<DT>>(fsm);
     launch_dependent(topk_finish_kernel<DT>, (unsigned)P.B, (unsigned)(32 * fw), fsm, st, P);
-    launch_dependent(topk_dense_kernel<DT>, (unsigned)P.B, NT, 0, st, P);
 }
 
 cudaError_t launch_topk_path(const SpecParams& P, int sms, cudaStream_t st)

@@ -51,18 +51,6 @@ __device__ __forceinline__ float key_float(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
-// The fixed-point mass 2^40 w (rounded toward zero) of w in [0, 1], from the float's bits with
-// integer operations only (a conversion to a 64-bit integer is not a fast-pipe instruction).
-__device__ __forceinline__ unsigned long long fixed_mass(float w)
-{
-    const uint32_t u = __float_as_uint(w);
-    const int e = (int)(u >> 23);  // biased exponent; w >= 0
-    if (e == 0) return 0ull;       // zero (the exponential flushes subnormals)
-    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
-    const int sh = e - 127 - 23 + 40;  // 2^40 w = m 2^sh, sh <= 17
-    return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0ull);
-}
-
 // fast path geometry: candidates have y >= -TOPP_CUT (mass at least 2^-14 of the row maximum's);
 // TOPP_BINS bins of width TOPP_CUT / TOPP_BINS over (-TOPP_CUT, 0] (anything lower in the last); the
 // crossing bin is resolved when it holds at most TOPP_SORT candidates.  The candidate list takes TOPP_LIST bytes: stored bf16 bit
@@ -322,7 +310,7 @@ __global__ void __launch_bounds__(NT, 5) topp_row_kernel(SpecParams P)
             }
             __syncthreads();
             // the row's total mass (every element; the stream's pairs of floats) in 2^-40 units
-            const double target = (double)P.top_p * (df_to_double(S) * 1099511627776.0);
+            const double target = (double)P.top_p * (df_to_double(S) * FIXED_ONE);
             // the crossing bin: thread t holds bins [8t, 8t + 8)
             constexpr int BPT = TOPP_BINS / NT;
             unsigned long long loc[BPT], s = 0ull;
@@ -409,9 +397,7 @@ __global__ void __launch_bounds__(NT, 5) topp_row_kernel(SpecParams P)
     }
     if (fast) {
         thr = sh_thr;
-        const double kept = (double)sh_kept * (1.0 / 1099511627776.0);
-        const float hi = (float)kept;
-        S = df_make(hi, (float)(kept - (double)hi));
+        S = fixed_to_df(sh_kept);
     }
 
     // ---- the nucleus threshold, fallback: a radix select on the key, weighted by fixed-point mass
@@ -487,9 +473,7 @@ __global__ void __launch_bounds__(NT, 5) topp_row_kernel(SpecParams P)
         if (KB < 32 && !(gk & 0x80000000u)) gk |= (1u << (32 - KB)) - 1u;
         thr = key_float(gk);
         // the kept mass as a pair of floats (2^-40 units, exact in fp64 up to 2^53)
-        const double kept = (double)sh_kept * (1.0 / 1099511627776.0);
-        const float hi = (float)kept;
-        S = df_make(hi, (float)(kept - (double)hi));
+        S = fixed_to_df(sh_kept);
     }
 
     // ---- the row's statistics, as the plain path's row plan forms them
