@@ -89,6 +89,7 @@ constexpr int U2 = 4, ST2 = 4, TV2 = 32 * U2 * ST2;  // residual pass over a row
 constexpr int RCV = 8;  // residual pass over 16-byte vectors: vectors per row and thread of one CTA
 constexpr int SEGV = 32;                             // vectors per residual segment
 enum { RES_PLAIN = 0, RES_MASK = 1, RES_THR = 2 };   // residual pass variants
+enum { MASK_NONE = 0, MASK_REGS = 1, MASK_RING = 2 };  // streaming kernel: where mask bits come from
 
 struct SpecParams {
     const void* target;   // [B, gamma+1, V]
@@ -176,6 +177,32 @@ struct TreeParams {
 };
 
 // ---------------------------------------------------------------- small device helpers
+
+// Pairs of fp32 in one 64-bit register, with the packed fp32 instructions of this GPU family: each
+// half is computed exactly as the scalar instruction would (same rounding, no flush to zero).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -355,6 +382,22 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
                  :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol) : "memory");
 }
 
+// Two bulk copies completing on one barrier: `bytes` and `bytes2` (multiples of 16; all addresses
+// 16-byte aligned) from global to shared memory.  Called by one thread.
+__device__ __forceinline__ void bulk_load2(void* dst, const void* src, unsigned bytes, void* dst2,
+                                           const void* src2, unsigned bytes2, uint64_t* bar,
+                                           uint64_t pol, uint64_t pol2)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes + bytes2) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_addr(dst2)), "l"(src2), "r"(bytes2), "r"(smem_addr(bar)), "l"(pol2) : "memory");
+}
+
 // One arrival on `bar` (release: this thread's earlier shared-memory reads are ordered before it).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
@@ -382,6 +425,10 @@ constexpr int STREAM_CHUNK_BYTES = 32768;
 constexpr int STREAM_NV = STREAM_CHUNK_BYTES / (NT * 16);  // 16-byte vectors per thread (8)
 constexpr int STREAM_STAGES = 3;
 constexpr int STREAM_SMEM = STREAM_STAGES * STREAM_CHUNK_BYTES;
+// a stage's grammar-mask bits when they travel with the chunk: one bit per element, at most a bf16
+// chunk's (STREAM_CHUNK_BYTES / 2 elements)
+constexpr int STREAM_MASK_BYTES = STREAM_CHUNK_BYTES / 16;
+constexpr int STREAM_SMEM_MASKED = STREAM_SMEM + STREAM_STAGES * STREAM_MASK_BYTES;
 
 // Warp-specialised streaming (the plain and tree kernels): one producer lane issues the CTA's chunks
 // ids blockIdx.x, + gridDim.x, ... (< nch) into the STREAM_STAGES-stage ring, refilling a stage once

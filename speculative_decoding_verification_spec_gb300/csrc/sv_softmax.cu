@@ -268,16 +268,21 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
 // (chunk, warp).  Warp-specialised: a producer warp fills the ring (ring_produce) and the consumer
 // warps release each stage on its "empty" mbarrier, so they never wait for one another.
 // NaN or +inf anywhere makes the partial's sum NaN, so the row merge reports the row non-finite.
-// MASK: the grammar mask's bits of the thread's vectors are applied to the raw vectors as they leave
-// shared memory.  They are loaded two chunks ahead into one of two register sets used in turn, so
-// their latency (a DRAM miss under full load) hides behind the chunks in between.
-template <int DT, bool MASK>
+// MASK (a grammar mask): the mask bits of the thread's vectors are applied to the raw vectors as
+// they leave shared memory.  MASK_RING: the producer copies a chunk's mask bits (one bit per
+// element) into the stage beside its logits, with a second bulk copy completing on the same barrier
+// (mask rows of a multiple of 16 bytes, 16-byte aligned).  MASK_REGS otherwise: each thread loads
+// its bits two chunks ahead into one of two register sets used in turn, so their latency hides
+// behind the chunks in between.
+template <int DT, int MASK>
 __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int CHUNK = NT * STREAM_NV * VEC;  // elements per chunk
     extern __shared__ __align__(128) uint4 ring[];  // STREAM_STAGES x (NT * STREAM_NV) vectors
+    // MASK_RING: then STREAM_STAGES x STREAM_MASK_BYTES of mask bits
+    uint32_t* mring = reinterpret_cast<uint32_t*>(ring + (size_t)STREAM_STAGES * NT * STREAM_NV);
     __shared__ __align__(8) uint64_t full[STREAM_STAGES];
     __shared__ __align__(8) uint64_t empty[STREAM_STAGES];
     __shared__ int sfail;  // a wait ran out in this CTA: nothing more is read
@@ -298,6 +303,41 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
         fence_mbar_init();
     }
     __syncthreads();
+    if (warp == WARPS && MASK == MASK_RING) {  // the producer, with each chunk's mask bits
+        if (lane == 0) {
+            int ps = 0;
+            unsigned pph = 0;
+            long long n = 0;
+            for (int id = blockIdx.x; id < nch; id += G0) {
+                if (*reinterpret_cast<volatile int*>(&sfail)) break;
+                if (n >= STREAM_STAGES && !mbar_wait(&empty[ps], pph ^ 1u, P.wait_limit)) {
+                    *reinterpret_cast<volatile int*>(&sfail) = 1;
+                    break;
+                }
+                const int rid = id / P.S1, cix = id - rid * P.S1;
+                const int b = rid / P.R, r = rid - b * P.R;
+                const int cbase = cix * CHUNK, cend = min(cbase + CHUNK, P.V);
+                // the chunk's mask words, rounded up to 16 bytes: inside the row, whose words are a
+                // multiple of four
+                const unsigned mbytes = (unsigned)((((cend - cbase + 31) >> 5) + 3) & ~3) * 4u;
+                bulk_load2(ring + (size_t)ps * NT * STREAM_NV, spec_row_ptr(P, b, r) + (size_t)cbase * ES,
+                           (unsigned)(cend - cbase) * ES,
+                           mring + (size_t)ps * (STREAM_MASK_BYTES / 4),
+                           spec_mask_row(P, b, r) + (size_t)cix * (CHUNK / 32), mbytes, &full[ps],
+                           pinned_row(P, r) ? policy_evict_normal() : policy_evict_first(),
+                           policy_evict_first());
+                ++n;
+                if (++ps == STREAM_STAGES) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
+            }
+            // the last fill of every stage: no later fill of that stage exists
+            for (long long j = (n > STREAM_STAGES ? n - STREAM_STAGES : 0); j < n; ++j)
+                (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u, MBAR_SPIN_LIMIT);
+        }
+        return;
+    }
     if (warp == WARPS) {  // the producer: the rows of the likely correction pairs stay in L2
         if (lane == 0)
             ring_produce(ring, full, empty, &sfail, nch, P.wait_limit,
@@ -369,12 +409,36 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
                 if (ok && cbase + (j * NT + tid) * VEC < cend) w[j] = lds128(sb + j * NT);
             }
         }
-        if constexpr (MASK) {
+        // MASK: vector j of every lane of the warp fully masked (bit j) is skipped below: its
+        // elements would only add 2^-inf = 0
+        unsigned skipm = 0u;
+        if constexpr (MASK != MASK_NONE) {
+            uint32_t bits[STREAM_NV];
+            if constexpr (MASK == MASK_REGS) {
 #pragma unroll
-            for (int j = 0; j < STREAM_NV; ++j) mask_raw<DT, VEC>(w[j], mreg[j]);
-            // this register set is free again: the bits of the chunk two ahead
-            if ((long long)id + 2 * G0 < nch) load_mask(pr, pc, mreg);
-            advance(pr, pc);
+                for (int j = 0; j < STREAM_NV; ++j) bits[j] = mreg[j];
+                // this register set is free again: the bits of the chunk two ahead
+                if ((long long)id + 2 * G0 < nch) load_mask(pr, pc, mreg);
+                advance(pr, pc);
+            } else {
+                // vector j * NT + tid of the chunk: word (j * NT + tid) * VEC / 32 of the stage's bits
+                const uint32_t* mw = mring + (size_t)s * (STREAM_MASK_BYTES / 4);
+#pragma unroll
+                for (int j = 0; j < STREAM_NV; ++j) {
+                    const int e0 = (j * NT + tid) * VEC;
+                    bits[j] = (ok && (!partial || cbase + e0 < cend))
+                                  ? (mw[e0 >> 5] >> (e0 & 31)) & ((1u << VEC) - 1u) : 0u;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < STREAM_NV; ++j) {
+                if (__all_sync(FULL, bits[j] == 0u)) {
+                    skipm |= 1u << j;
+                    w[j] = make_uint4(pad, pad, pad, pad);
+                } else {
+                    mask_raw<DT, VEC>(w[j], bits[j]);
+                }
+            }
         }
         // release the stage once every lane has read it; a warp whose wait ran out never releases
         // it (its copy may still land), which stops the producer
@@ -412,31 +476,41 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
             }
             const float M = warp_max(m);
             const float MC = __fmul_rn(M, c);
-            // sum of 2^(x c - MC) in four fp32 accumulators, combined in a fixed order
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            // sum of 2^(x c - MC) in four fp32 accumulators, combined in a fixed order: a0 and a1
+            // take the low and high elements of words x and z, a2 and a3 those of y and w, two at a
+            // time with the packed fp32 instructions (each half rounds as the scalar one would)
+            unsigned long long a01 = 0ull, a23 = 0ull;
             if (M != NEG_INF) {
+                const unsigned long long c2 = f2_pack(c, c), nmc2 = f2_pack(-MC, -MC);
+                auto acc2 = [&](unsigned long long& a, float lo, float hi) {
+                    float ylo, yhi;
+                    f2_unpack(f2_fma(f2_pack(lo, hi), c2, nmc2), ylo, yhi);
+                    a = f2_add(a, f2_pack(ex2(ylo), ex2(yhi)));
+                };
 #pragma unroll
                 for (int j = 0; j < STREAM_NV; ++j) {
+                    if (MASK != MASK_NONE && ((skipm >> j) & 1u)) continue;  // the same in every lane
                     if constexpr (DT == DT_BF16) {
-                        a0 += ex2(fmaf(bf16lo(w[j].x), c, -MC)); a1 += ex2(fmaf(bf16hi(w[j].x), c, -MC));
-                        a2 += ex2(fmaf(bf16lo(w[j].y), c, -MC)); a3 += ex2(fmaf(bf16hi(w[j].y), c, -MC));
-                        a0 += ex2(fmaf(bf16lo(w[j].z), c, -MC)); a1 += ex2(fmaf(bf16hi(w[j].z), c, -MC));
-                        a2 += ex2(fmaf(bf16lo(w[j].w), c, -MC)); a3 += ex2(fmaf(bf16hi(w[j].w), c, -MC));
+                        acc2(a01, bf16lo(w[j].x), bf16hi(w[j].x));
+                        acc2(a23, bf16lo(w[j].y), bf16hi(w[j].y));
+                        acc2(a01, bf16lo(w[j].z), bf16hi(w[j].z));
+                        acc2(a23, bf16lo(w[j].w), bf16hi(w[j].w));
                     } else {
-                        a0 += ex2(fmaf(__uint_as_float(w[j].x), c, -MC));
-                        a1 += ex2(fmaf(__uint_as_float(w[j].y), c, -MC));
-                        a2 += ex2(fmaf(__uint_as_float(w[j].z), c, -MC));
-                        a3 += ex2(fmaf(__uint_as_float(w[j].w), c, -MC));
+                        acc2(a01, __uint_as_float(w[j].x), __uint_as_float(w[j].y));
+                        acc2(a23, __uint_as_float(w[j].z), __uint_as_float(w[j].w));
                     }
                 }
             }
+            float a0, a1, a2, a3;
+            f2_unpack(a01, a0, a1);
+            f2_unpack(a23, a2, a3);
             pt.M = M;
             pt.MC = MC;
             pt.S = warp_sum((a0 + a1) + (a2 + a3));
         }
         if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
     };
-    if constexpr (MASK) {
+    if constexpr (MASK == MASK_REGS) {
         // two register sets in turn, so that no register move waits for a load still in flight
         uint32_t mA[STREAM_NV], mB[STREAM_NV];
         if (blockIdx.x < nch) load_mask(pr, pc, mA);
@@ -728,16 +802,17 @@ static void launch_softmax_plain(const SpecParams& P, int sms, cudaStream_t st)
     spec_resample_kernel<DT, VEC><<<persistent_grid<spec_resample_kernel<DT, VEC>>(P.tasks2, sms), NT, 0, st>>>(P);
 }
 
-template <int DT, bool MASK>
+template <int DT, int MASK>
 static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
 {
     constexpr auto K1 = spec_stream_kernel<DT, MASK>;
+    constexpr int smem = MASK == MASK_RING ? STREAM_SMEM_MASKED : STREAM_SMEM;
     mark_kernel_start(st);
-    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
+    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, smem, NT + 32), NT + 32, smem, st>>>(P);
     mark_kernel_stop(st);
     const int pw = (P.R <= 32) ? std::min(P.R, PLAN_WARPS) : WARPS;
     launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, (unsigned)(32 * pw), 0, st, P);
-    launch_dependent(spec_resample_chunk_kernel<DT, MASK ? RES_MASK : RES_PLAIN>,
+    launch_dependent(spec_resample_chunk_kernel<DT, MASK != MASK_NONE ? RES_MASK : RES_PLAIN>,
                      (unsigned)((long long)P.B * P.S2), NT, 0, st, P);
 }
 
@@ -748,10 +823,10 @@ cudaError_t launch_softmax_stats(const SpecParams& P, int sms, cudaStream_t st)
     mark_kernel_start(st);
     if (P.vec > 1) {
         if (P.dtype == DT_BF16) {
-            constexpr auto K1 = spec_stream_kernel<DT_BF16, false>;
+            constexpr auto K1 = spec_stream_kernel<DT_BF16, MASK_NONE>;
             K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
         } else {
-            constexpr auto K1 = spec_stream_kernel<DT_F32, false>;
+            constexpr auto K1 = spec_stream_kernel<DT_F32, MASK_NONE>;
             K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
         }
     } else if (P.dtype == DT_BF16) {
@@ -783,14 +858,18 @@ cudaError_t launch_softmax_resample_thr(const SpecParams& P, int sms, cudaStream
 cudaError_t launch_softmax_path(const SpecParams& P, int sms, cudaStream_t st)
 {
     const bool mask = P.mask != nullptr;
+    // the mask bits can travel with the chunks when every mask row is a whole number of 16 bytes
+    const bool ring_mask = mask && P.mwords % 4 == 0 && (reinterpret_cast<uintptr_t>(P.mask) & 15) == 0;
     if (P.dtype == DT_BF16 && P.vec == 8) {
-        if (mask) launch_softmax_chunk<DT_BF16, true>(P, sms, st);
-        else launch_softmax_chunk<DT_BF16, false>(P, sms, st);
+        if (mask && ring_mask) launch_softmax_chunk<DT_BF16, MASK_RING>(P, sms, st);
+        else if (mask) launch_softmax_chunk<DT_BF16, MASK_REGS>(P, sms, st);
+        else launch_softmax_chunk<DT_BF16, MASK_NONE>(P, sms, st);
     } else if (P.dtype == DT_BF16) {
         launch_softmax_plain<DT_BF16, 1>(P, sms, st);
     } else if (P.vec == 4) {
-        if (mask) launch_softmax_chunk<DT_F32, true>(P, sms, st);
-        else launch_softmax_chunk<DT_F32, false>(P, sms, st);
+        if (mask && ring_mask) launch_softmax_chunk<DT_F32, MASK_RING>(P, sms, st);
+        else if (mask) launch_softmax_chunk<DT_F32, MASK_REGS>(P, sms, st);
+        else launch_softmax_chunk<DT_F32, MASK_NONE>(P, sms, st);
     } else {
         launch_softmax_plain<DT_F32, 1>(P, sms, st);
     }
