@@ -278,6 +278,14 @@ __device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
     return r;
 }
 
+// fp32 maximum that propagates NaN
+__device__ __forceinline__ float fmax_nan(float a, float b)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 // one logit as fp32 (scalar path)
 __device__ __forceinline__ float load_logit(const void* row, int dtype, long long i)
 {

@@ -63,12 +63,6 @@ __device__ __forceinline__ TopkEntry ld_entry(const TopkEntry* p)
     return e;
 }
 
-__device__ __forceinline__ float fmax_nan_f(float a, float b)
-{
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
 
 // The k-th largest key (largest P with count(key >= P) >= k) among n keys produced by key_at(i),
 // by one warp: bitwise search from the top bit, counting with a warp reduction per bit.
@@ -400,16 +394,16 @@ __device__ uint32_t chunk_tau_key(const uint4* stage, const char* row, int cbase
                     if constexpr (DT == DT_BF16) {
                         pm = bmax2_nan(pm, bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w)));
                     } else {
-                        tm = fmax_nan_f(tm, fmax_nan_f(fmax_nan_f(__uint_as_float(q.x), __uint_as_float(q.y)),
-                                                       fmax_nan_f(__uint_as_float(q.z), __uint_as_float(q.w))));
+                        tm = fmax_nan(tm, fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                                       fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w))));
                     }
                 }
             }
-            if constexpr (DT == DT_BF16) tm = fmax_nan_f(bf16lo(pm), bf16hi(pm));
+            if constexpr (DT == DT_BF16) tm = fmax_nan(bf16lo(pm), bf16hi(pm));
         } else {
             for (int s = 0; s < EPT; ++s) {
                 const int e = cbase + s * NT + g;
-                if (e < cend) tm = fmax_nan_f(tm, load_logit(row, DT, e));
+                if (e < cend) tm = fmax_nan(tm, load_logit(row, DT, e));
             }
         }
         keys[j] = okey(tm);
@@ -708,7 +702,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
 #pragma unroll
                 for (int j = 1; j < G; ++j) {
                     if constexpr (DT == DT_BF16) m = bmax2_nan(m, w[g * G + j]);
-                    else m = __float_as_uint(fmax_nan_f(__uint_as_float(m), __uint_as_float(w[g * G + j])));
+                    else m = __float_as_uint(fmax_nan(__uint_as_float(m), __uint_as_float(w[g * G + j])));
                 }
                 gm[g] = m;
             }
@@ -717,11 +711,11 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 uint32_t pm = gm[0];
 #pragma unroll
                 for (int g = 1; g < NG; ++g) pm = bmax2_nan(pm, gm[g]);
-                tm = fmax_nan_f(bf16lo(pm), bf16hi(pm));
+                tm = fmax_nan(bf16lo(pm), bf16hi(pm));
             } else {
                 tm = __uint_as_float(gm[0]);
 #pragma unroll
-                for (int g = 1; g < NG; ++g) tm = fmax_nan_f(tm, __uint_as_float(gm[g]));
+                for (int g = 1; g < NG; ++g) tm = fmax_nan(tm, __uint_as_float(gm[g]));
             }
             const bool bad_now = __any_sync(FULL, tm != tm || tm == __int_as_float(0x7f800000));
 

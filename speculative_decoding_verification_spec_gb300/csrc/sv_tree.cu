@@ -12,13 +12,6 @@
 
 namespace sv {
 
-__device__ __forceinline__ float fmax_nan(float a, float b)
-{
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
 // (value, index) order: larger value first, then the lower index
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi)
 {

@@ -59,13 +59,6 @@ __device__ __forceinline__ float lg2(float x)
     return y;
 }
 
-__device__ __forceinline__ float fmax_nan(float a, float b)
-{
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
 // element e of a 16-byte vector
 template <int DT>
 __device__ __forceinline__ float ts_val(const uint4& w, int e)

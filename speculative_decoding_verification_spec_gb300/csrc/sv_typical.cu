@@ -143,23 +143,39 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
             }
             const float M = warp_max(m);
             const float MC = __fmul_rn(M, c);
-            float s0 = 0.f, s1 = 0.f, e0 = 0.f, e1 = 0.f;
+            // s0, e0 take the low elements of each word (fp32: words x and z), s1, e1 the high ones
+            // (y and w), two at a time with the packed fp32 instructions (each half rounds as the
+            // scalar one would).  A -inf logit is raised to -1e30 first (NaN kept), so that its
+            // y is finite and its e * y is 0, as typ_acc's clamp of y makes it.
+            unsigned long long s01 = 0ull, e01 = 0ull;
             if (M != NEG_INF) {
+                const unsigned long long c2 = f2_pack(c, c), nmc2 = f2_pack(-MC, -MC);
+                auto acc2 = [&](float lo, float hi) {
+                    const unsigned long long y2 = f2_fma(f2_pack(lo, hi), c2, nmc2);
+                    float ylo, yhi;
+                    f2_unpack(y2, ylo, yhi);
+                    const unsigned long long w2 = f2_pack(ex2(ylo), ex2(yhi));
+                    s01 = f2_add(s01, w2);
+                    e01 = f2_fma(w2, y2, e01);
+                };
 #pragma unroll
                 for (int j = 0; j < STREAM_NV; ++j) {
                     if constexpr (DT == DT_BF16) {
-                        typ_acc(bf16lo(w[j].x), c, MC, s0, e0); typ_acc(bf16hi(w[j].x), c, MC, s1, e1);
-                        typ_acc(bf16lo(w[j].y), c, MC, s0, e0); typ_acc(bf16hi(w[j].y), c, MC, s1, e1);
-                        typ_acc(bf16lo(w[j].z), c, MC, s0, e0); typ_acc(bf16hi(w[j].z), c, MC, s1, e1);
-                        typ_acc(bf16lo(w[j].w), c, MC, s0, e0); typ_acc(bf16hi(w[j].w), c, MC, s1, e1);
+                        constexpr uint32_t FLOOR2 = 0xf149f149u;  // bf16 -9.95e29, twice
+                        const uint32_t q[4] = {bmax2_nan(w[j].x, FLOOR2), bmax2_nan(w[j].y, FLOOR2),
+                                               bmax2_nan(w[j].z, FLOOR2), bmax2_nan(w[j].w, FLOOR2)};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) acc2(bf16lo(q[k]), bf16hi(q[k]));
                     } else {
-                        typ_acc(__uint_as_float(w[j].x), c, MC, s0, e0);
-                        typ_acc(__uint_as_float(w[j].y), c, MC, s1, e1);
-                        typ_acc(__uint_as_float(w[j].z), c, MC, s0, e0);
-                        typ_acc(__uint_as_float(w[j].w), c, MC, s1, e1);
+                        const float fl = -1.0e30f;
+                        acc2(fmax_nan(__uint_as_float(w[j].x), fl), fmax_nan(__uint_as_float(w[j].y), fl));
+                        acc2(fmax_nan(__uint_as_float(w[j].z), fl), fmax_nan(__uint_as_float(w[j].w), fl));
                     }
                 }
             }
+            float s0, s1, e0, e1;
+            f2_unpack(s01, s0, s1);
+            f2_unpack(e01, e0, e1);
             pt.M = M;
             pt.MC = MC;
             pt.S = warp_sum(s0 + s1);
