@@ -8,8 +8,11 @@
 //     fma() rounds once after the exact product, so the exponent carries only a small error near
 //     the row maximum, where probability mass sits; the rounding of MC shifts every exponent of a
 //     row equally and cancels between numerator and S.
-//   * per-thread and per-warp partial sums are fp32; sums across warps, chunks and segments are
-//     fp64, always in a fixed order, so results do not depend on CTA scheduling.
+//   * per-thread and per-warp partial sums are fp32 (two at a time with the packed fp32
+//     instructions where a loop carries pairs); sums across warps, chunks and segments are pairs of
+//     floats (about 48 bits) or fp64 lane totals, and masses that decide a kept set are fixed-point
+//     integers; every sum is taken in a fixed order or is exact, so results do not depend on CTA
+//     scheduling.
 #pragma once
 
 #include <utility>

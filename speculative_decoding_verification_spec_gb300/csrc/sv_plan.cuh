@@ -4,7 +4,8 @@
 // M7.1 section 0x03 / Module 16 "The Math: Speculative Sampling": draft token x_i is accepted when
 // u_i < a_i = min(1, p_i(x_i) / q_i(x_i)); M7.1 section 0x03G: the round stops at the first
 // rejection A; the correction row pair is (p_A, q_A), or the bonus row p_gamma when every draft
-// token is accepted (M7.1 section 0x03H).  The ratio is formed in the log2 domain in fp64:
+// token is accepted (M7.1 section 0x03H).  The ratio is formed in the log2 domain, in pairs of
+// floats (about 48 bits):
 //   log2 p_i(x) = fma(x, c, -MC_i) - log2(S_i)      (same exponent as the row's own sum)
 // so that MC's rounding cancels exactly.
 #pragma once

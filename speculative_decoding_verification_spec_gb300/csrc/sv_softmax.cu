@@ -4,14 +4,15 @@
 // Kernel 1 (row statistics).  Rows of 16-byte vectors: spec_stream_kernel, persistent CTAs that
 // fetch 32 KB chunks with bulk copies into a shared-memory ring and write one (max, sum of
 // 2^(x c - max c)) partial per (chunk, warp) -- the (m, l) pairs of M7.1 section 0x04J; then
-// spec_rowplan_kernel merges each row's partials (fp64, chunk order) with one warp per row, and
-// the last warp of a request runs the acceptance scan (sv_plan.cuh).  Rows that are not 16-byte
-// aligned use persistent warps with plain loads and do the same merge through completion counters.
+// spec_rowplan_kernel merges each row's partials (pairs of floats, chunk order) with one warp per
+// row, and the last warp of a request runs the acceptance scan (sv_plan.cuh).  Rows that are not
+// 16-byte aligned use persistent warps with plain loads and do the same merge through completion
+// counters.
 //
 // Kernel 2 (residual draw): r = max(p - q, 0) (M7.1 section 0x03C; p alone for the bonus, 0x03H)
 // over the selected row pair, summed per segment of 32 vectors; the last CTA of a request scans the
-// segment sums in fp64 in index order, finds the segment where the running mass passes u * Z, and
-// resolves the token inside it.
+// segment sums in index order (lane totals in fp64), finds the segment where the running mass
+// passes u * Z, and resolves the token inside it.
 //
 // Rows of the two row pairs most likely to be corrected (pairs 0 and 1) are read with the L2
 // evict_normal policy and all other rows evict_first, so that kernel 2 tends to find them in L2.
