@@ -413,6 +413,18 @@ void spec_set_kernel_events(void* start, void* stop);
  */
 int spec_set_wait_limit(int polls);
 
+/*
+ * Measurement aid: the cluster size of tree_verify_sample.  A request's walk runs on one
+ * thread-block cluster of CL CTAs that split the vocabulary into CL slices ("M7.7 - Draft Sources,
+ * Dependent Heads, Hardware-Aware Trees", 0x09A: every step of the walk needs the whole row).  By
+ * default (cl = 0) CL is the smallest power of two whose slices hold a row in registers (4 16-byte
+ * vectors per thread of 512), widened up to 8 while the GPU has an SM for every CTA.  cl = 1, 2, 4,
+ * 8 or 16 forces that size instead; a call whose row does not fit the forced slices returns
+ * SPEC_ERR_INVALID_ARG.  Any other value restores the default.  Returns the previous setting.
+ * Process-wide, read when a call is issued; not synchronised.
+ */
+int spec_set_tree_sample_cluster(int cl);
+
 /* Static description of a call-level status code. */
 const char* spec_status_string(spec_status s);
 

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     Workspace,
     load,
     set_kernel_events,
+    set_tree_sample_cluster,
     set_wait_limit,
     smc_verify,
     spec_verify,

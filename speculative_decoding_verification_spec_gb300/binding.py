@@ -21,7 +21,8 @@ ROW_BAD_PARENT, ROW_OVERFLOW, ROW_BAD_UNIFORM, ROW_BAD_QROW = 5, 6, 7, 8
 EXPORTS = ("spec_workspace_bytes", "spec_verify", "spec_verify_topk", "spec_verify_topp",
            "spec_verify_masked",
            "tree_verify_greedy", "spec_verify_greedy",
-           "tree_verify_sample", "tree_verify_typical", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_set_wait_limit", "spec_status_string")
+           "tree_verify_sample", "tree_verify_typical", "smc_verify", "spec_verify_noalloc", "spec_set_kernel_events", "spec_set_wait_limit",
+           "spec_set_tree_sample_cluster", "spec_status_string")
 
 # fixed scratch of spec_verify_noalloc (SPEC_NOALLOC_SCRATCH_BYTES in the header)
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -71,6 +72,8 @@ def load(path: str | None = None):
     lib.spec_set_kernel_events.restype = None
     lib.spec_set_wait_limit.argtypes = [I]
     lib.spec_set_wait_limit.restype = I
+    lib.spec_set_tree_sample_cluster.argtypes = [I]
+    lib.spec_set_tree_sample_cluster.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -148,6 +151,12 @@ def set_wait_limit(polls: int) -> int:
     so every request of a streaming call reports ROW_TIMEOUT; negative: the default).  Returns
     the previous limit."""
     return int(load().spec_set_wait_limit(int(polls)))
+
+
+def set_tree_sample_cluster(cl: int) -> int:
+    """Measurement aid: force tree_verify_sample's cluster size (1, 2, 4, 8 or 16 CTAs per request;
+    anything else: the automatic choice).  Returns the previous setting (0: automatic)."""
+    return int(load().spec_set_tree_sample_cluster(int(cl)))
 
 
 def workspace_bytes(B, gamma, V, top_k=0, tree_nodes=0) -> int:

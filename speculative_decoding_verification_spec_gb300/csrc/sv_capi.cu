@@ -16,6 +16,8 @@ namespace sv {
 KernelEvents g_kernel_events;
 // polls of a ring or segment wait before it gives up (spec_set_wait_limit); read at every call
 static int g_wait_limit = MBAR_SPIN_LIMIT;
+// tree_verify_sample's cluster size when forced (spec_set_tree_sample_cluster), else 0
+static int g_ts_cluster = 0;
 
 constexpr size_t ALIGN = 256;
 static inline size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
@@ -611,11 +613,16 @@ spec_status tree_verify_sample(const void* target_logits, const void* draft_logi
     int CL = 1;
     while (CL <= TS_MAX_CLUSTER && cdiv(nvec, (long long)CL * TS_NT) > TS_VPT) CL *= 2;
     if (CL > TS_MAX_CLUSTER) return SPEC_ERR_INVALID_ARG;  // V above the cluster's capacity
-    // ... widened, up to the portable 8, while the doubled cluster still leaves every CTA an SM of
-    // its own and each thread at least one vector (a wider cluster shares a row among more SMs, but
-    // every exchange between them then costs more)
-    const int sms = sm_count();
-    while (CL < 8 && 2LL * B * CL <= sms && nvec >= 2LL * CL * TS_NT) CL *= 2;
+    if (g_ts_cluster > 0) {  // a forced size (measurement aid), if its slices hold the row
+        if (cdiv(nvec, (long long)g_ts_cluster * TS_NT) > TS_VPT) return SPEC_ERR_INVALID_ARG;
+        CL = g_ts_cluster;
+    } else {
+        // ... widened, up to the portable 8, while the doubled cluster still leaves every CTA an
+        // SM of its own and each thread at least one vector (a wider cluster shares a row among
+        // more SMs, but every exchange between them then costs more)
+        const int sms = sm_count();
+        while (CL < 8 && 2LL * B * CL <= sms && nvec >= 2LL * CL * TS_NT) CL *= 2;
+    }
     if ((long long)B * CL > 0x7fffffffLL) return SPEC_ERR_INVALID_ARG;
 
     TreeSampleParams P;
@@ -647,6 +654,13 @@ void spec_set_kernel_events(void* start, void* stop)
 {
     g_kernel_events.start = static_cast<cudaEvent_t>(start);
     g_kernel_events.stop = static_cast<cudaEvent_t>(stop);
+}
+
+int spec_set_tree_sample_cluster(int cl)
+{
+    const int prev = g_ts_cluster;
+    g_ts_cluster = (cl == 1 || cl == 2 || cl == 4 || cl == 8 || cl == 16) ? cl : 0;
+    return prev;
 }
 
 int spec_set_wait_limit(int polls)

@@ -190,3 +190,22 @@ def test_unaligned_rows_take_the_element_path():
     for k in out:
         np.testing.assert_array_equal(out[k], g_ref[k])
     compare(g_ref, run_oracle(tb))
+
+
+@pytest.mark.parametrize("cl", [1, 2, 4, 8, 16])
+def test_forced_cluster_sizes(cl):
+    """The walk gives the oracle's results whatever the cluster size (the measurement aid that
+    forces it); a size whose slices cannot hold the row is refused."""
+    cfg = S.scaled(C6, B=6, V=16384, seed=2100 + cl)
+    tb = S.make_sample_tree_batch(cfg)
+    prev = sv.set_tree_sample_cluster(cl)
+    try:
+        compare(run_gpu(tb), run_oracle(tb))
+        if cl < 8:  # V = 128256 needs 8 CTAs of 512 threads at 4 vectors per thread
+            big = S.make_sample_tree_batch(S.scaled(C6, B=1, seed=2200))
+            with pytest.raises(sv.SpecVerifyError):
+                sv.tree_verify_sample(dev(big.target), dev(big.draft), dev(big.parents),
+                                      dev(big.tokens), dev(big.qrow), dev(big.uniforms),
+                                      big.cfg.temperature)
+    finally:
+        sv.set_tree_sample_cluster(prev)
