@@ -524,6 +524,29 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, uns
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// launch_dependent for a kernel of thread-block clusters of `cluster` CTAs along x
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent_cluster(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                            size_t smem, unsigned cluster, cudaStream_t st,
+                                            Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // raises a kernel's dynamic shared-memory limit to `smem` when above the default
 template <auto K>
 inline void set_smem_limit(size_t smem)

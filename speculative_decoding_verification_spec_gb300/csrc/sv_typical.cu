@@ -13,13 +13,18 @@
 // layout uses plain loads (typical_stats_kernel).  Partials with maxima MC_k merge at the row's MC
 // with d_k = MC_k - MC: S = sum 2^d_k S_k, E = sum 2^d_k (E_k + d_k S_k).
 //
-// Kernel 2 (typical_finish_kernel), one CTA per request: the rows' statistics, every node's test,
-// the walk, then the inverse-CDF draw over the accepted node's row: per segment of 32 vectors the
-// mass sum 2^y, a scan of the segment sums in index order (pairs of floats), and the token
-// resolved inside its segment.
+// Kernel 2 (typical_finish_kernel), one thread-block cluster of TYP_CL CTAs per request: the rows'
+// statistics (shared among the CTAs), every node's test and the walk (CTA 0), then the inverse-CDF
+// draw over the accepted node's row: per segment of 32 vectors the mass sum 2^y (the CTAs take a run
+// of segments each), a scan of the segment sums in index order (pairs of floats), and the token
+// resolved inside its segment (CTA 0).
+#include <cooperative_groups.h>
+
 #include "sv_plan.cuh"
 #include "sv_tree_walk.cuh"
 #include "sv_typical.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace sv {
 
@@ -246,6 +251,9 @@ __device__ __forceinline__ void typ_mass(const char* row, long long v, long long
     }
 }
 
+// One cluster of TYP_CL CTAs per request: the rows' statistics and the draw's segment sums are shared
+// among the CTAs (remote stores into CTA 0's shared memory), the tests, the walk, the scan and the
+// outputs run in CTA 0; four cluster barriers order the hand-offs.
 template <int DT, int VEC>
 __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
 {
@@ -253,8 +261,10 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
     __shared__ int sh_bad;
     __shared__ TreeWalk sh_walk;
     __shared__ int sh_tok;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = TYP_NT / 32;
-    const int b = blockIdx.x, N = P.t.N, R = P.t.R;
+    const int b = blockIdx.x / CL, N = P.t.N, R = P.t.R;
     const unsigned FULL = 0xffffffffu;
     int32_t* par = ysm;
     int32_t* tok = ysm + N;
@@ -266,34 +276,42 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
     float* rH = rL2S + R;
     float* segs = rH + R;
 
-    // the tree and the uniform do not depend on kernel 1
-    for (int i = tid; i < N; i += TYP_NT) {
-        par[i] = __ldg(P.t.parents + (size_t)b * N + i);
-        tok[i] = __ldg(P.t.tokens + (size_t)b * N + i);
-    }
+    // the tree and the uniform do not depend on kernel 1 (CTA 0 uses them)
+    if (rank == 0)
+        for (int i = tid; i < N; i += TYP_NT) {
+            par[i] = __ldg(P.t.parents + (size_t)b * N + i);
+            tok[i] = __ldg(P.t.tokens + (size_t)b * N + i);
+        }
     const float u = __ldg(P.uniforms + b);
     if (tid == 0) sh_bad = 0;
     pdl_wait();  // the partials of kernel 1
-    __syncthreads();
+    cluster.sync();  // CTA 0's flag is cleared before any CTA reports to it
+    // CTA 0's copies: every CTA writes its rows' statistics and its segment sums there
+    float* rMC0 = cluster.map_shared_rank(rMC, 0);
+    float* rL2S0 = cluster.map_shared_rank(rL2S, 0);
+    float* rH0 = cluster.map_shared_rank(rH, 0);
+    float* segs0 = cluster.map_shared_rank(segs, 0);
 
-    // ---- each row's statistics: one warp per row, the partials merged as pairs of floats.  A warp's
-    // rows (up to TYP_RPW of them) have their first 64 partials in flight together.
+    // ---- each row's statistics: one warp per row, the partials merged as pairs of floats.  CTA k of
+    // the cluster takes rows k, k + CL, ...; a warp's rows (up to TYP_RPW of them) have their first 64
+    // partials in flight together.
     constexpr int TYP_RPW = 3;
     int bad = 0;
-    for (int j0 = warp; j0 < R; j0 += nw * TYP_RPW) {
+    auto row_of = [&](int i) { return rank + CL * i; };
+    for (int i0 = warp; row_of(i0) < R; i0 += nw * TYP_RPW) {
         float4 q[TYP_RPW][2];
 #pragma unroll
         for (int t = 0; t < TYP_RPW; ++t)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int j = j0 + t * nw, k = lane + 32 * h;
+                const int j = row_of(i0 + t * nw), k = lane + 32 * h;
                 q[t][h] = make_float4(NEG_INF, NEG_INF, 0.f, 0.f);
                 if (j < R && k < P.np)
                     q[t][h] = __ldcg(reinterpret_cast<const float4*>(P.partials + ((size_t)b * R + j) * P.np + k));
             }
 #pragma unroll
         for (int t = 0; t < TYP_RPW; ++t) {
-            const int j = j0 + t * nw;
+            const int j = row_of(i0 + t * nw);
             if (j >= R) break;  // the same for every lane
             const TypPartial* pp = P.partials + ((size_t)b * R + j) * P.np;
             float Mr = fmaxf(q[t][0].x, q[t][1].x);
@@ -331,19 +349,19 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
                 bad = max(bad, tmo ? 2 : 1);
             }
             if (lane == 0) {
-                rMC[j] = MCr;
-                rL2S[j] = l2s;
-                rH[j] = H;
+                rMC0[j] = MCr;
+                rL2S0[j] = l2s;
+                rH0[j] = H;
                 if (P.aux_entropy) P.aux_entropy[(size_t)b * R + j] = H;
             }
         }
     }
-    if (bad && lane == 0) atomicMax(&sh_bad, bad);
-    __syncthreads();
+    if (bad && lane == 0) atomicMax(cluster.map_shared_rank(&sh_bad, 0), bad);
+    cluster.sync();  // CTA 0 holds every row's statistics
 
-    // ---- every node's own test: ln p_r(x) > min(ln eps, ln delta - H_r)
+    // ---- every node's own test: ln p_r(x) > min(ln eps, ln delta - H_r) (CTA 0)
     const char* row0 = typ_row(P, b, 0);
-    for (int i = tid; i < N; i += TYP_NT) {
+    for (int i = tid; rank == 0 && i < N; i += TYP_NT) {
         const int p = par[i], x = tok[i];
         int m = 0;
         float lnp = __int_as_float(0x7fc00000);
@@ -359,8 +377,8 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
     }
     __syncthreads();
 
-    // ---- the walk (warp 0)
-    if (warp == 0) {
+    // ---- the walk (warp 0 of CTA 0)
+    if (rank == 0 && warp == 0) {
         const int late = (u >= 0.f && u < 1.f) ? 0 : ROW_BAD_UNIFORM;
         const TreeWalk w = tree_walk(N, P.t.V, P.t.max_out, sh_bad, late, par, tok,
                                      [&](int i, int) { return match[i] != 0; }, depth, valid);
@@ -369,38 +387,44 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
             sh_tok = -1;
         }
     }
-    __syncthreads();
-    const TreeWalk w = sh_walk;
+    cluster.sync();  // the walk is visible to every CTA
+    const TreeWalk w = *cluster.map_shared_rank(&sh_walk, 0);
 
     // ---- the token after the path: inverse CDF over the accepted node's row with u
-    if (w.st == ROW_OK) {
-        const int r = w.node < 0 ? 0 : w.node + 1;
-        const char* rp = row0 + (size_t)r * P.t.V * esize(DT);
-        const float MC = rMC[r];
-        const long long nvec = P.t.nvec;
-        // per segment of 32 vectors its mass; a warp's segments in batches of TYP_SB, their loads
-        // in flight together
+    const int r = w.node < 0 ? 0 : w.node + 1;
+    const char* rp = row0 + (size_t)r * P.t.V * esize(DT);
+    const long long nvec = P.t.nvec;
+    if (w.st == ROW_OK) {  // the same in every CTA of the cluster
+        const float MC = rMC0[r];
+        // per segment of 32 vectors its mass: CTA k of the cluster takes the k-th run of segments, a
+        // warp its segments in batches of TYP_SB, their loads in flight together
+        const int sper = (P.nseg + CL - 1) / CL;
+        const int ga = min(rank * sper, P.nseg), gz = min(ga + sper, P.nseg);
         constexpr int TYP_SB = 8;
         const uint64_t pol = policy_evict_first();
-        for (int g0 = warp; g0 < P.nseg; g0 += nw * TYP_SB) {
+        for (int g0 = ga + warp; g0 < gz; g0 += nw * TYP_SB) {
             RawVec<DT, VEC> x[TYP_SB];  // raw bits until used: 4 registers per 16-byte vector
 #pragma unroll
             for (int k = 0; k < TYP_SB; ++k) {
                 const long long v = (long long)(g0 + k * nw) * 32 + lane;
                 x[k].fill_neg_inf();
-                if (g0 + k * nw < P.nseg && v < nvec) x[k].load(rp, v, pol);
+                if (g0 + k * nw < gz && v < nvec) x[k].load(rp, v, pol);
             }
 #pragma unroll
             for (int k = 0; k < TYP_SB; ++k) {
-                if (g0 + k * nw >= P.nseg) break;  // the same for every lane
+                if (g0 + k * nw >= gz) break;  // the same for every lane
                 float m[VEC];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) m[e] = ex2(fmaf(x[k].get(e), P.c, -MC));
                 const float ws = warp_sum(tree_sum(m));
-                if (lane == 0) segs[g0 + k * nw] = ws;
+                if (lane == 0) segs0[g0 + k * nw] = ws;
             }
         }
-        __syncthreads();
+    }
+    cluster.sync();  // CTA 0 holds every segment sum; the other CTAs are done
+    if (rank != 0) return;
+    if (w.st == ROW_OK) {
+        const float MC = rMC[r];
         if (warp == 0) {
             // lane totals of contiguous blocks of segments, scanned in index order as pairs of
             // floats (the fp64 pipe is slow on this part; a pair carries about 48 bits)
@@ -489,7 +513,8 @@ static cudaError_t launch_finish(const TypicalParams& P, cudaStream_t st)
 {
     const size_t smem = typical_finish_smem(P.t.N, P.nseg);
     set_smem_limit<typical_finish_kernel<DT, VEC>>(smem);
-    return launch_dependent(typical_finish_kernel<DT, VEC>, (unsigned)P.t.B, TYP_NT, smem, st, P);
+    return launch_dependent_cluster(typical_finish_kernel<DT, VEC>, (unsigned)((long long)P.t.B * TYP_CL),
+                                    TYP_NT, smem, TYP_CL, st, P);
 }
 
 template <int DT>

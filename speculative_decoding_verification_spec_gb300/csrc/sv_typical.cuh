@@ -6,7 +6,8 @@
 
 namespace sv {
 
-constexpr int TYP_NT = 1024;          // threads of the per-request finish CTA
+constexpr int TYP_NT = 1024;          // threads of each CTA of the per-request finish cluster
+constexpr int TYP_CL = 4;             // CTAs of the per-request finish cluster
 constexpr int TYP_MAX_NODES = 2048;   // the tree is staged in shared memory
 constexpr int TYP_MAX_SEGS = 16384;   // draw segments of one row (32 vectors each) in shared memory
 constexpr int TYP_SLICE = 1024;       // elements per partial on the scalar path
