@@ -230,9 +230,10 @@ __global__ void __launch_bounds__(NT) typical_stats_kernel(TypicalParams P)
 
 size_t typical_finish_smem(int N, int nseg)
 {
-    // par, tok, depth, valid, match [N] ints; MC, log2 S, H [N+1] floats; segment sums [nseg]
+    // par, tok, depth, valid, match [N] ints; MC, log2 S, H [N+1] floats; segment sums [nseg];
+    // each node's token logit [N] floats
     return (size_t)5 * N * sizeof(int32_t) + (size_t)3 * (N + 1) * sizeof(float) +
-           (size_t)nseg * sizeof(float);
+           (size_t)nseg * sizeof(float) + (size_t)N * sizeof(float);
 }
 
 // The mass 2^y of each element of vector v of a row (0 past the row's end): recomputed bit for bit
@@ -275,12 +276,18 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
     float* rL2S = rMC + R;
     float* rH = rL2S + R;
     float* segs = rH + R;
+    float* xlog = segs + P.nseg;
 
-    // the tree and the uniform do not depend on kernel 1 (CTA 0 uses them)
+    // the tree, each node's token logit and the uniform do not depend on kernel 1 (CTA 0 uses them)
+    const char* row0 = typ_row(P, b, 0);
     if (rank == 0)
         for (int i = tid; i < N; i += TYP_NT) {
-            par[i] = __ldg(P.t.parents + (size_t)b * N + i);
-            tok[i] = __ldg(P.t.tokens + (size_t)b * N + i);
+            const int p = __ldg(P.t.parents + (size_t)b * N + i), x = __ldg(P.t.tokens + (size_t)b * N + i);
+            par[i] = p;
+            tok[i] = x;
+            xlog[i] = (p >= -1 && p < i && x >= 0 && x < P.t.V)
+                          ? load_logit(row0 + (size_t)(p < 0 ? 0 : p + 1) * P.t.V * esize(DT), DT, x)
+                          : 0.f;
         }
     const float u = __ldg(P.uniforms + b);
     if (tid == 0) sh_bad = 0;
@@ -360,14 +367,13 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
     cluster.sync();  // CTA 0 holds every row's statistics
 
     // ---- every node's own test: ln p_r(x) > min(ln eps, ln delta - H_r) (CTA 0)
-    const char* row0 = typ_row(P, b, 0);
     for (int i = tid; rank == 0 && i < N; i += TYP_NT) {
         const int p = par[i], x = tok[i];
         int m = 0;
         float lnp = __int_as_float(0x7fc00000);
         if (!sh_bad && p >= -1 && p < i && x >= 0 && x < P.t.V) {
             const int r = p < 0 ? 0 : p + 1;
-            const float xl = load_logit(row0 + (size_t)r * P.t.V * esize(DT), DT, x);
+            const float xl = xlog[i];
             lnp = __fmul_rn(__fsub_rn(fmaf(xl, P.c, -rMC[r]), rL2S[r]), LN2_HI);
             const float lthr = fminf(P.ln_eps, __fsub_rn(P.ln_delta, rH[r]));
             m = lnp > lthr;
