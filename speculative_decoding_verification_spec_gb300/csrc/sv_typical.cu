@@ -291,8 +291,10 @@ __global__ void __launch_bounds__(TYP_NT) typical_finish_kernel(TypicalParams P)
         }
     const float u = __ldg(P.uniforms + b);
     if (tid == 0) sh_bad = 0;
+    // every CTA of the cluster has started and CTA 0's flag is cleared before any CTA reports to it
+    // (taken while kernel 1 still runs)
+    cluster.sync();
     pdl_wait();  // the partials of kernel 1
-    cluster.sync();  // CTA 0's flag is cleared before any CTA reports to it
     // CTA 0's copies: every CTA writes its rows' statistics and its segment sums there
     float* rMC0 = cluster.map_shared_rank(rMC, 0);
     float* rL2S0 = cluster.map_shared_rank(rL2S, 0);
