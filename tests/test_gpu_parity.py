@@ -94,6 +94,22 @@ def test_topk_shapes(V, k, dtype):
     check_spec(S.make_spec_batch(cfg))
 
 
+@pytest.mark.parametrize("B,V,k,dtype", [(40, 152064, 50, "bf16"), (40, 40000, 50, "f32"),
+                                         (80, 40003, 50, "bf16"), (40, 40000, 256, "bf16"),
+                                         (40, 16384, 7, "bf16"), (40, 20481, 300, "f32")])
+def test_topk_many_rows(B, V, k, dtype):
+    """More rows than the top-k streaming grid has CTAs (gamma=4: 9 rows per request), so every
+    CTA streams several rows: aligned and unaligned rows, one-chunk rows, k above the CTA's
+    threads (dense rows)."""
+    cfg = S.scaled(S.CONFIGS["c4"], B=B, gamma=4, V=V, top_k=k, dtype=dtype, seed=3500 + V + k)
+    check_spec(S.make_spec_batch(cfg))
+
+
+def test_topk_many_rows_ties():
+    cfg = S.scaled(S.CONFIGS["c4"], B=40, gamma=4, V=30000, top_k=50, seed=3600)
+    check_spec(_coarse(cfg, 1.0))
+
+
 @pytest.mark.parametrize("gamma", [0, 1, 2, 31, 32, 40])
 def test_gamma_range(gamma):
     cfg = S.scaled(S.CONFIGS["c3"], B=3, gamma=gamma, V=5000, seed=4000 + gamma)
