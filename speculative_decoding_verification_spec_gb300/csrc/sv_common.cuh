@@ -441,39 +441,75 @@ constexpr int STREAM_SMEM = STREAM_STAGES * STREAM_CHUNK_BYTES;
 constexpr int STREAM_MASK_BYTES = STREAM_CHUNK_BYTES / 16;
 constexpr int STREAM_SMEM_MASKED = STREAM_SMEM + STREAM_STAGES * STREAM_MASK_BYTES;
 
-// Warp-specialised streaming (the plain and tree kernels): one producer lane issues the CTA's chunks
-// ids blockIdx.x, + gridDim.x, ... (< nch) into the STREAM_STAGES-stage ring, refilling a stage once
-// all WARPS consumer warps have arrived on its "empty" mbarrier; the stage's "full" mbarrier completes
-// when the bytes land.  src(id, ptr, bytes, policy) describes chunk id.  A wait that runs out (after
-// `limit` polls), or a consumer's (sfail), stops the issue; the copies in flight are then waited for
-// with the full MBAR_SPIN_LIMIT, so the CTA never leaves while one could still land.
-template <class Src>
-__device__ void ring_produce(uint4* ring, uint64_t* full, uint64_t* empty, int* sfail, int nch,
-                             int limit, Src src)
+// Warp-specialised streaming (the plain, tree and typical kernels) with NG consumer groups per
+// CTA: group g (warps g * WARPS .. g * WARPS + WARPS - 1) is virtual CTA NG * blockIdx.x + g of
+// NG * gridDim.x, takes chunks vb, vb + that stride, ... and reads its own STREAM_STAGES-stage ring
+// (stages g * STREAM_STAGES ..).  With NG = 1 that is one ring per CTA and two CTAs per SM.  Two such
+// CTAs on one SM do not run equally fast: on the typical stream, whose chunks cost the most
+// arithmetic, the later CTA took about 15% longer per chunk, so the SMs' second CTAs finished last.
+// With NG = 2 (one CTA per SM) one producer lane feeds the two rings in turn, one chunk each, so a
+// group that falls behind holds the other back and the SM's chunks finish together.
+template <int NG>
+constexpr int stream_threads() { return NG * NT + 32; }  // the producer warp last
+
+// A consumer thread's place: its group, virtual CTA, the virtual CTAs, its thread and warp in the group
+template <int NG>
+struct StreamGroup {
+    int g, vb, stride, t, w;
+    __device__ __forceinline__ StreamGroup()
+    {
+        g = NG > 1 ? (int)threadIdx.x / NT : 0;
+        vb = NG * (int)blockIdx.x + g;
+        stride = NG * (int)gridDim.x;
+        t = (int)threadIdx.x - g * NT;
+        w = t >> 5;
+    }
+};
+
+// The producer lane.  issue(s, id) issues the copy of chunk id into stage s (of all the rings'
+// NG * STREAM_STAGES), completing on full[s]; a stage is refilled once all WARPS warps of
+// its group have arrived on empty[s].  A wait that runs out (after `limit` polls), or a consumer's
+// (sfail), stops the issue; the copies in flight are then waited for with the full
+// MBAR_SPIN_LIMIT, so the CTA never leaves while one could still land.
+template <int NG, class Issue>
+__device__ void ring_produce(uint64_t* full, uint64_t* empty, int* sfail, int nch, int limit, Issue issue)
 {
-    int stg = 0;
-    unsigned ph = 0;
-    long long n = 0;
-    for (int id = blockIdx.x; id < nch; id += gridDim.x) {
-        if (*reinterpret_cast<volatile int*>(sfail)) break;
-        if (n >= STREAM_STAGES && !mbar_wait(&empty[stg], ph ^ 1u, limit)) {
-            *reinterpret_cast<volatile int*>(sfail) = 1;
-            break;
-        }
-        const char* ptr;
-        unsigned bytes;
-        uint64_t pol;
-        src(id, ptr, bytes, pol);
-        bulk_load(ring + (size_t)stg * NT * STREAM_NV, ptr, bytes, &full[stg], pol);
-        ++n;
-        if (++stg == STREAM_STAGES) {
-            stg = 0;
-            ph ^= 1u;
+    int stg[NG], id[NG];
+    unsigned ph[NG];
+    long long n[NG];
+    const int stride = NG * (int)gridDim.x;
+    for (int g = 0; g < NG; ++g) {
+        stg[g] = 0;
+        ph[g] = 0u;
+        n[g] = 0;
+        id[g] = NG * (int)blockIdx.x + g;
+    }
+    for (bool more = true; more;) {
+        more = false;
+        for (int g = 0; g < NG; ++g) {
+            if (id[g] >= nch) continue;
+            const int s = g * STREAM_STAGES + stg[g];
+            if (*reinterpret_cast<volatile int*>(sfail) ||
+                (n[g] >= STREAM_STAGES && !mbar_wait(&empty[s], ph[g] ^ 1u, limit))) {
+                *reinterpret_cast<volatile int*>(sfail) = 1;
+                more = false;
+                break;
+            }
+            issue(s, id[g]);
+            ++n[g];
+            if (++stg[g] == STREAM_STAGES) {
+                stg[g] = 0;
+                ph[g] ^= 1u;
+            }
+            id[g] += stride;
+            more = true;
         }
     }
     // the last fill of every stage: no later fill of that stage exists, so its phase is unambiguous
-    for (long long j = (n > STREAM_STAGES ? n - STREAM_STAGES : 0); j < n; ++j)
-        (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u, MBAR_SPIN_LIMIT);
+    for (int g = 0; g < NG; ++g)
+        for (long long j = (n[g] > STREAM_STAGES ? n[g] - STREAM_STAGES : 0); j < n[g]; ++j)
+            (void)mbar_wait(&full[g * STREAM_STAGES + j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u,
+                            MBAR_SPIN_LIMIT);
 }
 
 // persistent grid of CTAs: resident CTAs per SM x SMs, at most one per task (the occupancy query

@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
     }
 }
 
+// consumer groups per CTA of the streaming kernel (see ring_produce): one, with two CTAs per SM;
+// two groups in one CTA per SM were slower here (plain rows by 1%, masked rows by 3%)
+constexpr int SPEC_GROUPS = 1;
+
 // Streaming kernel for rows of 16-byte vectors: persistent CTAs take 32 KB chunks round-robin,
 // fetched by bulk copies (TMA engine) into a ring of STREAM_STAGES shared-memory stages, so the
 // next chunks are in flight while one is reduced.  Each warp reduces its part of a chunk -- the
@@ -276,16 +280,17 @@ __global__ void __launch_bounds__(NT) spec_stats_kernel(SpecParams P)
 // its bits two chunks ahead into one of two register sets used in turn, so their latency hides
 // behind the chunks in between.
 template <int DT, int MASK>
-__global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
+__global__ void __launch_bounds__(stream_threads<SPEC_GROUPS>(), 2 / SPEC_GROUPS) spec_stream_kernel(SpecParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int CHUNK = NT * STREAM_NV * VEC;  // elements per chunk
-    extern __shared__ __align__(128) uint4 ring[];  // STREAM_STAGES x (NT * STREAM_NV) vectors
-    // MASK_RING: then STREAM_STAGES x STREAM_MASK_BYTES of mask bits
-    uint32_t* mring = reinterpret_cast<uint32_t*>(ring + (size_t)STREAM_STAGES * NT * STREAM_NV);
-    __shared__ __align__(8) uint64_t full[STREAM_STAGES];
-    __shared__ __align__(8) uint64_t empty[STREAM_STAGES];
+    // SPEC_GROUPS x STREAM_STAGES stages of NT * STREAM_NV vectors; MASK_RING: then as many
+    // stages of STREAM_MASK_BYTES of mask bits
+    extern __shared__ __align__(128) uint4 ring[];
+    uint32_t* mring = reinterpret_cast<uint32_t*>(ring + (size_t)SPEC_GROUPS * STREAM_STAGES * NT * STREAM_NV);
+    __shared__ __align__(8) uint64_t full[SPEC_GROUPS * STREAM_STAGES];
+    __shared__ __align__(8) uint64_t empty[SPEC_GROUPS * STREAM_STAGES];
     __shared__ int sfail;  // a wait ran out in this CTA: nothing more is read
 
     pdl_trigger();  // the row-merge kernel may be scheduled as SMs free up; it waits for this grid
@@ -293,79 +298,58 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned FULL = 0xffffffffu;
     const int nch = P.B * P.R * P.S1;  // < 2^31 (checked on the host)
-    const int G0 = gridDim.x;
     const float c = P.c;
     if (tid == 0) {
         sfail = 0;
-        for (int s = 0; s < STREAM_STAGES; ++s) {
+        for (int s = 0; s < SPEC_GROUPS * STREAM_STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], WARPS);
         }
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == WARPS && MASK == MASK_RING) {  // the producer, with each chunk's mask bits
-        if (lane == 0) {
-            int ps = 0;
-            unsigned pph = 0;
-            long long n = 0;
-            for (int id = blockIdx.x; id < nch; id += G0) {
-                if (*reinterpret_cast<volatile int*>(&sfail)) break;
-                if (n >= STREAM_STAGES && !mbar_wait(&empty[ps], pph ^ 1u, P.wait_limit)) {
-                    *reinterpret_cast<volatile int*>(&sfail) = 1;
-                    break;
-                }
-                const int rid = id / P.S1, cix = id - rid * P.S1;
-                const int b = rid / P.R, r = rid - b * P.R;
-                const int cbase = cix * CHUNK, cend = min(cbase + CHUNK, P.V);
-                // the chunk's mask words, rounded up to 16 bytes: inside the row, whose words are a
-                // multiple of four
-                const unsigned mbytes = (unsigned)((((cend - cbase + 31) >> 5) + 3) & ~3) * 4u;
-                bulk_load2(ring + (size_t)ps * NT * STREAM_NV, spec_row_ptr(P, b, r) + (size_t)cbase * ES,
-                           (unsigned)(cend - cbase) * ES,
-                           mring + (size_t)ps * (STREAM_MASK_BYTES / 4),
-                           spec_mask_row(P, b, r) + (size_t)cix * (CHUNK / 32), mbytes, &full[ps],
-                           pinned_row(P, r) ? policy_evict_normal() : policy_evict_first(),
-                           policy_evict_first());
-                ++n;
-                if (++ps == STREAM_STAGES) {
-                    ps = 0;
-                    pph ^= 1u;
-                }
-            }
-            // the last fill of every stage: no later fill of that stage exists
-            for (long long j = (n > STREAM_STAGES ? n - STREAM_STAGES : 0); j < n; ++j)
-                (void)mbar_wait(&full[j % STREAM_STAGES], (unsigned)(j / STREAM_STAGES) & 1u, MBAR_SPIN_LIMIT);
-        }
-        return;
-    }
-    if (warp == WARPS) {  // the producer: the rows of the likely correction pairs stay in L2
+    if (warp == SPEC_GROUPS * WARPS) {  // the producer: the rows of the likely correction pairs stay in L2
         if (lane == 0)
-            ring_produce(ring, full, empty, &sfail, nch, P.wait_limit,
-                         [&](int id, const char*& ptr, unsigned& bytes, uint64_t& pol) {
-                             const int row_id = id / P.S1, ci = id - row_id * P.S1;
-                             const int b = row_id / P.R, r = row_id - b * P.R;
-                             const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
-                             ptr = spec_row_ptr(P, b, r) + (size_t)cbase * ES;
-                             bytes = (unsigned)(cend - cbase) * ES;
-                             pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
-                         });
+            ring_produce<SPEC_GROUPS>(full, empty, &sfail, nch, P.wait_limit, [&](int s, int id) {
+                const int row_id = id / P.S1, ci = id - row_id * P.S1;
+                const int b = row_id / P.R, r = row_id - b * P.R;
+                const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+                const uint64_t pol = pinned_row(P, r) ? policy_evict_normal() : policy_evict_first();
+                if constexpr (MASK == MASK_RING) {
+                    // with the chunk's mask words, rounded up to 16 bytes: inside the row, whose
+                    // words are a multiple of four
+                    const unsigned mbytes = (unsigned)((((cend - cbase + 31) >> 5) + 3) & ~3) * 4u;
+                    bulk_load2(ring + (size_t)s * NT * STREAM_NV, spec_row_ptr(P, b, r) + (size_t)cbase * ES,
+                               (unsigned)(cend - cbase) * ES, mring + (size_t)s * (STREAM_MASK_BYTES / 4),
+                               spec_mask_row(P, b, r) + (size_t)ci * (CHUNK / 32), mbytes, &full[s], pol,
+                               policy_evict_first());
+                } else {
+                    bulk_load(ring + (size_t)s * NT * STREAM_NV, spec_row_ptr(P, b, r) + (size_t)cbase * ES,
+                              (unsigned)(cend - cbase) * ES, &full[s], pol);
+                }
+            });
         return;
     }
+    const StreamGroup<SPEC_GROUPS> sg;
+    uint64_t* gfull = full + sg.g * STREAM_STAGES;
+    uint64_t* gempty = empty + sg.g * STREAM_STAGES;
+    const uint4* gring = ring + (size_t)sg.g * STREAM_STAGES * NT * STREAM_NV;
+    const uint32_t* gmring = mring + (size_t)sg.g * STREAM_STAGES * (STREAM_MASK_BYTES / 4);
+    const int tid_g = sg.t;  // thread within the group
 
     bool failed = false;  // a wait ran out: the remaining chunks are reported, not read
     int stg = 0;          // it % STREAM_STAGES
     unsigned phase = 0;   // (it / STREAM_STAGES) & 1
-    // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
-    int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
-    const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
-    // the mask bits of chunk (rid, cix) for this thread's vectors: vector j * NT + tid of the chunk
-    // sits in word (j * NT + tid) * VEC / 32 of the chunk's CHUNK / 32 words, at a fixed shift
+    // chunk id = row_id * S1 + ci, advanced by the stride without a division per chunk
+    int row_id = sg.vb / P.S1, ci = sg.vb - row_id * P.S1;
+    const int drow = sg.stride / P.S1, dci = sg.stride - drow * P.S1;
+    // the mask bits of chunk (rid, cix) for this thread's vectors: vector j * NT + tid_g of the
+    // chunk sits in word (j * NT + tid_g) * VEC / 32 of the chunk's CHUNK / 32 words, at a fixed shift
     auto load_mask = [&](int rid, int cix, uint32_t (&out)[STREAM_NV]) {
         const int b = rid / P.R;
-        const uint32_t* mw = spec_mask_row(P, b, rid - b * P.R) + (size_t)cix * (CHUNK / 32) + (tid * VEC) / 32;
-        const unsigned sh = (unsigned)(tid * VEC) & 31u;
-        const int left = P.V - cix * CHUNK - tid * VEC;  // elements from this thread's first vector on
+        const uint32_t* mw = spec_mask_row(P, b, rid - b * P.R) + (size_t)cix * (CHUNK / 32) + (tid_g * VEC) / 32;
+        const unsigned sh = (unsigned)(tid_g * VEC) & 31u;
+        const int left = P.V - cix * CHUNK - tid_g * VEC;  // elements from this thread's first vector on
 #pragma unroll
         for (int j = 0; j < STREAM_NV; ++j) {
             uint32_t wv = 0u;
@@ -385,7 +369,7 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
     int pr = row_id, pc = ci;  // MASK: the chunk whose bits are loaded next
     // one chunk; with MASK, mreg holds its bits (loaded two chunks earlier) and is refilled
     auto process = [&](int id, uint32_t (&mreg)[STREAM_NV]) {
-        if (id != blockIdx.x) {
+        if (id != sg.vb) {
             advance(row_id, ci);
             if (++stg == STREAM_STAGES) {
                 stg = 0;
@@ -396,10 +380,10 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
         const bool partial = cbase + CHUNK > cend;
         const int s = stg;
         if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
-        bool ok = !failed && mbar_wait(&full[s], phase, P.wait_limit);
+        bool ok = !failed && mbar_wait(&gfull[s], phase, P.wait_limit);
         uint4 w[STREAM_NV];
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-        const uint4* sb = ring + (size_t)s * NT * STREAM_NV + tid;
+        const uint4* sb = gring + (size_t)s * NT * STREAM_NV + tid_g;
         if (ok && !partial) {
 #pragma unroll
             for (int j = 0; j < STREAM_NV; ++j) w[j] = lds128(sb + j * NT);
@@ -407,7 +391,7 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
 #pragma unroll
             for (int j = 0; j < STREAM_NV; ++j) {
                 w[j] = make_uint4(pad, pad, pad, pad);
-                if (ok && cbase + (j * NT + tid) * VEC < cend) w[j] = lds128(sb + j * NT);
+                if (ok && cbase + (j * NT + tid_g) * VEC < cend) w[j] = lds128(sb + j * NT);
             }
         }
         // MASK: vector j of every lane of the warp fully masked (bit j) is skipped below: its
@@ -419,14 +403,14 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
 #pragma unroll
                 for (int j = 0; j < STREAM_NV; ++j) bits[j] = mreg[j];
                 // this register set is free again: the bits of the chunk two ahead
-                if ((long long)id + 2 * G0 < nch) load_mask(pr, pc, mreg);
+                if ((long long)id + 2 * sg.stride < nch) load_mask(pr, pc, mreg);
                 advance(pr, pc);
             } else {
-                // vector j * NT + tid of the chunk: word (j * NT + tid) * VEC / 32 of the stage's bits
-                const uint32_t* mw = mring + (size_t)s * (STREAM_MASK_BYTES / 4);
+                // vector j * NT + tid_g of the chunk: word (j * NT + tid_g) * VEC / 32 of the stage's bits
+                const uint32_t* mw = gmring + (size_t)s * (STREAM_MASK_BYTES / 4);
 #pragma unroll
                 for (int j = 0; j < STREAM_NV; ++j) {
-                    const int e0 = (j * NT + tid) * VEC;
+                    const int e0 = (j * NT + tid_g) * VEC;
                     bits[j] = (ok && (!partial || cbase + e0 < cend))
                                   ? (mw[e0 >> 5] >> (e0 & 31)) & ((1u << VEC) - 1u) : 0u;
                 }
@@ -446,7 +430,7 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
         ok = __all_sync(FULL, ok);
         if (ok) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&gempty[s]);
         } else if (!failed) {
             failed = true;
             if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
@@ -509,22 +493,22 @@ __global__ void __launch_bounds__(NT + 32, 2) spec_stream_kernel(SpecParams P)
             pt.MC = MC;
             pt.S = warp_sum((a0 + a1) + (a2 + a3));
         }
-        if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
+        if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + sg.w] = pt;
     };
     if constexpr (MASK == MASK_REGS) {
         // two register sets in turn, so that no register move waits for a load still in flight
         uint32_t mA[STREAM_NV], mB[STREAM_NV];
-        if (blockIdx.x < nch) load_mask(pr, pc, mA);
+        if (sg.vb < nch) load_mask(pr, pc, mA);
         advance(pr, pc);
-        if ((long long)blockIdx.x + G0 < nch) load_mask(pr, pc, mB);
+        if ((long long)sg.vb + sg.stride < nch) load_mask(pr, pc, mB);
         advance(pr, pc);
-        for (int id = blockIdx.x; id < nch; id += 2 * G0) {
+        for (int id = sg.vb; id < nch; id += 2 * sg.stride) {
             process(id, mA);
-            if ((long long)id + G0 < nch) process(id + G0, mB);
+            if ((long long)id + sg.stride < nch) process(id + sg.stride, mB);
         }
     } else {
         uint32_t none[STREAM_NV];
-        for (int id = blockIdx.x; id < nch; id += G0) process(id, none);
+        for (int id = sg.vb; id < nch; id += sg.stride) process(id, none);
     }
 }
 
@@ -803,13 +787,21 @@ static void launch_softmax_plain(const SpecParams& P, int sms, cudaStream_t st)
     spec_resample_kernel<DT, VEC><<<persistent_grid<spec_resample_kernel<DT, VEC>>(P.tasks2, sms), NT, 0, st>>>(P);
 }
 
+// the streaming kernel's grid: as many CTAs as fit, at most one per SPEC_GROUPS chunks
+template <auto K>
+static unsigned stream_grid(const SpecParams& P, int sms, int smem)
+{
+    return cta_grid<K>(((long long)P.B * P.R * P.S1 + SPEC_GROUPS - 1) / SPEC_GROUPS, sms, smem,
+                       stream_threads<SPEC_GROUPS>());
+}
+
 template <int DT, int MASK>
 static void launch_softmax_chunk(const SpecParams& P, int sms, cudaStream_t st)
 {
     constexpr auto K1 = spec_stream_kernel<DT, MASK>;
-    constexpr int smem = MASK == MASK_RING ? STREAM_SMEM_MASKED : STREAM_SMEM;
+    constexpr int smem = SPEC_GROUPS * (MASK == MASK_RING ? STREAM_SMEM_MASKED : STREAM_SMEM);
     mark_kernel_start(st);
-    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, smem, NT + 32), NT + 32, smem, st>>>(P);
+    K1<<<stream_grid<K1>(P, sms, smem), stream_threads<SPEC_GROUPS>(), smem, st>>>(P);
     mark_kernel_stop(st);
     const int pw = (P.R <= 32) ? std::min(P.R, PLAN_WARPS) : WARPS;
     launch_dependent(spec_rowplan_kernel<DT>, (unsigned)P.B, (unsigned)(32 * pw), 0, st, P);
@@ -825,10 +817,12 @@ cudaError_t launch_softmax_stats(const SpecParams& P, int sms, cudaStream_t st)
     if (P.vec > 1) {
         if (P.dtype == DT_BF16) {
             constexpr auto K1 = spec_stream_kernel<DT_BF16, MASK_NONE>;
-            K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
+            K1<<<stream_grid<K1>(P, sms, SPEC_GROUPS * STREAM_SMEM), stream_threads<SPEC_GROUPS>(),
+                 SPEC_GROUPS * STREAM_SMEM, st>>>(P);
         } else {
             constexpr auto K1 = spec_stream_kernel<DT_F32, MASK_NONE>;
-            K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
+            K1<<<stream_grid<K1>(P, sms, SPEC_GROUPS * STREAM_SMEM), stream_threads<SPEC_GROUPS>(),
+                 SPEC_GROUPS * STREAM_SMEM, st>>>(P);
         }
     } else if (P.dtype == DT_BF16) {
         spec_stats_kernel<DT_BF16, 1><<<persistent_grid<spec_stats_kernel<DT_BF16, 1>>(P.tasks1, sms), NT, 0, st>>>(P);

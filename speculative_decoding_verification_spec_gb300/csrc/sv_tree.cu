@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(NT) tree_argmax_kernel(TreeParams P)
     }
 }
 
+// consumer groups per CTA of the streaming argmax (see ring_produce): one, with two CTAs per SM;
+// two groups in one CTA per SM gave the same time
+constexpr int TREE_GROUPS = 1;
+
 // Streaming argmax for rows of 16-byte vectors: persistent CTAs take 32 KB chunks round-robin,
 // fetched by bulk copies into a ring of shared-memory stages.  Each thread finds its maximum (via
 // the maxima of its vectors) and the first of its elements equal to it -- its vectors and their
@@ -196,52 +200,55 @@ __global__ void __launch_bounds__(NT) tree_argmax_kernel(TreeParams P)
 // a producer warp fills the ring (ring_produce) and the consumer warps release each stage on its
 // "empty" mbarrier, so they never wait for one another.
 template <int DT>
-__global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
+__global__ void __launch_bounds__(stream_threads<TREE_GROUPS>(), 2 / TREE_GROUPS) tree_stream_kernel(TreeParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int CHUNK = NT * STREAM_NV * VEC;
     extern __shared__ __align__(128) uint4 ring[];
-    __shared__ __align__(8) uint64_t full[STREAM_STAGES];
-    __shared__ __align__(8) uint64_t empty[STREAM_STAGES];
+    __shared__ __align__(8) uint64_t full[TREE_GROUPS * STREAM_STAGES];
+    __shared__ __align__(8) uint64_t empty[TREE_GROUPS * STREAM_STAGES];
     __shared__ int sfail;  // a wait ran out in this CTA: nothing more is read
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned FULL = 0xffffffffu;
     const int nch = P.B * P.R * P.S1;
-    const int G0 = gridDim.x;
     if (tid == 0) {
         sfail = 0;
-        for (int s = 0; s < STREAM_STAGES; ++s) {
+        for (int s = 0; s < TREE_GROUPS * STREAM_STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], WARPS);
         }
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == WARPS) {  // the producer
+    if (warp == TREE_GROUPS * WARPS) {  // the producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            ring_produce(ring, full, empty, &sfail, nch, P.wait_limit,
-                         [&](int id, const char*& ptr, unsigned& bytes, uint64_t& cp) {
-                             const int row_id = id / P.S1, ci = id - row_id * P.S1;
-                             const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
-                             ptr = reinterpret_cast<const char*>(P.logits) + ((size_t)row_id * P.V + cbase) * ES;
-                             bytes = (unsigned)(cend - cbase) * ES;
-                             cp = pol;
-                         });
+            ring_produce<TREE_GROUPS>(full, empty, &sfail, nch, P.wait_limit, [&](int s, int id) {
+                const int row_id = id / P.S1, ci = id - row_id * P.S1;
+                const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
+                bulk_load(ring + (size_t)s * NT * STREAM_NV,
+                          reinterpret_cast<const char*>(P.logits) + ((size_t)row_id * P.V + cbase) * ES,
+                          (unsigned)(cend - cbase) * ES, &full[s], pol);
+            });
         }
         return;
     }
+    const StreamGroup<TREE_GROUPS> sg;
+    uint64_t* gfull = full + sg.g * STREAM_STAGES;
+    uint64_t* gempty = empty + sg.g * STREAM_STAGES;
+    const uint4* gring = ring + (size_t)sg.g * STREAM_STAGES * NT * STREAM_NV;
+    const int tid_g = sg.t;  // thread within the group
 
     bool failed = false;
     int stg = 0;          // it % STREAM_STAGES
     unsigned phase = 0;   // (it / STREAM_STAGES) & 1
-    // chunk id = row_id * S1 + ci, advanced by G0 without a division per chunk
-    int row_id = blockIdx.x / P.S1, ci = blockIdx.x - row_id * P.S1;
-    const int drow = G0 / P.S1, dci = G0 - drow * P.S1;
-    for (int id = blockIdx.x; id < nch; id += G0) {
-        if (id != blockIdx.x) {
+    // chunk id = row_id * S1 + ci, advanced by the stride without a division per chunk
+    int row_id = sg.vb / P.S1, ci = sg.vb - row_id * P.S1;
+    const int drow = sg.stride / P.S1, dci = sg.stride - drow * P.S1;
+    for (int id = sg.vb; id < nch; id += sg.stride) {
+        if (id != sg.vb) {
             row_id += drow;
             ci += dci;
             if (ci >= P.S1) {
@@ -256,25 +263,25 @@ __global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, P.V);
         const int s = stg;
         if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
-        bool ok = !failed && mbar_wait(&full[s], phase, P.wait_limit);
+        bool ok = !failed && mbar_wait(&gfull[s], phase, P.wait_limit);
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-        const uint4* sb = ring + (size_t)s * NT * STREAM_NV;
+        const uint4* sb = gring + (size_t)s * NT * STREAM_NV;
         uint4 w[STREAM_NV];
         float vmax[STREAM_NV];
         int nin = 0;  // vectors of this thread inside the row
 #pragma unroll
         for (int j = 0; j < STREAM_NV; ++j) {
-            const bool in = cbase + (j * NT + tid) * VEC < cend;
+            const bool in = cbase + (j * NT + tid_g) * VEC < cend;
             nin += in;
             w[j] = make_uint4(pad, pad, pad, pad);
-            if (ok && in) w[j] = lds128(sb + j * NT + tid);
+            if (ok && in) w[j] = lds128(sb + j * NT + tid_g);
         }
         // release the stage once every lane has read it; a warp whose wait ran out never releases
         // it (its copy may still land), which stops the producer
         ok = __all_sync(FULL, ok);
         if (ok) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&gempty[s]);
         } else if (!failed) {
             failed = true;
             if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
                     for (int e = 3; e >= 0; --e)
                         if (__uint_as_float(q[e]) == tm) ef = e;
                 }
-                idx = cbase + (jf * NT + tid) * VEC + ef;
+                idx = cbase + (jf * NT + tid_g) * VEC + ef;
             }
             // warp: maximum value, then the lowest index holding it
             float bv = nan ? NEG_INF : tm;
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(NT + 32, 2) tree_stream_kernel(TreeParams P)
             pt.idx = bi;
             pt.nan = __any_sync(0xffffffffu, nan);
         }
-        if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + warp] = pt;
+        if (lane == 0) P.partials[((size_t)row_id * P.S1 + ci) * WARPS + sg.w] = pt;
     }
 }
 
@@ -426,7 +433,9 @@ static void launch_tree_chunk(const TreeParams& P, int sms, cudaStream_t st)
 {
     constexpr auto K1 = tree_stream_kernel<DT>;
     mark_kernel_start(st);
-    K1<<<cta_grid<K1>((long long)P.B * P.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32, STREAM_SMEM, st>>>(P);
+    constexpr int ssm = TREE_GROUPS * STREAM_SMEM, nth = stream_threads<TREE_GROUPS>();
+    K1<<<cta_grid<K1>(((long long)P.B * P.R * P.S1 + TREE_GROUPS - 1) / TREE_GROUPS, sms, ssm, nth), nth, ssm,
+         st>>>(P);
     mark_kernel_stop(st);
     const size_t smem = P.N <= TREE_SMEM_NODES ? (size_t)(4 * P.N + P.R) * sizeof(int32_t) : 0;
     set_smem_limit<tree_finish_kernel<DT>>(smem);

@@ -51,18 +51,23 @@ __device__ __forceinline__ bool df_lt(DFloat a, DFloat b)
 
 // ---------------------------------------------------------------- kernel 1: row statistics
 
-// Persistent CTAs over 32 KB chunks of the rows, fetched by bulk copies into a shared-memory ring
-// (a producer warp fills it, the consumer warps release each stage on its "empty" mbarrier).  Each
-// consumer warp writes one partial per chunk.  NaN or +inf anywhere makes the partial's S NaN.
+// consumer groups per CTA of the streaming kernel (see ring_produce): two, in one CTA per SM.  Its
+// chunks cost the most arithmetic of the streams, and two CTAs per SM finished unevenly.
+constexpr int TYP_GROUPS = 2;
+
+// Persistent CTAs over 32 KB chunks of the rows, fetched by bulk copies into shared-memory rings
+// (a producer warp fills them, the consumer warps of each group release each stage on its "empty"
+// mbarrier).  Each consumer warp writes one partial per chunk.  NaN or +inf anywhere makes the
+// partial's S NaN.
 template <int DT>
-__global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParams P)
+__global__ void __launch_bounds__(stream_threads<TYP_GROUPS>(), 1) typical_stream_kernel(TypicalParams P)
 {
     constexpr int VEC = (DT == DT_BF16) ? 8 : 4;
     constexpr int ES = (DT == DT_BF16) ? 2 : 4;
     constexpr int CHUNK = NT * STREAM_NV * VEC;
     extern __shared__ __align__(128) uint4 ring[];
-    __shared__ __align__(8) uint64_t full[STREAM_STAGES];
-    __shared__ __align__(8) uint64_t empty[STREAM_STAGES];
+    __shared__ __align__(8) uint64_t full[TYP_GROUPS * STREAM_STAGES];
+    __shared__ __align__(8) uint64_t empty[TYP_GROUPS * STREAM_STAGES];
     __shared__ int sfail;
 
     pdl_trigger();
@@ -70,35 +75,38 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
     const unsigned FULL = 0xffffffffu;
     const int S1 = P.S1, V = P.t.V;
     const int nch = P.t.B * P.t.R * S1;  // < 2^31 (checked on the host)
-    const int G0 = gridDim.x;
     const float c = P.c;
     if (tid == 0) {
         sfail = 0;
-        for (int s = 0; s < STREAM_STAGES; ++s) {
+        for (int s = 0; s < TYP_GROUPS * STREAM_STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], WARPS);
         }
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == WARPS) {
-        if (lane == 0)
-            ring_produce(ring, full, empty, &sfail, nch, P.t.wait_limit,
-                         [&](int id, const char*& ptr, unsigned& bytes, uint64_t& pol) {
-                             const int row = id / S1, ci = id - row * S1;
-                             const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, V);
-                             ptr = reinterpret_cast<const char*>(P.t.logits) +
-                                   ((size_t)row * V + cbase) * ES;
-                             bytes = (unsigned)(cend - cbase) * ES;
-                             pol = policy_evict_first();
-                         });
+    if (warp == TYP_GROUPS * WARPS) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            ring_produce<TYP_GROUPS>(full, empty, &sfail, nch, P.t.wait_limit, [&](int s, int id) {
+                const int row = id / S1, ci = id - row * S1;
+                const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, V);
+                bulk_load(ring + (size_t)s * NT * STREAM_NV,
+                          reinterpret_cast<const char*>(P.t.logits) + ((size_t)row * V + cbase) * ES,
+                          (unsigned)(cend - cbase) * ES, &full[s], pol);
+            });
+        }
         return;
     }
+    const StreamGroup<TYP_GROUPS> sg;
+    uint64_t* gfull = full + sg.g * STREAM_STAGES;
+    uint64_t* gempty = empty + sg.g * STREAM_STAGES;
+    const uint4* gring = ring + (size_t)sg.g * STREAM_STAGES * NT * STREAM_NV;
 
     bool failed = false;
     int stg = 0;
     unsigned phase = 0;
-    for (int id = blockIdx.x, it = 0; id < nch; id += G0, ++it) {
+    for (int id = sg.vb, it = 0; id < nch; id += sg.stride, ++it) {
         if (it > 0 && ++stg == STREAM_STAGES) {
             stg = 0;
             phase ^= 1u;
@@ -106,19 +114,19 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
         const int row = id / S1, ci = id - row * S1;
         const int cbase = ci * CHUNK, cend = min(cbase + CHUNK, V);
         if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
-        bool ok = !failed && mbar_wait(&full[stg], phase, P.t.wait_limit);
+        bool ok = !failed && mbar_wait(&gfull[stg], phase, P.t.wait_limit);
         uint4 w[STREAM_NV];
         const uint32_t pad = (DT == DT_BF16) ? 0xff80ff80u : 0xff800000u;
-        const uint4* sb = ring + (size_t)stg * NT * STREAM_NV + tid;
+        const uint4* sb = gring + (size_t)stg * NT * STREAM_NV + sg.t;
 #pragma unroll
         for (int j = 0; j < STREAM_NV; ++j) {
             w[j] = make_uint4(pad, pad, pad, pad);
-            if (ok && cbase + (j * NT + tid) * VEC < cend) w[j] = lds128(sb + j * NT);
+            if (ok && cbase + (j * NT + sg.t) * VEC < cend) w[j] = lds128(sb + j * NT);
         }
         ok = __all_sync(FULL, ok);
         if (ok) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stg]);
+            if (lane == 0) mbar_arrive(&gempty[stg]);
         } else if (!failed) {
             failed = true;
             if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
@@ -186,7 +194,7 @@ __global__ void __launch_bounds__(NT + 32, 2) typical_stream_kernel(TypicalParam
             pt.S = warp_sum(s0 + s1);
             pt.E = warp_sum(e0 + e1);
         }
-        if (lane == 0) P.partials[((size_t)row * S1 + ci) * WARPS + warp] = pt;
+        if (lane == 0) P.partials[((size_t)row * S1 + ci) * WARPS + sg.w] = pt;
     }
 }
 
@@ -531,8 +539,9 @@ static cudaError_t launch_typical(const TypicalParams& P, int sms, cudaStream_t 
     mark_kernel_start(st);
     if (P.t.vec > 1) {
         constexpr auto K1 = typical_stream_kernel<DT>;
-        K1<<<cta_grid<K1>((long long)P.t.B * P.t.R * P.S1, sms, STREAM_SMEM, NT + 32), NT + 32,
-             STREAM_SMEM, st>>>(P);
+        constexpr int smem = TYP_GROUPS * STREAM_SMEM, nth = stream_threads<TYP_GROUPS>();
+        K1<<<cta_grid<K1>(((long long)P.t.B * P.t.R * P.S1 + TYP_GROUPS - 1) / TYP_GROUPS, sms, smem, nth), nth,
+             smem, st>>>(P);
     } else {
         constexpr auto K1 = typical_stats_kernel<DT>;
         K1<<<persistent_grid<K1>((long long)P.t.B * P.t.R * P.S1, sms), NT, 0, st>>>(P);
