@@ -35,12 +35,15 @@ namespace sv {
 constexpr int TK_NREG = STREAM_CHUNK_BYTES / (NT * 4);  // 32-bit words per thread (32)
 constexpr int TK_NV = STREAM_NV;                        // 16-byte vectors per thread (8)
 constexpr int TK_STAGES = STREAM_STAGES;                // bulk-copy ring depth
-constexpr int TK_SMEM = STREAM_SMEM;                    // dynamic shared memory of kernel 1
+constexpr int TK_GROUPS = 2;               // kernel 1: consumer groups per CTA (one CTA per SM)
+constexpr int TK_SMEM = TK_GROUPS * STREAM_SMEM;        // dynamic shared memory of kernel 1: a ring per group
 // per-chunk candidate count codes
 constexpr int TK_OVERFLOW = -1, TK_NONFINITE = -2, TK_TIMEOUT = -3;
-constexpr int TK_PRODUCER = WARPS;         // kernel 1: the bulk-copy producer warp
+constexpr int TK_LEAD = 2;                 // kernel 1: chunks one group's producer may run ahead of the other's
+constexpr int TK_LEAD_POLLS = 1024;        // kernel 1: polls before a producer stops waiting for the other group
+constexpr int TK_PRODUCER = TK_GROUPS * WARPS;  // kernel 1: the first producer warp (one per group)
 constexpr int TK_SLOTS = 4;                // kernel 1: per-segment shared state, by segment mod 4
-constexpr int TK_THREADS = NT + 32;        // kernel 1: WARPS consumer warps + the producer warp
+constexpr int TK_THREADS = TK_GROUPS * (NT + 32);  // kernel 1: per group WARPS consumer warps + a producer
 
 // order-preserving 32-bit key of a float; -0 and +0 map to the same key
 __device__ __forceinline__ uint32_t okey(float x)
@@ -217,10 +220,10 @@ __device__ void topk_request_draw(const SpecParams& P, const Plan& pl, int nk, T
 // element index (within the row) of register slot s of this thread: vector j = s / VEC, element
 // e = s % VEC of it; vectors of a thread are NT apart
 template <int VEC>
-__device__ __forceinline__ int slot_elem(int cbase, int s)
+__device__ __forceinline__ int slot_elem(int cbase, int s, int t)
 {
-    if constexpr (VEC == 1) return cbase + s * NT + (int)threadIdx.x;
-    else return cbase + ((s / VEC) * NT + (int)threadIdx.x) * VEC + (s % VEC);
+    if constexpr (VEC == 1) return cbase + s * NT + t;
+    else return cbase + ((s / VEC) * NT + t) * VEC + (s % VEC);
 }
 
 // The k-th largest (with multiplicity) of the n keys key_at(0..n), by one warp: a radix select
@@ -444,7 +447,7 @@ __device__ uint32_t chunk_tau_key(const uint4* stage, const char* row, int cbase
 // reached, so the warps take turns turning the histogram into a tighter bound for the chunks still
 // to come, published as one 64-bit word (segment, key).
 template <int DT, bool BULK>
-__global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P)
+__global__ void __launch_bounds__(TK_THREADS, 1) topk_stream_kernel(SpecParams P)
 {
     constexpr int NREG = TK_NREG;
     constexpr int EPT = (DT == DT_BF16) ? 2 * NREG : NREG;  // elements per thread
@@ -455,66 +458,75 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     constexpr int EPG = (DT == DT_BF16) ? 2 * G : G;  // elements per group
     static_assert(NREG % G == 0, "register groups");
     static_assert((WARPS & (WARPS - 1)) == 0, "warps take turns by chunk index");
-    extern __shared__ __align__(128) uint4 ring[];  // BULK: TK_STAGES x (NT * TK_NV) vectors
-    __shared__ int hist[TK_SLOTS][TK_BINS];
-    __shared__ int scount[TK_SLOTS];        // groups listed in the segment
-    __shared__ int sflag[TK_SLOTS];         // 1: a NaN or +inf in the segment; 4: a wait ran out
-    __shared__ uint32_t tau_key[TK_SLOTS];  // the segment's tau, published by the producer
-    __shared__ int seg_id[TK_SLOTS];        // the segment in the slot (producer's books)
-    __shared__ unsigned long long pub;      // (segment << 32) | key of the latest running bound
-    __shared__ int sfail;                   // a wait ran out in this CTA: nothing more is read
-    __shared__ __align__(8) uint64_t full[TK_STAGES];
-    __shared__ __align__(8) uint64_t empty[TK_STAGES];
-    __shared__ __align__(8) uint64_t tau_bar[TK_SLOTS];
-    __shared__ __align__(8) uint64_t done_bar[TK_SLOTS];
+    // per consumer group (the first index); BULK: a ring of TK_STAGES x (NT * TK_NV) vectors each
+    extern __shared__ __align__(128) uint4 ring[];
+    __shared__ int hist[TK_GROUPS][TK_SLOTS][TK_BINS];
+    __shared__ int scount[TK_GROUPS][TK_SLOTS];        // groups listed in the segment
+    __shared__ int sflag[TK_GROUPS][TK_SLOTS];         // 1: a NaN or +inf in the segment; 4: a wait ran out
+    __shared__ uint32_t tau_key[TK_GROUPS][TK_SLOTS];  // the segment's tau, published by the producer
+    __shared__ int seg_id[TK_GROUPS][TK_SLOTS];        // the segment in the slot (producer's books)
+    __shared__ unsigned long long pub[TK_GROUPS];      // (segment << 32) | key of the latest running bound
+    __shared__ int issued[TK_GROUPS];                  // BULK: chunks issued; 2^30 once all are
+    __shared__ int sfail;                              // a wait ran out in this CTA: nothing more is read
+    __shared__ __align__(8) uint64_t full[TK_GROUPS][TK_STAGES];
+    __shared__ __align__(8) uint64_t empty[TK_GROUPS][TK_STAGES];
+    __shared__ __align__(8) uint64_t tau_bar[TK_GROUPS][TK_SLOTS];
+    __shared__ __align__(8) uint64_t done_bar[TK_GROUPS][TK_SLOTS];
 
     pdl_trigger();  // the finish kernel may be scheduled as SMs free up; it waits for this grid
     clear_counters(P.ctr_clear, P.ctr_words);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned FULL = 0xffffffffu;
     const int nsegs = P.B * P.R * P.nsegr;
-    const int G0 = gridDim.x;
+    const int G0 = TK_GROUPS * gridDim.x;  // virtual CTAs: group grp is TK_GROUPS * blockIdx.x + grp
     const int k = P.top_k;
+    // the consumer group a warp serves (consumer warps first, then one producer warp per group), and
+    // a consumer's thread and warp within its group
+    const int grp = warp < TK_GROUPS * WARPS ? warp / WARPS : warp - TK_GROUPS * WARPS;
+    const int ct = tid - grp * NT, cw = warp - grp * WARPS;
 
-    for (int i = tid; i < TK_SLOTS * TK_BINS; i += TK_THREADS) (&hist[0][0])[i] = 0;
-    if (tid < TK_SLOTS) {
-        scount[tid] = 0;
-        sflag[tid] = 0;
+    for (int i = tid; i < TK_GROUPS * TK_SLOTS * TK_BINS; i += TK_THREADS) (&hist[0][0][0])[i] = 0;
+    if (tid < TK_GROUPS * TK_SLOTS) {
+        (&scount[0][0])[tid] = 0;
+        (&sflag[0][0])[tid] = 0;
     }
     if (tid == 0) {
-        pub = ~0ull;  // segment field 0xffffffff: no bound yet
+        for (int g = 0; g < TK_GROUPS; ++g) {
+            pub[g] = ~0ull;  // segment field 0xffffffff: no bound yet
+            issued[g] = 0;
+            for (int s = 0; s < TK_STAGES; ++s) {
+                mbar_init(&full[g][s], 1);
+                mbar_init(&empty[g][s], WARPS);
+            }
+            for (int s = 0; s < TK_SLOTS; ++s) {
+                mbar_init(&tau_bar[g][s], 1);
+                mbar_init(&done_bar[g][s], WARPS);
+            }
+        }
         sfail = 0;
-        for (int s = 0; s < TK_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], WARPS);
-        }
-        for (int s = 0; s < TK_SLOTS; ++s) {
-            mbar_init(&tau_bar[s], 1);
-            mbar_init(&done_bar[s], WARPS);
-        }
         fence_mbar_init();
     }
     __syncthreads();
 
     // ------------------------------------------------------------------ producer warp
-    if (warp == TK_PRODUCER) {
+    if (warp >= TK_PRODUCER) {  // the producer warp of group grp
         const uint64_t pol = policy_evict_first();
         // the list length (or status) and final bound of the segment in slot `slot`, done or not
         auto publish = [&](int slot, bool done) {
-            const int psg = seg_id[slot];
-            const uint32_t key0 = tau_key[slot];
+            const int psg = seg_id[grp][slot];
+            const uint32_t key0 = tau_key[grp][slot];
             const float tau = (k <= NT) ? key_value(key0) : NEG_INF;
             float bnd = tau;
-            if (done && k <= NT && tau != NEG_INF) bnd = fmaxf(bnd, hist_bound(hist[slot], k, key0));
+            if (done && k <= NT && tau != NEG_INF) bnd = fmaxf(bnd, hist_bound(hist[grp][slot], k, key0));
             if (lane == 0) {
-                const int c = scount[slot], f = sflag[slot];
+                const int c = scount[grp][slot], f = sflag[grp][slot];
                 P.ccount[psg] = (!done || (f & 4)) ? TK_TIMEOUT : (f & 1) ? TK_NONFINITE
                               : (k > NT || c > P.cap_s) ? TK_OVERFLOW : c;
                 P.cbound[psg] = bnd;
             }
         };
         SegCursor pc;
-        pc.init(blockIdx.x, G0, P.nsegr);
+        pc.init(TK_GROUPS * blockIdx.x + grp, G0, P.nsegr);
         int stg = 0;
         unsigned ph = 0;
         long long n = 0;  // copies issued
@@ -524,17 +536,17 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             const int slot = m % TK_SLOTS;
             // the slot's previous segment: done by every consumer warp, published, cleared
             if (m >= TK_SLOTS) {
-                const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)((m - TK_SLOTS) / TK_SLOTS) & 1u, P.wait_limit));
+                const bool done = __all_sync(FULL, mbar_wait(&done_bar[grp][slot], (unsigned)((m - TK_SLOTS) / TK_SLOTS) & 1u, P.wait_limit));
                 publish(slot, done);
                 if (!done) ok = false;
 #pragma unroll
-                for (int i = 0; i < TK_BINS / 32; ++i) hist[slot][lane + 32 * i] = 0;
+                for (int i = 0; i < TK_BINS / 32; ++i) hist[grp][slot][lane + 32 * i] = 0;
                 if (lane == 0) {
-                    scount[slot] = 0;
-                    sflag[slot] = 0;
+                    scount[grp][slot] = 0;
+                    sflag[grp][slot] = 0;
                 }
             }
-            if (lane == 0) seg_id[slot] = pc.sg;
+            if (lane == 0) seg_id[grp][slot] = pc.sg;
             const int nst = min(P.sps, P.CT - pc.si * P.sps);
             const char* row = spec_row_ptr(P, pc.row_id / P.R, pc.row_id % P.R);
             // tau from the segment's first chunk, selected once the next copy is on its way (or at
@@ -546,8 +558,9 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 uint32_t key = 0;
                 if (k <= NT) {
                     if constexpr (BULK) {
-                        if (t_stg >= 0 && __all_sync(FULL, mbar_wait(&full[t_stg], t_ph, P.wait_limit))) {
-                            key = chunk_tau_key<DT, true>(ring + (size_t)t_stg * NT * TK_NV, nullptr, t_cbase, t_cend, k);
+                        if (t_stg >= 0 && __all_sync(FULL, mbar_wait(&full[grp][t_stg], t_ph, P.wait_limit))) {
+                            key = chunk_tau_key<DT, true>(ring + (size_t)(grp * TK_STAGES + t_stg) * NT * TK_NV,
+                                                          nullptr, t_cbase, t_cend, k);
                             fence_proxy_async_smem();  // these reads come before the stage's refill
                         } else {
                             ok = false;
@@ -558,9 +571,9 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 }
                 __syncwarp();  // the slot is clear before the consumers see this segment
                 if (lane == 0) {
-                    tau_key[slot] = key;
+                    tau_key[grp][slot] = key;
                     if (!ok) *reinterpret_cast<volatile int*>(&sfail) = 1;
-                    mbar_arrive(&tau_bar[slot]);
+                    mbar_arrive(&tau_bar[grp][slot]);
                 }
             };
             for (int st = 0; st < nst; ++st) {
@@ -570,9 +583,16 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     // lane 0: the stage's previous fill released by every consumer warp (bounded)
                     int go = 0;
                     if (lane == 0 && ok && !*reinterpret_cast<volatile int*>(&sfail)) {
-                        if (n < TK_STAGES || mbar_wait(&empty[stg], ph ^ 1u, P.wait_limit)) {
-                            bulk_load(ring + (size_t)stg * NT * TK_NV, row + (size_t)cbase * ES,
-                                      (unsigned)(cend - cbase) * ES, &full[stg], pol);
+                        // the other group no more than TK_LEAD chunks behind (a bounded wait; the two
+                        // groups share the SM, and one left to run ahead would leave the other's chunks
+                        // to the end)
+                        for (int sp = 0; sp < min(P.wait_limit, TK_LEAD_POLLS) &&
+                                         *reinterpret_cast<volatile int*>(&issued[grp ^ 1]) + TK_LEAD <= (int)n; ++sp)
+                            __nanosleep(32);
+                        if (n < TK_STAGES || mbar_wait(&empty[grp][stg], ph ^ 1u, P.wait_limit)) {
+                            bulk_load(ring + (size_t)(grp * TK_STAGES + stg) * NT * TK_NV, row + (size_t)cbase * ES,
+                                      (unsigned)(cend - cbase) * ES, &full[grp][stg], pol);
+                            *reinterpret_cast<volatile int*>(&issued[grp]) = (int)n + 1;
                             go = 1;
                         } else {
                             *reinterpret_cast<volatile int*>(&sfail) = 1;
@@ -600,10 +620,11 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             }
             if (nst == 1) publish_tau();
         }
+        if (lane == 0) *reinterpret_cast<volatile int*>(&issued[grp]) = 1 << 30;  // holds the other back no more
         // the last segments: published once every consumer warp is done with them
         for (int j = (m > TK_SLOTS ? m - TK_SLOTS : 0); j < m; ++j) {
             const int slot = j % TK_SLOTS;
-            const bool done = __all_sync(FULL, mbar_wait(&done_bar[slot], (unsigned)(j / TK_SLOTS) & 1u, P.wait_limit));
+            const bool done = __all_sync(FULL, mbar_wait(&done_bar[grp][slot], (unsigned)(j / TK_SLOTS) & 1u, P.wait_limit));
             publish(slot, done);
         }
         // the CTA may not leave while a copy is in flight: wait (bounded) for the last fill of
@@ -611,7 +632,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
         if constexpr (BULK) {
             if (lane == 0)
                 for (long long j = (n > TK_STAGES ? n - TK_STAGES : 0); j < n; ++j)
-                    (void)mbar_wait(&full[j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u, MBAR_SPIN_LIMIT);
+                    (void)mbar_wait(&full[grp][j % TK_STAGES], (unsigned)(j / TK_STAGES) & 1u, MBAR_SPIN_LIMIT);
         }
         return;
     }
@@ -622,7 +643,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
     int jseg = -1;        // this CTA's segment counter
     bool failed = false;  // a wait ran out: the remaining segments are marked, not read
     SegCursor cc;
-    cc.init(blockIdx.x, G0, P.nsegr);
+    cc.init(TK_GROUPS * blockIdx.x + grp, G0, P.nsegr);
     for (; cc.sg < nsegs; cc.next(G0, P.nsegr)) {
         const int sg = cc.sg;
         ++jseg;
@@ -643,8 +664,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             uint32_t w[NREG];
             if (!failed && *reinterpret_cast<volatile int*>(&sfail)) failed = true;
             if constexpr (BULK) {
-                bool ok = !failed && mbar_wait(&full[stg], ph, P.wait_limit);
-                const uint4* sb = ring + (size_t)stg * NT * TK_NV + tid;
+                bool ok = !failed && mbar_wait(&full[grp][stg], ph, P.wait_limit);
+                const uint4* sb = ring + (size_t)(grp * TK_STAGES + stg) * NT * TK_NV + ct;
                 if (ok && !partial) {
 #pragma unroll
                     for (int j = 0; j < TK_NV; ++j) {
@@ -656,7 +677,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
 #pragma unroll
                     for (int j = 0; j < TK_NV; ++j) {
                         uint4 q = make_uint4(pad, pad, pad, pad);
-                        if (ok && cbase + (j * NT + tid) * VEC < cend) q = lds128(sb + j * NT);
+                        if (ok && cbase + (j * NT + ct) * VEC < cend) q = lds128(sb + j * NT);
                         w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
                     }
                 }
@@ -665,7 +686,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                 ok = __all_sync(FULL, ok);
                 if (ok) {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stg]);
+                    if (lane == 0) mbar_arrive(&empty[grp][stg]);
                 } else if (!failed) {
                     failed = true;
                     if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
@@ -679,7 +700,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     const unsigned short* rp = reinterpret_cast<const unsigned short*>(row);
 #pragma unroll
                     for (int j = 0; j < NREG; ++j) {
-                        const int e0 = slot_elem<1>(cbase, 2 * j), e1 = slot_elem<1>(cbase, 2 * j + 1);
+                        const int e0 = slot_elem<1>(cbase, 2 * j, ct), e1 = slot_elem<1>(cbase, 2 * j + 1, ct);
                         const uint32_t lo = e0 < cend ? __ldg(rp + e0) : 0xff80u;
                         const uint32_t hi = e1 < cend ? __ldg(rp + e1) : 0xff80u;
                         w[j] = lo | (hi << 16);
@@ -688,7 +709,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     const float* rp = reinterpret_cast<const float*>(row);
 #pragma unroll
                     for (int j = 0; j < NREG; ++j) {
-                        const int e0 = slot_elem<1>(cbase, j);
+                        const int e0 = slot_elem<1>(cbase, j, ct);
                         w[j] = e0 < cend ? __float_as_uint(__ldg(rp + e0)) : 0xff800000u;
                     }
                 }
@@ -723,34 +744,34 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
             // does the warp touch the segment's slot, which the producer has cleared by then
             if (st == 0) {
                 if (!failed) {
-                    const bool got = __all_sync(FULL, mbar_wait(&tau_bar[slot], (unsigned)(jseg / TK_SLOTS) & 1u, P.wait_limit));
+                    const bool got = __all_sync(FULL, mbar_wait(&tau_bar[grp][slot], (unsigned)(jseg / TK_SLOTS) & 1u, P.wait_limit));
                     if (!got) {
                         failed = true;
                         if (lane == 0) *reinterpret_cast<volatile int*>(&sfail) = 1;
                     }
                 }
                 if (!failed && k <= NT) {
-                    key0 = tau_key[slot];
+                    key0 = tau_key[grp][slot];
                     tau_first = key_value(key0);
                 }
             }
             if (!failed) {
                 if (bad_now && !seg_bad) {
                     seg_bad = 1;
-                    if (lane == 0) atomicOr(&sflag[slot], 1);
+                    if (lane == 0) atomicOr(&sflag[grp][slot], 1);
                 }
                 float beta = tau_first;
                 {
-                    const unsigned long long pb = *reinterpret_cast<volatile unsigned long long*>(&pub);
+                    const unsigned long long pb = *reinterpret_cast<volatile unsigned long long*>(&pub[grp]);
                     if ((int)(pb >> 32) == sg) beta = fmaxf(beta, key_value((uint32_t)pb));
                 }
 
                 // ---- the warps take turns: a tighter bound from the histogram (counts of every
                 // warp so far), for the chunks still to come
-                if (warp == (st & (WARPS - 1)) && !seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
-                    const float nb = hist_bound(hist[slot], k, key0);
+                if (cw == (st & (WARPS - 1)) && !seg_bad && k <= NT && st + 1 < nst && tau_first != NEG_INF) {
+                    const float nb = hist_bound(hist[grp][slot], k, key0);
                     if (lane == 0 && nb > beta)
-                        *reinterpret_cast<volatile unsigned long long*>(&pub) =
+                        *reinterpret_cast<volatile unsigned long long*>(&pub[grp]) =
                             ((unsigned long long)(unsigned)sg << 32) | okey(nb);
                 }
 
@@ -771,15 +792,15 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     if (partial && pass) {  // groups that start past the row's end hold padding only
 #pragma unroll
                         for (int g = 0; g < NG; ++g)
-                            if (slot_elem<VEC>(cbase, EPG * g) >= cend) pass &= ~(1u << g);
+                            if (slot_elem<VEC>(cbase, EPG * g, ct) >= cend) pass &= ~(1u << g);
                     }
                     const int mine = __popc(pass);
                     if (__any_sync(FULL, mine)) {
                         const int incl = warp_incl_scan(mine);
                         int pos = 0;
-                        if (lane == 31) pos = atomicAdd(&scount[slot], incl);
+                        if (lane == 31) pos = atomicAdd(&scount[grp][slot], incl);
                         pos = __shfl_sync(FULL, pos, 31) + incl - mine;
-                        int* h = hist[slot];
+                        int* h = hist[grp][slot];
                         const bool count = tau_first != NEG_INF;
 #pragma unroll
                         for (int g = 0; g < NG; ++g) {
@@ -787,7 +808,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                                 TopkEntry en;
                                 if constexpr (DT == DT_BF16) en.x = fmaxf(bf16lo(gm[g]), bf16hi(gm[g]));
                                 else en.x = __uint_as_float(gm[g]);
-                                en.idx = slot_elem<VEC>(cbase, EPG * g);
+                                en.idx = slot_elem<VEC>(cbase, EPG * g, ct);
                                 if (pos < P.cap_s) {
                                     slist[pos] = en;
                                     sdata[pos] = make_uint4(w[G * g], w[G * g + 1], w[G * g + 2], w[G * g + 3]);
@@ -802,12 +823,12 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(SpecParams P
                     }
                 }
             } else if (lane == 0) {
-                atomicOr(&sflag[slot], 4);
+                atomicOr(&sflag[grp][slot], 4);
             }
             // ---- the segment's last chunk: this warp is done with the segment
             if (st + 1 == nst) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&done_bar[slot]);
+                if (lane == 0) mbar_arrive(&done_bar[grp][slot]);
             }
         }
     }
@@ -1237,7 +1258,8 @@ __device__ __noinline__ void topk_dense_request(const SpecParams& P, int b)
 template <int DT>
 static void launch_topk(const SpecParams& P, int sms, cudaStream_t st)
 {
-    const long long nsegs = (long long)P.B * P.R * P.nsegr;  // < 2^31 (checked on the host)
+    // one CTA per SM at most, TK_GROUPS segment sequences per CTA
+    const long long nsegs = ((long long)P.B * P.R * P.nsegr + TK_GROUPS - 1) / TK_GROUPS;
     mark_kernel_start(st);
     if (P.vec > 1) {
         constexpr auto K1 = topk_stream_kernel<DT, true>;
