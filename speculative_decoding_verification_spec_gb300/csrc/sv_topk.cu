@@ -6,9 +6,11 @@
 // at the threshold are all kept.
 //
 // Kernel 1 (topk_stream_kernel) streams every logit row once.  Rows are cut into 32 KB chunks and
-// runs of chunks (segments, at most 4 per row); persistent CTAs take segments round-robin.  For
-// 16-byte aligned rows a producer warp fetches the chunks with bulk copies (TMA engine) into a ring
-// of TK_STAGES shared-memory stages, so the next chunks are in flight while one is filtered.  Each
+// runs of chunks (segments, at most 4 per row); persistent CTAs, one per SM, each run two consumer
+// groups, and the groups take segments round-robin.  For 16-byte aligned rows a group's producer warp
+// fetches its chunks with bulk copies (TMA engine) into a ring of TK_STAGES shared-memory stages, so
+// the next chunks are in flight while one is filtered; a producer more than TK_LEAD chunks ahead of
+// the other group's waits a little, so that the SM's two groups finish together.  Each
 // consumer thread holds its 64 (bf16) or 32 (fp32) elements of a chunk in registers; the consumer
 // warps run independently of one another and meet once per segment.  The k-th largest of the NT
 // per-thread maxima of a segment's first chunk (NT disjoint groups, so at least k elements are >=
@@ -424,21 +426,29 @@ __device__ uint32_t chunk_tau_key(const uint4* stage, const char* row, int cbase
     return prefix;
 }
 
-// Kernel 1: warp-specialised.  BULK: rows of 16-byte vectors fetched by bulk copies into the stage
-// ring; otherwise the consumer warps load their elements straight into registers.  A CTA takes
-// segments (runs of up to P.sps chunks of one row) round-robin; segment j of the CTA uses slot
-// j % TK_SLOTS of the per-segment shared state (histogram, list length, flags, tau).
+// Kernel 1: warp-specialised, with TK_GROUPS consumer groups of WARPS warps per CTA (one CTA per
+// SM); group grp is virtual CTA TK_GROUPS * blockIdx.x + grp and has its own ring, producer warp
+// (warp TK_PRODUCER + grp) and per-segment state.  Two groups, rather than two CTAs of one group per
+// SM: two CTAs on one SM do not run equally fast (the later one took about 6% longer per chunk here),
+// and the SMs' second CTAs set the end of the grid.  BULK: rows of 16-byte vectors fetched by bulk
+// copies into the stage ring; otherwise the consumer warps load their elements straight into
+// registers.  A group takes segments (runs of up to P.sps chunks of one row) round-robin; segment j of
+// the group uses slot j % TK_SLOTS of its per-segment shared state (histogram, list length, flags, tau).
 //
-// Producer (warp WARPS): lane 0 issues one bulk copy per chunk once every consumer warp has
-// released the stage (an "empty" mbarrier per stage; a "full" mbarrier completes when the bytes
-// land).  The whole warp also keeps the books of the segments: before segment j starts it waits
-// until segment j - TK_SLOTS is done by every consumer warp (a "done" mbarrier per slot), publishes
-// that segment -- its list length (or a status) and its final bound from the complete histogram --
-// and clears the slot; once the first chunk of segment j has landed it selects the segment's first
-// bound tau from it and publishes it through a "tau" mbarrier.  So the consumer warps never wait
-// for one another, and they are at most TK_SLOTS - 1 segments apart from the producer.
+// Producer (warp TK_PRODUCER + grp): lane 0 issues one bulk copy per chunk once every consumer warp
+// of the group has released the stage, and while it is more than TK_LEAD chunks ahead of the other
+// group's producer it first waits (at most TK_LEAD_POLLS polls: a group that falls behind holds the
+// other back, so both end together; the wait only paces, nothing depends on it).  Copies complete
+// on mbarriers: an "empty" mbarrier per stage, which every consumer warp of the group has
+// released; a "full" mbarrier completes when the bytes land.  The whole warp also keeps the books of
+// the group's segments: before segment j starts it waits until segment j - TK_SLOTS is done by every
+// consumer warp of the group (a "done" mbarrier per slot), publishes that segment -- its list length
+// (or a status) and its final bound from the complete histogram -- and clears the slot; once the
+// first chunk of segment j has landed it selects the segment's first bound tau from it and publishes
+// it through a "tau" mbarrier.  So the consumer warps never wait for one another, and they are at
+// most TK_SLOTS - 1 segments apart from their producer.
 //
-// Consumers (warps 0..WARPS-1): each waits on its chunk's full barrier, reads its 64 (bf16) or 32
+// Consumers (warps grp * WARPS ..): each waits on its chunk's full barrier, reads its 64 (bf16) or 32
 // (fp32) elements into registers and releases the stage.  Elements sit in groups of 4 registers
 // (one 16-byte vector); a group whose maximum reaches the current bound beta goes to the segment's
 // list (positions reserved with one shared-memory atomic per warp and chunk), and its maximum is
